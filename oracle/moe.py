@@ -1,0 +1,165 @@
+"""Plain float64 CPU reference of the fused MoE layer with weight-only-quantized experts.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the product path never
+imports this module.
+
+What is computed, and where it comes from
+-----------------------------------------
+* Dequantization.  "Marlin moe integration" (description: GPTQ checkpoints
+  ``gptq-4bit-128g`` with and without ``actorder_True``; review: the kernel
+  receives INT4 weights and scales) gives int4 codes with one scale per group
+  of 128 input channels, the group of channel k being ``g_idx[k]`` under
+  act-order.  Zero point 8 (symmetric codes 0..15) is this build's reading;
+  the pages print no formula.  "[Kernel] W8A16 Int8 inside FusedMoE"
+  (feature description) gives symmetric per-column, per-expert int8 with the
+  weights cast to the activation type before the matmul; a "column" is read
+  as one output feature of the expert matrix.
+* Expert FFN.  Mixtral-style experts: ``W13`` stacks the gate rows (0..I-1)
+  over the up rows (I..2I-1); ``t = SiLU(gate·x) * (up·x)``, ``y = W2·t``.
+  The pages name the Mixtral models and the fused MoE kernel but print no
+  formula; this is the plain reading.
+* Routing-weighted sum.  ``out[m] = sum_j topk_weights[m, j] * y(m, j)`` with
+  ``y(m, j)`` the FFN of expert ``topk_ids[m, j]`` applied to token m.
+* moe_align_block_size.  "Marlin moe integration" (review thread: the
+  ``moe_align_block_size_kernel`` the fused kernel relies on; block size 16
+  tied to the Marlin tile) groups the token-expert pairs by expert and pads
+  each expert's group to a multiple of the block size.  Readings for what the
+  pages leave open: pair index p = m*k + j; within an expert pairs keep
+  ascending p; padding and the tail hold the sentinel P; experts are laid out
+  in ascending id; an expert with no pairs takes no block; blocks past the
+  padded total map to expert -1; pairs whose id is outside [0, E) are dropped.
+
+Everything is float64 (the oracle does not round intermediates); dequantized
+weights are exact in float64 because codes have at most 8 bits and scales at
+most 24.
+
+Pins (CPU tests, none of which reuses these formulas): quantize/dequantize
+round trip against the offline quantizer; act-order identity and joint
+permutation invariance; closed-form layers built from scaled permutation
+matrices; zero input and all-zero-point weights; linearity in the routing
+weights and invariance under permuting the top-k slots; a scalar brute-force
+layer on tiny inputs; moe_align against hand-worked examples, a brute-force
+stable sort and its structural invariants.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------
+# dequantization
+# ----------------------------------------------------------------------------
+def dequant_int4(q: np.ndarray, s: np.ndarray, g_idx: np.ndarray | None,
+                 group_size: int) -> np.ndarray:
+    """W[n, k] = (q[n, k] - 8) * s[g(k), n], float64 [N, K].
+
+    q: codes 0..15 [N, K]; s: scales [K/G, N]; g(k) = g_idx[k] under
+    act-order, else k // G ("Marlin moe integration": GPTQ 4-bit group-128,
+    with or without act order).
+    """
+    N, K = q.shape
+    if g_idx is None:
+        g = np.arange(K) // group_size
+    else:
+        g = np.asarray(g_idx, np.int64)
+    scale_nk = np.asarray(s, np.float64)[g, :].T          # [N, K]: s[g(k), n]
+    return (q.astype(np.float64) - 8.0) * scale_nk
+
+
+def dequant_int8(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """W[n, k] = q[n, k] * s[n] ("[Kernel] W8A16 Int8 inside FusedMoE": symmetric
+    per-column, per-expert int8), float64 [N, K]."""
+    return q.astype(np.float64) * np.asarray(s, np.float64)[:, None]
+
+
+def dequant_layer_expert(layer, e: int):
+    """Dequantized (W13_e [2I, H], W2_e [H, I]) of expert e of a canonical layer."""
+    wl = layer.wl
+    if wl.qt == "int4":
+        g13 = None if layer.g13 is None else layer.g13[e]
+        g2 = None if layer.g2 is None else layer.g2[e]
+        w13 = dequant_int4(layer.q13[e], layer.s13[e], g13, wl.group_size)
+        w2 = dequant_int4(layer.q2[e], layer.s2[e], g2, wl.group_size)
+    else:
+        w13 = dequant_int8(layer.q13[e], layer.s13[e])
+        w2 = dequant_int8(layer.q2[e], layer.s2[e])
+    return w13, w2
+
+
+# ----------------------------------------------------------------------------
+# expert FFN and the routed layer
+# ----------------------------------------------------------------------------
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z / (1 + exp(-z))."""
+    return z / (1.0 + np.exp(-z))
+
+
+def expert_ffn(xrows: np.ndarray, w13: np.ndarray, w2: np.ndarray) -> np.ndarray:
+    """y = W2 · (SiLU(gate·x) * (up·x)) for each row x of ``xrows`` [R, H]."""
+    I = w13.shape[0] // 2
+    h = np.asarray(xrows, np.float64) @ w13.T               # [R, 2I]
+    t = silu(h[:, :I]) * h[:, I:]                           # [R, I]
+    return t @ w2.T                                         # [R, H]
+
+
+def moe_forward_rows(layer, x: np.ndarray, topk_ids: np.ndarray,
+                     topk_weights: np.ndarray, rows) -> np.ndarray:
+    """Layer output for the tokens ``rows`` only (each row is independent).
+
+    Returns float64 [len(rows), H].  Used to check sampled tokens of large
+    workloads; ``moe_forward`` is this over all rows.
+    """
+    rows = np.asarray(list(rows), np.int64)
+    E = layer.wl.E
+    ids = np.asarray(topk_ids)[rows]                        # [R, k]
+    w = np.asarray(topk_weights, np.float64)[rows]          # [R, k]
+    R, k = ids.shape
+    H = layer.wl.H
+    y = np.zeros((R, k, H), np.float64)                     # y(m, j)
+    for e in range(E):
+        sel = np.nonzero(ids == e)
+        if sel[0].size == 0:
+            continue
+        w13, w2 = dequant_layer_expert(layer, e)
+        y[sel[0], sel[1], :] = expert_ffn(np.asarray(x, np.float64)[rows[sel[0]]], w13, w2)
+        del w13, w2
+    out = np.zeros((R, H), np.float64)
+    for j in range(k):
+        out += w[:, j:j + 1] * y[:, j, :]
+    return out
+
+
+def moe_forward(layer, x: np.ndarray, topk_ids: np.ndarray,
+                topk_weights: np.ndarray) -> np.ndarray:
+    """out[m] = sum_j topk_weights[m, j] * FFN_{topk_ids[m, j]}(x[m]), float64 [M, H]."""
+    return moe_forward_rows(layer, x, topk_ids, topk_weights, range(np.asarray(x).shape[0]))
+
+
+# ----------------------------------------------------------------------------
+# moe_align_block_size
+# ----------------------------------------------------------------------------
+def moe_align(topk_ids: np.ndarray, E: int, block: int, capacity: int | None = None):
+    """Group token-expert pairs by expert, padded per expert to ``block``.
+
+    Returns (sorted_ids int32 [capacity], expert_ids int32 [ceil(capacity/block)],
+    num_post_padded int).  Default capacity is the worst case P + E*(block-1).
+    """
+    flat = np.asarray(topk_ids).reshape(-1).astype(np.int64)
+    P = flat.size
+    if capacity is None:
+        capacity = P + E * (block - 1)
+    counts = [int(np.count_nonzero(flat == e)) for e in range(E)]
+    padded = [int(math.ceil(c / block)) * block for c in counts]
+    offsets = [0] * E
+    for e in range(1, E):
+        offsets[e] = offsets[e - 1] + padded[e - 1]
+    total = sum(padded)
+    sorted_ids = np.full(capacity, P, np.int32)
+    expert_ids = np.full(-(-capacity // block), -1, np.int32)
+    for e in range(E):
+        pairs = np.nonzero(flat == e)[0]                    # ascending pair index
+        sorted_ids[offsets[e]:offsets[e] + pairs.size] = pairs
+        expert_ids[offsets[e] // block:(offsets[e] + padded[e]) // block] = e
+    return sorted_ids, expert_ids, total

@@ -1,0 +1,268 @@
+"""Seeded generators for the layer's weights, activations and routing.
+
+Shapes and value distributions follow the workloads the pages run the fused
+MoE layer on (Mixtral-8x7B and 8x22B GPTQ int4 group-128 with and without
+act-order, ExpertsInt8 per-column int8 on Mixtral and a DeepSeek-V2-like
+many-expert layer).  Weights are N(0, 0.02) floats quantized offline by
+round-to-nearest (the pages keep quantization off the kernel's path and in
+test utilities), activations are N(0, 1), and router logits are N(0, 1)
+(plus a Zipf(1.1) per-expert bias for the skewed many-expert layer), softmaxed
+with top-k selection and renormalised.
+
+Seeds: weights from ``seed`` (default 0), activations from ``seed + 1`` and
+router logits from ``seed + 2``, each expert's matrices from their own
+sub-stream so that generation can run in parallel and stays reproducible.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    E: int            # experts
+    k: int            # top-k
+    H: int            # hidden size
+    I: int            # expert intermediate size
+    qt: str           # "int4" (group scales, zero point 8) or "int8" (per output column)
+    group_size: int   # 128 for int4, -1 (one group per column) for int8
+    act: str          # activation / scale storage type: "f16" or "bf16"
+    act_order: bool   # int4 only: random per-expert g_idx permutation
+    zipf: float       # 0: unbiased router; >0: Zipf exponent of the per-expert logit bias
+    Ms: tuple         # token counts this workload is measured at
+    w_std: float = 0.02
+
+    def flops(self, M: int) -> float:
+        """Useful FLOPs of one layer call: 2·M·k·3·H·I (padding excluded)."""
+        return 2.0 * M * self.k * 3.0 * self.H * self.I
+
+    def expert_weight_bytes(self) -> int:
+        """Stored weight + scale bytes of one expert (W13 and W2)."""
+        n = 3 * self.H * self.I
+        if self.qt == "int4":
+            return n // 2 + (n // self.group_size) * 2
+        return n + (2 * self.I + self.H) * 4
+
+
+WORKLOADS = {
+    # small layer the oracle finishes in well under a second
+    "tiny": Workload("tiny", 8, 2, 256, 512, "int4", 128, "f16", False, 0.0, (16,)),
+    # Mixtral-8x7B GPTQ int4 g128 (decode sweep)
+    "mixtral8x7b_w4": Workload("mixtral8x7b_w4", 8, 2, 4096, 14336, "int4", 128, "f16",
+                               False, 0.0, (1, 4, 8, 16, 64)),
+    # same shape with act-order g_idx
+    "mixtral8x7b_w4_actorder": Workload("mixtral8x7b_w4_actorder", 8, 2, 4096, 14336, "int4",
+                                        128, "f16", True, 0.0, (1, 16, 128, 512)),
+    # same shape, ExpertsInt8 (per-column int8, bf16 activations)
+    "mixtral8x7b_w8": Workload("mixtral8x7b_w8", 8, 2, 4096, 14336, "int8", -1, "bf16",
+                               False, 0.0, (1, 16, 128, 512)),
+    # DeepSeek-V2-like many-expert layer with a skewed router
+    "deepseekv2_w8": Workload("deepseekv2_w8", 160, 6, 5120, 1536, "int8", -1, "bf16",
+                              False, 1.1, (1, 32, 256, 1024)),
+    # Mixtral-8x22B prefill, tensor-core-bound
+    "mixtral8x22b_w4": Workload("mixtral8x22b_w4", 8, 2, 6144, 16384, "int4", 128, "bf16",
+                                False, 0.0, (2048, 4096, 8192)),
+}
+
+
+# ----------------------------------------------------------------------------
+# storage rounding (float32 arrays holding values exact in the target type)
+# ----------------------------------------------------------------------------
+def round_to_f16(a: np.ndarray) -> np.ndarray:
+    return np.asarray(a, np.float32).astype(np.float16).astype(np.float32)
+
+
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even float32 -> bfloat16, returned as float32."""
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32)
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def round_to(a: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f16":
+        return round_to_f16(a)
+    if dtype == "bf16":
+        return round_to_bf16(a)
+    if dtype == "f32":
+        return np.asarray(a, np.float32)
+    raise ValueError(dtype)
+
+
+def to_u16_bits(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Bit patterns of float32 values that are exact in ``dtype`` (f16/bf16)."""
+    a = np.ascontiguousarray(a, np.float32)
+    if dtype == "f16":
+        return a.astype(np.float16).view(np.uint16)
+    if dtype == "bf16":
+        return (a.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    raise ValueError(dtype)
+
+
+# ----------------------------------------------------------------------------
+# offline round-to-nearest quantizers (test utilities, not the kernel path)
+# ----------------------------------------------------------------------------
+def quantize_int4_rtn(w: np.ndarray, group_size: int, g_idx: np.ndarray | None,
+                      scale_dtype: str):
+    """Symmetric int4 with zero point 8 and one scale per (group, output row).
+
+    w: float32 [N, K]; g_idx: int32 [K] group of each input channel (None:
+    channel k is in group k // group_size).  Returns codes uint8 [N, K] in
+    0..15 and scales float32 [K/G, N] holding values exact in ``scale_dtype``.
+    Scale = absmax/7 of the group (a zero group gets scale 1), rounded to the
+    storage type; codes = clamp(rint(w/scale), -8, 7) + 8.
+    """
+    N, K = w.shape
+    G = group_size
+    ng = K // G
+    if g_idx is None:
+        g_idx = (np.arange(K) // G).astype(np.int32)
+    order = np.argsort(g_idx, kind="stable")
+    grouped = np.abs(w[:, order]).reshape(N, ng, G)
+    absmax = grouped.max(axis=2)                      # [N, ng]
+    s = absmax / np.float32(7.0)
+    s[s == 0] = 1.0
+    s = round_to(s, scale_dtype).astype(np.float32)   # [N, ng]
+    s_el = s[:, g_idx]                                # [N, K]
+    q = np.clip(np.rint(w / s_el), -8, 7) + 8
+    return q.astype(np.uint8), np.ascontiguousarray(s.T)
+
+
+def quantize_int8_rtn(w: np.ndarray):
+    """Symmetric per-output-column int8: scale = absmax/127 (float32), codes in -127..127."""
+    absmax = np.abs(w).max(axis=1)
+    s = (absmax / np.float32(127.0)).astype(np.float32)
+    s[s == 0] = 1.0
+    q = np.clip(np.rint(w / s[:, None]), -127, 127)
+    return q.astype(np.int8), s
+
+
+# ----------------------------------------------------------------------------
+# layer weights
+# ----------------------------------------------------------------------------
+@dataclass
+class QuantLayer:
+    """Canonical (pre-pack) quantized expert weights.
+
+    int4: q13 uint8 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), s13 float32
+          [E, H/G, 2I]; q2 uint8 [E, H, I], s2 float32 [E, I/G, H];
+          g13 int32 [E, H] / g2 int32 [E, I] or None (no act-order).
+    int8: q13 int8 [E, 2I, H], s13 float32 [E, 2I]; q2 int8 [E, H, I],
+          s2 float32 [E, H]; no g_idx.
+    """
+    wl: Workload
+    q13: np.ndarray
+    s13: np.ndarray
+    q2: np.ndarray
+    s2: np.ndarray
+    g13: np.ndarray | None = None
+    g2: np.ndarray | None = None
+    meta: dict = field(default_factory=dict)
+
+
+def _actorder_gidx(rng: np.random.Generator, K: int, G: int) -> np.ndarray:
+    """Random act-order: channel perm[i] lands in group i // G."""
+    perm = rng.permutation(K)
+    g = np.empty(K, np.int32)
+    g[perm] = (np.arange(K) // G).astype(np.int32)
+    return g
+
+
+def _gen_expert(wl: Workload, seed: int, e: int):
+    out = {}
+    for mat, (N, K) in (("13", (2 * wl.I, wl.H)), ("2", (wl.H, wl.I))):
+        sub = 0 if mat == "13" else 1
+        rng = np.random.default_rng([seed, e, sub])
+        w = rng.standard_normal((N, K), dtype=np.float32)
+        w *= np.float32(wl.w_std)
+        if wl.qt == "int4":
+            g = None
+            if wl.act_order:
+                g = _actorder_gidx(np.random.default_rng([seed, e, 2 + sub]), K, wl.group_size)
+            q, s = quantize_int4_rtn(w, wl.group_size, g, wl.act)
+            out[mat] = (q, s, g)
+        else:
+            q, s = quantize_int8_rtn(w)
+            out[mat] = (q, s, None)
+        del w
+    return out
+
+
+def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> QuantLayer:
+    E, H, I = wl.E, wl.H, wl.I
+    if wl.qt == "int4":
+        G = wl.group_size
+        q13 = np.empty((E, 2 * I, H), np.uint8)
+        s13 = np.empty((E, H // G, 2 * I), np.float32)
+        q2 = np.empty((E, H, I), np.uint8)
+        s2 = np.empty((E, I // G, H), np.float32)
+    else:
+        q13 = np.empty((E, 2 * I, H), np.int8)
+        s13 = np.empty((E, 2 * I), np.float32)
+        q2 = np.empty((E, H, I), np.int8)
+        s2 = np.empty((E, H), np.float32)
+    g13 = np.empty((E, H), np.int32) if wl.act_order else None
+    g2 = np.empty((E, I), np.int32) if wl.act_order else None
+
+    def one(e):
+        r = _gen_expert(wl, seed, e)
+        q13[e], s13[e], g = r["13"]
+        if g13 is not None:
+            g13[e] = g
+        q2[e], s2[e], g = r["2"]
+        if g2 is not None:
+            g2[e] = g
+
+    if threads is None:
+        threads = max(1, min(8, os.cpu_count() or 1))
+    big = 3 * H * I > (1 << 22)
+    if threads > 1 and big and E > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(E)))
+    else:
+        for e in range(E):
+            one(e)
+    return QuantLayer(wl, q13, s13, q2, s2, g13, g2)
+
+
+# ----------------------------------------------------------------------------
+# activations and routing
+# ----------------------------------------------------------------------------
+@dataclass
+class Inputs:
+    x: np.ndarray             # float32 [M, H], values exact in the activation type
+    topk_ids: np.ndarray      # int32 [M, k]
+    topk_weights: np.ndarray  # float32 [M, k]
+    logits: np.ndarray        # float32 [M, E]
+
+
+def route_topk(logits: np.ndarray, k: int):
+    """Softmax -> top-k (ties go to the lower expert id) -> renormalise."""
+    z = logits.astype(np.float64)
+    z = z - z.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=1, keepdims=True)
+    ids = np.argsort(-p, axis=1, kind="stable")[:, :k]
+    w = np.take_along_axis(p, ids, axis=1)
+    w /= w.sum(axis=1, keepdims=True)
+    return ids.astype(np.int32), w.astype(np.float32)
+
+
+def make_inputs(wl: Workload, M: int, seed: int = 0) -> Inputs:
+    rx = np.random.default_rng(seed + 1)
+    x = round_to(rx.standard_normal((M, wl.H), dtype=np.float32), wl.act)
+    rr = np.random.default_rng(seed + 2)
+    logits = rr.standard_normal((M, wl.E), dtype=np.float32)
+    if wl.zipf > 0:
+        rank = np.random.default_rng([seed + 2, 1]).permutation(wl.E) + 1
+        logits = logits + (-wl.zipf * np.log(rank)).astype(np.float32)[None, :]
+    ids, w = route_topk(logits, wl.k)
+    return Inputs(x, ids, w, logits.astype(np.float32))

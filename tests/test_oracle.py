@@ -1,0 +1,393 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each check ties the oracle to something other than its own formulas: the
+offline quantizer it inverts, closed forms of layers built from scaled
+permutation matrices, algebraic invariants of the routed sum, a scalar
+brute-force layer, and hand-worked moe_align examples.  A plausible slip in
+the oracle (a dropped zero point, a transposed operand, SiLU on the wrong half,
+a wrong scale or group index, a lost routing weight, an unstable sort) fails
+at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import QuantLayer, Workload, make_inputs, make_layer, quantize_int4_rtn, quantize_int8_rtn
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _wl(**kw):
+    base = dict(name="t", E=4, k=2, H=32, I=64, qt="int4", group_size=16, act="f16",
+                act_order=False, zipf=0.0, Ms=(3,))
+    base.update(kw)
+    return Workload(**base)
+
+
+# ----------------------------------------------------------------------------
+# dequantization vs the offline quantizer
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("act_order", [False, True])
+@pytest.mark.parametrize("sdt", ["f16", "bf16"])
+def test_int4_round_trip(act_order, sdt):
+    rng = np.random.default_rng(5)
+    N, K, G = 48, 256, 32
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    g = None
+    if act_order:
+        perm = rng.permutation(K)
+        g = np.empty(K, np.int32)
+        g[perm] = np.arange(K) // G
+    q, s = quantize_int4_rtn(w, G, g, sdt)
+    assert q.dtype == np.uint8 and q.min() >= 0 and q.max() <= 15
+    assert s.shape == (K // G, N)
+    wh = oracle.dequant_int4(q, s, g, G)
+    gk = (np.arange(K) // G) if g is None else g
+    half_step = 0.5 * s[gk, :].T.astype(np.float64)
+    err = np.abs(w.astype(np.float64) - wh)
+    assert np.all(err <= half_step * (1 + 1e-5) + 1e-12)
+    # the largest code of each group reaches the group's absmax within a step
+    assert np.all(np.abs(wh).max(axis=1) > 0)
+
+
+def test_int4_dequant_hand_values():
+    # two rows, four channels, group size 2; scales are powers of two
+    q = np.array([[8, 9, 0, 15], [7, 8, 12, 4]], np.uint8)
+    s = np.array([[0.5, 0.25], [2.0, 1.0]], np.float32)      # [K/G, N]
+    want = np.array([[0.0, 0.5, -16.0, 14.0], [-0.25, 0.0, 4.0, -4.0]])
+    assert np.array_equal(oracle.dequant_int4(q, s, None, 2), want)
+    # act-order: channels 0 and 3 in group 1, channels 1 and 2 in group 0
+    g = np.array([1, 0, 0, 1], np.int32)
+    want_ao = np.array([[0.0, 0.5, -4.0, 14.0], [-1.0, 0.0, 1.0, -4.0]])
+    assert np.array_equal(oracle.dequant_int4(q, s, g, 2), want_ao)
+
+
+def test_int8_round_trip_and_hand_values():
+    rng = np.random.default_rng(6)
+    w = (rng.standard_normal((40, 96)) * 0.02).astype(np.float32)
+    q, s = quantize_int8_rtn(w)
+    assert q.dtype == np.int8 and q.min() >= -127 and q.max() <= 127
+    wh = oracle.dequant_int8(q, s)
+    assert np.all(np.abs(w - wh) <= 0.5 * s[:, None] * (1 + 1e-5))
+    q2 = np.array([[1, -2], [127, -127]], np.int8)
+    s2 = np.array([0.5, 0.25], np.float32)
+    assert np.array_equal(oracle.dequant_int8(q2, s2), np.array([[0.5, -1.0], [31.75, -31.75]]))
+
+
+# ----------------------------------------------------------------------------
+# closed forms: experts built from scaled permutation matrices
+# ----------------------------------------------------------------------------
+def _perm_layer(qt, E, H, G, act_order, seed):
+    """Gate = diag(a), up = b·P1, down = c·P2 per expert, with a, b, c varying per row.
+
+    Returns the canonical layer plus the per-expert (pi1, pi2, a, b, c) that
+    define the closed form y_h = c_h · SiLU(a_j x_j) · b_j x_{pi1(j)}, j = pi2(h).
+    """
+    I = H
+    rng = np.random.default_rng(seed)
+    wl = _wl(E=E, H=H, I=I, qt=qt, group_size=G if qt == "int4" else -1, act_order=act_order)
+    spec = []
+    if qt == "int4":
+        q13 = np.full((E, 2 * I, H), 8, np.uint8)
+        q2 = np.full((E, H, I), 8, np.uint8)
+        s13 = np.zeros((E, H // G, 2 * I), np.float32)
+        s2 = np.zeros((E, I // G, H), np.float32)
+        g13 = np.zeros((E, H), np.int32) if act_order else None
+        g2 = np.zeros((E, I), np.int32) if act_order else None
+    else:
+        q13 = np.zeros((E, 2 * I, H), np.int8)
+        q2 = np.zeros((E, H, I), np.int8)
+        s13 = np.zeros((E, 2 * I), np.float32)
+        s2 = np.zeros((E, H), np.float32)
+        g13 = g2 = None
+    for e in range(E):
+        pi1 = rng.permutation(H)
+        pi2 = rng.permutation(I)
+        if qt == "int4":
+            ga = np.arange(H) // G
+            gb = np.arange(I) // G
+            if act_order:
+                p = rng.permutation(H); ga = np.empty(H, np.int64); ga[p] = np.arange(H) // G
+                p = rng.permutation(I); gb = np.empty(I, np.int64); gb[p] = np.arange(I) // G
+                g13[e] = ga
+                g2[e] = gb
+            # power-of-two scales that differ by group and by row
+            s13[e] = 2.0 ** -(1 + (np.arange(H // G)[:, None] + np.arange(2 * I)[None, :]) % 4)
+            s2[e] = 2.0 ** -(1 + (2 * np.arange(I // G)[:, None] + np.arange(H)[None, :]) % 3)
+            da = rng.integers(1, 8, I)          # gate code offset from zero point
+            db = rng.integers(-8, 8, I)
+            dc = rng.integers(-8, 8, H)
+            a = np.empty(I); b = np.empty(I); c = np.empty(H)
+            for j in range(I):
+                q13[e, j, j] = 8 + da[j]
+                a[j] = da[j] * s13[e, ga[j], j]
+                q13[e, I + j, pi1[j]] = 8 + db[j]
+                b[j] = db[j] * s13[e, ga[pi1[j]], I + j]
+            for h in range(H):
+                q2[e, h, pi2[h]] = 8 + dc[h]
+                c[h] = dc[h] * s2[e, gb[pi2[h]], h]
+        else:
+            s13[e] = 2.0 ** -(2 + np.arange(2 * I) % 5)
+            s2[e] = 2.0 ** -(1 + np.arange(H) % 3)
+            da = rng.integers(1, 128, I)
+            db = rng.integers(-127, 128, I)
+            dc = rng.integers(-127, 128, H)
+            a = np.empty(I); b = np.empty(I); c = np.empty(H)
+            for j in range(I):
+                q13[e, j, j] = da[j]; a[j] = da[j] * s13[e, j]
+                q13[e, I + j, pi1[j]] = db[j]; b[j] = db[j] * s13[e, I + j]
+            for h in range(H):
+                q2[e, h, pi2[h]] = dc[h]; c[h] = dc[h] * s2[e, h]
+        spec.append((pi1, pi2, a, b, c))
+    return QuantLayer(wl, q13, s13, q2, s2, g13, g2), spec
+
+
+def _closed_form(spec, x, ids, w):
+    M, H = x.shape
+    out = np.zeros((M, H))
+    for m in range(M):
+        for jj in range(ids.shape[1]):
+            pi1, pi2, a, b, c = spec[ids[m, jj]]
+            for h in range(H):
+                j = pi2[h]
+                gate = a[j] * x[m, j]
+                up = b[j] * x[m, pi1[j]]
+                out[m, h] += w[m, jj] * c[h] * (gate / (1.0 + math.exp(-gate))) * up
+    return out
+
+
+@pytest.mark.parametrize("qt,act_order", [("int4", False), ("int4", True), ("int8", False)])
+def test_closed_form_permutation_experts(qt, act_order):
+    E, H = 4, 32
+    layer, spec = _perm_layer(qt, E, H, 8, act_order, seed=11)
+    rng = np.random.default_rng(12)
+    M, k = 5, 2
+    x = rng.standard_normal((M, H))
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(M)]).astype(np.int32)
+    w = rng.random((M, k)).astype(np.float32)
+    got = oracle.moe_forward(layer, x, ids, w)
+    want = _closed_form(spec, x, ids, w.astype(np.float64))
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_topk_all_experts_uniform_is_dense_average():
+    E, H = 4, 16
+    layer, spec = _perm_layer("int4", E, H, 8, False, seed=13)
+    x = np.random.default_rng(14).standard_normal((3, H))
+    ids = np.tile(np.arange(E, dtype=np.int32), (3, 1))
+    w = np.full((3, E), 1.0 / E)
+    got = oracle.moe_forward(layer, x, ids, w)
+    dense = sum(_closed_form(spec, x, np.full((3, 1), e, np.int32), np.ones((3, 1))) for e in range(E)) / E
+    np.testing.assert_allclose(got, dense, rtol=1e-12, atol=1e-13)
+
+
+def test_top1_weight1_is_single_expert():
+    layer, spec = _perm_layer("int8", 3, 16, 8, False, seed=15)
+    x = np.random.default_rng(16).standard_normal((4, 16))
+    for e in range(3):
+        ids = np.full((4, 1), e, np.int32)
+        got = oracle.moe_forward(layer, x, ids, np.ones((4, 1), np.float32))
+        pi1, pi2, a, b, c = spec[e]
+        want = np.empty_like(x)
+        for m in range(4):
+            for h in range(16):
+                j = pi2[h]
+                g = a[j] * x[m, j]
+                want[m, h] = c[h] * g / (1 + math.exp(-g)) * b[j] * x[m, pi1[j]]
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# special cases and invariants on random quantized layers
+# ----------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def small():
+    wl = _wl(E=6, k=2, H=64, I=96, group_size=32, act_order=True)
+    layer = make_layer(wl, seed=3)
+    inp = make_inputs(wl, 7, seed=3)
+    return wl, layer, inp
+
+
+def test_zero_input_gives_zero(small):
+    wl, layer, inp = small
+    out = oracle.moe_forward(layer, np.zeros_like(inp.x), inp.topk_ids, inp.topk_weights)
+    assert np.all(out == 0.0)
+
+
+def test_zero_point_codes_give_zero(small):
+    wl, layer, inp = small
+    flat = QuantLayer(wl, np.full_like(layer.q13, 8), layer.s13, layer.q2, layer.s2, layer.g13, layer.g2)
+    out = oracle.moe_forward(flat, inp.x, inp.topk_ids, inp.topk_weights)
+    assert np.all(out == 0.0)
+    flat2 = QuantLayer(wl, layer.q13, layer.s13, np.full_like(layer.q2, 8), layer.s2, layer.g13, layer.g2)
+    assert np.all(oracle.moe_forward(flat2, inp.x, inp.topk_ids, inp.topk_weights) == 0.0)
+
+
+def test_linear_in_routing_weights(small):
+    wl, layer, inp = small
+    rng = np.random.default_rng(21)
+    w1 = rng.random(inp.topk_weights.shape)
+    w2 = rng.random(inp.topk_weights.shape)
+    o1 = oracle.moe_forward(layer, inp.x, inp.topk_ids, w1)
+    o2 = oracle.moe_forward(layer, inp.x, inp.topk_ids, w2)
+    o12 = oracle.moe_forward(layer, inp.x, inp.topk_ids, w1 + 3.0 * w2)
+    np.testing.assert_allclose(o12, o1 + 3.0 * o2, rtol=1e-11, atol=1e-12)
+
+
+def test_slot_permutation_invariance(small):
+    wl, layer, inp = small
+    o = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    rev = oracle.moe_forward(layer, inp.x, inp.topk_ids[:, ::-1], inp.topk_weights[:, ::-1])
+    np.testing.assert_allclose(rev, o, rtol=1e-12, atol=1e-13)
+
+
+def test_duplicate_expert_in_a_row_is_summed(small):
+    wl, layer, inp = small
+    ids = np.repeat(inp.topk_ids[:, :1], 2, axis=1)
+    w = inp.topk_weights.astype(np.float64)
+    o = oracle.moe_forward(layer, inp.x, ids, w)
+    single = oracle.moe_forward(layer, inp.x, ids[:, :1], (w[:, 0] + w[:, 1])[:, None])
+    np.testing.assert_allclose(o, single, rtol=1e-12, atol=1e-13)
+
+
+def test_actorder_identity_gidx_matches_plain_groups():
+    wl = _wl(E=3, H=64, I=64, group_size=16)
+    layer = make_layer(wl, seed=8)
+    inp = make_inputs(wl, 4, seed=8)
+    ident13 = np.tile((np.arange(64) // 16).astype(np.int32), (3, 1))
+    ident2 = ident13.copy()
+    ao = QuantLayer(wl, layer.q13, layer.s13, layer.q2, layer.s2, ident13, ident2)
+    a = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    b = oracle.moe_forward(ao, inp.x, inp.topk_ids, inp.topk_weights)
+    assert np.array_equal(a, b)
+
+
+def test_actorder_joint_permutation_invariance(small):
+    wl, layer, inp = small
+    rng = np.random.default_rng(9)
+    ph = rng.permutation(wl.H)      # hidden channels: x columns, W13 K dim, g13
+    pi = rng.permutation(wl.I)      # intermediate channels: gate/up rows, W2 K dim, g2
+    rows13 = np.concatenate([pi, wl.I + pi])
+    L2 = QuantLayer(wl,
+                    layer.q13[:, rows13][:, :, ph], layer.s13[:, :, rows13],
+                    layer.q2[:, :, pi], layer.s2,
+                    layer.g13[:, ph], layer.g2[:, pi])
+    # the permuted W2 K order also moves the output rows of W13, so the output
+    # columns of W2 (hidden) stay put while the input columns move with ph
+    o = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    o2 = oracle.moe_forward(L2, inp.x[:, ph], inp.topk_ids, inp.topk_weights)
+    np.testing.assert_allclose(o2, o, rtol=1e-11, atol=1e-12)
+
+
+def _brute_force(layer, x, ids, w):
+    """Scalar loops straight from the definitions, dequantizing inside the dot products."""
+    wl = layer.wl
+    E, H, I = wl.E, wl.H, wl.I
+    M, k = ids.shape
+    out = [[0.0] * H for _ in range(M)]
+
+    def wq13(e, n, c):
+        if wl.qt == "int4":
+            g = c // wl.group_size if layer.g13 is None else int(layer.g13[e, c])
+            return (int(layer.q13[e, n, c]) - 8) * float(layer.s13[e, g, n])
+        return int(layer.q13[e, n, c]) * float(layer.s13[e, n])
+
+    def wq2(e, h, c):
+        if wl.qt == "int4":
+            g = c // wl.group_size if layer.g2 is None else int(layer.g2[e, c])
+            return (int(layer.q2[e, h, c]) - 8) * float(layer.s2[e, g, h])
+        return int(layer.q2[e, h, c]) * float(layer.s2[e, h])
+
+    for m in range(M):
+        for j in range(k):
+            e = int(ids[m, j])
+            t = []
+            for i in range(I):
+                gsum = 0.0
+                usum = 0.0
+                for c in range(H):
+                    gsum += wq13(e, i, c) * float(x[m, c])
+                    usum += wq13(e, I + i, c) * float(x[m, c])
+                t.append(gsum / (1.0 + math.exp(-gsum)) * usum)
+            for h in range(H):
+                acc = 0.0
+                for i in range(I):
+                    acc += wq2(e, h, i) * t[i]
+                out[m][h] += float(w[m, j]) * acc
+    return np.array(out)
+
+
+@pytest.mark.parametrize("qt,act_order", [("int4", False), ("int4", True), ("int8", False)])
+def test_brute_force_tiny(qt, act_order):
+    wl = _wl(E=4, k=2, H=32, I=48, qt=qt, group_size=16 if qt == "int4" else -1, act_order=act_order)
+    layer = make_layer(wl, seed=17)
+    inp = make_inputs(wl, 3, seed=17)
+    got = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    want = _brute_force(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+
+
+def test_forward_rows_match_full(small):
+    wl, layer, inp = small
+    full = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    part = oracle.moe_forward_rows(layer, inp.x, inp.topk_ids, inp.topk_weights, [5, 1])
+    assert np.array_equal(part, full[[5, 1]])
+
+
+# ----------------------------------------------------------------------------
+# moe_align
+# ----------------------------------------------------------------------------
+def test_moe_align_golden():
+    with open(os.path.join(GOLDEN, "moe_align_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        ids = np.array(c["topk_ids"], np.int32)
+        s, ex, n = oracle.moe_align(ids, c["E"], c["block"])
+        assert s.tolist() == c["sorted_ids"], c["name"]
+        assert ex.tolist() == c["expert_ids"], c["name"]
+        assert n == c["num_post_padded"], c["name"]
+
+
+def _align_by_sorting(ids, E, B):
+    """Independent construction: stable sort of valid pairs by (expert, pair)."""
+    flat = [int(v) for v in np.asarray(ids).reshape(-1)]
+    P = len(flat)
+    cap = P + E * (B - 1)
+    order = sorted((p for p in range(P) if 0 <= flat[p] < E), key=lambda p: (flat[p], p))
+    sorted_ids, expert_ids = [], []
+    pos = 0
+    while pos < len(order):
+        e = flat[order[pos]]
+        grp = [p for p in order[pos:] if flat[p] == e]
+        pos += len(grp)
+        while len(grp) % B:
+            grp.append(P)
+        sorted_ids += grp
+        expert_ids += [e] * (len(grp) // B)
+    total = len(sorted_ids)
+    sorted_ids += [P] * (cap - total)
+    expert_ids += [-1] * (-(-cap // B) - len(expert_ids))
+    return sorted_ids, expert_ids, total
+
+
+@pytest.mark.parametrize("M,k,E,B", [(1, 2, 8, 16), (17, 2, 8, 16), (64, 6, 160, 16),
+                                     (33, 2, 8, 64), (100, 4, 16, 1), (5, 8, 3, 4)])
+def test_moe_align_vs_sort_and_invariants(M, k, E, B):
+    rng = np.random.default_rng(M * 131 + E)
+    ids = rng.integers(0, E, (M, k)).astype(np.int32)
+    s, ex, n = oracle.moe_align(ids, E, B)
+    rs, rex, rn = _align_by_sorting(ids, E, B)
+    assert s.tolist() == rs and ex.tolist() == rex and n == rn
+    P = M * k
+    real = s[s < P]
+    assert sorted(real.tolist()) == list(range(P))
+    assert n % B == 0
+    for b in range(n // B):
+        blk = s[b * B:(b + 1) * B]
+        e = ex[b]
+        assert all(ids.reshape(-1)[p] == e for p in blk if p < P)
+    assert np.all(ex[n // B:] == -1)
