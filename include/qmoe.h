@@ -1,0 +1,272 @@
+/*
+ * qmoe.h - C ABI of libqmoe, a GB300 (sm_103a) fused mixture-of-experts layer
+ * whose expert weights are weight-only quantized (W4A16 GPTQ-style int4 with
+ * group scales and optional act-order, or W8A16 per-column int8).
+ *
+ * The layer computed by qmoe_forward, for tokens m = 0..M-1 and top-k slots j:
+ *
+ *     e     = topk_ids[m, j]
+ *     h     = W13_e · x[m]                  (W13_e = [gate_e ; up_e], 2I x H)
+ *     t     = SiLU(h[0:I]) * h[I:2I]
+ *     y     = W2_e · t                      (W2_e: H x I)
+ *     out[m] = sum_j topk_weights[m, j] * y
+ *
+ * with the expert matrices dequantized on the fly:
+ *     int4:  W[n, k] = (q[n, k] - 8) * s[g(k), n],  g(k) = g_idx[k] (act-order) or k / 128
+ *     int8:  W[n, k] = q[n, k] * s[n]
+ *
+ * Sources (web pages on this method):
+ *   "Marlin moe integration" (nm-vllm pull request): the fused MoE kernel takes
+ *     already-quantized INT4 weights and scales on the hot path, quantization
+ *     lives in test utilities; GPTQ 4-bit group-128 checkpoints with and without
+ *     act-order; moe_align_block_size with block size 16; scales normalised to
+ *     the half type on load.
+ *   "[Kernel] W8A16 Int8 inside FusedMoE" (vLLM pull request): symmetric
+ *     per-column, per-expert int8 cast to FP16/BF16 before the matmul; explicit
+ *     W8A16 vs W8A8 naming.
+ *   "Add GPTQ Marlin 2:4 sparse structured support": group 128 or channel-wise,
+ *     4 or 8 bits.
+ *   "[WIP] AWQ Faster Kernels" (vLLM issue): the batch dimension must reach the
+ *     kernel chooser (so M is always an explicit argument here); packed-dimension
+ *     bugs in weight loading (so the packing dimension is documented below).
+ *
+ * Conventions for every entry point:
+ *   - No function allocates memory, and none synchronises the stream except
+ *     qmoe_read_device_status.  All device work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*; NULL is the legacy default stream) and
+ *     runs asynchronously.  Every buffer is owned by the caller.
+ *   - Arguments are validated before anything is launched; on any error
+ *     nothing is launched and the status says why.  No exception crosses the ABI.
+ *   - Device pointers must be device (or managed) memory of the current CUDA
+ *     device; a pointer of another device gives QMOE_ERR_DEVICE_MISMATCH.
+ *   - Faults the host cannot see (a top-k id outside [0, E), a kernel wait that
+ *     ran past its time limit) are recorded in the workspace and read back with
+ *     qmoe_read_device_status.
+ *   - The library is stateless apart from per-device caches of the SM count and
+ *     the driver's tensor-map entry point; calls are thread-safe.
+ */
+#ifndef QMOE_H_
+#define QMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMOE_ABI_VERSION 1
+
+typedef enum {
+  QMOE_OK = 0,
+  QMOE_ERR_INVALID_ARG = 1,     /* bad size, null pointer, misalignment, bad enum */
+  QMOE_ERR_UNSUPPORTED = 2,     /* valid but not implemented (shape, group size, dtype combo) */
+  QMOE_ERR_DEVICE_MISMATCH = 3, /* a pointer is not device memory of the current device */
+  QMOE_ERR_WORKSPACE = 4,       /* workspace null or smaller than qmoe_workspace_size */
+  QMOE_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed */
+  QMOE_ERR_TIMEOUT = 6,         /* device: a pipeline wait ran past its limit and the kernel gave up */
+  QMOE_ERR_BAD_EXPERT_ID = 7    /* device: a top-k id outside [0, E); that pair was dropped */
+} qmoe_status;
+
+typedef enum {
+  QMOE_INT4_GROUP = 1,   /* 4-bit codes 0..15, zero point 8, one scale per 128 input channels */
+  QMOE_INT8_PER_COL = 2  /* signed 8-bit codes, one float32 scale per output feature */
+} qmoe_quant_type;
+
+typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
+
+/*
+ * One MoE layer, weights already packed by qmoe_pack_int4 / qmoe_pack_int8.
+ * All pointers are device memory owned by the caller and must stay valid
+ * while work that uses them is in flight.
+ *
+ *   E, H, I      experts, hidden size, expert intermediate size.
+ *                Constraints: 1 <= E <= 1024; H % 128 == 0; I % 128 == 0.
+ *   group_size   int4: 128 (the only group size built); int8: -1.
+ *   qt           quantization type.
+ *   act_dtype    F16 or BF16: type of x and out, and of the MMA operands.
+ *   scale_dtype  int4: must equal act_dtype (scales are normalised to the
+ *                activation type when packed); int8: F32.
+ *   w13, w2      packed expert weights (sizes: qmoe_packed_bytes), 256-byte aligned.
+ *   s13, s2      int8 only: float32 scales packed by qmoe_pack_int8
+ *                ([E, 2I] in packed row order, [E, H]); NULL for int4 (int4
+ *                scales are inside the packed weights).
+ *   perm13       int4 act-order only: int32 [E, H] written by qmoe_pack_int4
+ *                (hidden channel of each sorted K position); NULL otherwise.
+ *                Act-order of W2 needs no runtime table: it is folded into the
+ *                row order of the packed W13.
+ */
+typedef struct {
+  int32_t E, H, I;
+  int32_t group_size;
+  qmoe_quant_type qt;
+  qmoe_dtype act_dtype;
+  qmoe_dtype scale_dtype;
+  const void* w13;
+  const void* w2;
+  const float* s13;
+  const float* s2;
+  const int32_t* perm13;
+} qmoe_layer;
+
+/*
+ * Optional tuning knobs (zero = automatic).  Results are identical up to
+ * floating-point summation order whatever the knobs say.
+ *   split1, split2  split-K factor of the gate/up and down GEMMs (1..64).
+ *   token_tile      largest number of token rows one GEMM work item carries
+ *                   (multiple of 16, 16..256).
+ */
+typedef struct {
+  int32_t split1;
+  int32_t split2;
+  int32_t token_tile;
+  int32_t reserved[5];
+} qmoe_options;
+
+/* ------------------------------------------------------------------------ */
+/* Weight packing (host memory in, host memory out; off the hot path).       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of one packed matrix for all E experts: W13 is (rows = 2I, K = H),
+ * W2 is (rows = H, K = I).  Returns 0 for an unsupported combination.
+ * int4: E * (rows/128) * (K/128) * 8448; int8: E * (rows/128) * (K/128) * 16384.
+ */
+size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K, int32_t group_size);
+
+/*
+ * Pack int4 GPTQ-style weights ("Marlin moe integration": the kernel receives
+ * already-quantized INT4 weights and scales; GPTQ group 128, act-order).
+ * Canonical inputs (host, row-major, one code per byte, packing dimension = K):
+ *   q13 uint8 [E, 2I, H] codes 0..15 (rows 0..I-1 gate, I..2I-1 up)
+ *   s13 uint16 [E, H/128, 2I] scale bit patterns of scale_dtype (f16 or bf16)
+ *   g13 int32 [E, H] group of each hidden channel, or NULL (group = k/128)
+ *   q2  uint8 [E, H, I],  s2 uint16 [E, I/128, H],  g2 int32 [E, I] or NULL
+ * Outputs (host): w13_packed, w2_packed (qmoe_packed_bytes each) and, when
+ * g13 != NULL, perm13_out int32 [E, H]; perm13_out is ignored when g13 == NULL.
+ * Act-order requires every group to hold exactly 128 channels (as GPTQ's
+ * act-order produces); otherwise QMOE_ERR_UNSUPPORTED.  Codes above 15 give
+ * QMOE_ERR_INVALID_ARG.
+ */
+qmoe_status qmoe_pack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                           const uint8_t* q13, const uint16_t* s13, const int32_t* g13,
+                           const uint8_t* q2, const uint16_t* s2, const int32_t* g2,
+                           void* w13_packed, void* w2_packed, int32_t* perm13_out);
+
+/* Exact inverse of qmoe_pack_int4 given the same g13 / g2 (round-trip checks). */
+qmoe_status qmoe_unpack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size,
+                             const void* w13_packed, const void* w2_packed,
+                             const int32_t* g13, const int32_t* g2,
+                             uint8_t* q13, uint16_t* s13, uint8_t* q2, uint16_t* s2);
+
+/*
+ * Pack W8A16 per-column int8 ("[Kernel] W8A16 Int8 inside FusedMoE":
+ * symmetric per-column, per-expert int8).  Canonical inputs (host):
+ *   q13 int8 [E, 2I, H], s13 float [E, 2I]; q2 int8 [E, H, I], s2 float [E, H].
+ * Outputs (host): w13_packed, w2_packed, s13_packed float [E, 2I] (packed row
+ * order), s2_packed float [E, H].  Codes of -128 give QMOE_ERR_INVALID_ARG.
+ */
+qmoe_status qmoe_pack_int8(int32_t E, int32_t H, int32_t I,
+                           const int8_t* q13, const float* s13, const int8_t* q2, const float* s2,
+                           void* w13_packed, float* s13_packed, void* w2_packed, float* s2_packed);
+
+/* Exact inverse of qmoe_pack_int8. */
+qmoe_status qmoe_unpack_int8(int32_t E, int32_t H, int32_t I,
+                             const void* w13_packed, const float* s13_packed,
+                             const void* w2_packed, const float* s2_packed,
+                             int8_t* q13, float* s13, int8_t* q2, float* s2);
+
+/* ------------------------------------------------------------------------ */
+/* moe_align_block_size                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Group the P = M*top_k token-expert pairs by expert and pad each group to a
+ * multiple of `block` ("Marlin moe integration": moe_align_block_size_kernel,
+ * block size 16 tied to the kernel tile).  Deterministic and stable:
+ *   sorted_ids      int32 [capacity]: experts in ascending id, each expert's
+ *                   pair indices p = m*top_k + j ascending, padded with P;
+ *                   the tail past the padded total also holds P.
+ *   expert_ids      int32 [ceil(capacity/block)]: expert of each block; -1
+ *                   for blocks past the padded total.
+ *   num_post_padded int32 [1]: padded total (a multiple of block).
+ * Device inputs: topk_ids int32 [M, top_k].  Requirements: 1 <= E <= 1024,
+ * 1 <= block <= 256, capacity >= M*top_k + E*(block-1), M*top_k < 2^31.
+ * Ids outside [0, E) are dropped (not placed).  M == 0 is valid.
+ */
+qmoe_status qmoe_moe_align(const int32_t* topk_ids, int64_t M, int32_t top_k, int32_t E, int32_t block,
+                           int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                           int64_t capacity, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Forward                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes qmoe_forward needs for this layer, M and top_k (0 on invalid input). */
+size_t qmoe_workspace_size(const qmoe_layer* layer, int64_t M, int32_t top_k);
+size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts);
+
+/*
+ * out[M, H] (act_dtype, overwritten) = the layer applied to x[M, H] (act_dtype)
+ * with routing topk_ids int32 [M, top_k] and topk_weights float32 [M, top_k].
+ * All buffers are device memory; x, out and the workspace 256-byte aligned.
+ * workspace: at least qmoe_workspace_size bytes; its contents need no
+ * initialisation and are scratch after the call.  Two forwards that share a
+ * workspace must be ordered on the GPU (same stream or events).
+ * Requirements: 1 <= top_k <= E; M*top_k < 2^31.  M == 0 launches nothing.
+ */
+qmoe_status qmoe_forward(const qmoe_layer* layer, const void* x, int64_t M,
+                         const int32_t* topk_ids, const float* topk_weights, int32_t top_k,
+                         void* out, void* workspace, size_t workspace_bytes, void* stream);
+qmoe_status qmoe_forward_ex(const qmoe_layer* layer, const void* x, int64_t M,
+                            const int32_t* topk_ids, const float* topk_weights, int32_t top_k,
+                            void* out, void* workspace, size_t workspace_bytes, void* stream,
+                            const qmoe_options* opts);
+
+/*
+ * qmoe_forward_ex with CUDA events recorded around each kernel launch, for
+ * measuring per-kernel device time inside a timed region.  `events` holds
+ * n_events (>= 12) cudaEvent_t handles created by the caller; for launch i
+ * (0 moe_align, 1 token gather, 2 gate/up GEMM, 3 split-K SiLU reduce,
+ * 4 down GEMM, 5 output reduce) event 2i is recorded on `stream` just before
+ * it and event 2i+1 just after.  A launch the plan skips (3 when the gate/up
+ * GEMM is not split) gets both events at the same point.  *n_launches
+ * (optional) receives the number of kernels launched.  Null events give
+ * QMOE_ERR_INVALID_ARG.
+ */
+qmoe_status qmoe_forward_profiled(const qmoe_layer* layer, const void* x, int64_t M,
+                                  const int32_t* topk_ids, const float* topk_weights, int32_t top_k,
+                                  void* out, void* workspace, size_t workspace_bytes, void* stream,
+                                  const qmoe_options* opts, void* const* events, int32_t n_events,
+                                  int32_t* n_launches);
+
+/*
+ * Same layer with x, topk_ids, topk_weights and out in HOST memory (page-locked
+ * memory makes the copies asynchronous).  The call enqueues the host-to-device
+ * copies of the inputs, the forward, and the device-to-host copy of out on
+ * `stream`; out is valid once the stream has been synchronised.  The workspace
+ * (device) must hold qmoe_workspace_size_host bytes: the device staging of the
+ * inputs and output lives in it.
+ */
+size_t qmoe_workspace_size_host(const qmoe_layer* layer, int64_t M, int32_t top_k);
+qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64_t M,
+                              const int32_t* topk_ids_host, const float* topk_weights_host, int32_t top_k,
+                              void* out_host, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream` and return the first device-side fault recorded in
+ * `workspace` by the most recent forward that used it (QMOE_OK if none).
+ */
+qmoe_status qmoe_read_device_status(const void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* qmoe_status_string(qmoe_status status);
+
+/* QMOE_ABI_VERSION of the loaded library. */
+int32_t qmoe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_H_ */

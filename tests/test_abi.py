@@ -1,0 +1,156 @@
+"""Host-side checks of libqmoe (no GPU): the library loads, exports every
+function include/qmoe.h declares, packs weights in the documented layout with
+a bit-exact round trip, and rejects bad arguments before touching a device."""
+import ctypes
+import re
+
+import numpy as np
+import pytest
+
+import weight_only_quantized_moe_gb300 as q
+from weight_only_quantized_moe_gb300 import _native as N
+from synth import Workload, make_layer, to_u16_bits
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    from weight_only_quantized_moe_gb300 import build
+    build.build()
+    return q.lib()
+
+
+def _declared_functions():
+    text = open(N.HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmoe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert len(names) >= 15
+    dll = ctypes.CDLL(N.LIB_PATH)
+    missing = [n for n in names if not hasattr(dll, n)]
+    assert not missing, missing
+    assert q.lib().qmoe_abi_version() == 1
+    for s in range(0, 8):
+        assert q.status_string(s)
+
+
+def _wl(qt, act_order=False, E=3, H=256, I=384):
+    return Workload("t", E, 2, H, I, qt, 128 if qt == "int4" else -1, "bf16" if qt == "int8" else "f16",
+                    act_order, 0.0, (1,))
+
+
+@pytest.mark.parametrize("act_order", [False, True])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_pack_int4_round_trip(act_order, act):
+    wl = _wl("int4", act_order)
+    wl = Workload(wl.name, wl.E, wl.k, wl.H, wl.I, "int4", 128, act, act_order, 0.0, (1,))
+    L = make_layer(wl, seed=2)
+    s13b, s2b = to_u16_bits(L.s13, act), to_u16_bits(L.s2, act)
+    pk = q.qmoe_pack_int4(wl.E, wl.H, wl.I, act, L.q13, s13b, L.g13, L.q2, s2b, L.g2)
+    assert pk["w13"].nbytes == wl.E * (2 * wl.I // 128) * (wl.H // 128) * 8448
+    q13, s13, q2, s2 = q.qmoe_unpack_int4(wl.E, wl.H, wl.I, pk["w13"], pk["w2"], L.g13, L.g2)
+    assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
+    assert np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
+    if act_order:
+        # perm13 lists each expert's hidden channels by group, ascending inside a group
+        for e in range(wl.E):
+            p = pk["perm13"][e]
+            assert sorted(p.tolist()) == list(range(wl.H))
+            g = L.g13[e][p]
+            assert np.all(np.diff(g) >= 0)
+            assert all(np.all(np.diff(p[g == gg]) > 0) for gg in range(wl.H // 128))
+
+
+def test_pack_int4_layout_matches_documented_nibble_order():
+    # one expert, gate row 0 and up row 0 carry distinct codes along K
+    E, H, I = 1, 128, 128
+    q13 = np.full((E, 2 * I, H), 8, np.uint8)
+    q13[0, 0, :] = np.arange(H) % 16          # gate channel 0 -> packed row 0
+    q13[0, I, :] = (np.arange(H) * 7) % 16    # up channel 0 -> packed row 1
+    s13 = np.full((E, 1, 2 * I), 0x3C00, np.uint16)
+    s13[0, 0, I] = 0x4000
+    q2 = np.full((E, H, I), 8, np.uint8)
+    s2 = np.full((E, 1, H), 0x3C00, np.uint16)
+    pk = q.qmoe_pack_int4(E, H, I, "f16", q13, s13, None, q2, s2, None)
+    blk = pk["w13"][:8448]                   # tile 0, K stage 0
+    for r, codes in ((0, q13[0, 0]), (1, q13[0, I])):
+        for c in range(4):
+            for j in range(4):
+                word = int.from_bytes(bytes(blk[(c * 128 + r) * 16 + 4 * j:(c * 128 + r) * 16 + 4 * j + 4]), "little")
+                for i in range(4):
+                    k0 = 32 * c + 8 * j + 2 * i
+                    assert (word >> (4 * i)) & 15 == codes[k0]
+                    assert (word >> (4 * (i + 4))) & 15 == codes[k0 + 1]
+    assert int.from_bytes(bytes(blk[8192:8194]), "little") == 0x3C00
+    assert int.from_bytes(bytes(blk[8194:8196]), "little") == 0x4000
+
+
+def test_pack_int8_round_trip():
+    wl = _wl("int8")
+    L = make_layer(wl, seed=4)
+    pk = q.qmoe_pack_int8(wl.E, wl.H, wl.I, L.q13, L.s13, L.q2, L.s2)
+    q13, s13, q2, s2 = q.qmoe_unpack_int8(wl.E, wl.H, wl.I, pk["w13"], pk["s13"], pk["w2"], pk["s2"])
+    assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
+    assert np.array_equal(s13, L.s13) and np.array_equal(s2, L.s2)
+    # packed row order interleaves gate and up channels
+    assert np.array_equal(pk["s13"][0, 0::2], L.s13[0, :wl.I])
+    assert np.array_equal(pk["s13"][0, 1::2], L.s13[0, wl.I:])
+
+
+def test_pack_rejects_bad_codes_and_groups():
+    E, H, I = 1, 128, 128
+    q13 = np.full((E, 2 * I, H), 8, np.uint8)
+    s = np.full((E, 1, 2 * I), 0x3C00, np.uint16)
+    q2 = np.full((E, H, I), 8, np.uint8)
+    s2 = np.full((E, 1, H), 0x3C00, np.uint16)
+    bad = q13.copy()
+    bad[0, 3, 5] = 16
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_pack_int4(E, H, I, "f16", bad, s, None, q2, s2, None)
+    assert ei.value.status == q.QMOE_ERR_INVALID_ARG
+    g = np.zeros((E, H), np.int32)
+    g[0, :64] = 0
+    g[0, 64:] = 1  # group 1 does not exist for H = 128
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_pack_int4(E, H, I, "f16", q13, s, g, q2, s2, None)
+    assert ei.value.status == q.QMOE_ERR_UNSUPPORTED
+    q8 = np.zeros((E, 2 * I, H), np.int8)
+    q8[0, 0, 0] = -128
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_pack_int8(E, H, I, q8, np.ones((E, 2 * I), np.float32), np.zeros((E, H, I), np.int8),
+                         np.ones((E, H), np.float32))
+    assert ei.value.status == q.QMOE_ERR_INVALID_ARG
+
+
+def _layer_struct(**kw):
+    base = dict(E=8, H=256, I=512, group_size=128, qt=N.QMOE_INT4_GROUP, act_dtype=N.QMOE_F16,
+                scale_dtype=N.QMOE_F16, w13=None, w2=None, s13=None, s2=None, perm13=None)
+    base.update(kw)
+    return N.QmoeLayer(**base)
+
+
+def test_workspace_size_and_validation_are_host_only():
+    L = q.lib()
+    ok = _layer_struct()
+    n = L.qmoe_workspace_size(ctypes.byref(ok), 16, 2)
+    assert n > 0 and n % 256 == 0
+    assert L.qmoe_workspace_size(ctypes.byref(ok), 4096, 2) > n
+    assert L.qmoe_workspace_size_host(ctypes.byref(ok), 16, 2) > n
+    for bad in (_layer_struct(H=200), _layer_struct(I=100), _layer_struct(E=0), _layer_struct(E=2000),
+                _layer_struct(group_size=64), _layer_struct(scale_dtype=N.QMOE_BF16),
+                _layer_struct(qt=N.QMOE_INT8_PER_COL, group_size=-1, scale_dtype=N.QMOE_F16),
+                _layer_struct(act_dtype=N.QMOE_F32, scale_dtype=N.QMOE_F32)):
+        assert L.qmoe_workspace_size(ctypes.byref(bad), 16, 2) == 0
+    assert L.qmoe_workspace_size(ctypes.byref(ok), 16, 9) == 0     # top_k > E
+    assert L.qmoe_workspace_size(ctypes.byref(ok), -1, 2) == 0
+    # forward rejects before any device access
+    st = L.qmoe_forward(ctypes.byref(_layer_struct(H=200)), None, 4, None, None, 2, None, None, 0, None)
+    assert st == q.QMOE_ERR_UNSUPPORTED
+    st = L.qmoe_forward(ctypes.byref(ok), None, 4, None, None, 2, None, None, 0, None)
+    assert st == q.QMOE_ERR_WORKSPACE
+    # moe_align argument checks
+    assert L.qmoe_moe_align(None, 4, 2, 8, 16, None, None, None, 1000, None) == q.QMOE_ERR_INVALID_ARG
+    assert L.qmoe_moe_align(None, 4, 2, 8, 0, None, None, None, 1000, None) == q.QMOE_ERR_INVALID_ARG
+    assert L.qmoe_moe_align(None, 4, 2, 8, 16, None, None, None, 10, None) == q.QMOE_ERR_INVALID_ARG

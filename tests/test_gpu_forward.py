@@ -1,0 +1,147 @@
+"""The fused layer on the GPU (through the C ABI) against the float64 oracle.
+
+Shapes are small enough for the oracle to finish in seconds yet span several
+128-row weight tiles, several 128-wide K stages, ragged token chunks, split-K
+and multi-chunk experts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_quantized_moe_gb300 as q
+from synth import Inputs, Workload, make_inputs, make_layer, route_topk
+from tests.gpu_util import assert_parity, device_inputs, device_layer, ensure_built, run_forward
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _wl(qt="int4", act="f16", act_order=False, E=8, k=2, H=384, I=256, zipf=0.0):
+    return Workload(f"t_{qt}_{act}_{act_order}", E, k, H, I, qt, 128 if qt == "int4" else -1, act, act_order,
+                    zipf, (1,))
+
+
+_LAYERS = {}
+
+
+def _layer(wl, seed=0):
+    key = (wl, seed)
+    if key not in _LAYERS:
+        L = make_layer(wl, seed=seed)
+        _LAYERS[key] = (L, device_layer(L))
+    return _LAYERS[key]
+
+
+def _check(wl, M, seed=0, opts=None, inp=None, what=""):
+    L, dl = _layer(wl)
+    if inp is None:
+        inp = make_inputs(wl, M, seed=seed + 10)
+    x, ids, w = device_inputs(wl, inp)
+    out, _ = run_forward(dl, x, ids, w, opts=opts)
+    got = out.float().cpu().numpy()
+    ref = oracle.moe_forward(L, inp.x, inp.topk_ids, inp.topk_weights)
+    return assert_parity(got, ref, what or f"{wl.name} M={M}")
+
+
+VARIANTS = [("int4", "f16", False), ("int4", "bf16", False), ("int4", "f16", True), ("int4", "bf16", True),
+            ("int8", "bf16", False), ("int8", "f16", False)]
+
+
+@pytest.mark.parametrize("qt,act,ao", VARIANTS)
+@pytest.mark.parametrize("M", [1, 7, 64, 129])
+def test_forward_parity(qt, act, ao, M):
+    _check(_wl(qt, act, ao), M)
+
+
+@pytest.mark.parametrize("qt,act,ao", VARIANTS[:1] + VARIANTS[3:5])
+@pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 256), (3, 2, 32)])
+def test_forward_forced_split_and_tile(qt, act, ao, split1, split2, tile):
+    _check(_wl(qt, act, ao), 40, opts=q.make_options(split1, split2, tile))
+
+
+def test_multi_chunk_expert_and_empty_experts():
+    wl = _wl("int4", "bf16")
+    M = 300
+    base = make_inputs(wl, M, seed=21)
+    ids = base.topk_ids.copy()
+    ids[:, 0] = 3                          # expert 3 takes every token -> several chunks
+    ids[:, 1] = np.where(ids[:, 1] == 3, 5, ids[:, 1])
+    ids[::7, 1] = 6
+    inp = Inputs(base.x, ids.astype(np.int32), base.topk_weights, base.logits)
+    _check(wl, M, inp=inp, what="one hot expert")
+
+
+def test_many_experts_topk6_skewed():
+    wl = _wl("int8", "bf16", E=160, k=6, H=256, I=256, zipf=1.1)
+    for M in (1, 5, 96):
+        _check(wl, M)
+
+
+def test_many_experts_int4_actorder():
+    wl = _wl("int4", "f16", True, E=64, k=4, H=256, I=384)
+    _check(wl, 33)
+
+
+def test_deterministic_and_host_path_identical():
+    wl = _wl("int4", "f16", True)
+    L, dl = _layer(wl)
+    inp = make_inputs(wl, 50, seed=5)
+    x, ids, w = device_inputs(wl, inp)
+    a, _ = run_forward(dl, x, ids, w)
+    b, _ = run_forward(dl, x, ids, w)
+    assert torch.equal(a, b)
+    xh = x.cpu().pin_memory()
+    idsh = ids.cpu().pin_memory()
+    wh = w.cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    ws = q.alloc_workspace(q.qmoe_workspace_size_host(dl, 50, wl.k))
+    q.qmoe_forward_host(dl, xh, idsh, wh, outh, ws)
+    assert q.qmoe_read_device_status(ws) == q.QMOE_OK
+    assert torch.equal(outh, a.cpu())
+
+
+def test_zero_tokens_is_a_no_op():
+    wl = _wl()
+    _, dl = _layer(wl)
+    x = torch.empty((0, wl.H), dtype=torch.float16, device="cuda")
+    ids = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    w = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    out = q.qmoe_forward(dl, x, ids, w, workspace=q.alloc_workspace(256))
+    assert out.shape == (0, wl.H)
+
+
+def test_bad_expert_id_is_reported_and_dropped():
+    wl = _wl()
+    L, dl = _layer(wl)
+    inp = make_inputs(wl, 6, seed=8)
+    ids = inp.topk_ids.copy()
+    ids[2, 1] = 99
+    x, dids, w = device_inputs(wl, Inputs(inp.x, ids, inp.topk_weights, inp.logits))
+    out, st = run_forward(dl, x, dids, w, check_status=False)
+    assert st == q.QMOE_ERR_BAD_EXPERT_ID
+    wts = inp.topk_weights.copy()
+    wts[2, 1] = 0.0
+    ids_ok = ids.copy()
+    ids_ok[2, 1] = 0
+    ref = oracle.moe_forward(L, inp.x, ids_ok, wts)
+    assert_parity(out.float().cpu().numpy(), ref, "bad id dropped")
+
+
+def test_rejects_wrong_device_pointer_and_small_workspace():
+    wl = _wl()
+    _, dl = _layer(wl)
+    inp = make_inputs(wl, 4, seed=1)
+    x, ids, w = device_inputs(wl, inp)
+    ws = q.alloc_workspace(q.qmoe_workspace_size(dl, 4, 2) - 1024)
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_forward(dl, x, ids, w, workspace=ws)
+    assert ei.value.status == q.QMOE_ERR_WORKSPACE
+    ws = q.alloc_workspace(q.qmoe_workspace_size(dl, 4, 2))
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_forward(dl, x.cpu(), ids, w, workspace=ws)
+    assert ei.value.status == q.QMOE_ERR_DEVICE_MISMATCH

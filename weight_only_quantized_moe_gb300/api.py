@@ -1,0 +1,252 @@
+"""Python face of libqmoe with the C ABI's names (argument marshalling only).
+
+Host packing takes and returns numpy arrays; the forward and moe_align take
+torch CUDA tensors and run on the current torch stream unless one is given.
+"""
+from __future__ import annotations
+
+from ctypes import POINTER, byref, c_float, c_int32, c_uint8, c_uint16, c_void_p
+
+import numpy as np
+import torch
+
+from . import _native as N
+
+_ACT = {"f16": N.QMOE_F16, "bf16": N.QMOE_BF16}
+_TORCH_ACT = {"f16": torch.float16, "bf16": torch.bfloat16}
+_QT = {"int4": N.QMOE_INT4_GROUP, "int8": N.QMOE_INT8_PER_COL}
+
+
+def _np_ptr(a, ctype):
+    return None if a is None else a.ctypes.data_as(POINTER(ctype))
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+def packed_bytes(qt: str, E: int, rows: int, K: int) -> int:
+    return int(N.lib().qmoe_packed_bytes(_QT[qt], E, rows, K, 128 if qt == "int4" else -1))
+
+
+# ----------------------------------------------------------------------------
+# packing (host)
+# ----------------------------------------------------------------------------
+def qmoe_pack_int4(E, H, I, scale_dtype, q13, s13_bits, g13, q2, s2_bits, g2):
+    """Pack canonical int4 weights (see include/qmoe.h).  Scales are uint16 bit patterns."""
+    q13 = np.ascontiguousarray(q13, np.uint8)
+    q2 = np.ascontiguousarray(q2, np.uint8)
+    s13_bits = np.ascontiguousarray(s13_bits, np.uint16)
+    s2_bits = np.ascontiguousarray(s2_bits, np.uint16)
+    g13 = None if g13 is None else np.ascontiguousarray(g13, np.int32)
+    g2 = None if g2 is None else np.ascontiguousarray(g2, np.int32)
+    w13 = np.empty(packed_bytes("int4", E, 2 * I, H), np.uint8)
+    w2 = np.empty(packed_bytes("int4", E, H, I), np.uint8)
+    perm13 = np.empty((E, H), np.int32) if g13 is not None else None
+    st = N.lib().qmoe_pack_int4(E, H, I, 128, _ACT[scale_dtype], _np_ptr(q13, c_uint8), _np_ptr(s13_bits, c_uint16),
+                                _np_ptr(g13, c_int32), _np_ptr(q2, c_uint8), _np_ptr(s2_bits, c_uint16),
+                                _np_ptr(g2, c_int32), w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
+                                _np_ptr(perm13, c_int32))
+    N.check(st, "qmoe_pack_int4")
+    return {"w13": w13, "w2": w2, "perm13": perm13}
+
+
+def qmoe_unpack_int4(E, H, I, w13, w2, g13, g2):
+    q13 = np.empty((E, 2 * I, H), np.uint8)
+    s13 = np.empty((E, H // 128, 2 * I), np.uint16)
+    q2 = np.empty((E, H, I), np.uint8)
+    s2 = np.empty((E, I // 128, H), np.uint16)
+    g13 = None if g13 is None else np.ascontiguousarray(g13, np.int32)
+    g2 = None if g2 is None else np.ascontiguousarray(g2, np.int32)
+    st = N.lib().qmoe_unpack_int4(E, H, I, 128, w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
+                                  _np_ptr(g13, c_int32), _np_ptr(g2, c_int32), _np_ptr(q13, c_uint8),
+                                  _np_ptr(s13, c_uint16), _np_ptr(q2, c_uint8), _np_ptr(s2, c_uint16))
+    N.check(st, "qmoe_unpack_int4")
+    return q13, s13, q2, s2
+
+
+def qmoe_pack_int8(E, H, I, q13, s13, q2, s2):
+    q13 = np.ascontiguousarray(q13, np.int8)
+    q2 = np.ascontiguousarray(q2, np.int8)
+    s13 = np.ascontiguousarray(s13, np.float32)
+    s2 = np.ascontiguousarray(s2, np.float32)
+    w13 = np.empty(packed_bytes("int8", E, 2 * I, H), np.uint8)
+    w2 = np.empty(packed_bytes("int8", E, H, I), np.uint8)
+    s13p = np.empty((E, 2 * I), np.float32)
+    s2p = np.empty((E, H), np.float32)
+    st = N.lib().qmoe_pack_int8(E, H, I, q13.ctypes.data_as(c_void_p), _np_ptr(s13, c_float),
+                                q2.ctypes.data_as(c_void_p), _np_ptr(s2, c_float), w13.ctypes.data_as(c_void_p),
+                                _np_ptr(s13p, c_float), w2.ctypes.data_as(c_void_p), _np_ptr(s2p, c_float))
+    N.check(st, "qmoe_pack_int8")
+    return {"w13": w13, "w2": w2, "s13": s13p, "s2": s2p}
+
+
+def qmoe_unpack_int8(E, H, I, w13, s13p, w2, s2p):
+    q13 = np.empty((E, 2 * I, H), np.int8)
+    s13 = np.empty((E, 2 * I), np.float32)
+    q2 = np.empty((E, H, I), np.int8)
+    s2 = np.empty((E, H), np.float32)
+    st = N.lib().qmoe_unpack_int8(E, H, I, w13.ctypes.data_as(c_void_p), _np_ptr(s13p, c_float),
+                                  w2.ctypes.data_as(c_void_p), _np_ptr(s2p, c_float), q13.ctypes.data_as(c_void_p),
+                                  _np_ptr(s13, c_float), q2.ctypes.data_as(c_void_p), _np_ptr(s2, c_float))
+    N.check(st, "qmoe_unpack_int8")
+    return q13, s13, q2, s2
+
+
+def _scale_bits(s: np.ndarray, act: str) -> np.ndarray:
+    """uint16 bit patterns of float32 scales that are exact in the activation type."""
+    t = torch.from_numpy(np.ascontiguousarray(s, np.float32)).to(_TORCH_ACT[act])
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# device layer
+# ----------------------------------------------------------------------------
+class DeviceLayer:
+    """A packed layer resident on one CUDA device plus its C descriptor."""
+
+    def __init__(self, qt, E, H, I, act, w13, w2, s13=None, s2=None, perm13=None):
+        self.qt, self.E, self.H, self.I, self.act = qt, E, H, I, act
+        self.w13, self.w2, self.s13, self.s2, self.perm13 = w13, w2, s13, s2, perm13
+        self.struct = N.QmoeLayer(
+            E, H, I, 128 if qt == "int4" else -1, _QT[qt], _ACT[act],
+            _ACT[act] if qt == "int4" else N.QMOE_F32,
+            w13.data_ptr(), w2.data_ptr(),
+            None if s13 is None else s13.data_ptr(), None if s2 is None else s2.data_ptr(),
+            None if perm13 is None else perm13.data_ptr())
+
+    @property
+    def torch_dtype(self):
+        return _TORCH_ACT[self.act]
+
+    def weight_bytes(self) -> int:
+        n = self.w13.numel() + self.w2.numel()
+        if self.s13 is not None:
+            n += 4 * (self.s13.numel() + self.s2.numel())
+        return n
+
+    @classmethod
+    def from_packed(cls, qt, E, H, I, act, packed, device="cuda"):
+        def dev(a, dt=None):
+            if a is None:
+                return None
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        return cls(qt, E, H, I, act, dev(packed["w13"]), dev(packed["w2"]),
+                   dev(packed.get("s13")) if qt == "int8" else None,
+                   dev(packed.get("s2")) if qt == "int8" else None,
+                   dev(packed.get("perm13")))
+
+    @classmethod
+    def from_canonical(cls, qt, act, q13, s13, q2, s2, g13=None, g2=None, device="cuda"):
+        """Pack canonical codes/scales on the host and upload them.
+
+        int4: q uint8 codes, s float32 [E, K/128, N] (exact in ``act``), g int32 or None.
+        int8: q int8 codes, s float32 [E, N].
+        """
+        E, N2, H = q13.shape
+        I = N2 // 2
+        if qt == "int4":
+            packed = qmoe_pack_int4(E, H, I, act, q13, _scale_bits(s13, act), g13, q2, _scale_bits(s2, act), g2)
+        else:
+            packed = qmoe_pack_int8(E, H, I, q13, s13, q2, s2)
+        return cls.from_packed(qt, E, H, I, act, packed, device)
+
+
+# ----------------------------------------------------------------------------
+# device entry points
+# ----------------------------------------------------------------------------
+def make_options(split1=0, split2=0, token_tile=0):
+    return N.QmoeOptions(split1, split2, token_tile)
+
+
+def qmoe_moe_align(topk_ids: torch.Tensor, E: int, block: int, capacity: int | None = None, stream=None):
+    assert topk_ids.is_cuda and topk_ids.dtype == torch.int32 and topk_ids.is_contiguous()
+    M, k = topk_ids.shape
+    P = M * k
+    if capacity is None:
+        capacity = P + E * (block - 1)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(max(capacity, 1), dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(max(-(-capacity // block), 1), dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    st = N.lib().qmoe_moe_align(c_void_p(topk_ids.data_ptr()), M, k, E, block, c_void_p(sorted_ids.data_ptr()),
+                                c_void_p(expert_ids.data_ptr()), c_void_p(npp.data_ptr()), capacity,
+                                _stream_ptr(stream))
+    N.check(st, "qmoe_moe_align")
+    return sorted_ids[:capacity], expert_ids[:-(-capacity // block)], npp
+
+
+def qmoe_workspace_size(layer: DeviceLayer, M: int, k: int, opts=None) -> int:
+    if opts is None:
+        n = N.lib().qmoe_workspace_size(byref(layer.struct), M, k)
+    else:
+        n = N.lib().qmoe_workspace_size_ex(byref(layer.struct), M, k, byref(opts))
+    if n == 0 and M > 0:
+        raise N.QmoeError(N.QMOE_ERR_INVALID_ARG, "qmoe_workspace_size")
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def qmoe_forward(layer: DeviceLayer, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, opts=None, stream=None):
+    M, H = x.shape
+    k = topk_ids.shape[1]
+    assert x.dtype == layer.torch_dtype and x.is_contiguous() and H == layer.H
+    assert topk_ids.dtype == torch.int32 and topk_weights.dtype == torch.float32
+    assert topk_ids.is_contiguous() and topk_weights.is_contiguous()
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = alloc_workspace(qmoe_workspace_size(layer, M, k, opts), x.device)
+    args = (byref(layer.struct), c_void_p(x.data_ptr()), M, c_void_p(topk_ids.data_ptr()),
+            c_void_p(topk_weights.data_ptr()), k, c_void_p(out.data_ptr()), c_void_p(workspace.data_ptr()),
+            workspace.numel(), _stream_ptr(stream))
+    if opts is None:
+        st = N.lib().qmoe_forward(*args)
+    else:
+        st = N.lib().qmoe_forward_ex(*args, byref(opts))
+    N.check(st, "qmoe_forward")
+    return out
+
+
+def qmoe_forward_profiled(layer: DeviceLayer, x, topk_ids, topk_weights, out, workspace, events, opts=None,
+                          stream=None) -> int:
+    """qmoe_forward_ex with the 12 torch.cuda.Event objects recorded around its six launch slots
+    (see include/qmoe.h).  Returns the number of kernels launched."""
+    from ctypes import c_int32 as _i32
+    M = x.shape[0]
+    k = topk_ids.shape[1]
+    evs = (c_void_p * len(events))(*[c_void_p(e.cuda_event) for e in events])
+    n = _i32(0)
+    st = N.lib().qmoe_forward_profiled(byref(layer.struct), c_void_p(x.data_ptr()), M, c_void_p(topk_ids.data_ptr()),
+                                       c_void_p(topk_weights.data_ptr()), k, c_void_p(out.data_ptr()),
+                                       c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream),
+                                       None if opts is None else byref(opts), evs, len(events), byref(n))
+    N.check(st, "qmoe_forward_profiled")
+    return int(n.value)
+
+
+def qmoe_workspace_size_host(layer: DeviceLayer, M: int, k: int) -> int:
+    return int(N.lib().qmoe_workspace_size_host(byref(layer.struct), M, k))
+
+
+def qmoe_forward_host(layer: DeviceLayer, x_host: torch.Tensor, topk_ids_host: torch.Tensor,
+                      topk_weights_host: torch.Tensor, out_host: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """Host buffers in and out (pinned recommended); returns once the work is enqueued."""
+    M, _ = x_host.shape
+    k = topk_ids_host.shape[1]
+    st = N.lib().qmoe_forward_host(byref(layer.struct), c_void_p(x_host.data_ptr()), M,
+                                   c_void_p(topk_ids_host.data_ptr()), c_void_p(topk_weights_host.data_ptr()), k,
+                                   c_void_p(out_host.data_ptr()), c_void_p(workspace.data_ptr()), workspace.numel(),
+                                   _stream_ptr(stream))
+    N.check(st, "qmoe_forward_host")
+    return out_host
+
+
+def qmoe_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(N.lib().qmoe_read_device_status(c_void_p(workspace.data_ptr()), _stream_ptr(stream)))

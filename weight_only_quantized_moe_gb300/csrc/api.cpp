@@ -1,0 +1,718 @@
+// api.cpp - host side of libqmoe: argument validation, weight packing,
+// workspace planning, tensor-map encoding and the launch sequence of the
+// fused MoE forward.  The C ABI is declared in include/qmoe.h.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+#include "qmoe.h"
+#include "qmoe_internal.h"
+
+namespace qmoe {
+namespace {
+
+constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
+constexpr int kDefaultSms = 152;
+
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// small host utilities
+// ---------------------------------------------------------------------------
+template <class F>
+void parallel_for(int64_t n, F&& f) {
+  const int64_t hw = std::max<int64_t>(1, std::thread::hardware_concurrency());
+  const int64_t nt = std::min<int64_t>(hw, n);
+  if (nt <= 1) {
+    for (int64_t i = 0; i < n; ++i) f(i);
+    return;
+  }
+  std::atomic<int64_t> next{0};
+  std::vector<std::thread> ts;
+  for (int64_t t = 0; t < nt; ++t)
+    ts.emplace_back([&] {
+      for (int64_t i = next++; i < n; i = next++) f(i);
+    });
+  for (auto& t : ts) t.join();
+}
+
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  static std::mutex mu;
+  static int cache[128] = {0};
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  if (dev >= 0 && dev < 128) cache[dev] = n;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Row-major [rows, K] 16-bit matrix, boxes of 64 elements (128 B) x 16 rows, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K) {
+  auto fn = tensor_map_encoder();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {K, rows};
+  cuuint64_t strides[1] = {K * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+qmoe_status check_dev_ptr(const void* p, int dev) {
+  if (p == nullptr) return QMOE_ERR_INVALID_ARG;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_DEVICE_MISMATCH;
+  }
+  if (a.type == cudaMemoryTypeManaged) return QMOE_OK;
+  if (a.type != cudaMemoryTypeDevice || a.device != dev) return QMOE_ERR_DEVICE_MISMATCH;
+  return QMOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------------------
+// layer validation and the forward plan
+// ---------------------------------------------------------------------------
+qmoe_status validate_layer_dims(const qmoe_layer* L) {
+  if (L == nullptr) return QMOE_ERR_INVALID_ARG;
+  if (L->E < 1 || L->E > 1024 || L->H <= 0 || L->I <= 0) return QMOE_ERR_INVALID_ARG;
+  if (L->H % 128 != 0 || L->I % 128 != 0) return QMOE_ERR_UNSUPPORTED;
+  if (L->act_dtype != QMOE_F16 && L->act_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
+  if (L->qt == QMOE_INT4_GROUP) {
+    if (L->group_size != 128) return QMOE_ERR_UNSUPPORTED;
+    if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
+  } else if (L->qt == QMOE_INT8_PER_COL) {
+    if (L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
+    if (L->scale_dtype != QMOE_F32) return QMOE_ERR_UNSUPPORTED;
+    if (L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
+  } else {
+    return QMOE_ERR_INVALID_ARG;
+  }
+  return QMOE_OK;
+}
+
+struct Plan {
+  int64_t M = 0, P = 0;
+  int k = 0;
+  int T = 0, acc_bufs = 0, a_stages = 0, smem_stages = 0, stage_bytes = 0;
+  int S1 = 1, S2 = 1;
+  int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
+  int64_t cap = 0, nblocks = 0, max_chunks = 0;
+  size_t off_status = 0, off_sorted = 0, off_expert = 0, off_scalars = 0, off_chunks = 0, off_xg = 0, off_inter = 0,
+         off_h = 0, off_y = 0, total = 0;
+};
+
+// Makespan of n equal work items split s ways over C persistent CTAs, in
+// units of one unsplit item, plus a small charge per split for the reduce.
+double split_cost(int64_t n, int s, int C) {
+  const int64_t waves = (n * s + C - 1) / C;
+  return static_cast<double>(waves) / s + 0.002 * s;
+}
+
+int choose_split(int64_t n_items, int k_stages, int C, double must_gain) {
+  const int smax = std::max(1, std::min(64, k_stages / 4));
+  int best = 1;
+  double best_cost = split_cost(n_items, 1, C);
+  const double base = best_cost;
+  for (int s = 2; s <= smax; ++s) {
+    const double c = split_cost(n_items, s, C);
+    if (c < best_cost) {
+      best_cost = c;
+      best = s;
+    }
+  }
+  return best_cost < base * must_gain ? best : 1;
+}
+
+qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_options* o, int sms, Plan* pl) {
+  qmoe_status st = validate_layer_dims(L);
+  if (st != QMOE_OK) return st;
+  if (M < 0 || k < 1 || k > L->E) return QMOE_ERR_INVALID_ARG;
+  if (M * static_cast<int64_t>(k) >= (int64_t(1) << 31) - int64_t(L->E) * kAlignBlock) return QMOE_ERR_UNSUPPORTED;
+  Plan p;
+  p.M = M;
+  p.k = k;
+  p.P = M * k;
+  const int64_t P = p.P;
+  // token tile: every expert's rows fit one chunk at decode sizes
+  int T = 128;
+  if (P <= 128) T = static_cast<int>(std::max<int64_t>(16, (P + 15) / 16 * 16));
+  if (o != nullptr && o->token_tile != 0) {
+    if (o->token_tile < 16 || o->token_tile > kMaxTokenTile || o->token_tile % 16 != 0) return QMOE_ERR_INVALID_ARG;
+    T = o->token_tile;
+  }
+  p.T = T;
+  p.acc_bufs = (2 * T + 2 * 64 <= 512) ? 2 : 1;
+  p.a_stages = std::min(8, (512 - p.acc_bufs * T) / 64);
+  p.stage_bytes = (L->qt == QMOE_INT4_GROUP) ? kInt4StageBytes : kInt8StageBytes;
+  const size_t stage = static_cast<size_t>(T) * 256 + ((p.stage_bytes + 1023) & ~1023);
+  p.smem_stages = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / stage));
+  if (p.smem_stages < 2) return QMOE_ERR_UNSUPPORTED;
+  p.n_tiles1 = 2 * L->I / kTileRows;
+  p.n_tiles2 = L->H / kTileRows;
+  p.kst1 = L->H / kStageK;
+  p.kst2 = L->I / kStageK;
+  p.cap = P + static_cast<int64_t>(L->E) * (kAlignBlock - 1);
+  p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
+  p.max_chunks = (p.cap + T - 1) / T + L->E;
+  // expected chunks for the split heuristic (uniform routing)
+  const double d = L->E * (1.0 - std::pow(1.0 - 1.0 / L->E, static_cast<double>(P)));
+  const int64_t est_chunks = std::max<int64_t>(std::max<int64_t>(1, static_cast<int64_t>(std::ceil(d))), (P + T - 1) / T);
+  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, 0.8);
+  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, 0.97);
+  if (o != nullptr && o->split1 != 0) {
+    if (o->split1 < 1 || o->split1 > 64 || o->split1 > p.kst1) return QMOE_ERR_INVALID_ARG;
+    p.S1 = o->split1;
+  }
+  if (o != nullptr && o->split2 != 0) {
+    if (o->split2 < 1 || o->split2 > 64 || o->split2 > p.kst2) return QMOE_ERR_INVALID_ARG;
+    p.S2 = o->split2;
+  }
+  size_t off = 0;
+  p.off_status = off;   off += 256;
+  p.off_sorted = off;   off += al256(p.cap * 4);
+  p.off_expert = off;   off += al256(p.nblocks * 4);
+  p.off_scalars = off;  off += 256;  // num_post_padded, n_chunks
+  p.off_chunks = off;   off += al256(p.max_chunks * sizeof(Chunk));
+  p.off_xg = off;       off += al256(static_cast<size_t>(p.cap) * L->H * 2);
+  p.off_inter = off;    off += al256(static_cast<size_t>(p.cap) * L->I * 2);
+  p.off_h = off;        off += (p.S1 > 1) ? al256(static_cast<size_t>(p.S1) * p.cap * 2 * L->I * 4) : 0;
+  p.off_y = off;        off += al256(static_cast<size_t>(p.S2) * P * L->H * 4);
+  p.total = off;
+  *pl = p;
+  return QMOE_OK;
+}
+
+qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const int32_t* topk_ids,
+                         const float* topk_weights, int32_t k, void* out, void* ws, size_t ws_bytes,
+                         cudaStream_t stream, const qmoe_options* opts, void* const* events = nullptr,
+                         int32_t* n_launches = nullptr) {
+  const int sms = current_sm_count();
+  Plan pl;
+  qmoe_status st = make_plan(L, M, k, opts, sms, &pl);
+  if (st != QMOE_OK) return st;
+  if (M == 0) return QMOE_OK;
+  if (ws == nullptr || ws_bytes < pl.total) return QMOE_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  const void* ptrs[] = {x, topk_ids, topk_weights, out, ws, L->w13, L->w2};
+  for (const void* p : ptrs)
+    if ((st = check_dev_ptr(p, dev)) != QMOE_OK) return st;
+  const bool int4 = L->qt == QMOE_INT4_GROUP;
+  if (!int4) {
+    if ((st = check_dev_ptr(L->s13, dev)) != QMOE_OK) return st;
+    if ((st = check_dev_ptr(L->s2, dev)) != QMOE_OK) return st;
+  }
+  if (L->perm13 != nullptr && (st = check_dev_ptr(L->perm13, dev)) != QMOE_OK) return st;
+  if (!aligned(x, 256) || !aligned(out, 256) || !aligned(ws, 256) || !aligned(L->w13, 256) ||
+      !aligned(L->w2, 256) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+      (L->perm13 != nullptr && !aligned(L->perm13, 16)) || (!int4 && (!aligned(L->s13, 16) || !aligned(L->s2, 16))))
+    return QMOE_ERR_INVALID_ARG;
+  if (tensor_map_encoder() == nullptr) return QMOE_ERR_CUDA;
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(base + pl.off_status);
+  int32_t* sorted = reinterpret_cast<int32_t*>(base + pl.off_sorted);
+  int32_t* expert = reinterpret_cast<int32_t*>(base + pl.off_expert);
+  int32_t* npp = reinterpret_cast<int32_t*>(base + pl.off_scalars);
+  int32_t* nch = npp + 1;
+  Chunk* chunks = reinterpret_cast<Chunk*>(base + pl.off_chunks);
+  void* xg = base + pl.off_xg;
+  void* inter = base + pl.off_inter;
+  float* h = reinterpret_cast<float*>(base + pl.off_h);
+  float* y = reinterpret_cast<float*>(base + pl.off_y);
+  const bool bf16 = L->act_dtype == QMOE_BF16;
+  const int P = static_cast<int>(pl.P);
+
+  CUtensorMap map_xg, map_inter;
+  if (!encode_rows_map(&map_xg, xg, pl.cap, L->H) || !encode_rows_map(&map_inter, inter, pl.cap, L->I))
+    return QMOE_ERR_CUDA;
+
+  // events (profiling only): 2i before and 2i+1 after launch i
+  auto rec = [&](int idx) {
+    if (events != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(events[idx]), stream);
+  };
+  int launched = 0;
+  rec(0);
+  cudaError_t err = launch_align(topk_ids, P, L->E, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch,
+                                 status, stream);
+  rec(1);
+  launched += (err == cudaSuccess);
+  rec(2);
+  if (err == cudaSuccess) {
+    err = launch_gather(x, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, sms, stream);
+    launched += (err == cudaSuccess);
+  }
+  rec(3);
+  GemmParams g1{};
+  g1.w = static_cast<const uint8_t*>(L->w13);
+  g1.row_scale = int4 ? nullptr : L->s13;
+  g1.chunks = chunks;
+  g1.n_chunks = nch;
+  g1.sorted_ids = sorted;
+  g1.topk_w = topk_weights;
+  g1.status = status;
+  g1.n_tiles = pl.n_tiles1;
+  g1.k_stages = pl.kst1;
+  g1.split = pl.S1;
+  g1.token_tile = pl.T;
+  g1.acc_bufs = pl.acc_bufs;
+  g1.a_stages = pl.a_stages;
+  g1.smem_stages = pl.smem_stages;
+  g1.stage_bytes = pl.stage_bytes;
+  g1.P = P;
+  g1.chunk_group = 8;
+  g1.inter_ld = L->I;
+  if (pl.S1 == 1) {
+    g1.epi_mode = kEpiSiluToAct;
+    g1.out = inter;
+    g1.out_ld = L->I;
+    g1.out_split_stride = 0;
+  } else {
+    g1.epi_mode = kEpiPartialRows;
+    g1.out = h;
+    g1.out_ld = 2LL * L->I;
+    g1.out_split_stride = pl.cap * 2LL * L->I;
+  }
+  GemmParams g2 = g1;
+  g2.w = static_cast<const uint8_t*>(L->w2);
+  g2.row_scale = int4 ? nullptr : L->s2;
+  g2.n_tiles = pl.n_tiles2;
+  g2.k_stages = pl.kst2;
+  g2.split = pl.S2;
+  g2.epi_mode = kEpiWeightedPairs;
+  g2.out = y;
+  g2.out_ld = L->H;
+  g2.out_split_stride = pl.P * static_cast<int64_t>(L->H);
+
+  const int64_t items1 = pl.max_chunks * pl.n_tiles1 * pl.S1;
+  const int64_t items2 = pl.max_chunks * pl.n_tiles2 * pl.S2;
+  const int grid1 = static_cast<int>(std::min<int64_t>(sms, items1));
+  const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
+  rec(4);
+  if (err == cudaSuccess) {
+    err = launch_gemm(int4, bf16, &map_xg, g1, grid1, stream);
+    launched += (err == cudaSuccess);
+  }
+  rec(5);
+  rec(6);
+  if (err == cudaSuccess && pl.S1 > 1) {
+    err = launch_silu_reduce(h, npp, pl.S1, pl.cap, L->I, bf16, inter, sms, stream);
+    launched += (err == cudaSuccess);
+  }
+  rec(7);
+  rec(8);
+  if (err == cudaSuccess) {
+    err = launch_gemm(int4, bf16, &map_inter, g2, grid2, stream);
+    launched += (err == cudaSuccess);
+  }
+  rec(9);
+  rec(10);
+  if (err == cudaSuccess) {
+    err = launch_out_reduce(y, pl.S2, M, k, L->H, bf16, out, sms, stream);
+    launched += (err == cudaSuccess);
+  }
+  rec(11);
+  if (n_launches != nullptr) *n_launches = launched;
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+size_t host_staging_bytes(const qmoe_layer* L, int64_t M, int32_t k) {
+  return 2 * al256(static_cast<size_t>(M) * L->H * 2) + 2 * al256(static_cast<size_t>(M) * k * 4);
+}
+
+// ---------------------------------------------------------------------------
+// packing
+// ---------------------------------------------------------------------------
+// Stable order of the K positions by group; checks that each group has exactly 128 members.
+bool sorted_by_group(const int32_t* g, int K, std::vector<int32_t>& perm) {
+  const int ng = K / 128;
+  std::vector<int> count(ng, 0);
+  for (int kk = 0; kk < K; ++kk) {
+    if (g[kk] < 0 || g[kk] >= ng) return false;
+    ++count[g[kk]];
+  }
+  for (int c : count)
+    if (c != 128) return false;
+  perm.resize(K);
+  std::vector<int> cur(ng);
+  for (int i = 0; i < ng; ++i) cur[i] = i * 128;
+  for (int kk = 0; kk < K; ++kk) perm[cur[g[kk]]++] = kk;
+  return true;
+}
+
+// Packed row r of W13 tile t -> canonical row: rows 2j / 2j+1 of the tile are
+// gate / up of intermediate channel 64t + j in the new (act-order sorted) order.
+inline int w13_canon_row(int t, int r, int I, const int32_t* perm2) {
+  const int jn = 64 * t + (r >> 1);
+  const int j = perm2 ? perm2[jn] : jn;
+  return (r & 1) ? I + j : j;
+}
+
+// int4 tile stage: 4 chunks x 128 rows x 16 B, then 128 x 2 B scales.
+// Chunk c of a row holds sorted K = 32c..32c+31; word j of it holds
+// K = 32c+8j .. +7 with nibble i <- K 32c+8j+2i and nibble i+4 <- K 32c+8j+2i+1.
+void pack_int4_matrix(const uint8_t* q, const uint16_t* s, int rows, int K, int I_for_w13, const int32_t* perm2_rows,
+                      const int32_t* kperm, uint8_t* out, std::atomic<bool>& bad) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * kInt4StageBytes;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, perm2_rows) : t * 128 + r;
+        const uint8_t* qrow = q + static_cast<size_t>(cr) * K;
+        for (int c = 0; c < 4; ++c)
+          for (int j = 0; j < 4; ++j) {
+            uint32_t word = 0;
+            for (int i = 0; i < 4; ++i) {
+              const int k0 = ks * 128 + 32 * c + 8 * j + 2 * i;
+              const int c0 = kperm ? kperm[k0] : k0;
+              const int c1 = kperm ? kperm[k0 + 1] : k0 + 1;
+              const uint8_t a = qrow[c0], b = qrow[c1];
+              if (a > 15 || b > 15) bad = true;
+              word |= static_cast<uint32_t>(a & 15) << (4 * i);
+              word |= static_cast<uint32_t>(b & 15) << (4 * (i + 4));
+            }
+            uint8_t* dst = blk + (c * 128 + r) * 16 + j * 4;
+            dst[0] = word & 0xFF;
+            dst[1] = (word >> 8) & 0xFF;
+            dst[2] = (word >> 16) & 0xFF;
+            dst[3] = (word >> 24) & 0xFF;
+          }
+        const uint16_t sb = s[static_cast<size_t>(ks) * rows + cr];
+        blk[8192 + r * 2] = sb & 0xFF;
+        blk[8192 + r * 2 + 1] = sb >> 8;
+      }
+    }
+}
+
+void unpack_int4_matrix(const uint8_t* in, int rows, int K, int I_for_w13, const int32_t* perm2_rows,
+                        const int32_t* kperm, uint8_t* q, uint16_t* s) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * kInt4StageBytes;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, perm2_rows) : t * 128 + r;
+        uint8_t* qrow = q + static_cast<size_t>(cr) * K;
+        for (int c = 0; c < 4; ++c)
+          for (int j = 0; j < 4; ++j) {
+            const uint8_t* src = blk + (c * 128 + r) * 16 + j * 4;
+            const uint32_t word = src[0] | (src[1] << 8) | (src[2] << 16) | (static_cast<uint32_t>(src[3]) << 24);
+            for (int i = 0; i < 4; ++i) {
+              const int k0 = ks * 128 + 32 * c + 8 * j + 2 * i;
+              qrow[kperm ? kperm[k0] : k0] = (word >> (4 * i)) & 15;
+              qrow[kperm ? kperm[k0 + 1] : k0 + 1] = (word >> (4 * (i + 4))) & 15;
+            }
+          }
+        s[static_cast<size_t>(ks) * rows + cr] = static_cast<uint16_t>(blk[8192 + r * 2] | (blk[8192 + r * 2 + 1] << 8));
+      }
+    }
+}
+
+// int8 tile stage: 8 chunks x 128 rows x 16 B; chunk c holds K = 16c..16c+15 in byte order.
+void pack_int8_matrix(const int8_t* q, int rows, int K, int I_for_w13, uint8_t* out, std::atomic<bool>& bad) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * kInt8StageBytes;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
+        const int8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
+        for (int c = 0; c < 8; ++c)
+          for (int b = 0; b < 16; ++b) {
+            const int8_t v = qrow[16 * c + b];
+            if (v == -128) bad = true;
+            blk[(c * 128 + r) * 16 + b] = static_cast<uint8_t>(v);
+          }
+      }
+    }
+}
+
+void unpack_int8_matrix(const uint8_t* in, int rows, int K, int I_for_w13, int8_t* q) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * kInt8StageBytes;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
+        int8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
+        for (int c = 0; c < 8; ++c)
+          for (int b = 0; b < 16; ++b) qrow[16 * c + b] = static_cast<int8_t>(blk[(c * 128 + r) * 16 + b]);
+      }
+    }
+}
+
+bool pack_dims_ok(int32_t E, int32_t H, int32_t I) {
+  return E >= 1 && E <= 1024 && H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0;
+}
+
+}  // namespace
+}  // namespace qmoe
+
+using namespace qmoe;
+
+extern "C" {
+
+int32_t qmoe_abi_version(void) { return QMOE_ABI_VERSION; }
+
+const char* qmoe_status_string(qmoe_status s) {
+  switch (s) {
+    case QMOE_OK: return "ok";
+    case QMOE_ERR_INVALID_ARG: return "invalid argument";
+    case QMOE_ERR_UNSUPPORTED: return "unsupported shape, group size or type combination";
+    case QMOE_ERR_DEVICE_MISMATCH: return "pointer is not device memory of the current device";
+    case QMOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case QMOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case QMOE_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+    case QMOE_ERR_BAD_EXPERT_ID: return "a top-k expert id is outside [0, E)";
+  }
+  return "unknown status";
+}
+
+size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K, int32_t group_size) {
+  if (E < 1 || rows <= 0 || K <= 0 || rows % 128 != 0 || K % 128 != 0) return 0;
+  const size_t tiles = static_cast<size_t>(E) * (rows / 128) * (K / 128);
+  if (qt == QMOE_INT4_GROUP && group_size == 128) return tiles * kInt4StageBytes;
+  if (qt == QMOE_INT8_PER_COL && group_size == -1) return tiles * kInt8StageBytes;
+  return 0;
+}
+
+qmoe_status qmoe_pack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                           const uint8_t* q13, const uint16_t* s13, const int32_t* g13, const uint8_t* q2,
+                           const uint16_t* s2, const int32_t* g2, void* w13_packed, void* w2_packed,
+                           int32_t* perm13_out) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128) return QMOE_ERR_UNSUPPORTED;
+  if (scale_dtype != QMOE_F16 && scale_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed || (g13 && !perm13_out)) return QMOE_ERR_INVALID_ARG;
+  std::atomic<bool> bad{false}, badg{false};
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, 2 * I, H, 128);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, H, I, 128);
+  parallel_for(E, [&](int64_t e) {
+    std::vector<int32_t> p13, p2;
+    if (g13 && !sorted_by_group(g13 + e * H, H, p13)) { badg = true; return; }
+    if (g2 && !sorted_by_group(g2 + e * I, I, p2)) { badg = true; return; }
+    if (g13) std::memcpy(perm13_out + e * H, p13.data(), sizeof(int32_t) * H);
+    pack_int4_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, s13 + static_cast<size_t>(e) * (H / 128) * 2 * I,
+                     2 * I, H, I, g2 ? p2.data() : nullptr, g13 ? p13.data() : nullptr,
+                     static_cast<uint8_t*>(w13_packed) + e * b13, bad);
+    pack_int4_matrix(q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H, H, I, 0,
+                     nullptr, g2 ? p2.data() : nullptr, static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+  });
+  if (badg) return QMOE_ERR_UNSUPPORTED;
+  if (bad) return QMOE_ERR_INVALID_ARG;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_unpack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                             const void* w2_packed, const int32_t* g13, const int32_t* g2, uint8_t* q13,
+                             uint16_t* s13, uint8_t* q2, uint16_t* s2) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed) return QMOE_ERR_INVALID_ARG;
+  std::atomic<bool> badg{false};
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, 2 * I, H, 128);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, H, I, 128);
+  parallel_for(E, [&](int64_t e) {
+    std::vector<int32_t> p13, p2;
+    if (g13 && !sorted_by_group(g13 + e * H, H, p13)) { badg = true; return; }
+    if (g2 && !sorted_by_group(g2 + e * I, I, p2)) { badg = true; return; }
+    unpack_int4_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, 2 * I, H, I, g2 ? p2.data() : nullptr,
+                       g13 ? p13.data() : nullptr, q13 + static_cast<size_t>(e) * 2 * I * H,
+                       s13 + static_cast<size_t>(e) * (H / 128) * 2 * I);
+    unpack_int4_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, H, I, 0, nullptr, g2 ? p2.data() : nullptr,
+                       q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H);
+  });
+  return badg ? QMOE_ERR_UNSUPPORTED : QMOE_OK;
+}
+
+qmoe_status qmoe_pack_int8(int32_t E, int32_t H, int32_t I, const int8_t* q13, const float* s13, const int8_t* q2,
+                           const float* s2, void* w13_packed, float* s13_packed, void* w2_packed, float* s2_packed) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !s13_packed || !w2_packed || !s2_packed)
+    return QMOE_ERR_INVALID_ARG;
+  std::atomic<bool> bad{false};
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, 2 * I, H, -1);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, H, I, -1);
+  parallel_for(E, [&](int64_t e) {
+    pack_int8_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, 2 * I, H, I,
+                     static_cast<uint8_t*>(w13_packed) + e * b13, bad);
+    pack_int8_matrix(q2 + static_cast<size_t>(e) * H * I, H, I, 0, static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+    for (int t = 0; t < 2 * I / 128; ++t)
+      for (int r = 0; r < 128; ++r)
+        s13_packed[static_cast<size_t>(e) * 2 * I + t * 128 + r] = s13[static_cast<size_t>(e) * 2 * I + w13_canon_row(t, r, I, nullptr)];
+    std::memcpy(s2_packed + static_cast<size_t>(e) * H, s2 + static_cast<size_t>(e) * H, sizeof(float) * H);
+  });
+  return bad ? QMOE_ERR_INVALID_ARG : QMOE_OK;
+}
+
+qmoe_status qmoe_unpack_int8(int32_t E, int32_t H, int32_t I, const void* w13_packed, const float* s13_packed,
+                             const void* w2_packed, const float* s2_packed, int8_t* q13, float* s13, int8_t* q2,
+                             float* s2) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !s13_packed || !w2_packed || !s2_packed)
+    return QMOE_ERR_INVALID_ARG;
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, 2 * I, H, -1);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, H, I, -1);
+  parallel_for(E, [&](int64_t e) {
+    unpack_int8_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, 2 * I, H, I,
+                       q13 + static_cast<size_t>(e) * 2 * I * H);
+    unpack_int8_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, H, I, 0, q2 + static_cast<size_t>(e) * H * I);
+    for (int t = 0; t < 2 * I / 128; ++t)
+      for (int r = 0; r < 128; ++r)
+        s13[static_cast<size_t>(e) * 2 * I + w13_canon_row(t, r, I, nullptr)] = s13_packed[static_cast<size_t>(e) * 2 * I + t * 128 + r];
+    std::memcpy(s2 + static_cast<size_t>(e) * H, s2_packed + static_cast<size_t>(e) * H, sizeof(float) * H);
+  });
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_moe_align(const int32_t* topk_ids, int64_t M, int32_t top_k, int32_t E, int32_t block,
+                           int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded, int64_t capacity,
+                           void* stream) {
+  if (M < 0 || top_k < 1 || E < 1 || E > 1024 || block < 1 || block > 256) return QMOE_ERR_INVALID_ARG;
+  const int64_t P = M * top_k;
+  if (P >= (int64_t(1) << 31) - int64_t(E) * block) return QMOE_ERR_UNSUPPORTED;
+  if (capacity < P + static_cast<int64_t>(E) * (block - 1)) return QMOE_ERR_INVALID_ARG;
+  if (!sorted_ids || !expert_ids || !num_post_padded || (P > 0 && !topk_ids)) return QMOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  qmoe_status st;
+  if (P > 0 && (st = check_dev_ptr(topk_ids, dev)) != QMOE_OK) return st;
+  if ((st = check_dev_ptr(sorted_ids, dev)) != QMOE_OK) return st;
+  if ((st = check_dev_ptr(expert_ids, dev)) != QMOE_OK) return st;
+  if ((st = check_dev_ptr(num_post_padded, dev)) != QMOE_OK) return st;
+  const cudaError_t err = launch_align(topk_ids, static_cast<int32_t>(P), E, block, capacity, sorted_ids, expert_ids,
+                                       num_post_padded, 0, nullptr, nullptr, nullptr,
+                                       static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts) {
+  Plan pl;
+  if (make_plan(layer, M, top_k, opts, current_sm_count(), &pl) != QMOE_OK) return 0;
+  return pl.total;
+}
+
+size_t qmoe_workspace_size(const qmoe_layer* layer, int64_t M, int32_t top_k) {
+  return qmoe_workspace_size_ex(layer, M, top_k, nullptr);
+}
+
+qmoe_status qmoe_forward_ex(const qmoe_layer* layer, const void* x, int64_t M, const int32_t* topk_ids,
+                            const float* topk_weights, int32_t top_k, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream, const qmoe_options* opts) {
+  return forward_impl(layer, x, M, topk_ids, topk_weights, top_k, out, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream), opts);
+}
+
+qmoe_status qmoe_forward(const qmoe_layer* layer, const void* x, int64_t M, const int32_t* topk_ids,
+                         const float* topk_weights, int32_t top_k, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return forward_impl(layer, x, M, topk_ids, topk_weights, top_k, out, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream), nullptr);
+}
+
+qmoe_status qmoe_forward_profiled(const qmoe_layer* layer, const void* x, int64_t M, const int32_t* topk_ids,
+                                  const float* topk_weights, int32_t top_k, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream, const qmoe_options* opts,
+                                  void* const* events, int32_t n_events, int32_t* n_launches) {
+  if (events == nullptr || n_events < 12) return QMOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 12; ++i)
+    if (events[i] == nullptr) return QMOE_ERR_INVALID_ARG;
+  if (n_launches != nullptr) *n_launches = 0;
+  return forward_impl(layer, x, M, topk_ids, topk_weights, top_k, out, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream), opts, events, n_launches);
+}
+
+size_t qmoe_workspace_size_host(const qmoe_layer* layer, int64_t M, int32_t top_k) {
+  const size_t w = qmoe_workspace_size(layer, M, top_k);
+  if (w == 0) return 0;
+  return al256(w) + host_staging_bytes(layer, M, top_k);
+}
+
+qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64_t M, const int32_t* topk_ids_host,
+                              const float* topk_weights_host, int32_t top_k, void* out_host, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  const size_t w = qmoe_workspace_size(layer, M, top_k);
+  if (w == 0) return validate_layer_dims(layer) != QMOE_OK ? validate_layer_dims(layer) : QMOE_ERR_INVALID_ARG;
+  if (M == 0) return QMOE_OK;
+  if (!x_host || !topk_ids_host || !topk_weights_host || !out_host) return QMOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < qmoe_workspace_size_host(layer, M, top_k)) return QMOE_ERR_WORKSPACE;
+  const size_t xb = static_cast<size_t>(M) * layer->H * 2;
+  const size_t pb = static_cast<size_t>(M) * top_k * 4;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  uint8_t* stage = base + al256(w);
+  void* x_dev = stage;
+  int32_t* ids_dev = reinterpret_cast<int32_t*>(stage + al256(xb));
+  float* w_dev = reinterpret_cast<float*>(stage + al256(xb) + al256(pb));
+  void* out_dev = stage + al256(xb) + 2 * al256(pb);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(ids_dev, topk_ids_host, pb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(w_dev, topk_weights_host, pb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  const qmoe_status st = forward_impl(layer, x_dev, M, ids_dev, w_dev, top_k, out_dev, workspace, w, s, nullptr);
+  if (st != QMOE_OK) return st;
+  if (cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_read_device_status(const void* workspace, void* stream) {
+  if (workspace == nullptr) return QMOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  int32_t v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  return static_cast<qmoe_status>(v);
+}
+
+}  // extern "C"

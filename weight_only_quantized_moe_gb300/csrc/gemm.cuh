@@ -1,0 +1,449 @@
+// gemm.cuh - grouped expert GEMM with on-the-fly weight dequantization for sm_103a.
+//
+// What it computes (pages "Marlin moe integration" and "[Kernel] W8A16 Int8
+// inside FusedMoE": the fused MoE kernel consumes already-quantized expert
+// weights and casts them to FP16/BF16 inside the kernel before the matmul):
+// for one expert e, a tile of 128 output features and a chunk of token rows,
+//     acc[f, t] = sum_k W_e[f, k] * B[t, k]
+// where W_e is dequantized from packed int4 (with its group scale) or int8,
+// and B is the chunk's rows of the gathered activations (gate/up GEMM) or of
+// the intermediate (down GEMM).  The epilogue then applies SiLU(gate)*up, or
+// the routing weight, per the mode.
+//
+// Design for GB300 (prior-art Marlin/Triton kernels staged both operands in
+// shared memory; here only the tokens are):
+//   * swap-AB: the 128 weight rows are the MMA's M; the chunk's token rows
+//     (16..256) are N, so tiny decode batches waste no tensor work.
+//   * the dequantized weight tile goes registers -> TMEM (tcgen05.st) and is
+//     the MMA's A operand straight from tensor memory; dequantized weights
+//     never touch shared memory, which carries only the packed bytes and the
+//     token tile.
+//   * the packed weights (one contiguous block per 128x128 tile, scales
+//     appended) arrive by 1-D bulk TMA; token tiles by 2-D tensor TMA with
+//     128-byte swizzle, the layout the MMA's shared-memory descriptor reads.
+//   * warp roles: 1 TMA producer thread, 1 MMA thread, two dequant
+//     warpgroups taking alternate stages, one epilogue warpgroup reading the
+//     fp32 accumulators out of TMEM; a persistent grid walks the work items.
+//   * every mbarrier wait is bounded (see ptx.cuh); a wait that gives up
+//     records QMOE_ERR_TIMEOUT in the status word and the CTA winds down after
+//     waiting for its own copies and MMAs, then frees its TMEM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "qmoe_internal.h"
+
+namespace qmoe {
+
+constexpr int kGemmThreads = 512;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kDequantWarp0 = 8;  // warps 8..15: two warpgroups
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBarrierBytes = 1024;
+
+__host__ __device__ inline uint32_t gemm_w_region(int stage_bytes) { return (stage_bytes + 1023u) & ~1023u; }
+__host__ __device__ inline uint32_t gemm_stage_bytes(int token_tile, int stage_bytes) {
+  return static_cast<uint32_t>(token_tile) * 256u + gemm_w_region(stage_bytes);
+}
+
+struct WorkItem {
+  int e, row0, nrows, tile, split_idx, ks0, ks1;
+};
+
+// Work item i -> (split, chunk, tile).  Items of one split are rastered in
+// groups of `chunk_group` chunks: tiles vary slowest inside a group so that the
+// CTAs running at the same time share the group's token tiles and each expert
+// weight tile in L2.
+__device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i, WorkItem& w) {
+  const int per_split = nch * p.n_tiles;
+  const int s = i / per_split;
+  const int r = i - s * per_split;
+  const int grp_items = p.chunk_group * p.n_tiles;
+  const int g = r / grp_items;
+  const int rem = r - g * grp_items;
+  const int c0 = g * p.chunk_group;
+  const int cg = min(p.chunk_group, nch - c0);
+  const int tile = rem / cg;
+  const int c = c0 + (rem - tile * cg);
+  const Chunk ch = p.chunks[c];
+  w.e = ch.expert;
+  w.row0 = ch.row0;
+  w.nrows = ch.nrows;
+  w.tile = tile;
+  w.split_idx = s;
+  w.ks0 = static_cast<int>(static_cast<int64_t>(p.k_stages) * s / p.split);
+  w.ks1 = static_cast<int>(static_cast<int64_t>(p.k_stages) * (s + 1) / p.split);
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int32_t* status) {
+  *abort_flag = 1;
+  if (status != nullptr) atomicCAS(status, 0, kStatusTimeout);
+}
+
+// Wait that only gives up on the time limit (used while draining in-flight work).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const int never = 0;
+  return mbar_wait(bar, parity, &never);
+}
+
+// ---------------------------------------------------------------------------
+// Dequantization of one 128-K stage of one weight row into 64 TMEM columns
+// (column c holds K elements 2c (low half) and 2c+1 (high half)).
+// ---------------------------------------------------------------------------
+// int4: packed chunk c (16 bytes) of the row holds K = 32c .. 32c+31; in word j
+// of the chunk, nibble i holds K = 32c+8j+2i and nibble i+4 holds K = 32c+8j+2i+1.
+// Magic-number conversion: (nibble | 0x4300) is the bf16 value 128 + q and
+// (nibble | 0x6400) the f16 value 1024 + q, both exact; subtracting 136 (1032)
+// gives q - 8 exactly, and one multiply by the group scale rounds once.
+template <bool BF16>
+__device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[64]) {
+  const uint32_t magic = BF16 ? 0x43004300u : 0x64006400u;
+  const uint32_t bias_bits = BF16 ? 0x43084308u : 0x64086408u;  // 136 (bf16) / 1032 (f16)
+  const uint32_t s2bits = sbits | (sbits << 16);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t t = ((w[j] >> (4 * i)) & 0x000F000Fu) | magic;
+        uint32_t r;
+        if (BF16) {
+          __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&bias_bits));
+          v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&s2bits));
+          r = *reinterpret_cast<uint32_t*>(&v);
+        } else {
+          __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), *reinterpret_cast<const __half2*>(&bias_bits));
+          v = __hmul2(v, *reinterpret_cast<const __half2*>(&s2bits));
+          r = *reinterpret_cast<uint32_t*>(&v);
+        }
+        out[16 * c + 4 * j + i] = r;
+      }
+    }
+  }
+}
+
+// int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
+// per-row scale is applied to the fp32 accumulator in the epilogue, so the
+// conversion is exact: f16 via (0x64 << 8 | (q + 128)) - 1152; bf16 via the
+// float32 pattern 0x4B0000uu - (2^23 + 128) and a pack to bf16x2.
+template <bool BF16>
+__device__ __forceinline__ void dequant_int8_row(const uint4 (&pk)[8], uint32_t (&out)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t u = w[j] ^ 0x80808080u;
+      if (BF16) {
+        const float f0 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7540))) - 8388736.0f;
+        const float f1 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7541))) - 8388736.0f;
+        const float f2 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7542))) - 8388736.0f;
+        const float f3 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7543))) - 8388736.0f;
+        __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
+        out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
+        out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
+      } else {
+        const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+        const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+        const uint32_t bias = 0x64806480u;  // 1152
+        __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias));
+        __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&bias));
+        out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
+        out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_dev(float g) { return g / (1.0f + __expf(-g)); }
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t to_act_bits(float v) {
+  if (BF16) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&b);
+  } else {
+    __half h = __float2half_rn(v);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <bool INT4, bool BF16>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    qmoe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int T = p.token_tile;
+  const uint32_t b_bytes = static_cast<uint32_t>(T) * 256u;
+  const uint32_t st_bytes = gemm_stage_bytes(T, p.stage_bytes);
+  const int NS = p.smem_stages, NA = p.a_stages, ACCB = p.acc_bufs;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * st_bytes);
+  uint64_t* empty = full + NS;
+  uint64_t* afull = empty + NS;
+  uint64_t* aempty = afull + NA;
+  uint64_t* accfull = aempty + NA;
+  uint64_t* accempty = accfull + 2;
+  uint64_t* drain = accempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 4 + 1);  // 4 dequant warps + 1 MMA commit
+    }
+    for (int j = 0; j < NA; ++j) {
+      mbar_init(smem_u32(afull + j), 4);
+      mbar_init(smem_u32(aempty + j), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(accfull + b), 1);
+      mbar_init(smem_u32(accempty + b), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&tmap_b);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int nch = *p.n_chunks;
+  const int n_items = nch * p.n_tiles * p.split;
+  const uint32_t a_col0 = static_cast<uint32_t>(ACCB * T);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_b = policy_evict_last();
+      int g = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        WorkItem it;
+        decode_item(p, nch, i, it);
+        const uint8_t* wsrc =
+            p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages * static_cast<int64_t>(p.stage_bytes);
+        const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + static_cast<uint32_t>(it.nrows) * 256u;
+        for (int ks = it.ks0; ks < it.ks1; ++ks) {
+          const int s = g % NS;
+          if (!mbar_wait(smem_u32(empty + s), ((g / NS) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * st_bytes;
+          const uint32_t fb = smem_u32(full + s);
+          mbar_arrive_expect_tx(fb, tx);
+          tma_load_1d(smem_u32(st + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
+                      pol_w);
+          for (int a = 0; a < 2; ++a)
+            for (int r = 0; r < it.nrows; r += 16)
+              tma_load_2d(smem_u32(st + a * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64, it.row0 + r, fb,
+                          pol_b);
+          ++g;
+        }
+      }
+      if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
+      // wait for every copy still in flight into this CTA's shared memory
+      for (int j = (g > NS ? g - NS : 0); j < g; ++j) mbar_wait_drain(smem_u32(full + (j % NS)), (j / NS) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int g = 0, itn = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        WorkItem it;
+        decode_item(p, nch, i, it);
+        const int b = itn % ACCB;
+        const int use = itn / ACCB;
+        if (!mbar_wait(smem_u32(accempty + b), (use & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * T);
+        const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), BF16);
+        for (int ks = it.ks0; ks < it.ks1; ++ks) {
+          const int s = g % NS;
+          const int ja = g % NA;
+          if (!mbar_wait(smem_u32(full + s), (g / NS) & 1, abort_flag) ||
+              !mbar_wait(smem_u32(afull + ja), (g / NA) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ja * 64);
+          const uint32_t b_base = smem_u32(smem + s * st_bytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bdesc =
+                make_sdesc_k_sw128(b_base + static_cast<uint32_t>((kk >> 2) * T * 128 + (kk & 3) * 32));
+            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc, idesc,
+                       (ks > it.ks0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(empty + s));
+          mma_commit(smem_u32(aempty + ja));
+          ++g;
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(accfull + b));
+        ++itn;
+      }
+      if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
+      // all MMAs this thread issued must finish before TMEM is released
+      mma_commit(smem_u32(drain));
+      mbar_wait_drain(smem_u32(drain), 0);
+    }
+  } else if (warp >= kDequantWarp0) {
+    // ------------------------------------------------------------ dequant warpgroups
+    const int wg = (warp - kDequantWarp0) >> 2;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      WorkItem it;
+      decode_item(p, nch, i, it);
+      for (int ks = it.ks0; ks < it.ks1; ++ks, ++g) {
+        if ((g & 1) != wg) continue;
+        const int s = g % NS;
+        const int ja = g % NA;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (g / NS) & 1, abort_flag));
+        if (!ok) break;
+        const uint8_t* wst = smem + s * st_bytes + b_bytes;
+        uint32_t out[64];
+        if (INT4) {
+          uint4 pk[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
+          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(empty + s));
+          dequant_int4_row<BF16>(pk, sbits, out);
+        } else {
+          uint4 pk[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(empty + s));
+          dequant_int8_row<BF16>(pk, out);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ja), ((g / NA) & 1) ^ 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ja * 64);
+        tmem_st_32x32b_x32<0>(ta, out);
+        tmem_st_32x32b_x32<32>(ta + 32, out);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(afull + ja));
+      }
+    }
+    if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ epilogue warpgroup
+    const int q = warp;
+    const int row = q * 32 + lane;  // weight row of the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int itn = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+      WorkItem it;
+      decode_item(p, nch, i, it);
+      const int b = itn % ACCB;
+      const int use = itn / ACCB;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const float rs =
+          INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
+      const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(b * T);
+      for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
+        tmem_wait_ld();
+        if (c0 + 16 >= it.nrows) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(accempty + b));
+        }
+        float f[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) f[c] = __uint_as_float(v[c]) * rs;
+        if (p.epi_mode == kEpiSiluToAct) {
+          // rows 2j / 2j+1 of the tile are gate / up of intermediate channel tile*64 + j
+          const bool even = (lane & 1) == 0;
+          const int jch = it.tile * (kTileRows / 2) + (row >> 1);
+          uint16_t* inter = static_cast<uint16_t*>(p.out);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float send = even ? f[c + 8] : f[c];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float gt = even ? f[c] : recv;
+            const float up = even ? recv : f[c + 8];
+            const int col = even ? c : c + 8;
+            inter[static_cast<int64_t>(it.row0 + c0 + col) * p.inter_ld + jch] = to_act_bits<BF16>(silu_dev(gt) * up);
+          }
+        } else if (p.epi_mode == kEpiPartialRows) {
+          float* h = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            h[static_cast<int64_t>(it.row0 + c0 + c) * p.out_ld + it.tile * kTileRows + row] = f[c];
+        } else {
+          float* y = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int pair = __ldg(p.sorted_ids + it.row0 + c0 + c);
+            if (pair < p.P)
+              y[static_cast<int64_t>(pair) * p.out_ld + it.tile * kTileRows + row] = f[c] * __ldg(p.topk_w + pair);
+          }
+        }
+      }
+      ++itn;
+    }
+    if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool INT4, bool BF16>
+cudaError_t launch_gemm_t(const CUtensorMap* tmap_b, const GemmParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = gemm_smem_bytes(p);
+  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<INT4, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  qmoe_gemm_kernel<INT4, BF16><<<grid, kGemmThreads, smem, stream>>>(*tmap_b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,82 @@
+// qmoe_internal.h - declarations shared by the host dispatcher and the CUDA
+// translation units of libqmoe (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace qmoe {
+
+// Packed weight geometry (see the pack functions in api.cpp).
+constexpr int kTileRows = 128;        // output features per GEMM work item (MMA M)
+constexpr int kStageK = 128;          // K elements per pipeline stage (= one int4 group)
+constexpr int kInt4StageBytes = 8448; // 128 rows x 128 K x 4 bit + 128 scales x 2 B
+constexpr int kInt8StageBytes = 16384;
+constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
+constexpr int kMaxTokenTile = 256;
+
+// Device-side status codes (values match qmoe_status).
+constexpr int kStatusTimeout = 6;
+constexpr int kStatusBadExpert = 7;
+
+// One work-item row range of one expert, produced by the align kernel.
+struct Chunk {
+  int32_t expert;
+  int32_t row0;
+  int32_t nrows;  // multiple of 16, <= token tile
+  int32_t pad;
+};
+
+enum EpiMode : int32_t {
+  kEpiSiluToAct = 0,   // gate/up GEMM, whole K: inter[row, j] = SiLU(gate)*up in the activation type
+  kEpiPartialRows = 1, // gate/up GEMM, split K: fp32 partial [split][row][2I] (interleaved gate/up)
+  kEpiWeightedPairs = 2 // down GEMM: fp32 y[split][pair][H] = topk_weight * acc
+};
+
+struct GemmParams {
+  const uint8_t* w;          // packed weights [E][n_tiles][k_stages][stage_bytes]
+  const float* row_scale;    // int8: per packed row [E][n_tiles*128]; int4: null
+  const Chunk* chunks;       // [max_chunks]
+  const int32_t* n_chunks;   // device scalar
+  const int32_t* sorted_ids; // down GEMM epilogue
+  const float* topk_w;       // flat [P]
+  void* out;
+  int32_t* status;
+  int64_t out_ld;            // elements per output row
+  int64_t out_split_stride;  // elements per split slab
+  int32_t n_tiles;
+  int32_t k_stages;
+  int32_t split;
+  int32_t token_tile;        // T: B rows per stage buffer, TMEM columns per accumulator
+  int32_t acc_bufs;          // 1 or 2
+  int32_t a_stages;          // TMEM A stages (64 columns each)
+  int32_t smem_stages;       // shared-memory pipeline depth
+  int32_t stage_bytes;       // packed weight bytes per stage
+  int32_t epi_mode;
+  int32_t P;                 // number of token-expert pairs
+  int32_t chunk_group;       // work-item raster: chunks per group
+  int32_t inter_ld;          // I (for the SiLU epilogue)
+};
+
+// Host-side launchers (defined in the .cu files); return cudaError_t of the launch.
+cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t block, int64_t capacity,
+                         int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded, int32_t token_tile,
+                         Chunk* chunks, int32_t* n_chunks, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_gather(const void* x, const int32_t* sorted_ids, const int32_t* expert_ids,
+                          const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
+                               int32_t I, bool bf16, void* inter, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_out_reduce(const float* y, int32_t split, int64_t M, int32_t top_k, int32_t H, bool bf16,
+                              void* out, int num_sms, cudaStream_t stream);
+
+size_t gemm_smem_bytes(const GemmParams& p);
+cudaError_t launch_gemm(bool int4, bool bf16, const CUtensorMap* tmap_b, const GemmParams& p, int grid,
+                        cudaStream_t stream);
+
+}  // namespace qmoe
