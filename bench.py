@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of the fused weight-only-quantized MoE layer on GB300.
+
+One step = one full layer forward (moe_align, token gather, gate/up GEMM with
+fused SiLU*up, down GEMM with the routing weight, top-k reduce) over one batch
+of M tokens of a synthetic workload shaped like the pages' models.  Prints ONE
+JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--M M] [--no-sweep]
+
+--impl reference times the CPU oracle (float64 numpy) on a bounded sample of
+the same workload; it is the only other place this file runs the oracle.
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(independent replicas; the layer is not sharded), value = all ranks' tokens /
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, make_inputs, make_layer  # noqa: E402
+
+METRIC = "quant-MoE layer tokens/s, TFLOP/s & weight GB/s vs roofline, M=1..8192"
+DEFAULT_WORKLOAD = "mixtral8x7b_w4"
+DEFAULT_M = 16
+L2_BYTES = 129 * 1024 * 1024
+LAUNCH_NAMES = ["moe_align", "gather", "gemm_gate_up", "silu_reduce", "gemm_down", "out_reduce"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-sample-s", type=float, default=20.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_config(wl, M, extra=None):
+    cfg = {"workload": f"{wl.name}: E={wl.E} top-{wl.k} H={wl.H} I={wl.I} {wl.qt}"
+                       f"{' g128' if wl.qt == 'int4' else ' per-column'}{' act-order' if wl.act_order else ''}"
+                       f" {wl.act} activations, M={M}",
+           "E": wl.E, "top_k": wl.k, "hidden": wl.H, "intermediate": wl.I, "quant": wl.qt,
+           "group_size": wl.group_size, "act_order": wl.act_order, "act_dtype": wl.act, "M": M}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------
+def oracle_sample(wl, layer, inp, budget_s):
+    """Time the oracle on the first tokens of the batch, one token at a time,
+    until about budget_s seconds of CPU work; returns (tokens, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    n = 0
+    M = inp.x.shape[0]
+    while n < M:
+        oracle.moe_forward_rows(layer, inp.x, inp.topk_ids, inp.topk_weights, [n])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return n, time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(wl, dl, inp):
+    """Bytes the method must move per layer call: the touched experts' packed
+    weights and scales, x in, intermediate write + read, out."""
+    d = len(np.unique(inp.topk_ids))
+    M = inp.x.shape[0]
+    P = M * wl.k
+    per_expert_w13 = dl.w13.numel() // wl.E + (2 * wl.I * 4 if wl.qt == "int8" else 0)
+    per_expert_w2 = dl.w2.numel() // wl.E + (wl.H * 4 if wl.qt == "int8" else 0)
+    act = 2
+    gemm1 = d * per_expert_w13 + P * wl.H * act + P * wl.I * act
+    gemm2 = d * per_expert_w2 + P * wl.I * act + P * wl.H * 4
+    total = d * (per_expert_w13 + per_expert_w2) + M * wl.H * act * 2 + 2 * P * wl.I * act
+    return {"distinct_experts": d, "gemm_gate_up": gemm1, "gemm_down": gemm2, "layer": total,
+            "weights": d * (per_expert_w13 + per_expert_w2)}
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import weight_only_quantized_moe_gb300 as q
+    from weight_only_quantized_moe_gb300 import build as qbuild
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    qbuild.build()
+    q.lib()
+    wl = WORKLOADS[args.workload]
+    M = args.M or (DEFAULT_M if DEFAULT_M in wl.Ms else wl.Ms[0])
+    layer = make_layer(wl, seed=0)
+    base = q.DeviceLayer.from_canonical(wl.qt, wl.act, layer.q13, layer.s13, layer.q2, layer.s2, layer.g13,
+                                        layer.g2, device=dev)
+    # rotate through copies of the packed weights so that no step finds them in L2
+    copies = [base]
+    n_copies = max(1, min(4, math.ceil(3 * L2_BYTES / max(1, base.weight_bytes())) + 1))
+    for _ in range(n_copies - 1):
+        copies.append(q.DeviceLayer(base.qt, base.E, base.H, base.I, base.act, base.w13.clone(), base.w2.clone(),
+                                    None if base.s13 is None else base.s13.clone(),
+                                    None if base.s2 is None else base.s2.clone(),
+                                    None if base.perm13 is None else base.perm13.clone()))
+    del layer
+    stream = torch.cuda.current_stream()
+
+    def measure(M, steps, warmup, profile=True):
+        inp = make_inputs(wl, M, seed=0)
+        x = torch.from_numpy(inp.x).to(base.torch_dtype).to(dev)
+        ids = torch.from_numpy(inp.topk_ids).to(dev)
+        w = torch.from_numpy(inp.topk_weights).to(dev)
+        out = torch.empty_like(x)
+        ws = q.alloc_workspace(q.qmoe_workspace_size(base, M, wl.k), dev)
+        for i in range(warmup):
+            q.qmoe_forward(copies[i % len(copies)], x, ids, w, out=out, workspace=ws)
+        st = q.qmoe_read_device_status(ws)
+        if st != q.QMOE_OK:
+            raise RuntimeError(f"device status after warm-up: {q.status_string(st)}")
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(dev.index) as clk:
+            e0.record(stream)
+            for i in range(steps):
+                q.qmoe_forward(copies[i % len(copies)], x, ids, w, out=out, workspace=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        res = {"M": M, "ms": ms, "clocks": clk.summary(), "inp": inp}
+        if profile:
+            # second pass over the same K steps with CUDA events around each kernel launch
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(steps)]
+            launches = 0
+            for i in range(steps):
+                launches += q.qmoe_forward_profiled(copies[i % len(copies)], x, ids, w, out, ws, evs[i])
+            torch.cuda.synchronize()
+            per = {}
+            for j, name in enumerate(LAUNCH_NAMES):
+                per[name] = sum(evs[i][2 * j].elapsed_time(evs[i][2 * j + 1]) for i in range(steps)) / steps
+            res["kernel_ms"] = per
+            res["launches_per_step"] = launches / steps
+        st = q.qmoe_read_device_status(ws)
+        if st != q.QMOE_OK:
+            raise RuntimeError(f"device status: {q.status_string(st)}")
+        res["bytes"] = algorithmic_bytes(wl, base, inp)
+        res["copies"] = len(copies)
+        res["x"], res["ids"], res["w"] = x, ids, w
+        return res
+
+    main = measure(M, args.steps, args.warmup)
+    ms = main["ms"]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the host-buffer entry point: pinned H2D of x/ids/weights,
+    # the forward, D2H of out, every step
+    xh = main["x"].cpu().pin_memory()
+    idh = main["ids"].cpu().pin_memory()
+    wh = main["w"].cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    wsh = q.alloc_workspace(q.qmoe_workspace_size_host(base, M, wl.k), dev)
+    for i in range(args.warmup):
+        q.qmoe_forward_host(copies[i % len(copies)], xh, idh, wh, outh, wsh)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        q.qmoe_forward_host(copies[i % len(copies)], xh, idh, wh, outh, wsh)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        for Ms in wl.Ms:
+            if Ms == M:
+                continue
+            r = measure(Ms, max(5, args.steps // 5), 3)
+            sweep.append(r)
+    return wl, M, main, ms, e2e_ms, sweep, base
+
+
+def summarize(wl, r, hbm, tc):
+    M = r["M"]
+    ms = r["ms"]
+    k = r["kernel_ms"]
+    by = r["bytes"]
+    flops = wl.flops(M)
+    return {"M": M, "ms": round(ms, 5), "tokens_per_s": M / (ms * 1e-3),
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "weight_gbs": by["weights"] / (ms * 1e-3) / 1e9,
+            "hbm_frac_layer": by["layer"] / (ms * 1e-3) / 1e9 / hbm,
+            "distinct_experts": by["distinct_experts"],
+            "kernel_ms": {n: round(v, 5) for n, v in k.items()}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return run_reference(args)
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    wl, M, main_r, ms, e2e_ms, sweep, base = run_gpu(args, rank, world)
+    hbm, tc_burst, tc_sust, peak_src = peaks()
+    if rank == 0:
+        import oracle  # noqa: F401  (CPU baseline leg only)
+        layer_cpu = make_layer(wl, seed=0)
+        n_tok, secs = oracle_sample(wl, layer_cpu, main_r["inp"], args.cpu_sample_s)
+        cpu_tps = n_tok / secs
+        by = main_r["bytes"]
+        kms = main_r["kernel_ms"]
+        dominant = max(("gemm_gate_up", "gemm_down"), key=lambda n: kms[n])
+        ach = by[dominant] / (kms[dominant] * 1e-3) / 1e9
+        flops = wl.flops(M)
+        line = {
+            "metric": METRIC,
+            "value": world * M / (ms * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": f"{wl.act} MMA operands, f32 accumulate, {wl.qt} weights",
+            "data": "synthetic (seeded N(0,0.02) weights quantized offline, N(0,1) activations, random router)",
+            "config": workload_config(wl, M),
+            "tflops": world * flops / (ms * 1e-3) / 1e12,
+            "weight_gbs": world * by["weights"] / (ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                         "frac": ach / hbm, "traffic": None,
+                         "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
+                         "algorithmic_bytes_per_launch": by[dominant],
+                         "layer_frac": by["layer"] / (ms * 1e-3) / 1e9 / hbm},
+            "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"float64 numpy oracle on the first {n_tok} of the {M} tokens "
+                                       f"(each token dequantizes its {wl.k} experts), {secs:.1f} s"},
+            "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(M * wl.H * 2 + 2 * M * wl.k * 4),
+                    "d2h_bytes_per_step": int(M * wl.H * 2), "ms_per_step": e2e_ms},
+            "gpu_launches": int(round(main_r["launches_per_step"] * args.steps)),
+            "clocks": main_r["clocks"],
+            "kernel_ms": {n: round(v, 5) for n, v in kms.items()},
+            "sweep": [summarize(wl, r, hbm, tc_burst) for r in sweep],
+        }
+        line["config"]["l2"] = (f"inputs larger than L2: {by['weights'] / 1e6:.0f} MB of touched expert weights per "
+                                f"step, rotated across {main_r['copies']} packed copies between steps (L2 129 MB)")
+        print(json.dumps(line))
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    wl = WORKLOADS[args.workload]
+    M = args.M or (DEFAULT_M if DEFAULT_M in wl.Ms else wl.Ms[0])
+    layer = make_layer(wl, seed=0)
+    inp = make_inputs(wl, M, seed=0)
+    budget = max(1.0, min(args.cpu_sample_s, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, layer, inp, budget / 4)
+    toks, secs = 0, 0.0
+    for _ in range(args.steps):
+        n, s = oracle_sample(wl, layer, inp, budget)
+        toks += n
+        secs += s
+    v = toks / secs
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, M), "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"each step: float64 oracle on leading tokens of the M={M} batch for about "
+                                       f"{budget:.1f} s; {toks} tokens in {secs:.1f} s"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -18,6 +18,7 @@ from .gen import (  # noqa: F401
     quantize_int4_rtn,
     quantize_int8_rtn,
     round_to_bf16,
+    route_topk,
     round_to_f16,
     to_u16_bits,
 )

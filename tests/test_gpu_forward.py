@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import weight_only_quantized_moe_gb300 as q
-from synth import Inputs, Workload, make_inputs, make_layer, route_topk
+from synth import Inputs, Workload, make_inputs, make_layer
 from tests.gpu_util import assert_parity, device_inputs, device_layer, ensure_built, run_forward
 
 pytestmark = pytest.mark.gpu
