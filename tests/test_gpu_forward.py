@@ -59,9 +59,23 @@ def test_forward_parity(qt, act, ao, M):
 
 
 @pytest.mark.parametrize("qt,act,ao", VARIANTS[:1] + VARIANTS[3:5])
-@pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 256), (3, 2, 32)])
+@pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 128), (3, 2, 32)])
 def test_forward_forced_split_and_tile(qt, act, ao, split1, split2, tile):
     _check(_wl(qt, act, ao), 40, opts=q.make_options(split1, split2, tile))
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_int8_token_tile_256(act):
+    # one 256-row chunk per expert: a single TMEM accumulator
+    _check(_wl("int8", act), 300, opts=q.make_options(0, 0, 256))
+
+
+def test_int4_rejects_token_tile_above_128():
+    wl = _wl("int4", "bf16")
+    _, dl = _layer(wl)
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_workspace_size(dl, 40, 2, q.make_options(0, 0, 256))
+    assert ei.value.status == q.QMOE_ERR_INVALID_ARG
 
 
 def test_multi_chunk_expert_and_empty_experts():

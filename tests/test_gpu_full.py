@@ -1,0 +1,72 @@
+"""Full-size parity: every benchmark workload at its full shape, launched as
+bench.py launches it (default plan), checked on sampled tokens that the
+oracle computes one by one (tokens are independent rows of the layer)."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_quantized_moe_gb300 as q
+from synth import WORKLOADS, make_inputs, make_layer
+from tests.gpu_util import assert_parity, device_inputs, device_layer, ensure_built, run_forward
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+# (workload, M, number of sampled tokens)
+CASES = [
+    ("mixtral8x7b_w4", 16, 4),
+    ("mixtral8x7b_w4", 1, 1),
+    ("mixtral8x7b_w4_actorder", 16, 3),
+    ("mixtral8x7b_w8", 128, 3),
+    ("deepseekv2_w8", 256, 3),
+    ("mixtral8x22b_w4", 2048, 2),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+_cache = {}
+
+
+def _layer(name):
+    if name not in _cache:
+        _cache.clear()
+        gc.collect()
+        torch.cuda.empty_cache()
+        L = make_layer(WORKLOADS[name], seed=0)
+        _cache[name] = (L, device_layer(L))
+    return _cache[name]
+
+
+@pytest.mark.parametrize("name,M,n_sample", CASES)
+def test_full_size_sampled(name, M, n_sample):
+    wl = WORKLOADS[name]
+    L, dl = _layer(name)
+    inp = make_inputs(wl, M, seed=0)
+    x, ids, w = device_inputs(wl, inp)
+    out, _ = run_forward(dl, x, ids, w)
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    # sample tokens whose experts overlap, so the oracle dequantizes few experts
+    rng = np.random.default_rng(M)
+    first = int(rng.integers(M))
+    rows = [first]
+    want = set(inp.topk_ids[first].tolist())
+    for m in rng.permutation(M):
+        if len(rows) >= n_sample:
+            break
+        if int(m) not in rows and len(want | set(inp.topk_ids[m].tolist())) <= len(want) + wl.k // 2:
+            rows.append(int(m))
+            want |= set(inp.topk_ids[m].tolist())
+    for m in rng.permutation(M):
+        if len(rows) >= n_sample:
+            break
+        if int(m) not in rows:
+            rows.append(int(m))
+    ref = oracle.moe_forward_rows(L, inp.x, inp.topk_ids, inp.topk_weights, rows)
+    assert_parity(got[rows], ref, f"{name} M={M} rows={rows}")

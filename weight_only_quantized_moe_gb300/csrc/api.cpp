@@ -127,7 +127,7 @@ qmoe_status validate_layer_dims(const qmoe_layer* L) {
 struct Plan {
   int64_t M = 0, P = 0;
   int k = 0;
-  int T = 0, acc_bufs = 0, a_stages = 0, smem_stages = 0, stage_bytes = 0;
+  int T = 0, acc_bufs = 0, a_col0 = 0, a_stages = 0, ns1 = 0, ns2 = 0, stage_bytes = 0, b_terms2 = 1;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -174,13 +174,26 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     if (o->token_tile < 16 || o->token_tile > kMaxTokenTile || o->token_tile % 16 != 0) return QMOE_ERR_INVALID_ARG;
     T = o->token_tile;
   }
+  const bool int4 = L->qt == QMOE_INT4_GROUP;
+  if (int4 && T > 128) return QMOE_ERR_INVALID_ARG;  // running sum + two group partials must fit TMEM
   p.T = T;
-  p.acc_bufs = (2 * T + 2 * 64 <= 512) ? 2 : 1;
-  p.a_stages = std::min(8, (512 - p.acc_bufs * T) / 64);
-  p.stage_bytes = (L->qt == QMOE_INT4_GROUP) ? kInt4StageBytes : kInt8StageBytes;
-  const size_t stage = static_cast<size_t>(T) * 256 + ((p.stage_bytes + 1023) & ~1023);
-  p.smem_stages = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / stage));
-  if (p.smem_stages < 2) return QMOE_ERR_UNSUPPORTED;
+  if (int4) {
+    p.acc_bufs = 1;
+    p.a_col0 = 3 * T;
+  } else {
+    p.acc_bufs = (2 * T + 2 * 64 <= 512) ? 2 : 1;
+    p.a_col0 = p.acc_bufs * T;
+  }
+  p.a_stages = std::min(8, (512 - p.a_col0) / 64);
+  if (p.a_stages < 2) return QMOE_ERR_UNSUPPORTED;
+  p.stage_bytes = int4 ? kInt4StageBytes : kInt8StageBytes;
+  // bf16: the intermediate is kept as two bf16 terms (hi + rounding residual)
+  p.b_terms2 = (L->act_dtype == QMOE_BF16) ? 2 : 1;
+  const size_t wreg = (p.stage_bytes + 1023) & ~1023;
+  p.ns1 = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(T) * 256 + wreg)));
+  p.ns2 = static_cast<int>(
+      std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(p.b_terms2) * T * 256 + wreg)));
+  if (p.ns1 < 2 || p.ns2 < 2) return QMOE_ERR_UNSUPPORTED;
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
@@ -208,7 +221,7 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.off_scalars = off;  off += 256;  // num_post_padded, n_chunks
   p.off_chunks = off;   off += al256(p.max_chunks * sizeof(Chunk));
   p.off_xg = off;       off += al256(static_cast<size_t>(p.cap) * L->H * 2);
-  p.off_inter = off;    off += al256(static_cast<size_t>(p.cap) * L->I * 2);
+  p.off_inter = off;    off += al256(static_cast<size_t>(p.b_terms2) * p.cap * L->I * 2);
   p.off_h = off;        off += (p.S1 > 1) ? al256(static_cast<size_t>(p.S1) * p.cap * 2 * L->I * 4) : 0;
   p.off_y = off;        off += al256(static_cast<size_t>(p.S2) * P * L->H * 4);
   p.total = off;
@@ -261,7 +274,8 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const int P = static_cast<int>(pl.P);
 
   CUtensorMap map_xg, map_inter;
-  if (!encode_rows_map(&map_xg, xg, pl.cap, L->H) || !encode_rows_map(&map_inter, inter, pl.cap, L->I))
+  if (!encode_rows_map(&map_xg, xg, pl.cap, L->H) ||
+      !encode_rows_map(&map_inter, inter, static_cast<uint64_t>(pl.b_terms2) * pl.cap, L->I))
     return QMOE_ERR_CUDA;
 
   // events (profiling only): 2i before and 2i+1 after launch i
@@ -293,8 +307,12 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.split = pl.S1;
   g1.token_tile = pl.T;
   g1.acc_bufs = pl.acc_bufs;
+  g1.a_col0 = pl.a_col0;
   g1.a_stages = pl.a_stages;
-  g1.smem_stages = pl.smem_stages;
+  g1.smem_stages = pl.ns1;
+  g1.b_terms = 1;
+  g1.b_lo_row0 = 0;
+  g1.inter_lo_offset = (pl.b_terms2 == 2) ? pl.cap * static_cast<int64_t>(L->I) : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
   g1.chunk_group = 8;
@@ -317,6 +335,10 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g2.k_stages = pl.kst2;
   g2.split = pl.S2;
   g2.epi_mode = kEpiWeightedPairs;
+  g2.smem_stages = pl.ns2;
+  g2.b_terms = pl.b_terms2;
+  g2.b_lo_row0 = static_cast<int32_t>(pl.cap);
+  g2.inter_lo_offset = 0;
   g2.out = y;
   g2.out_ld = L->H;
   g2.out_split_stride = pl.P * static_cast<int64_t>(L->H);
@@ -333,7 +355,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(5);
   rec(6);
   if (err == cudaSuccess && pl.S1 > 1) {
-    err = launch_silu_reduce(h, npp, pl.S1, pl.cap, L->I, bf16, inter, sms, stream);
+    err = launch_silu_reduce(h, npp, pl.S1, pl.cap, L->I, bf16, inter, g1.inter_lo_offset, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(7);

@@ -220,7 +220,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 template <bool BF16>
 __global__ void __launch_bounds__(256)
     silu_reduce_kernel(const float* __restrict__ h, const int32_t* __restrict__ num_post_padded, int32_t split,
-                       int64_t cap_rows, int32_t I, uint16_t* __restrict__ inter) {
+                       int64_t cap_rows, int32_t I, uint16_t* __restrict__ inter, int64_t lo_offset) {
   const int64_t total = static_cast<int64_t>(*num_post_padded) * (I / 2);  // two j per thread
   const int64_t slab = cap_rows * 2 * static_cast<int64_t>(I);
   for (int64_t t = blockIdx.x * 256LL + threadIdx.x; t < total; t += static_cast<int64_t>(gridDim.x) * 256) {
@@ -234,27 +234,32 @@ __global__ void __launch_bounds__(256)
     }
     const float r0 = silu_f(acc.x) * acc.y;
     const float r1 = silu_f(acc.z) * acc.w;
-    uint32_t packed;
+    uint32_t packed, packed_lo = 0;
     if (BF16) {
       __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
       packed = *reinterpret_cast<uint32_t*>(&b);
+      // second bf16 term carries the rounding residual of the first
+      __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __bfloat162float(b.x), r1 - __bfloat162float(b.y));
+      packed_lo = *reinterpret_cast<uint32_t*>(&l);
     } else {
       __half2 b = __floats2half2_rn(r0, r1);
       packed = *reinterpret_cast<uint32_t*>(&b);
     }
     reinterpret_cast<uint32_t*>(inter + row * I)[j2] = packed;
+    if (lo_offset != 0) reinterpret_cast<uint32_t*>(inter + lo_offset + row * I)[j2] = packed_lo;
   }
 }
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
-                               int32_t I, bool bf16, void* inter, int num_sms, cudaStream_t stream) {
+                               int32_t I, bool bf16, void* inter, int64_t inter_lo_offset, int num_sms,
+                               cudaStream_t stream) {
   const int grid = 4 * num_sms;
   if (bf16)
     silu_reduce_kernel<true><<<grid, 256, 0, stream>>>(h, num_post_padded, split, cap_rows, I,
-                                                       static_cast<uint16_t*>(inter));
+                                                       static_cast<uint16_t*>(inter), inter_lo_offset);
   else
     silu_reduce_kernel<false><<<grid, 256, 0, stream>>>(h, num_post_padded, split, cap_rows, I,
-                                                        static_cast<uint16_t*>(inter));
+                                                        static_cast<uint16_t*>(inter), 0);
   return cudaGetLastError();
 }
 

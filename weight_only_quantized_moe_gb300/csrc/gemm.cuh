@@ -97,12 +97,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // of the chunk, nibble i holds K = 32c+8j+2i and nibble i+4 holds K = 32c+8j+2i+1.
 // Magic-number conversion: (nibble | 0x4300) is the bf16 value 128 + q and
 // (nibble | 0x6400) the f16 value 1024 + q, both exact; subtracting 136 (1032)
-// gives q - 8 exactly, and one multiply by the group scale rounds once.
+// gives q - 8 exactly.  The group scale is not applied here: it multiplies the
+// group's fp32 partial sum (see the accumulate role), so the MMA operand is exact.
 template <bool BF16>
-__device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[64]) {
+__device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t (&out)[64]) {
   const uint32_t magic = BF16 ? 0x43004300u : 0x64006400u;
   const uint32_t bias_bits = BF16 ? 0x43084308u : 0x64086408u;  // 136 (bf16) / 1032 (f16)
-  const uint32_t s2bits = sbits | (sbits << 16);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
@@ -115,11 +115,9 @@ __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t 
         if (BF16) {
           __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t),
                                      *reinterpret_cast<const __nv_bfloat162*>(&bias_bits));
-          v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&s2bits));
           r = *reinterpret_cast<uint32_t*>(&v);
         } else {
           __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), *reinterpret_cast<const __half2*>(&bias_bits));
-          v = __hmul2(v, *reinterpret_cast<const __half2*>(&s2bits));
           r = *reinterpret_cast<uint32_t*>(&v);
         }
         out[16 * c + 4 * j + i] = r;
@@ -174,8 +172,59 @@ __device__ __forceinline__ uint16_t to_act_bits(float v) {
   }
 }
 
+template <bool BF16>
+__device__ __forceinline__ float act_bits_to_float(uint16_t b) {
+  if (BF16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  __half h = *reinterpret_cast<__half*>(&b);
+  return __half2float(h);
+}
+
+// Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values,
+// scales applied).  Modes: SiLU(gate)*up into the intermediate (gate/up rows
+// are adjacent lanes), fp32 gate/up partials, or routing-weighted down output.
+template <bool BF16>
+__device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkItem& it, int c0, int row, int lane,
+                                               const float (&f)[16]) {
+  if (p.epi_mode == kEpiSiluToAct) {
+    // rows 2j / 2j+1 of the tile are gate / up of intermediate channel tile*64 + j
+    const bool even = (lane & 1) == 0;
+    const int jch = it.tile * (kTileRows / 2) + (row >> 1);
+    uint16_t* inter = static_cast<uint16_t*>(p.out);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float send = even ? f[c + 8] : f[c];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+      const float gt = even ? f[c] : recv;
+      const float up = even ? recv : f[c + 8];
+      const int col = even ? c : c + 8;
+      const float v = silu_dev(gt) * up;
+      const int64_t idx = static_cast<int64_t>(it.row0 + c0 + col) * p.inter_ld + jch;
+      const uint16_t hi = to_act_bits<BF16>(v);
+      inter[idx] = hi;
+      if (p.inter_lo_offset != 0) inter[p.inter_lo_offset + idx] = to_act_bits<BF16>(v - act_bits_to_float<BF16>(hi));
+    }
+  } else if (p.epi_mode == kEpiPartialRows) {
+    float* h = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) h[static_cast<int64_t>(it.row0 + c0 + c) * p.out_ld + it.tile * kTileRows + row] = f[c];
+  } else {
+    float* y = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int pair = __ldg(p.sorted_ids + it.row0 + c0 + c);
+      if (pair < p.P)
+        y[static_cast<int64_t>(pair) * p.out_ld + it.tile * kTileRows + row] = f[c] * __ldg(p.topk_w + pair);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
+//
+// TMEM columns: int8 keeps acc_bufs fp32 accumulators of T columns ([b*T, b*T+T));
+// int4 keeps a running fp32 sum [0, T) and two group partials [T, 3T) that the
+// MMA writes one 128-K group at a time, so each group's scale multiplies an
+// fp32 partial instead of rounding the weights.  The A stages follow at a_col0.
 // ---------------------------------------------------------------------------
 template <bool INT4, bool BF16>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -184,8 +233,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int T = p.token_tile;
-  const uint32_t b_bytes = static_cast<uint32_t>(T) * 256u;
-  const uint32_t st_bytes = gemm_stage_bytes(T, p.stage_bytes);
+  const int NB = p.b_terms;
+  const uint32_t b_bytes = static_cast<uint32_t>(NB * T) * 256u;
+  const uint32_t st_bytes = gemm_stage_bytes(NB * T, p.stage_bytes);
   const int NS = p.smem_stages, NA = p.a_stages, ACCB = p.acc_bufs;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * st_bytes);
@@ -230,7 +280,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int nch = *p.n_chunks;
   const int n_items = nch * p.n_tiles * p.split;
-  const uint32_t a_col0 = static_cast<uint32_t>(ACCB * T);
+  const uint32_t a_col0 = static_cast<uint32_t>(p.a_col0);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -244,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         decode_item(p, nch, i, it);
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages * static_cast<int64_t>(p.stage_bytes);
-        const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + static_cast<uint32_t>(it.nrows) * 256u;
+        const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + static_cast<uint32_t>(NB * it.nrows) * 256u;
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           const int s = g % NS;
           if (!mbar_wait(smem_u32(empty + s), ((g / NS) & 1) ^ 1, abort_flag)) {
@@ -256,10 +306,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(fb, tx);
           tma_load_1d(smem_u32(st + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
                       pol_w);
-          for (int a = 0; a < 2; ++a)
-            for (int r = 0; r < it.nrows; r += 16)
-              tma_load_2d(smem_u32(st + a * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64, it.row0 + r, fb,
-                          pol_b);
+          for (int h = 0; h < NB; ++h)
+            for (int a = 0; a < 2; ++a)
+              for (int r = 0; r < it.nrows; r += 16)
+                tma_load_2d(smem_u32(st + (h * 2 + a) * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64,
+                            h * p.b_lo_row0 + it.row0 + r, fb, pol_b);
           ++g;
         }
       }
@@ -275,18 +326,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
         decode_item(p, nch, i, it);
-        const int b = itn % ACCB;
-        const int use = itn / ACCB;
-        if (!mbar_wait(smem_u32(accempty + b), (use & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * T);
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), BF16);
+        int b = 0;
+        if (!INT4) {
+          b = itn % ACCB;
+          if (!mbar_wait(smem_u32(accempty + b), ((itn / ACCB) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           const int s = g % NS;
           const int ja = g % NA;
+          uint32_t d_tmem;
+          if (INT4) {
+            // one partial per 128-K group, double buffered
+            if (!mbar_wait(smem_u32(accempty + (g & 1)), ((g >> 1) & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            d_tmem = tmem + static_cast<uint32_t>(T + (g & 1) * T);
+          } else {
+            d_tmem = tmem + static_cast<uint32_t>(b * T);
+          }
           if (!mbar_wait(smem_u32(full + s), (g / NS) & 1, abort_flag) ||
               !mbar_wait(smem_u32(afull + ja), (g / NA) & 1, abort_flag)) {
             ok = false;
@@ -295,19 +357,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ja * 64);
           const uint32_t b_base = smem_u32(smem + s * st_bytes);
+          const bool first_k = INT4 || ks == it.ks0;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bdesc =
-                make_sdesc_k_sw128(b_base + static_cast<uint32_t>((kk >> 2) * T * 128 + (kk & 3) * 32));
-            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc, idesc,
-                       (ks > it.ks0 || kk > 0) ? 1u : 0u);
+            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * T * 128 + (kk & 3) * 32);
+            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), make_sdesc_k_sw128(b_base + koff), idesc,
+                       (!first_k || kk > 0) ? 1u : 0u);
+            if (NB == 2)
+              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
+                         make_sdesc_k_sw128(b_base + static_cast<uint32_t>(2 * T * 128) + koff), idesc, 1u);
           }
           mma_commit(smem_u32(empty + s));
           mma_commit(smem_u32(aempty + ja));
+          if (INT4) mma_commit(smem_u32(accfull + (g & 1)));
           ++g;
         }
         if (!ok) break;
-        mma_commit(smem_u32(accfull + b));
+        if (!INT4) mma_commit(smem_u32(accfull + b));
         ++itn;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
@@ -338,10 +404,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint4 pk[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
-          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(empty + s));
-          dequant_int4_row<BF16>(pk, sbits, out);
+          dequant_int4_row<BF16>(pk, out);
         } else {
           uint4 pk[8];
 #pragma unroll
@@ -364,62 +429,73 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
   } else if (warp < 4) {
-    // ------------------------------------------------------------ epilogue warpgroup
+    // ------------------------------------------------------------ accumulate / epilogue warpgroup
     const int q = warp;
     const int row = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    int itn = 0;
+    int itn = 0, g = 0;
     bool ok = true;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
-      const int b = itn % ACCB;
-      const int use = itn / ACCB;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const float rs =
-          INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
-      const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(b * T);
-      for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
-        tmem_wait_ld();
-        if (c0 + 16 >= it.nrows) {
+      if (INT4) {
+        // running sum += scale(group, row) * partial(group), group by group
+        const uint8_t* sblk = p.w +
+                              ((static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages) *
+                                  static_cast<int64_t>(p.stage_bytes) +
+                              8192 + row * 2;
+        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g) {
+          const uint16_t sb = __ldg(reinterpret_cast<const unsigned short*>(sblk + static_cast<int64_t>(ks) * p.stage_bytes));
+          const float scale = act_bits_to_float<BF16>(sb);
+          const int pb = g & 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + pb), (g >> 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const bool first = ks == it.ks0, last = ks == it.ks1 - 1;
+          const uint32_t tpart = tmem + lane_base + static_cast<uint32_t>(T + pb * T);
+          const uint32_t tacc = tmem + lane_base;
+          for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+            uint32_t v[16], a[16];
+            tmem_ld_32x32b_x16(tpart + static_cast<uint32_t>(c0), v);
+            if (!first) tmem_ld_32x32b_x16(tacc + static_cast<uint32_t>(c0), a);
+            tmem_wait_ld();
+            float f[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              f[c] = first ? scale * __uint_as_float(v[c]) : fmaf(scale, __uint_as_float(v[c]), __uint_as_float(a[c]));
+            if (last) {
+              epilogue_store<BF16>(p, it, c0, row, lane, f);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) a[c] = __float_as_uint(f[c]);
+              tmem_st_32x32b_x16(tacc + static_cast<uint32_t>(c0), a);
+            }
+          }
+          if (!last) tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(accempty + b));
+          if (lane == 0) mbar_arrive(smem_u32(accempty + pb));
         }
-        float f[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) f[c] = __uint_as_float(v[c]) * rs;
-        if (p.epi_mode == kEpiSiluToAct) {
-          // rows 2j / 2j+1 of the tile are gate / up of intermediate channel tile*64 + j
-          const bool even = (lane & 1) == 0;
-          const int jch = it.tile * (kTileRows / 2) + (row >> 1);
-          uint16_t* inter = static_cast<uint16_t*>(p.out);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float send = even ? f[c + 8] : f[c];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const float gt = even ? f[c] : recv;
-            const float up = even ? recv : f[c + 8];
-            const int col = even ? c : c + 8;
-            inter[static_cast<int64_t>(it.row0 + c0 + col) * p.inter_ld + jch] = to_act_bits<BF16>(silu_dev(gt) * up);
+      } else {
+        const int b = itn % ACCB;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), (itn / ACCB) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float rs = __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
+        const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(b * T);
+        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
+          tmem_wait_ld();
+          if (c0 + 16 >= it.nrows) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(accempty + b));
           }
-        } else if (p.epi_mode == kEpiPartialRows) {
-          float* h = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
+          float f[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            h[static_cast<int64_t>(it.row0 + c0 + c) * p.out_ld + it.tile * kTileRows + row] = f[c];
-        } else {
-          float* y = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int pair = __ldg(p.sorted_ids + it.row0 + c0 + c);
-            if (pair < p.P)
-              y[static_cast<int64_t>(pair) * p.out_ld + it.tile * kTileRows + row] = f[c] * __ldg(p.topk_w + pair);
-          }
+          for (int c = 0; c < 16; ++c) f[c] = __uint_as_float(v[c]) * rs;
+          epilogue_store<BF16>(p, it, c0, row, lane, f);
         }
       }
       ++itn;

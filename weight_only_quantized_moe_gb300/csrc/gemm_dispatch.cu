@@ -9,7 +9,7 @@ cudaError_t launch_gemm_i8_f16(const CUtensorMap*, const GemmParams&, int, cudaS
 cudaError_t launch_gemm_i8_bf16(const CUtensorMap*, const GemmParams&, int, cudaStream_t);
 
 size_t gemm_smem_bytes(const GemmParams& p) {
-  return 1024 + static_cast<size_t>(p.smem_stages) * gemm_stage_bytes(p.token_tile, p.stage_bytes) + kBarrierBytes;
+  return 1024 + static_cast<size_t>(p.smem_stages) * gemm_stage_bytes(p.b_terms * p.token_tile, p.stage_bytes) + kBarrierBytes;
 }
 
 cudaError_t launch_gemm(bool int4, bool bf16, const CUtensorMap* tmap_b, const GemmParams& p, int grid,

@@ -46,14 +46,18 @@ struct GemmParams {
   int32_t* status;
   int64_t out_ld;            // elements per output row
   int64_t out_split_stride;  // elements per split slab
+  int64_t inter_lo_offset;   // SiLU epilogue with a two-term intermediate: elements from hi to lo slab (0: one term)
   int32_t n_tiles;
   int32_t k_stages;
   int32_t split;
   int32_t token_tile;        // T: B rows per stage buffer, TMEM columns per accumulator
-  int32_t acc_bufs;          // 1 or 2
+  int32_t acc_bufs;          // int8: 1 or 2 TMEM accumulators; int4: unused (one running sum + two group partials)
+  int32_t a_col0;            // first TMEM column of the A stages
   int32_t a_stages;          // TMEM A stages (64 columns each)
   int32_t smem_stages;       // shared-memory pipeline depth
   int32_t stage_bytes;       // packed weight bytes per stage
+  int32_t b_terms;           // 1, or 2 when the B operand is a hi+lo pair of bf16 matrices
+  int32_t b_lo_row0;         // row offset of the lo term in the B tensor map
   int32_t epi_mode;
   int32_t P;                 // number of token-expert pairs
   int32_t chunk_group;       // work-item raster: chunks per group
@@ -70,7 +74,8 @@ cudaError_t launch_gather(const void* x, const int32_t* sorted_ids, const int32_
                           int32_t H, int32_t block, int64_t cap_rows, void* xg, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
-                               int32_t I, bool bf16, void* inter, int num_sms, cudaStream_t stream);
+                               int32_t I, bool bf16, void* inter, int64_t inter_lo_offset, int num_sms,
+                               cudaStream_t stream);
 
 cudaError_t launch_out_reduce(const float* y, int32_t split, int64_t M, int32_t top_k, int32_t H, bool bf16,
                               void* out, int num_sms, cudaStream_t stream);
