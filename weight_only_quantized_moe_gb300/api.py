@@ -221,6 +221,9 @@ def qmoe_forward_profiled(layer: DeviceLayer, x, topk_ids, topk_weights, out, wo
     from ctypes import c_int32 as _i32
     M = x.shape[0]
     k = topk_ids.shape[1]
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+            e.record(torch.cuda.current_stream() if stream is None else stream)
     evs = (c_void_p * len(events))(*[c_void_p(e.cuda_event) for e in events])
     n = _i32(0)
     st = N.lib().qmoe_forward_profiled(byref(layer.struct), c_void_p(x.data_ptr()), M, c_void_p(topk_ids.data_ptr()),

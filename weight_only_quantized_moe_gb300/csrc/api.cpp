@@ -193,7 +193,7 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.ns1 = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(T) * 256 + wreg)));
   p.ns2 = static_cast<int>(
       std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(p.b_terms2) * T * 256 + wreg)));
-  if (p.ns1 < 2 || p.ns2 < 2) return QMOE_ERR_UNSUPPORTED;
+  if (p.ns1 < 2 || p.ns2 < 2) return QMOE_ERR_INVALID_ARG;  // only a forced token tile gets here
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;

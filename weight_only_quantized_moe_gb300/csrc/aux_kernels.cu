@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "ptx.cuh"
 #include "qmoe_internal.h"
 
 namespace qmoe {
@@ -62,6 +63,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   __shared__ int warp_sums[32];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();  // no-op unless launched as a dependent
 
   if (tid == 0) {
     s_bad = 0;
@@ -154,10 +157,10 @@ cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  moe_align_kernel<<<1, kAlignThreads, smem, stream>>>(topk_ids, P, E, block, capacity, sorted_ids, expert_ids,
-                                                       num_post_padded, chunks ? token_tile : 0, chunks, n_chunks,
-                                                       status);
-  return cudaGetLastError();
+  // first kernel of a forward: ordinary stream order behind the caller's work
+  return launch_kernel(moe_align_kernel, dim3(1), dim3(kAlignThreads), smem, stream, false, topk_ids, P, E, block,
+                       capacity, sorted_ids, expert_ids, num_post_padded, chunks ? token_tile : 0, chunks, n_chunks,
+                       status);
 }
 
 // ---------------------------------------------------------------------------
@@ -173,6 +176,8 @@ __global__ void __launch_bounds__(kGatherThreads)
                   const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_post_padded,
                   const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B,
                   uint16_t* __restrict__ xg) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int total = *num_post_padded;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (kGatherThreads / 32);
@@ -205,10 +210,9 @@ cudaError_t launch_gather(const void* x, const int32_t* sorted_ids, const int32_
                           int32_t H, int32_t block, int64_t cap_rows, void* xg, int num_sms, cudaStream_t stream) {
   const int64_t want = (cap_rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
-  gather_kernel<<<grid, kGatherThreads, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_ids, expert_ids,
-                                                     num_post_padded, perm13, P, top_k, H, block,
-                                                     static_cast<uint16_t*>(xg));
-  return cudaGetLastError();
+  return launch_kernel(gather_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, true,
+                       static_cast<const uint16_t*>(x), sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H,
+                       block, static_cast<uint16_t*>(xg));
 }
 
 // ---------------------------------------------------------------------------
@@ -221,6 +225,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(256)
     silu_reduce_kernel(const float* __restrict__ h, const int32_t* __restrict__ num_post_padded, int32_t split,
                        int64_t cap_rows, int32_t I, uint16_t* __restrict__ inter, int64_t lo_offset) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t total = static_cast<int64_t>(*num_post_padded) * (I / 2);  // two j per thread
   const int64_t slab = cap_rows * 2 * static_cast<int64_t>(I);
   for (int64_t t = blockIdx.x * 256LL + threadIdx.x; t < total; t += static_cast<int64_t>(gridDim.x) * 256) {
@@ -255,12 +261,10 @@ cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, i
                                cudaStream_t stream) {
   const int grid = 4 * num_sms;
   if (bf16)
-    silu_reduce_kernel<true><<<grid, 256, 0, stream>>>(h, num_post_padded, split, cap_rows, I,
-                                                       static_cast<uint16_t*>(inter), inter_lo_offset);
-  else
-    silu_reduce_kernel<false><<<grid, 256, 0, stream>>>(h, num_post_padded, split, cap_rows, I,
-                                                        static_cast<uint16_t*>(inter), 0);
-  return cudaGetLastError();
+    return launch_kernel(silu_reduce_kernel<true>, dim3(grid), dim3(256), 0, stream, true, h, num_post_padded, split,
+                         cap_rows, I, static_cast<uint16_t*>(inter), inter_lo_offset);
+  return launch_kernel(silu_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, h, num_post_padded, split,
+                       cap_rows, I, static_cast<uint16_t*>(inter), int64_t(0));
 }
 
 // ---------------------------------------------------------------------------
@@ -271,6 +275,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(256)
     out_reduce_kernel(const float* __restrict__ y, int32_t split, int64_t M, int32_t top_k, int32_t H,
                       uint16_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t total = M * (H / 4);
   const int64_t slab = M * top_k * static_cast<int64_t>(H);
   for (int64_t t = blockIdx.x * 256LL + threadIdx.x; t < total; t += static_cast<int64_t>(gridDim.x) * 256) {
@@ -303,10 +309,10 @@ cudaError_t launch_out_reduce(const float* y, int32_t split, int64_t M, int32_t 
   const int64_t want = (M * (H / 4) + 255) / 256;
   const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
   if (bf16)
-    out_reduce_kernel<true><<<grid, 256, 0, stream>>>(y, split, M, top_k, H, static_cast<uint16_t*>(out));
-  else
-    out_reduce_kernel<false><<<grid, 256, 0, stream>>>(y, split, M, top_k, H, static_cast<uint16_t*>(out));
-  return cudaGetLastError();
+    return launch_kernel(out_reduce_kernel<true>, dim3(grid), dim3(256), 0, stream, true, y, split, M, top_k, H,
+                         static_cast<uint16_t*>(out));
+  return launch_kernel(out_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, y, split, M, top_k, H,
+                       static_cast<uint16_t*>(out));
 }
 
 }  // namespace qmoe

@@ -277,6 +277,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // everything above overlaps the previous kernel; its results are read below
+  pdl_launch_dependents();
+  pdl_wait();
 
   const int nch = *p.n_chunks;
   const int n_items = nch * p.n_tiles * p.split;
@@ -518,8 +521,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* tmap_b, const GemmParams& p, int gr
   cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<INT4, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  qmoe_gemm_kernel<INT4, BF16><<<grid, kGemmThreads, smem, stream>>>(*tmap_b, p);
-  return cudaGetLastError();
+  return launch_kernel(qmoe_gemm_kernel<INT4, BF16>, dim3(grid), dim3(kGemmThreads), smem, stream, true, *tmap_b, p);
 }
 
 }  // namespace qmoe
