@@ -91,6 +91,21 @@ def oracle_sample(wl, layer, inp, budget_s):
     return n, time.perf_counter() - t0
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Slowest rank's time: every rank contributes its own ms, all get the max."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Replicas: every rank processes its own batch; value = all ranks' tokens / slowest rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -241,11 +256,7 @@ def run_gpu(args, rank, world):
         return res
 
     main = measure(M, args.steps, args.warmup)
-    ms = main["ms"]
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(main["ms"], world, dev)
 
     # end to end through the host-buffer entry point: pinned H2D of x/ids/weights,
     # the forward, D2H of out, every step
@@ -263,11 +274,7 @@ def run_gpu(args, rank, world):
         q.qmoe_forward_host(copies[i % len(copies)], xh, idh, wh, outh, wsh)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     sweep = []
     if not args.no_sweep and rank == 0:
@@ -318,7 +325,7 @@ def main():
         flops = wl.flops(M)
         line = {
             "metric": METRIC,
-            "value": world * M / (ms * 1e-3),
+            "value": whole_job_tokens_per_s(M, world, ms),
             "unit": "tokens/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -340,7 +347,7 @@ def main():
             "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"float64 numpy oracle on the first {n_tok} of the {M} tokens "
                                        f"(each token dequantizes its {wl.k} experts), {secs:.1f} s"},
-            "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": whole_job_tokens_per_s(M, world, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(M * wl.H * 2 + 2 * M * wl.k * 4),
                     "d2h_bytes_per_step": int(M * wl.H * 2), "ms_per_step": e2e_ms},
             "gpu_launches": int(round(main_r["launches_per_step"] * args.steps)),

@@ -122,7 +122,13 @@ typedef struct {
   int32_t split1;
   int32_t split2;
   int32_t token_tile;
-  int32_t reserved[5];
+  /* Test hook for the device-side failure path (0 = off).  1: in the gate/up
+   * GEMM, CTA 0 arms its first pipeline stage without issuing the copies that
+   * complete it, so its consumers wait on a phase that never completes; the
+   * bounded waits give up after about a second, record QMOE_ERR_TIMEOUT and the
+   * kernel exits with the CUDA context intact (the output is then garbage). */
+  int32_t fault_injection;
+  int32_t reserved[4];
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */

@@ -313,6 +313,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.b_terms = 1;
   g1.b_lo_row0 = 0;
   g1.inter_lo_offset = (pl.b_terms2 == 2) ? pl.cap * static_cast<int64_t>(L->I) : 0;
+  g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
   g1.chunk_group = 8;
@@ -339,6 +340,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g2.b_terms = pl.b_terms2;
   g2.b_lo_row0 = static_cast<int32_t>(pl.cap);
   g2.inter_lo_offset = 0;
+  g2.fault_injection = 0;
   g2.out = y;
   g2.out_ld = L->H;
   g2.out_split_stride = pl.P * static_cast<int64_t>(L->H);

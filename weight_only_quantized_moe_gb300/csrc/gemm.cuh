@@ -307,6 +307,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* st = smem + s * st_bytes;
           const uint32_t fb = smem_u32(full + s);
           mbar_arrive_expect_tx(fb, tx);
+          if (p.fault_injection == 1 && blockIdx.x == 0 && g == 0) {
+            ++g;  // armed, never filled: the consumers' bounded waits must give up
+            continue;
+          }
           tma_load_1d(smem_u32(st + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
                       pol_w);
           for (int h = 0; h < NB; ++h)

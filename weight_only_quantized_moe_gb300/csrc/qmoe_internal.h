@@ -62,6 +62,7 @@ struct GemmParams {
   int32_t P;                 // number of token-expert pairs
   int32_t chunk_group;       // work-item raster: chunks per group
   int32_t inter_ld;          // I (for the SiLU epilogue)
+  int32_t fault_injection;   // 1: CTA 0 arms its first stage without copies (failure-path test)
 };
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
