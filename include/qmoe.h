@@ -262,6 +262,32 @@ qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64
                               void* out_host, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * qmoe_forward for callers that cannot allocate device memory at call time --
+ * for example an inference-engine plugin whose memory plan is fixed before it
+ * runs and that is handed no scratch buffer, or a serving loop that must not
+ * enter an allocator (cudaMalloc can synchronise the device).  The pages have
+ * no counterpart to this entry point.
+ *
+ * The forward's scratch is a 64 MiB array of device memory inside the library
+ * image (resident on every GPU that loads the library until the process
+ * exits); the call allocates nothing.  x, topk_ids, topk_weights and out are
+ * as for qmoe_forward.  A layer/M/top_k whose qmoe_workspace_size exceeds
+ * 64 MiB gives QMOE_ERR_WORKSPACE and launches nothing.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture on the device.
+ *   - All calls share the one array, so calls whose GPU work overlaps (other
+ *     streams, other host threads) race on it and give wrong results; order
+ *     them on the GPU.  The array keeps the last call's contents; the forward
+ *     needs none of it cleared.
+ *   - Device-side faults (a bad expert id, a kernel wait timeout) are recorded
+ *     in the shared array and are not reported by this entry point.
+ */
+qmoe_status qmoe_forward_noalloc(const qmoe_layer* layer, const void* x, int64_t M,
+                                 const int32_t* topk_ids, const float* topk_weights, int32_t top_k,
+                                 void* out, void* stream);
+
+/*
  * Synchronise `stream` and return the first device-side fault recorded in
  * `workspace` by the most recent forward that used it (QMOE_OK if none).
  */

@@ -26,6 +26,7 @@ from .api import (  # noqa: F401
     packed_bytes,
     qmoe_forward,
     qmoe_forward_host,
+    qmoe_forward_noalloc,
     qmoe_forward_profiled,
     qmoe_moe_align,
     qmoe_pack_int4,

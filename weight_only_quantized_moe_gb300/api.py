@@ -253,3 +253,18 @@ def qmoe_forward_host(layer: DeviceLayer, x_host: torch.Tensor, topk_ids_host: t
 
 def qmoe_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     return int(N.lib().qmoe_read_device_status(c_void_p(workspace.data_ptr()), _stream_ptr(stream)))
+
+
+def qmoe_forward_noalloc(layer: DeviceLayer, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                         out: torch.Tensor | None = None, stream=None):
+    """qmoe_forward with the library's built-in 64 MiB device scratch instead of a
+    caller workspace, for callers that may not allocate (see include/qmoe.h)."""
+    M = x.shape[0]
+    k = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    st = N.lib().qmoe_forward_noalloc(byref(layer.struct), c_void_p(x.data_ptr()), M, c_void_p(topk_ids.data_ptr()),
+                                      c_void_p(topk_weights.data_ptr()), k, c_void_p(out.data_ptr()),
+                                      _stream_ptr(stream))
+    N.check(st, "qmoe_forward_noalloc")
+    return out

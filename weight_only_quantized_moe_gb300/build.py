@@ -31,6 +31,7 @@ SOURCES = [
     "gemm_i4_bf16.cu",
     "gemm_i8_f16.cu",
     "gemm_i8_bf16.cu",
+    "noalloc.cu",
 ]
 
 

@@ -508,6 +508,13 @@ bool pack_dims_ok(int32_t E, int32_t H, int32_t I) {
 }
 
 }  // namespace
+
+qmoe_status forward_into_workspace(const qmoe_layer* layer, const void* x, int64_t M, const int32_t* topk_ids,
+                                   const float* topk_weights, int32_t top_k, void* out, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream) {
+  return forward_impl(layer, x, M, topk_ids, topk_weights, top_k, out, ws, ws_bytes, stream, nullptr);
+}
+
 }  // namespace qmoe
 
 using namespace qmoe;

@@ -105,3 +105,12 @@ cudaError_t launch_gemm(bool int4, bool bf16, const CUtensorMap* tmap_b, const G
                         cudaStream_t stream);
 
 }  // namespace qmoe
+
+#include "qmoe.h"
+
+namespace qmoe {
+// The forward on a caller-supplied device workspace of ws_bytes bytes (api.cpp).
+qmoe_status forward_into_workspace(const qmoe_layer* layer, const void* x, int64_t M, const int32_t* topk_ids,
+                                   const float* topk_weights, int32_t top_k, void* out, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+}  // namespace qmoe
