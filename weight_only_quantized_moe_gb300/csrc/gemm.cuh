@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 4 + 1);  // 4 dequant warps + 1 MMA commit
+      // 4 dequant warps + 1 MMA commit (+ 4 accumulate warps, which read the int4 group scale from the stage)
+      mbar_init(smem_u32(empty + s), INT4 ? 4 + 1 + 4 : 4 + 1);
     }
     for (int j = 0; j < NA; ++j) {
       mbar_init(smem_u32(afull + j), 4);
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
+      Ring st;
       int g = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -299,25 +301,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages * static_cast<int64_t>(p.stage_bytes);
         const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + static_cast<uint32_t>(NB * it.nrows) * 256u;
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          const int s = g % NS;
-          if (!mbar_wait(smem_u32(empty + s), ((g / NS) & 1) ^ 1, abort_flag)) {
+          if (!mbar_wait(smem_u32(empty + st.idx), st.phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * st_bytes;
-          const uint32_t fb = smem_u32(full + s);
+          uint8_t* sp = smem + st.idx * st_bytes;
+          const uint32_t fb = smem_u32(full + st.idx);
           mbar_arrive_expect_tx(fb, tx);
-          if (p.fault_injection == 1 && blockIdx.x == 0 && g == 0) {
-            ++g;  // armed, never filled: the consumers' bounded waits must give up
-            continue;
+          if (!(p.fault_injection == 1 && blockIdx.x == 0 && g == 0)) {  // injected: armed, never filled
+            tma_load_1d(smem_u32(sp + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
+                        pol_w);
+            for (int h = 0; h < NB; ++h)
+              for (int a = 0; a < 2; ++a)
+                for (int r = 0; r < it.nrows; r += 16)
+                  tma_load_2d(smem_u32(sp + (h * 2 + a) * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64,
+                              h * p.b_lo_row0 + it.row0 + r, fb, pol_b);
           }
-          tma_load_1d(smem_u32(st + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
-                      pol_w);
-          for (int h = 0; h < NB; ++h)
-            for (int a = 0; a < 2; ++a)
-              for (int r = 0; r < it.nrows; r += 16)
-                tma_load_2d(smem_u32(st + (h * 2 + a) * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64,
-                            h * p.b_lo_row0 + it.row0 + r, fb, pol_b);
+          st.next(NS);
           ++g;
         }
       }
@@ -328,6 +328,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      Ring fr, ar;
       int g = 0, itn = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -336,15 +337,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), BF16);
         int b = 0;
         if (!INT4) {
-          b = itn % ACCB;
-          if (!mbar_wait(smem_u32(accempty + b), ((itn / ACCB) & 1) ^ 1, abort_flag)) {
+          b = (ACCB == 2) ? (itn & 1) : 0;
+          const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
+          if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
         }
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          const int s = g % NS;
-          const int ja = g % NA;
           uint32_t d_tmem;
           if (INT4) {
             // one partial per 128-K group, double buffered
@@ -356,27 +356,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             d_tmem = tmem + static_cast<uint32_t>(b * T);
           }
-          if (!mbar_wait(smem_u32(full + s), (g / NS) & 1, abort_flag) ||
-              !mbar_wait(smem_u32(afull + ja), (g / NA) & 1, abort_flag)) {
+          if (!mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag) ||
+              !mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ja * 64);
-          const uint32_t b_base = smem_u32(smem + s * st_bytes);
+          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
+          // descriptor of the stage's first K step; later K steps only move its start address
+          const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes));
           const bool first_k = INT4 || ks == it.ks0;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * T * 128 + (kk & 3) * 32);
-            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), make_sdesc_k_sw128(b_base + koff), idesc,
+            const uint64_t koff16 = static_cast<uint64_t>(((kk >> 2) * T * 128 + (kk & 3) * 32) >> 4);
+            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc,
                        (!first_k || kk > 0) ? 1u : 0u);
             if (NB == 2)
               mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
-                         make_sdesc_k_sw128(b_base + static_cast<uint32_t>(2 * T * 128) + koff), idesc, 1u);
+                         bdesc0 + koff16 + static_cast<uint64_t>((2 * T * 128) >> 4), idesc, 1u);
           }
-          mma_commit(smem_u32(empty + s));
-          mma_commit(smem_u32(aempty + ja));
+          mma_commit(smem_u32(empty + fr.idx));
+          mma_commit(smem_u32(aempty + ar.idx));
           if (INT4) mma_commit(smem_u32(accfull + (g & 1)));
+          fr.next(NS);
+          ar.next(NA);
           ++g;
         }
         if (!ok) break;
@@ -394,44 +397,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    Ring fr, ar;
     int g = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
-      for (int ks = it.ks0; ks < it.ks1; ++ks, ++g) {
+      for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, fr.next(NS), ar.next(NA)) {
         if ((g & 1) != wg) continue;
-        const int s = g % NS;
-        const int ja = g % NA;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (g / NS) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag));
         if (!ok) break;
-        const uint8_t* wst = smem + s * st_bytes + b_bytes;
+        const uint8_t* wst = smem + fr.idx * st_bytes + b_bytes;
         uint32_t out[64];
         if (INT4) {
           uint4 pk[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(empty + s));
+          if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
           dequant_int4_row<BF16>(pk, out);
         } else {
           uint4 pk[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(empty + s));
+          if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
           dequant_int8_row<BF16>(pk, out);
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ja), ((g / NA) & 1) ^ 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ar.idx), ar.phase ^ 1u, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ja * 64);
+        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64);
         tmem_st_32x32b_x32<0>(ta, out);
         tmem_st_32x32b_x32<32>(ta + 32, out);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(afull + ja));
+        if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
       }
     }
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
@@ -441,51 +443,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int itn = 0, g = 0;
+    Ring sr;  // stage that holds the current group's scales
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
       if (INT4) {
         // running sum += scale(group, row) * partial(group), group by group
-        const uint8_t* sblk = p.w +
-                              ((static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages) *
-                                  static_cast<int64_t>(p.stage_bytes) +
-                              8192 + row * 2;
-        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g) {
-          const uint16_t sb = __ldg(reinterpret_cast<const unsigned short*>(sblk + static_cast<int64_t>(ks) * p.stage_bytes));
-          const float scale = act_bits_to_float<BF16>(sb);
+        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, sr.next(NS)) {
           const int pb = g & 1;
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + pb), (g >> 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
+          // the group's MMAs are done but its stage is still held for us: take the scale, release the stage
+          const uint16_t sb = *reinterpret_cast<const uint16_t*>(smem + sr.idx * st_bytes + b_bytes + 8192 + row * 2);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(empty + sr.idx));
+          const float scale = act_bits_to_float<BF16>(sb);
           const bool first = ks == it.ks0, last = ks == it.ks1 - 1;
+          if (!first) tmem_wait_st();  // the previous group's running-sum stores
           const uint32_t tpart = tmem + lane_base + static_cast<uint32_t>(T + pb * T);
           const uint32_t tacc = tmem + lane_base;
-          for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-            uint32_t v[16], a[16];
-            tmem_ld_32x32b_x16(tpart + static_cast<uint32_t>(c0), v);
-            if (!first) tmem_ld_32x32b_x16(tacc + static_cast<uint32_t>(c0), a);
+          for (int c0 = 0; c0 < it.nrows; c0 += 32) {
+            const bool two = c0 + 32 <= it.nrows;
+            uint32_t v[32], a[32];
+            tmem_ld_32x32b_x16<0>(tpart + static_cast<uint32_t>(c0), v);
+            if (two) tmem_ld_32x32b_x16<16>(tpart + static_cast<uint32_t>(c0 + 16), v);
+            if (!first) {
+              tmem_ld_32x32b_x16<0>(tacc + static_cast<uint32_t>(c0), a);
+              if (two) tmem_ld_32x32b_x16<16>(tacc + static_cast<uint32_t>(c0 + 16), a);
+            }
             tmem_wait_ld();
-            float f[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              f[c] = first ? scale * __uint_as_float(v[c]) : fmaf(scale, __uint_as_float(v[c]), __uint_as_float(a[c]));
-            if (last) {
-              epilogue_store<BF16>(p, it, c0, row, lane, f);
-            } else {
+            for (int h = 0; h < 2; ++h) {
+              if (h == 1 && !two) break;
+              float f[16];
 #pragma unroll
-              for (int c = 0; c < 16; ++c) a[c] = __float_as_uint(f[c]);
-              tmem_st_32x32b_x16(tacc + static_cast<uint32_t>(c0), a);
+              for (int c = 0; c < 16; ++c)
+                f[c] = first ? scale * __uint_as_float(v[16 * h + c])
+                             : fmaf(scale, __uint_as_float(v[16 * h + c]), __uint_as_float(a[16 * h + c]));
+              if (last) {
+                epilogue_store<BF16>(p, it, c0 + 16 * h, row, lane, f);
+              } else {
+                uint32_t o[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(f[c]);
+                tmem_st_32x32b_x16(tacc + static_cast<uint32_t>(c0 + 16 * h), o);
+              }
             }
           }
-          if (!last) tmem_wait_st();
+          // the partial has been read (wait::ld above); running-sum stores may still be in flight
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(accempty + pb));
         }
+        if (!ok) break;
       } else {
-        const int b = itn % ACCB;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), (itn / ACCB) & 1, abort_flag));
+        const int b = (ACCB == 2) ? (itn & 1) : 0;
+        const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const float rs = __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
@@ -507,6 +523,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       ++itn;
     }
+    if (INT4) tmem_wait_st();  // no running-sum store may be in flight when TMEM is released
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
   }
 

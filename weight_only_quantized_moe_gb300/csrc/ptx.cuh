@@ -14,6 +14,9 @@ namespace qmoe {
 // Limit for any single pipeline wait.  Real waits are micro-seconds; a wait
 // that reaches this limit means the pipeline is broken and the kernel stops.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// Suspend-time hint of one try_wait: the thread wakes as soon as the phase
+// completes; the hint only bounds one sleep, so the limit above stays checked.
+constexpr uint32_t kSuspendHintNs = 1000000u;  // 1 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -62,14 +65,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       : "memory");
 }
 
+// Test for completion of the phase with the given parity.  The thread is
+// suspended (it issues nothing) until the phase completes or the hinted time
+// passes, so waiting warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -86,6 +92,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
+
+// Position in a ring of n pipeline slots plus the phase parity of the current lap.
+struct Ring {
+  int idx = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 // ---------------------------------------------------------------------------
 // TMA (bulk async copies, completion counted on an mbarrier in bytes)
@@ -215,13 +233,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Warp-collective TMEM load: 16 consecutive 32-bit columns per lane.
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)[16]) {
+// Warp-collective TMEM load: 16 consecutive 32-bit columns per lane into v[OFF .. OFF+15].
+template <int OFF = 0, int N = 16>
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(OFF + 16 <= N, "destination range");
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "=r"(v[OFF + 0]), "=r"(v[OFF + 1]), "=r"(v[OFF + 2]), "=r"(v[OFF + 3]), "=r"(v[OFF + 4]), "=r"(v[OFF + 5]),
+        "=r"(v[OFF + 6]), "=r"(v[OFF + 7]), "=r"(v[OFF + 8]), "=r"(v[OFF + 9]), "=r"(v[OFF + 10]),
+        "=r"(v[OFF + 11]), "=r"(v[OFF + 12]), "=r"(v[OFF + 13]), "=r"(v[OFF + 14]), "=r"(v[OFF + 15])
       : "r"(taddr)
       : "memory");
 }
