@@ -365,15 +365,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // descriptor of the stage's first K step; later K steps only move its start address
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes));
-          const bool first_k = INT4 || ks == it.ks0;
+          const uint32_t acc0 = (INT4 || ks == it.ks0) ? 0u : 1u;
+          // The MMAs of a stage go out as one branch-free sequence: a branch between
+          // two tcgen05.mma instructions roughly triples their issue cost.
+          const uint64_t atom16 = static_cast<uint64_t>((T * 128) >> 4);
+          if (NB == 2) {
+            const uint64_t lo16 = static_cast<uint64_t>((2 * T * 128) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t koff16 = static_cast<uint64_t>(((kk >> 2) * T * 128 + (kk & 3) * 32) >> 4);
-            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc,
-                       (!first_k || kk > 0) ? 1u : 0u);
-            if (NB == 2)
-              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8),
-                         bdesc0 + koff16 + static_cast<uint64_t>((2 * T * 128) >> 4), idesc, 1u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t koff16 = (kk >> 2) * atom16 + static_cast<uint64_t>((kk & 3) * 2);
+              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc, kk > 0 ? 1u : acc0);
+              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16 + lo16, idesc, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t koff16 = (kk >> 2) * atom16 + static_cast<uint64_t>((kk & 3) * 2);
+              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc, kk > 0 ? 1u : acc0);
+            }
           }
           mma_commit(smem_u32(empty + fr.idx));
           mma_commit(smem_u32(aempty + ar.idx));
