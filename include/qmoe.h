@@ -114,8 +114,7 @@ typedef struct {
  * floating-point summation order whatever the knobs say.
  *   split1, split2  split-K factor of the gate/up and down GEMMs (1..64).
  *   token_tile      largest number of token rows one GEMM work item carries
- *                   (multiple of 16, 16..128; int8 weights with f16
- *                   activations also take up to 256).  Other values give
+ *                   (multiple of 16, 16..128).  Other values give
  *                   QMOE_ERR_INVALID_ARG.
  */
 typedef struct {

@@ -64,14 +64,15 @@ def test_forward_forced_split_and_tile(qt, act, ao, split1, split2, tile):
     _check(_wl(qt, act, ao), 40, opts=q.make_options(split1, split2, tile))
 
 
-def test_int8_f16_token_tile_256():
-    # one 256-row chunk per expert: a single TMEM accumulator
-    _check(_wl("int8", "f16"), 300, opts=q.make_options(0, 0, 256))
+@pytest.mark.parametrize("qt,act", [("int8", "f16"), ("int8", "bf16")])
+def test_int8_token_tile_128_single_accumulator_per_issuer(qt, act):
+    # 128-row chunks: each MMA issuer has one TMEM accumulator, summed by the epilogue
+    _check(_wl(qt, act), 300, opts=q.make_options(0, 0, 128))
 
 
-@pytest.mark.parametrize("qt,act", [("int4", "bf16"), ("int4", "f16"), ("int8", "bf16")])
+@pytest.mark.parametrize("qt,act", [("int4", "bf16"), ("int4", "f16"), ("int8", "bf16"), ("int8", "f16")])
 def test_token_tile_above_128_rejected(qt, act):
-    # int4 keeps three fp32 tiles in TMEM; bf16 doubles the down GEMM's token tile
+    # TMEM holds three fp32 tiles of the token tile (int4) or two per MMA issuer (int8) plus A stages
     wl = _wl(qt, act)
     _, dl = _layer(wl)
     with pytest.raises(q.QmoeError) as ei:

@@ -175,14 +175,15 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     T = o->token_tile;
   }
   const bool int4 = L->qt == QMOE_INT4_GROUP;
-  if (int4 && T > 128) return QMOE_ERR_INVALID_ARG;  // running sum + two group partials must fit TMEM
+  if (T > 128) return QMOE_ERR_INVALID_ARG;  // TMEM holds three T-column tiles (int4) or two (int8) plus A stages
   p.T = T;
   if (int4) {
     p.acc_bufs = 1;
     p.a_col0 = 3 * T;
   } else {
-    p.acc_bufs = (2 * T + 2 * 64 <= 512) ? 2 : 1;
-    p.a_col0 = p.acc_bufs * T;
+    // one accumulator per MMA issuer (two), double buffered when TMEM allows
+    p.acc_bufs = (4 * T + 2 * 64 <= 512) ? 2 : 1;
+    p.a_col0 = 2 * p.acc_bufs * T;
   }
   p.a_stages = std::min(8, (512 - p.a_col0) / 64);
   if (p.a_stages < 2) return QMOE_ERR_UNSUPPORTED;

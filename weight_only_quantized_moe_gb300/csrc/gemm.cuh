@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* aempty = afull + NA;
   uint64_t* accfull = aempty + NA;
   uint64_t* accempty = accfull + 2;
-  uint64_t* drain = accempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = accempty + 2;  // one per MMA issuer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -262,10 +262,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(aempty + j), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(accfull + b), 1);
+      // int4: one commit per group partial; int8: one commit from each of the two MMA issuers per item
+      mbar_init(smem_u32(accfull + b), INT4 ? 1 : 2);
       mbar_init(smem_u32(accempty + b), 4);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(drain + 1), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -325,9 +327,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // wait for every copy still in flight into this CTA's shared memory
       for (int j = (g > NS ? g - NS : 0); j < g; ++j) mbar_wait_drain(smem_u32(full + (j % NS)), (j / NS) & 1);
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads (warps 5 and 6) issue the MMAs of even and odd stages: one
+    // thread's issue rate, with the waits and commits around each stage, is
+    // below what the tensor core accepts at small N, and the two run in parallel.
     if (lane == 0) {
+      const int id = warp - kMmaWarp;
       Ring fr, ar;
       int g = 0, itn = 0;
       bool ok = true;
@@ -336,6 +342,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         decode_item(p, nch, i, it);
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), BF16);
         int b = 0;
+        uint32_t acc_col = 0;
         if (!INT4) {
           b = (ACCB == 2) ? (itn & 1) : 0;
           const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
@@ -343,18 +350,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          acc_col = static_cast<uint32_t>((id * ACCB + b) * T);
         }
-        for (int ks = it.ks0; ks < it.ks1; ++ks) {
+        uint32_t acc_first = 0u;  // int8: the issuer's first stage of the item overwrites its accumulator
+        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, fr.next(NS), ar.next(NA)) {
+          if ((g & 1) != id) continue;
           uint32_t d_tmem;
           if (INT4) {
-            // one partial per 128-K group, double buffered
-            if (!mbar_wait(smem_u32(accempty + (g & 1)), ((g >> 1) & 1) ^ 1, abort_flag)) {
+            // one partial per 128-K group; even groups use partial 0, odd groups partial 1
+            if (!mbar_wait(smem_u32(accempty + id), ((g >> 1) & 1) ^ 1, abort_flag)) {
               ok = false;
               break;
             }
-            d_tmem = tmem + static_cast<uint32_t>(T + (g & 1) * T);
+            d_tmem = tmem + static_cast<uint32_t>(T + id * T);
           } else {
-            d_tmem = tmem + static_cast<uint32_t>(b * T);
+            d_tmem = tmem + acc_col;
           }
           if (!mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag) ||
               !mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag)) {
@@ -365,7 +375,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // descriptor of the stage's first K step; later K steps only move its start address
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes));
-          const uint32_t acc0 = (INT4 || ks == it.ks0) ? 0u : 1u;
+          const uint32_t acc0 = INT4 ? 0u : acc_first;
+          acc_first = 1u;
           // The MMAs of a stage go out as one branch-free sequence: a branch between
           // two tcgen05.mma instructions roughly triples their issue cost.
           const uint64_t atom16 = static_cast<uint64_t>((T * 128) >> 4);
@@ -386,19 +397,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           mma_commit(smem_u32(empty + fr.idx));
           mma_commit(smem_u32(aempty + ar.idx));
-          if (INT4) mma_commit(smem_u32(accfull + (g & 1)));
-          fr.next(NS);
-          ar.next(NA);
-          ++g;
+          if (INT4) mma_commit(smem_u32(accfull + id));
         }
         if (!ok) break;
+        // int8: every issuer signals the item's end, also when it had no stage of it
         if (!INT4) mma_commit(smem_u32(accfull + b));
         ++itn;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
       // all MMAs this thread issued must finish before TMEM is released
-      mma_commit(smem_u32(drain));
-      mbar_wait_drain(smem_u32(drain), 0);
+      mma_commit(smem_u32(drain + id));
+      mbar_wait_drain(smem_u32(drain + id), 0);
     }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant warpgroups
@@ -513,11 +522,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag));
         if (!ok) break;
         tc_fence_after();
+        // issuer 0 took the item's even global stages, issuer 1 the odd ones
+        const int n_st = it.ks1 - it.ks0;
+        const bool has0 = n_st >= 2 || (g & 1) == 0;
+        const bool has1 = n_st >= 2 || (g & 1) == 1;
+        g += n_st;
         const float rs = __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
-        const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(b * T);
+        const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(b * T);
+        const uint32_t t1 = tmem + lane_base + static_cast<uint32_t>((ACCB + b) * T);
         for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
+          uint32_t v[16], w[16];
+          if (has0) tmem_ld_32x32b_x16(t0 + static_cast<uint32_t>(c0), v);
+          if (has1) tmem_ld_32x32b_x16(t1 + static_cast<uint32_t>(c0), w);
           tmem_wait_ld();
           if (c0 + 16 >= it.nrows) {
             tc_fence_before();
@@ -526,7 +542,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           float f[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) f[c] = __uint_as_float(v[c]) * rs;
+          for (int c = 0; c < 16; ++c)
+            f[c] = ((has0 ? __uint_as_float(v[c]) : 0.0f) + (has1 ? __uint_as_float(w[c]) : 0.0f)) * rs;
           epilogue_store<BF16>(p, it, c0, row, lane, f);
         }
       }

@@ -15,7 +15,7 @@ constexpr int kStageK = 128;          // K elements per pipeline stage (= one in
 constexpr int kInt4StageBytes = 8448; // 128 rows x 128 K x 4 bit + 128 scales x 2 B
 constexpr int kInt8StageBytes = 16384;
 constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
-constexpr int kMaxTokenTile = 256;
+constexpr int kMaxTokenTile = 128;
 
 // Device-side status codes (values match qmoe_status).
 constexpr int kStatusTimeout = 6;
@@ -51,7 +51,7 @@ struct GemmParams {
   int32_t k_stages;
   int32_t split;
   int32_t token_tile;        // T: B rows per stage buffer, TMEM columns per accumulator
-  int32_t acc_bufs;          // int8: 1 or 2 TMEM accumulators; int4: unused (one running sum + two group partials)
+  int32_t acc_bufs;          // int8: 1 or 2 TMEM accumulators per MMA issuer; int4: unused (running sum + two group partials)
   int32_t a_col0;            // first TMEM column of the A stages
   int32_t a_stages;          // TMEM A stages (64 columns each)
   int32_t smem_stages;       // shared-memory pipeline depth
