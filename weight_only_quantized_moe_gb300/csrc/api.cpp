@@ -177,7 +177,8 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   const bool int4 = L->qt == QMOE_INT4_GROUP;
   if (T > 128) return QMOE_ERR_INVALID_ARG;  // TMEM holds three T-column tiles (int4) or two (int8) plus A stages
   p.T = T;
-  if (int4) {
+  if (int4 && L->act_dtype == QMOE_BF16) {
+    // group-scaled accumulation: running sum + two group partials
     p.acc_bufs = 1;
     p.a_col0 = 3 * T;
   } else {

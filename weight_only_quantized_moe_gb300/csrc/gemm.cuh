@@ -97,12 +97,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // of the chunk, nibble i holds K = 32c+8j+2i and nibble i+4 holds K = 32c+8j+2i+1.
 // Magic-number conversion: (nibble | 0x4300) is the bf16 value 128 + q and
 // (nibble | 0x6400) the f16 value 1024 + q, both exact; subtracting 136 (1032)
-// gives q - 8 exactly.  The group scale is not applied here: it multiplies the
-// group's fp32 partial sum (see the accumulate role), so the MMA operand is exact.
-template <bool BF16>
-__device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t (&out)[64]) {
+// gives q - 8 exactly.  With bf16 activations the group scale is not applied
+// here: it multiplies the group's fp32 partial sum (see the accumulate role), so
+// the MMA operand is exact (a bf16 (q - 8) * s would lose up to 3 bits).  With f16
+// activations the product is rounded once to f16 (11 bits) and the MMA
+// accumulates the whole K range.
+// SCALED: also multiply by the group scale (one rounding of (q - 8) * s), for
+// paths that accumulate the whole K range inside the MMA.
+template <bool BF16, bool SCALED>
+__device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[64]) {
   const uint32_t magic = BF16 ? 0x43004300u : 0x64006400u;
   const uint32_t bias_bits = BF16 ? 0x43084308u : 0x64086408u;  // 136 (bf16) / 1032 (f16)
+  const uint32_t s2bits = sbits | (sbits << 16);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
@@ -115,9 +121,11 @@ __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t 
         if (BF16) {
           __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t),
                                      *reinterpret_cast<const __nv_bfloat162*>(&bias_bits));
+          if (SCALED) v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&s2bits));
           r = *reinterpret_cast<uint32_t*>(&v);
         } else {
           __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), *reinterpret_cast<const __half2*>(&bias_bits));
+          if (SCALED) v = __hmul2(v, *reinterpret_cast<const __half2*>(&s2bits));
           r = *reinterpret_cast<uint32_t*>(&v);
         }
         out[16 * c + 4 * j + i] = r;
@@ -250,20 +258,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // group-scaled accumulation (exact int4 operands, fp32 group scales): int4 with bf16 activations
+  constexpr bool GS = INT4 && BF16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(full + s), 1);
       // 4 dequant warps + 1 MMA commit (+ 4 accumulate warps, which read the int4 group scale from the stage)
-      mbar_init(smem_u32(empty + s), INT4 ? 4 + 1 + 4 : 4 + 1);
+      mbar_init(smem_u32(empty + s), GS ? 4 + 1 + 4 : 4 + 1);
     }
     for (int j = 0; j < NA; ++j) {
       mbar_init(smem_u32(afull + j), 4);
       mbar_init(smem_u32(aempty + j), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      // int4: one commit per group partial; int8: one commit from each of the two MMA issuers per item
-      mbar_init(smem_u32(accfull + b), INT4 ? 1 : 2);
+      // group-scaled: one commit per group partial; otherwise one commit from each of the two MMA issuers per item
+      mbar_init(smem_u32(accfull + b), GS ? 1 : 2);
       mbar_init(smem_u32(accempty + b), 4);
     }
     mbar_init(smem_u32(drain), 1);
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), BF16);
         int b = 0;
         uint32_t acc_col = 0;
-        if (!INT4) {
+        if (!GS) {
           b = (ACCB == 2) ? (itn & 1) : 0;
           const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
           if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag)) {
@@ -352,11 +362,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           acc_col = static_cast<uint32_t>((id * ACCB + b) * T);
         }
-        uint32_t acc_first = 0u;  // int8: the issuer's first stage of the item overwrites its accumulator
+        uint32_t acc_first = 0u;  // the issuer's first stage of the item overwrites its accumulator
         for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, fr.next(NS), ar.next(NA)) {
           if ((g & 1) != id) continue;
           uint32_t d_tmem;
-          if (INT4) {
+          if (GS) {
             // one partial per 128-K group; even groups use partial 0, odd groups partial 1
             if (!mbar_wait(smem_u32(accempty + id), ((g >> 1) & 1) ^ 1, abort_flag)) {
               ok = false;
@@ -375,7 +385,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // descriptor of the stage's first K step; later K steps only move its start address
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes));
-          const uint32_t acc0 = INT4 ? 0u : acc_first;
+          const uint32_t acc0 = GS ? 0u : acc_first;
           acc_first = 1u;
           // The MMAs of a stage go out as one branch-free sequence: a branch between
           // two tcgen05.mma instructions roughly triples their issue cost.
@@ -397,11 +407,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           mma_commit(smem_u32(empty + fr.idx));
           mma_commit(smem_u32(aempty + ar.idx));
-          if (INT4) mma_commit(smem_u32(accfull + id));
+          if (GS) mma_commit(smem_u32(accfull + id));
         }
         if (!ok) break;
-        // int8: every issuer signals the item's end, also when it had no stage of it
-        if (!INT4) mma_commit(smem_u32(accfull + b));
+        // every issuer signals the item's end, also when it had no stage of it
+        if (!GS) mma_commit(smem_u32(accfull + b));
         ++itn;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
@@ -431,9 +441,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint4 pk[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
+          const uint32_t sbits = GS ? 0u : *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-          dequant_int4_row<BF16>(pk, out);
+          dequant_int4_row<BF16, !GS>(pk, sbits, out);
         } else {
           uint4 pk[8];
 #pragma unroll
@@ -466,7 +477,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
-      if (INT4) {
+      if (GS) {
         // running sum += scale(group, row) * partial(group), group by group
         for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, sr.next(NS)) {
           const int pb = g & 1;
@@ -527,7 +538,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const bool has0 = n_st >= 2 || (g & 1) == 0;
         const bool has1 = n_st >= 2 || (g & 1) == 1;
         g += n_st;
-        const float rs = __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
+        const float rs =
+            INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
         const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(b * T);
         const uint32_t t1 = tmem + lane_base + static_cast<uint32_t>((ACCB + b) * T);
         for (int c0 = 0; c0 < it.nrows; c0 += 16) {
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       ++itn;
     }
-    if (INT4) tmem_wait_st();  // no running-sum store may be in flight when TMEM is released
+    if (GS) tmem_wait_st();  // no running-sum store may be in flight when TMEM is released
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
   }
 
