@@ -106,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // paths that accumulate the whole K range inside the MMA.
 template <bool BF16, bool SCALED>
 __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[64]) {
-  const uint32_t magic = BF16 ? 0x43004300u : 0x64006400u;
+  const uint32_t magic = 0x43004300u;                            // bf16 128
   const uint32_t bias_bits = BF16 ? 0x43084308u : 0x64086408u;  // 136 (bf16) / 1032 (f16)
   const uint32_t s2bits = sbits | (sbits << 16);
 #pragma unroll
@@ -114,21 +114,36 @@ __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t 
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+      if constexpr (!BF16) {
+        // f16: nibbles i = 1, 3 stay in bits 4..7 of their half: (nibble << 4) | 0x6400 is
+        // 1024 + 16q, and fma(v, 1/16, -72) = q - 8 exactly; one shift per word serves i = 2, 3.
+        const uint32_t w8 = w[j] >> 8;
+        const uint32_t src[2] = {w[j], w8};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t t = ((w[j] >> (4 * i)) & 0x000F000Fu) | magic;
-        uint32_t r;
-        if (BF16) {
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t lo = (src[h] & 0x000F000Fu) | 0x64006400u;
+          const uint32_t hi = (src[h] & 0x00F000F0u) | 0x64006400u;
+          __half2 vl = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias_bits));
+          const uint32_t sixteenth = 0x2C002C00u, m72 = 0xD480D480u;  // 1/16, -72
+          __half2 vh = __hfma2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&sixteenth),
+                               *reinterpret_cast<const __half2*>(&m72));
+          if (SCALED) {
+            vl = __hmul2(vl, *reinterpret_cast<const __half2*>(&s2bits));
+            vh = __hmul2(vh, *reinterpret_cast<const __half2*>(&s2bits));
+          }
+          out[16 * c + 4 * j + 2 * h] = *reinterpret_cast<uint32_t*>(&vl);
+          out[16 * c + 4 * j + 2 * h + 1] = *reinterpret_cast<uint32_t*>(&vh);
+        }
+      } else {
+        // bf16: only 7 mantissa bits, so every nibble is shifted down to bits 0..3
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t t = ((w[j] >> (4 * i)) & 0x000F000Fu) | magic;
           __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t),
                                      *reinterpret_cast<const __nv_bfloat162*>(&bias_bits));
           if (SCALED) v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&s2bits));
-          r = *reinterpret_cast<uint32_t*>(&v);
-        } else {
-          __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), *reinterpret_cast<const __half2*>(&bias_bits));
-          if (SCALED) v = __hmul2(v, *reinterpret_cast<const __half2*>(&s2bits));
-          r = *reinterpret_cast<uint32_t*>(&v);
+          out[16 * c + 4 * j + i] = *reinterpret_cast<uint32_t*>(&v);
         }
-        out[16 * c + 4 * j + i] = r;
       }
     }
   }
