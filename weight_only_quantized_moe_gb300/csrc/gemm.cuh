@@ -21,9 +21,13 @@
 //   * the packed weights (one contiguous block per 128x128 tile, scales
 //     appended) arrive by 1-D bulk TMA; token tiles by 2-D tensor TMA with
 //     128-byte swizzle, the layout the MMA's shared-memory descriptor reads.
-//   * warp roles: 1 TMA producer thread, 1 MMA thread, two dequant
-//     warpgroups taking alternate stages, one epilogue warpgroup reading the
-//     fp32 accumulators out of TMEM; a persistent grid walks the work items.
+//   * warp roles: two TMA producer threads (warps 4, 7), two MMA-issuing
+//     threads (warps 5, 6) and two dequant warpgroups (warps 8-15), each pair
+//     taking the even and the odd pipeline stages; one epilogue warpgroup
+//     (warps 0-3) reads the fp32 accumulators out of TMEM.  Issuing a stage's
+//     copies or MMAs costs one thread several hundred cycles, so the stage
+//     rate at decode sizes needs two issuers of each.  A persistent grid walks
+//     the work items.
 //   * every mbarrier wait is bounded (see ptx.cuh); a wait that gives up
 //     records QMOE_ERR_TIMEOUT in the status word and the CTA winds down after
 //     waiting for its own copies and MMAs, then frees its TMEM.
@@ -39,6 +43,7 @@ namespace qmoe {
 
 constexpr int kGemmThreads = 512;
 constexpr int kProducerWarp = 4;
+constexpr int kProducerWarp2 = 7;
 constexpr int kMmaWarp = 5;
 constexpr int kDequantWarp0 = 8;  // warps 8..15: two warpgroups
 constexpr uint32_t kTmemCols = 512;
@@ -313,9 +318,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int n_items = nch * p.n_tiles * p.split;
   const uint32_t a_col0 = static_cast<uint32_t>(p.a_col0);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == kProducerWarp || warp == kProducerWarp2) {
+    // ------------------------------------------------------------ TMA producers
+    // Two threads (warps 4 and 7) issue the copies of even and odd stages: issuing
+    // one stage's bulk and tensor copies takes one thread several hundred cycles.
     if (lane == 0) {
+      const int id = (warp == kProducerWarp) ? 0 : 1;
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
       Ring st;
@@ -327,8 +335,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages * static_cast<int64_t>(p.stage_bytes);
         const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + static_cast<uint32_t>(NB * it.nrows) * 256u;
-        for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          if (!mbar_wait(smem_u32(empty + st.idx), st.phase ^ 1u, abort_flag)) {
+        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, st.next(NS)) {
+          if ((g & 1) != id) continue;
+          if (!mbar_wait(smem_u32(empty + st.idx), st.phase ^ 1u, abort_flag, 128)) {
             ok = false;
             break;
           }
@@ -344,13 +353,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   tma_load_2d(smem_u32(sp + (h * 2 + a) * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64,
                               h * p.b_lo_row0 + it.row0 + r, fb, pol_b);
           }
-          st.next(NS);
-          ++g;
         }
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
-      // wait for every copy still in flight into this CTA's shared memory
-      for (int j = (g > NS ? g - NS : 0); j < g; ++j) mbar_wait_drain(smem_u32(full + (j % NS)), (j / NS) & 1);
+      // wait for every copy this thread may still have in flight into the CTA's shared memory
+      // (its stages among the last NS before the first one it did not issue)
+      for (int j = (g > NS ? g - NS : 0); j < g; ++j)
+        if ((j & 1) == id) mbar_wait_drain(smem_u32(full + (j % NS)), (j / NS) & 1);
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issuers
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!GS) {
           b = (ACCB == 2) ? (itn & 1) : 0;
           const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
-          if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag)) {
+          if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
             ok = false;
             break;
           }
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t d_tmem;
           if (GS) {
             // one partial per 128-K group; even groups use partial 0, odd groups partial 1
-            if (!mbar_wait(smem_u32(accempty + id), ((g >> 1) & 1) ^ 1, abort_flag)) {
+            if (!mbar_wait(smem_u32(accempty + id), ((g >> 1) & 1) ^ 1, abort_flag, 16)) {
               ok = false;
               break;
             }
@@ -391,8 +400,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             d_tmem = tmem + acc_col;
           }
-          if (!mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag) ||
-              !mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag)) {
+          if (!mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag, 16) ||
+              !mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 16)) {
             ok = false;
             break;
           }
@@ -496,7 +505,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // running sum += scale(group, row) * partial(group), group by group
         for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, sr.next(NS)) {
           const int pb = g & 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + pb), (g >> 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + pb), (g >> 1) & 1, abort_flag, 32));
           if (!ok) break;
           tc_fence_after();
           // the group's MMAs are done but its stage is still held for us: take the scale, release the stage
@@ -545,7 +554,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         const int b = (ACCB == 2) ? (itn & 1) : 0;
         const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
         if (!ok) break;
         tc_fence_after();
         // issuer 0 took the item's even global stages, issuer 1 the odd ones

@@ -82,14 +82,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Returns false if
 // the CTA abort flag was raised or the time limit passed (the caller then
-// raises the abort flag itself and winds down).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+// raises the abort flag itself and winds down).  Between polls the warp sleeps
+// with exponential backoff up to `max_sleep_ns`, so waiting warps leave the
+// issue slots to working ones; callers on the critical path pass a small cap.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint32_t max_sleep_ns = 64) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (true) {
+  uint32_t sleep_ns = 8;
+  for (uint32_t it = 1;; ++it) {
+    if (max_sleep_ns != 0) {
+      __nanosleep(sleep_ns);
+      sleep_ns = sleep_ns * 2 < max_sleep_ns ? sleep_ns * 2 : max_sleep_ns;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 31) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 
