@@ -37,7 +37,7 @@ METRIC = "quant-MoE layer tokens/s, TFLOP/s & weight GB/s vs roofline, M=1..8192
 DEFAULT_WORKLOAD = "mixtral8x7b_w4"
 DEFAULT_M = 16
 L2_BYTES = 129 * 1024 * 1024
-LAUNCH_NAMES = ["moe_align", "gather", "gemm_gate_up", "silu_reduce", "gemm_down", "out_reduce"]
+LAUNCH_NAMES = ["moe_align", "gather", "gemm_gate_up", "silu_reduce", "inter_rescale", "gemm_down", "out_reduce"]
 
 
 def parse():
@@ -237,7 +237,7 @@ def run_gpu(args, rank, world):
         res = {"M": M, "ms": ms, "clocks": clk.summary(), "inp": inp}
         if profile:
             # second pass over the same K steps with CUDA events around each kernel launch
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(steps)]
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(LAUNCH_NAMES))] for _ in range(steps)]
             launches = 0
             for i in range(steps):
                 launches += q.qmoe_forward_profiled(copies[i % len(copies)], x, ids, w, out, ws, evs[i])

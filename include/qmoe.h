@@ -233,9 +233,10 @@ qmoe_status qmoe_forward_ex(const qmoe_layer* layer, const void* x, int64_t M,
 /*
  * qmoe_forward_ex with CUDA events recorded around each kernel launch, for
  * measuring per-kernel device time inside a timed region.  `events` holds
- * n_events (>= 12) cudaEvent_t handles created by the caller; for launch i
+ * n_events (>= 14) cudaEvent_t handles created by the caller; for launch i
  * (0 moe_align, 1 token gather, 2 gate/up GEMM, 3 split-K SiLU reduce,
- * 4 down GEMM, 5 output reduce) event 2i is recorded on `stream` just before
+ * 4 intermediate rescale, 5 down GEMM, 6 output reduce) event 2i is recorded
+ * on `stream` just before
  * it and event 2i+1 just after.  A launch the plan skips (3 when the gate/up
  * GEMM is not split) gets both events at the same point.  *n_launches
  * (optional) receives the number of kernels launched.  Null events give

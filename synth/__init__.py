@@ -17,6 +17,7 @@ from .gen import (  # noqa: F401
     make_inputs,
     quantize_int4_rtn,
     quantize_int8_rtn,
+    round_to,
     round_to_bf16,
     route_topk,
     round_to_f16,

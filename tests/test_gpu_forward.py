@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import weight_only_quantized_moe_gb300 as q
-from synth import Inputs, Workload, make_inputs, make_layer
+from synth import Inputs, Workload, make_inputs, make_layer, round_to
 from tests.gpu_util import assert_parity, device_inputs, device_layer, ensure_built, run_forward
 
 pytestmark = pytest.mark.gpu
@@ -72,12 +72,40 @@ def test_int8_token_tile_128_single_accumulator_per_issuer(qt, act):
 
 @pytest.mark.parametrize("qt,act", [("int4", "bf16"), ("int4", "f16"), ("int8", "bf16"), ("int8", "f16")])
 def test_token_tile_above_128_rejected(qt, act):
-    # TMEM holds three fp32 tiles of the token tile (int4) or two per MMA issuer (int8) plus A stages
+    # TMEM (512 columns) holds one fp32 accumulator of the token tile per MMA issuer plus the A stages
     wl = _wl(qt, act)
     _, dl = _layer(wl)
     with pytest.raises(q.QmoeError) as ei:
         q.qmoe_workspace_size(dl, 40, 2, q.make_options(0, 0, 256))
     assert ei.value.status == q.QMOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("qt,act,ao,exps,spread", [("int4", "bf16", False, (24, -24), 8),
+                                                    ("int4", "bf16", True, (16, -20), 8),
+                                                    ("int8", "bf16", False, (30, -30), 8),
+                                                    ("int4", "f16", False, (0,), 4),
+                                                    ("int8", "f16", False, (-2,), 4)])
+def test_activation_magnitudes(qt, act, ao, exps, spread):
+    """Both GEMMs run in f16 on rows scaled by powers of two: bf16 inputs far
+    outside f16's range, and rows of very different magnitude, keep the bar per
+    row.  (f16 layers stay where their f16 output is representable.)"""
+    wl = _wl(qt, act, ao)
+    L, dl = _layer(wl)
+    M = 48
+    base = make_inputs(wl, M, seed=31)
+    rng = np.random.default_rng(7)
+    for ex in exps:
+        # every row scaled by 2^ex and rows spread over a further 2^-spread .. 2^spread
+        row_e = ex + rng.integers(-spread, spread + 1, size=(M, 1))
+        x = round_to(np.ldexp(base.x.astype(np.float64), row_e), act).astype(np.float32)
+        inp = Inputs(x, base.topk_ids, base.topk_weights, base.logits)
+        xd, ids, w = device_inputs(wl, inp)
+        out, _ = run_forward(dl, xd, ids, w)
+        got = out.float().cpu().numpy()
+        ref = oracle.moe_forward(L, inp.x, inp.topk_ids, inp.topk_weights)
+        assert np.isfinite(got).all()
+        for m in range(M):
+            assert_parity(got[m:m + 1], ref[m:m + 1], f"{wl.name} 2^{ex} row {m}")
 
 
 def test_multi_chunk_expert_and_empty_experts():

@@ -216,7 +216,7 @@ def qmoe_forward(layer: DeviceLayer, x: torch.Tensor, topk_ids: torch.Tensor, to
 
 def qmoe_forward_profiled(layer: DeviceLayer, x, topk_ids, topk_weights, out, workspace, events, opts=None,
                           stream=None) -> int:
-    """qmoe_forward_ex with the 12 torch.cuda.Event objects recorded around its six launch slots
+    """qmoe_forward_ex with the 14 torch.cuda.Event objects recorded around its seven launch slots
     (see include/qmoe.h).  Returns the number of kernels launched."""
     from ctypes import c_int32 as _i32
     M = x.shape[0]

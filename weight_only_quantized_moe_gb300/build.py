@@ -29,8 +29,7 @@ SOURCES = [
     "gemm_dispatch.cu",
     "gemm_i4_f16.cu",
     "gemm_i4_bf16.cu",
-    "gemm_i8_f16.cu",
-    "gemm_i8_bf16.cu",
+    "gemm_i8.cu",
     "noalloc.cu",
 ]
 

@@ -77,12 +77,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Row-major [rows, K] 16-bit matrix, boxes of 64 elements (128 B) x 16 rows, 128-byte swizzle.
-bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K) {
+// A [rows, K] 16-bit row-major matrix; one copy of box {64, box_rows} fetches
+// 64 K of box_rows rows as [row][128 B] (128-byte swizzled).
+bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
   auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {K, rows};
   cuuint64_t strides[1] = {K * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -127,12 +129,12 @@ qmoe_status validate_layer_dims(const qmoe_layer* L) {
 struct Plan {
   int64_t M = 0, P = 0;
   int k = 0;
-  int T = 0, acc_bufs = 0, a_col0 = 0, a_stages = 0, ns1 = 0, ns2 = 0, stage_bytes = 0, b_terms2 = 1;
+  int T = 0, acc_bufs = 0, a_col0 = 0, a_stages = 0, ns = 0, stage_bytes = 0;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
-  size_t off_status = 0, off_sorted = 0, off_expert = 0, off_scalars = 0, off_chunks = 0, off_xg = 0, off_inter = 0,
-         off_h = 0, off_y = 0, total = 0;
+  size_t off_status = 0, off_sorted = 0, off_expert = 0, off_scalars = 0, off_chunks = 0, off_xg = 0, off_xscale = 0,
+         off_inter32 = 0, off_inter16 = 0, off_iscale = 0, off_h = 0, off_y = 0, total = 0;
 };
 
 // Makespan of n equal work items split s ways over C persistent CTAs, in
@@ -175,27 +177,15 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     T = o->token_tile;
   }
   const bool int4 = L->qt == QMOE_INT4_GROUP;
-  if (T > 128) return QMOE_ERR_INVALID_ARG;  // TMEM holds three T-column tiles (int4) or two (int8) plus A stages
   p.T = T;
-  if (int4 && L->act_dtype == QMOE_BF16) {
-    // group-scaled accumulation: running sum + two group partials
-    p.acc_bufs = 1;
-    p.a_col0 = 3 * T;
-  } else {
-    // one accumulator per MMA issuer (two), double buffered when TMEM allows
-    p.acc_bufs = (4 * T + 2 * 64 <= 512) ? 2 : 1;
-    p.a_col0 = 2 * p.acc_bufs * T;
-  }
+  // TMEM (512 columns): one fp32 accumulator of T columns per MMA issuer (two),
+  // double buffered when that leaves room for two 64-column A stages
+  p.acc_bufs = (4 * T + 2 * 64 <= 512) ? 2 : 1;
+  p.a_col0 = 2 * p.acc_bufs * T;
   p.a_stages = std::min(8, (512 - p.a_col0) / 64);
-  if (p.a_stages < 2) return QMOE_ERR_UNSUPPORTED;
   p.stage_bytes = int4 ? kInt4StageBytes : kInt8StageBytes;
-  // bf16: the intermediate is kept as two bf16 terms (hi + rounding residual)
-  p.b_terms2 = (L->act_dtype == QMOE_BF16) ? 2 : 1;
   const size_t wreg = (p.stage_bytes + 1023) & ~1023;
-  p.ns1 = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(T) * 256 + wreg)));
-  p.ns2 = static_cast<int>(
-      std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(p.b_terms2) * T * 256 + wreg)));
-  if (p.ns1 < 2 || p.ns2 < 2) return QMOE_ERR_INVALID_ARG;  // only a forced token tile gets here
+  p.ns = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(T) * 256 + wreg)));
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
@@ -223,7 +213,10 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.off_scalars = off;  off += 256;  // num_post_padded, n_chunks
   p.off_chunks = off;   off += al256(p.max_chunks * sizeof(Chunk));
   p.off_xg = off;       off += al256(static_cast<size_t>(p.cap) * L->H * 2);
-  p.off_inter = off;    off += al256(static_cast<size_t>(p.b_terms2) * p.cap * L->I * 2);
+  p.off_xscale = off;   off += al256(static_cast<size_t>(p.cap) * 4);
+  p.off_inter32 = off;  off += al256(static_cast<size_t>(p.cap) * L->I * 4);
+  p.off_inter16 = off;  off += al256(static_cast<size_t>(p.cap) * L->I * 2);
+  p.off_iscale = off;   off += al256(static_cast<size_t>(p.cap) * 4);
   p.off_h = off;        off += (p.S1 > 1) ? al256(static_cast<size_t>(p.S1) * p.cap * 2 * L->I * 4) : 0;
   p.off_y = off;        off += al256(static_cast<size_t>(p.S2) * P * L->H * 4);
   p.total = off;
@@ -269,15 +262,17 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   int32_t* nch = npp + 1;
   Chunk* chunks = reinterpret_cast<Chunk*>(base + pl.off_chunks);
   void* xg = base + pl.off_xg;
-  void* inter = base + pl.off_inter;
+  float* xscale = reinterpret_cast<float*>(base + pl.off_xscale);
+  float* inter32 = reinterpret_cast<float*>(base + pl.off_inter32);
+  void* inter16 = base + pl.off_inter16;
+  float* iscale = reinterpret_cast<float*>(base + pl.off_iscale);
   float* h = reinterpret_cast<float*>(base + pl.off_h);
   float* y = reinterpret_cast<float*>(base + pl.off_y);
   const bool bf16 = L->act_dtype == QMOE_BF16;
   const int P = static_cast<int>(pl.P);
 
   CUtensorMap map_xg, map_inter;
-  if (!encode_rows_map(&map_xg, xg, pl.cap, L->H) ||
-      !encode_rows_map(&map_inter, inter, static_cast<uint64_t>(pl.b_terms2) * pl.cap, L->I))
+  if (!encode_rows_map(&map_xg, xg, pl.cap, L->H, pl.T) || !encode_rows_map(&map_inter, inter16, pl.cap, L->I, pl.T))
     return QMOE_ERR_CUDA;
 
   // events (profiling only): 2i before and 2i+1 after launch i
@@ -292,13 +287,15 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   launched += (err == cudaSuccess);
   rec(2);
   if (err == cudaSuccess) {
-    err = launch_gather(x, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, sms, stream);
+    err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, sms,
+                        stream);
     launched += (err == cudaSuccess);
   }
   rec(3);
   GemmParams g1{};
   g1.w = static_cast<const uint8_t*>(L->w13);
   g1.row_scale = int4 ? nullptr : L->s13;
+  g1.col_scale = xscale;
   g1.chunks = chunks;
   g1.n_chunks = nch;
   g1.sorted_ids = sorted;
@@ -311,10 +308,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.acc_bufs = pl.acc_bufs;
   g1.a_col0 = pl.a_col0;
   g1.a_stages = pl.a_stages;
-  g1.smem_stages = pl.ns1;
-  g1.b_terms = 1;
-  g1.b_lo_row0 = 0;
-  g1.inter_lo_offset = (pl.b_terms2 == 2) ? pl.cap * static_cast<int64_t>(L->I) : 0;
+  g1.smem_stages = pl.ns;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -322,7 +316,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.inter_ld = L->I;
   if (pl.S1 == 1) {
     g1.epi_mode = kEpiSiluToAct;
-    g1.out = inter;
+    g1.out = inter32;
     g1.out_ld = L->I;
     g1.out_split_stride = 0;
   } else {
@@ -334,14 +328,11 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   GemmParams g2 = g1;
   g2.w = static_cast<const uint8_t*>(L->w2);
   g2.row_scale = int4 ? nullptr : L->s2;
+  g2.col_scale = iscale;
   g2.n_tiles = pl.n_tiles2;
   g2.k_stages = pl.kst2;
   g2.split = pl.S2;
   g2.epi_mode = kEpiWeightedPairs;
-  g2.smem_stages = pl.ns2;
-  g2.b_terms = pl.b_terms2;
-  g2.b_lo_row0 = static_cast<int32_t>(pl.cap);
-  g2.inter_lo_offset = 0;
   g2.fault_injection = 0;
   g2.out = y;
   g2.out_ld = L->H;
@@ -353,28 +344,34 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
-    err = launch_gemm(int4, bf16, &map_xg, g1, grid1, stream);
+    err = launch_gemm(int4, bf16, &map_xg, g1, grid1, stream);  // int4 scales have the activation dtype
     launched += (err == cudaSuccess);
   }
   rec(5);
   rec(6);
   if (err == cudaSuccess && pl.S1 > 1) {
-    err = launch_silu_reduce(h, npp, pl.S1, pl.cap, L->I, bf16, inter, g1.inter_lo_offset, sms, stream);
+    err = launch_silu_reduce(h, npp, pl.S1, pl.cap, L->I, inter32, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(7);
   rec(8);
   if (err == cudaSuccess) {
-    err = launch_gemm(int4, bf16, &map_inter, g2, grid2, stream);
+    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(9);
   rec(10);
   if (err == cudaSuccess) {
-    err = launch_out_reduce(y, pl.S2, M, k, L->H, bf16, out, sms, stream);
+    err = launch_gemm(int4, bf16, &map_inter, g2, grid2, stream);
     launched += (err == cudaSuccess);
   }
   rec(11);
+  rec(12);
+  if (err == cudaSuccess) {
+    err = launch_out_reduce(y, pl.S2, M, k, L->H, bf16, out, sms, stream);
+    launched += (err == cudaSuccess);
+  }
+  rec(13);
   if (n_launches != nullptr) *n_launches = launched;
   return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
@@ -688,8 +685,8 @@ qmoe_status qmoe_forward_profiled(const qmoe_layer* layer, const void* x, int64_
                                   const float* topk_weights, int32_t top_k, void* out, void* workspace,
                                   size_t workspace_bytes, void* stream, const qmoe_options* opts,
                                   void* const* events, int32_t n_events, int32_t* n_launches) {
-  if (events == nullptr || n_events < 12) return QMOE_ERR_INVALID_ARG;
-  for (int i = 0; i < 12; ++i)
+  if (events == nullptr || n_events < 14) return QMOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 14; ++i)
     if (events[i] == nullptr) return QMOE_ERR_INVALID_ARG;
   if (n_launches != nullptr) *n_launches = 0;
   return forward_impl(layer, x, M, topk_ids, topk_weights, top_k, out, workspace, workspace_bytes,

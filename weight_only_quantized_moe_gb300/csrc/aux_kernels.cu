@@ -2,6 +2,7 @@
 //   moe_align_block_size  (group token-expert pairs by expert, pad to the block)
 //   token gather          (sorted, padded, act-order-permuted activation rows)
 //   split-K SiLU reduce   (sum gate/up partials, apply SiLU(gate)*up)
+//   intermediate rescale  (fp32 intermediate -> per-row scaled f16 for the down GEMM)
 //   output reduce         (sum the top-k weighted expert outputs per token)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -164,18 +165,56 @@ cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
 }
 
 // ---------------------------------------------------------------------------
-// Token gather: xg[row, :] = x[sorted_ids[row] / top_k, perm13_e] (zeros for
-// padding rows).  Rows are the B operand of the gate/up GEMM; with act-order
-// the hidden channels are put in each expert's sorted-group order so the GEMM
-// walks K in whole quantization groups.
+// Per-row power-of-two scaling into f16.
+//
+// Both GEMMs multiply in f16 (11-bit significand) whatever the activation type:
+// a bf16 row (8-bit significand) times a power of two is exact in f16 as long as
+// it stays in f16's normal range, so each row r is stored as v * 2^-e_r with
+// e_r = floor(log2 max|v|) - 14 (the row's largest magnitude lands in
+// [2^14, 2^15)) and 2^e_r is kept beside it; the GEMM epilogue multiplies the
+// fp32 accumulator column back by 2^e_r.  Elements below 2^-28 of the row's
+// largest lose significand bits, which does not move a dot product.
+// ---------------------------------------------------------------------------
+// Returns (2^e, 2^-e) for a row whose largest magnitude is amax.
+__device__ __forceinline__ float2 row_exponent_scale(float amax) {
+  if (!(amax > 0.0f) || !(amax <= 3.4028235e38f)) return make_float2(1.0f, 1.0f);  // zero, inf or NaN
+  int e = ((__float_as_int(amax) >> 23) & 0xFF) - 127 - 14;
+  e = max(-100, min(100, e));
+  // both powers of two built from their exponent fields
+  return make_float2(__int_as_float((127 + e) << 23), __int_as_float((127 - e) << 23));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float act_to_float(uint16_t b) {
+  if (BF16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  return __half2float(*reinterpret_cast<const __half*>(&b));
+}
+
+__device__ __forceinline__ uint16_t f16_bits(float v) {
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+// ---------------------------------------------------------------------------
+// Token gather: xg[row, :] = x[sorted_ids[row] / top_k, perm13_e] * 2^-e_row in
+// f16, xscale[row] = 2^e_row (zeros and 1 for padding rows).  Rows are the B
+// operand of the gate/up GEMM; with act-order the hidden channels are put in
+// each expert's sorted-group order so the GEMM walks K in whole quantization
+// groups.
 // ---------------------------------------------------------------------------
 constexpr int kGatherThreads = 256;
 
+template <bool BF16>
 __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                   const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_post_padded,
                   const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B,
-                  uint16_t* __restrict__ xg) {
+                  uint16_t* __restrict__ xg, float* __restrict__ xscale) {
   pdl_launch_dependents();
   pdl_wait();
   const int total = *num_post_padded;
@@ -187,44 +226,66 @@ __global__ void __launch_bounds__(kGatherThreads)
     if (p >= P) {
       uint4* d4 = reinterpret_cast<uint4*>(dst);
       for (int i = lane; i < H / 8; i += 32) d4[i] = make_uint4(0, 0, 0, 0);
+      if (lane == 0) xscale[row] = 1.0f;
       continue;
     }
     const uint16_t* src = x + static_cast<int64_t>(p / top_k) * H;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    float amax = 0.0f;
+    for (int i = lane; i < H / 8; i += 32) {
+      const uint4 v = __ldg(s4 + i);
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(act_to_float<BF16>(e[k])));
+    }
+    amax = warp_max(amax);
+    const float2 sc = row_exponent_scale(amax);
+    const float inv = sc.y;
+    if (lane == 0) xscale[row] = sc.x;
     if (perm13 == nullptr) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
-      for (int i = lane; i < H / 8; i += 32) d4[i] = __ldg(s4 + i);
+      for (int i = lane; i < H / 8; i += 32) {
+        const uint4 v = __ldg(s4 + i);
+        const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+        uint4 o;
+        uint16_t* oe = reinterpret_cast<uint16_t*>(&o);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) oe[k] = f16_bits(act_to_float<BF16>(e[k]) * inv);
+        d4[i] = o;
+      }
     } else {
       const int32_t* pr = perm13 + static_cast<int64_t>(expert_ids[row / B]) * H;
       uint32_t* d2 = reinterpret_cast<uint32_t*>(dst);
       for (int i = lane; i < H / 2; i += 32) {
         const int2 k2 = __ldg(reinterpret_cast<const int2*>(pr) + i);
-        d2[i] = static_cast<uint32_t>(__ldg(src + k2.x)) | (static_cast<uint32_t>(__ldg(src + k2.y)) << 16);
+        d2[i] = static_cast<uint32_t>(f16_bits(act_to_float<BF16>(__ldg(src + k2.x)) * inv)) |
+                (static_cast<uint32_t>(f16_bits(act_to_float<BF16>(__ldg(src + k2.y)) * inv)) << 16);
       }
     }
   }
 }
 
-cudaError_t launch_gather(const void* x, const int32_t* sorted_ids, const int32_t* expert_ids,
+cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, void* xg, int num_sms, cudaStream_t stream) {
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
+                          cudaStream_t stream) {
   const int64_t want = (cap_rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
-  return launch_kernel(gather_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, true,
-                       static_cast<const uint16_t*>(x), sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H,
-                       block, static_cast<uint16_t*>(xg));
+  auto kern = bf16 ? gather_kernel<true> : gather_kernel<false>;
+  return launch_kernel(kern, dim3(grid), dim3(kGatherThreads), 0, stream, true, static_cast<const uint16_t*>(x),
+                       sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block,
+                       static_cast<uint16_t*>(xg), xscale);
 }
 
 // ---------------------------------------------------------------------------
-// Split-K gate/up reduce: inter[row, j] = SiLU(sum_s h[s, row, 2j]) * sum_s h[s, row, 2j+1]
+// Split-K gate/up reduce: inter32[row, j] = SiLU(sum_s h[s, row, 2j]) * sum_s h[s, row, 2j+1]
 // (the packed gate/up GEMM interleaves gate and up rows, so h is [.., g0, u0, g1, u1, ..]).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <bool BF16>
 __global__ void __launch_bounds__(256)
     silu_reduce_kernel(const float* __restrict__ h, const int32_t* __restrict__ num_post_padded, int32_t split,
-                       int64_t cap_rows, int32_t I, uint16_t* __restrict__ inter, int64_t lo_offset) {
+                       int64_t cap_rows, int32_t I, float* __restrict__ inter32) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t total = static_cast<int64_t>(*num_post_padded) * (I / 2);  // two j per thread
@@ -238,33 +299,72 @@ __global__ void __launch_bounds__(256)
       const float4 v = __ldg(reinterpret_cast<const float4*>(h + s * slab + base));
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    const float r0 = silu_f(acc.x) * acc.y;
-    const float r1 = silu_f(acc.z) * acc.w;
-    uint32_t packed, packed_lo = 0;
-    if (BF16) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
-      packed = *reinterpret_cast<uint32_t*>(&b);
-      // second bf16 term carries the rounding residual of the first
-      __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __bfloat162float(b.x), r1 - __bfloat162float(b.y));
-      packed_lo = *reinterpret_cast<uint32_t*>(&l);
-    } else {
-      __half2 b = __floats2half2_rn(r0, r1);
-      packed = *reinterpret_cast<uint32_t*>(&b);
-    }
-    reinterpret_cast<uint32_t*>(inter + row * I)[j2] = packed;
-    if (lo_offset != 0) reinterpret_cast<uint32_t*>(inter + lo_offset + row * I)[j2] = packed_lo;
+    reinterpret_cast<float2*>(inter32 + row * I)[j2] = make_float2(silu_f(acc.x) * acc.y, silu_f(acc.z) * acc.w);
   }
 }
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
-                               int32_t I, bool bf16, void* inter, int64_t inter_lo_offset, int num_sms,
-                               cudaStream_t stream) {
-  const int grid = 4 * num_sms;
-  if (bf16)
-    return launch_kernel(silu_reduce_kernel<true>, dim3(grid), dim3(256), 0, stream, true, h, num_post_padded, split,
-                         cap_rows, I, static_cast<uint16_t*>(inter), inter_lo_offset);
-  return launch_kernel(silu_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, h, num_post_padded, split,
-                       cap_rows, I, static_cast<uint16_t*>(inter), int64_t(0));
+                               int32_t I, float* inter32, int num_sms, cudaStream_t stream) {
+  return launch_kernel(silu_reduce_kernel, dim3(4 * num_sms), dim3(256), 0, stream, true, h, num_post_padded, split,
+                       cap_rows, I, inter32);
+}
+
+// ---------------------------------------------------------------------------
+// Intermediate rescale: inter16[row, :] = inter32[row, :] * 2^-e_row in f16 and
+// iscale[row] = 2^e_row (the down GEMM's B operand and its column scale).  One
+// CTA per row (the absmax is a block reduction); padding rows get zeros and
+// scale 1 without reading inter32.
+// ---------------------------------------------------------------------------
+constexpr int kRescaleThreads = 256;
+
+__global__ void __launch_bounds__(kRescaleThreads)
+    inter_rescale_kernel(const float* __restrict__ inter32, const int32_t* __restrict__ num_post_padded,
+                         const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I,
+                         uint16_t* __restrict__ inter16, float* __restrict__ iscale) {
+  __shared__ float red[kRescaleThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int total = *num_post_padded;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int row = blockIdx.x; row < total; row += gridDim.x) {
+    if (sorted_ids[row] >= P) {  // uniform across the CTA
+      uint4* d4 = reinterpret_cast<uint4*>(inter16 + static_cast<int64_t>(row) * I);
+      for (int i = threadIdx.x; i < I / 8; i += kRescaleThreads) d4[i] = make_uint4(0, 0, 0, 0);
+      if (threadIdx.x == 0) iscale[row] = 1.0f;
+      continue;
+    }
+    const float4* s4 = reinterpret_cast<const float4*>(inter32 + static_cast<int64_t>(row) * I);
+    float amax = 0.0f;
+    for (int i = threadIdx.x; i < I / 4; i += kRescaleThreads) {
+      const float4 v = __ldg(s4 + i);
+      amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kRescaleThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    __syncthreads();  // red is reused by the next row
+    const float2 sc = row_exponent_scale(amax);
+    if (threadIdx.x == 0) iscale[row] = sc.x;
+    uint2* d2 = reinterpret_cast<uint2*>(inter16 + static_cast<int64_t>(row) * I);
+    for (int i = threadIdx.x; i < I / 4; i += kRescaleThreads) {
+      const float4 v = __ldg(s4 + i);
+      uint2 o;
+      o.x = static_cast<uint32_t>(f16_bits(v.x * sc.y)) | (static_cast<uint32_t>(f16_bits(v.y * sc.y)) << 16);
+      o.y = static_cast<uint32_t>(f16_bits(v.z * sc.y)) | (static_cast<uint32_t>(f16_bits(v.w * sc.y)) << 16);
+      d2[i] = o;
+    }
+  }
+}
+
+cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
+                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
+                                 cudaStream_t stream) {
+  const int grid = static_cast<int>(cap_rows < 8LL * num_sms ? (cap_rows > 0 ? cap_rows : 1) : 8LL * num_sms);
+  return launch_kernel(inter_rescale_kernel, dim3(grid), dim3(kRescaleThreads), 0, stream, true, inter32,
+                       num_post_padded, sorted_ids, P, I, static_cast<uint16_t*>(inter16), iscale);
 }
 
 // ---------------------------------------------------------------------------

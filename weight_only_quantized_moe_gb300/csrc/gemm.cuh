@@ -10,17 +10,25 @@
 // the intermediate (down GEMM).  The epilogue then applies SiLU(gate)*up, or
 // the routing weight, per the mode.
 //
+// Numerics: both operands are f16 whatever the activation type.  B rows are
+// stored scaled by a power of two per row (exact, see aux_kernels.cu) and the
+// epilogue multiplies each accumulator column back; int4 weights (q - 8) * s
+// are exact in f16 when s is a bf16 scale (3 + 8 significant bits) and rounded
+// once when s is an f16 scale; int8 codes are exact and their per-row scale is
+// applied to the fp32 accumulator.
+//
 // Design for GB300 (prior-art Marlin/Triton kernels staged both operands in
 // shared memory; here only the tokens are):
 //   * swap-AB: the 128 weight rows are the MMA's M; the chunk's token rows
-//     (16..256) are N, so tiny decode batches waste no tensor work.
+//     (16..128) are N, so tiny decode batches waste no tensor work.
 //   * the dequantized weight tile goes registers -> TMEM (tcgen05.st) and is
 //     the MMA's A operand straight from tensor memory; dequantized weights
 //     never touch shared memory, which carries only the packed bytes and the
 //     token tile.
 //   * the packed weights (one contiguous block per 128x128 tile, scales
-//     appended) arrive by 1-D bulk TMA; token tiles by 2-D tensor TMA with
-//     128-byte swizzle, the layout the MMA's shared-memory descriptor reads.
+//     appended) arrive by 1-D bulk TMA; a stage's token tile by two 2-D tensor
+//     TMA copies with 128-byte swizzle, the layout the MMA's shared-memory
+//     descriptor reads.
 //   * warp roles: two TMA producer threads (warps 4, 7), two MMA-issuing
 //     threads (warps 5, 6) and two dequant warpgroups (warps 8-15), each pair
 //     taking the even and the odd pipeline stages; one epilogue warpgroup
@@ -96,59 +104,44 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 
 // ---------------------------------------------------------------------------
 // Dequantization of one 128-K stage of one weight row into 64 TMEM columns
-// (column c holds K elements 2c (low half) and 2c+1 (high half)).
+// (column c holds K elements 2c (low half) and 2c+1 (high half)), as f16.
 // ---------------------------------------------------------------------------
 // int4: packed chunk c (16 bytes) of the row holds K = 32c .. 32c+31; in word j
 // of the chunk, nibble i holds K = 32c+8j+2i and nibble i+4 holds K = 32c+8j+2i+1.
-// Magic-number conversion: (nibble | 0x4300) is the bf16 value 128 + q and
-// (nibble | 0x6400) the f16 value 1024 + q, both exact; subtracting 136 (1032)
-// gives q - 8 exactly.  With bf16 activations the group scale is not applied
-// here: it multiplies the group's fp32 partial sum (see the accumulate role), so
-// the MMA operand is exact (a bf16 (q - 8) * s would lose up to 3 bits).  With f16
-// activations the product is rounded once to f16 (11 bits) and the MMA
-// accumulates the whole K range.
-// SCALED: also multiply by the group scale (one rounding of (q - 8) * s), for
-// paths that accumulate the whole K range inside the MMA.
-template <bool BF16, bool SCALED>
+// Magic-number conversion: (nibble | 0x6400) is the f16 value 1024 + q, exact,
+// and subtracting 1032 gives q - 8 exactly; nibbles i = 1, 3 stay in bits 4..7
+// of their half, where (nibble << 4) | 0x6400 is 1024 + 16q and
+// fma(v, 1/16, -72) = q - 8 exactly, so one shift per word serves i = 2, 3.
+// One multiply by the group scale rounds once (exact for bf16 scales).
+template <bool BF16S>
 __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[64]) {
-  const uint32_t magic = 0x43004300u;                            // bf16 128
-  const uint32_t bias_bits = BF16 ? 0x43084308u : 0x64086408u;  // 136 (bf16) / 1032 (f16)
-  const uint32_t s2bits = sbits | (sbits << 16);
+  const uint32_t bias_bits = 0x64086408u;                        // 1032
+  const uint32_t sixteenth = 0x2C002C00u, m72 = 0xD480D480u;     // 1/16, -72
+  uint16_t s16;
+  if (BF16S) {
+    const __half h = __float2half_rn(__uint_as_float(sbits << 16));
+    s16 = *reinterpret_cast<const uint16_t*>(&h);
+  } else {
+    s16 = static_cast<uint16_t>(sbits);
+  }
+  const uint32_t s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      if constexpr (!BF16) {
-        // f16: nibbles i = 1, 3 stay in bits 4..7 of their half: (nibble << 4) | 0x6400 is
-        // 1024 + 16q, and fma(v, 1/16, -72) = q - 8 exactly; one shift per word serves i = 2, 3.
-        const uint32_t w8 = w[j] >> 8;
-        const uint32_t src[2] = {w[j], w8};
+      const uint32_t src[2] = {w[j], w[j] >> 8};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t lo = (src[h] & 0x000F000Fu) | 0x64006400u;
-          const uint32_t hi = (src[h] & 0x00F000F0u) | 0x64006400u;
-          __half2 vl = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias_bits));
-          const uint32_t sixteenth = 0x2C002C00u, m72 = 0xD480D480u;  // 1/16, -72
-          __half2 vh = __hfma2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&sixteenth),
-                               *reinterpret_cast<const __half2*>(&m72));
-          if (SCALED) {
-            vl = __hmul2(vl, *reinterpret_cast<const __half2*>(&s2bits));
-            vh = __hmul2(vh, *reinterpret_cast<const __half2*>(&s2bits));
-          }
-          out[16 * c + 4 * j + 2 * h] = *reinterpret_cast<uint32_t*>(&vl);
-          out[16 * c + 4 * j + 2 * h + 1] = *reinterpret_cast<uint32_t*>(&vh);
-        }
-      } else {
-        // bf16: only 7 mantissa bits, so every nibble is shifted down to bits 0..3
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t t = ((w[j] >> (4 * i)) & 0x000F000Fu) | magic;
-          __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t),
-                                     *reinterpret_cast<const __nv_bfloat162*>(&bias_bits));
-          if (SCALED) v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&s2bits));
-          out[16 * c + 4 * j + i] = *reinterpret_cast<uint32_t*>(&v);
-        }
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t lo = (src[h] & 0x000F000Fu) | 0x64006400u;
+        const uint32_t hi = (src[h] & 0x00F000F0u) | 0x64006400u;
+        __half2 vl = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias_bits));
+        __half2 vh = __hfma2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&sixteenth),
+                             *reinterpret_cast<const __half2*>(&m72));
+        vl = __hmul2(vl, *reinterpret_cast<const __half2*>(&s2bits));
+        vh = __hmul2(vh, *reinterpret_cast<const __half2*>(&s2bits));
+        out[16 * c + 4 * j + 2 * h] = *reinterpret_cast<uint32_t*>(&vl);
+        out[16 * c + 4 * j + 2 * h + 1] = *reinterpret_cast<uint32_t*>(&vh);
       }
     }
   }
@@ -156,68 +149,38 @@ __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t 
 
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
 // per-row scale is applied to the fp32 accumulator in the epilogue, so the
-// conversion is exact: f16 via (0x64 << 8 | (q + 128)) - 1152; bf16 via the
-// float32 pattern 0x4B0000uu - (2^23 + 128) and a pack to bf16x2.
-template <bool BF16>
+// conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.
 __device__ __forceinline__ void dequant_int8_row(const uint4 (&pk)[8], uint32_t (&out)[64]) {
+  const uint32_t bias = 0x64806480u;  // 1152
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t u = w[j] ^ 0x80808080u;
-      if (BF16) {
-        const float f0 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7540))) - 8388736.0f;
-        const float f1 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7541))) - 8388736.0f;
-        const float f2 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7542))) - 8388736.0f;
-        const float f3 = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7543))) - 8388736.0f;
-        __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
-        out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
-        out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
-      } else {
-        const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
-        const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
-        const uint32_t bias = 0x64806480u;  // 1152
-        __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias));
-        __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&bias));
-        out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
-        out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
-      }
+      const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+      const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+      __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias));
+      __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&bias));
+      out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
+      out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
     }
   }
 }
 
 __device__ __forceinline__ float silu_dev(float g) { return g / (1.0f + __expf(-g)); }
 
-template <bool BF16>
-__device__ __forceinline__ uint16_t to_act_bits(float v) {
-  if (BF16) {
-    __nv_bfloat16 b = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t*>(&b);
-  } else {
-    __half h = __float2half_rn(v);
-    return *reinterpret_cast<uint16_t*>(&h);
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float act_bits_to_float(uint16_t b) {
-  if (BF16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
-  __half h = *reinterpret_cast<__half*>(&b);
-  return __half2float(h);
-}
-
-// Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values,
-// scales applied).  Modes: SiLU(gate)*up into the intermediate (gate/up rows
-// are adjacent lanes), fp32 gate/up partials, or routing-weighted down output.
-template <bool BF16>
+// Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values with
+// every scale applied).  Modes: SiLU(gate)*up into the fp32 intermediate
+// (gate/up rows are adjacent lanes), fp32 gate/up partials, or the
+// routing-weighted down output.
 __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkItem& it, int c0, int row, int lane,
                                                const float (&f)[16]) {
   if (p.epi_mode == kEpiSiluToAct) {
     // rows 2j / 2j+1 of the tile are gate / up of intermediate channel tile*64 + j
     const bool even = (lane & 1) == 0;
     const int jch = it.tile * (kTileRows / 2) + (row >> 1);
-    uint16_t* inter = static_cast<uint16_t*>(p.out);
+    float* inter = static_cast<float*>(p.out);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const float send = even ? f[c + 8] : f[c];
@@ -225,11 +188,7 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
       const float gt = even ? f[c] : recv;
       const float up = even ? recv : f[c + 8];
       const int col = even ? c : c + 8;
-      const float v = silu_dev(gt) * up;
-      const int64_t idx = static_cast<int64_t>(it.row0 + c0 + col) * p.inter_ld + jch;
-      const uint16_t hi = to_act_bits<BF16>(v);
-      inter[idx] = hi;
-      if (p.inter_lo_offset != 0) inter[p.inter_lo_offset + idx] = to_act_bits<BF16>(v - act_bits_to_float<BF16>(hi));
+      inter[static_cast<int64_t>(it.row0 + c0 + col) * p.inter_ld + jch] = silu_dev(gt) * up;
     }
   } else if (p.epi_mode == kEpiPartialRows) {
     float* h = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
@@ -247,23 +206,19 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 }
 
 // ---------------------------------------------------------------------------
-// The kernel
-//
-// TMEM columns: int8 keeps acc_bufs fp32 accumulators of T columns ([b*T, b*T+T));
-// int4 keeps a running fp32 sum [0, T) and two group partials [T, 3T) that the
-// MMA writes one 128-K group at a time, so each group's scale multiplies an
-// fp32 partial instead of rounding the weights.  The A stages follow at a_col0.
+// The kernel.  TMEM columns: each of the two MMA issuers owns acc_bufs fp32
+// accumulators of T columns (issuer i, buffer b at [(i*acc_bufs + b) * T]);
+// the A stages follow at a_col0.
 // ---------------------------------------------------------------------------
-template <bool INT4, bool BF16>
+template <bool INT4, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     qmoe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int T = p.token_tile;
-  const int NB = p.b_terms;
-  const uint32_t b_bytes = static_cast<uint32_t>(NB * T) * 256u;
-  const uint32_t st_bytes = gemm_stage_bytes(NB * T, p.stage_bytes);
+  const uint32_t b_bytes = static_cast<uint32_t>(T) * 256u;
+  const uint32_t st_bytes = gemm_stage_bytes(T, p.stage_bytes);
   const int NS = p.smem_stages, NA = p.a_stages, ACCB = p.acc_bufs;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * st_bytes);
@@ -278,23 +233,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // group-scaled accumulation (exact int4 operands, fp32 group scales): int4 with bf16 activations
-  constexpr bool GS = INT4 && BF16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      // 4 dequant warps + 1 MMA commit (+ 4 accumulate warps, which read the int4 group scale from the stage)
-      mbar_init(smem_u32(empty + s), GS ? 4 + 1 + 4 : 4 + 1);
+      mbar_init(smem_u32(empty + s), 4 + 1);  // 4 dequant warps + 1 MMA commit
     }
     for (int j = 0; j < NA; ++j) {
       mbar_init(smem_u32(afull + j), 4);
       mbar_init(smem_u32(aempty + j), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      // group-scaled: one commit per group partial; otherwise one commit from each of the two MMA issuers per item
-      mbar_init(smem_u32(accfull + b), GS ? 1 : 2);
-      mbar_init(smem_u32(accempty + b), 4);
+      mbar_init(smem_u32(accfull + b), 2);   // one commit from each MMA issuer per item
+      mbar_init(smem_u32(accempty + b), 4);  // the 4 epilogue warps
     }
     mbar_init(smem_u32(drain), 1);
     mbar_init(smem_u32(drain + 1), 1);
@@ -334,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         decode_item(p, nch, i, it);
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages * static_cast<int64_t>(p.stage_bytes);
-        const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + static_cast<uint32_t>(NB * it.nrows) * 256u;
+        const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + b_bytes;
         for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, st.next(NS)) {
           if ((g & 1) != id) continue;
           if (!mbar_wait(smem_u32(empty + st.idx), st.phase ^ 1u, abort_flag, 128)) {
@@ -347,11 +298,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!(p.fault_injection == 1 && blockIdx.x == 0 && g == 0)) {  // injected: armed, never filled
             tma_load_1d(smem_u32(sp + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
                         pol_w);
-            for (int h = 0; h < NB; ++h)
-              for (int a = 0; a < 2; ++a)
-                for (int r = 0; r < it.nrows; r += 16)
-                  tma_load_2d(smem_u32(sp + (h * 2 + a) * T * 128 + r * 128), &tmap_b, ks * kStageK + a * 64,
-                              h * p.b_lo_row0 + it.row0 + r, fb, pol_b);
+            // the stage's B tile as two copies of box {64 K, T rows} (one per 64-K half), landing
+            // as [half][row][128 B]; rows past the chunk (or past the buffer, zero-filled) go unused
+            tma_load_2d(smem_u32(sp), &tmap_b, ks * kStageK, it.row0, fb, pol_b);
+            tma_load_2d(smem_u32(sp + T * 128), &tmap_b, ks * kStageK + 64, it.row0, fb, pol_b);
           }
         }
       }
@@ -363,9 +313,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issuers
-    // Two threads (warps 5 and 6) issue the MMAs of even and odd stages: one
-    // thread's issue rate, with the waits and commits around each stage, is
-    // below what the tensor core accepts at small N, and the two run in parallel.
+    // Two threads (warps 5 and 6) issue the MMAs of even and odd stages into
+    // their own accumulators: one thread's issue rate, with the waits and
+    // commits around each stage, is below what the tensor core accepts at small
+    // N, and the two run in parallel.
     if (lane == 0) {
       const int id = warp - kMmaWarp;
       Ring fr, ar;
@@ -374,32 +325,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
         decode_item(p, nch, i, it);
-        const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), BF16);
-        int b = 0;
-        uint32_t acc_col = 0;
-        if (!GS) {
-          b = (ACCB == 2) ? (itn & 1) : 0;
-          const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
-          if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
-            ok = false;
-            break;
-          }
-          acc_col = static_cast<uint32_t>((id * ACCB + b) * T);
+        const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
+        const int b = (ACCB == 2) ? (itn & 1) : 0;
+        const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
+        if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
+          ok = false;
+          break;
         }
-        uint32_t acc_first = 0u;  // the issuer's first stage of the item overwrites its accumulator
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
+        uint32_t acc0 = 0u;  // the issuer's first stage of the item overwrites its accumulator
         for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, fr.next(NS), ar.next(NA)) {
           if ((g & 1) != id) continue;
-          uint32_t d_tmem;
-          if (GS) {
-            // one partial per 128-K group; even groups use partial 0, odd groups partial 1
-            if (!mbar_wait(smem_u32(accempty + id), ((g >> 1) & 1) ^ 1, abort_flag, 16)) {
-              ok = false;
-              break;
-            }
-            d_tmem = tmem + static_cast<uint32_t>(T + id * T);
-          } else {
-            d_tmem = tmem + acc_col;
-          }
           if (!mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag, 16) ||
               !mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 16)) {
             ok = false;
@@ -409,33 +345,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // descriptor of the stage's first K step; later K steps only move its start address
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes));
-          const uint32_t acc0 = GS ? 0u : acc_first;
-          acc_first = 1u;
+          const uint64_t atom16 = static_cast<uint64_t>((T * 128) >> 4);
           // The MMAs of a stage go out as one branch-free sequence: a branch between
           // two tcgen05.mma instructions roughly triples their issue cost.
-          const uint64_t atom16 = static_cast<uint64_t>((T * 128) >> 4);
-          if (NB == 2) {
-            const uint64_t lo16 = static_cast<uint64_t>((2 * T * 128) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t koff16 = (kk >> 2) * atom16 + static_cast<uint64_t>((kk & 3) * 2);
-              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc, kk > 0 ? 1u : acc0);
-              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16 + lo16, idesc, 1u);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t koff16 = (kk >> 2) * atom16 + static_cast<uint64_t>((kk & 3) * 2);
-              mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc, kk > 0 ? 1u : acc0);
-            }
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t koff16 = (kk >> 2) * atom16 + static_cast<uint64_t>((kk & 3) * 2);
+            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc, kk > 0 ? 1u : acc0);
           }
+          acc0 = 1u;
           mma_commit(smem_u32(empty + fr.idx));
           mma_commit(smem_u32(aempty + ar.idx));
-          if (GS) mma_commit(smem_u32(accfull + id));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
-        if (!GS) mma_commit(smem_u32(accfull + b));
+        mma_commit(smem_u32(accfull + b));
         ++itn;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
@@ -465,17 +389,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint4 pk[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
-          const uint32_t sbits = GS ? 0u : *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
+          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-          dequant_int4_row<BF16, !GS>(pk, sbits, out);
+          dequant_int4_row<BF16S>(pk, sbits, out);
         } else {
           uint4 pk[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-          dequant_int8_row<BF16>(pk, out);
+          dequant_int8_row(pk, out);
         }
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ar.idx), ar.phase ^ 1u, abort_flag));
         if (!ok) break;
@@ -491,101 +415,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
   } else if (warp < 4) {
-    // ------------------------------------------------------------ accumulate / epilogue warpgroup
+    // ------------------------------------------------------------ epilogue warpgroup
     const int q = warp;
     const int row = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int itn = 0, g = 0;
-    Ring sr;  // stage that holds the current group's scales
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
-      if (GS) {
-        // running sum += scale(group, row) * partial(group), group by group
-        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, sr.next(NS)) {
-          const int pb = g & 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + pb), (g >> 1) & 1, abort_flag, 32));
-          if (!ok) break;
-          tc_fence_after();
-          // the group's MMAs are done but its stage is still held for us: take the scale, release the stage
-          const uint16_t sb = *reinterpret_cast<const uint16_t*>(smem + sr.idx * st_bytes + b_bytes + 8192 + row * 2);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(empty + sr.idx));
-          const float scale = act_bits_to_float<BF16>(sb);
-          const bool first = ks == it.ks0, last = ks == it.ks1 - 1;
-          if (!first) tmem_wait_st();  // the previous group's running-sum stores
-          const uint32_t tpart = tmem + lane_base + static_cast<uint32_t>(T + pb * T);
-          const uint32_t tacc = tmem + lane_base;
-          for (int c0 = 0; c0 < it.nrows; c0 += 32) {
-            const bool two = c0 + 32 <= it.nrows;
-            uint32_t v[32], a[32];
-            tmem_ld_32x32b_x16<0>(tpart + static_cast<uint32_t>(c0), v);
-            if (two) tmem_ld_32x32b_x16<16>(tpart + static_cast<uint32_t>(c0 + 16), v);
-            if (!first) {
-              tmem_ld_32x32b_x16<0>(tacc + static_cast<uint32_t>(c0), a);
-              if (two) tmem_ld_32x32b_x16<16>(tacc + static_cast<uint32_t>(c0 + 16), a);
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (h == 1 && !two) break;
-              float f[16];
-#pragma unroll
-              for (int c = 0; c < 16; ++c)
-                f[c] = first ? scale * __uint_as_float(v[16 * h + c])
-                             : fmaf(scale, __uint_as_float(v[16 * h + c]), __uint_as_float(a[16 * h + c]));
-              if (last) {
-                epilogue_store<BF16>(p, it, c0 + 16 * h, row, lane, f);
-              } else {
-                uint32_t o[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(f[c]);
-                tmem_st_32x32b_x16(tacc + static_cast<uint32_t>(c0 + 16 * h), o);
-              }
-            }
-          }
-          // the partial has been read (wait::ld above); running-sum stores may still be in flight
+      const int b = (ACCB == 2) ? (itn & 1) : 0;
+      const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
+      if (!ok) break;
+      tc_fence_after();
+      // issuer 0 took the item's even global stages, issuer 1 the odd ones
+      const int n_st = it.ks1 - it.ks0;
+      const bool has0 = n_st >= 2 || (g & 1) == 0;
+      const bool has1 = n_st >= 2 || (g & 1) == 1;
+      g += n_st;
+      const float rs =
+          INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
+      const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(b * T);
+      const uint32_t t1 = tmem + lane_base + static_cast<uint32_t>((ACCB + b) * T);
+      for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+        uint32_t v[16], w[16];
+        if (has0) tmem_ld_32x32b_x16(t0 + static_cast<uint32_t>(c0), v);
+        if (has1) tmem_ld_32x32b_x16(t1 + static_cast<uint32_t>(c0), w);
+        tmem_wait_ld();
+        if (c0 + 16 >= it.nrows) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(accempty + pb));
+          if (lane == 0) mbar_arrive(smem_u32(accempty + b));
         }
-        if (!ok) break;
-      } else {
-        const int b = (ACCB == 2) ? (itn & 1) : 0;
-        const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
-        if (!ok) break;
-        tc_fence_after();
-        // issuer 0 took the item's even global stages, issuer 1 the odd ones
-        const int n_st = it.ks1 - it.ks0;
-        const bool has0 = n_st >= 2 || (g & 1) == 0;
-        const bool has1 = n_st >= 2 || (g & 1) == 1;
-        g += n_st;
-        const float rs =
-            INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
-        const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(b * T);
-        const uint32_t t1 = tmem + lane_base + static_cast<uint32_t>((ACCB + b) * T);
-        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-          uint32_t v[16], w[16];
-          if (has0) tmem_ld_32x32b_x16(t0 + static_cast<uint32_t>(c0), v);
-          if (has1) tmem_ld_32x32b_x16(t1 + static_cast<uint32_t>(c0), w);
-          tmem_wait_ld();
-          if (c0 + 16 >= it.nrows) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(accempty + b));
-          }
-          float f[16];
+        float f[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            f[c] = ((has0 ? __uint_as_float(v[c]) : 0.0f) + (has1 ? __uint_as_float(w[c]) : 0.0f)) * rs;
-          epilogue_store<BF16>(p, it, c0, row, lane, f);
+        for (int c = 0; c < 16; ++c) {
+          const float cs = __ldg(p.col_scale + it.row0 + c0 + c);
+          f[c] = ((has0 ? __uint_as_float(v[c]) : 0.0f) + (has1 ? __uint_as_float(w[c]) : 0.0f)) * rs * cs;
         }
+        epilogue_store(p, it, c0, row, lane, f);
       }
       ++itn;
     }
-    if (GS) tmem_wait_st();  // no running-sum store may be in flight when TMEM is released
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
   }
 
@@ -598,13 +470,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <bool INT4, bool BF16>
+template <bool INT4, bool BF16S>
 cudaError_t launch_gemm_t(const CUtensorMap* tmap_b, const GemmParams& p, int grid, cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p);
-  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<INT4, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<INT4, BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_kernel(qmoe_gemm_kernel<INT4, BF16>, dim3(grid), dim3(kGemmThreads), smem, stream, true, *tmap_b, p);
+  return launch_kernel(qmoe_gemm_kernel<INT4, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, *tmap_b, p);
 }
 
 }  // namespace qmoe

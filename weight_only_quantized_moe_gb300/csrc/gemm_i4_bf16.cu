@@ -1,5 +1,5 @@
 // gemm_i4_bf16.cu - instantiation of the grouped dequant GEMM for int4 weights
-// and bf16 activations (one translation unit per variant so they compile in parallel).
+// with bf16 group scales (one translation unit per variant so they compile in parallel).
 #include "gemm.cuh"
 
 namespace qmoe {

@@ -1,5 +1,5 @@
 // gemm_i4_f16.cu - instantiation of the grouped dequant GEMM for int4 weights
-// and f16 activations (one translation unit per variant so they compile in parallel).
+// with f16 group scales (one translation unit per variant so they compile in parallel).
 #include "gemm.cuh"
 
 namespace qmoe {

@@ -1,0 +1,11 @@
+// gemm_i8.cu - instantiation of the grouped dequant GEMM for int8 weights
+// (one translation unit per variant so they compile in parallel).
+#include "gemm.cuh"
+
+namespace qmoe {
+
+cudaError_t launch_gemm_i8(const CUtensorMap* tmap_b, const GemmParams& p, int grid, cudaStream_t stream) {
+  return launch_gemm_t<false, false>(tmap_b, p, grid, stream);
+}
+
+}  // namespace qmoe

@@ -30,7 +30,7 @@ struct Chunk {
 };
 
 enum EpiMode : int32_t {
-  kEpiSiluToAct = 0,   // gate/up GEMM, whole K: inter[row, j] = SiLU(gate)*up in the activation type
+  kEpiSiluToAct = 0,   // gate/up GEMM, whole K: fp32 inter[row, j] = SiLU(gate)*up
   kEpiPartialRows = 1, // gate/up GEMM, split K: fp32 partial [split][row][2I] (interleaved gate/up)
   kEpiWeightedPairs = 2 // down GEMM: fp32 y[split][pair][H] = topk_weight * acc
 };
@@ -38,6 +38,7 @@ enum EpiMode : int32_t {
 struct GemmParams {
   const uint8_t* w;          // packed weights [E][n_tiles][k_stages][stage_bytes]
   const float* row_scale;    // int8: per packed row [E][n_tiles*128]; int4: null
+  const float* col_scale;    // per B row (token row): 2^e of its power-of-two f16 scaling
   const Chunk* chunks;       // [max_chunks]
   const int32_t* n_chunks;   // device scalar
   const int32_t* sorted_ids; // down GEMM epilogue
@@ -46,18 +47,15 @@ struct GemmParams {
   int32_t* status;
   int64_t out_ld;            // elements per output row
   int64_t out_split_stride;  // elements per split slab
-  int64_t inter_lo_offset;   // SiLU epilogue with a two-term intermediate: elements from hi to lo slab (0: one term)
   int32_t n_tiles;
   int32_t k_stages;
   int32_t split;
   int32_t token_tile;        // T: B rows per stage buffer, TMEM columns per accumulator
-  int32_t acc_bufs;          // int8: 1 or 2 TMEM accumulators per MMA issuer; int4: unused (running sum + two group partials)
+  int32_t acc_bufs;          // TMEM accumulators per MMA issuer (1 or 2)
   int32_t a_col0;            // first TMEM column of the A stages
   int32_t a_stages;          // TMEM A stages (64 columns each)
   int32_t smem_stages;       // shared-memory pipeline depth
   int32_t stage_bytes;       // packed weight bytes per stage
-  int32_t b_terms;           // 1, or 2 when the B operand is a hi+lo pair of bf16 matrices
-  int32_t b_lo_row0;         // row offset of the lo term in the B tensor map
   int32_t epi_mode;
   int32_t P;                 // number of token-expert pairs
   int32_t chunk_group;       // work-item raster: chunks per group
@@ -89,19 +87,23 @@ cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
                          int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded, int32_t token_tile,
                          Chunk* chunks, int32_t* n_chunks, int32_t* status, cudaStream_t stream);
 
-cudaError_t launch_gather(const void* x, const int32_t* sorted_ids, const int32_t* expert_ids,
+cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, void* xg, int num_sms, cudaStream_t stream);
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
+                          cudaStream_t stream);
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
-                               int32_t I, bool bf16, void* inter, int64_t inter_lo_offset, int num_sms,
-                               cudaStream_t stream);
+                               int32_t I, float* inter32, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
+                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
+                                 cudaStream_t stream);
 
 cudaError_t launch_out_reduce(const float* y, int32_t split, int64_t M, int32_t top_k, int32_t H, bool bf16,
                               void* out, int num_sms, cudaStream_t stream);
 
 size_t gemm_smem_bytes(const GemmParams& p);
-cudaError_t launch_gemm(bool int4, bool bf16, const CUtensorMap* tmap_b, const GemmParams& p, int grid,
+cudaError_t launch_gemm(bool int4, bool bf16_scales, const CUtensorMap* tmap_b, const GemmParams& p, int grid,
                         cudaStream_t stream);
 
 }  // namespace qmoe
