@@ -22,7 +22,6 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -43,7 +42,7 @@ LAUNCH_NAMES = ["moe_align", "gather", "gemm_gate_up", "silu_reduce", "inter_res
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
@@ -117,53 +116,77 @@ def cpu_cores():
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock-event reasons of one GPU every ~2 ms
+    while the timed region runs (NVML through ctypes; read-only queries)."""
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.rows = []
+        self.max_mhz = None
+        self.err = None
+        self.nvml = None
+        self.handle = None
+        self.thread = None
+        self.stop = None
+
+    def _open(self):
+        import ctypes
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+        if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        self.nvml, self.handle = nv, h
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, self.SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _loop(self):
+        import ctypes
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (self.nvml.nvmlDeviceGetClockInfo(self.handle, self.SM, ctypes.byref(c)) == 0 and
+                    self.reasons_fn(self.handle, ctypes.byref(r)) == 0):
+                self.rows.append((float(c.value), int(r.value)))
+            time.sleep(0.002)
 
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+            self._open()
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            t0 = time.time()
+            while not self.rows and time.time() - t0 < 2.0:  # first sample before the timed region
+                time.sleep(0.001)
+        except Exception as e:  # no NVML on this host
+            self.err = f"nvml unavailable: {e}"
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                self.out = ""
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=2.0)
 
     def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in (self.out or "").strip().splitlines():
-            f = [s.strip() for s in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
-            except ValueError:
-                continue
+        if self.err is not None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.err], "samples": 0}
+        rows = self.rows[1:] if len(self.rows) > 1 else self.rows  # the first sample precedes the region
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        reasons = set()
-        for r in rows:
-            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[2:]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "samples": 0}
+        reasons = sorted({name for _, bits in rows for b, name in self.REASONS.items() if bits & b})
+        return {"sm_mhz": statistics.median(c for c, _ in rows), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(rows)}
 
 
 # ----------------------------------------------------------------------------
@@ -183,6 +206,30 @@ def algorithmic_bytes(wl, dl, inp):
     total = d * (per_expert_w13 + per_expert_w2) + M * wl.H * act * 2 + 2 * P * wl.I * act
     return {"distinct_experts": d, "gemm_gate_up": gemm1, "gemm_down": gemm2, "layer": total,
             "weights": d * (per_expert_w13 + per_expert_w2)}
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "weight_only_quantized_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, M, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    if there is none for this workload or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if len(p) >= 5 and not p[0].startswith("#") and p[0] == workload and int(p[1]) == M and p[2] == kernel:
+                return int(p[3]) if p[4] == cur else None
+    return None
 
 
 def run_gpu(args, rank, world):
@@ -340,7 +387,7 @@ def main():
             "tflops": world * flops / (ms * 1e-3) / 1e12,
             "weight_gbs": world * by["weights"] / (ms * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                         "frac": ach / hbm, "traffic": None,
+                         "frac": ach / hbm, "traffic": recorded_traffic(wl.name, M, dominant),
                          "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
                          "algorithmic_bytes_per_launch": by[dominant],
                          "layer_frac": by["layer"] / (ms * 1e-3) / 1e9 / hbm},
