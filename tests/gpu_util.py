@@ -32,8 +32,12 @@ def device_inputs(wl, inp, device="cuda"):
     return x, ids, w
 
 
-def run_forward(dl, x, ids, w, opts=None, check_status=True):
+def run_forward(dl, x, ids, w, opts=None, check_status=True, ws_fill=0xFF):
     ws = q.alloc_workspace(q.qmoe_workspace_size(dl, x.shape[0], ids.shape[1], opts), x.device)
+    if ws_fill is not None:
+        # all-ones bytes are NaN in every float type: a read of a workspace byte the
+        # forward did not write first would show up in the output
+        ws.fill_(ws_fill)
     out = q.qmoe_forward(dl, x, ids, w, workspace=ws, opts=opts)
     st = q.qmoe_read_device_status(ws)
     if check_status:

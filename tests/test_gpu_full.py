@@ -70,3 +70,27 @@ def test_full_size_sampled(name, M, n_sample):
             rows.append(int(m))
     ref = oracle.moe_forward_rows(L, inp.x, inp.topk_ids, inp.topk_weights, rows)
     assert_parity(got[rows], ref, f"{name} M={M} rows={rows}")
+
+
+@pytest.mark.parametrize("stage_groups", [1, 2])
+def test_full_size_long_items_repeated(stage_groups):
+    """Whole-K work items (no split) at decode size: every CTA runs hundreds of
+    pipeline stages through the even/odd producer, dequant and MMA roles.
+    Repeated runs on a NaN-filled workspace catch ordering faults that only
+    show under some interleavings."""
+    name, M = "mixtral8x7b_w4", 16
+    wl = WORKLOADS[name]
+    L, dl = _layer(name)
+    inp = make_inputs(wl, M, seed=0)
+    x, ids, w = device_inputs(wl, inp)
+    rows = [0, 5, 11]
+    ref = oracle.moe_forward_rows(L, inp.x, inp.topk_ids, inp.topk_weights, rows)
+    first = None
+    for rep in range(6):
+        out, _ = run_forward(dl, x, ids, w, opts=q.make_options(1, 1, 0, 0, stage_groups))
+        got = out.float().cpu().numpy()
+        assert_parity(got[rows], ref, f"{name} M={M} split 1 stage_groups {stage_groups} rep {rep}")
+        if first is None:
+            first = got
+        else:
+            assert np.array_equal(first, got), "whole-K forward not bit-reproducible"

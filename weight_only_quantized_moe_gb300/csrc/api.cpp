@@ -1,8 +1,6 @@
 // api.cpp - host side of libqmoe: argument validation, weight packing,
-// workspace planning, tensor-map encoding and the launch sequence of the
-// fused MoE forward.  The C ABI is declared in include/qmoe.h.
-#include <cudaTypedefs.h>
-
+// workspace planning and the launch sequence of the fused MoE forward.  The C
+// ABI is declared in include/qmoe.h.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -61,36 +59,6 @@ int current_sm_count() {
   return n;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    else
-      cudaGetLastError();
-  });
-  return fn;
-}
-
-// Row-major [rows, K] 16-bit matrix, boxes of 64 elements (128 B) x 16 rows, 128-byte swizzle.
-// A [rows, K] 16-bit row-major matrix; one copy of box {64, box_rows} fetches
-// 64 K of box_rows rows as [row][128 B] (128-byte swizzled).
-bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
-  auto fn = tensor_map_encoder();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {K, rows};
-  cuuint64_t strides[1] = {K * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 qmoe_status check_dev_ptr(const void* p, int dev) {
   if (p == nullptr) return QMOE_ERR_INVALID_ARG;
   cudaPointerAttributes a;
@@ -129,7 +97,8 @@ qmoe_status validate_layer_dims(const qmoe_layer* L) {
 struct Plan {
   int64_t M = 0, P = 0;
   int k = 0;
-  int T = 0, acc_bufs = 0, a_col0 = 0, a_stages = 0, ns = 0, stage_bytes = 0;
+  int T = 0, acc_bufs = 0, a_col0 = 0, stage_bytes = 0;
+  int ks1 = 1, ks2 = 1, ns1 = 0, ns2 = 0, na1 = 0, na2 = 0;  // per GEMM: groups per stage, smem / TMEM A stages
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -182,22 +151,48 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   // double buffered when that leaves room for two 64-column A stages
   p.acc_bufs = (4 * T + 2 * 64 <= 512) ? 2 : 1;
   p.a_col0 = 2 * p.acc_bufs * T;
-  p.a_stages = std::min(8, (512 - p.a_col0) / 64);
   p.stage_bytes = int4 ? kInt4StageBytes : kInt8StageBytes;
-  const size_t wreg = (p.stage_bytes + 1023) & ~1023;
-  p.ns = static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / (static_cast<size_t>(T) * 256 + wreg)));
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
-  p.cap = P + static_cast<int64_t>(L->E) * (kAlignBlock - 1);
+  // Pipeline stages of two quantization groups halve the per-stage barrier and
+  // MMA-issue overhead; they are used when K has an even number of groups and
+  // at least four such stages fit in shared memory.
+  // Both rings have an even number of slots: the even and odd stages go to two
+  // separate producer / dequant / MMA roles, and with an even ring every slot is
+  // only ever used by one of them, so each waiter sees every phase of its
+  // barriers.  (With an odd ring a role would see every other use of a slot and
+  // a parity wait could pass on a phase two behind.)
+  auto smem_stages = [&](int ks) {
+    const size_t per = static_cast<size_t>(T) * 256 * ks + ((static_cast<size_t>(p.stage_bytes) * ks + 1023) & ~size_t(1023));
+    return static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / per)) & ~1;
+  };
+  auto a_stages = [&](int ks) { return std::min(8, (512 - p.a_col0) / (64 * ks)) & ~1; };
+  const int forced_ks = (o != nullptr) ? o->stage_groups : 0;
+  if (forced_ks < 0 || forced_ks > 2) return QMOE_ERR_INVALID_ARG;
+  if (forced_ks == 2 && (p.kst1 % 2 != 0 || p.kst2 % 2 != 0 || smem_stages(2) < 2 || a_stages(2) < 2))
+    return QMOE_ERR_INVALID_ARG;
+  auto pick = [&](int kst, int* ks, int* ns, int* na) {
+    if (forced_ks != 0)
+      *ks = forced_ks;
+    else
+      *ks = (kst % 2 == 0 && smem_stages(2) >= 4 && a_stages(2) >= 2) ? 2 : 1;
+    *ns = smem_stages(*ks);
+    *na = a_stages(*ks);
+  };
+  pick(p.kst1, &p.ks1, &p.ns1, &p.na1);
+  pick(p.kst2, &p.ks2, &p.ns2, &p.na2);
+  if (p.ns1 < 2 || p.ns2 < 2 || p.na1 < 2 || p.na2 < 2) return QMOE_ERR_UNSUPPORTED;
+  // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
+  p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
   p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
   p.max_chunks = (p.cap + T - 1) / T + L->E;
   // expected chunks for the split heuristic (uniform routing)
   const double d = L->E * (1.0 - std::pow(1.0 - 1.0 / L->E, static_cast<double>(P)));
   const int64_t est_chunks = std::max<int64_t>(std::max<int64_t>(1, static_cast<int64_t>(std::ceil(d))), (P + T - 1) / T);
-  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, 0.8);
-  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, 0.97);
+  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1 / p.ks1, sms, 0.8);
+  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2 / p.ks2, sms, 0.97);
   if (o != nullptr && o->split1 != 0) {
     if (o->split1 < 1 || o->split1 > 64 || o->split1 > p.kst1) return QMOE_ERR_INVALID_ARG;
     p.S1 = o->split1;
@@ -205,6 +200,18 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   if (o != nullptr && o->split2 != 0) {
     if (o->split2 < 1 || o->split2 > 64 || o->split2 > p.kst2) return QMOE_ERR_INVALID_ARG;
     p.S2 = o->split2;
+  }
+  // a forced split finer than the stages of two groups falls back to one-group stages
+  if (forced_ks == 2 && (p.S1 > p.kst1 / 2 || p.S2 > p.kst2 / 2)) return QMOE_ERR_INVALID_ARG;
+  if (p.S1 > p.kst1 / p.ks1) {
+    p.ks1 = 1;
+    p.ns1 = smem_stages(1);
+    p.na1 = a_stages(1);
+  }
+  if (p.S2 > p.kst2 / p.ks2) {
+    p.ks2 = 1;
+    p.ns2 = smem_stages(1);
+    p.na2 = a_stages(1);
   }
   size_t off = 0;
   p.off_status = off;   off += 256;
@@ -252,7 +259,6 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
       !aligned(L->w2, 256) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
       (L->perm13 != nullptr && !aligned(L->perm13, 16)) || (!int4 && (!aligned(L->s13, 16) || !aligned(L->s2, 16))))
     return QMOE_ERR_INVALID_ARG;
-  if (tensor_map_encoder() == nullptr) return QMOE_ERR_CUDA;
 
   uint8_t* base = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(base + pl.off_status);
@@ -271,9 +277,6 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const bool bf16 = L->act_dtype == QMOE_BF16;
   const int P = static_cast<int>(pl.P);
 
-  CUtensorMap map_xg, map_inter;
-  if (!encode_rows_map(&map_xg, xg, pl.cap, L->H, pl.T) || !encode_rows_map(&map_inter, inter16, pl.cap, L->I, pl.T))
-    return QMOE_ERR_CUDA;
 
   // events (profiling only): 2i before and 2i+1 after launch i
   auto rec = [&](int idx) {
@@ -287,13 +290,15 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   launched += (err == cudaSuccess);
   rec(2);
   if (err == cudaSuccess) {
-    err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, sms,
-                        stream);
+    err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, pl.ks1, xg, xscale,
+                        sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(3);
   GemmParams g1{};
   g1.w = static_cast<const uint8_t*>(L->w13);
+  g1.b = static_cast<const uint8_t*>(xg);
+  g1.b_unit_stride = pl.cap * 256 * pl.ks1;
   g1.row_scale = int4 ? nullptr : L->s13;
   g1.col_scale = xscale;
   g1.chunks = chunks;
@@ -302,13 +307,14 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.topk_w = topk_weights;
   g1.status = status;
   g1.n_tiles = pl.n_tiles1;
-  g1.k_stages = pl.kst1;
+  g1.k_groups = pl.kst1;
+  g1.ks = pl.ks1;
   g1.split = pl.S1;
   g1.token_tile = pl.T;
   g1.acc_bufs = pl.acc_bufs;
   g1.a_col0 = pl.a_col0;
-  g1.a_stages = pl.a_stages;
-  g1.smem_stages = pl.ns;
+  g1.a_stages = pl.na1;
+  g1.smem_stages = pl.ns1;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -327,10 +333,15 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   }
   GemmParams g2 = g1;
   g2.w = static_cast<const uint8_t*>(L->w2);
+  g2.b = static_cast<const uint8_t*>(inter16);
+  g2.b_unit_stride = pl.cap * 256 * pl.ks2;
   g2.row_scale = int4 ? nullptr : L->s2;
   g2.col_scale = iscale;
   g2.n_tiles = pl.n_tiles2;
-  g2.k_stages = pl.kst2;
+  g2.k_groups = pl.kst2;
+  g2.ks = pl.ks2;
+  g2.a_stages = pl.na2;
+  g2.smem_stages = pl.ns2;
   g2.split = pl.S2;
   g2.epi_mode = kEpiWeightedPairs;
   g2.fault_injection = 0;
@@ -344,7 +355,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
-    err = launch_gemm(int4, bf16, &map_xg, g1, grid1, stream);  // int4 scales have the activation dtype
+    err = launch_gemm(int4, bf16, g1, grid1, stream);  // int4 scales have the activation dtype
     launched += (err == cudaSuccess);
   }
   rec(5);
@@ -356,19 +367,19 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(7);
   rec(8);
   if (err == cudaSuccess) {
-    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, sms, stream);
+    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, pl.ks2, inter16, iscale, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(9);
   rec(10);
   if (err == cudaSuccess) {
-    err = launch_gemm(int4, bf16, &map_inter, g2, grid2, stream);
+    err = launch_gemm(int4, bf16, g2, grid2, stream);
     launched += (err == cudaSuccess);
   }
   rec(11);
   rec(12);
   if (err == cudaSuccess) {
-    err = launch_out_reduce(y, pl.S2, M, k, L->H, bf16, out, sms, stream);
+    err = launch_out_reduce(y, topk_ids, L->E, pl.S2, M, k, L->H, bf16, out, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(13);

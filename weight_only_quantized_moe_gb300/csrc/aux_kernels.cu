@@ -201,20 +201,35 @@ __device__ __forceinline__ uint16_t f16_bits(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// Token gather: xg[row, :] = x[sorted_ids[row] / top_k, perm13_e] * 2^-e_row in
-// f16, xscale[row] = 2^e_row (zeros and 1 for padding rows).  Rows are the B
-// operand of the gate/up GEMM; with act-order the hidden channels are put in
-// each expert's sorted-group order so the GEMM walks K in whole quantization
-// groups.
+// Token gather: row `row` of the gate/up GEMM's B operand is
+// x[sorted_ids[row] / top_k, perm13_e] * 2^-e_row in f16, stored in the
+// pre-staged layout (staged_offset), with xscale[row] = 2^e_row; padding rows
+// are zeros with scale 1.  With act-order the hidden channels are put in each
+// expert's sorted-group order so the GEMM walks K in whole quantization groups.
+// One warp per row; lane work unit = 8 consecutive K (one 16-byte piece).
 // ---------------------------------------------------------------------------
 constexpr int kGatherThreads = 256;
+
+template <bool BF16>
+__device__ __forceinline__ uint4 scale_to_f16x8(const uint16_t (&e)[8], float inv) {
+  uint4 o;
+  o.x = static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[0]) * inv)) |
+        (static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[1]) * inv)) << 16);
+  o.y = static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[2]) * inv)) |
+        (static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[3]) * inv)) << 16);
+  o.z = static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[4]) * inv)) |
+        (static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[5]) * inv)) << 16);
+  o.w = static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[6]) * inv)) |
+        (static_cast<uint32_t>(f16_bits(act_to_float<BF16>(e[7]) * inv)) << 16);
+  return o;
+}
 
 template <bool BF16>
 __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                   const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_post_padded,
-                  const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B,
-                  uint16_t* __restrict__ xg, float* __restrict__ xscale) {
+                  const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B, int64_t cap,
+                  int32_t ks, uint8_t* __restrict__ xg, float* __restrict__ xscale) {
   pdl_launch_dependents();
   pdl_wait();
   const int total = *num_post_padded;
@@ -222,10 +237,9 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int warps = gridDim.x * (kGatherThreads / 32);
   for (int row = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); row < total; row += warps) {
     const int p = sorted_ids[row];
-    uint16_t* dst = xg + static_cast<int64_t>(row) * H;
     if (p >= P) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      for (int i = lane; i < H / 8; i += 32) d4[i] = make_uint4(0, 0, 0, 0);
+      for (int c = lane; c < H / 8; c += 32)
+        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, ks, cap)) = make_uint4(0, 0, 0, 0);
       if (lane == 0) xscale[row] = 1.0f;
       continue;
     }
@@ -243,23 +257,19 @@ __global__ void __launch_bounds__(kGatherThreads)
     const float inv = sc.y;
     if (lane == 0) xscale[row] = sc.x;
     if (perm13 == nullptr) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      for (int i = lane; i < H / 8; i += 32) {
-        const uint4 v = __ldg(s4 + i);
-        const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
-        uint4 o;
-        uint16_t* oe = reinterpret_cast<uint16_t*>(&o);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) oe[k] = f16_bits(act_to_float<BF16>(e[k]) * inv);
-        d4[i] = o;
+      for (int c = lane; c < H / 8; c += 32) {
+        const uint4 v = __ldg(s4 + c);
+        uint16_t e[8];
+        *reinterpret_cast<uint4*>(e) = v;
+        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, ks, cap)) = scale_to_f16x8<BF16>(e, inv);
       }
     } else {
-      const int32_t* pr = perm13 + static_cast<int64_t>(expert_ids[row / B]) * H;
-      uint32_t* d2 = reinterpret_cast<uint32_t*>(dst);
-      for (int i = lane; i < H / 2; i += 32) {
-        const int2 k2 = __ldg(reinterpret_cast<const int2*>(pr) + i);
-        d2[i] = static_cast<uint32_t>(f16_bits(act_to_float<BF16>(__ldg(src + k2.x)) * inv)) |
-                (static_cast<uint32_t>(f16_bits(act_to_float<BF16>(__ldg(src + k2.y)) * inv)) << 16);
+      const int4* pr4 = reinterpret_cast<const int4*>(perm13 + static_cast<int64_t>(expert_ids[row / B]) * H);
+      for (int c = lane; c < H / 8; c += 32) {
+        const int4 ka = __ldg(pr4 + 2 * c), kb = __ldg(pr4 + 2 * c + 1);
+        uint16_t e[8] = {__ldg(src + ka.x), __ldg(src + ka.y), __ldg(src + ka.z), __ldg(src + ka.w),
+                         __ldg(src + kb.x), __ldg(src + kb.y), __ldg(src + kb.z), __ldg(src + kb.w)};
+        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, ks, cap)) = scale_to_f16x8<BF16>(e, inv);
       }
     }
   }
@@ -267,14 +277,14 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
-                          cudaStream_t stream) {
+                          int32_t H, int32_t block, int64_t cap_rows, int32_t ks, void* xg, float* xscale,
+                          int num_sms, cudaStream_t stream) {
   const int64_t want = (cap_rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
   auto kern = bf16 ? gather_kernel<true> : gather_kernel<false>;
   return launch_kernel(kern, dim3(grid), dim3(kGatherThreads), 0, stream, true, static_cast<const uint16_t*>(x),
-                       sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block,
-                       static_cast<uint16_t*>(xg), xscale);
+                       sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block, cap_rows, ks,
+                       static_cast<uint8_t*>(xg), xscale);
 }
 
 // ---------------------------------------------------------------------------
@@ -310,17 +320,17 @@ cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, i
 }
 
 // ---------------------------------------------------------------------------
-// Intermediate rescale: inter16[row, :] = inter32[row, :] * 2^-e_row in f16 and
-// iscale[row] = 2^e_row (the down GEMM's B operand and its column scale).  One
-// CTA per row (the absmax is a block reduction); padding rows get zeros and
-// scale 1 without reading inter32.
+// Intermediate rescale: row `row` of the down GEMM's B operand is
+// inter32[row, :] * 2^-e_row in f16 in the pre-staged layout (staged_offset),
+// iscale[row] = 2^e_row.  One CTA per row (the absmax is a block reduction);
+// padding rows get zeros and scale 1 without reading inter32.
 // ---------------------------------------------------------------------------
 constexpr int kRescaleThreads = 256;
 
 __global__ void __launch_bounds__(kRescaleThreads)
     inter_rescale_kernel(const float* __restrict__ inter32, const int32_t* __restrict__ num_post_padded,
-                         const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I,
-                         uint16_t* __restrict__ inter16, float* __restrict__ iscale) {
+                         const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I, int64_t cap, int32_t ks,
+                         uint8_t* __restrict__ inter16, float* __restrict__ iscale) {
   __shared__ float red[kRescaleThreads / 32];
   pdl_launch_dependents();
   pdl_wait();
@@ -328,8 +338,8 @@ __global__ void __launch_bounds__(kRescaleThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int row = blockIdx.x; row < total; row += gridDim.x) {
     if (sorted_ids[row] >= P) {  // uniform across the CTA
-      uint4* d4 = reinterpret_cast<uint4*>(inter16 + static_cast<int64_t>(row) * I);
-      for (int i = threadIdx.x; i < I / 8; i += kRescaleThreads) d4[i] = make_uint4(0, 0, 0, 0);
+      for (int c = threadIdx.x; c < I / 8; c += kRescaleThreads)
+        *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, ks, cap)) = make_uint4(0, 0, 0, 0);
       if (threadIdx.x == 0) iscale[row] = 1.0f;
       continue;
     }
@@ -348,33 +358,36 @@ __global__ void __launch_bounds__(kRescaleThreads)
     __syncthreads();  // red is reused by the next row
     const float2 sc = row_exponent_scale(amax);
     if (threadIdx.x == 0) iscale[row] = sc.x;
-    uint2* d2 = reinterpret_cast<uint2*>(inter16 + static_cast<int64_t>(row) * I);
-    for (int i = threadIdx.x; i < I / 4; i += kRescaleThreads) {
-      const float4 v = __ldg(s4 + i);
-      uint2 o;
-      o.x = static_cast<uint32_t>(f16_bits(v.x * sc.y)) | (static_cast<uint32_t>(f16_bits(v.y * sc.y)) << 16);
-      o.y = static_cast<uint32_t>(f16_bits(v.z * sc.y)) | (static_cast<uint32_t>(f16_bits(v.w * sc.y)) << 16);
-      d2[i] = o;
+    for (int c = threadIdx.x; c < I / 8; c += kRescaleThreads) {
+      const float4 a = __ldg(s4 + 2 * c), b = __ldg(s4 + 2 * c + 1);
+      uint4 o;
+      o.x = static_cast<uint32_t>(f16_bits(a.x * sc.y)) | (static_cast<uint32_t>(f16_bits(a.y * sc.y)) << 16);
+      o.y = static_cast<uint32_t>(f16_bits(a.z * sc.y)) | (static_cast<uint32_t>(f16_bits(a.w * sc.y)) << 16);
+      o.z = static_cast<uint32_t>(f16_bits(b.x * sc.y)) | (static_cast<uint32_t>(f16_bits(b.y * sc.y)) << 16);
+      o.w = static_cast<uint32_t>(f16_bits(b.z * sc.y)) | (static_cast<uint32_t>(f16_bits(b.w * sc.y)) << 16);
+      *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, ks, cap)) = o;
     }
   }
 }
 
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
-                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
-                                 cudaStream_t stream) {
+                                 int32_t P, int32_t I, int64_t cap_rows, int32_t ks, void* inter16, float* iscale,
+                                 int num_sms, cudaStream_t stream) {
   const int grid = static_cast<int>(cap_rows < 8LL * num_sms ? (cap_rows > 0 ? cap_rows : 1) : 8LL * num_sms);
   return launch_kernel(inter_rescale_kernel, dim3(grid), dim3(kRescaleThreads), 0, stream, true, inter32,
-                       num_post_padded, sorted_ids, P, I, static_cast<uint16_t*>(inter16), iscale);
+                       num_post_padded, sorted_ids, P, I, cap_rows, ks, static_cast<uint8_t*>(inter16), iscale);
 }
 
 // ---------------------------------------------------------------------------
 // Output reduce: out[m, n] = sum_j sum_s y[s, m*top_k + j, n] in a fixed order
-// (the routing weight is already applied by the down GEMM's epilogue).
+// (the routing weight is already applied by the down GEMM's epilogue).  Slots
+// whose expert id is outside [0, E) were dropped by moe_align, so no GEMM wrote
+// their y rows: they are skipped.
 // ---------------------------------------------------------------------------
 template <bool BF16>
 __global__ void __launch_bounds__(256)
-    out_reduce_kernel(const float* __restrict__ y, int32_t split, int64_t M, int32_t top_k, int32_t H,
-                      uint16_t* __restrict__ out) {
+    out_reduce_kernel(const float* __restrict__ y, const int32_t* __restrict__ topk_ids, int32_t E, int32_t split,
+                      int64_t M, int32_t top_k, int32_t H, uint16_t* __restrict__ out) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t total = M * (H / 4);
@@ -384,6 +397,8 @@ __global__ void __launch_bounds__(256)
     const int n4 = static_cast<int>(t - m * (H / 4));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < top_k; ++j) {
+      const int e = __ldg(topk_ids + m * top_k + j);
+      if (e < 0 || e >= E) continue;
       const int64_t base = (m * top_k + j) * H + 4LL * n4;
       for (int s = 0; s < split; ++s) {
         const float4 v = __ldg(reinterpret_cast<const float4*>(y + s * slab + base));
@@ -404,15 +419,15 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-cudaError_t launch_out_reduce(const float* y, int32_t split, int64_t M, int32_t top_k, int32_t H, bool bf16,
-                              void* out, int num_sms, cudaStream_t stream) {
+cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E, int32_t split, int64_t M,
+                              int32_t top_k, int32_t H, bool bf16, void* out, int num_sms, cudaStream_t stream) {
   const int64_t want = (M * (H / 4) + 255) / 256;
   const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
   if (bf16)
-    return launch_kernel(out_reduce_kernel<true>, dim3(grid), dim3(256), 0, stream, true, y, split, M, top_k, H,
-                         static_cast<uint16_t*>(out));
-  return launch_kernel(out_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, y, split, M, top_k, H,
-                       static_cast<uint16_t*>(out));
+    return launch_kernel(out_reduce_kernel<true>, dim3(grid), dim3(256), 0, stream, true, y, topk_ids, E, split, M,
+                         top_k, H, static_cast<uint16_t*>(out));
+  return launch_kernel(out_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, y, topk_ids, E, split, M,
+                       top_k, H, static_cast<uint16_t*>(out));
 }
 
 }  // namespace qmoe

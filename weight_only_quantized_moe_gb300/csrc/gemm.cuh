@@ -25,10 +25,12 @@
 //     the MMA's A operand straight from tensor memory; dequantized weights
 //     never touch shared memory, which carries only the packed bytes and the
 //     token tile.
-//   * the packed weights (one contiguous block per 128x128 tile, scales
-//     appended) arrive by 1-D bulk TMA; a stage's token tile by two 2-D tensor
-//     TMA copies with 128-byte swizzle, the layout the MMA's shared-memory
-//     descriptor reads.
+//   * a pipeline stage covers `ks` (1 or 2) quantization groups of 128 K.  Its
+//     packed weights (contiguous blocks per 128x128 tile, scales appended) and
+//     its token tile arrive as two 1-D bulk TMA copies: the producers of the
+//     B operand (gather, rescale) store it pre-staged, per stage and 8-row
+//     group, in the 128-byte-swizzled K-major layout the MMA's shared-memory
+//     descriptor reads, so a chunk's tile for one stage is one contiguous run.
 //   * warp roles: two TMA producer threads (warps 4, 7), two MMA-issuing
 //     threads (warps 5, 6) and two dequant warpgroups (warps 8-15), each pair
 //     taking the even and the odd pipeline stages; one epilogue warpgroup
@@ -57,9 +59,11 @@ constexpr int kDequantWarp0 = 8;  // warps 8..15: two warpgroups
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarrierBytes = 1024;
 
-__host__ __device__ inline uint32_t gemm_w_region(int stage_bytes) { return (stage_bytes + 1023u) & ~1023u; }
-__host__ __device__ inline uint32_t gemm_stage_bytes(int token_tile, int stage_bytes) {
-  return static_cast<uint32_t>(token_tile) * 256u + gemm_w_region(stage_bytes);
+__host__ __device__ inline uint32_t gemm_w_region(int bytes) { return (bytes + 1023u) & ~1023u; }
+// Shared memory of one pipeline stage: the token tile (T rows x ks*128 K x 2 B)
+// then the packed weights of ks groups.
+__host__ __device__ inline uint32_t gemm_stage_bytes(int token_tile, int group_bytes, int ks) {
+  return static_cast<uint32_t>(token_tile) * 256u * ks + gemm_w_region(group_bytes * ks);
 }
 
 struct WorkItem {
@@ -87,8 +91,9 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i,
   w.nrows = ch.nrows;
   w.tile = tile;
   w.split_idx = s;
-  w.ks0 = static_cast<int>(static_cast<int64_t>(p.k_stages) * s / p.split);
-  w.ks1 = static_cast<int>(static_cast<int64_t>(p.k_stages) * (s + 1) / p.split);
+  const int k_units = p.k_groups / p.ks;
+  w.ks0 = static_cast<int>(static_cast<int64_t>(k_units) * s / p.split);
+  w.ks1 = static_cast<int>(static_cast<int64_t>(k_units) * (s + 1) / p.split);
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int32_t* status) {
@@ -168,6 +173,18 @@ __device__ __forceinline__ void dequant_int8_row(const uint4 (&pk)[8], uint32_t 
   }
 }
 
+// The NK MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
+// between two tcgen05.mma instructions roughly triples their issue cost.  The
+// A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
+// 128-byte swizzled rows, with each 64-K block 1024 bytes after the previous.
+template <int NK>
+__device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+  for (int kk = 0; kk < NK; ++kk)
+    mma_ts_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2),
+               idesc, kk > 0 ? 1u : acc0);
+}
+
 __device__ __forceinline__ float silu_dev(float g) { return g / (1.0f + __expf(-g)); }
 
 // Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values with
@@ -208,17 +225,19 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 // ---------------------------------------------------------------------------
 // The kernel.  TMEM columns: each of the two MMA issuers owns acc_bufs fp32
 // accumulators of T columns (issuer i, buffer b at [(i*acc_bufs + b) * T]);
-// the A stages follow at a_col0.
+// the A stages (64*ks columns each) follow at a_col0.
 // ---------------------------------------------------------------------------
 template <bool INT4, bool BF16S>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    qmoe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int T = p.token_tile;
-  const uint32_t b_bytes = static_cast<uint32_t>(T) * 256u;
-  const uint32_t st_bytes = gemm_stage_bytes(T, p.stage_bytes);
+  const int KS = p.ks;
+  const uint32_t b_bytes = static_cast<uint32_t>(T) * 256u * KS;
+  const uint32_t st_bytes = gemm_stage_bytes(T, p.stage_bytes, KS);
+  // NS and NA are even (the host plan guarantees it): stage g always lands in a
+  // slot of parity g & 1, so each parity role sees every phase of its barriers.
   const int NS = p.smem_stages, NA = p.a_stages, ACCB = p.acc_bufs;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * st_bytes);
@@ -256,7 +275,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&tmap_b);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -272,7 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == kProducerWarp || warp == kProducerWarp2) {
     // ------------------------------------------------------------ TMA producers
     // Two threads (warps 4 and 7) issue the copies of even and odd stages: issuing
-    // one stage's bulk and tensor copies takes one thread several hundred cycles.
+    // one stage's copies takes one thread a few hundred cycles.
     if (lane == 0) {
       const int id = (warp == kProducerWarp) ? 0 : 1;
       const uint64_t pol_w = policy_evict_first();
@@ -283,9 +301,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
         decode_item(p, nch, i, it);
+        const int64_t unit_w = static_cast<int64_t>(p.stage_bytes) * KS;
         const uint8_t* wsrc =
-            p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_stages * static_cast<int64_t>(p.stage_bytes);
-        const uint32_t tx = static_cast<uint32_t>(p.stage_bytes) + b_bytes;
+            p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_groups * static_cast<int64_t>(p.stage_bytes);
+        // the chunk's rows of one stage of the pre-staged B operand: one contiguous run
+        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u * KS;
+        const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256 * KS;
+        const uint32_t tx = static_cast<uint32_t>(unit_w) + b_run;
         for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, st.next(NS)) {
           if ((g & 1) != id) continue;
           if (!mbar_wait(smem_u32(empty + st.idx), st.phase ^ 1u, abort_flag, 128)) {
@@ -296,12 +318,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = smem_u32(full + st.idx);
           mbar_arrive_expect_tx(fb, tx);
           if (!(p.fault_injection == 1 && blockIdx.x == 0 && g == 0)) {  // injected: armed, never filled
-            tma_load_1d(smem_u32(sp + b_bytes), wsrc + static_cast<int64_t>(ks) * p.stage_bytes, p.stage_bytes, fb,
-                        pol_w);
-            // the stage's B tile as two copies of box {64 K, T rows} (one per 64-K half), landing
-            // as [half][row][128 B]; rows past the chunk (or past the buffer, zero-filled) go unused
-            tma_load_2d(smem_u32(sp), &tmap_b, ks * kStageK, it.row0, fb, pol_b);
-            tma_load_2d(smem_u32(sp + T * 128), &tmap_b, ks * kStageK + 64, it.row0, fb, pol_b);
+            tma_load_1d(smem_u32(sp + b_bytes), wsrc + ks * unit_w, static_cast<uint32_t>(unit_w), fb, pol_w);
+            tma_load_1d(smem_u32(sp), bsrc + ks * p.b_unit_stride, b_run, fb, pol_b);
           }
         }
       }
@@ -342,17 +360,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
-          // descriptor of the stage's first K step; later K steps only move its start address
-          const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes));
-          const uint64_t atom16 = static_cast<uint64_t>((T * 128) >> 4);
-          // The MMAs of a stage go out as one branch-free sequence: a branch between
-          // two tcgen05.mma instructions roughly triples their issue cost.
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t koff16 = (kk >> 2) * atom16 + static_cast<uint64_t>((kk & 3) * 2);
-            mma_ts_f16(d_tmem, a_tmem + static_cast<uint32_t>(kk * 8), bdesc0 + koff16, idesc, kk > 0 ? 1u : acc0);
-          }
+          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64 * KS);
+          // B tile layout [8-row group][64-K block][8 rows][128 B]: 8-row groups are
+          // 2048*ks bytes apart; later K steps only move the start address
+          const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes), 2048u * KS);
+          if (KS == 2)
+            mma_stage<16>(d_tmem, a_tmem, bdesc0, idesc, acc0);
+          else
+            mma_stage<8>(d_tmem, a_tmem, bdesc0, idesc, acc0);
           acc0 = 1u;
           mma_commit(smem_u32(empty + fr.idx));
           mma_commit(smem_u32(aempty + ar.idx));
@@ -384,29 +399,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag));
         if (!ok) break;
         const uint8_t* wst = smem + fr.idx * st_bytes + b_bytes;
-        uint32_t out[64];
-        if (INT4) {
-          uint4 pk[4];
+        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 * KS);
+        for (int j = 0; j < KS; ++j) {  // one 128-K group at a time: 64 TMEM columns each
+          const uint8_t* wj = wst + j * p.stage_bytes;
+          uint32_t out[64];
+          if (INT4) {
+            uint4 pk[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
-          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-          dequant_int4_row<BF16S>(pk, sbits, out);
-        } else {
-          uint4 pk[8];
+            for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wj + (c * 128 + row) * 16);
+            const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wj + 8192 + row * 2);
+            if (j == KS - 1) {  // the stage's packed bytes are all in registers
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
+            }
+            dequant_int4_row<BF16S>(pk, sbits, out);
+          } else {
+            uint4 pk[8];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + (c * 128 + row) * 16);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-          dequant_int8_row(pk, out);
+            for (int c = 0; c < 8; ++c) pk[c] = *reinterpret_cast<const uint4*>(wj + (c * 128 + row) * 16);
+            if (j == KS - 1) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
+            }
+            dequant_int8_row(pk, out);
+          }
+          if (j == 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ar.idx), ar.phase ^ 1u, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st_32x32b_x32<0>(ta + static_cast<uint32_t>(64 * j), out);
+          tmem_st_32x32b_x32<32>(ta + static_cast<uint32_t>(64 * j + 32), out);
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ar.idx), ar.phase ^ 1u, abort_flag));
         if (!ok) break;
-        tc_fence_after();
-        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64);
-        tmem_st_32x32b_x32<0>(ta, out);
-        tmem_st_32x32b_x32<32>(ta + 32, out);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -471,12 +496,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <bool INT4, bool BF16S>
-cudaError_t launch_gemm_t(const CUtensorMap* tmap_b, const GemmParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_t(const GemmParams& p, int grid, cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p);
   cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<INT4, BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_kernel(qmoe_gemm_kernel<INT4, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, *tmap_b, p);
+  return launch_kernel(qmoe_gemm_kernel<INT4, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, p);
 }
 
 }  // namespace qmoe

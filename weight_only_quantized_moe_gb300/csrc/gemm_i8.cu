@@ -4,8 +4,8 @@
 
 namespace qmoe {
 
-cudaError_t launch_gemm_i8(const CUtensorMap* tmap_b, const GemmParams& p, int grid, cudaStream_t stream) {
-  return launch_gemm_t<false, false>(tmap_b, p, grid, stream);
+cudaError_t launch_gemm_i8(const GemmParams& p, int grid, cudaStream_t stream) {
+  return launch_gemm_t<false, false>(p, grid, stream);
 }
 
 }  // namespace qmoe

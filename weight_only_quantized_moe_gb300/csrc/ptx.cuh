@@ -7,7 +7,6 @@
 #pragma once
 
 #include <cstdint>
-#include <cuda.h>
 
 namespace qmoe {
 
@@ -125,19 +124,6 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       : "memory");
 }
 
-// 2-D tiled copy through a tensor map; x is the innermost coordinate (elements).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -200,13 +186,13 @@ __host__ __device__ __forceinline__ uint32_t make_idesc_m128(uint32_t n, bool bf
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart.  `saddr` may be offset by multiples of 32 bytes inside a
-// 1024-byte aligned swizzle atom to step along K.
-__device__ __forceinline__ uint64_t make_sdesc_k_sw128(uint32_t saddr) {
+// `sbo` bytes apart (a multiple of 1024).  `saddr` may be offset by multiples
+// of 32 bytes inside a 1024-byte aligned swizzle atom to step along K.
+__device__ __forceinline__ uint64_t make_sdesc_k_sw128(uint32_t saddr, uint32_t sbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
   d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused for swizzled K-major)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;  // stride byte offset: next 8-row group
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                   // swizzle mode: 128 B
   return d;
