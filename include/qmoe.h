@@ -116,11 +116,6 @@ typedef struct {
  *   token_tile      largest number of token rows one GEMM work item carries
  *                   (multiple of 16, 16..128).  Other values give
  *                   QMOE_ERR_INVALID_ARG.
- *   stage_groups    128-K quantization groups per GEMM pipeline stage (1 or
- *                   2; 0 = automatic).  2 needs an even number of groups
- *                   along K in both GEMMs and room for the deeper stages,
- *                   else QMOE_ERR_INVALID_ARG; a split finer than the
- *                   two-group stages also gives QMOE_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t split1;
@@ -132,8 +127,7 @@ typedef struct {
    * bounded waits give up after about a second, record QMOE_ERR_TIMEOUT and the
    * kernel exits with the CUDA context intact (the output is then garbage). */
   int32_t fault_injection;
-  int32_t stage_groups;
-  int32_t reserved[3];
+  int32_t reserved[4];
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */

@@ -97,8 +97,7 @@ qmoe_status validate_layer_dims(const qmoe_layer* L) {
 struct Plan {
   int64_t M = 0, P = 0;
   int k = 0;
-  int T = 0, acc_bufs = 0, a_col0 = 0, stage_bytes = 0;
-  int ks1 = 1, ks2 = 1, ns1 = 0, ns2 = 0, na1 = 0, na2 = 0;  // per GEMM: groups per stage, smem / TMEM A stages
+  int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -147,43 +146,31 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   }
   const bool int4 = L->qt == QMOE_INT4_GROUP;
   p.T = T;
-  // TMEM (512 columns): one fp32 accumulator of T columns per MMA issuer (two),
-  // double buffered when that leaves room for two 64-column A stages
-  p.acc_bufs = (4 * T + 2 * 64 <= 512) ? 2 : 1;
-  p.a_col0 = 2 * p.acc_bufs * T;
   p.stage_bytes = int4 ? kInt4StageBytes : kInt8StageBytes;
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
-  // Pipeline stages of two quantization groups halve the per-stage barrier and
-  // MMA-issue overhead; they are used when K has an even number of groups and
-  // at least four such stages fit in shared memory.
-  // Both rings have an even number of slots: the even and odd stages go to two
-  // separate producer / dequant / MMA roles, and with an even ring every slot is
-  // only ever used by one of them, so each waiter sees every phase of its
-  // barriers.  (With an odd ring a role would see every other use of a slot and
-  // a parity wait could pass on a phase two behind.)
-  auto smem_stages = [&](int ks) {
-    const size_t per = static_cast<size_t>(T) * 256 * ks + ((static_cast<size_t>(p.stage_bytes) * ks + 1023) & ~size_t(1023));
-    return static_cast<int>(std::min<size_t>(12, (kMaxDynSmem - 2048) / per)) & ~1;
-  };
-  auto a_stages = [&](int ks) { return std::min(8, (512 - p.a_col0) / (64 * ks)) & ~1; };
-  const int forced_ks = (o != nullptr) ? o->stage_groups : 0;
-  if (forced_ks < 0 || forced_ks > 2) return QMOE_ERR_INVALID_ARG;
-  if (forced_ks == 2 && (p.kst1 % 2 != 0 || p.kst2 % 2 != 0 || smem_stages(2) < 2 || a_stages(2) < 2))
-    return QMOE_ERR_INVALID_ARG;
-  auto pick = [&](int kst, int* ks, int* ns, int* na) {
-    if (forced_ks != 0)
-      *ks = forced_ks;
-    else
-      *ks = (kst % 2 == 0 && smem_stages(2) >= 4 && a_stages(2) >= 2) ? 2 : 1;
-    *ns = smem_stages(*ks);
-    *na = a_stages(*ks);
-  };
-  pick(p.kst1, &p.ks1, &p.ns1, &p.na1);
-  pick(p.kst2, &p.ks2, &p.ns2, &p.na2);
-  if (p.ns1 < 2 || p.ns2 < 2 || p.na1 < 2 || p.na2 < 2) return QMOE_ERR_UNSUPPORTED;
+  // MMA issuers: two (even / odd stages, one accumulator each) while the token
+  // tile is small and one thread's MMA issue rate is the limit; one when the
+  // tile is large and the tensor pipe is, which leaves TMEM for two
+  // accumulator buffers so the epilogue overlaps the next item's MMAs.
+  p.issuers = (T <= 64) ? 2 : 1;
+  // TMEM (512 columns): accumulators (issuers x buffers x T columns), then the
+  // 64-column A slots, at least two of them
+  p.acc_bufs = (p.issuers * 2 * T + 2 * 64 <= 512) ? 2 : 1;
+  p.a_col0 = p.issuers * p.acc_bufs * T;
+  // Rings of an even number of slots: the even and odd stages go to separate
+  // producer and dequant roles (and MMA issuers), and with an even ring every
+  // slot is only ever used by one of them, so each waiter sees every phase of
+  // its barriers.  (With an odd ring a role would see every other use of a slot
+  // and a parity wait could pass on a phase two behind.)
+  p.ab_stages = std::min(8, (512 - p.a_col0) / 64) & ~1;
+  const size_t wslot = (static_cast<size_t>(p.stage_bytes) + 1023) & ~size_t(1023);
+  const size_t b_bytes = static_cast<size_t>(p.ab_stages) * T * 256;
+  if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return QMOE_ERR_UNSUPPORTED;
+  p.w_stages = static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
+  if (p.w_stages < 2 || p.ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
   // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
   p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
   p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
@@ -191,8 +178,8 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   // expected chunks for the split heuristic (uniform routing)
   const double d = L->E * (1.0 - std::pow(1.0 - 1.0 / L->E, static_cast<double>(P)));
   const int64_t est_chunks = std::max<int64_t>(std::max<int64_t>(1, static_cast<int64_t>(std::ceil(d))), (P + T - 1) / T);
-  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1 / p.ks1, sms, 0.8);
-  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2 / p.ks2, sms, 0.97);
+  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, 0.8);
+  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, 0.97);
   if (o != nullptr && o->split1 != 0) {
     if (o->split1 < 1 || o->split1 > 64 || o->split1 > p.kst1) return QMOE_ERR_INVALID_ARG;
     p.S1 = o->split1;
@@ -201,18 +188,7 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     if (o->split2 < 1 || o->split2 > 64 || o->split2 > p.kst2) return QMOE_ERR_INVALID_ARG;
     p.S2 = o->split2;
   }
-  // a forced split finer than the stages of two groups falls back to one-group stages
-  if (forced_ks == 2 && (p.S1 > p.kst1 / 2 || p.S2 > p.kst2 / 2)) return QMOE_ERR_INVALID_ARG;
-  if (p.S1 > p.kst1 / p.ks1) {
-    p.ks1 = 1;
-    p.ns1 = smem_stages(1);
-    p.na1 = a_stages(1);
-  }
-  if (p.S2 > p.kst2 / p.ks2) {
-    p.ks2 = 1;
-    p.ns2 = smem_stages(1);
-    p.na2 = a_stages(1);
-  }
+
   size_t off = 0;
   p.off_status = off;   off += 256;
   p.off_sorted = off;   off += al256(p.cap * 4);
@@ -290,15 +266,15 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   launched += (err == cudaSuccess);
   rec(2);
   if (err == cudaSuccess) {
-    err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, pl.ks1, xg, xscale,
-                        sms, stream);
+    err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, sms,
+                        stream);
     launched += (err == cudaSuccess);
   }
   rec(3);
   GemmParams g1{};
   g1.w = static_cast<const uint8_t*>(L->w13);
   g1.b = static_cast<const uint8_t*>(xg);
-  g1.b_unit_stride = pl.cap * 256 * pl.ks1;
+  g1.b_unit_stride = pl.cap * 256;
   g1.row_scale = int4 ? nullptr : L->s13;
   g1.col_scale = xscale;
   g1.chunks = chunks;
@@ -308,13 +284,13 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.status = status;
   g1.n_tiles = pl.n_tiles1;
   g1.k_groups = pl.kst1;
-  g1.ks = pl.ks1;
   g1.split = pl.S1;
   g1.token_tile = pl.T;
   g1.acc_bufs = pl.acc_bufs;
   g1.a_col0 = pl.a_col0;
-  g1.a_stages = pl.na1;
-  g1.smem_stages = pl.ns1;
+  g1.issuers = pl.issuers;
+  g1.w_stages = pl.w_stages;
+  g1.ab_stages = pl.ab_stages;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -334,14 +310,11 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   GemmParams g2 = g1;
   g2.w = static_cast<const uint8_t*>(L->w2);
   g2.b = static_cast<const uint8_t*>(inter16);
-  g2.b_unit_stride = pl.cap * 256 * pl.ks2;
+  g2.b_unit_stride = pl.cap * 256;
   g2.row_scale = int4 ? nullptr : L->s2;
   g2.col_scale = iscale;
   g2.n_tiles = pl.n_tiles2;
   g2.k_groups = pl.kst2;
-  g2.ks = pl.ks2;
-  g2.a_stages = pl.na2;
-  g2.smem_stages = pl.ns2;
   g2.split = pl.S2;
   g2.epi_mode = kEpiWeightedPairs;
   g2.fault_injection = 0;
@@ -367,7 +340,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(7);
   rec(8);
   if (err == cudaSuccess) {
-    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, pl.ks2, inter16, iscale, sms, stream);
+    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(9);

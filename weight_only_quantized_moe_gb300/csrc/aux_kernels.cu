@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                   const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_post_padded,
                   const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B, int64_t cap,
-                  int32_t ks, uint8_t* __restrict__ xg, float* __restrict__ xscale) {
+                  uint8_t* __restrict__ xg, float* __restrict__ xscale) {
   pdl_launch_dependents();
   pdl_wait();
   const int total = *num_post_padded;
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     const int p = sorted_ids[row];
     if (p >= P) {
       for (int c = lane; c < H / 8; c += 32)
-        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, ks, cap)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = make_uint4(0, 0, 0, 0);
       if (lane == 0) xscale[row] = 1.0f;
       continue;
     }
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kGatherThreads)
         const uint4 v = __ldg(s4 + c);
         uint16_t e[8];
         *reinterpret_cast<uint4*>(e) = v;
-        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, ks, cap)) = scale_to_f16x8<BF16>(e, inv);
+        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
       }
     } else {
       const int4* pr4 = reinterpret_cast<const int4*>(perm13 + static_cast<int64_t>(expert_ids[row / B]) * H);
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kGatherThreads)
         const int4 ka = __ldg(pr4 + 2 * c), kb = __ldg(pr4 + 2 * c + 1);
         uint16_t e[8] = {__ldg(src + ka.x), __ldg(src + ka.y), __ldg(src + ka.z), __ldg(src + ka.w),
                          __ldg(src + kb.x), __ldg(src + kb.y), __ldg(src + kb.z), __ldg(src + kb.w)};
-        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, ks, cap)) = scale_to_f16x8<BF16>(e, inv);
+        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
       }
     }
   }
@@ -277,13 +277,13 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, int32_t ks, void* xg, float* xscale,
-                          int num_sms, cudaStream_t stream) {
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
+                          cudaStream_t stream) {
   const int64_t want = (cap_rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
   auto kern = bf16 ? gather_kernel<true> : gather_kernel<false>;
   return launch_kernel(kern, dim3(grid), dim3(kGatherThreads), 0, stream, true, static_cast<const uint16_t*>(x),
-                       sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block, cap_rows, ks,
+                       sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block, cap_rows,
                        static_cast<uint8_t*>(xg), xscale);
 }
 
@@ -329,7 +329,7 @@ constexpr int kRescaleThreads = 256;
 
 __global__ void __launch_bounds__(kRescaleThreads)
     inter_rescale_kernel(const float* __restrict__ inter32, const int32_t* __restrict__ num_post_padded,
-                         const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I, int64_t cap, int32_t ks,
+                         const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I, int64_t cap,
                          uint8_t* __restrict__ inter16, float* __restrict__ iscale) {
   __shared__ float red[kRescaleThreads / 32];
   pdl_launch_dependents();
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kRescaleThreads)
   for (int row = blockIdx.x; row < total; row += gridDim.x) {
     if (sorted_ids[row] >= P) {  // uniform across the CTA
       for (int c = threadIdx.x; c < I / 8; c += kRescaleThreads)
-        *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, ks, cap)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, cap)) = make_uint4(0, 0, 0, 0);
       if (threadIdx.x == 0) iscale[row] = 1.0f;
       continue;
     }
@@ -365,17 +365,17 @@ __global__ void __launch_bounds__(kRescaleThreads)
       o.y = static_cast<uint32_t>(f16_bits(a.z * sc.y)) | (static_cast<uint32_t>(f16_bits(a.w * sc.y)) << 16);
       o.z = static_cast<uint32_t>(f16_bits(b.x * sc.y)) | (static_cast<uint32_t>(f16_bits(b.y * sc.y)) << 16);
       o.w = static_cast<uint32_t>(f16_bits(b.z * sc.y)) | (static_cast<uint32_t>(f16_bits(b.w * sc.y)) << 16);
-      *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, ks, cap)) = o;
+      *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, cap)) = o;
     }
   }
 }
 
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
-                                 int32_t P, int32_t I, int64_t cap_rows, int32_t ks, void* inter16, float* iscale,
-                                 int num_sms, cudaStream_t stream) {
+                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
+                                 cudaStream_t stream) {
   const int grid = static_cast<int>(cap_rows < 8LL * num_sms ? (cap_rows > 0 ? cap_rows : 1) : 8LL * num_sms);
   return launch_kernel(inter_rescale_kernel, dim3(grid), dim3(kRescaleThreads), 0, stream, true, inter32,
-                       num_post_padded, sorted_ids, P, I, cap_rows, ks, static_cast<uint8_t*>(inter16), iscale);
+                       num_post_padded, sorted_ids, P, I, cap_rows, static_cast<uint8_t*>(inter16), iscale);
 }
 
 // ---------------------------------------------------------------------------

@@ -25,19 +25,28 @@
 //     the MMA's A operand straight from tensor memory; dequantized weights
 //     never touch shared memory, which carries only the packed bytes and the
 //     token tile.
-//   * a pipeline stage covers `ks` (1 or 2) quantization groups of 128 K.  Its
-//     packed weights (contiguous blocks per 128x128 tile, scales appended) and
-//     its token tile arrive as two 1-D bulk TMA copies: the producers of the
-//     B operand (gather, rescale) store it pre-staged, per stage and 8-row
-//     group, in the 128-byte-swizzled K-major layout the MMA's shared-memory
-//     descriptor reads, so a chunk's tile for one stage is one contiguous run.
-//   * warp roles: two TMA producer threads (warps 4, 7), two MMA-issuing
-//     threads (warps 5, 6) and two dequant warpgroups (warps 8-15), each pair
-//     taking the even and the odd pipeline stages; one epilogue warpgroup
-//     (warps 0-3) reads the fp32 accumulators out of TMEM.  Issuing a stage's
-//     copies or MMAs costs one thread several hundred cycles, so the stage
-//     rate at decode sizes needs two issuers of each.  A persistent grid walks
-//     the work items.
+//   * one pipeline stage = one 128-K quantization group.  Two rings: packed
+//     weights (deep: they stream from HBM) and token tiles (each slot paired
+//     with a TMEM A slot; token tiles come from L2).  Both arrive by 1-D bulk
+//     TMA copies: the producers of the B operand (gather, rescale) store it
+//     pre-staged, per 128-K group and 8-row group, in the 128-byte-swizzled
+//     K-major layout the MMA's shared-memory descriptor reads, so a chunk's
+//     tile for one stage is one contiguous run.
+//   * warp roles (24 warps): two TMA producer threads (warps 4, 7) and two
+//     dequant sets of 8 warps (warps 8-15, 16-23) take the even and the odd
+//     stages; each dequant warp converts half of a stage row for 32 rows (one
+//     TMEM lane quadrant).  The MMAs are issued by two threads (warps 5, 6;
+//     even / odd stages, each into its own accumulator) when the token tile is
+//     small and the MMA issue rate is the limit, and by one thread (warp 5)
+//     when it is large and the tensor pipe is, so that two accumulator buffers
+//     fit in TMEM.  Warps 0-3 are the epilogue.  A persistent grid walks the
+//     work items.
+//   * barriers per stage: the dequant set waits for the weights and the token
+//     tile, releases the weight slot, writes A and signals it; the issuer
+//     waits for that one signal, issues the stage's MMAs and commits one
+//     release of the token-tile/A slot.  Every ring has an even number of
+//     slots, so each slot belongs to one parity role, and each role sees every
+//     phase of the barriers it waits on.
 //   * every mbarrier wait is bounded (see ptx.cuh); a wait that gives up
 //     records QMOE_ERR_TIMEOUT in the status word and the CTA winds down after
 //     waiting for its own copies and MMAs, then frees its TMEM.
@@ -51,19 +60,20 @@
 
 namespace qmoe {
 
-constexpr int kGemmThreads = 512;
+constexpr int kGemmThreads = 768;
 constexpr int kProducerWarp = 4;
 constexpr int kProducerWarp2 = 7;
 constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 8;  // warps 8..15: two warpgroups
+constexpr int kDequantWarp0 = 8;  // warps 8..23: two sets of 8
+constexpr int kDequantWarps = 8;  // per set
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarrierBytes = 1024;
 
-__host__ __device__ inline uint32_t gemm_w_region(int bytes) { return (bytes + 1023u) & ~1023u; }
-// Shared memory of one pipeline stage: the token tile (T rows x ks*128 K x 2 B)
-// then the packed weights of ks groups.
-__host__ __device__ inline uint32_t gemm_stage_bytes(int token_tile, int group_bytes, int ks) {
-  return static_cast<uint32_t>(token_tile) * 256u * ks + gemm_w_region(group_bytes * ks);
+__host__ __device__ inline uint32_t gemm_w_slot(int group_bytes) { return (group_bytes + 1023u) & ~1023u; }
+// Dynamic shared memory: weight ring, token-tile ring, barriers (+1 KB alignment slack).
+__host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int ab_stages, int token_tile) {
+  return 1024 + static_cast<size_t>(w_stages) * gemm_w_slot(group_bytes) +
+         static_cast<size_t>(ab_stages) * token_tile * 256 + kBarrierBytes;
 }
 
 struct WorkItem {
@@ -91,9 +101,8 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i,
   w.nrows = ch.nrows;
   w.tile = tile;
   w.split_idx = s;
-  const int k_units = p.k_groups / p.ks;
-  w.ks0 = static_cast<int>(static_cast<int64_t>(k_units) * s / p.split);
-  w.ks1 = static_cast<int>(static_cast<int64_t>(k_units) * (s + 1) / p.split);
+  w.ks0 = static_cast<int>(static_cast<int64_t>(p.k_groups) * s / p.split);
+  w.ks1 = static_cast<int>(static_cast<int64_t>(p.k_groups) * (s + 1) / p.split);
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int32_t* status) {
@@ -108,8 +117,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-// Dequantization of one 128-K stage of one weight row into 64 TMEM columns
-// (column c holds K elements 2c (low half) and 2c+1 (high half)), as f16.
+// Dequantization of half a stage row (64 K) into 32 TMEM columns (column c
+// holds K elements 2c (low half) and 2c+1 (high half)), as f16.
 // ---------------------------------------------------------------------------
 // int4: packed chunk c (16 bytes) of the row holds K = 32c .. 32c+31; in word j
 // of the chunk, nibble i holds K = 32c+8j+2i and nibble i+4 holds K = 32c+8j+2i+1.
@@ -118,20 +127,20 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // of their half, where (nibble << 4) | 0x6400 is 1024 + 16q and
 // fma(v, 1/16, -72) = q - 8 exactly, so one shift per word serves i = 2, 3.
 // One multiply by the group scale rounds once (exact for bf16 scales).
+// `pk` holds chunks 2h and 2h+1 of the row for half h.
 template <bool BF16S>
-__device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[64]) {
+__device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t (&out)[32]) {
   const uint32_t bias_bits = 0x64086408u;                        // 1032
   const uint32_t sixteenth = 0x2C002C00u, m72 = 0xD480D480u;     // 1/16, -72
   uint16_t s16;
   if (BF16S) {
-    const __half h = __float2half_rn(__uint_as_float(sbits << 16));
-    s16 = *reinterpret_cast<const uint16_t*>(&h);
+    s16 = __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
   } else {
     s16 = static_cast<uint16_t>(sbits);
   }
   const uint32_t s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -154,11 +163,12 @@ __device__ __forceinline__ void dequant_int4_row(const uint4 (&pk)[4], uint32_t 
 
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
 // per-row scale is applied to the fp32 accumulator in the epilogue, so the
-// conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.
-__device__ __forceinline__ void dequant_int8_row(const uint4 (&pk)[8], uint32_t (&out)[64]) {
+// conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.  `pk` holds
+// chunks 4h .. 4h+3 of the row for half h.
+__device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t (&out)[32]) {
   const uint32_t bias = 0x64806480u;  // 1152
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -173,19 +183,18 @@ __device__ __forceinline__ void dequant_int8_row(const uint4 (&pk)[8], uint32_t 
   }
 }
 
-// The NK MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
+// The 8 MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
 // between two tcgen05.mma instructions roughly triples their issue cost.  The
 // A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
-// 128-byte swizzled rows, with each 64-K block 1024 bytes after the previous.
-template <int NK>
+// 128-byte swizzled rows, the second 64-K block 1024 bytes after the first.
 __device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
 #pragma unroll
-  for (int kk = 0; kk < NK; ++kk)
+  for (int kk = 0; kk < 8; ++kk)
     mma_ts_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2),
                idesc, kk > 0 ? 1u : acc0);
 }
 
-__device__ __forceinline__ float silu_dev(float g) { return g / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_dev(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values with
 // every scale applied).  Modes: SiLU(gate)*up into the fp32 intermediate
@@ -223,9 +232,10 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  TMEM columns: each of the two MMA issuers owns acc_bufs fp32
-// accumulators of T columns (issuer i, buffer b at [(i*acc_bufs + b) * T]);
-// the A stages (64*ks columns each) follow at a_col0.
+// The kernel.  Shared memory: weight ring (w_stages slots), token-tile ring
+// (ab_stages slots of T rows), barriers.  TMEM columns: issuer i owns acc_bufs
+// fp32 accumulators of T columns at [(i*acc_bufs + b) * T]; token-tile slot j
+// pairs with the 64-column A slot at a_col0 + 64j.
 // ---------------------------------------------------------------------------
 template <bool INT4, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
@@ -233,18 +243,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int T = p.token_tile;
-  const int KS = p.ks;
-  const uint32_t b_bytes = static_cast<uint32_t>(T) * 256u * KS;
-  const uint32_t st_bytes = gemm_stage_bytes(T, p.stage_bytes, KS);
-  // NS and NA are even (the host plan guarantees it): stage g always lands in a
-  // slot of parity g & 1, so each parity role sees every phase of its barriers.
-  const int NS = p.smem_stages, NA = p.a_stages, ACCB = p.acc_bufs;
+  const int NW = p.w_stages, NB = p.ab_stages, ACCB = p.acc_bufs, NI = p.issuers;
+  const uint32_t wslot = gemm_w_slot(p.stage_bytes);
+  const uint32_t bslot = static_cast<uint32_t>(T) * 256u;
+  uint8_t* wring = smem;
+  uint8_t* bring = smem + NW * wslot;
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * st_bytes);
-  uint64_t* empty = full + NS;
-  uint64_t* afull = empty + NS;
-  uint64_t* aempty = afull + NA;
-  uint64_t* accfull = aempty + NA;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(bring + NB * bslot);
+  uint64_t* wempty = wfull + NW;
+  uint64_t* bfull = wempty + NW;
+  uint64_t* afull = bfull + NB;
+  uint64_t* sfree = afull + NB;  // token-tile slot and its A slot are free again
+  uint64_t* accfull = sfree + NB;
   uint64_t* accempty = accfull + 2;
   uint64_t* drain = accempty + 2;  // one per MMA issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
@@ -254,16 +264,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 4 + 1);  // 4 dequant warps + 1 MMA commit
+    for (int s = 0; s < NW; ++s) {
+      mbar_init(smem_u32(wfull + s), 1);
+      mbar_init(smem_u32(wempty + s), kDequantWarps);
     }
-    for (int j = 0; j < NA; ++j) {
-      mbar_init(smem_u32(afull + j), 4);
-      mbar_init(smem_u32(aempty + j), 1);
+    for (int j = 0; j < NB; ++j) {
+      mbar_init(smem_u32(bfull + j), 1);
+      mbar_init(smem_u32(afull + j), kDequantWarps);
+      mbar_init(smem_u32(sfree + j), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(accfull + b), 2);   // one commit from each MMA issuer per item
+      mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
       mbar_init(smem_u32(accempty + b), 4);  // the 4 epilogue warps
     }
     mbar_init(smem_u32(drain), 1);
@@ -289,55 +300,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 
   if (warp == kProducerWarp || warp == kProducerWarp2) {
     // ------------------------------------------------------------ TMA producers
-    // Two threads (warps 4 and 7) issue the copies of even and odd stages: issuing
-    // one stage's copies takes one thread a few hundred cycles.
+    // Two threads (warps 4 and 7) issue the copies of even and odd stages.
     if (lane == 0) {
       const int id = (warp == kProducerWarp) ? 0 : 1;
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
-      Ring st;
+      Ring wr, br;
       int g = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
         decode_item(p, nch, i, it);
-        const int64_t unit_w = static_cast<int64_t>(p.stage_bytes) * KS;
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_groups * static_cast<int64_t>(p.stage_bytes);
         // the chunk's rows of one stage of the pre-staged B operand: one contiguous run
-        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u * KS;
-        const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256 * KS;
-        const uint32_t tx = static_cast<uint32_t>(unit_w) + b_run;
-        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, st.next(NS)) {
+        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u;
+        const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256;
+        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, wr.next(NW), br.next(NB)) {
           if ((g & 1) != id) continue;
-          if (!mbar_wait(smem_u32(empty + st.idx), st.phase ^ 1u, abort_flag, 128)) {
+          const bool inject = p.fault_injection == 1 && blockIdx.x == 0 && g == 0;  // armed, never filled
+          if (!mbar_wait(smem_u32(wempty + wr.idx), wr.phase ^ 1u, abort_flag, 128)) {
             ok = false;
             break;
           }
-          uint8_t* sp = smem + st.idx * st_bytes;
-          const uint32_t fb = smem_u32(full + st.idx);
-          mbar_arrive_expect_tx(fb, tx);
-          if (!(p.fault_injection == 1 && blockIdx.x == 0 && g == 0)) {  // injected: armed, never filled
-            tma_load_1d(smem_u32(sp + b_bytes), wsrc + ks * unit_w, static_cast<uint32_t>(unit_w), fb, pol_w);
-            tma_load_1d(smem_u32(sp), bsrc + ks * p.b_unit_stride, b_run, fb, pol_b);
+          const uint32_t wb = smem_u32(wfull + wr.idx);
+          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(p.stage_bytes));
+          if (!inject)
+            tma_load_1d(smem_u32(wring + wr.idx * wslot), wsrc + static_cast<int64_t>(ks) * p.stage_bytes,
+                        static_cast<uint32_t>(p.stage_bytes), wb, pol_w);
+          // the token-tile slot and its TMEM A slot are free once the MMAs of the
+          // slot's previous stage completed
+          if (!mbar_wait(smem_u32(sfree + br.idx), br.phase ^ 1u, abort_flag, 128)) {
+            ok = false;
+            break;
           }
+          const uint32_t bb = smem_u32(bfull + br.idx);
+          mbar_arrive_expect_tx(bb, b_run);
+          if (!inject) tma_load_1d(smem_u32(bring + br.idx * bslot), bsrc + ks * p.b_unit_stride, b_run, bb, pol_b);
         }
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
-      // wait for every copy this thread may still have in flight into the CTA's shared memory
-      // (its stages among the last NS before the first one it did not issue)
-      for (int j = (g > NS ? g - NS : 0); j < g; ++j)
-        if ((j & 1) == id) mbar_wait_drain(smem_u32(full + (j % NS)), (j / NS) & 1);
+      // wait for every copy this thread may still have in flight into the CTA's shared
+      // memory: its stages among the last NW (weights) and NB (token tiles) it issued
+      for (int j = (g > NW ? g - NW : 0); j < g; ++j)
+        if ((j & 1) == id) mbar_wait_drain(smem_u32(wfull + (j % NW)), (j / NW) & 1);
+      for (int j = (g > NB ? g - NB : 0); j < g; ++j)
+        if ((j & 1) == id) mbar_wait_drain(smem_u32(bfull + (j % NB)), (j / NB) & 1);
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issuers
-    // Two threads (warps 5 and 6) issue the MMAs of even and odd stages into
-    // their own accumulators: one thread's issue rate, with the waits and
-    // commits around each stage, is below what the tensor core accepts at small
-    // N, and the two run in parallel.
-    if (lane == 0) {
-      const int id = warp - kMmaWarp;
-      Ring fr, ar;
+    // With two issuers (small token tiles) each takes every other stage into its
+    // own accumulator: one thread's issue rate, with the wait and commit around
+    // each stage, is below what the tensor core accepts at small N.  With one
+    // (large tiles) warp 5 takes every stage.
+    const int id = warp - kMmaWarp;
+    if (lane == 0 && id < NI) {
+      Ring br;
       int g = 0, itn = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -352,25 +370,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         }
         const uint32_t d_tmem = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
         uint32_t acc0 = 0u;  // the issuer's first stage of the item overwrites its accumulator
-        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, fr.next(NS), ar.next(NA)) {
-          if ((g & 1) != id) continue;
-          if (!mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag, 16) ||
-              !mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 16)) {
+        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, br.next(NB)) {
+          if (NI == 2 && (g & 1) != id) continue;
+          // the dequant set signals A only after the stage's token tile has landed
+          if (!mbar_wait(smem_u32(afull + br.idx), br.phase, abort_flag, 16)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64 * KS);
-          // B tile layout [8-row group][64-K block][8 rows][128 B]: 8-row groups are
-          // 2048*ks bytes apart; later K steps only move the start address
-          const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(smem + fr.idx * st_bytes), 2048u * KS);
-          if (KS == 2)
-            mma_stage<16>(d_tmem, a_tmem, bdesc0, idesc, acc0);
-          else
-            mma_stage<8>(d_tmem, a_tmem, bdesc0, idesc, acc0);
+          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(br.idx * 64);
+          // token tile [8-row group][64-K block][8 rows][128 B]: 8-row groups 2048 bytes apart
+          const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
+          mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
           acc0 = 1u;
-          mma_commit(smem_u32(empty + fr.idx));
-          mma_commit(smem_u32(aempty + ar.idx));
+          mma_commit(smem_u32(sfree + br.idx));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
@@ -383,59 +396,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_wait_drain(smem_u32(drain + id), 0);
     }
   } else if (warp >= kDequantWarp0) {
-    // ------------------------------------------------------------ dequant warpgroups
-    const int wg = (warp - kDequantWarp0) >> 2;
-    const int q = warp & 3;
+    // ------------------------------------------------------------ dequant sets
+    const int set = (warp - kDequantWarp0) >> 3;
+    const int q = warp & 3;             // TMEM lane quadrant = rows 32q .. 32q+31
+    const int half = (warp >> 2) & 1;   // K half of the stage row: columns 32*half .. +31
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    Ring fr, ar;
+    Ring wr, br;
     int g = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
-      for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, fr.next(NS), ar.next(NA)) {
-        if ((g & 1) != wg) continue;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + fr.idx), fr.phase, abort_flag));
+      for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, wr.next(NW), br.next(NB)) {
+        if ((g & 1) != set) continue;
+        // weights landed; token tile landed, which also means the MMAs of the
+        // A slot's previous stage completed (the producer waited for that)
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag) &&
+                                         mbar_wait(smem_u32(bfull + br.idx), br.phase, abort_flag));
         if (!ok) break;
-        const uint8_t* wst = smem + fr.idx * st_bytes + b_bytes;
-        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 * KS);
-        for (int j = 0; j < KS; ++j) {  // one 128-K group at a time: 64 TMEM columns each
-          const uint8_t* wj = wst + j * p.stage_bytes;
-          uint32_t out[64];
-          if (INT4) {
-            uint4 pk[4];
+        tc_fence_after();
+        const uint8_t* wst = wring + wr.idx * wslot;
+        uint32_t out[32];
+        if (INT4) {
+          uint4 pk[2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wj + (c * 128 + row) * 16);
-            const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wj + 8192 + row * 2);
-            if (j == KS - 1) {  // the stage's packed bytes are all in registers
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-            }
-            dequant_int4_row<BF16S>(pk, sbits, out);
-          } else {
-            uint4 pk[8];
+          for (int c = 0; c < 2; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((2 * half + c) * 128 + row) * 16);
+          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+          dequant_int4_half<BF16S>(pk, sbits, out);
+        } else {
+          uint4 pk[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) pk[c] = *reinterpret_cast<const uint4*>(wj + (c * 128 + row) * 16);
-            if (j == KS - 1) {
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(empty + fr.idx));
-            }
-            dequant_int8_row(pk, out);
-          }
-          if (j == 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(aempty + ar.idx), ar.phase ^ 1u, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-          }
-          tmem_st_32x32b_x32<0>(ta + static_cast<uint32_t>(64 * j), out);
-          tmem_st_32x32b_x32<32>(ta + static_cast<uint32_t>(64 * j + 32), out);
+          for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((4 * half + c) * 128 + row) * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+          dequant_int8_half(pk, out);
         }
-        if (!ok) break;
+        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(br.idx * 64 + 32 * half);
+        tmem_st_32x32b_x32<0>(ta, out);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
+        if (lane == 0) mbar_arrive(smem_u32(afull + br.idx));
       }
     }
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
@@ -454,10 +458,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
       if (!ok) break;
       tc_fence_after();
-      // issuer 0 took the item's even global stages, issuer 1 the odd ones
+      // with two issuers, issuer 0 took the item's even global stages and issuer 1 the odd ones
       const int n_st = it.ks1 - it.ks0;
-      const bool has0 = n_st >= 2 || (g & 1) == 0;
-      const bool has1 = n_st >= 2 || (g & 1) == 1;
+      const bool has0 = NI == 1 ? n_st >= 1 : (n_st >= 2 || (g & 1) == 0);
+      const bool has1 = NI == 2 && (n_st >= 2 || (g & 1) == 1);
       g += n_st;
       const float rs =
           INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
@@ -473,12 +477,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(accempty + b));
         }
+        float cs[16];
+        const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + it.row0 + c0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 v4 = __ldg(cs4 + c);
+          cs[4 * c] = v4.x;
+          cs[4 * c + 1] = v4.y;
+          cs[4 * c + 2] = v4.z;
+          cs[4 * c + 3] = v4.w;
+        }
         float f[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float cs = __ldg(p.col_scale + it.row0 + c0 + c);
-          f[c] = ((has0 ? __uint_as_float(v[c]) : 0.0f) + (has1 ? __uint_as_float(w[c]) : 0.0f)) * rs * cs;
-        }
+        for (int c = 0; c < 16; ++c)
+          f[c] = ((has0 ? __uint_as_float(v[c]) : 0.0f) + (has1 ? __uint_as_float(w[c]) : 0.0f)) * rs * cs[c];
         epilogue_store(p, it, c0, row, lane, f);
       }
       ++itn;

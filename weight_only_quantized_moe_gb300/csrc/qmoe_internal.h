@@ -35,18 +35,16 @@ enum EpiMode : int32_t {
 };
 
 // Pre-staged B operand (the gathered activations, the f16 intermediate): K is
-// cut into units of ks*128; unit u holds all cap rows (cap a multiple of 16)
-// as [row / 8][64-K block][row % 8][128 B], the eight 16-byte pieces of every
+// cut into 128-K groups; group u holds all cap rows (cap a multiple of 16) as
+// [row / 8][64-K block][row % 8][128 B], the eight 16-byte pieces of every
 // 128-byte row XOR-swizzled by row % 8 (the 128-byte swizzle of a K-major MMA
-// operand).  A chunk's rows of one unit are one contiguous run of
-// nrows * ks * 256 bytes.  Byte offset of the piece holding elements k..k+7
+// operand).  A chunk's rows of one group are one contiguous run of
+// nrows * 256 bytes.  Byte offset of the piece holding elements k..k+7
 // (k % 8 == 0) of row r:
-__host__ __device__ inline int64_t staged_offset(int64_t r, int k, int ks, int64_t cap) {
-  const int unit = k / (128 * ks), kin = k - unit * 128 * ks;
-  const int blk = kin >> 6, piece = (kin & 63) >> 3;
+__host__ __device__ inline int64_t staged_offset(int64_t r, int k, int64_t cap) {
+  const int unit = k >> 7, blk = (k >> 6) & 1, piece = (k & 63) >> 3;
   const int sw = static_cast<int>(r & 7);
-  return static_cast<int64_t>(unit) * cap * 256 * ks + (r >> 3) * (2048LL * ks) + blk * 1024 + sw * 128 +
-         ((piece ^ sw) << 4);
+  return static_cast<int64_t>(unit) * cap * 256 + (r >> 3) * 2048 + blk * 1024 + sw * 128 + ((piece ^ sw) << 4);
 }
 
 struct GemmParams {
@@ -62,16 +60,16 @@ struct GemmParams {
   int32_t* status;
   int64_t out_ld;            // elements per output row
   int64_t out_split_stride;  // elements per split slab
-  int64_t b_unit_stride;     // bytes per K unit of the staged B operand (cap * 256 * ks)
+  int64_t b_unit_stride;     // bytes per 128-K group of the staged B operand (cap * 256)
   int32_t n_tiles;
-  int32_t k_groups;          // 128-K quantization groups along K
-  int32_t ks;                // groups per pipeline stage (1 or 2)
+  int32_t k_groups;          // 128-K quantization groups along K = pipeline stages per tile
   int32_t split;
   int32_t token_tile;        // T: B rows per stage buffer, TMEM columns per accumulator
   int32_t acc_bufs;          // TMEM accumulators per MMA issuer (1 or 2)
-  int32_t a_col0;            // first TMEM column of the A stages
-  int32_t a_stages;          // TMEM A stages (64 columns each)
-  int32_t smem_stages;       // shared-memory pipeline depth
+  int32_t issuers;           // MMA-issuing threads (1 or 2)
+  int32_t a_col0;            // first TMEM column of the A slots
+  int32_t w_stages;          // packed-weight ring depth (even)
+  int32_t ab_stages;         // token-tile ring depth = TMEM A slots of 64 columns (even)
   int32_t stage_bytes;       // packed weight bytes per 128-K group
   int32_t epi_mode;
   int32_t P;                 // number of token-expert pairs
@@ -106,15 +104,15 @@ cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
 
 cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, int32_t ks, void* xg, float* xscale,
-                          int num_sms, cudaStream_t stream);
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
+                          cudaStream_t stream);
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
                                int32_t I, float* inter32, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
-                                 int32_t P, int32_t I, int64_t cap_rows, int32_t ks, void* inter16, float* iscale,
-                                 int num_sms, cudaStream_t stream);
+                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
+                                 cudaStream_t stream);
 
 cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E, int32_t split, int64_t M,
                               int32_t top_k, int32_t H, bool bf16, void* out, int num_sms, cudaStream_t stream);
