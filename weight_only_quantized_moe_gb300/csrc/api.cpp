@@ -151,21 +151,26 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
-  // MMA issuers: two (even / odd stages, one accumulator each) while the token
-  // tile is small and one thread's MMA issue rate is the limit; one when the
-  // tile is large and the tensor pipe is, which leaves TMEM for two
-  // accumulator buffers so the epilogue overlaps the next item's MMAs.
-  p.issuers = (T <= 64) ? 2 : 1;
+  // MMA issuers: up to three (stage g to issuer g mod n, one accumulator each)
+  // while the token tile is small and one thread's MMA issue rate is the
+  // limit; one when the tile is large and the tensor pipe is, which leaves TMEM
+  // for two accumulator buffers so the epilogue overlaps the next item's MMAs.
+  p.issuers = (T <= 32) ? 3 : (T <= 64) ? 2 : 1;
+  // Ring sizes are multiples of every role's stride (2 for the producers and
+  // dequant sets, the issuer count for the issuers): each slot then belongs to
+  // one role of each kind, and each waiter sees every phase of its barriers.
+  // (Otherwise a role would see only some uses of a slot and a parity wait
+  // could pass on a phase two behind.)
+  const int ring_mult = (p.issuers == 3) ? 6 : 2;
   // TMEM (512 columns): accumulators (issuers x buffers x T columns), then the
-  // 64-column A slots, at least two of them
-  p.acc_bufs = (p.issuers * 2 * T + 2 * 64 <= 512) ? 2 : 1;
+  // 64-column A slots paired with the token-tile ring (at most 8)
+  auto a_slots = [&](int accb) {
+    const int n = std::min(8, (512 - p.issuers * accb * T) / 64);
+    return n / ring_mult * ring_mult;
+  };
+  p.acc_bufs = a_slots(2) >= ring_mult ? 2 : 1;
   p.a_col0 = p.issuers * p.acc_bufs * T;
-  // Rings of an even number of slots: the even and odd stages go to separate
-  // producer and dequant roles (and MMA issuers), and with an even ring every
-  // slot is only ever used by one of them, so each waiter sees every phase of
-  // its barriers.  (With an odd ring a role would see every other use of a slot
-  // and a parity wait could pass on a phase two behind.)
-  p.ab_stages = std::min(8, (512 - p.a_col0) / 64) & ~1;
+  p.ab_stages = a_slots(p.acc_bufs);
   const size_t wslot = (static_cast<size_t>(p.stage_bytes) + 1023) & ~size_t(1023);
   const size_t b_bytes = static_cast<size_t>(p.ab_stages) * T * 256;
   if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return QMOE_ERR_UNSUPPORTED;

@@ -32,21 +32,22 @@
 //     pre-staged, per 128-K group and 8-row group, in the 128-byte-swizzled
 //     K-major layout the MMA's shared-memory descriptor reads, so a chunk's
 //     tile for one stage is one contiguous run.
-//   * warp roles (24 warps): two TMA producer threads (warps 4, 7) and two
+//   * warp roles (25 warps): two TMA producer threads (warps 4, 7) and two
 //     dequant sets of 8 warps (warps 8-15, 16-23) take the even and the odd
 //     stages; each dequant warp converts half of a stage row for 32 rows (one
-//     TMEM lane quadrant).  The MMAs are issued by two threads (warps 5, 6;
-//     even / odd stages, each into its own accumulator) when the token tile is
-//     small and the MMA issue rate is the limit, and by one thread (warp 5)
-//     when it is large and the tensor pipe is, so that two accumulator buffers
-//     fit in TMEM.  Warps 0-3 are the epilogue.  A persistent grid walks the
-//     work items.
+//     TMEM lane quadrant).  The MMAs are issued by up to three threads (warps
+//     5, 6, 24; stage g goes to issuer g mod NI, each with its own
+//     accumulator) while the token tile is small and one thread's MMA issue
+//     rate is the limit, and by one thread (warp 5) when the tile is large and
+//     the tensor pipe is, so that two accumulator buffers fit in TMEM.  Warps
+//     0-3 are the epilogue.  A persistent grid walks the work items.
 //   * barriers per stage: the dequant set waits for the weights and the token
 //     tile, releases the weight slot, writes A and signals it; the issuer
 //     waits for that one signal, issues the stage's MMAs and commits one
-//     release of the token-tile/A slot.  Every ring has an even number of
-//     slots, so each slot belongs to one parity role, and each role sees every
-//     phase of the barriers it waits on.
+//     release of the token-tile/A slot.  Every ring's size is a multiple of
+//     the stride of each role that uses it (2 for producers and dequant sets,
+//     NI for the issuers), so each slot belongs to one role of each kind and
+//     each role sees every phase of the barriers it waits on.
 //   * every mbarrier wait is bounded (see ptx.cuh); a wait that gives up
 //     records QMOE_ERR_TIMEOUT in the status word and the CTA winds down after
 //     waiting for its own copies and MMAs, then frees its TMEM.
@@ -60,12 +61,14 @@
 
 namespace qmoe {
 
-constexpr int kGemmThreads = 768;
+constexpr int kGemmThreads = 800;  // 25 warps
 constexpr int kProducerWarp = 4;
 constexpr int kProducerWarp2 = 7;
-constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 8;  // warps 8..23: two sets of 8
-constexpr int kDequantWarps = 8;  // per set
+constexpr int kMmaWarp = 5;        // issuers 0 and 1: warps 5 and 6; issuer 2: warp 24
+constexpr int kMmaWarp3 = 24;
+constexpr int kDequantWarp0 = 8;   // warps 8..23: two sets of 8
+constexpr int kDequantWarps = 8;   // per set
+constexpr int kMaxIssuers = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarrierBytes = 1024;
 
@@ -103,6 +106,13 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i,
   w.split_idx = s;
   w.ks0 = static_cast<int>(static_cast<int64_t>(p.k_groups) * s / p.split);
   w.ks1 = static_cast<int>(static_cast<int64_t>(p.k_groups) * (s + 1) / p.split);
+}
+
+// First stage index >= g0 that a role taking every r-th stage from stage `phase` owns.
+__device__ __forceinline__ int first_own(int g0, int phase, int r) {
+  int m = (phase - g0) % r;
+  if (m < 0) m += r;
+  return g0 + m;
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int32_t* status) {
@@ -235,7 +245,9 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 // The kernel.  Shared memory: weight ring (w_stages slots), token-tile ring
 // (ab_stages slots of T rows), barriers.  TMEM columns: issuer i owns acc_bufs
 // fp32 accumulators of T columns at [(i*acc_bufs + b) * T]; token-tile slot j
-// pairs with the 64-column A slot at a_col0 + 64j.
+// pairs with the 64-column A slot at a_col0 + 64j.  Every role walks only its
+// own stages (every 2nd for producers and dequant sets, every NI-th for the MMA
+// issuers), stepping its ring position by the same stride.
 // ---------------------------------------------------------------------------
 template <bool INT4, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint64_t* accfull = sfree + NB;
   uint64_t* accempty = accfull + 2;
   uint64_t* drain = accempty + 2;  // one per MMA issuer
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -277,8 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
       mbar_init(smem_u32(accempty + b), 4);  // the 4 epilogue warps
     }
-    mbar_init(smem_u32(drain), 1);
-    mbar_init(smem_u32(drain + 1), 1);
+    for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(drain + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -306,18 +317,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
       Ring wr, br;
-      int g = 0;
+      wr.idx = br.idx = id;
+      int g0 = 0, last_w = -1, last_b = -1;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
         decode_item(p, nch, i, it);
+        const int n_st = it.ks1 - it.ks0;
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_groups * static_cast<int64_t>(p.stage_bytes);
         // the chunk's rows of one stage of the pre-staged B operand: one contiguous run
         const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u;
         const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256;
-        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, wr.next(NW), br.next(NB)) {
-          if ((g & 1) != id) continue;
+        for (int g = first_own(g0, id, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
+          const int ks = it.ks0 + (g - g0);
           const bool inject = p.fault_injection == 1 && blockIdx.x == 0 && g == 0;  // armed, never filled
           if (!mbar_wait(smem_u32(wempty + wr.idx), wr.phase ^ 1u, abort_flag, 128)) {
             ok = false;
@@ -328,6 +341,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           if (!inject)
             tma_load_1d(smem_u32(wring + wr.idx * wslot), wsrc + static_cast<int64_t>(ks) * p.stage_bytes,
                         static_cast<uint32_t>(p.stage_bytes), wb, pol_w);
+          last_w = g;
           // the token-tile slot and its TMEM A slot are free once the MMAs of the
           // slot's previous stage completed
           if (!mbar_wait(smem_u32(sfree + br.idx), br.phase ^ 1u, abort_flag, 128)) {
@@ -337,30 +351,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           const uint32_t bb = smem_u32(bfull + br.idx);
           mbar_arrive_expect_tx(bb, b_run);
           if (!inject) tma_load_1d(smem_u32(bring + br.idx * bslot), bsrc + ks * p.b_unit_stride, b_run, bb, pol_b);
+          last_b = g;
         }
+        g0 += n_st;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
       // wait for every copy this thread may still have in flight into the CTA's shared
-      // memory: its stages among the last NW (weights) and NB (token tiles) it issued
-      for (int j = (g > NW ? g - NW : 0); j < g; ++j)
-        if ((j & 1) == id) mbar_wait_drain(smem_u32(wfull + (j % NW)), (j / NW) & 1);
-      for (int j = (g > NB ? g - NB : 0); j < g; ++j)
-        if ((j & 1) == id) mbar_wait_drain(smem_u32(bfull + (j % NB)), (j / NB) & 1);
+      // memory: its stages among the last NW (weights) and NB (token tiles) it armed
+      for (int j = (last_w >= NW ? last_w - NW + 2 : id); j <= last_w; j += 2)
+        mbar_wait_drain(smem_u32(wfull + (j % NW)), (j / NW) & 1);
+      for (int j = (last_b >= NB ? last_b - NB + 2 : id); j <= last_b; j += 2)
+        mbar_wait_drain(smem_u32(bfull + (j % NB)), (j / NB) & 1);
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1 || warp == kMmaWarp3) {
     // ------------------------------------------------------------ MMA issuers
-    // With two issuers (small token tiles) each takes every other stage into its
-    // own accumulator: one thread's issue rate, with the wait and commit around
+    // With NI issuers, issuer i takes stages i, i+NI, ... into its own
+    // accumulator: one thread's MMA issue rate, with the wait and commit around
     // each stage, is below what the tensor core accepts at small N.  With one
     // (large tiles) warp 5 takes every stage.
-    const int id = warp - kMmaWarp;
+    const int id = (warp == kMmaWarp3) ? 2 : warp - kMmaWarp;
     if (lane == 0 && id < NI) {
       Ring br;
-      int g = 0, itn = 0;
+      br.idx = id;
+      int g0 = 0, itn = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
         decode_item(p, nch, i, it);
+        const int n_st = it.ks1 - it.ks0;
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
         const int b = (ACCB == 2) ? (itn & 1) : 0;
         const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
@@ -370,8 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         }
         const uint32_t d_tmem = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
         uint32_t acc0 = 0u;  // the issuer's first stage of the item overwrites its accumulator
-        for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, br.next(NB)) {
-          if (NI == 2 && (g & 1) != id) continue;
+        for (int g = first_own(g0, id, NI); g < g0 + n_st; g += NI, br.step(NI, NB)) {
           // the dequant set signals A only after the stage's token tile has landed
           if (!mbar_wait(smem_u32(afull + br.idx), br.phase, abort_flag, 16)) {
             ok = false;
@@ -388,6 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
         mma_commit(smem_u32(accfull + b));
+        g0 += n_st;
         ++itn;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
@@ -403,13 +421,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     Ring wr, br;
-    int g = 0;
+    wr.idx = br.idx = set;
+    int g0 = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
-      for (int ks = it.ks0; ks < it.ks1; ++ks, ++g, wr.next(NW), br.next(NB)) {
-        if ((g & 1) != set) continue;
+      const int n_st = it.ks1 - it.ks0;
+      for (int g = first_own(g0, set, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
         // weights landed; token tile landed, which also means the MMAs of the
         // A slot's previous stage completed (the producer waited for that)
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag) &&
@@ -441,6 +460,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(afull + br.idx));
       }
+      g0 += n_st;
     }
     if (!ok && lane == 0) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
   } else if (warp < 4) {
@@ -448,7 +468,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     const int q = warp;
     const int row = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    int itn = 0, g = 0;
+    int itn = 0, g0 = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
@@ -458,39 +478,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
       if (!ok) break;
       tc_fence_after();
-      // with two issuers, issuer 0 took the item's even global stages and issuer 1 the odd ones
+      // issuer j took the item's stages g0 + n with (g0 + n) % NI == j
       const int n_st = it.ks1 - it.ks0;
-      const bool has0 = NI == 1 ? n_st >= 1 : (n_st >= 2 || (g & 1) == 0);
-      const bool has1 = NI == 2 && (n_st >= 2 || (g & 1) == 1);
-      g += n_st;
+      bool has[kMaxIssuers];
+#pragma unroll
+      for (int j = 0; j < kMaxIssuers; ++j) has[j] = j < NI && first_own(g0, j, NI) < g0 + n_st;
+      g0 += n_st;
       const float rs =
           INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
-      const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(b * T);
-      const uint32_t t1 = tmem + lane_base + static_cast<uint32_t>((ACCB + b) * T);
       for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-        uint32_t v[16], w[16];
-        if (has0) tmem_ld_32x32b_x16(t0 + static_cast<uint32_t>(c0), v);
-        if (has1) tmem_ld_32x32b_x16(t1 + static_cast<uint32_t>(c0), w);
-        tmem_wait_ld();
+        float f[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) f[c] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxIssuers; ++j) {
+          if (!has[j]) continue;
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tmem + lane_base + static_cast<uint32_t>((j * ACCB + b) * T + c0), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) f[c] += __uint_as_float(v[c]);
+        }
         if (c0 + 16 >= it.nrows) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(accempty + b));
         }
-        float cs[16];
         const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + it.row0 + c0);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const float4 v4 = __ldg(cs4 + c);
-          cs[4 * c] = v4.x;
-          cs[4 * c + 1] = v4.y;
-          cs[4 * c + 2] = v4.z;
-          cs[4 * c + 3] = v4.w;
+          f[4 * c] *= rs * v4.x;
+          f[4 * c + 1] *= rs * v4.y;
+          f[4 * c + 2] *= rs * v4.z;
+          f[4 * c + 3] *= rs * v4.w;
         }
-        float f[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          f[c] = ((has0 ? __uint_as_float(v[c]) : 0.0f) + (has1 ? __uint_as_float(w[c]) : 0.0f)) * rs * cs[c];
         epilogue_store(p, it, c0, row, lane, f);
       }
       ++itn;

@@ -13,9 +13,10 @@ size_t gemm_smem_bytes(const GemmParams& p) {
 
 cudaError_t launch_gemm(bool int4, bool bf16_scales, const GemmParams& p, int grid,
                         cudaStream_t stream) {
-  // the even/odd role split needs rings of even size (see qmoe_gemm_kernel)
-  if (p.w_stages < 2 || p.ab_stages < 2 || (p.w_stages & 1) || (p.ab_stages & 1) || p.issuers < 1 || p.issuers > 2)
-    return cudaErrorInvalidValue;
+  // ring sizes must be multiples of every role's stride (see qmoe_gemm_kernel)
+  if (p.issuers < 1 || p.issuers > kMaxIssuers) return cudaErrorInvalidValue;
+  const int mult = (p.issuers == 3) ? 6 : 2;
+  if (p.w_stages < 2 || (p.w_stages & 1) || p.ab_stages < mult || p.ab_stages % mult != 0) return cudaErrorInvalidValue;
   if (int4)
     return bf16_scales ? launch_gemm_i4_bf16(p, grid, stream) : launch_gemm_i4_f16(p, grid, stream);
   return launch_gemm_i8(p, grid, stream);

@@ -110,6 +110,15 @@ struct Ring {
       phase ^= 1u;
     }
   }
+  // Advance by r slots of a ring of n slots, n a multiple of r (a role that
+  // takes every r-th stage).
+  __device__ __forceinline__ void step(int r, int n) {
+    idx += r;
+    if (idx >= n) {
+      idx -= n;
+      phase ^= 1u;
+    }
+  }
 };
 
 // ---------------------------------------------------------------------------
