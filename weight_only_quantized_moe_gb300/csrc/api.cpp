@@ -105,20 +105,23 @@ struct Plan {
          off_inter32 = 0, off_inter16 = 0, off_iscale = 0, off_h = 0, off_y = 0, total = 0;
 };
 
-// Makespan of n equal work items split s ways over C persistent CTAs, in
-// units of one unsplit item, plus a small charge per split for the reduce.
-double split_cost(int64_t n, int s, int C) {
-  const int64_t waves = (n * s + C - 1) / C;
-  return static_cast<double>(waves) / s + 0.002 * s;
+// Makespan, in pipeline stages, of n work items of k stages each split s ways
+// over C persistent CTAs.  A CTA's items run back to back; each item costs the
+// longer of its stages and its epilogue (`epi` stages' worth, overlapped with
+// the next item's stages when TMEM holds two accumulator buffers).  Each split
+// beyond the first adds `reduce` stages' worth of partial-sum traffic.
+double split_cost(int64_t n, int k, int s, int C, double epi, double reduce) {
+  const int64_t per_cta = (n * s + C - 1) / C;
+  return static_cast<double>(per_cta) * std::max(static_cast<double>(k) / s, epi) + reduce * (s - 1);
 }
 
-int choose_split(int64_t n_items, int k_stages, int C, double must_gain) {
+int choose_split(int64_t n_items, int k_stages, int C, double epi, double reduce, double must_gain) {
   const int smax = std::max(1, std::min(64, k_stages / 4));
   int best = 1;
-  double best_cost = split_cost(n_items, 1, C);
+  double best_cost = split_cost(n_items, k_stages, 1, C, epi, reduce);
   const double base = best_cost;
   for (int s = 2; s <= smax; ++s) {
-    const double c = split_cost(n_items, s, C);
+    const double c = split_cost(n_items, k_stages, s, C, epi, reduce);
     if (c < best_cost) {
       best_cost = c;
       best = s;
@@ -183,8 +186,15 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   // expected chunks for the split heuristic (uniform routing)
   const double d = L->E * (1.0 - std::pow(1.0 - 1.0 / L->E, static_cast<double>(P)));
   const int64_t est_chunks = std::max<int64_t>(std::max<int64_t>(1, static_cast<int64_t>(std::ceil(d))), (P + T - 1) / T);
-  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, 0.8);
-  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, 0.97);
+  // Epilogue time of one item in pipeline stages (measured on GB300: about 3k
+  // cycles for a 16-row chunk, 15k for a 128-row one, against 0.7k-1.1k per
+  // stage).  Partial sums of one extra split: written and read once in fp32,
+  // in stage-times of the whole GPU's weight stream (~1.3 MB per stage-time)
+  // (plus half a stage per split for summing the partials).
+  const double epi = 4.0 + T / 8.0;
+  const double stage_bytes_gpu = 1.3e6;
+  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, epi, 0.5 + 8.0 * P * 2 * L->I / stage_bytes_gpu, 0.8);
+  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, epi, 0.5 + 8.0 * P * L->H / stage_bytes_gpu, 0.97);
   if (o != nullptr && o->split1 != 0) {
     if (o->split1 < 1 || o->split1 > 64 || o->split1 > p.kst1) return QMOE_ERR_INVALID_ARG;
     p.S1 = o->split1;
