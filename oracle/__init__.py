@@ -17,4 +17,5 @@ from .moe import (  # noqa: F401
     moe_forward,
     moe_forward_rows,
     moe_align,
+    route_topk,
 )

@@ -20,6 +20,12 @@ What is computed, and where it comes from
   formula; this is the plain reading.
 * Routing-weighted sum.  ``out[m] = sum_j topk_weights[m, j] * y(m, j)`` with
   ``y(m, j)`` the FFN of expert ``topk_ids[m, j]`` applied to token m.
+* Router (the step before the layer; the pages are silent on it).  The
+  Mixtral-style layers these kernels serve route each token by a softmax over
+  its expert logits, keep the top-k experts, and renormalise the kept
+  probabilities to sum to one (optionally not, as some many-expert models
+  do).  Readings: experts are ranked by logit, ties go to the lower expert
+  id, the slots are filled in rank order.
 * moe_align_block_size.  "Marlin moe integration" (review thread: the
   ``moe_align_block_size_kernel`` the fused kernel relies on; block size 16
   tied to the Marlin tile) groups the token-expert pairs by expert and pads
@@ -135,6 +141,40 @@ def moe_forward(layer, x: np.ndarray, topk_ids: np.ndarray,
                 topk_weights: np.ndarray) -> np.ndarray:
     """out[m] = sum_j topk_weights[m, j] * FFN_{topk_ids[m, j]}(x[m]), float64 [M, H]."""
     return moe_forward_rows(layer, x, topk_ids, topk_weights, range(np.asarray(x).shape[0]))
+
+
+# ----------------------------------------------------------------------------
+# router: softmax -> top-k -> (optional) renormalisation
+# ----------------------------------------------------------------------------
+def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
+    """Top-k routing of each token row of ``logits`` [M, E].
+
+    k rounds per row, each taking the largest logit not yet taken (the lowest
+    expert id among equal logits).  Weights are the softmax probabilities of
+    the kept experts, p_e = exp(l_e) / sum_j exp(l_j), divided by their sum
+    when ``renormalize``.  Returns (ids int32 [M, k], weights float64 [M, k]).
+    """
+    lg = np.asarray(logits, np.float64)
+    M, E = lg.shape
+    ids = np.zeros((M, k), np.int32)
+    w = np.zeros((M, k), np.float64)
+    for m in range(M):
+        row = lg[m]
+        taken = np.zeros(E, bool)
+        for r in range(k):
+            best = -1
+            for e in range(E):
+                if taken[e]:
+                    continue
+                if best < 0 or row[e] > row[best]:
+                    best = e
+            taken[best] = True
+            ids[m, r] = best
+        top = row.max()
+        p = np.exp(row - top)                               # softmax numerators, max shifted to 1
+        kept = p[ids[m]]
+        w[m] = kept / (kept.sum() if renormalize else p.sum())
+    return ids, w
 
 
 # ----------------------------------------------------------------------------

@@ -391,3 +391,51 @@ def test_moe_align_vs_sort_and_invariants(M, k, E, B):
         e = ex[b]
         assert all(ids.reshape(-1)[p] == e for p in blk if p < P)
     assert np.all(ex[n // B:] == -1)
+
+
+# ----------------------------------------------------------------------------
+# router: softmax -> top-k -> renormalise
+# ----------------------------------------------------------------------------
+def test_route_topk_hand_examples():
+    # ties go to the lower expert id, slots in rank order
+    ids, w = oracle.route_topk(np.array([[1.0, 3.0, 3.0, 0.0]]), 2)
+    assert ids.tolist() == [[1, 2]]
+    np.testing.assert_allclose(w, [[0.5, 0.5]], rtol=0, atol=1e-15)
+    # renormalised top-2 of logits (0, ln 3): weights 1/4 and 3/4, the larger first
+    ids, w = oracle.route_topk(np.array([[0.0, math.log(3.0), -50.0]]), 2)
+    assert ids.tolist() == [[1, 0]]
+    np.testing.assert_allclose(w, [[0.75, 0.25]], rtol=1e-14)
+    # without renormalisation the weights are the plain softmax probabilities
+    ids, w = oracle.route_topk(np.array([[0.0, math.log(3.0), math.log(4.0)]]), 1, renormalize=False)
+    assert ids.tolist() == [[2]]
+    np.testing.assert_allclose(w, [[0.5]], rtol=1e-14)       # 4 / (1 + 3 + 4)
+
+
+def test_route_topk_vs_sort_and_closed_forms():
+    rng = np.random.default_rng(11)
+    for E, k in [(8, 2), (16, 5), (160, 6), (7, 7)]:
+        # integer-valued logits make ties frequent
+        lg = rng.integers(-3, 4, size=(40, E)).astype(np.float64) * 0.5
+        ids, w = oracle.route_topk(lg, k)
+        idsn, wn = oracle.route_topk(lg, k, renormalize=False)
+        for m in range(lg.shape[0]):
+            want = sorted(range(E), key=lambda e: (-lg[m, e], e))[:k]   # stable rank order
+            assert ids[m].tolist() == want and idsn[m].tolist() == want
+            assert len(set(ids[m].tolist())) == k
+            # renormalised weights: sum 1, ratios exp(l_i - l_j)
+            assert abs(w[m].sum() - 1.0) < 1e-12
+            for r in range(1, k):
+                assert abs(w[m, r] / w[m, 0] - math.exp(lg[m, want[r]] - lg[m, want[0]])) < 1e-12
+            # plain softmax: against the full distribution computed directly
+            full = np.exp(lg[m]) / np.exp(lg[m]).sum()
+            np.testing.assert_allclose(wn[m], full[want], rtol=1e-12)
+        if k == E:
+            assert np.allclose(wn.sum(axis=1), 1.0)
+
+
+def test_route_topk_large_logits_do_not_overflow():
+    lg = np.array([[1e4, 1e4 - 1.0, -1e4], [-1e4, -1e4 + math.log(2.0), 0.0]])
+    ids, w = oracle.route_topk(lg, 2)
+    assert ids.tolist() == [[0, 1], [2, 1]]
+    np.testing.assert_allclose(w[0], [1 / (1 + math.exp(-1)), math.exp(-1) / (1 + math.exp(-1))], rtol=1e-12)
+    np.testing.assert_allclose(w[1], [1.0, 0.0], atol=1e-12)
