@@ -288,6 +288,33 @@ qmoe_status qmoe_forward_noalloc(const qmoe_layer* layer, const void* x, int64_t
                                  void* out, void* stream);
 
 /*
+ * Router, the step before the layer (the pages take its output, the top-k
+ * expert ids and weights, as the fused kernel's input; the Mixtral-style
+ * layers they run route by softmax, top-k and renormalisation).  For each
+ * token row of logits [M, E] (logits_dtype QMOE_F32, QMOE_F16 or QMOE_BF16,
+ * device memory): topk_ids int32 [M, top_k] = the top_k experts by logit in
+ * descending order, ties going to the lower expert id; topk_weights float32
+ * [M, top_k] = their softmax probabilities exp(l_e) / sum_j exp(l_j),
+ * divided by the sum of the kept ones when renormalize != 0.  NaN logits
+ * count as -inf; a row of -inf logits routes uniformly.  Computed in fp32.
+ * Requirements: 1 <= E <= 1024, 1 <= top_k <= E (QMOE_ERR_INVALID_ARG), and
+ * top_k <= 32 (QMOE_ERR_UNSUPPORTED).  Asynchronous on `stream`.
+ */
+qmoe_status qmoe_route_topk(const void* logits, qmoe_dtype logits_dtype, int64_t M, int32_t E, int32_t top_k,
+                            int32_t renormalize, int32_t* topk_ids, float* topk_weights, void* stream);
+
+/*
+ * The router then the layer in one call: out = the layer applied to x with
+ * the routing qmoe_route_topk computes from logits (E = layer->E).  The
+ * routing is kept in the workspace, which needs qmoe_workspace_size_logits
+ * bytes (0 on invalid input); arguments otherwise as for qmoe_forward.
+ */
+size_t qmoe_workspace_size_logits(const qmoe_layer* layer, int64_t M, int32_t top_k);
+qmoe_status qmoe_forward_logits(const qmoe_layer* layer, const void* x, int64_t M, const void* logits,
+                                qmoe_dtype logits_dtype, int32_t top_k, int32_t renormalize, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronise `stream` and return the first device-side fault recorded in
  * `workspace` by the most recent forward that used it (QMOE_OK if none).
  */

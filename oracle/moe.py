@@ -152,9 +152,11 @@ def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
     k rounds per row, each taking the largest logit not yet taken (the lowest
     expert id among equal logits).  Weights are the softmax probabilities of
     the kept experts, p_e = exp(l_e) / sum_j exp(l_j), divided by their sum
-    when ``renormalize``.  Returns (ids int32 [M, k], weights float64 [M, k]).
+    when ``renormalize``; a row whose logits are all -inf routes uniformly.
+    NaN logits count as -inf.  Returns (ids int32 [M, k], weights float64 [M, k]).
     """
     lg = np.asarray(logits, np.float64)
+    lg = np.where(np.isnan(lg), -np.inf, lg)
     M, E = lg.shape
     ids = np.zeros((M, k), np.int32)
     w = np.zeros((M, k), np.float64)
@@ -171,7 +173,8 @@ def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
             taken[best] = True
             ids[m, r] = best
         top = row.max()
-        p = np.exp(row - top)                               # softmax numerators, max shifted to 1
+        # softmax numerators with the maximum shifted to 1 (a row of -inf logits: uniform)
+        p = np.ones(E) if top == -np.inf else np.exp(row - top)
         kept = p[ids[m]]
         w[m] = kept / (kept.sum() if renormalize else p.sum())
     return ids, w

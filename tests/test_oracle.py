@@ -439,3 +439,13 @@ def test_route_topk_large_logits_do_not_overflow():
     assert ids.tolist() == [[0, 1], [2, 1]]
     np.testing.assert_allclose(w[0], [1 / (1 + math.exp(-1)), math.exp(-1) / (1 + math.exp(-1))], rtol=1e-12)
     np.testing.assert_allclose(w[1], [1.0, 0.0], atol=1e-12)
+
+
+def test_route_topk_masked_rows():
+    inf = math.inf
+    ids, w = oracle.route_topk(np.array([[-inf, 2.0, -inf, float("nan")], [-inf] * 4]), 3)
+    assert ids[0].tolist() == [1, 0, 2] and ids[1].tolist() == [0, 1, 2]
+    np.testing.assert_allclose(w[0], [1.0, 0.0, 0.0])
+    np.testing.assert_allclose(w[1], [1 / 3] * 3)
+    _, wn = oracle.route_topk(np.array([[-inf] * 4]), 2, renormalize=False)
+    np.testing.assert_allclose(wn[0], [0.25, 0.25])

@@ -26,13 +26,16 @@ from .api import (  # noqa: F401
     packed_bytes,
     qmoe_forward,
     qmoe_forward_host,
+    qmoe_forward_logits,
     qmoe_forward_noalloc,
     qmoe_forward_profiled,
     qmoe_moe_align,
     qmoe_pack_int4,
     qmoe_pack_int8,
     qmoe_read_device_status,
+    qmoe_route_topk,
     qmoe_unpack_int4,
+    qmoe_workspace_size_logits,
     qmoe_unpack_int8,
     qmoe_workspace_size,
     qmoe_workspace_size_host,

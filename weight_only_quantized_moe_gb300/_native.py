@@ -81,6 +81,11 @@ _SIGS = {
     "qmoe_forward_host": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_void_p, c_int32, c_void_p,
                                     c_void_p, c_size_t, c_void_p]),
     "qmoe_read_device_status": (c_int32, [c_void_p, c_void_p]),
+    "qmoe_route_topk": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                  c_void_p]),
+    "qmoe_workspace_size_logits": (c_size_t, [POINTER(QmoeLayer), c_int64, c_int32]),
+    "qmoe_forward_logits": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_int32, c_int32, c_int32,
+                                      c_void_p, c_void_p, c_size_t, c_void_p]),
     "qmoe_forward_noalloc": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_void_p, c_int32,
                                        c_void_p, c_void_p]),
 }

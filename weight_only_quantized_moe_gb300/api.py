@@ -268,3 +268,47 @@ def qmoe_forward_noalloc(layer: DeviceLayer, x: torch.Tensor, topk_ids: torch.Te
                                       _stream_ptr(stream))
     N.check(st, "qmoe_forward_noalloc")
     return out
+
+
+_LOGIT_DT = {torch.float32: N.QMOE_F32, torch.float16: N.QMOE_F16, torch.bfloat16: N.QMOE_BF16}
+
+
+def qmoe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, topk_ids: torch.Tensor | None = None,
+                    topk_weights: torch.Tensor | None = None, stream=None):
+    """Top-k router on the GPU (softmax, top-k with ties to the lower id,
+    optional renormalisation): returns (topk_ids int32 [M, k], topk_weights float32 [M, k])."""
+    assert logits.is_cuda and logits.is_contiguous() and logits.dim() == 2 and logits.dtype in _LOGIT_DT
+    M, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((M, k), dtype=torch.int32, device=logits.device)
+    if topk_weights is None:
+        topk_weights = torch.empty((M, k), dtype=torch.float32, device=logits.device)
+    st = N.lib().qmoe_route_topk(c_void_p(logits.data_ptr()), _LOGIT_DT[logits.dtype], M, E, k,
+                                 1 if renormalize else 0, c_void_p(topk_ids.data_ptr()),
+                                 c_void_p(topk_weights.data_ptr()), _stream_ptr(stream))
+    N.check(st, "qmoe_route_topk")
+    return topk_ids, topk_weights
+
+
+def qmoe_workspace_size_logits(layer: DeviceLayer, M: int, k: int) -> int:
+    n = int(N.lib().qmoe_workspace_size_logits(byref(layer.struct), M, k))
+    if n == 0:
+        raise N.QmoeError(N.QMOE_ERR_INVALID_ARG, "qmoe_workspace_size_logits")
+    return n
+
+
+def qmoe_forward_logits(layer: DeviceLayer, x: torch.Tensor, logits: torch.Tensor, k: int, renormalize: bool = True,
+                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """The router then the layer in one call (routing kept in the workspace)."""
+    M, H = x.shape
+    assert x.dtype == layer.torch_dtype and x.is_contiguous() and H == layer.H
+    assert logits.is_contiguous() and logits.shape == (M, layer.E) and logits.dtype in _LOGIT_DT
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = alloc_workspace(qmoe_workspace_size_logits(layer, M, k), x.device)
+    st = N.lib().qmoe_forward_logits(byref(layer.struct), c_void_p(x.data_ptr()), M, c_void_p(logits.data_ptr()),
+                                     _LOGIT_DT[logits.dtype], k, 1 if renormalize else 0, c_void_p(out.data_ptr()),
+                                     c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    N.check(st, "qmoe_forward_logits")
+    return out

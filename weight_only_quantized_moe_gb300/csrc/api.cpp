@@ -730,6 +730,57 @@ qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64
   return QMOE_OK;
 }
 
+qmoe_status qmoe_route_topk(const void* logits, qmoe_dtype logits_dtype, int64_t M, int32_t E, int32_t top_k,
+                            int32_t renormalize, int32_t* topk_ids, float* topk_weights, void* stream) {
+  if (M < 0 || E < 1 || E > 1024 || top_k < 1 || top_k > E) return QMOE_ERR_INVALID_ARG;
+  if (top_k > 32) return QMOE_ERR_UNSUPPORTED;
+  int dt = 0;
+  if (logits_dtype == QMOE_F32)
+    dt = 0;
+  else if (logits_dtype == QMOE_F16)
+    dt = 1;
+  else if (logits_dtype == QMOE_BF16)
+    dt = 2;
+  else
+    return QMOE_ERR_INVALID_ARG;
+  if (M == 0) return QMOE_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  qmoe_status st;
+  const void* ptrs[] = {logits, topk_ids, topk_weights};
+  for (const void* p : ptrs)
+    if ((st = check_dev_ptr(p, dev)) != QMOE_OK) return st;
+  if (!aligned(logits, dt == 0 ? 4 : 2) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+    return QMOE_ERR_INVALID_ARG;
+  const cudaError_t err = launch_route_topk(logits, dt, M, E, top_k, renormalize != 0 ? 1 : 0, topk_ids,
+                                            topk_weights, current_sm_count(), static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+size_t qmoe_workspace_size_logits(const qmoe_layer* layer, int64_t M, int32_t top_k) {
+  const size_t w = qmoe_workspace_size(layer, M, top_k);
+  if (w == 0) return 0;
+  return al256(w) + 2 * al256(static_cast<size_t>(M) * top_k * 4);
+}
+
+qmoe_status qmoe_forward_logits(const qmoe_layer* layer, const void* x, int64_t M, const void* logits,
+                                qmoe_dtype logits_dtype, int32_t top_k, int32_t renormalize, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  const size_t w = qmoe_workspace_size(layer, M, top_k);
+  if (w == 0) return validate_layer_dims(layer) != QMOE_OK ? validate_layer_dims(layer) : QMOE_ERR_INVALID_ARG;
+  if (M == 0) return QMOE_OK;
+  if (workspace == nullptr || workspace_bytes < qmoe_workspace_size_logits(layer, M, top_k)) return QMOE_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  int32_t* ids = reinterpret_cast<int32_t*>(base + al256(w));
+  float* wts = reinterpret_cast<float*>(base + al256(w) + al256(static_cast<size_t>(M) * top_k * 4));
+  qmoe_status st = qmoe_route_topk(logits, logits_dtype, M, layer->E, top_k, renormalize, ids, wts, stream);
+  if (st != QMOE_OK) return st;
+  return forward_impl(layer, x, M, ids, wts, top_k, out, workspace, w, static_cast<cudaStream_t>(stream), nullptr);
+}
+
 qmoe_status qmoe_read_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return QMOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {

@@ -430,4 +430,97 @@ cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E
                        top_k, H, static_cast<uint16_t*>(out));
 }
 
+// ---------------------------------------------------------------------------
+// Router: per token row, the top-k experts by logit (ties go to the lower
+// expert id) in rank order and their softmax probabilities, renormalised over
+// the kept experts when asked.  One warp per row; lane l holds the logits of
+// experts l, l+32, ... (E <= 1024) in registers; k rounds of a warp arg-max.
+// NaN logits count as -inf.
+// ---------------------------------------------------------------------------
+constexpr int kRouteThreads = 256;
+
+template <int DT>  // 0: f32, 1: f16, 2: bf16
+__device__ __forceinline__ float load_logit(const void* base, int64_t i) {
+  float v;
+  if (DT == 0) {
+    v = __ldg(static_cast<const float*>(base) + i);
+  } else {
+    const uint16_t b = __ldg(static_cast<const uint16_t*>(base) + i);
+    v = (DT == 1) ? __half2float(__ushort_as_half(b)) : __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  return (v != v) ? -INFINITY : v;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_topk_kernel(const void* __restrict__ logits, int64_t M, int32_t E, int32_t k, int32_t renormalize,
+                      int32_t* __restrict__ topk_ids, float* __restrict__ topk_weights) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRouteThreads / 32);
+  for (int64_t m = blockIdx.x * static_cast<int64_t>(kRouteThreads / 32) + (threadIdx.x >> 5); m < M; m += warps) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < E) ? load_logit<DT>(logits, m * E + e) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float my_v = -INFINITY;
+    int my_e = 0;
+    for (int r = 0; r < k; ++r) {
+      float best = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && (v[j] > best || (v[j] == best && e < be))) {
+          best = v[j];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, d);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, d);
+        if (ov > best || (ov == best && oe < be)) {
+          best = ov;
+          be = oe;
+        }
+      }
+      if (lane == (be & 31)) taken |= 1u << (be >> 5);
+      if (lane == r) {
+        my_v = best;
+        my_e = be;
+      }
+    }
+    // the first kept logit is the row maximum; a row of -inf logits routes uniformly
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    const bool masked = top == -INFINITY;
+    const float pk = (lane < k) ? (masked ? 1.0f : expf(my_v - top)) : 0.0f;
+    float denom = 0.0f;
+    if (renormalize) {
+      denom = pk;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (lane + 32 * j < E) denom += masked ? 1.0f : expf(v[j] - top);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, d);
+    if (lane < k) {
+      topk_ids[m * k + lane] = my_e;
+      topk_weights[m * k + lane] = pk / denom;
+    }
+  }
+}
+
+cudaError_t launch_route_topk(const void* logits, int dtype, int64_t M, int32_t E, int32_t k, int32_t renormalize,
+                              int32_t* topk_ids, float* topk_weights, int num_sms, cudaStream_t stream) {
+  const int64_t want = (M + (kRouteThreads / 32) - 1) / (kRouteThreads / 32);
+  const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
+  auto kern = dtype == 0 ? route_topk_kernel<0> : dtype == 1 ? route_topk_kernel<1> : route_topk_kernel<2>;
+  return launch_kernel(kern, dim3(grid), dim3(kRouteThreads), 0, stream, false, logits, M, E, k, renormalize,
+                       topk_ids, topk_weights);
+}
+
 }  // namespace qmoe

@@ -117,6 +117,10 @@ cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_p
 cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E, int32_t split, int64_t M,
                               int32_t top_k, int32_t H, bool bf16, void* out, int num_sms, cudaStream_t stream);
 
+// dtype: 0 f32, 1 f16, 2 bf16 logits; 1 <= E <= 1024, 1 <= k <= min(E, 32).
+cudaError_t launch_route_topk(const void* logits, int dtype, int64_t M, int32_t E, int32_t k, int32_t renormalize,
+                              int32_t* topk_ids, float* topk_weights, int num_sms, cudaStream_t stream);
+
 size_t gemm_smem_bytes(const GemmParams& p);
 cudaError_t launch_gemm(bool int4, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream);
 
