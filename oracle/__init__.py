@@ -11,6 +11,7 @@ inputs and hand-worked examples); see the module docstrings for the pins.
 from .moe import (  # noqa: F401
     dequant_int4,
     dequant_int8,
+    dequant_int8_group,
     dequant_layer_expert,
     silu,
     expert_ffn,

@@ -58,20 +58,24 @@ import numpy as np
 # dequantization
 # ----------------------------------------------------------------------------
 def dequant_int4(q: np.ndarray, s: np.ndarray, g_idx: np.ndarray | None,
-                 group_size: int) -> np.ndarray:
-    """W[n, k] = (q[n, k] - 8) * s[g(k), n], float64 [N, K].
+                 group_size: int, zeros: np.ndarray | None = None) -> np.ndarray:
+    """W[n, k] = (q[n, k] - z[g(k), n]) * s[g(k), n], float64 [N, K].
 
     q: codes 0..15 [N, K]; s: scales [K/G, N]; g(k) = g_idx[k] under
     act-order, else k // G ("Marlin moe integration": GPTQ 4-bit group-128,
-    with or without act order).
+    with or without act order); group_size -1 is one group over all of K
+    (channel-wise, "Add GPTQ Marlin 2:4 sparse structured support" lists
+    group 128 or -1).  z: per-group zero points [K/G, N] (asymmetric, AWQ
+    style: "[WIP] AWQ Faster Kernels"), or 8 for every group when None.
     """
     N, K = q.shape
     if g_idx is None:
-        g = np.arange(K) // group_size
+        g = np.arange(K) // (K if group_size < 0 else group_size)
     else:
         g = np.asarray(g_idx, np.int64)
     scale_nk = np.asarray(s, np.float64)[g, :].T          # [N, K]: s[g(k), n]
-    return (q.astype(np.float64) - 8.0) * scale_nk
+    zero_nk = 8.0 if zeros is None else np.asarray(zeros, np.float64)[g, :].T
+    return (q.astype(np.float64) - zero_nk) * scale_nk
 
 
 def dequant_int8(q: np.ndarray, s: np.ndarray) -> np.ndarray:
@@ -80,14 +84,28 @@ def dequant_int8(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return q.astype(np.float64) * np.asarray(s, np.float64)[:, None]
 
 
+def dequant_int8_group(q: np.ndarray, s: np.ndarray, group_size: int) -> np.ndarray:
+    """W[n, k] = q[n, k] * s[k // G, n]: symmetric int8 with one scale per group of
+    G input channels ("Add GPTQ Marlin 2:4 sparse structured support" lists
+    8-bit with group 128), float64 [N, K]."""
+    K = q.shape[1]
+    scale_nk = np.asarray(s, np.float64)[np.arange(K) // group_size, :].T
+    return q.astype(np.float64) * scale_nk
+
+
 def dequant_layer_expert(layer, e: int):
     """Dequantized (W13_e [2I, H], W2_e [H, I]) of expert e of a canonical layer."""
     wl = layer.wl
-    if wl.qt == "int4":
+    if wl.qt in ("int4", "int4zp"):
         g13 = None if layer.g13 is None else layer.g13[e]
         g2 = None if layer.g2 is None else layer.g2[e]
-        w13 = dequant_int4(layer.q13[e], layer.s13[e], g13, wl.group_size)
-        w2 = dequant_int4(layer.q2[e], layer.s2[e], g2, wl.group_size)
+        z13 = None if layer.z13 is None else layer.z13[e]
+        z2 = None if layer.z2 is None else layer.z2[e]
+        w13 = dequant_int4(layer.q13[e], layer.s13[e], g13, wl.group_size, z13)
+        w2 = dequant_int4(layer.q2[e], layer.s2[e], g2, wl.group_size, z2)
+    elif wl.qt == "int8g":
+        w13 = dequant_int8_group(layer.q13[e], layer.s13[e], wl.group_size)
+        w2 = dequant_int8_group(layer.q2[e], layer.s2[e], wl.group_size)
     else:
         w13 = dequant_int8(layer.q13[e], layer.s13[e])
         w2 = dequant_int8(layer.q2[e], layer.s2[e])

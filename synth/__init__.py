@@ -16,6 +16,8 @@ from .gen import (  # noqa: F401
     make_layer,
     make_inputs,
     quantize_int4_rtn,
+    quantize_int4_rtn_zp,
+    quantize_int8_group,
     quantize_int8_rtn,
     round_to,
     round_to_bf16,

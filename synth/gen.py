@@ -32,8 +32,9 @@ class Workload:
     k: int            # top-k
     H: int            # hidden size
     I: int            # expert intermediate size
-    qt: str           # "int4" (group scales, zero point 8) or "int8" (per output column)
-    group_size: int   # 128 for int4, -1 (one group per column) for int8
+    qt: str           # "int4" (zero point 8), "int4zp" (per-group zero points), "int8" (per
+                      # output column) or "int8g" (group scales)
+    group_size: int   # 128 or -1 (whole K is one group) for int4 / int4zp; -1 for int8; 128 for int8g
     act: str          # activation / scale storage type: "f16" or "bf16"
     act_order: bool   # int4 only: random per-expert g_idx permutation
     zipf: float       # 0: unbiased router; >0: Zipf exponent of the per-expert logit bias
@@ -45,10 +46,15 @@ class Workload:
         return 2.0 * M * self.k * 3.0 * self.H * self.I
 
     def expert_weight_bytes(self) -> int:
-        """Stored weight + scale bytes of one expert (W13 and W2)."""
+        """Stored weight + scale (+ zero point) bytes of one expert (W13 and W2)."""
         n = 3 * self.H * self.I
+        groups = (2 * self.I + self.H) if self.group_size < 0 else n // self.group_size
         if self.qt == "int4":
-            return n // 2 + (n // self.group_size) * 2
+            return n // 2 + groups * 2
+        if self.qt == "int4zp":
+            return n // 2 + groups * 2 + groups // 2
+        if self.qt == "int8g":
+            return n + groups * 2
         return n + (2 * self.I + self.H) * 4
 
 
@@ -121,7 +127,7 @@ def quantize_int4_rtn(w: np.ndarray, group_size: int, g_idx: np.ndarray | None,
     storage type; codes = clamp(rint(w/scale), -8, 7) + 8.
     """
     N, K = w.shape
-    G = group_size
+    G = K if group_size < 0 else group_size
     ng = K // G
     if g_idx is None:
         g_idx = (np.arange(K) // G).astype(np.int32)
@@ -134,6 +140,45 @@ def quantize_int4_rtn(w: np.ndarray, group_size: int, g_idx: np.ndarray | None,
     s_el = s[:, g_idx]                                # [N, K]
     q = np.clip(np.rint(w / s_el), -8, 7) + 8
     return q.astype(np.uint8), np.ascontiguousarray(s.T)
+
+
+def quantize_int4_rtn_zp(w: np.ndarray, group_size: int, g_idx: np.ndarray | None, scale_dtype: str):
+    """Asymmetric int4 (AWQ-style): one scale and one zero point per (group, output row).
+
+    Scale = (max - min)/15 of the group (a constant group gets scale 1), rounded
+    to the storage type; zero point z = clamp(rint(-min/scale), 0, 15); codes =
+    clamp(rint(w/scale) + z, 0, 15).  Returns codes uint8 [N, K], scales float32
+    [K/G, N] and zero points uint8 [K/G, N].
+    """
+    N, K = w.shape
+    G = K if group_size < 0 else group_size
+    ng = K // G
+    if g_idx is None:
+        g_idx = (np.arange(K) // G).astype(np.int32)
+    order = np.argsort(g_idx, kind="stable")
+    grouped = w[:, order].reshape(N, ng, G)
+    lo = grouped.min(axis=2)
+    hi = grouped.max(axis=2)
+    s = (hi - lo) / np.float32(15.0)
+    s[s == 0] = 1.0
+    s = round_to(s, scale_dtype).astype(np.float32)
+    z = np.clip(np.rint(-lo / s), 0, 15).astype(np.float32)
+    q = np.clip(np.rint(w / s[:, g_idx]) + z[:, g_idx], 0, 15)
+    return q.astype(np.uint8), np.ascontiguousarray(s.T), np.ascontiguousarray(z.T.astype(np.uint8))
+
+
+def quantize_int8_group(w: np.ndarray, group_size: int, scale_dtype: str):
+    """Symmetric int8 with one scale per (group of input channels, output row):
+    scale = absmax/127 rounded to the storage type, codes in -127..127.
+    Returns codes int8 [N, K] and scales float32 [K/G, N]."""
+    N, K = w.shape
+    G = group_size
+    absmax = np.abs(w).reshape(N, K // G, G).max(axis=2)
+    s = absmax / np.float32(127.0)
+    s[s == 0] = 1.0
+    s = round_to(s, scale_dtype).astype(np.float32)
+    q = np.clip(np.rint(w / np.repeat(s, G, axis=1)), -127, 127)
+    return q.astype(np.int8), np.ascontiguousarray(s.T)
 
 
 def quantize_int8_rtn(w: np.ndarray):
@@ -152,11 +197,15 @@ def quantize_int8_rtn(w: np.ndarray):
 class QuantLayer:
     """Canonical (pre-pack) quantized expert weights.
 
-    int4: q13 uint8 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), s13 float32
-          [E, H/G, 2I]; q2 uint8 [E, H, I], s2 float32 [E, I/G, H];
-          g13 int32 [E, H] / g2 int32 [E, I] or None (no act-order).
+    int4 / int4zp: q13 uint8 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), s13
+          float32 [E, H/G, 2I]; q2 uint8 [E, H, I], s2 float32 [E, I/G, H];
+          g13 int32 [E, H] / g2 int32 [E, I] or None (no act-order); int4zp
+          also z13 uint8 [E, H/G, 2I], z2 uint8 [E, I/G, H] (G = K when the
+          group size is -1).
     int8: q13 int8 [E, 2I, H], s13 float32 [E, 2I]; q2 int8 [E, H, I],
           s2 float32 [E, H]; no g_idx.
+    int8g: q13 int8 [E, 2I, H], s13 float32 [E, H/G, 2I]; q2 int8 [E, H, I],
+          s2 float32 [E, I/G, H]; no g_idx.
     """
     wl: Workload
     q13: np.ndarray
@@ -165,6 +214,8 @@ class QuantLayer:
     s2: np.ndarray
     g13: np.ndarray | None = None
     g2: np.ndarray | None = None
+    z13: np.ndarray | None = None
+    z2: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
 
 
@@ -183,27 +234,40 @@ def _gen_expert(wl: Workload, seed: int, e: int):
         rng = np.random.default_rng([seed, e, sub])
         w = rng.standard_normal((N, K), dtype=np.float32)
         w *= np.float32(wl.w_std)
-        if wl.qt == "int4":
+        if wl.qt in ("int4", "int4zp"):
             g = None
             if wl.act_order:
                 g = _actorder_gidx(np.random.default_rng([seed, e, 2 + sub]), K, wl.group_size)
-            q, s = quantize_int4_rtn(w, wl.group_size, g, wl.act)
-            out[mat] = (q, s, g)
+            if wl.qt == "int4":
+                q, s = quantize_int4_rtn(w, wl.group_size, g, wl.act)
+                out[mat] = (q, s, g, None)
+            else:
+                q, s, z = quantize_int4_rtn_zp(w, wl.group_size, g, wl.act)
+                out[mat] = (q, s, g, z)
+        elif wl.qt == "int8g":
+            q, s = quantize_int8_group(w, wl.group_size, wl.act)
+            out[mat] = (q, s, None, None)
         else:
             q, s = quantize_int8_rtn(w)
-            out[mat] = (q, s, None)
+            out[mat] = (q, s, None, None)
         del w
     return out
 
 
 def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> QuantLayer:
     E, H, I = wl.E, wl.H, wl.I
-    if wl.qt == "int4":
-        G = wl.group_size
-        q13 = np.empty((E, 2 * I, H), np.uint8)
-        s13 = np.empty((E, H // G, 2 * I), np.float32)
-        q2 = np.empty((E, H, I), np.uint8)
-        s2 = np.empty((E, I // G, H), np.float32)
+    z13 = z2 = None
+    if wl.qt in ("int4", "int4zp", "int8g"):
+        n13 = 1 if wl.group_size < 0 else H // wl.group_size
+        n2 = 1 if wl.group_size < 0 else I // wl.group_size
+        cdt = np.int8 if wl.qt == "int8g" else np.uint8
+        q13 = np.empty((E, 2 * I, H), cdt)
+        s13 = np.empty((E, n13, 2 * I), np.float32)
+        q2 = np.empty((E, H, I), cdt)
+        s2 = np.empty((E, n2, H), np.float32)
+        if wl.qt == "int4zp":
+            z13 = np.empty((E, n13, 2 * I), np.uint8)
+            z2 = np.empty((E, n2, H), np.uint8)
     else:
         q13 = np.empty((E, 2 * I, H), np.int8)
         s13 = np.empty((E, 2 * I), np.float32)
@@ -214,12 +278,16 @@ def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> Quant
 
     def one(e):
         r = _gen_expert(wl, seed, e)
-        q13[e], s13[e], g = r["13"]
+        q13[e], s13[e], g, z = r["13"]
         if g13 is not None:
             g13[e] = g
-        q2[e], s2[e], g = r["2"]
+        if z13 is not None:
+            z13[e] = z
+        q2[e], s2[e], g, z = r["2"]
         if g2 is not None:
             g2[e] = g
+        if z2 is not None:
+            z2[e] = z
 
     if threads is None:
         threads = max(1, min(8, os.cpu_count() or 1))
@@ -230,7 +298,7 @@ def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> Quant
     else:
         for e in range(E):
             one(e)
-    return QuantLayer(wl, q13, s13, q2, s2, g13, g2)
+    return QuantLayer(wl, q13, s13, q2, s2, g13, g2, z13, z2)
 
 
 # ----------------------------------------------------------------------------

@@ -16,7 +16,8 @@ import numpy as np
 import pytest
 
 import oracle
-from synth import QuantLayer, Workload, make_inputs, make_layer, quantize_int4_rtn, quantize_int8_rtn
+from synth import (QuantLayer, Workload, make_inputs, make_layer, quantize_int4_rtn, quantize_int4_rtn_zp,
+                   quantize_int8_group, quantize_int8_rtn)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -290,17 +291,23 @@ def _brute_force(layer, x, ids, w):
     M, k = ids.shape
     out = [[0.0] * H for _ in range(M)]
 
+    def wq(q, s, gi, z, e, n, c):
+        if wl.qt in ("int4", "int4zp", "int8g"):
+            if gi is not None:
+                g = int(gi[e, c])
+            elif wl.group_size < 0:
+                g = 0
+            else:
+                g = c // wl.group_size
+            zero = 0 if wl.qt == "int8g" else (8 if z is None else int(z[e, g, n]))
+            return (int(q[e, n, c]) - zero) * float(s[e, g, n])
+        return int(q[e, n, c]) * float(s[e, n])
+
     def wq13(e, n, c):
-        if wl.qt == "int4":
-            g = c // wl.group_size if layer.g13 is None else int(layer.g13[e, c])
-            return (int(layer.q13[e, n, c]) - 8) * float(layer.s13[e, g, n])
-        return int(layer.q13[e, n, c]) * float(layer.s13[e, n])
+        return wq(layer.q13, layer.s13, layer.g13, layer.z13, e, n, c)
 
     def wq2(e, h, c):
-        if wl.qt == "int4":
-            g = c // wl.group_size if layer.g2 is None else int(layer.g2[e, c])
-            return (int(layer.q2[e, h, c]) - 8) * float(layer.s2[e, g, h])
-        return int(layer.q2[e, h, c]) * float(layer.s2[e, h])
+        return wq(layer.q2, layer.s2, layer.g2, layer.z2, e, h, c)
 
     for m in range(M):
         for j in range(k):
@@ -321,9 +328,11 @@ def _brute_force(layer, x, ids, w):
     return np.array(out)
 
 
-@pytest.mark.parametrize("qt,act_order", [("int4", False), ("int4", True), ("int8", False)])
-def test_brute_force_tiny(qt, act_order):
-    wl = _wl(E=4, k=2, H=32, I=48, qt=qt, group_size=16 if qt == "int4" else -1, act_order=act_order)
+@pytest.mark.parametrize("qt,act_order,gs", [("int4", False, 16), ("int4", True, 16), ("int8", False, -1),
+                                             ("int4zp", False, 16), ("int4zp", True, 16), ("int4", False, -1),
+                                             ("int4zp", False, -1), ("int8g", False, 16)])
+def test_brute_force_tiny(qt, act_order, gs):
+    wl = _wl(E=4, k=2, H=32, I=48, qt=qt, group_size=gs, act_order=act_order)
     layer = make_layer(wl, seed=17)
     inp = make_inputs(wl, 3, seed=17)
     got = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
@@ -449,3 +458,72 @@ def test_route_topk_masked_rows():
     np.testing.assert_allclose(w[1], [1 / 3] * 3)
     _, wn = oracle.route_topk(np.array([[-inf] * 4]), 2, renormalize=False)
     np.testing.assert_allclose(wn[0], [0.25, 0.25])
+
+
+# ----------------------------------------------------------------------------
+# other weight formats: asymmetric int4 (zero points), channel-wise int4, grouped int8
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("act_order", [False, True])
+@pytest.mark.parametrize("sdt", ["f16", "bf16"])
+def test_int4_zero_point_round_trip(act_order, sdt):
+    rng = np.random.default_rng(21)
+    N, K, G = 24, 256, 128
+    w = (rng.standard_normal((N, K)) * 0.02 + 0.01).astype(np.float32)   # off-centre groups
+    g = None
+    if act_order:
+        perm = rng.permutation(K)
+        g = np.empty(K, np.int32)
+        g[perm] = np.arange(K) // G
+    q, s, z = quantize_int4_rtn_zp(w, G, g, sdt)
+    assert q.max() <= 15 and z.max() <= 15
+    wd = oracle.dequant_int4(q, s, g, G, z)
+    gk = (np.arange(K) // G) if g is None else g
+    s_el = s[gk, :].T
+    assert np.all(np.abs(wd - w) <= s_el * (1.0 + 1e-6))                 # within one step
+    inside = (q > 0) & (q < 15)
+    assert np.all(np.abs(wd - w)[inside] <= s_el[inside] * (0.5 + 1e-6))  # half a step unless clipped
+
+
+def test_int4_zero_point_hand_values_and_symmetric_case():
+    q = np.array([[3, 12, 0, 15]], np.uint8)
+    s = np.array([[0.5, 0.25]])                 # [K/G, N] with G = 2, N = 1 -> shape [2, 1]
+    s = s.T
+    z = np.array([[5], [15]], np.uint8)
+    got = oracle.dequant_int4(q, s, None, 2, z)
+    np.testing.assert_array_equal(got, [[-1.0, 3.5, -3.75, 0.0]])
+    # zero points of 8 everywhere are the symmetric format, bit for bit
+    rng = np.random.default_rng(2)
+    q = rng.integers(0, 16, size=(16, 256)).astype(np.uint8)
+    s = rng.random((2, 16)) + 0.1
+    assert np.array_equal(oracle.dequant_int4(q, s, None, 128, np.full((2, 16), 8, np.uint8)),
+                          oracle.dequant_int4(q, s, None, 128))
+
+
+def test_int4_channel_wise_is_one_group():
+    rng = np.random.default_rng(3)
+    q = rng.integers(0, 16, size=(8, 256)).astype(np.uint8)
+    s1 = rng.random((1, 8)) + 0.1
+    a = oracle.dequant_int4(q, s1, None, -1)
+    b = oracle.dequant_int4(q, np.repeat(s1, 2, axis=0), None, 128)   # the same scale in both groups
+    c = oracle.dequant_int4(q, s1, None, 256)
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+    w = rng.standard_normal((8, 256)).astype(np.float32) * 0.02
+    qq, ss = quantize_int4_rtn(w, -1, None, "f16")
+    assert ss.shape == (1, 8)
+    assert np.all(np.abs(oracle.dequant_int4(qq, ss, None, -1) - w) <= ss[0][:, None] * (0.5 + 1e-6))
+
+
+@pytest.mark.parametrize("sdt", ["f16", "bf16"])
+def test_int8_group_round_trip_hand_values_and_per_column_case(sdt):
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((16, 384)) * 0.02).astype(np.float32)
+    q, s = quantize_int8_group(w, 128, sdt)
+    assert s.shape == (3, 16) and np.abs(q.astype(np.int32)).max() <= 127
+    wd = oracle.dequant_int8_group(q, s, 128)
+    assert np.all(np.abs(wd - w) <= np.repeat(s.T, 128, axis=1) * (0.5 + 1e-6))
+    qh = np.array([[-127, 5, 1, -2]], np.int8)
+    sh = np.array([[0.5], [0.25]])
+    np.testing.assert_array_equal(oracle.dequant_int8_group(qh, sh, 2), [[-63.5, 2.5, 0.25, -0.5]])
+    # one scale repeated over every group is the per-column format
+    s_col = rng.random(16) + 0.1
+    assert np.array_equal(oracle.dequant_int8_group(q, np.tile(s_col, (3, 1)), 128), oracle.dequant_int8(q, s_col))
