@@ -69,30 +69,38 @@ typedef enum {
 } qmoe_status;
 
 typedef enum {
-  QMOE_INT4_GROUP = 1,   /* 4-bit codes 0..15, zero point 8, one scale per 128 input channels */
-  QMOE_INT8_PER_COL = 2  /* signed 8-bit codes, one float32 scale per output feature */
+  QMOE_INT4_GROUP = 1,    /* 4-bit codes 0..15, zero point 8, one scale per 128 input channels
+                             (group_size 128) or per output feature (group_size -1) */
+  QMOE_INT8_PER_COL = 2,  /* signed 8-bit codes, one float32 scale per output feature */
+  QMOE_INT4_GROUP_ZP = 3, /* 4-bit codes 0..15 with a zero point 0..15 and a scale per group
+                             (128 input channels, or all of them with group_size -1) */
+  QMOE_INT8_GROUP = 4     /* signed 8-bit codes, one scale per 128 input channels */
 } qmoe_quant_type;
 
 typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
 
 /*
- * One MoE layer, weights already packed by qmoe_pack_int4 / qmoe_pack_int8.
+ * One MoE layer, weights already packed by one of the qmoe_pack_* functions.
  * All pointers are device memory owned by the caller and must stay valid
  * while work that uses them is in flight.
  *
  *   E, H, I      experts, hidden size, expert intermediate size.
  *                Constraints: 1 <= E <= 1024; H % 128 == 0; I % 128 == 0.
- *   group_size   int4: 128 (the only group size built); int8: -1.
+ *   group_size   QMOE_INT4_GROUP / QMOE_INT4_GROUP_ZP: 128 or -1
+ *                (channel-wise); QMOE_INT8_PER_COL: -1; QMOE_INT8_GROUP: 128.
  *   qt           quantization type.
- *   act_dtype    F16 or BF16: type of x and out, and of the MMA operands.
- *   scale_dtype  int4: must equal act_dtype (scales are normalised to the
- *                activation type when packed); int8: F32.
+ *   act_dtype    F16 or BF16: type of x and out (the MMAs run in f16).
+ *   scale_dtype  int4 and grouped int8: must equal act_dtype (scales are
+ *                normalised to the activation type when packed);
+ *                per-column int8: F32.
  *   w13, w2      packed expert weights (sizes: qmoe_packed_bytes), 256-byte aligned.
- *   s13, s2      int8 only: float32 scales packed by qmoe_pack_int8
- *                ([E, 2I] in packed row order, [E, H]); NULL for int4 (int4
- *                scales are inside the packed weights).
- *   perm13       int4 act-order only: int32 [E, H] written by qmoe_pack_int4
- *                (hidden channel of each sorted K position); NULL otherwise.
+ *   s13, s2      per-column int8 only: float32 scales packed by
+ *                qmoe_pack_int8 ([E, 2I] in packed row order, [E, H]); NULL
+ *                otherwise (the other formats keep their scales and zero
+ *                points inside the packed weights).
+ *   perm13       int4 act-order only (group_size 128): int32 [E, H] written
+ *                by qmoe_pack_int4 / qmoe_pack_int4_zp (hidden channel of
+ *                each sorted K position); NULL otherwise.
  *                Act-order of W2 needs no runtime table: it is folded into the
  *                row order of the packed W13.
  */
@@ -137,7 +145,10 @@ typedef struct {
 /*
  * Bytes of one packed matrix for all E experts: W13 is (rows = 2I, K = H),
  * W2 is (rows = H, K = I).  Returns 0 for an unsupported combination.
- * int4: E * (rows/128) * (K/128) * 8448; int8: E * (rows/128) * (K/128) * 16384.
+ * Per 128 x 128 block: QMOE_INT4_GROUP 8448 (group_size 128 or -1),
+ * QMOE_INT4_GROUP_ZP 8576 (group_size 128 or -1), QMOE_INT8_PER_COL 16384
+ * (group_size -1), QMOE_INT8_GROUP 16640 (group_size 128); times
+ * E * (rows/128) * (K/128).
  */
 size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K, int32_t group_size);
 
@@ -153,7 +164,10 @@ size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K,
  * g13 != NULL, perm13_out int32 [E, H]; perm13_out is ignored when g13 == NULL.
  * Act-order requires every group to hold exactly 128 channels (as GPTQ's
  * act-order produces); otherwise QMOE_ERR_UNSUPPORTED.  Codes above 15 give
- * QMOE_ERR_INVALID_ARG.
+ * QMOE_ERR_INVALID_ARG.  group_size -1 is one scale per output feature over
+ * all of K ("Add GPTQ Marlin 2:4 sparse structured support" lists group 128
+ * or -1, channel-wise): s13 is then [E, 1, 2I] and s2 [E, 1, H], and g13 /
+ * g2 must be NULL (QMOE_ERR_UNSUPPORTED otherwise).
  */
 qmoe_status qmoe_pack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
                            const uint8_t* q13, const uint16_t* s13, const int32_t* g13,
@@ -165,6 +179,44 @@ qmoe_status qmoe_unpack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size
                              const void* w13_packed, const void* w2_packed,
                              const int32_t* g13, const int32_t* g2,
                              uint8_t* q13, uint16_t* s13, uint8_t* q2, uint16_t* s2);
+
+/*
+ * Pack asymmetric int4 with one zero point per group ("[WIP] AWQ Faster
+ * Kernels": AWQ checkpoints store per-group zero points):
+ * W[n, k] = (q[n, k] - z[g(k), n]) * s[g(k), n].  Arguments as for
+ * qmoe_pack_int4 plus z13 uint8 [E, H/128, 2I] and z2 uint8 [E, I/128, H]
+ * (zero points 0..15; [E, 1, *] with group_size -1).  Zero points above 15
+ * give QMOE_ERR_INVALID_ARG.  The layer's qt is QMOE_INT4_GROUP_ZP.
+ */
+qmoe_status qmoe_pack_int4_zp(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                              const uint8_t* q13, const uint16_t* s13, const uint8_t* z13, const int32_t* g13,
+                              const uint8_t* q2, const uint16_t* s2, const uint8_t* z2, const int32_t* g2,
+                              void* w13_packed, void* w2_packed, int32_t* perm13_out);
+
+/* Exact inverse of qmoe_pack_int4_zp given the same g13 / g2. */
+qmoe_status qmoe_unpack_int4_zp(int32_t E, int32_t H, int32_t I, int32_t group_size,
+                                const void* w13_packed, const void* w2_packed,
+                                const int32_t* g13, const int32_t* g2,
+                                uint8_t* q13, uint16_t* s13, uint8_t* z13,
+                                uint8_t* q2, uint16_t* s2, uint8_t* z2);
+
+/*
+ * Pack symmetric int8 with one scale per 128 input channels ("Add GPTQ Marlin
+ * 2:4 sparse structured support" lists 8-bit with group 128):
+ * W[n, k] = q[n, k] * s[k / 128, n].  Canonical inputs (host):
+ *   q13 int8 [E, 2I, H], s13 uint16 [E, H/128, 2I] scale bit patterns of
+ *   scale_dtype (f16 or bf16); q2 int8 [E, H, I], s2 uint16 [E, I/128, H].
+ * Outputs (host): w13_packed, w2_packed (the scales live inside the packed
+ * blocks).  Codes of -128 give QMOE_ERR_INVALID_ARG.  The layer's qt is
+ * QMOE_INT8_GROUP with group_size 128.
+ */
+qmoe_status qmoe_pack_int8_group(int32_t E, int32_t H, int32_t I, qmoe_dtype scale_dtype,
+                                 const int8_t* q13, const uint16_t* s13, const int8_t* q2, const uint16_t* s2,
+                                 void* w13_packed, void* w2_packed);
+
+/* Exact inverse of qmoe_pack_int8_group. */
+qmoe_status qmoe_unpack_int8_group(int32_t E, int32_t H, int32_t I, const void* w13_packed, const void* w2_packed,
+                                   int8_t* q13, uint16_t* s13, int8_t* q2, uint16_t* s2);
 
 /*
  * Pack W8A16 per-column int8 ("[Kernel] W8A16 Int8 inside FusedMoE":

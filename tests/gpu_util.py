@@ -22,7 +22,8 @@ def ensure_built():
 def device_layer(layer, device="cuda"):
     wl = layer.wl
     return q.DeviceLayer.from_canonical(wl.qt, wl.act, layer.q13, layer.s13, layer.q2, layer.s2,
-                                        layer.g13, layer.g2, device=device)
+                                        layer.g13, layer.g2, device=device, z13=layer.z13, z2=layer.z2,
+                                        group_size=wl.group_size)
 
 
 def device_inputs(wl, inp, device="cuda"):

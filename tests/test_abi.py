@@ -154,3 +154,65 @@ def test_workspace_size_and_validation_are_host_only():
     assert L.qmoe_moe_align(None, 4, 2, 8, 16, None, None, None, 1000, None) == q.QMOE_ERR_INVALID_ARG
     assert L.qmoe_moe_align(None, 4, 2, 8, 0, None, None, None, 1000, None) == q.QMOE_ERR_INVALID_ARG
     assert L.qmoe_moe_align(None, 4, 2, 8, 16, None, None, None, 10, None) == q.QMOE_ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------
+# other weight formats: zero points, channel-wise int4, grouped int8
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("act_order,gs", [(False, 128), (True, 128), (False, -1)])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_pack_int4_zero_points_round_trip(act_order, gs, act):
+    wl = Workload("zp", 4, 2, 256, 384, "int4zp", gs, act, act_order, 0.0, (1,))
+    L = make_layer(wl, seed=6)
+    s13b, s2b = to_u16_bits(L.s13, act), to_u16_bits(L.s2, act)
+    pk = q.qmoe_pack_int4(wl.E, wl.H, wl.I, act, L.q13, s13b, L.g13, L.q2, s2b, L.g2, gs, L.z13, L.z2)
+    assert pk["w13"].nbytes == wl.E * (2 * wl.I // 128) * (wl.H // 128) * 8576
+    q13, s13, q2, s2, z13, z2 = q.qmoe_unpack_int4(wl.E, wl.H, wl.I, pk["w13"], pk["w2"], L.g13, L.g2, gs, zp=True)
+    assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
+    assert np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
+    assert np.array_equal(z13, L.z13) and np.array_equal(z2, L.z2)
+
+
+def test_pack_int4_channel_wise_round_trip_and_block_scales():
+    wl = Workload("cw", 2, 2, 256, 256, "int4", -1, "f16", False, 0.0, (1,))
+    L = make_layer(wl, seed=7)
+    assert L.s13.shape == (2, 1, 512)
+    s13b, s2b = to_u16_bits(L.s13, "f16"), to_u16_bits(L.s2, "f16")
+    pk = q.qmoe_pack_int4(wl.E, wl.H, wl.I, "f16", L.q13, s13b, None, L.q2, s2b, None, -1)
+    q13, s13, q2, s2 = q.qmoe_unpack_int4(wl.E, wl.H, wl.I, pk["w13"], pk["w2"], None, None, -1)
+    assert np.array_equal(q13, L.q13) and np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
+    # every K block of a W2 tile carries the row's one scale (bytes 8192.. of each 8448-byte block)
+    blk = pk["w2"][: (wl.I // 128) * 8448].reshape(wl.I // 128, 8448)
+    sc = blk[:, 8192:8448].view(np.uint16)
+    assert np.array_equal(sc[0], sc[1]) and np.array_equal(sc[0], s2b[0, 0, :128])
+    # channel-wise scales cannot carry an act-order g_idx
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_pack_int4(wl.E, wl.H, wl.I, "f16", L.q13, s13b, np.zeros((2, 256), np.int32), L.q2, s2b, None, -1)
+    assert ei.value.status == q.QMOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_pack_int8_group_round_trip(act):
+    wl = Workload("i8g", 3, 2, 256, 384, "int8g", 128, act, False, 0.0, (1,))
+    L = make_layer(wl, seed=8)
+    s13b, s2b = to_u16_bits(L.s13, act), to_u16_bits(L.s2, act)
+    pk = q.qmoe_pack_int8_group(wl.E, wl.H, wl.I, act, L.q13, s13b, L.q2, s2b)
+    assert pk["w13"].nbytes == wl.E * (2 * wl.I // 128) * (wl.H // 128) * 16640
+    q13, s13, q2, s2 = q.qmoe_unpack_int8_group(wl.E, wl.H, wl.I, pk["w13"], pk["w2"])
+    assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
+    assert np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
+
+
+def test_pack_rejects_bad_zero_points():
+    wl = Workload("zp", 1, 2, 128, 128, "int4zp", 128, "f16", False, 0.0, (1,))
+    L = make_layer(wl, seed=9)
+    s13b, s2b = to_u16_bits(L.s13, "f16"), to_u16_bits(L.s2, "f16")
+    z13 = L.z13.copy()
+    z13[0, 0, 3] = 16
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_pack_int4(1, 128, 128, "f16", L.q13, s13b, None, L.q2, s2b, None, 128, z13, L.z2)
+    assert ei.value.status == q.QMOE_ERR_INVALID_ARG
+    assert q.packed_bytes("int4zp", 1, 256, 128) == 2 * 8576
+    assert q.packed_bytes("int8g", 1, 256, 128) == 2 * 16640
+    assert q.packed_bytes("int4", 1, 256, 128, -1) == 2 * 8448
+    assert q.packed_bytes("int8g", 1, 256, 128, -1) == 0

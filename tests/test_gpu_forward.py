@@ -21,9 +21,10 @@ def _built():
     ensure_built()
 
 
-def _wl(qt="int4", act="f16", act_order=False, E=8, k=2, H=384, I=256, zipf=0.0):
-    return Workload(f"t_{qt}_{act}_{act_order}", E, k, H, I, qt, 128 if qt == "int4" else -1, act, act_order,
-                    zipf, (1,))
+def _wl(qt="int4", act="f16", act_order=False, E=8, k=2, H=384, I=256, zipf=0.0, gs=None):
+    if gs is None:
+        gs = -1 if qt == "int8" else 128
+    return Workload(f"t_{qt}_{act}_{act_order}_{gs}", E, k, H, I, qt, gs, act, act_order, zipf, (1,))
 
 
 _LAYERS = {}
@@ -50,12 +51,28 @@ def _check(wl, M, seed=0, opts=None, inp=None, what=""):
 
 VARIANTS = [("int4", "f16", False), ("int4", "bf16", False), ("int4", "f16", True), ("int4", "bf16", True),
             ("int8", "bf16", False), ("int8", "f16", False)]
+# weight formats beyond the pages' two: per-group zero points, channel-wise int4, group-128 int8
+OTHER_FORMATS = [("int4zp", "f16", False, 128), ("int4zp", "bf16", True, 128), ("int4zp", "bf16", False, -1),
+                 ("int4", "f16", False, -1), ("int4", "bf16", False, -1), ("int8g", "f16", False, 128),
+                 ("int8g", "bf16", False, 128)]
 
 
 @pytest.mark.parametrize("qt,act,ao", VARIANTS)
 @pytest.mark.parametrize("M", [1, 7, 64, 129])
 def test_forward_parity(qt, act, ao, M):
     _check(_wl(qt, act, ao), M)
+
+
+@pytest.mark.parametrize("qt,act,ao,gs", OTHER_FORMATS)
+@pytest.mark.parametrize("M", [1, 40, 129])
+def test_forward_parity_other_formats(qt, act, ao, gs, M):
+    _check(_wl(qt, act, ao, gs=gs), M)
+
+
+@pytest.mark.parametrize("qt,act,ao,gs", OTHER_FORMATS[:2] + OTHER_FORMATS[5:6])
+@pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 128)])
+def test_forward_other_formats_forced_split_and_tile(qt, act, ao, gs, split1, split2, tile):
+    _check(_wl(qt, act, ao, gs=gs), 40, opts=q.make_options(split1, split2, tile))
 
 
 @pytest.mark.parametrize("qt,act,ao", VARIANTS[:1] + VARIANTS[3:5])

@@ -9,13 +9,21 @@ import torch
 
 import oracle
 import weight_only_quantized_moe_gb300 as q
-from synth import WORKLOADS, make_inputs, make_layer
+from synth import WORKLOADS, Workload, make_inputs, make_layer
 from tests.gpu_util import assert_parity, device_inputs, device_layer, ensure_built, run_forward
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
+# the Mixtral-8x7B shape in the other weight formats (zero points, group-128 int8)
+WORKLOADS_OTHER = {
+    "mixtral8x7b_w4zp": Workload("mixtral8x7b_w4zp", 8, 2, 4096, 14336, "int4zp", 128, "bf16", False, 0.0, (16,)),
+    "mixtral8x7b_w8g": Workload("mixtral8x7b_w8g", 8, 2, 4096, 14336, "int8g", 128, "f16", False, 0.0, (16,)),
+}
+
 # (workload, M, number of sampled tokens)
 CASES = [
+    ("mixtral8x7b_w4zp", 16, 2),
+    ("mixtral8x7b_w8g", 16, 2),
     ("mixtral8x7b_w4", 16, 4),
     ("mixtral8x7b_w4", 1, 1),
     ("mixtral8x7b_w4_actorder", 16, 3),
@@ -38,14 +46,14 @@ def _layer(name):
         _cache.clear()
         gc.collect()
         torch.cuda.empty_cache()
-        L = make_layer(WORKLOADS[name], seed=0)
+        L = make_layer(WORKLOADS.get(name) or WORKLOADS_OTHER[name], seed=0)
         _cache[name] = (L, device_layer(L))
     return _cache[name]
 
 
 @pytest.mark.parametrize("name,M,n_sample", CASES)
 def test_full_size_sampled(name, M, n_sample):
-    wl = WORKLOADS[name]
+    wl = WORKLOADS.get(name) or WORKLOADS_OTHER[name]
     L, dl = _layer(name)
     inp = make_inputs(wl, M, seed=0)
     x, ids, w = device_inputs(wl, inp)

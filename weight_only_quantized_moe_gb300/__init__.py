@@ -22,6 +22,7 @@ from ._native import (  # noqa: F401
 from .api import (  # noqa: F401
     DeviceLayer,
     alloc_workspace,
+    default_group_size,
     make_options,
     packed_bytes,
     qmoe_forward,
@@ -32,9 +33,11 @@ from .api import (  # noqa: F401
     qmoe_moe_align,
     qmoe_pack_int4,
     qmoe_pack_int8,
+    qmoe_pack_int8_group,
     qmoe_read_device_status,
     qmoe_route_topk,
     qmoe_unpack_int4,
+    qmoe_unpack_int8_group,
     qmoe_workspace_size_logits,
     qmoe_unpack_int8,
     qmoe_workspace_size,

@@ -14,7 +14,12 @@ from . import _native as N
 
 _ACT = {"f16": N.QMOE_F16, "bf16": N.QMOE_BF16}
 _TORCH_ACT = {"f16": torch.float16, "bf16": torch.bfloat16}
-_QT = {"int4": N.QMOE_INT4_GROUP, "int8": N.QMOE_INT8_PER_COL}
+_QT = {"int4": N.QMOE_INT4_GROUP, "int4zp": N.QMOE_INT4_GROUP_ZP, "int8": N.QMOE_INT8_PER_COL,
+       "int8g": N.QMOE_INT8_GROUP}
+
+
+def default_group_size(qt: str) -> int:
+    return -1 if qt == "int8" else 128
 
 
 def _np_ptr(a, ctype):
@@ -27,43 +32,97 @@ def _stream_ptr(stream):
     return c_void_p(stream.cuda_stream)
 
 
-def packed_bytes(qt: str, E: int, rows: int, K: int) -> int:
-    return int(N.lib().qmoe_packed_bytes(_QT[qt], E, rows, K, 128 if qt == "int4" else -1))
+def packed_bytes(qt: str, E: int, rows: int, K: int, group_size: int | None = None) -> int:
+    gs = default_group_size(qt) if group_size is None else group_size
+    return int(N.lib().qmoe_packed_bytes(_QT[qt], E, rows, K, gs))
 
 
 # ----------------------------------------------------------------------------
 # packing (host)
 # ----------------------------------------------------------------------------
-def qmoe_pack_int4(E, H, I, scale_dtype, q13, s13_bits, g13, q2, s2_bits, g2):
-    """Pack canonical int4 weights (see include/qmoe.h).  Scales are uint16 bit patterns."""
+def qmoe_pack_int4(E, H, I, scale_dtype, q13, s13_bits, g13, q2, s2_bits, g2, group_size=128, z13=None, z2=None):
+    """Pack canonical int4 weights (see include/qmoe.h).  Scales are uint16 bit
+    patterns [E, K/G, N] ([E, 1, N] with group_size -1); zero points z13/z2
+    (uint8, same shapes) select the asymmetric format (qmoe_pack_int4_zp)."""
     q13 = np.ascontiguousarray(q13, np.uint8)
     q2 = np.ascontiguousarray(q2, np.uint8)
     s13_bits = np.ascontiguousarray(s13_bits, np.uint16)
     s2_bits = np.ascontiguousarray(s2_bits, np.uint16)
     g13 = None if g13 is None else np.ascontiguousarray(g13, np.int32)
     g2 = None if g2 is None else np.ascontiguousarray(g2, np.int32)
-    w13 = np.empty(packed_bytes("int4", E, 2 * I, H), np.uint8)
-    w2 = np.empty(packed_bytes("int4", E, H, I), np.uint8)
+    qt = "int4" if z13 is None else "int4zp"
+    w13 = np.empty(packed_bytes(qt, E, 2 * I, H, group_size), np.uint8)
+    w2 = np.empty(packed_bytes(qt, E, H, I, group_size), np.uint8)
     perm13 = np.empty((E, H), np.int32) if g13 is not None else None
-    st = N.lib().qmoe_pack_int4(E, H, I, 128, _ACT[scale_dtype], _np_ptr(q13, c_uint8), _np_ptr(s13_bits, c_uint16),
-                                _np_ptr(g13, c_int32), _np_ptr(q2, c_uint8), _np_ptr(s2_bits, c_uint16),
-                                _np_ptr(g2, c_int32), w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
-                                _np_ptr(perm13, c_int32))
-    N.check(st, "qmoe_pack_int4")
+    if z13 is None:
+        st = N.lib().qmoe_pack_int4(E, H, I, group_size, _ACT[scale_dtype], _np_ptr(q13, c_uint8),
+                                    _np_ptr(s13_bits, c_uint16), _np_ptr(g13, c_int32), _np_ptr(q2, c_uint8),
+                                    _np_ptr(s2_bits, c_uint16), _np_ptr(g2, c_int32), w13.ctypes.data_as(c_void_p),
+                                    w2.ctypes.data_as(c_void_p), _np_ptr(perm13, c_int32))
+        N.check(st, "qmoe_pack_int4")
+    else:
+        z13 = np.ascontiguousarray(z13, np.uint8)
+        z2 = np.ascontiguousarray(z2, np.uint8)
+        st = N.lib().qmoe_pack_int4_zp(E, H, I, group_size, _ACT[scale_dtype], _np_ptr(q13, c_uint8),
+                                       _np_ptr(s13_bits, c_uint16), _np_ptr(z13, c_uint8), _np_ptr(g13, c_int32),
+                                       _np_ptr(q2, c_uint8), _np_ptr(s2_bits, c_uint16), _np_ptr(z2, c_uint8),
+                                       _np_ptr(g2, c_int32), w13.ctypes.data_as(c_void_p),
+                                       w2.ctypes.data_as(c_void_p), _np_ptr(perm13, c_int32))
+        N.check(st, "qmoe_pack_int4_zp")
     return {"w13": w13, "w2": w2, "perm13": perm13}
 
 
-def qmoe_unpack_int4(E, H, I, w13, w2, g13, g2):
+def qmoe_unpack_int4(E, H, I, w13, w2, g13, g2, group_size=128, zp=False):
+    """Inverse of qmoe_pack_int4: (q13, s13, q2, s2), plus (z13, z2) when ``zp``."""
+    n13 = 1 if group_size < 0 else H // 128
+    n2 = 1 if group_size < 0 else I // 128
     q13 = np.empty((E, 2 * I, H), np.uint8)
-    s13 = np.empty((E, H // 128, 2 * I), np.uint16)
+    s13 = np.empty((E, n13, 2 * I), np.uint16)
     q2 = np.empty((E, H, I), np.uint8)
-    s2 = np.empty((E, I // 128, H), np.uint16)
+    s2 = np.empty((E, n2, H), np.uint16)
     g13 = None if g13 is None else np.ascontiguousarray(g13, np.int32)
     g2 = None if g2 is None else np.ascontiguousarray(g2, np.int32)
-    st = N.lib().qmoe_unpack_int4(E, H, I, 128, w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
-                                  _np_ptr(g13, c_int32), _np_ptr(g2, c_int32), _np_ptr(q13, c_uint8),
-                                  _np_ptr(s13, c_uint16), _np_ptr(q2, c_uint8), _np_ptr(s2, c_uint16))
-    N.check(st, "qmoe_unpack_int4")
+    if not zp:
+        st = N.lib().qmoe_unpack_int4(E, H, I, group_size, w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
+                                      _np_ptr(g13, c_int32), _np_ptr(g2, c_int32), _np_ptr(q13, c_uint8),
+                                      _np_ptr(s13, c_uint16), _np_ptr(q2, c_uint8), _np_ptr(s2, c_uint16))
+        N.check(st, "qmoe_unpack_int4")
+        return q13, s13, q2, s2
+    z13 = np.empty((E, n13, 2 * I), np.uint8)
+    z2 = np.empty((E, n2, H), np.uint8)
+    st = N.lib().qmoe_unpack_int4_zp(E, H, I, group_size, w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
+                                     _np_ptr(g13, c_int32), _np_ptr(g2, c_int32), _np_ptr(q13, c_uint8),
+                                     _np_ptr(s13, c_uint16), _np_ptr(z13, c_uint8), _np_ptr(q2, c_uint8),
+                                     _np_ptr(s2, c_uint16), _np_ptr(z2, c_uint8))
+    N.check(st, "qmoe_unpack_int4_zp")
+    return q13, s13, q2, s2, z13, z2
+
+
+def qmoe_pack_int8_group(E, H, I, scale_dtype, q13, s13_bits, q2, s2_bits):
+    """Pack canonical group-128 int8 weights (scales as uint16 bit patterns [E, K/128, N])."""
+    q13 = np.ascontiguousarray(q13, np.int8)
+    q2 = np.ascontiguousarray(q2, np.int8)
+    s13_bits = np.ascontiguousarray(s13_bits, np.uint16)
+    s2_bits = np.ascontiguousarray(s2_bits, np.uint16)
+    w13 = np.empty(packed_bytes("int8g", E, 2 * I, H), np.uint8)
+    w2 = np.empty(packed_bytes("int8g", E, H, I), np.uint8)
+    st = N.lib().qmoe_pack_int8_group(E, H, I, _ACT[scale_dtype], q13.ctypes.data_as(c_void_p),
+                                      _np_ptr(s13_bits, c_uint16), q2.ctypes.data_as(c_void_p),
+                                      _np_ptr(s2_bits, c_uint16), w13.ctypes.data_as(c_void_p),
+                                      w2.ctypes.data_as(c_void_p))
+    N.check(st, "qmoe_pack_int8_group")
+    return {"w13": w13, "w2": w2}
+
+
+def qmoe_unpack_int8_group(E, H, I, w13, w2):
+    q13 = np.empty((E, 2 * I, H), np.int8)
+    s13 = np.empty((E, H // 128, 2 * I), np.uint16)
+    q2 = np.empty((E, H, I), np.int8)
+    s2 = np.empty((E, I // 128, H), np.uint16)
+    st = N.lib().qmoe_unpack_int8_group(E, H, I, w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
+                                        q13.ctypes.data_as(c_void_p), _np_ptr(s13, c_uint16),
+                                        q2.ctypes.data_as(c_void_p), _np_ptr(s2, c_uint16))
+    N.check(st, "qmoe_unpack_int8_group")
     return q13, s13, q2, s2
 
 
@@ -107,12 +166,13 @@ def _scale_bits(s: np.ndarray, act: str) -> np.ndarray:
 class DeviceLayer:
     """A packed layer resident on one CUDA device plus its C descriptor."""
 
-    def __init__(self, qt, E, H, I, act, w13, w2, s13=None, s2=None, perm13=None):
+    def __init__(self, qt, E, H, I, act, w13, w2, s13=None, s2=None, perm13=None, group_size=None):
         self.qt, self.E, self.H, self.I, self.act = qt, E, H, I, act
+        self.group_size = default_group_size(qt) if group_size is None else group_size
         self.w13, self.w2, self.s13, self.s2, self.perm13 = w13, w2, s13, s2, perm13
         self.struct = N.QmoeLayer(
-            E, H, I, 128 if qt == "int4" else -1, _QT[qt], _ACT[act],
-            _ACT[act] if qt == "int4" else N.QMOE_F32,
+            E, H, I, self.group_size, _QT[qt], _ACT[act],
+            N.QMOE_F32 if qt == "int8" else _ACT[act],
             w13.data_ptr(), w2.data_ptr(),
             None if s13 is None else s13.data_ptr(), None if s2 is None else s2.data_ptr(),
             None if perm13 is None else perm13.data_ptr())
@@ -128,7 +188,7 @@ class DeviceLayer:
         return n
 
     @classmethod
-    def from_packed(cls, qt, E, H, I, act, packed, device="cuda"):
+    def from_packed(cls, qt, E, H, I, act, packed, device="cuda", group_size=None):
         def dev(a, dt=None):
             if a is None:
                 return None
@@ -136,22 +196,29 @@ class DeviceLayer:
         return cls(qt, E, H, I, act, dev(packed["w13"]), dev(packed["w2"]),
                    dev(packed.get("s13")) if qt == "int8" else None,
                    dev(packed.get("s2")) if qt == "int8" else None,
-                   dev(packed.get("perm13")))
+                   dev(packed.get("perm13")), group_size)
 
     @classmethod
-    def from_canonical(cls, qt, act, q13, s13, q2, s2, g13=None, g2=None, device="cuda"):
+    def from_canonical(cls, qt, act, q13, s13, q2, s2, g13=None, g2=None, device="cuda", z13=None, z2=None,
+                       group_size=None):
         """Pack canonical codes/scales on the host and upload them.
 
-        int4: q uint8 codes, s float32 [E, K/128, N] (exact in ``act``), g int32 or None.
-        int8: q int8 codes, s float32 [E, N].
+        int4 / int4zp: q uint8 codes, s float32 [E, K/G, N] (exact in ``act``;
+        G = K for group_size -1), g int32 or None, int4zp zero points z uint8
+        like s.  int8: q int8 codes, s float32 [E, N].  int8g: q int8 codes,
+        s float32 [E, K/128, N] (exact in ``act``).
         """
         E, N2, H = q13.shape
         I = N2 // 2
-        if qt == "int4":
-            packed = qmoe_pack_int4(E, H, I, act, q13, _scale_bits(s13, act), g13, q2, _scale_bits(s2, act), g2)
+        gs = default_group_size(qt) if group_size is None else group_size
+        if qt in ("int4", "int4zp"):
+            packed = qmoe_pack_int4(E, H, I, act, q13, _scale_bits(s13, act), g13, q2, _scale_bits(s2, act), g2,
+                                    gs, z13 if qt == "int4zp" else None, z2 if qt == "int4zp" else None)
+        elif qt == "int8g":
+            packed = qmoe_pack_int8_group(E, H, I, act, q13, _scale_bits(s13, act), q2, _scale_bits(s2, act))
         else:
             packed = qmoe_pack_int8(E, H, I, q13, s13, q2, s2)
-        return cls.from_packed(qt, E, H, I, act, packed, device)
+        return cls.from_packed(qt, E, H, I, act, packed, device, gs)
 
 
 # ----------------------------------------------------------------------------

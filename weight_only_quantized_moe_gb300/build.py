@@ -29,7 +29,11 @@ SOURCES = [
     "gemm_dispatch.cu",
     "gemm_i4_f16.cu",
     "gemm_i4_bf16.cu",
+    "gemm_i4z_f16.cu",
+    "gemm_i4z_bf16.cu",
     "gemm_i8.cu",
+    "gemm_i8g_f16.cu",
+    "gemm_i8g_bf16.cu",
     "noalloc.cu",
 ]
 

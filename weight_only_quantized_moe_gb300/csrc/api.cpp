@@ -76,14 +76,37 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ---------------------------------------------------------------------------
 // layer validation and the forward plan
 // ---------------------------------------------------------------------------
+int stage_bytes_of(int32_t qt) {
+  switch (qt) {
+    case QMOE_INT4_GROUP: return kInt4StageBytes;
+    case QMOE_INT4_GROUP_ZP: return kInt4ZpStageBytes;
+    case QMOE_INT8_GROUP: return kInt8GroupStageBytes;
+    default: return kInt8StageBytes;
+  }
+}
+
+QuantKind kind_of(int32_t qt) {
+  switch (qt) {
+    case QMOE_INT4_GROUP: return kQ4;
+    case QMOE_INT4_GROUP_ZP: return kQ4Z;
+    case QMOE_INT8_GROUP: return kQ8G;
+    default: return kQ8;
+  }
+}
+
 qmoe_status validate_layer_dims(const qmoe_layer* L) {
   if (L == nullptr) return QMOE_ERR_INVALID_ARG;
   if (L->E < 1 || L->E > 1024 || L->H <= 0 || L->I <= 0) return QMOE_ERR_INVALID_ARG;
   if (L->H % 128 != 0 || L->I % 128 != 0) return QMOE_ERR_UNSUPPORTED;
   if (L->act_dtype != QMOE_F16 && L->act_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
-  if (L->qt == QMOE_INT4_GROUP) {
+  if (L->qt == QMOE_INT4_GROUP || L->qt == QMOE_INT4_GROUP_ZP) {
+    if (L->group_size != 128 && L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
+    if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
+    if (L->group_size == -1 && L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
+  } else if (L->qt == QMOE_INT8_GROUP) {
     if (L->group_size != 128) return QMOE_ERR_UNSUPPORTED;
     if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
+    if (L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
   } else if (L->qt == QMOE_INT8_PER_COL) {
     if (L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
     if (L->scale_dtype != QMOE_F32) return QMOE_ERR_UNSUPPORTED;
@@ -147,9 +170,8 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     if (o->token_tile < 16 || o->token_tile > kMaxTokenTile || o->token_tile % 16 != 0) return QMOE_ERR_INVALID_ARG;
     T = o->token_tile;
   }
-  const bool int4 = L->qt == QMOE_INT4_GROUP;
   p.T = T;
-  p.stage_bytes = int4 ? kInt4StageBytes : kInt8StageBytes;
+  p.stage_bytes = stage_bytes_of(L->qt);
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
@@ -240,15 +262,17 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const void* ptrs[] = {x, topk_ids, topk_weights, out, ws, L->w13, L->w2};
   for (const void* p : ptrs)
     if ((st = check_dev_ptr(p, dev)) != QMOE_OK) return st;
-  const bool int4 = L->qt == QMOE_INT4_GROUP;
-  if (!int4) {
+  // only per-column int8 keeps its scales outside the packed weight blocks
+  const bool row_scales = L->qt == QMOE_INT8_PER_COL;
+  if (row_scales) {
     if ((st = check_dev_ptr(L->s13, dev)) != QMOE_OK) return st;
     if ((st = check_dev_ptr(L->s2, dev)) != QMOE_OK) return st;
   }
   if (L->perm13 != nullptr && (st = check_dev_ptr(L->perm13, dev)) != QMOE_OK) return st;
   if (!aligned(x, 256) || !aligned(out, 256) || !aligned(ws, 256) || !aligned(L->w13, 256) ||
       !aligned(L->w2, 256) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
-      (L->perm13 != nullptr && !aligned(L->perm13, 16)) || (!int4 && (!aligned(L->s13, 16) || !aligned(L->s2, 16))))
+      (L->perm13 != nullptr && !aligned(L->perm13, 16)) ||
+      (row_scales && (!aligned(L->s13, 16) || !aligned(L->s2, 16))))
     return QMOE_ERR_INVALID_ARG;
 
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -290,7 +314,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.w = static_cast<const uint8_t*>(L->w13);
   g1.b = static_cast<const uint8_t*>(xg);
   g1.b_unit_stride = pl.cap * 256;
-  g1.row_scale = int4 ? nullptr : L->s13;
+  g1.row_scale = row_scales ? L->s13 : nullptr;
   g1.col_scale = xscale;
   g1.chunks = chunks;
   g1.n_chunks = nch;
@@ -326,7 +350,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g2.w = static_cast<const uint8_t*>(L->w2);
   g2.b = static_cast<const uint8_t*>(inter16);
   g2.b_unit_stride = pl.cap * 256;
-  g2.row_scale = int4 ? nullptr : L->s2;
+  g2.row_scale = row_scales ? L->s2 : nullptr;
   g2.col_scale = iscale;
   g2.n_tiles = pl.n_tiles2;
   g2.k_groups = pl.kst2;
@@ -343,7 +367,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
-    err = launch_gemm(int4, bf16, g1, grid1, stream);  // int4 scales have the activation dtype
+    err = launch_gemm(kind_of(L->qt), bf16, g1, grid1, stream);  // in-block scales have the activation dtype
     launched += (err == cudaSuccess);
   }
   rec(5);
@@ -361,7 +385,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(9);
   rec(10);
   if (err == cudaSuccess) {
-    err = launch_gemm(int4, bf16, g2, grid2, stream);
+    err = launch_gemm(kind_of(L->qt), bf16, g2, grid2, stream);
     launched += (err == cudaSuccess);
   }
   rec(11);
@@ -407,15 +431,21 @@ inline int w13_canon_row(int t, int r, int I, const int32_t* perm2) {
   return (r & 1) ? I + j : j;
 }
 
-// int4 tile stage: 4 chunks x 128 rows x 16 B, then 128 x 2 B scales.
+// int4 tile stage: 4 chunks x 128 rows x 16 B, then 128 x 2 B scales (and, with
+// zero points, 128 x 1 B zero points).
 // Chunk c of a row holds sorted K = 32c..32c+31; word j of it holds
 // K = 32c+8j .. +7 with nibble i <- K 32c+8j+2i and nibble i+4 <- K 32c+8j+2i+1.
-void pack_int4_matrix(const uint8_t* q, const uint16_t* s, int rows, int K, int I_for_w13, const int32_t* perm2_rows,
-                      const int32_t* kperm, uint8_t* out, std::atomic<bool>& bad) {
+// s (and z) are [groups][rows]; with one group over all of K (channel-wise) the
+// row's one scale is repeated in every stage block.
+void pack_int4_matrix(const uint8_t* q, const uint16_t* s, const uint8_t* z, bool channel_wise, int rows, int K,
+                      int I_for_w13, const int32_t* perm2_rows, const int32_t* kperm, uint8_t* out,
+                      std::atomic<bool>& bad) {
   const int n_tiles = rows / 128, kst = K / 128;
+  const size_t blk_bytes = z ? kInt4ZpStageBytes : kInt4StageBytes;
   for (int t = 0; t < n_tiles; ++t)
     for (int ks = 0; ks < kst; ++ks) {
-      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * kInt4StageBytes;
+      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * blk_bytes;
+      const int grp = channel_wise ? 0 : ks;
       for (int r = 0; r < 128; ++r) {
         const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, perm2_rows) : t * 128 + r;
         const uint8_t* qrow = q + static_cast<size_t>(cr) * K;
@@ -437,19 +467,26 @@ void pack_int4_matrix(const uint8_t* q, const uint16_t* s, int rows, int K, int 
             dst[2] = (word >> 16) & 0xFF;
             dst[3] = (word >> 24) & 0xFF;
           }
-        const uint16_t sb = s[static_cast<size_t>(ks) * rows + cr];
+        const uint16_t sb = s[static_cast<size_t>(grp) * rows + cr];
         blk[8192 + r * 2] = sb & 0xFF;
         blk[8192 + r * 2 + 1] = sb >> 8;
+        if (z) {
+          const uint8_t zv = z[static_cast<size_t>(grp) * rows + cr];
+          if (zv > 15) bad = true;
+          blk[8448 + r] = zv;
+        }
       }
     }
 }
 
-void unpack_int4_matrix(const uint8_t* in, int rows, int K, int I_for_w13, const int32_t* perm2_rows,
-                        const int32_t* kperm, uint8_t* q, uint16_t* s) {
+void unpack_int4_matrix(const uint8_t* in, bool zp, bool channel_wise, int rows, int K, int I_for_w13,
+                        const int32_t* perm2_rows, const int32_t* kperm, uint8_t* q, uint16_t* s, uint8_t* z) {
   const int n_tiles = rows / 128, kst = K / 128;
+  const size_t blk_bytes = zp ? kInt4ZpStageBytes : kInt4StageBytes;
   for (int t = 0; t < n_tiles; ++t)
     for (int ks = 0; ks < kst; ++ks) {
-      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * kInt4StageBytes;
+      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * blk_bytes;
+      const int grp = channel_wise ? 0 : ks;
       for (int r = 0; r < 128; ++r) {
         const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, perm2_rows) : t * 128 + r;
         uint8_t* qrow = q + static_cast<size_t>(cr) * K;
@@ -463,17 +500,21 @@ void unpack_int4_matrix(const uint8_t* in, int rows, int K, int I_for_w13, const
               qrow[kperm ? kperm[k0 + 1] : k0 + 1] = (word >> (4 * (i + 4))) & 15;
             }
           }
-        s[static_cast<size_t>(ks) * rows + cr] = static_cast<uint16_t>(blk[8192 + r * 2] | (blk[8192 + r * 2 + 1] << 8));
+        s[static_cast<size_t>(grp) * rows + cr] = static_cast<uint16_t>(blk[8192 + r * 2] | (blk[8192 + r * 2 + 1] << 8));
+        if (zp && z) z[static_cast<size_t>(grp) * rows + cr] = blk[8448 + r];
       }
     }
 }
 
-// int8 tile stage: 8 chunks x 128 rows x 16 B; chunk c holds K = 16c..16c+15 in byte order.
-void pack_int8_matrix(const int8_t* q, int rows, int K, int I_for_w13, uint8_t* out, std::atomic<bool>& bad) {
+// int8 tile stage: 8 chunks x 128 rows x 16 B; chunk c holds K = 16c..16c+15 in
+// byte order.  With group scales (s [groups][rows], 16-bit) 128 x 2 B scales follow.
+void pack_int8_matrix(const int8_t* q, const uint16_t* s, int rows, int K, int I_for_w13, uint8_t* out,
+                      std::atomic<bool>& bad) {
   const int n_tiles = rows / 128, kst = K / 128;
+  const size_t blk_bytes = s ? kInt8GroupStageBytes : kInt8StageBytes;
   for (int t = 0; t < n_tiles; ++t)
     for (int ks = 0; ks < kst; ++ks) {
-      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * kInt8StageBytes;
+      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * blk_bytes;
       for (int r = 0; r < 128; ++r) {
         const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
         const int8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
@@ -483,20 +524,28 @@ void pack_int8_matrix(const int8_t* q, int rows, int K, int I_for_w13, uint8_t* 
             if (v == -128) bad = true;
             blk[(c * 128 + r) * 16 + b] = static_cast<uint8_t>(v);
           }
+        if (s) {
+          const uint16_t sb = s[static_cast<size_t>(ks) * rows + cr];
+          blk[16384 + r * 2] = sb & 0xFF;
+          blk[16384 + r * 2 + 1] = sb >> 8;
+        }
       }
     }
 }
 
-void unpack_int8_matrix(const uint8_t* in, int rows, int K, int I_for_w13, int8_t* q) {
+void unpack_int8_matrix(const uint8_t* in, bool grouped, int rows, int K, int I_for_w13, int8_t* q, uint16_t* s) {
   const int n_tiles = rows / 128, kst = K / 128;
+  const size_t blk_bytes = grouped ? kInt8GroupStageBytes : kInt8StageBytes;
   for (int t = 0; t < n_tiles; ++t)
     for (int ks = 0; ks < kst; ++ks) {
-      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * kInt8StageBytes;
+      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * blk_bytes;
       for (int r = 0; r < 128; ++r) {
         const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
         int8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
         for (int c = 0; c < 8; ++c)
           for (int b = 0; b < 16; ++b) qrow[16 * c + b] = static_cast<int8_t>(blk[(c * 128 + r) * 16 + b]);
+        if (grouped && s)
+          s[static_cast<size_t>(ks) * rows + cr] = static_cast<uint16_t>(blk[16384 + r * 2] | (blk[16384 + r * 2 + 1] << 8));
       }
     }
 }
@@ -538,58 +587,110 @@ const char* qmoe_status_string(qmoe_status s) {
 size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K, int32_t group_size) {
   if (E < 1 || rows <= 0 || K <= 0 || rows % 128 != 0 || K % 128 != 0) return 0;
   const size_t tiles = static_cast<size_t>(E) * (rows / 128) * (K / 128);
-  if (qt == QMOE_INT4_GROUP && group_size == 128) return tiles * kInt4StageBytes;
+  const bool g128_or_cw = group_size == 128 || group_size == -1;
+  if (qt == QMOE_INT4_GROUP && g128_or_cw) return tiles * kInt4StageBytes;
+  if (qt == QMOE_INT4_GROUP_ZP && g128_or_cw) return tiles * kInt4ZpStageBytes;
   if (qt == QMOE_INT8_PER_COL && group_size == -1) return tiles * kInt8StageBytes;
+  if (qt == QMOE_INT8_GROUP && group_size == 128) return tiles * kInt8GroupStageBytes;
   return 0;
 }
 
-qmoe_status qmoe_pack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
-                           const uint8_t* q13, const uint16_t* s13, const int32_t* g13, const uint8_t* q2,
-                           const uint16_t* s2, const int32_t* g2, void* w13_packed, void* w2_packed,
-                           int32_t* perm13_out) {
+}  // extern "C"
+
+namespace {
+
+qmoe_status pack_int4_any(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                          const uint8_t* q13, const uint16_t* s13, const uint8_t* z13, const int32_t* g13,
+                          const uint8_t* q2, const uint16_t* s2, const uint8_t* z2, const int32_t* g2,
+                          void* w13_packed, void* w2_packed, int32_t* perm13_out) {
   if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
-  if (group_size != 128) return QMOE_ERR_UNSUPPORTED;
+  if (group_size != 128 && group_size != -1) return QMOE_ERR_UNSUPPORTED;
+  if (group_size == -1 && (g13 || g2)) return QMOE_ERR_UNSUPPORTED;
   if (scale_dtype != QMOE_F16 && scale_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
   if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed || (g13 && !perm13_out)) return QMOE_ERR_INVALID_ARG;
+  const bool zp = z13 != nullptr;
+  if (zp != (z2 != nullptr)) return QMOE_ERR_INVALID_ARG;
+  const bool cw = group_size == -1;
+  const qmoe_quant_type qt = zp ? QMOE_INT4_GROUP_ZP : QMOE_INT4_GROUP;
   std::atomic<bool> bad{false}, badg{false};
-  const size_t b13 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, 2 * I, H, 128);
-  const size_t b2 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, H, I, 128);
+  const size_t b13 = qmoe_packed_bytes(qt, 1, 2 * I, H, group_size);
+  const size_t b2 = qmoe_packed_bytes(qt, 1, H, I, group_size);
+  const size_t ng13 = cw ? 1 : H / 128, ng2 = cw ? 1 : I / 128;
   parallel_for(E, [&](int64_t e) {
     std::vector<int32_t> p13, p2;
     if (g13 && !sorted_by_group(g13 + e * H, H, p13)) { badg = true; return; }
     if (g2 && !sorted_by_group(g2 + e * I, I, p2)) { badg = true; return; }
     if (g13) std::memcpy(perm13_out + e * H, p13.data(), sizeof(int32_t) * H);
-    pack_int4_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, s13 + static_cast<size_t>(e) * (H / 128) * 2 * I,
-                     2 * I, H, I, g2 ? p2.data() : nullptr, g13 ? p13.data() : nullptr,
-                     static_cast<uint8_t*>(w13_packed) + e * b13, bad);
-    pack_int4_matrix(q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H, H, I, 0,
-                     nullptr, g2 ? p2.data() : nullptr, static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+    pack_int4_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, s13 + e * ng13 * 2 * I,
+                     zp ? z13 + e * ng13 * 2 * I : nullptr, cw, 2 * I, H, I, g2 ? p2.data() : nullptr,
+                     g13 ? p13.data() : nullptr, static_cast<uint8_t*>(w13_packed) + e * b13, bad);
+    pack_int4_matrix(q2 + static_cast<size_t>(e) * H * I, s2 + e * ng2 * H, zp ? z2 + e * ng2 * H : nullptr, cw, H,
+                     I, 0, nullptr, g2 ? p2.data() : nullptr, static_cast<uint8_t*>(w2_packed) + e * b2, bad);
   });
   if (badg) return QMOE_ERR_UNSUPPORTED;
   if (bad) return QMOE_ERR_INVALID_ARG;
   return QMOE_OK;
 }
 
-qmoe_status qmoe_unpack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
-                             const void* w2_packed, const int32_t* g13, const int32_t* g2, uint8_t* q13,
-                             uint16_t* s13, uint8_t* q2, uint16_t* s2) {
+qmoe_status unpack_int4_any(int32_t E, int32_t H, int32_t I, int32_t group_size, bool zp, const void* w13_packed,
+                            const void* w2_packed, const int32_t* g13, const int32_t* g2, uint8_t* q13,
+                            uint16_t* s13, uint8_t* z13, uint8_t* q2, uint16_t* s2, uint8_t* z2) {
   if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
-  if (group_size != 128) return QMOE_ERR_UNSUPPORTED;
-  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128 && group_size != -1) return QMOE_ERR_UNSUPPORTED;
+  if (group_size == -1 && (g13 || g2)) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed || (zp && (!z13 || !z2))) return QMOE_ERR_INVALID_ARG;
+  const bool cw = group_size == -1;
+  const qmoe_quant_type qt = zp ? QMOE_INT4_GROUP_ZP : QMOE_INT4_GROUP;
   std::atomic<bool> badg{false};
-  const size_t b13 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, 2 * I, H, 128);
-  const size_t b2 = qmoe_packed_bytes(QMOE_INT4_GROUP, 1, H, I, 128);
+  const size_t b13 = qmoe_packed_bytes(qt, 1, 2 * I, H, group_size);
+  const size_t b2 = qmoe_packed_bytes(qt, 1, H, I, group_size);
+  const size_t ng13 = cw ? 1 : H / 128, ng2 = cw ? 1 : I / 128;
   parallel_for(E, [&](int64_t e) {
     std::vector<int32_t> p13, p2;
     if (g13 && !sorted_by_group(g13 + e * H, H, p13)) { badg = true; return; }
     if (g2 && !sorted_by_group(g2 + e * I, I, p2)) { badg = true; return; }
-    unpack_int4_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, 2 * I, H, I, g2 ? p2.data() : nullptr,
-                       g13 ? p13.data() : nullptr, q13 + static_cast<size_t>(e) * 2 * I * H,
-                       s13 + static_cast<size_t>(e) * (H / 128) * 2 * I);
-    unpack_int4_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, H, I, 0, nullptr, g2 ? p2.data() : nullptr,
-                       q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H);
+    unpack_int4_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, zp, cw, 2 * I, H, I,
+                       g2 ? p2.data() : nullptr, g13 ? p13.data() : nullptr, q13 + static_cast<size_t>(e) * 2 * I * H,
+                       s13 + e * ng13 * 2 * I, zp ? z13 + e * ng13 * 2 * I : nullptr);
+    unpack_int4_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, zp, cw, H, I, 0, nullptr,
+                       g2 ? p2.data() : nullptr, q2 + static_cast<size_t>(e) * H * I, s2 + e * ng2 * H,
+                       zp ? z2 + e * ng2 * H : nullptr);
   });
   return badg ? QMOE_ERR_UNSUPPORTED : QMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qmoe_status qmoe_pack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                           const uint8_t* q13, const uint16_t* s13, const int32_t* g13, const uint8_t* q2,
+                           const uint16_t* s2, const int32_t* g2, void* w13_packed, void* w2_packed,
+                           int32_t* perm13_out) {
+  return pack_int4_any(E, H, I, group_size, scale_dtype, q13, s13, nullptr, g13, q2, s2, nullptr, g2, w13_packed,
+                       w2_packed, perm13_out);
+}
+
+qmoe_status qmoe_unpack_int4(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                             const void* w2_packed, const int32_t* g13, const int32_t* g2, uint8_t* q13,
+                             uint16_t* s13, uint8_t* q2, uint16_t* s2) {
+  return unpack_int4_any(E, H, I, group_size, false, w13_packed, w2_packed, g13, g2, q13, s13, nullptr, q2, s2,
+                         nullptr);
+}
+
+qmoe_status qmoe_pack_int4_zp(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                              const uint8_t* q13, const uint16_t* s13, const uint8_t* z13, const int32_t* g13,
+                              const uint8_t* q2, const uint16_t* s2, const uint8_t* z2, const int32_t* g2,
+                              void* w13_packed, void* w2_packed, int32_t* perm13_out) {
+  if (!z13 || !z2) return QMOE_ERR_INVALID_ARG;
+  return pack_int4_any(E, H, I, group_size, scale_dtype, q13, s13, z13, g13, q2, s2, z2, g2, w13_packed, w2_packed,
+                       perm13_out);
+}
+
+qmoe_status qmoe_unpack_int4_zp(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                                const void* w2_packed, const int32_t* g13, const int32_t* g2, uint8_t* q13,
+                                uint16_t* s13, uint8_t* z13, uint8_t* q2, uint16_t* s2, uint8_t* z2) {
+  return unpack_int4_any(E, H, I, group_size, true, w13_packed, w2_packed, g13, g2, q13, s13, z13, q2, s2, z2);
 }
 
 qmoe_status qmoe_pack_int8(int32_t E, int32_t H, int32_t I, const int8_t* q13, const float* s13, const int8_t* q2,
@@ -601,9 +702,10 @@ qmoe_status qmoe_pack_int8(int32_t E, int32_t H, int32_t I, const int8_t* q13, c
   const size_t b13 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, 2 * I, H, -1);
   const size_t b2 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, H, I, -1);
   parallel_for(E, [&](int64_t e) {
-    pack_int8_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, 2 * I, H, I,
+    pack_int8_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, nullptr, 2 * I, H, I,
                      static_cast<uint8_t*>(w13_packed) + e * b13, bad);
-    pack_int8_matrix(q2 + static_cast<size_t>(e) * H * I, H, I, 0, static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+    pack_int8_matrix(q2 + static_cast<size_t>(e) * H * I, nullptr, H, I, 0,
+                     static_cast<uint8_t*>(w2_packed) + e * b2, bad);
     for (int t = 0; t < 2 * I / 128; ++t)
       for (int r = 0; r < 128; ++r)
         s13_packed[static_cast<size_t>(e) * 2 * I + t * 128 + r] = s13[static_cast<size_t>(e) * 2 * I + w13_canon_row(t, r, I, nullptr)];
@@ -621,13 +723,47 @@ qmoe_status qmoe_unpack_int8(int32_t E, int32_t H, int32_t I, const void* w13_pa
   const size_t b13 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, 2 * I, H, -1);
   const size_t b2 = qmoe_packed_bytes(QMOE_INT8_PER_COL, 1, H, I, -1);
   parallel_for(E, [&](int64_t e) {
-    unpack_int8_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, 2 * I, H, I,
-                       q13 + static_cast<size_t>(e) * 2 * I * H);
-    unpack_int8_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, H, I, 0, q2 + static_cast<size_t>(e) * H * I);
+    unpack_int8_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, false, 2 * I, H, I,
+                       q13 + static_cast<size_t>(e) * 2 * I * H, nullptr);
+    unpack_int8_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, false, H, I, 0,
+                       q2 + static_cast<size_t>(e) * H * I, nullptr);
     for (int t = 0; t < 2 * I / 128; ++t)
       for (int r = 0; r < 128; ++r)
         s13[static_cast<size_t>(e) * 2 * I + w13_canon_row(t, r, I, nullptr)] = s13_packed[static_cast<size_t>(e) * 2 * I + t * 128 + r];
     std::memcpy(s2 + static_cast<size_t>(e) * H, s2_packed + static_cast<size_t>(e) * H, sizeof(float) * H);
+  });
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_pack_int8_group(int32_t E, int32_t H, int32_t I, qmoe_dtype scale_dtype, const int8_t* q13,
+                                 const uint16_t* s13, const int8_t* q2, const uint16_t* s2, void* w13_packed,
+                                 void* w2_packed) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (scale_dtype != QMOE_F16 && scale_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed) return QMOE_ERR_INVALID_ARG;
+  std::atomic<bool> bad{false};
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT8_GROUP, 1, 2 * I, H, 128);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT8_GROUP, 1, H, I, 128);
+  parallel_for(E, [&](int64_t e) {
+    pack_int8_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, s13 + static_cast<size_t>(e) * (H / 128) * 2 * I,
+                     2 * I, H, I, static_cast<uint8_t*>(w13_packed) + e * b13, bad);
+    pack_int8_matrix(q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H, H, I, 0,
+                     static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+  });
+  return bad ? QMOE_ERR_INVALID_ARG : QMOE_OK;
+}
+
+qmoe_status qmoe_unpack_int8_group(int32_t E, int32_t H, int32_t I, const void* w13_packed, const void* w2_packed,
+                                   int8_t* q13, uint16_t* s13, int8_t* q2, uint16_t* s2) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed) return QMOE_ERR_INVALID_ARG;
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT8_GROUP, 1, 2 * I, H, 128);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT8_GROUP, 1, H, I, 128);
+  parallel_for(E, [&](int64_t e) {
+    unpack_int8_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, true, 2 * I, H, I,
+                       q13 + static_cast<size_t>(e) * 2 * I * H, s13 + static_cast<size_t>(e) * (H / 128) * 2 * I);
+    unpack_int8_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, true, H, I, 0,
+                       q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H);
   });
   return QMOE_OK;
 }

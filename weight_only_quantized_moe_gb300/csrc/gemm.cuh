@@ -137,11 +137,15 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // of their half, where (nibble << 4) | 0x6400 is 1024 + 16q and
 // fma(v, 1/16, -72) = q - 8 exactly, so one shift per word serves i = 2, 3.
 // One multiply by the group scale rounds once (exact for bf16 scales).
-// `pk` holds chunks 2h and 2h+1 of the row for half h.
+// `pk` holds chunks 2h and 2h+1 of the row for half h.  With a zero point z
+// (0..15; 8 for the symmetric format) the two constants become 1024 + z and
+// -(64 + z), still exact, so zero points cost no instruction.
 template <bool BF16S>
-__device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t (&out)[32]) {
-  const uint32_t bias_bits = 0x64086408u;                        // 1032
-  const uint32_t sixteenth = 0x2C002C00u, m72 = 0xD480D480u;     // 1/16, -72
+__device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t z,
+                                                  uint32_t (&out)[32]) {
+  const uint32_t bias_bits = 0x64006400u | z | (z << 16);                      // 1024 + z
+  const uint32_t sixteenth = 0x2C002C00u;                                      // 1/16
+  const uint32_t m72 = 0xD400D400u | (z << 4) | (z << 20);                     // -(64 + z)
   uint16_t s16;
   if (BF16S) {
     s16 = __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
@@ -172,11 +176,19 @@ __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t
 }
 
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
-// per-row scale is applied to the fp32 accumulator in the epilogue, so the
-// conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.  `pk` holds
-// chunks 4h .. 4h+3 of the row for half h.
-__device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t (&out)[32]) {
+// conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.  A per-row
+// (per-column of W) scale is applied to the fp32 accumulator in the epilogue;
+// a group scale (GS) multiplies here, rounding once.  `pk` holds chunks
+// 4h .. 4h+3 of the row for half h.
+template <bool GS, bool BF16S>
+__device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[32]) {
   const uint32_t bias = 0x64806480u;  // 1152
+  uint32_t s2bits = 0;
+  if (GS) {
+    const uint16_t s16 =
+        BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16))) : static_cast<uint16_t>(sbits);
+    s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
+  }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
@@ -187,6 +199,10 @@ __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t
       const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
       __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias));
       __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&bias));
+      if (GS) {
+        a = __hmul2(a, *reinterpret_cast<const __half2*>(&s2bits));
+        b = __hmul2(b, *reinterpret_cast<const __half2*>(&s2bits));
+      }
       out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
       out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
     }
@@ -249,8 +265,9 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 // own stages (every 2nd for producers and dequant sets, every NI-th for the MMA
 // issuers), stepping its ring position by the same stride.
 // ---------------------------------------------------------------------------
-template <bool INT4, bool BF16S>
+template <int KIND, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
+  constexpr bool INT4 = KIND == kQ4 || KIND == kQ4Z;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -442,16 +459,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 #pragma unroll
           for (int c = 0; c < 2; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((2 * half + c) * 128 + row) * 16);
           const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
+          const uint32_t zp = (KIND == kQ4Z) ? static_cast<uint32_t>(wst[8448 + row]) : 8u;
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-          dequant_int4_half<BF16S>(pk, sbits, out);
+          dequant_int4_half<BF16S>(pk, sbits, zp, out);
         } else {
           uint4 pk[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((4 * half + c) * 128 + row) * 16);
+          const uint32_t sbits = (KIND == kQ8G) ? *reinterpret_cast<const uint16_t*>(wst + 16384 + row * 2) : 0u;
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-          dequant_int8_half(pk, out);
+          dequant_int8_half<KIND == kQ8G, BF16S>(pk, sbits, out);
         }
         const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(br.idx * 64 + 32 * half);
         tmem_st_32x32b_x32<0>(ta, out);
@@ -484,8 +503,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 #pragma unroll
       for (int j = 0; j < kMaxIssuers; ++j) has[j] = j < NI && first_own(g0, j, NI) < g0 + n_st;
       g0 += n_st;
-      const float rs =
-          INT4 ? 1.0f : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
+      const float rs = (KIND != kQ8)
+                           ? 1.0f
+                           : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
       for (int c0 = 0; c0 < it.nrows; c0 += 16) {
         float f[16];
 #pragma unroll
@@ -529,13 +549,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   }
 }
 
-template <bool INT4, bool BF16S>
+template <int KIND, bool BF16S>
 cudaError_t launch_gemm_t(const GemmParams& p, int grid, cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p);
-  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<INT4, BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<KIND, BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_kernel(qmoe_gemm_kernel<INT4, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, p);
+  return launch_kernel(qmoe_gemm_kernel<KIND, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, p);
 }
 
 }  // namespace qmoe

@@ -5,21 +5,27 @@ namespace qmoe {
 
 cudaError_t launch_gemm_i4_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i4_bf16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i4z_f16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i4z_bf16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i8g_f16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i8g_bf16(const GemmParams&, int, cudaStream_t);
 
 size_t gemm_smem_bytes(const GemmParams& p) {
   return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.ab_stages, p.token_tile);
 }
 
-cudaError_t launch_gemm(bool int4, bool bf16_scales, const GemmParams& p, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream) {
   // ring sizes must be multiples of every role's stride (see qmoe_gemm_kernel)
   if (p.issuers < 1 || p.issuers > kMaxIssuers) return cudaErrorInvalidValue;
   const int mult = (p.issuers == 3) ? 6 : 2;
   if (p.w_stages < 2 || (p.w_stages & 1) || p.ab_stages < mult || p.ab_stages % mult != 0) return cudaErrorInvalidValue;
-  if (int4)
-    return bf16_scales ? launch_gemm_i4_bf16(p, grid, stream) : launch_gemm_i4_f16(p, grid, stream);
-  return launch_gemm_i8(p, grid, stream);
+  switch (kind) {
+    case kQ4: return bf16_scales ? launch_gemm_i4_bf16(p, grid, stream) : launch_gemm_i4_f16(p, grid, stream);
+    case kQ4Z: return bf16_scales ? launch_gemm_i4z_bf16(p, grid, stream) : launch_gemm_i4z_f16(p, grid, stream);
+    case kQ8G: return bf16_scales ? launch_gemm_i8g_bf16(p, grid, stream) : launch_gemm_i8g_f16(p, grid, stream);
+    default: return launch_gemm_i8(p, grid, stream);
+  }
 }
 
 }  // namespace qmoe

@@ -1,0 +1,11 @@
+// gemm_i4z_f16.cu - instantiation of the grouped dequant GEMM for int4 weights with zero points and f16 group scales
+// (one translation unit per variant so they compile in parallel).
+#include "gemm.cuh"
+
+namespace qmoe {
+
+cudaError_t launch_gemm_i4z_f16(const GemmParams& p, int grid, cudaStream_t stream) {
+  return launch_gemm_t<kQ4Z, false>(p, grid, stream);
+}
+
+}  // namespace qmoe

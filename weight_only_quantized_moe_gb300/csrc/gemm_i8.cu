@@ -1,11 +1,11 @@
-// gemm_i8.cu - instantiation of the grouped dequant GEMM for int8 weights
+// gemm_i8.cu - instantiation of the grouped dequant GEMM for int8 weights with per-column scales
 // (one translation unit per variant so they compile in parallel).
 #include "gemm.cuh"
 
 namespace qmoe {
 
 cudaError_t launch_gemm_i8(const GemmParams& p, int grid, cudaStream_t stream) {
-  return launch_gemm_t<false, false>(p, grid, stream);
+  return launch_gemm_t<kQ8, false>(p, grid, stream);
 }
 
 }  // namespace qmoe

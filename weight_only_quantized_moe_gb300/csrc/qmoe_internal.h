@@ -13,6 +13,11 @@ constexpr int kTileRows = 128;        // output features per GEMM work item (MMA
 constexpr int kStageK = 128;          // K elements per pipeline stage (= one int4 group)
 constexpr int kInt4StageBytes = 8448; // 128 rows x 128 K x 4 bit + 128 scales x 2 B
 constexpr int kInt8StageBytes = 16384;
+constexpr int kInt4ZpStageBytes = 8576;   // int4 block + 128 zero-point bytes
+constexpr int kInt8GroupStageBytes = 16640;  // int8 block + 128 x 2 B scales
+
+// Weight formats of the GEMM kernel (template parameter).
+enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3 };
 constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
 constexpr int kMaxTokenTile = 128;
 
@@ -122,7 +127,7 @@ cudaError_t launch_route_topk(const void* logits, int dtype, int64_t M, int32_t 
                               int32_t* topk_ids, float* topk_weights, int num_sms, cudaStream_t stream);
 
 size_t gemm_smem_bytes(const GemmParams& p);
-cudaError_t launch_gemm(bool int4, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream);
 
 }  // namespace qmoe
 
