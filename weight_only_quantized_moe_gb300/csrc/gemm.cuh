@@ -140,12 +140,27 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // `pk` holds chunks 2h and 2h+1 of the row for half h.  With a zero point z
 // (0..15; 8 for the symmetric format) the two constants become 1024 + z and
 // -(64 + z), still exact, so zero points cost no instruction.
+// One 32-bit word's two nibble pairs (lo: bits 0..3 / 16..19, hi: bits 4..7 /
+// 20..23 of `src`) to two f16x2 values (q - z) * s: two LOP3, one subtract, one
+// FMA and two multiplies, written out so that nothing else is generated.
+__device__ __forceinline__ void cvt_int4_word_half(uint32_t src, uint32_t bias, uint32_t m64z, uint32_t s2,
+                                                   uint32_t& lo_out, uint32_t& hi_out) {
+  asm("{\n\t.reg .b32 lo, hi;\n\t"
+      "lop3.b32 lo, %2, 0x000F000F, 0x64006400, 0xEA;\n\t"   // (src & mask) | 0x6400: 1024 + q
+      "lop3.b32 hi, %2, 0x00F000F0, 0x64006400, 0xEA;\n\t"   // 1024 + 16 q
+      "sub.rn.f16x2 lo, lo, %3;\n\t"                        // q - z
+      "fma.rn.f16x2 hi, hi, %6, %4;\n\t"                    // (1024 + 16q) / 16 - (64 + z) = q - z
+      "mul.rn.f16x2 %0, lo, %5;\n\t"
+      "mul.rn.f16x2 %1, hi, %5;\n\t}"
+      : "=r"(lo_out), "=r"(hi_out)
+      : "r"(src), "r"(bias), "r"(m64z), "r"(s2), "r"(0x2C002C00u));
+}
+
 template <bool BF16S>
 __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t z,
                                                   uint32_t (&out)[32]) {
   const uint32_t bias_bits = 0x64006400u | z | (z << 16);                      // 1024 + z
-  const uint32_t sixteenth = 0x2C002C00u;                                      // 1/16
-  const uint32_t m72 = 0xD400D400u | (z << 4) | (z << 20);                     // -(64 + z)
+  const uint32_t m64z = 0xD400D400u | (z << 4) | (z << 20);                    // -(64 + z)
   uint16_t s16;
   if (BF16S) {
     s16 = __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
@@ -158,19 +173,8 @@ __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t src[2] = {w[j], w[j] >> 8};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t lo = (src[h] & 0x000F000Fu) | 0x64006400u;
-        const uint32_t hi = (src[h] & 0x00F000F0u) | 0x64006400u;
-        __half2 vl = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias_bits));
-        __half2 vh = __hfma2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&sixteenth),
-                             *reinterpret_cast<const __half2*>(&m72));
-        vl = __hmul2(vl, *reinterpret_cast<const __half2*>(&s2bits));
-        vh = __hmul2(vh, *reinterpret_cast<const __half2*>(&s2bits));
-        out[16 * c + 4 * j + 2 * h] = *reinterpret_cast<uint32_t*>(&vl);
-        out[16 * c + 4 * j + 2 * h + 1] = *reinterpret_cast<uint32_t*>(&vh);
-      }
+      cvt_int4_word_half(w[j], bias_bits, m64z, s2bits, out[16 * c + 4 * j], out[16 * c + 4 * j + 1]);
+      cvt_int4_word_half(w[j] >> 8, bias_bits, m64z, s2bits, out[16 * c + 4 * j + 2], out[16 * c + 4 * j + 3]);
     }
   }
 }
