@@ -42,7 +42,8 @@
 //     the tensor pipe is, so that two accumulator buffers fit in TMEM.  Warps
 //     0-3 are the epilogue.  A persistent grid walks the work items.
 //   * barriers per stage: the dequant set waits for the weights and the token
-//     tile, releases the weight slot, writes A and signals it; the issuer
+//     tile (one barrier counts both copies), releases the weight slot, writes A
+//     and signals it; the issuer
 //     waits for that one signal, issues the stage's MMAs and commits one
 //     release of the token-tile/A slot.  Every ring's size is a multiple of
 //     the stride of each role that uses it (2 for producers and dequant sets,
@@ -184,9 +185,36 @@ __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t
 // (per-column of W) scale is applied to the fp32 accumulator in the epilogue;
 // a group scale (GS) multiplies here, rounding once.  `pk` holds chunks
 // 4h .. 4h+3 of the row for half h.
+// One 32-bit word (4 int8 codes) to two f16x2 values: flip the sign bit
+// (q + 128), place each byte under the exponent 0x64 (1024 + q + 128) and
+// subtract 1152; with a group scale, multiply.
+template <bool GS>
+__device__ __forceinline__ void cvt_int8_word(uint32_t w, uint32_t s2, uint32_t& a_out, uint32_t& b_out) {
+  if (GS) {
+    asm("{\n\t.reg .b32 u, lo, hi;\n\t"
+        "xor.b32 u, %2, 0x80808080;\n\t"
+        "prmt.b32 lo, u, 0x64646464, 0x4140;\n\t"
+        "prmt.b32 hi, u, 0x64646464, 0x4342;\n\t"
+        "sub.rn.f16x2 lo, lo, %3;\n\t"
+        "sub.rn.f16x2 hi, hi, %3;\n\t"
+        "mul.rn.f16x2 %0, lo, %4;\n\t"
+        "mul.rn.f16x2 %1, hi, %4;\n\t}"
+        : "=r"(a_out), "=r"(b_out)
+        : "r"(w), "r"(0x64806480u), "r"(s2));
+  } else {
+    asm("{\n\t.reg .b32 u, lo, hi;\n\t"
+        "xor.b32 u, %2, 0x80808080;\n\t"
+        "prmt.b32 lo, u, 0x64646464, 0x4140;\n\t"
+        "prmt.b32 hi, u, 0x64646464, 0x4342;\n\t"
+        "sub.rn.f16x2 %0, lo, %3;\n\t"
+        "sub.rn.f16x2 %1, hi, %3;\n\t}"
+        : "=r"(a_out), "=r"(b_out)
+        : "r"(w), "r"(0x64806480u));
+  }
+}
+
 template <bool GS, bool BF16S>
 __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t sbits, uint32_t (&out)[32]) {
-  const uint32_t bias = 0x64806480u;  // 1152
   uint32_t s2bits = 0;
   if (GS) {
     const uint16_t s16 =
@@ -197,19 +225,7 @@ __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t
   for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t u = w[j] ^ 0x80808080u;
-      const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
-      const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
-      __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&bias));
-      __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), *reinterpret_cast<const __half2*>(&bias));
-      if (GS) {
-        a = __hmul2(a, *reinterpret_cast<const __half2*>(&s2bits));
-        b = __hmul2(b, *reinterpret_cast<const __half2*>(&s2bits));
-      }
-      out[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&a);
-      out[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&b);
-    }
+    for (int j = 0; j < 4; ++j) cvt_int8_word<GS>(w[j], s2bits, out[8 * c + 2 * j], out[8 * c + 2 * j + 1]);
   }
 }
 
@@ -282,10 +298,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint8_t* wring = smem;
   uint8_t* bring = smem + NW * wslot;
 
+  // wfull[i] completes when a stage's weights AND its token tile have landed (the
+  // producer arms it for both copies; the token-tile copy, issued later, counts on it)
   uint64_t* wfull = reinterpret_cast<uint64_t*>(bring + NB * bslot);
   uint64_t* wempty = wfull + NW;
-  uint64_t* bfull = wempty + NW;
-  uint64_t* afull = bfull + NB;
+  uint64_t* afull = wempty + NW;
   uint64_t* sfree = afull + NB;  // token-tile slot and its A slot are free again
   uint64_t* accfull = sfree + NB;
   uint64_t* accempty = accfull + 2;
@@ -302,7 +319,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_init(smem_u32(wempty + s), kDequantWarps);
     }
     for (int j = 0; j < NB; ++j) {
-      mbar_init(smem_u32(bfull + j), 1);
       mbar_init(smem_u32(afull + j), kDequantWarps);
       mbar_init(smem_u32(sfree + j), 1);
     }
@@ -358,7 +374,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             break;
           }
           const uint32_t wb = smem_u32(wfull + wr.idx);
-          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(p.stage_bytes));
+          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(p.stage_bytes) + b_run);
           if (!inject)
             tma_load_1d(smem_u32(wring + wr.idx * wslot), wsrc + static_cast<int64_t>(ks) * p.stage_bytes,
                         static_cast<uint32_t>(p.stage_bytes), wb, pol_w);
@@ -369,20 +385,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             ok = false;
             break;
           }
-          const uint32_t bb = smem_u32(bfull + br.idx);
-          mbar_arrive_expect_tx(bb, b_run);
-          if (!inject) tma_load_1d(smem_u32(bring + br.idx * bslot), bsrc + ks * p.b_unit_stride, b_run, bb, pol_b);
+          if (!inject) tma_load_1d(smem_u32(bring + br.idx * bslot), bsrc + ks * p.b_unit_stride, b_run, wb, pol_b);
           last_b = g;
         }
         g0 += n_st;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
       // wait for every copy this thread may still have in flight into the CTA's shared
-      // memory: its stages among the last NW (weights) and NB (token tiles) it armed
+      // memory: both copies of a stage count on its wfull barrier, so the stages
+      // among the last NW it armed cover them (a stage whose token-tile copy was
+      // never issued after an abort leaves its barrier pending: the drain wait
+      // then runs into its time limit, with no copy in flight)
+      (void)last_b;
       for (int j = (last_w >= NW ? last_w - NW + 2 : id); j <= last_w; j += 2)
         mbar_wait_drain(smem_u32(wfull + (j % NW)), (j / NW) & 1);
-      for (int j = (last_b >= NB ? last_b - NB + 2 : id); j <= last_b; j += 2)
-        mbar_wait_drain(smem_u32(bfull + (j % NB)), (j / NB) & 1);
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1 || warp == kMmaWarp3) {
     // ------------------------------------------------------------ MMA issuers
@@ -450,10 +466,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       decode_item(p, nch, i, it);
       const int n_st = it.ks1 - it.ks0;
       for (int g = first_own(g0, set, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
-        // weights landed; token tile landed, which also means the MMAs of the
-        // A slot's previous stage completed (the producer waited for that)
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag) &&
-                                         mbar_wait(smem_u32(bfull + br.idx), br.phase, abort_flag));
+        // weights and token tile landed; the latter also means the MMAs of the A
+        // slot's previous stage completed (the producer waited for that)
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint8_t* wst = wring + wr.idx * wslot;
