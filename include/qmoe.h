@@ -122,8 +122,14 @@ typedef struct {
  * floating-point summation order whatever the knobs say.
  *   split1, split2  split-K factor of the gate/up and down GEMMs (1..64).
  *   token_tile      largest number of token rows one GEMM work item carries
- *                   (multiple of 16, 16..128).  Other values give
- *                   QMOE_ERR_INVALID_ARG.
+ *                   (multiple of 16, 16..128).
+ *   issuers         threads issuing the GEMMs' tensor-core MMAs (1..3), each
+ *                   with its own TMEM accumulator; the automatic choice is 3
+ *                   for token tiles of up to 32 rows, 2 up to 64, else 1.  The
+ *                   automatic token tile is the power of two from 16 to 128
+ *                   at least twice the mean number of pairs per expert.
+ * Other values, or an issuer count whose accumulators leave too little tensor
+ * memory for the pipeline, give QMOE_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t split1;
@@ -135,7 +141,8 @@ typedef struct {
    * bounded waits give up after about a second, record QMOE_ERR_TIMEOUT and the
    * kernel exits with the CUDA context intact (the output is then garbage). */
   int32_t fault_injection;
-  int32_t reserved[4];
+  int32_t issuers;
+  int32_t reserved[3];
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */

@@ -216,3 +216,21 @@ def test_pack_rejects_bad_zero_points():
     assert q.packed_bytes("int8g", 1, 256, 128) == 2 * 16640
     assert q.packed_bytes("int4", 1, 256, 128, -1) == 2 * 8448
     assert q.packed_bytes("int8g", 1, 256, 128, -1) == 0
+
+
+def test_options_layout_and_issuer_validation():
+    """qmoe_options is 8 int32 fields; the issuer-count knob is checked on the host."""
+    assert ctypes.sizeof(N.QmoeOptions) == 32
+    L = q.lib()
+    ok = _layer_struct()
+
+    def size(M, **kw):
+        return L.qmoe_workspace_size_ex(ctypes.byref(ok), M, 2, ctypes.byref(q.make_options(**kw)))
+
+    assert size(16) == L.qmoe_workspace_size(ctypes.byref(ok), 16, 2)
+    for n in (1, 2, 3):
+        assert size(16, issuers=n) > 0          # 16-row token tile: any issuer count fits
+    assert size(4096, issuers=2) > 0           # 128-row tile, two issuers: 256 accumulator columns
+    assert size(4096, issuers=3) == 0          # 384 accumulator columns leave no room for A slots
+    assert size(16, issuers=4) == 0
+    assert size(16, issuers=-1) == 0

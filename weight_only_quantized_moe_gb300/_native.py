@@ -42,7 +42,7 @@ class QmoeLayer(ctypes.Structure):
 
 class QmoeOptions(ctypes.Structure):
     _fields_ = [("split1", c_int32), ("split2", c_int32), ("token_tile", c_int32), ("fault_injection", c_int32),
-                ("reserved", c_int32 * 4)]
+                ("issuers", c_int32), ("reserved", c_int32 * 3)]
 
 
 class QmoeError(RuntimeError):

@@ -163,9 +163,10 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.k = k;
   p.P = M * k;
   const int64_t P = p.P;
-  // token tile: every expert's rows fit one chunk at decode sizes
-  int T = 128;
-  if (P <= 128) T = static_cast<int>(std::max<int64_t>(16, (P + 15) / 16 * 16));
+  // token tile: a power of two from 16 to 128, at least twice the mean number of
+  // pairs per expert, so that at decode sizes each expert's rows are one chunk
+  int T = 16;
+  while (T < 128 && T * static_cast<int64_t>(L->E) < 2 * P) T *= 2;
   if (o != nullptr && o->token_tile != 0) {
     if (o->token_tile < 16 || o->token_tile > kMaxTokenTile || o->token_tile % 16 != 0) return QMOE_ERR_INVALID_ARG;
     T = o->token_tile;
@@ -176,11 +177,16 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
-  // MMA issuers: up to three (stage g to issuer g mod n, one accumulator each)
-  // while the token tile is small and one thread's MMA issue rate is the
-  // limit; one when the tile is large and the tensor pipe is, which leaves TMEM
-  // for two accumulator buffers so the epilogue overlaps the next item's MMAs.
+  // MMA issuers (stage g to issuer g mod n, one accumulator each): one thread
+  // issues a tcgen05.mma about every 86 cycles whatever its N, so small token
+  // tiles take three; a 128-row tile keeps the tensor pipe busy from one
+  // thread, which leaves TMEM for two accumulator buffers so the epilogue
+  // overlaps the next item's MMAs.
   p.issuers = (T <= 32) ? 3 : (T <= 64) ? 2 : 1;
+  if (o != nullptr && o->issuers != 0) {
+    if (o->issuers < 1 || o->issuers > 3) return QMOE_ERR_INVALID_ARG;
+    p.issuers = o->issuers;
+  }
   // Ring sizes are multiples of every role's stride (2 for the producers and
   // dequant sets, the issuer count for the issuers): each slot then belongs to
   // one role of each kind, and each waiter sees every phase of its barriers.
@@ -196,6 +202,7 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.acc_bufs = a_slots(2) >= ring_mult ? 2 : 1;
   p.a_col0 = p.issuers * p.acc_bufs * T;
   p.ab_stages = a_slots(p.acc_bufs);
+  if (p.ab_stages < ring_mult) return (o != nullptr && o->issuers != 0) ? QMOE_ERR_INVALID_ARG : QMOE_ERR_UNSUPPORTED;
   const size_t wslot = (static_cast<size_t>(p.stage_bytes) + 1023) & ~size_t(1023);
   const size_t b_bytes = static_cast<size_t>(p.ab_stages) * T * 256;
   if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return QMOE_ERR_UNSUPPORTED;
