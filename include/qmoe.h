@@ -127,7 +127,7 @@ typedef struct {
  *                   with its own TMEM accumulator; the automatic choice is 3
  *                   for token tiles of up to 32 rows, 2 up to 64, else 1.  The
  *                   automatic token tile is the power of two from 16 to 128
- *                   at least twice the mean number of pairs per expert.
+ *                   at least 1.5 times the mean number of pairs per expert.
  * Other values, or an issuer count whose accumulators leave too little tensor
  * memory for the pipeline, give QMOE_ERR_INVALID_ARG.
  */
