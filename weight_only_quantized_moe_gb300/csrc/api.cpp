@@ -370,12 +370,10 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g2.out_ld = L->H;
   g2.out_split_stride = pl.P * static_cast<int64_t>(L->H);
 
-  // the GEMMs run as CTA pairs, one work item (chunk x tile pair x split) per pair at a time
-  const int64_t items1 = pl.max_chunks * ((pl.n_tiles1 + 1) / 2) * pl.S1;
-  const int64_t items2 = pl.max_chunks * ((pl.n_tiles2 + 1) / 2) * pl.S2;
-  const int pairs = std::max(1, sms / 2);
-  const int grid1 = 2 * static_cast<int>(std::min<int64_t>(pairs, items1));
-  const int grid2 = 2 * static_cast<int>(std::min<int64_t>(pairs, items2));
+  const int64_t items1 = pl.max_chunks * pl.n_tiles1 * pl.S1;
+  const int64_t items2 = pl.max_chunks * pl.n_tiles2 * pl.S2;
+  const int grid1 = static_cast<int>(std::min<int64_t>(sms, items1));
+  const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
     err = launch_gemm(kind_of(L->qt), bf16, g1, grid1, stream);  // in-block scales have the activation dtype

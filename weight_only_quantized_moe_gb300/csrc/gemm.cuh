@@ -19,16 +19,8 @@
 //
 // Design for GB300 (prior-art Marlin/Triton kernels staged both operands in
 // shared memory; here only the tokens are):
-//   * CTA pairs: the kernel runs as clusters of two CTAs on two SMs.  A work
-//     item is a chunk of token rows against a pair of 128-row weight tiles;
-//     each CTA dequantizes its own tile into its own TMEM and copies half of
-//     the token tile into its shared memory, and one thread of the even CTA
-//     issues M = 256 MMAs (tcgen05 cta_group::2) that read both.  One MMA
-//     instruction then covers two SMs' work: a thread issues a tcgen05.mma
-//     every ~50-90 cycles whatever its size, which bounded the single-CTA
-//     form at small N.
-//   * swap-AB: the 256 weight rows of a tile pair are the MMA's M; the chunk's
-//     token rows (16..128) are N, so tiny decode batches waste no tensor work.
+//   * swap-AB: the 128 weight rows are the MMA's M; the chunk's token rows
+//     (16..128) are N, so tiny decode batches waste no tensor work.
 //   * the dequantized weight tile goes registers -> TMEM (tcgen05.st) and is
 //     the MMA's A operand straight from tensor memory; dequantized weights
 //     never touch shared memory, which carries only the packed bytes and the
@@ -40,24 +32,20 @@
 //     pre-staged, per 128-K group and 8-row group, in the 128-byte-swizzled
 //     K-major layout the MMA's shared-memory descriptor reads, so a chunk's
 //     tile for one stage is one contiguous run.
-//   * warp roles (25 warps per CTA): two TMA producer threads (warps 4, 7) and
-//     two dequant sets of 8 warps (warps 8-15, 16-23) take the even and the
-//     odd stages; each dequant warp converts half of a stage row for 32 rows
-//     (one TMEM lane quadrant).  In the even CTA, the MMAs are issued by up to
-//     three threads (warps 5, 6, 24; stage g goes to issuer g mod NI, each
-//     with its own accumulator) while the token tile is small and the issue
+//   * warp roles (25 warps): two TMA producer threads (warps 4, 7) and two
+//     dequant sets of 8 warps (warps 8-15, 16-23) take the even and the odd
+//     stages; each dequant warp converts half of a stage row for 32 rows (one
+//     TMEM lane quadrant).  The MMAs are issued by up to three threads (warps
+//     5, 6, 24; stage g goes to issuer g mod NI, each with its own
+//     accumulator) while the token tile is small and one thread's MMA issue
 //     rate is the limit, and by one thread (warp 5) when the tile is large and
 //     the tensor pipe is, so that two accumulator buffers fit in TMEM.  Warps
-//     0-3 are the epilogue of each CTA's own tile.  A persistent grid of
-//     pairs walks the work items; both CTAs of a pair walk the same stages.
-//   * barriers per stage: each CTA's dequant set waits for its weights and
-//     its half of the token tile (one barrier counts both copies), releases
-//     the weight slot, writes A and signals the even CTA's A barrier (which
-//     counts the dequant warps of both CTAs); the issuer waits for that one
-//     barrier, issues the stage's MMAs and commits one release of the
-//     token-tile/A slot, multicast to both CTAs.  Accumulators: the commit at
-//     an item's end reaches both CTAs' epilogues, and both release the
-//     accumulator on the even CTA's barrier.  Every ring's size is a multiple of
+//     0-3 are the epilogue.  A persistent grid walks the work items.
+//   * barriers per stage: the dequant set waits for the weights and the token
+//     tile (one barrier counts both copies), releases the weight slot, writes A
+//     and signals it; the issuer
+//     waits for that one signal, issues the stage's MMAs and commits one
+//     release of the token-tile/A slot.  Every ring's size is a multiple of
 //     the stride of each role that uses it (2 for producers and dequant sets,
 //     NI for the issuers), so each slot belongs to one role of each kind and
 //     each role sees every phase of the barriers it waits on.
@@ -94,35 +82,28 @@ __host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group
 
 struct WorkItem {
   int e, row0, nrows, tile, split_idx, ks0, ks1;
-  bool phantom;  // odd tile count: the odd CTA's tile of the last pair does not exist
 };
 
-// Work item i -> (split, chunk, tile pair); this CTA (rank 0 or 1 of the pair)
-// takes tile 2 * pair + rank.  With an odd tile count the last pair's odd tile
-// is a phantom: that CTA re-reads the last real tile (the pair MMA needs its A
-// rows and its half of B) and its epilogue stores nothing.  Items of one split
-// are rastered in groups of `chunk_group` chunks: tile pairs vary slowest
-// inside a group so that the pairs running at the same time share the group's
-// token tiles and each expert weight tile in L2.
-__device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i, uint32_t rank, WorkItem& w) {
-  const int n_pairs = (p.n_tiles + 1) >> 1;
-  const int per_split = nch * n_pairs;
+// Work item i -> (split, chunk, tile).  Items of one split are rastered in
+// groups of `chunk_group` chunks: tiles vary slowest inside a group so that the
+// CTAs running at the same time share the group's token tiles and each expert
+// weight tile in L2.
+__device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i, WorkItem& w) {
+  const int per_split = nch * p.n_tiles;
   const int s = i / per_split;
   const int r = i - s * per_split;
-  const int grp_items = p.chunk_group * n_pairs;
+  const int grp_items = p.chunk_group * p.n_tiles;
   const int g = r / grp_items;
   const int rem = r - g * grp_items;
   const int c0 = g * p.chunk_group;
   const int cg = min(p.chunk_group, nch - c0);
-  const int pair = rem / cg;
-  const int c = c0 + (rem - pair * cg);
+  const int tile = rem / cg;
+  const int c = c0 + (rem - tile * cg);
   const Chunk ch = p.chunks[c];
-  const int tile = 2 * pair + static_cast<int>(rank);
   w.e = ch.expert;
   w.row0 = ch.row0;
   w.nrows = ch.nrows;
-  w.phantom = tile >= p.n_tiles;
-  w.tile = w.phantom ? p.n_tiles - 1 : tile;
+  w.tile = tile;
   w.split_idx = s;
   w.ks0 = static_cast<int>(static_cast<int64_t>(p.k_groups) * s / p.split);
   w.ks1 = static_cast<int>(static_cast<int64_t>(p.k_groups) * (s + 1) / p.split);
@@ -248,16 +229,15 @@ __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t
   }
 }
 
-// The 8 pair MMAs of one stage (K = 16 each) as one branch-free sequence: a
-// branch between two tcgen05.mma instructions roughly triples their issue
-// cost.  The A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes
-// along the 128-byte swizzled rows, the second 64-K block 1024 bytes after the
-// first.
+// The 8 MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
+// between two tcgen05.mma instructions roughly triples their issue cost.  The
+// A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
+// 128-byte swizzled rows, the second 64-K block 1024 bytes after the first.
 __device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts_f16_pair(d, a + static_cast<uint32_t>(kk * 8),
-                    bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2), idesc, kk > 0 ? 1u : acc0);
+    mma_ts_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2),
+               idesc, kk > 0 ? 1u : acc0);
 }
 
 __device__ __forceinline__ float silu_dev(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -298,9 +278,8 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 }
 
 // ---------------------------------------------------------------------------
-// The kernel (launched as clusters of 2 CTAs).  Shared memory: weight ring
-// (w_stages slots), token-tile ring (ab_stages slots of T rows, of which a CTA
-// fills half), barriers.  TMEM columns: issuer i owns acc_bufs
+// The kernel.  Shared memory: weight ring (w_stages slots), token-tile ring
+// (ab_stages slots of T rows), barriers.  TMEM columns: issuer i owns acc_bufs
 // fp32 accumulators of T columns at [(i*acc_bufs + b) * T]; token-tile slot j
 // pairs with the 64-column A slot at a_col0 + 64j.  Every role walks only its
 // own stages (every 2nd for producers and dequant sets, every NI-th for the MMA
@@ -333,8 +312,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_cta_rank();  // 0: issues the pair's MMAs
-  const int cluster = static_cast<int>(blockIdx.x >> 1), n_clusters = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NW; ++s) {
@@ -342,22 +319,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_init(smem_u32(wempty + s), kDequantWarps);
     }
     for (int j = 0; j < NB; ++j) {
-      mbar_init(smem_u32(afull + j), 2 * kDequantWarps);  // (even CTA's) the dequant warps of both CTAs
+      mbar_init(smem_u32(afull + j), kDequantWarps);
       mbar_init(smem_u32(sfree + j), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
-      mbar_init(smem_u32(accempty + b), 8);  // (even CTA's) the 4 epilogue warps of both CTAs
+      mbar_init(smem_u32(accempty + b), 4);  // the 4 epilogue warps
     }
     for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(drain + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  // the peer's barriers are initialised before anyone arrives on them remotely
-  cluster_sync();
   if (warp == kMmaWarp) {
-    tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
-    tmem_relinquish_pair();
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -368,7 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   pdl_wait();
 
   const int nch = *p.n_chunks;
-  const int n_items = nch * ((p.n_tiles + 1) >> 1) * p.split;
+  const int n_items = nch * p.n_tiles * p.split;
   const uint32_t a_col0 = static_cast<uint32_t>(p.a_col0);
 
   if (warp == kProducerWarp || warp == kProducerWarp2) {
@@ -382,16 +357,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       wr.idx = br.idx = id;
       int g0 = 0, last_w = -1, last_b = -1;
       bool ok = true;
-      for (int i = cluster; i < n_items && ok; i += n_clusters) {
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
-        decode_item(p, nch, i, rank, it);
+        decode_item(p, nch, i, it);
         const int n_st = it.ks1 - it.ks0;
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_groups * static_cast<int64_t>(p.stage_bytes);
-        // this CTA's half of the chunk's rows (N/2, whole 8-row groups) of one stage
-        // of the pre-staged B operand: one contiguous run
-        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 128u;
-        const uint8_t* bsrc = p.b + (static_cast<int64_t>(it.row0) + static_cast<int64_t>(rank) * (it.nrows >> 1)) * 256;
+        // the chunk's rows of one stage of the pre-staged B operand: one contiguous run
+        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u;
+        const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256;
         for (int g = first_own(g0, id, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
           const int ks = it.ks0 + (g - g0);
           const bool inject = p.fault_injection == 1 && blockIdx.x == 0 && g == 0;  // armed, never filled
@@ -433,16 +407,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     // each stage, is below what the tensor core accepts at small N.  With one
     // (large tiles) warp 5 takes every stage.
     const int id = (warp == kMmaWarp3) ? 2 : warp - kMmaWarp;
-    if (lane == 0 && id < NI && rank == 0) {
+    if (lane == 0 && id < NI) {
       Ring br;
       br.idx = id;
       int g0 = 0, itn = 0;
       bool ok = true;
-      for (int i = cluster; i < n_items && ok; i += n_clusters) {
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         WorkItem it;
-        decode_item(p, nch, i, rank, it);
+        decode_item(p, nch, i, it);
         const int n_st = it.ks1 - it.ks0;
-        const uint32_t idesc = make_idesc_m256(static_cast<uint32_t>(it.nrows), false);
+        const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
         const int b = (ACCB == 2) ? (itn & 1) : 0;
         const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
         if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
@@ -463,21 +437,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
           mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
           acc0 = 1u;
-          mma_commit_pair(smem_u32(sfree + br.idx));
+          mma_commit(smem_u32(sfree + br.idx));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
-        mma_commit_pair(smem_u32(accfull + b));
+        mma_commit(smem_u32(accfull + b));
         g0 += n_st;
         ++itn;
       }
       if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
-      // all MMAs this thread issued must finish before TMEM is released (in both CTAs)
-      mma_commit_pair(smem_u32(drain + id));
-      mbar_wait_drain(smem_u32(drain + id), 0);
-    } else if (lane == 0 && id < NI) {
-      // odd CTA: its TMEM and shared memory stay in use until the even CTA's
-      // issuer reports all its MMAs complete
+      // all MMAs this thread issued must finish before TMEM is released
+      mma_commit(smem_u32(drain + id));
       mbar_wait_drain(smem_u32(drain + id), 0);
     }
   } else if (warp >= kDequantWarp0) {
@@ -491,9 +461,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     wr.idx = br.idx = set;
     int g0 = 0;
     bool ok = true;
-    for (int i = cluster; i < n_items && ok; i += n_clusters) {
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
-      decode_item(p, nch, i, rank, it);
+      decode_item(p, nch, i, it);
       const int n_st = it.ks1 - it.ks0;
       for (int g = first_own(g0, set, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
         // weights and token tile landed; the latter also means the MMAs of the A
@@ -526,7 +496,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(afull + br.idx), 0));
+        if (lane == 0) mbar_arrive(smem_u32(afull + br.idx));
       }
       g0 += n_st;
     }
@@ -538,9 +508,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int itn = 0, g0 = 0;
     bool ok = true;
-    for (int i = cluster; i < n_items && ok; i += n_clusters) {
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
-      decode_item(p, nch, i, rank, it);
+      decode_item(p, nch, i, it);
       const int b = (ACCB == 2) ? (itn & 1) : 0;
       const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
@@ -571,7 +541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         if (c0 + 16 >= it.nrows) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(accempty + b), 0));
+          if (lane == 0) mbar_arrive(smem_u32(accempty + b));
         }
         const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + it.row0 + c0);
 #pragma unroll
@@ -582,7 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           f[4 * c + 2] *= rs * v4.z;
           f[4 * c + 3] *= rs * v4.w;
         }
-        if (!it.phantom) epilogue_store(p, it, c0, row, lane, f);
+        epilogue_store(p, it, c0, row, lane, f);
       }
       ++itn;
     }
@@ -590,13 +560,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   }
 
   // ------------------------------------------------------------ teardown
-  // (no remote arrive and no pair MMA touches either CTA after the cluster barrier)
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc_pair(tmem, kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -606,9 +574,7 @@ cudaError_t launch_gemm_t(const GemmParams& p, int grid, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<KIND, BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  // clusters of 2 CTAs (grid even)
-  if (grid % 2 != 0) return cudaErrorInvalidValue;
-  return launch_kernel_cluster(qmoe_gemm_kernel<KIND, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, 2, p);
+  return launch_kernel(qmoe_gemm_kernel<KIND, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, p);
 }
 
 }  // namespace qmoe

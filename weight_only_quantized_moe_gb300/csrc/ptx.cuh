@@ -38,27 +38,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
-// thread-block clusters (the GEMM runs on CTA pairs)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_cta_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of both CTAs arrives; returns once all have (release / acquire
-// at cluster scope, so mbarrier initialisation and shared-memory writes before
-// it are visible to the peer CTA after it).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Shared::cluster address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
-  return r;
-}
-
-// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -98,17 +77,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
-}
-
-// Arrive once on the barrier at shared::cluster address `remote_bar` (the peer
-// CTA's, or this CTA's own through the cluster window).  Default semantics
-// (release at CTA scope): the callers order their tensor-memory stores or loads
-// with tcgen05.wait + tcgen05.fence::before_thread_sync, and the waiter with
-// tcgen05.fence::after_thread_sync, as for a local barrier.  A release at
-// cluster scope would cost the arriving thread ~320 cycles (measured on GB300)
-// and triple the round trip.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
 // Wait until the phase with the given parity has completed.  Returns false if
@@ -181,19 +149,16 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor-core MMA
 // ---------------------------------------------------------------------------
-// The GEMM kernel uses the CTA-pair (cta_group::2) forms throughout: one warp
-// in each CTA of the pair executes the allocation (same column count), and
-// both CTAs receive the same TMEM address.
-// Allocate `ncols` TMEM columns (power of two >= 32) in both CTAs of the pair.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+// Allocate `ncols` TMEM columns (power of two >= 32); one full warp executes it.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                : "memory");
 }
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -202,37 +167,31 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Pair MMA, issued by one thread of the pair's even CTA: D (+)= A * B^T with
-// M = 256 (rows 0-127 in the even CTA's TMEM lanes, 128-255 in the odd CTA's,
-// A and D at the same TMEM address in both), N from idesc (each CTA's shared
-// memory holds N/2 rows of B at the same address), K = 16 (16-bit types).
-__device__ __forceinline__ void mma_ts_f16_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T ; M = 128, N from idesc, K = 16 (16-bit types).
+__device__ __forceinline__ void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive once on the barrier at this shared-memory offset in both CTAs of the
-// pair when every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(static_cast<uint16_t>(0x3))
-      : "memory");
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
 }
 
-// Instruction descriptor of kind::f16: D f32, A/B f16 or bf16, both K-major, M = 256 (pair).
-__host__ __device__ __forceinline__ uint32_t make_idesc_m256(uint32_t n, bool bf16) {
+// Instruction descriptor of kind::f16: D f32, A/B f16 or bf16, both K-major, M = 128.
+__host__ __device__ __forceinline__ uint32_t make_idesc_m128(uint32_t n, bool bf16) {
   const uint32_t ab = bf16 ? 1u : 0u;
   return (1u << 4)             // D format: f32
          | (ab << 7)           // A format
          | (ab << 10)          // B format
          | ((n >> 3) << 17)    // N / 8
-         | ((256u >> 4) << 24);  // M / 16
+         | ((128u >> 4) << 24);  // M / 16
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups

@@ -102,32 +102,6 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// The same for a kernel taking GemmParams, with thread-block clusters of
-// `cluster_x` CTAs along x (grid.x a multiple of it).
-inline cudaError_t launch_kernel_cluster(void (*kern)(GemmParams), dim3 grid, dim3 block, size_t smem,
-                                         cudaStream_t stream, bool pdl, int cluster_x, const GemmParams& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  attr[n].id = cudaLaunchAttributeClusterDimension;
-  attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
-  attr[n].val.clusterDim.y = 1;
-  attr[n].val.clusterDim.z = 1;
-  ++n;
-  if (pdl) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
 // Host-side launchers (defined in the .cu files); return cudaError_t of the launch.
 cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t block, int64_t capacity,
                          int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded, int32_t token_tile,
