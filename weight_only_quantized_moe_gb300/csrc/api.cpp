@@ -220,12 +220,14 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   // Epilogue time of one item in pipeline stages (measured on GB300: about 3k
   // cycles for a 16-row chunk, 15k for a 128-row one, against 0.7k-1.1k per
   // stage).  Partial sums of one extra split: written and read once in fp32,
-  // in stage-times of the whole GPU's weight stream (~1.3 MB per stage-time)
-  // (plus half a stage per split for summing the partials).
+  // in stage-times of the whole GPU's weight stream (~1.3 MB per stage-time),
+  // plus two stages per split for the extra items' pipeline fill and drain
+  // and for summing the partials (fitted on GB300: Mixtral-8x7B decode runs
+  // its down GEMM fastest split 4 ways, not 7).
   const double epi = 4.0 + T / 8.0;
   const double stage_bytes_gpu = 1.3e6;
-  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, epi, 0.5 + 8.0 * P * 2 * L->I / stage_bytes_gpu, 0.8);
-  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, epi, 0.5 + 8.0 * P * L->H / stage_bytes_gpu, 0.97);
+  p.S1 = choose_split(est_chunks * p.n_tiles1, p.kst1, sms, epi, 2.0 + 8.0 * P * 2 * L->I / stage_bytes_gpu, 0.8);
+  p.S2 = choose_split(est_chunks * p.n_tiles2, p.kst2, sms, epi, 2.0 + 8.0 * P * L->H / stage_bytes_gpu, 0.99);
   if (o != nullptr && o->split1 != 0) {
     if (o->split1 < 1 || o->split1 > 64 || o->split1 > p.kst1) return QMOE_ERR_INVALID_ARG;
     p.S1 = o->split1;
