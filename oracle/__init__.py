@@ -9,6 +9,7 @@ own formulas (round trips, closed forms, invariants, brute force on tiny
 inputs and hand-worked examples); see the module docstrings for the pins.
 """
 from .moe import (  # noqa: F401
+    decompress_24,
     dequant_int4,
     dequant_int8,
     dequant_int8_group,

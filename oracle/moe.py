@@ -78,6 +78,25 @@ def dequant_int4(q: np.ndarray, s: np.ndarray, g_idx: np.ndarray | None,
     return (q.astype(np.float64) - zero_nk) * scale_nk
 
 
+def decompress_24(values: np.ndarray, positions: np.ndarray, zero_code: int = 8) -> np.ndarray:
+    """Dense codes [N, K] of a 2:4-compressed matrix ("Add GPTQ Marlin 2:4
+    sparse structured support"): for every aligned group j of 4 input channels,
+    values[n, 2j] and values[n, 2j+1] are the codes at channels 4j + i0 and
+    4j + i1 with positions[n, j] = (i0, i1), i0 < i1; the other two channels
+    hold `zero_code` (value 0 under zero point 8).
+    values: uint8 [N, K/2]; positions: int [N, K/4, 2]."""
+    values = np.asarray(values)
+    positions = np.asarray(positions, np.int64)
+    N, half = values.shape
+    K = 2 * half
+    q = np.full((N, K), zero_code, np.uint8)
+    rows = np.arange(N)[:, None]
+    base = 4 * np.arange(K // 4)[None, :]
+    q[rows, base + positions[:, :, 0]] = values[:, 0::2]
+    q[rows, base + positions[:, :, 1]] = values[:, 1::2]
+    return q
+
+
 def dequant_int8(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """W[n, k] = q[n, k] * s[n] ("[Kernel] W8A16 Int8 inside FusedMoE": symmetric
     per-column, per-expert int8), float64 [N, K]."""
@@ -96,7 +115,8 @@ def dequant_int8_group(q: np.ndarray, s: np.ndarray, group_size: int) -> np.ndar
 def dequant_layer_expert(layer, e: int):
     """Dequantized (W13_e [2I, H], W2_e [H, I]) of expert e of a canonical layer."""
     wl = layer.wl
-    if wl.qt in ("int4", "int4zp"):
+    if wl.qt in ("int4", "int4zp", "int4s24"):
+        # int4s24: the canonical codes are dense, 8 (value 0) at the pruned channels
         g13 = None if layer.g13 is None else layer.g13[e]
         g2 = None if layer.g2 is None else layer.g2[e]
         z13 = None if layer.z13 is None else layer.z13[e]

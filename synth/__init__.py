@@ -15,6 +15,8 @@ from .gen import (  # noqa: F401
     Inputs,
     make_layer,
     make_inputs,
+    prune_24,
+    quantize_int4_24,
     quantize_int4_rtn,
     quantize_int4_rtn_zp,
     quantize_int8_group,

@@ -32,8 +32,9 @@ class Workload:
     k: int            # top-k
     H: int            # hidden size
     I: int            # expert intermediate size
-    qt: str           # "int4" (zero point 8), "int4zp" (per-group zero points), "int8" (per
-                      # output column) or "int8g" (group scales)
+    qt: str           # "int4" (zero point 8), "int4zp" (per-group zero points), "int4s24"
+                      # (int4, 2:4 sparse along K), "int8" (per output column) or "int8g"
+                      # (group scales)
     group_size: int   # 128 or -1 (whole K is one group) for int4 / int4zp; -1 for int8; 128 for int8g
     act: str          # activation / scale storage type: "f16" or "bf16"
     act_order: bool   # int4 only: random per-expert g_idx permutation
@@ -51,6 +52,8 @@ class Workload:
         groups = (2 * self.I + self.H) if self.group_size < 0 else n // self.group_size
         if self.qt == "int4":
             return n // 2 + groups * 2
+        if self.qt == "int4s24":   # half the values, 2 bits of position each
+            return n // 4 + n // 8 + groups * 2
         if self.qt == "int4zp":
             return n // 2 + groups * 2 + groups // 2
         if self.qt == "int8g":
@@ -73,6 +76,9 @@ WORKLOADS = {
     # DeepSeek-V2-like many-expert layer with a skewed router
     "deepseekv2_w8": Workload("deepseekv2_w8", 160, 6, 5120, 1536, "int8", -1, "bf16",
                               False, 1.1, (1, 32, 256, 1024)),
+    # Mixtral-8x7B shape with 2:4-sparse int4 g128 experts
+    "mixtral8x7b_w4s24": Workload("mixtral8x7b_w4s24", 8, 2, 4096, 14336, "int4s24", 128, "f16",
+                                  False, 0.0, (1, 16, 64)),
     # Mixtral-8x22B prefill, tensor-core-bound
     "mixtral8x22b_w4": Workload("mixtral8x22b_w4", 8, 2, 6144, 16384, "int4", 128, "bf16",
                                 False, 0.0, (2048, 4096, 8192)),
@@ -140,6 +146,28 @@ def quantize_int4_rtn(w: np.ndarray, group_size: int, g_idx: np.ndarray | None,
     s_el = s[:, g_idx]                                # [N, K]
     q = np.clip(np.rint(w / s_el), -8, 7) + 8
     return q.astype(np.uint8), np.ascontiguousarray(s.T)
+
+
+def prune_24(w: np.ndarray) -> np.ndarray:
+    """2:4 structured sparsity along K: in every aligned group of 4 input
+    channels keep the 2 entries of largest magnitude (ties go to the lower
+    channel) and zero the other 2.  w: float32 [N, K], K % 4 == 0."""
+    N, K = w.shape
+    g = np.abs(w).reshape(N, K // 4, 4)
+    # stable descending order by magnitude: lower index first among equals
+    order = np.argsort(-g, axis=2, kind="stable")
+    keep = np.zeros_like(g, dtype=bool)
+    np.put_along_axis(keep, order[:, :, :2], True, axis=2)
+    return np.where(keep.reshape(N, K), w, np.float32(0.0)).astype(np.float32)
+
+
+def quantize_int4_24(w: np.ndarray, group_size: int, scale_dtype: str):
+    """2:4-sparse int4 ("Add GPTQ Marlin 2:4 sparse structured support": 4-bit,
+    group 128 or channel-wise): prune_24, then symmetric int4 RTN with zero
+    point 8 on the pruned matrix, so every pruned entry has code 8 (value 0)
+    and every aligned group of 4 codes along K holds at most 2 codes other
+    than 8.  Returns codes uint8 [N, K] and scales float32 [K/G, N]."""
+    return quantize_int4_rtn(prune_24(w), group_size, None, scale_dtype)
 
 
 def quantize_int4_rtn_zp(w: np.ndarray, group_size: int, g_idx: np.ndarray | None, scale_dtype: str):
@@ -234,7 +262,10 @@ def _gen_expert(wl: Workload, seed: int, e: int):
         rng = np.random.default_rng([seed, e, sub])
         w = rng.standard_normal((N, K), dtype=np.float32)
         w *= np.float32(wl.w_std)
-        if wl.qt in ("int4", "int4zp"):
+        if wl.qt == "int4s24":
+            q, s = quantize_int4_24(w, wl.group_size, wl.act)
+            out[mat] = (q, s, None, None)
+        elif wl.qt in ("int4", "int4zp"):
             g = None
             if wl.act_order:
                 g = _actorder_gidx(np.random.default_rng([seed, e, 2 + sub]), K, wl.group_size)
@@ -257,7 +288,7 @@ def _gen_expert(wl: Workload, seed: int, e: int):
 def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> QuantLayer:
     E, H, I = wl.E, wl.H, wl.I
     z13 = z2 = None
-    if wl.qt in ("int4", "int4zp", "int8g"):
+    if wl.qt in ("int4", "int4zp", "int4s24", "int8g"):
         n13 = 1 if wl.group_size < 0 else H // wl.group_size
         n2 = 1 if wl.group_size < 0 else I // wl.group_size
         cdt = np.int8 if wl.qt == "int8g" else np.uint8

@@ -16,8 +16,8 @@ import numpy as np
 import pytest
 
 import oracle
-from synth import (QuantLayer, Workload, make_inputs, make_layer, quantize_int4_rtn, quantize_int4_rtn_zp,
-                   quantize_int8_group, quantize_int8_rtn)
+from synth import (QuantLayer, Workload, make_inputs, make_layer, prune_24, quantize_int4_24, quantize_int4_rtn,
+                   quantize_int4_rtn_zp, quantize_int8_group, quantize_int8_rtn)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -292,7 +292,7 @@ def _brute_force(layer, x, ids, w):
     out = [[0.0] * H for _ in range(M)]
 
     def wq(q, s, gi, z, e, n, c):
-        if wl.qt in ("int4", "int4zp", "int8g"):
+        if wl.qt in ("int4", "int4zp", "int4s24", "int8g"):
             if gi is not None:
                 g = int(gi[e, c])
             elif wl.group_size < 0:
@@ -330,7 +330,8 @@ def _brute_force(layer, x, ids, w):
 
 @pytest.mark.parametrize("qt,act_order,gs", [("int4", False, 16), ("int4", True, 16), ("int8", False, -1),
                                              ("int4zp", False, 16), ("int4zp", True, 16), ("int4", False, -1),
-                                             ("int4zp", False, -1), ("int8g", False, 16)])
+                                             ("int4zp", False, -1), ("int8g", False, 16), ("int4s24", False, 16),
+                                             ("int4s24", False, -1)])
 def test_brute_force_tiny(qt, act_order, gs):
     wl = _wl(E=4, k=2, H=32, I=48, qt=qt, group_size=gs, act_order=act_order)
     layer = make_layer(wl, seed=17)
@@ -527,3 +528,82 @@ def test_int8_group_round_trip_hand_values_and_per_column_case(sdt):
     # one scale repeated over every group is the per-column format
     s_col = rng.random(16) + 0.1
     assert np.array_equal(oracle.dequant_int8_group(q, np.tile(s_col, (3, 1)), 128), oracle.dequant_int8(q, s_col))
+
+
+# ----------------------------------------------------------------------------
+# 2:4 structured sparsity ("Add GPTQ Marlin 2:4 sparse structured support")
+# ----------------------------------------------------------------------------
+def test_decompress_24_worked_example():
+    # one row, K = 8: group 0 keeps channels 0 and 2, group 1 keeps 5 and 7
+    values = np.array([[3, 12, 0, 15]], np.uint8)
+    positions = np.array([[[0, 2], [1, 3]]])
+    got = oracle.decompress_24(values, positions)
+    np.testing.assert_array_equal(got, [[3, 8, 12, 8, 8, 0, 8, 15]])
+
+
+def _compress_24_loops(q):
+    """Scalar compressor: per group of 4, the channels whose code is not 8, padded
+    with the lowest remaining channels; None if a group has more than two."""
+    N, K = q.shape
+    values = np.zeros((N, K // 2), np.uint8)
+    positions = np.zeros((N, K // 4, 2), np.int64)
+    for n in range(N):
+        for j in range(K // 4):
+            nz = [i for i in range(4) if q[n, 4 * j + i] != 8]
+            if len(nz) > 2:
+                return None
+            for i in range(4):
+                if len(nz) < 2 and i not in nz:
+                    nz.append(i)
+            nz = sorted(nz[:2])
+            positions[n, j] = nz
+            values[n, 2 * j] = q[n, 4 * j + nz[0]]
+            values[n, 2 * j + 1] = q[n, 4 * j + nz[1]]
+    return values, positions
+
+
+def test_decompress_24_inverts_scalar_compressor():
+    rng = np.random.default_rng(5)
+    N, K = 7, 64
+    q = np.full((N, K), 8, np.uint8)
+    for n in range(N):
+        for j in range(K // 4):
+            keep = rng.choice(4, size=rng.integers(0, 3), replace=False)
+            q[n, 4 * j + keep] = rng.integers(0, 16, size=keep.size)
+    values, positions = _compress_24_loops(q)
+    np.testing.assert_array_equal(oracle.decompress_24(values, positions), q)
+    # a swapped position pair puts the values at the wrong channels
+    bad = positions.copy()
+    bad[0, 0] = bad[0, 0][::-1]
+    if values[0, 0] != values[0, 1]:
+        assert not np.array_equal(oracle.decompress_24(values, bad), q)
+
+
+def test_prune_24_keeps_two_largest_per_group():
+    rng = np.random.default_rng(6)
+    w = rng.standard_normal((5, 32)).astype(np.float32)
+    w[0, 0:4] = [1.0, -1.0, 1.0, 0.5]          # ties: the lower channels win
+    p = prune_24(w)
+    for n in range(w.shape[0]):
+        for j in range(w.shape[1] // 4):
+            g = [abs(float(v)) for v in w[n, 4 * j:4 * j + 4]]
+            order = sorted(range(4), key=lambda i: (-g[i], i))[:2]
+            for i in range(4):
+                want = w[n, 4 * j + i] if i in order else 0.0
+                assert p[n, 4 * j + i] == want
+    np.testing.assert_array_equal(p[0, 0:4], [1.0, -1.0, 0.0, 0.0])
+    np.testing.assert_array_equal(prune_24(p), p)
+
+
+@pytest.mark.parametrize("gs", [16, -1])
+def test_quantize_int4_24_structure_and_round_trip(gs):
+    rng = np.random.default_rng(7)
+    w = (0.02 * rng.standard_normal((12, 64))).astype(np.float32)
+    q, s = quantize_int4_24(w, gs, "f16")
+    nz = (q.reshape(12, 16, 4) != 8).sum(axis=2)
+    assert nz.max() <= 2
+    p = prune_24(w)
+    assert np.all(q[p == 0] == 8)
+    deq = oracle.dequant_int4(q, s, None, gs)
+    g = np.arange(64) // (64 if gs < 0 else gs)
+    assert np.all(np.abs(deq - p) <= s[g, :].T / 2 + 1e-12)
