@@ -63,7 +63,8 @@ def peaks():
 
 def workload_config(wl, M, extra=None):
     cfg = {"workload": f"{wl.name}: E={wl.E} top-{wl.k} H={wl.H} I={wl.I} {wl.qt}"
-                       f"{' g128' if wl.qt == 'int4' else ' per-column'}{' act-order' if wl.act_order else ''}"
+                       f"{' g128' if wl.group_size == 128 else ' per-column'}"
+                       f"{' 2:4-sparse' if wl.qt == 'int4s24' else ''}{' act-order' if wl.act_order else ''}"
                        f" {wl.act} activations, M={M}",
            "E": wl.E, "top_k": wl.k, "hidden": wl.H, "intermediate": wl.I, "quant": wl.qt,
            "group_size": wl.group_size, "act_order": wl.act_order, "act_dtype": wl.act, "M": M}

@@ -74,7 +74,10 @@ typedef enum {
   QMOE_INT8_PER_COL = 2,  /* signed 8-bit codes, one float32 scale per output feature */
   QMOE_INT4_GROUP_ZP = 3, /* 4-bit codes 0..15 with a zero point 0..15 and a scale per group
                              (128 input channels, or all of them with group_size -1) */
-  QMOE_INT8_GROUP = 4     /* signed 8-bit codes, one scale per 128 input channels */
+  QMOE_INT8_GROUP = 4,    /* signed 8-bit codes, one scale per 128 input channels */
+  QMOE_INT4_GROUP_24 = 5  /* as QMOE_INT4_GROUP, 2:4 sparse along K: in every aligned group of
+                             4 input channels at most 2 codes differ from 8 (value 0); only
+                             those 2 codes and their positions are stored */
 } qmoe_quant_type;
 
 typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
@@ -86,8 +89,9 @@ typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
  *
  *   E, H, I      experts, hidden size, expert intermediate size.
  *                Constraints: 1 <= E <= 1024; H % 128 == 0; I % 128 == 0.
- *   group_size   QMOE_INT4_GROUP / QMOE_INT4_GROUP_ZP: 128 or -1
- *                (channel-wise); QMOE_INT8_PER_COL: -1; QMOE_INT8_GROUP: 128.
+ *   group_size   QMOE_INT4_GROUP / QMOE_INT4_GROUP_ZP / QMOE_INT4_GROUP_24: 128
+ *                or -1 (channel-wise); QMOE_INT8_PER_COL: -1; QMOE_INT8_GROUP: 128.
+ *                QMOE_INT4_GROUP_24 takes no act-order permutation.
  *   qt           quantization type.
  *   act_dtype    F16 or BF16: type of x and out (the MMAs run in f16).
  *   scale_dtype  int4 and grouped int8: must equal act_dtype (scales are
@@ -153,9 +157,9 @@ typedef struct {
  * Bytes of one packed matrix for all E experts: W13 is (rows = 2I, K = H),
  * W2 is (rows = H, K = I).  Returns 0 for an unsupported combination.
  * Per 128 x 128 block: QMOE_INT4_GROUP 8448 (group_size 128 or -1),
- * QMOE_INT4_GROUP_ZP 8576 (group_size 128 or -1), QMOE_INT8_PER_COL 16384
- * (group_size -1), QMOE_INT8_GROUP 16640 (group_size 128); times
- * E * (rows/128) * (K/128).
+ * QMOE_INT4_GROUP_ZP 8576 (group_size 128 or -1), QMOE_INT4_GROUP_24 6400
+ * (group_size 128 or -1), QMOE_INT8_PER_COL 16384 (group_size -1),
+ * QMOE_INT8_GROUP 16640 (group_size 128); times E * (rows/128) * (K/128).
  */
 size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K, int32_t group_size);
 
@@ -220,6 +224,27 @@ qmoe_status qmoe_unpack_int4_zp(int32_t E, int32_t H, int32_t I, int32_t group_s
 qmoe_status qmoe_pack_int8_group(int32_t E, int32_t H, int32_t I, qmoe_dtype scale_dtype,
                                  const int8_t* q13, const uint16_t* s13, const int8_t* q2, const uint16_t* s2,
                                  void* w13_packed, void* w2_packed);
+
+/*
+ * Pack 2:4-sparse int4 ("Add GPTQ Marlin 2:4 sparse structured support":
+ * 4-bit, group 128 or channel-wise, 2:4 structured sparsity).  Canonical
+ * inputs (host) as for qmoe_pack_int4 without g_idx: q13 uint8 [E, 2I, H] and
+ * q2 uint8 [E, H, I] dense codes 0..15 with zero point 8, where every aligned
+ * group of 4 consecutive input channels holds at most 2 codes other than 8;
+ * s13 uint16 [E, H/128 (or 1), 2I], s2 uint16 [E, I/128 (or 1), H] scale bit
+ * patterns of scale_dtype.  Per group of 4 the packer keeps the channels whose
+ * code is not 8, padded with the lowest remaining channels, as 2 codes and 2
+ * two-bit positions.  Outputs (host): w13_packed, w2_packed.  A group with
+ * more than 2 codes other than 8, or a code above 15, gives
+ * QMOE_ERR_INVALID_ARG.  The layer's qt is QMOE_INT4_GROUP_24.
+ */
+qmoe_status qmoe_pack_int4_24(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                              const uint8_t* q13, const uint16_t* s13, const uint8_t* q2, const uint16_t* s2,
+                              void* w13_packed, void* w2_packed);
+
+/* Exact inverse of qmoe_pack_int4_24 (dense codes, 8 at the pruned channels). */
+qmoe_status qmoe_unpack_int4_24(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                                const void* w2_packed, uint8_t* q13, uint16_t* s13, uint8_t* q2, uint16_t* s2);
 
 /* Exact inverse of qmoe_pack_int8_group. */
 qmoe_status qmoe_unpack_int8_group(int32_t E, int32_t H, int32_t I, const void* w13_packed, const void* w2_packed,

@@ -234,3 +234,48 @@ def test_options_layout_and_issuer_validation():
     assert size(4096, issuers=3) == 0          # 384 accumulator columns leave no room for A slots
     assert size(16, issuers=4) == 0
     assert size(16, issuers=-1) == 0
+
+
+@pytest.mark.parametrize("act,gs", [("f16", 128), ("bf16", 128), ("f16", -1)])
+def test_pack_int4_24_round_trip_and_layout(act, gs):
+    import oracle
+    wl = Workload("s24", 2, 2, 256, 384, "int4s24", gs, act, False, 0.0, (1,))
+    L = make_layer(wl, seed=10)
+    s13b, s2b = to_u16_bits(L.s13, act), to_u16_bits(L.s2, act)
+    pk = q.qmoe_pack_int4_24(wl.E, wl.H, wl.I, act, L.q13, s13b, L.q2, s2b, gs)
+    assert pk["w13"].nbytes == wl.E * (2 * wl.I // 128) * (wl.H // 128) * 6400
+    q13, s13, q2, s2 = q.qmoe_unpack_int4_24(wl.E, wl.H, wl.I, pk["w13"], pk["w2"], gs)
+    assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
+    assert np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
+    # the packed block read back through the oracle's definition of the format:
+    # W2 of expert 0, tile 0, K block 0, half h, row r holds channels 64h .. 64h+63 of row r
+    blk = pk["w2"][:6400]
+    for r in (0, 77, 127):
+        for h in (0, 1):
+            codes = blk[(h * 128 + r) * 16:(h * 128 + r) * 16 + 16]
+            pos = int.from_bytes(bytes(blk[4096 + (h * 128 + r) * 8:4096 + (h * 128 + r) * 8 + 8]), "little")
+            vals = np.zeros((1, 32), np.uint8)
+            positions = np.zeros((1, 16, 2), np.int64)
+            for g in range(16):
+                j, i = divmod(g, 4)
+                word = int.from_bytes(bytes(codes[4 * j:4 * j + 4]), "little")
+                vals[0, 2 * g] = (word >> (4 * i)) & 15
+                vals[0, 2 * g + 1] = (word >> (4 * (i + 4))) & 15
+                m = (pos >> (4 * g)) & 15
+                positions[0, g] = (m & 3, m >> 2)
+                assert (m & 3) < (m >> 2)
+            dense = oracle.decompress_24(vals, positions)
+            assert np.array_equal(dense[0], L.q2[0, r, 64 * h:64 * h + 64])
+        assert int.from_bytes(bytes(blk[6144 + 2 * r:6146 + 2 * r]), "little") == s2b[0, 0, r]
+
+
+def test_pack_int4_24_rejects_three_of_four():
+    wl = Workload("s24", 1, 2, 128, 128, "int4s24", 128, "f16", False, 0.0, (1,))
+    L = make_layer(wl, seed=11)
+    s13b, s2b = to_u16_bits(L.s13, "f16"), to_u16_bits(L.s2, "f16")
+    q2 = L.q2.copy()
+    q2[0, 5, 8:12] = [1, 2, 3, 8]
+    with pytest.raises(q.QmoeError) as ei:
+        q.qmoe_pack_int4_24(1, 128, 128, "f16", L.q13, s13b, q2, s2b)
+    assert ei.value.status == q.QMOE_ERR_INVALID_ARG
+    assert q.packed_bytes("int4s24", 1, 256, 128) == 2 * 6400

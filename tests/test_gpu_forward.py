@@ -54,7 +54,8 @@ VARIANTS = [("int4", "f16", False), ("int4", "bf16", False), ("int4", "f16", Tru
 # weight formats beyond the pages' two: per-group zero points, channel-wise int4, group-128 int8
 OTHER_FORMATS = [("int4zp", "f16", False, 128), ("int4zp", "bf16", True, 128), ("int4zp", "bf16", False, -1),
                  ("int4", "f16", False, -1), ("int4", "bf16", False, -1), ("int8g", "f16", False, 128),
-                 ("int8g", "bf16", False, 128)]
+                 ("int8g", "bf16", False, 128), ("int4s24", "f16", False, 128), ("int4s24", "bf16", False, 128),
+                 ("int4s24", "f16", False, -1)]
 
 
 @pytest.mark.parametrize("qt,act,ao", VARIANTS)
@@ -69,7 +70,7 @@ def test_forward_parity_other_formats(qt, act, ao, gs, M):
     _check(_wl(qt, act, ao, gs=gs), M)
 
 
-@pytest.mark.parametrize("qt,act,ao,gs", OTHER_FORMATS[:2] + OTHER_FORMATS[5:6])
+@pytest.mark.parametrize("qt,act,ao,gs", OTHER_FORMATS[:2] + OTHER_FORMATS[5:6] + OTHER_FORMATS[7:8])
 @pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 128)])
 def test_forward_other_formats_forced_split_and_tile(qt, act, ao, gs, split1, split2, tile):
     _check(_wl(qt, act, ao, gs=gs), 40, opts=q.make_options(split1, split2, tile))

@@ -24,6 +24,7 @@ WORKLOADS_OTHER = {
 CASES = [
     ("mixtral8x7b_w4zp", 16, 2),
     ("mixtral8x7b_w8g", 16, 2),
+    ("mixtral8x7b_w4s24", 16, 2),
     ("mixtral8x7b_w4", 16, 4),
     ("mixtral8x7b_w4", 1, 1),
     ("mixtral8x7b_w4_actorder", 16, 3),

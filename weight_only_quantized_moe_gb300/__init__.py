@@ -34,10 +34,12 @@ from .api import (  # noqa: F401
     qmoe_pack_int4,
     qmoe_pack_int8,
     qmoe_pack_int8_group,
+    qmoe_pack_int4_24,
     qmoe_read_device_status,
     qmoe_route_topk,
     qmoe_unpack_int4,
     qmoe_unpack_int8_group,
+    qmoe_unpack_int4_24,
     qmoe_workspace_size_logits,
     qmoe_unpack_int8,
     qmoe_workspace_size,

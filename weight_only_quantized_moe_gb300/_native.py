@@ -27,6 +27,7 @@ QMOE_INT4_GROUP = 1
 QMOE_INT8_PER_COL = 2
 QMOE_INT4_GROUP_ZP = 3
 QMOE_INT8_GROUP = 4
+QMOE_INT4_GROUP_24 = 5
 QMOE_F16 = 1
 QMOE_BF16 = 2
 QMOE_F32 = 3
@@ -74,6 +75,10 @@ _SIGS = {
                                       POINTER(c_uint8), POINTER(c_uint16), POINTER(c_uint8)]),
     "qmoe_pack_int8_group": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_void_p, POINTER(c_uint16), c_void_p,
                                        POINTER(c_uint16), c_void_p, c_void_p]),
+    "qmoe_pack_int4_24": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32, POINTER(c_uint8), POINTER(c_uint16),
+                                    POINTER(c_uint8), POINTER(c_uint16), c_void_p, c_void_p]),
+    "qmoe_unpack_int4_24": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, POINTER(c_uint8),
+                                      POINTER(c_uint16), POINTER(c_uint8), POINTER(c_uint16)]),
     "qmoe_unpack_int8_group": (c_int32, [c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, POINTER(c_uint16),
                                          c_void_p, POINTER(c_uint16)]),
     "qmoe_pack_int8": (c_int32, [c_int32, c_int32, c_int32, c_void_p, POINTER(c_float), c_void_p, POINTER(c_float),

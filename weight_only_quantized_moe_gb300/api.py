@@ -15,7 +15,7 @@ from . import _native as N
 _ACT = {"f16": N.QMOE_F16, "bf16": N.QMOE_BF16}
 _TORCH_ACT = {"f16": torch.float16, "bf16": torch.bfloat16}
 _QT = {"int4": N.QMOE_INT4_GROUP, "int4zp": N.QMOE_INT4_GROUP_ZP, "int8": N.QMOE_INT8_PER_COL,
-       "int8g": N.QMOE_INT8_GROUP}
+       "int8g": N.QMOE_INT8_GROUP, "int4s24": N.QMOE_INT4_GROUP_24}
 
 
 def default_group_size(qt: str) -> int:
@@ -126,6 +126,38 @@ def qmoe_unpack_int8_group(E, H, I, w13, w2):
     return q13, s13, q2, s2
 
 
+def qmoe_pack_int4_24(E, H, I, scale_dtype, q13, s13_bits, q2, s2_bits, group_size=128):
+    """Pack 2:4-sparse int4: dense codes (8 at the pruned channels, at most 2
+    other codes per aligned group of 4 input channels) and uint16 scale bit
+    patterns [E, K/G, N] ([E, 1, N] with group_size -1)."""
+    q13 = np.ascontiguousarray(q13, np.uint8)
+    q2 = np.ascontiguousarray(q2, np.uint8)
+    s13_bits = np.ascontiguousarray(s13_bits, np.uint16)
+    s2_bits = np.ascontiguousarray(s2_bits, np.uint16)
+    w13 = np.empty(packed_bytes("int4s24", E, 2 * I, H, group_size), np.uint8)
+    w2 = np.empty(packed_bytes("int4s24", E, H, I, group_size), np.uint8)
+    st = N.lib().qmoe_pack_int4_24(E, H, I, group_size, _ACT[scale_dtype], _np_ptr(q13, c_uint8),
+                                   _np_ptr(s13_bits, c_uint16), _np_ptr(q2, c_uint8), _np_ptr(s2_bits, c_uint16),
+                                   w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p))
+    N.check(st, "qmoe_pack_int4_24")
+    return {"w13": w13, "w2": w2}
+
+
+def qmoe_unpack_int4_24(E, H, I, w13, w2, group_size=128):
+    """Inverse of qmoe_pack_int4_24: dense (q13, s13, q2, s2)."""
+    n13 = 1 if group_size < 0 else H // 128
+    n2 = 1 if group_size < 0 else I // 128
+    q13 = np.empty((E, 2 * I, H), np.uint8)
+    s13 = np.empty((E, n13, 2 * I), np.uint16)
+    q2 = np.empty((E, H, I), np.uint8)
+    s2 = np.empty((E, n2, H), np.uint16)
+    st = N.lib().qmoe_unpack_int4_24(E, H, I, group_size, w13.ctypes.data_as(c_void_p), w2.ctypes.data_as(c_void_p),
+                                     _np_ptr(q13, c_uint8), _np_ptr(s13, c_uint16), _np_ptr(q2, c_uint8),
+                                     _np_ptr(s2, c_uint16))
+    N.check(st, "qmoe_unpack_int4_24")
+    return q13, s13, q2, s2
+
+
 def qmoe_pack_int8(E, H, I, q13, s13, q2, s2):
     q13 = np.ascontiguousarray(q13, np.int8)
     q2 = np.ascontiguousarray(q2, np.int8)
@@ -205,8 +237,9 @@ class DeviceLayer:
 
         int4 / int4zp: q uint8 codes, s float32 [E, K/G, N] (exact in ``act``;
         G = K for group_size -1), g int32 or None, int4zp zero points z uint8
-        like s.  int8: q int8 codes, s float32 [E, N].  int8g: q int8 codes,
-        s float32 [E, K/128, N] (exact in ``act``).
+        like s.  int4s24: as int4 without g, codes 2:4 sparse along K.  int8: q
+        int8 codes, s float32 [E, N].  int8g: q int8 codes, s float32
+        [E, K/128, N] (exact in ``act``).
         """
         E, N2, H = q13.shape
         I = N2 // 2
@@ -214,6 +247,8 @@ class DeviceLayer:
         if qt in ("int4", "int4zp"):
             packed = qmoe_pack_int4(E, H, I, act, q13, _scale_bits(s13, act), g13, q2, _scale_bits(s2, act), g2,
                                     gs, z13 if qt == "int4zp" else None, z2 if qt == "int4zp" else None)
+        elif qt == "int4s24":
+            packed = qmoe_pack_int4_24(E, H, I, act, q13, _scale_bits(s13, act), q2, _scale_bits(s2, act), gs)
         elif qt == "int8g":
             packed = qmoe_pack_int8_group(E, H, I, act, q13, _scale_bits(s13, act), q2, _scale_bits(s2, act))
         else:

@@ -31,6 +31,8 @@ SOURCES = [
     "gemm_i4_bf16.cu",
     "gemm_i4z_f16.cu",
     "gemm_i4z_bf16.cu",
+    "gemm_i4s_f16.cu",
+    "gemm_i4s_bf16.cu",
     "gemm_i8.cu",
     "gemm_i8g_f16.cu",
     "gemm_i8g_bf16.cu",

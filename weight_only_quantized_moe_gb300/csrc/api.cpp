@@ -81,6 +81,7 @@ int stage_bytes_of(int32_t qt) {
     case QMOE_INT4_GROUP: return kInt4StageBytes;
     case QMOE_INT4_GROUP_ZP: return kInt4ZpStageBytes;
     case QMOE_INT8_GROUP: return kInt8GroupStageBytes;
+    case QMOE_INT4_GROUP_24: return kInt4SparseStageBytes;
     default: return kInt8StageBytes;
   }
 }
@@ -90,6 +91,7 @@ QuantKind kind_of(int32_t qt) {
     case QMOE_INT4_GROUP: return kQ4;
     case QMOE_INT4_GROUP_ZP: return kQ4Z;
     case QMOE_INT8_GROUP: return kQ8G;
+    case QMOE_INT4_GROUP_24: return kQ4S;
     default: return kQ8;
   }
 }
@@ -103,6 +105,10 @@ qmoe_status validate_layer_dims(const qmoe_layer* L) {
     if (L->group_size != 128 && L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
     if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
     if (L->group_size == -1 && L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
+  } else if (L->qt == QMOE_INT4_GROUP_24) {
+    if (L->group_size != 128 && L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
+    if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
+    if (L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
   } else if (L->qt == QMOE_INT8_GROUP) {
     if (L->group_size != 128) return QMOE_ERR_UNSUPPORTED;
     if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
@@ -517,6 +523,94 @@ void unpack_int4_matrix(const uint8_t* in, bool zp, bool channel_wise, int rows,
     }
 }
 
+// 2:4-sparse int4 tile stage (6400 B): kept codes [half][row][16 B], positions
+// [half][row][8 B], then 128 x 2 B scales.  Half h covers K = 64h .. 64h+63, 16
+// groups of 4 channels.  Word j of a row's 16 code bytes holds groups 4j..4j+3
+// of the half: nibble i <- the first kept code of group 4j+i, nibble i+4 <- the
+// second.  Positions: nibble g (g = 0..15, little-endian over the 8 bytes) is
+// i0 | i1 << 2 for group g, i0 < i1 the kept channels within the group.
+// Per group the kept channels are those with a code other than 8, padded with
+// the lowest remaining channels; more than 2 sets `bad`.
+void pack_int4_24_matrix(const uint8_t* q, const uint16_t* s, bool channel_wise, int rows, int K, int I_for_w13,
+                         uint8_t* out, std::atomic<bool>& bad) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * kInt4SparseStageBytes;
+      const int grp = channel_wise ? 0 : ks;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
+        const uint8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
+        for (int h = 0; h < 2; ++h) {
+          uint8_t v0[16], v1[16];
+          uint64_t pos = 0;
+          for (int g = 0; g < 16; ++g) {
+            const uint8_t* c4 = qrow + 64 * h + 4 * g;
+            int keep[4], n = 0;
+            for (int i = 0; i < 4; ++i) {
+              if (c4[i] > 15) bad = true;
+              if (c4[i] != 8) {
+                if (n == 2) bad = true;
+                else keep[n++] = i;
+              }
+            }
+            for (int i = 0; i < 4 && n < 2; ++i)
+              if (c4[i] == 8 && (n == 0 || keep[0] != i)) keep[n++] = i;
+            if (keep[0] > keep[1]) std::swap(keep[0], keep[1]);
+            v0[g] = c4[keep[0]] & 15;
+            v1[g] = c4[keep[1]] & 15;
+            pos |= static_cast<uint64_t>(keep[0] | (keep[1] << 2)) << (4 * g);
+          }
+          uint8_t* vdst = blk + (h * 128 + r) * 16;
+          for (int j = 0; j < 4; ++j) {
+            uint32_t word = 0;
+            for (int i = 0; i < 4; ++i) {
+              word |= static_cast<uint32_t>(v0[4 * j + i]) << (4 * i);
+              word |= static_cast<uint32_t>(v1[4 * j + i]) << (4 * (i + 4));
+            }
+            for (int b = 0; b < 4; ++b) vdst[4 * j + b] = static_cast<uint8_t>(word >> (8 * b));
+          }
+          uint8_t* pdst = blk + 4096 + (h * 128 + r) * 8;
+          for (int b = 0; b < 8; ++b) pdst[b] = static_cast<uint8_t>(pos >> (8 * b));
+        }
+        const uint16_t sb = s[static_cast<size_t>(grp) * rows + cr];
+        blk[6144 + r * 2] = sb & 0xFF;
+        blk[6144 + r * 2 + 1] = sb >> 8;
+      }
+    }
+}
+
+void unpack_int4_24_matrix(const uint8_t* in, bool channel_wise, int rows, int K, int I_for_w13, uint8_t* q,
+                           uint16_t* s) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * kInt4SparseStageBytes;
+      const int grp = channel_wise ? 0 : ks;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
+        uint8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t* vsrc = blk + (h * 128 + r) * 16;
+          const uint8_t* psrc = blk + 4096 + (h * 128 + r) * 8;
+          uint64_t pos = 0;
+          for (int b = 0; b < 8; ++b) pos |= static_cast<uint64_t>(psrc[b]) << (8 * b);
+          for (int g = 0; g < 16; ++g) {
+            const int j = g / 4, i = g % 4;
+            const uint32_t word = vsrc[4 * j] | (vsrc[4 * j + 1] << 8) | (vsrc[4 * j + 2] << 16) |
+                                  (static_cast<uint32_t>(vsrc[4 * j + 3]) << 24);
+            const int p = static_cast<int>((pos >> (4 * g)) & 15);
+            uint8_t* c4 = qrow + 64 * h + 4 * g;
+            for (int x = 0; x < 4; ++x) c4[x] = 8;
+            c4[p & 3] = (word >> (4 * i)) & 15;
+            c4[p >> 2] = (word >> (4 * (i + 4))) & 15;
+          }
+        }
+        s[static_cast<size_t>(grp) * rows + cr] = static_cast<uint16_t>(blk[6144 + r * 2] | (blk[6144 + r * 2 + 1] << 8));
+      }
+    }
+}
+
 // int8 tile stage: 8 chunks x 128 rows x 16 B; chunk c holds K = 16c..16c+15 in
 // byte order.  With group scales (s [groups][rows], 16-bit) 128 x 2 B scales follow.
 void pack_int8_matrix(const int8_t* q, const uint16_t* s, int rows, int K, int I_for_w13, uint8_t* out,
@@ -603,6 +697,7 @@ size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K,
   if (qt == QMOE_INT4_GROUP_ZP && g128_or_cw) return tiles * kInt4ZpStageBytes;
   if (qt == QMOE_INT8_PER_COL && group_size == -1) return tiles * kInt8StageBytes;
   if (qt == QMOE_INT8_GROUP && group_size == 128) return tiles * kInt8GroupStageBytes;
+  if (qt == QMOE_INT4_GROUP_24 && g128_or_cw) return tiles * kInt4SparseStageBytes;
   return 0;
 }
 
@@ -775,6 +870,45 @@ qmoe_status qmoe_unpack_int8_group(int32_t E, int32_t H, int32_t I, const void* 
                        q13 + static_cast<size_t>(e) * 2 * I * H, s13 + static_cast<size_t>(e) * (H / 128) * 2 * I);
     unpack_int8_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, true, H, I, 0,
                        q2 + static_cast<size_t>(e) * H * I, s2 + static_cast<size_t>(e) * (I / 128) * H);
+  });
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_pack_int4_24(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                              const uint8_t* q13, const uint16_t* s13, const uint8_t* q2, const uint16_t* s2,
+                              void* w13_packed, void* w2_packed) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128 && group_size != -1) return QMOE_ERR_UNSUPPORTED;
+  if (scale_dtype != QMOE_F16 && scale_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed) return QMOE_ERR_INVALID_ARG;
+  const bool cw = group_size == -1;
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT4_GROUP_24, 1, 2 * I, H, group_size);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT4_GROUP_24, 1, H, I, group_size);
+  const size_t ng13 = cw ? 1 : H / 128, ng2 = cw ? 1 : I / 128;
+  std::atomic<bool> bad{false};
+  parallel_for(E, [&](int64_t e) {
+    pack_int4_24_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, s13 + e * ng13 * 2 * I, cw, 2 * I, H, I,
+                        static_cast<uint8_t*>(w13_packed) + e * b13, bad);
+    pack_int4_24_matrix(q2 + static_cast<size_t>(e) * H * I, s2 + e * ng2 * H, cw, H, I, 0,
+                        static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+  });
+  return bad ? QMOE_ERR_INVALID_ARG : QMOE_OK;
+}
+
+qmoe_status qmoe_unpack_int4_24(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                                const void* w2_packed, uint8_t* q13, uint16_t* s13, uint8_t* q2, uint16_t* s2) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128 && group_size != -1) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed) return QMOE_ERR_INVALID_ARG;
+  const bool cw = group_size == -1;
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT4_GROUP_24, 1, 2 * I, H, group_size);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT4_GROUP_24, 1, H, I, group_size);
+  const size_t ng13 = cw ? 1 : H / 128, ng2 = cw ? 1 : I / 128;
+  parallel_for(E, [&](int64_t e) {
+    unpack_int4_24_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, cw, 2 * I, H, I,
+                          q13 + static_cast<size_t>(e) * 2 * I * H, s13 + e * ng13 * 2 * I);
+    unpack_int4_24_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, cw, H, I, 0,
+                          q2 + static_cast<size_t>(e) * H * I, s2 + e * ng2 * H);
   });
   return QMOE_OK;
 }

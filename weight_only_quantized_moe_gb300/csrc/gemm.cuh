@@ -180,6 +180,50 @@ __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t
   }
 }
 
+// 2:4-sparse int4: a row's half (64 K, 16 groups of 4 channels) is 16 bytes of
+// kept codes and 8 bytes of positions.  Word j of the codes holds groups
+// 4j..4j+3 with nibble i the first kept code of group 4j+i and nibble i+4 its
+// second, so the int4 conversion above turns each word into four f16x2 values
+// (first kept, second kept) * s, one per group.  Position nibble g holds
+// i0 | i1 << 2 (the kept channels of group g); a 16-entry table maps it to two
+// byte-permute selectors that place the kept values at K 4g+i0 and 4g+i1 of
+// output columns 2g (K 4g, 4g+1) and 2g+1 (K 4g+2, 4g+3) and zeros elsewhere.
+// Table entry m: byte pair 0x10 picks the first kept value, 0x32 the second,
+// 0x54 a zero (from the permute's second operand).
+__host__ __device__ inline uint32_t sparse24_pair_selector(int m, int p) {
+  const int i0 = m & 3, i1 = m >> 2;
+  return p == i0 ? 0x10u : (p == i1 ? 0x32u : 0x54u);
+}
+
+template <bool BF16S>
+__device__ __forceinline__ void dequant_int4_24_half(const uint4& pk, const uint2& pos, uint32_t sbits,
+                                                     const uint2* sel_tab, uint32_t (&out)[32]) {
+  const uint32_t bias_bits = 0x64086408u;  // 1024 + 8
+  const uint32_t m64z = 0xD480D480u;       // -(64 + 8)
+  uint16_t s16;
+  if (BF16S) {
+    s16 = __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
+  } else {
+    s16 = static_cast<uint16_t>(sbits);
+  }
+  const uint32_t s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
+  const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t r[4];
+    cvt_int4_word_half(w[j], bias_bits, m64z, s2bits, r[0], r[1]);
+    cvt_int4_word_half(w[j] >> 8, bias_bits, m64z, s2bits, r[2], r[3]);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int g = 4 * j + x;
+      const uint32_t m = ((g < 8 ? pos.x : pos.y) >> (4 * (g & 7))) & 15u;
+      const uint2 sel = sel_tab[m];
+      out[2 * g] = __byte_perm(r[x], 0u, sel.x);
+      out[2 * g + 1] = __byte_perm(r[x], 0u, sel.y);
+    }
+  }
+}
+
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
 // conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.  A per-row
 // (per-column of W) scale is applied to the fp32 accumulator in the epilogue;
@@ -309,6 +353,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint64_t* drain = accempty + 2;  // one per MMA issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // 2:4-sparse int4: position -> byte-permute selectors, in the barrier area's last 128 bytes
+  uint2* sel_tab = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(wfull) + kBarrierBytes - 128);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -329,6 +375,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(drain + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if (KIND == kQ4S && threadIdx.x < 16) {
+    const int m = static_cast<int>(threadIdx.x);
+    sel_tab[m] = make_uint2(sparse24_pair_selector(m, 0) | (sparse24_pair_selector(m, 1) << 8),
+                            sparse24_pair_selector(m, 2) | (sparse24_pair_selector(m, 3) << 8));
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -482,6 +533,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
           dequant_int4_half<BF16S>(pk, sbits, zp, out);
+        } else if (KIND == kQ4S) {
+          const uint4 pk = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 16);
+          const uint2 pos = *reinterpret_cast<const uint2*>(wst + 4096 + (half * 128 + row) * 8);
+          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 6144 + row * 2);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+          dequant_int4_24_half<BF16S>(pk, pos, sbits, sel_tab, out);
         } else {
           uint4 pk[4];
 #pragma unroll

@@ -15,9 +15,11 @@ constexpr int kInt4StageBytes = 8448; // 128 rows x 128 K x 4 bit + 128 scales x
 constexpr int kInt8StageBytes = 16384;
 constexpr int kInt4ZpStageBytes = 8576;   // int4 block + 128 zero-point bytes
 constexpr int kInt8GroupStageBytes = 16640;  // int8 block + 128 x 2 B scales
+// 2:4-sparse int4: 128 rows x 64 kept codes (4 KB), their 2-bit positions (2 KB), 128 x 2 B scales
+constexpr int kInt4SparseStageBytes = 6400;
 
 // Weight formats of the GEMM kernel (template parameter).
-enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3 };
+enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3, kQ4S = 4 };
 constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
 constexpr int kMaxTokenTile = 128;
 
