@@ -279,3 +279,42 @@ def test_pack_int4_24_rejects_three_of_four():
         q.qmoe_pack_int4_24(1, 128, 128, "f16", L.q13, s13b, q2, s2b)
     assert ei.value.status == q.QMOE_ERR_INVALID_ARG
     assert q.packed_bytes("int4s24", 1, 256, 128) == 2 * 6400
+
+
+def test_pack_int4_24_sparse_corner_groups():
+    """Groups with 0 or 1 codes other than 8 (padded with the lowest free channels)
+    and every kept-position pair round-trip exactly; channel-wise scales repeat."""
+    wl = Workload("s24c", 1, 2, 256, 128, "int4s24", -1, "f16", False, 0.0, (1,))
+    L = make_layer(wl, seed=12)
+    s13b, s2b = to_u16_bits(L.s13, "f16"), to_u16_bits(L.s2, "f16")
+    q2 = np.full_like(L.q2, 8)
+    pairs = [(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)]
+    for r in range(q2.shape[1]):
+        for g in range(q2.shape[2] // 4):
+            kind = (r + g) % 9
+            base = 4 * g
+            if kind < 6:
+                i0, i1 = pairs[kind]
+                q2[0, r, base + i0] = (r + g) % 16 if (r + g) % 16 != 8 else 1
+                q2[0, r, base + i1] = (3 * r + g) % 16 if (3 * r + g) % 16 != 8 else 2
+            elif kind < 8:
+                q2[0, r, base + (r + kind) % 4] = 15   # one code only
+            # kind == 8: the whole group is zero
+    pk = q.qmoe_pack_int4_24(1, 256, 128, "f16", L.q13, s13b, q2, s2b, -1)
+    q13, s13, q2b, s2 = q.qmoe_unpack_int4_24(1, 256, 128, pk["w13"], pk["w2"], -1)
+    assert np.array_equal(q2b, q2) and np.array_equal(q13, L.q13)
+    assert np.array_equal(s2, s2b) and np.array_equal(s13, s13b)
+    # channel-wise: both 128-K blocks of a W13 tile (K = H = 256) carry the rows' one scale
+    blk = pk["w13"].reshape(-1, 6400)
+    assert np.array_equal(blk[0, 6144:6400], blk[1, 6144:6400])
+    assert not np.array_equal(blk[0, 6144:6400], blk[2, 6144:6400])
+
+
+def test_packed_bytes_per_format():
+    tiles = 3 * (256 // 128) * (384 // 128)
+    for qt, gs, per in [("int4", 128, 8448), ("int4", -1, 8448), ("int4zp", 128, 8576), ("int4s24", 128, 6400),
+                        ("int4s24", -1, 6400), ("int8", -1, 16384), ("int8g", 128, 16640)]:
+        assert q.packed_bytes(qt, 3, 256, 384, gs) == tiles * per
+    for qt, gs in [("int4", 64), ("int4s24", 256), ("int8", 128), ("int8g", -1)]:
+        assert q.packed_bytes(qt, 3, 256, 384, gs) == 0
+    assert q.packed_bytes("int4s24", 3, 200, 384, 128) == 0
