@@ -298,6 +298,33 @@ size_t qmoe_workspace_size(const qmoe_layer* layer, int64_t M, int32_t top_k);
 size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts);
 
 /*
+ * The launch plan qmoe_forward_ex would use (host only; no device access when
+ * num_sms > 0).  Fields: token_tile (token rows per GEMM work item), issuers
+ * (MMA-issuing threads per CTA), acc_bufs (TMEM accumulators per issuer),
+ * split1 / split2 (split-K of the gate/up and down GEMMs), w_stages (packed-
+ * weight ring depth), ab_stages (token-tile / TMEM A ring depth), stage_bytes
+ * (packed bytes per 128 x 128 block), workspace_bytes.  num_sms: the GPU's
+ * SM count the plan is sized for (0: the current device's).  Errors as
+ * qmoe_workspace_size_ex (QMOE_ERR_INVALID_ARG / QMOE_ERR_UNSUPPORTED), and
+ * QMOE_ERR_INVALID_ARG for a null info pointer or num_sms < 0.
+ */
+typedef struct {
+  int32_t token_tile;
+  int32_t issuers;
+  int32_t acc_bufs;
+  int32_t split1;
+  int32_t split2;
+  int32_t w_stages;
+  int32_t ab_stages;
+  int32_t stage_bytes;
+  int64_t workspace_bytes;
+  int32_t reserved[6];
+} qmoe_plan_info;
+
+qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts,
+                               int32_t num_sms, qmoe_plan_info* info);
+
+/*
  * out[M, H] (act_dtype, overwritten) = the layer applied to x[M, H] (act_dtype)
  * with routing topk_ids int32 [M, top_k] and topk_weights float32 [M, top_k].
  * All buffers are device memory; x, out and the workspace 256-byte aligned.

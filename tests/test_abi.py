@@ -318,3 +318,59 @@ def test_packed_bytes_per_format():
     for qt, gs in [("int4", 64), ("int4s24", 256), ("int8", 128), ("int8g", -1)]:
         assert q.packed_bytes(qt, 3, 256, 384, gs) == 0
     assert q.packed_bytes("int4s24", 3, 200, 384, 128) == 0
+
+
+def _plan(layer_kw, M, k=2, sms=152, **opts):
+    return q.qmoe_describe_plan(_layer_struct(**layer_kw), M, k, q.make_options(**opts) if opts else None, sms)
+
+
+MIXTRAL = dict(E=8, H=4096, I=14336, group_size=128, qt=N.QMOE_INT4_GROUP)
+
+
+@pytest.mark.parametrize("M,T,ni,s2", [(1, 16, 3, 2), (4, 16, 3, 3), (16, 16, 3, 4), (32, 16, 3, 4), (64, 32, 3, 4),
+                                       (128, 64, 2, 4), (256, 128, 1, 1), (2048, 128, 1, 1)])
+def test_plan_token_tile_issuers_and_split(M, T, ni, s2):
+    """Token tile: the power of two >= 1.5 x mean pairs per expert (16..128); issuers 3 / 2 / 1 by tile;
+    down-GEMM split as fitted on GB300 for the Mixtral-8x7B shape."""
+    p = _plan(MIXTRAL, M)
+    assert (p["token_tile"], p["issuers"], p["split2"]) == (T, ni, s2)
+    assert p["split1"] == 1 and p["stage_bytes"] == 8448
+    assert p["workspace_bytes"] == L_ws(MIXTRAL, M)
+
+
+def L_ws(kw, M):
+    return q.lib().qmoe_workspace_size(ctypes.byref(_layer_struct(**kw)), M, 2)
+
+
+def test_plan_rings_and_tmem_constraints():
+    """Every plan keeps the ring rules the kernel relies on: even weight ring, A ring a multiple of
+    lcm(2, issuers), TMEM columns (accumulators + 64-column A slots) within 512, shared memory within
+    227 KB."""
+    for qt, gs, per in [(N.QMOE_INT4_GROUP, 128, 8448), (N.QMOE_INT4_GROUP_24, 128, 6400),
+                        (N.QMOE_INT8_PER_COL, -1, 16384), (N.QMOE_INT8_GROUP, 128, 16640)]:
+        sdt = N.QMOE_F32 if qt == N.QMOE_INT8_PER_COL else N.QMOE_F16
+        for M in (1, 16, 64, 128, 512, 4096):
+            for ni in (0, 1, 2, 3):
+                try:
+                    p = _plan(dict(E=8, H=4096, I=14336, group_size=gs, qt=qt, scale_dtype=sdt), M, issuers=ni)
+                except q.QmoeError:
+                    assert ni != 0          # the automatic choice always has a plan
+                    continue
+                T, NI = p["token_tile"], p["issuers"]
+                mult = 6 if NI == 3 else 2
+                assert p["w_stages"] % 2 == 0 and p["w_stages"] >= 2
+                assert p["ab_stages"] % mult == 0 and p["ab_stages"] >= mult
+                assert NI * p["acc_bufs"] * T + 64 * p["ab_stages"] <= 512
+                wslot = (per + 1023) // 1024 * 1024
+                assert 1024 + p["w_stages"] * wslot + p["ab_stages"] * T * 256 + 1024 <= 232448
+                assert p["stage_bytes"] == per
+
+
+def test_plan_overrides_and_other_workloads():
+    p = _plan(MIXTRAL, 16, split1=3, split2=5, token_tile=48, issuers=2)
+    assert (p["split1"], p["split2"], p["token_tile"], p["issuers"]) == (3, 5, 48, 2)
+    ds = dict(E=160, H=5120, I=1536, group_size=-1, qt=N.QMOE_INT8_PER_COL, scale_dtype=N.QMOE_F32)
+    assert _plan(ds, 1024, k=6)["token_tile"] == 64      # 6144 pairs over 160 experts
+    assert _plan(ds, 1, k=6)["token_tile"] == 16
+    with pytest.raises(q.QmoeError):
+        q.qmoe_describe_plan(_layer_struct(**MIXTRAL), 16, 2, None, -1)

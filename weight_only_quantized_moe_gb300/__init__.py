@@ -43,5 +43,6 @@ from .api import (  # noqa: F401
     qmoe_workspace_size_logits,
     qmoe_unpack_int8,
     qmoe_workspace_size,
+    qmoe_describe_plan,
     qmoe_workspace_size_host,
 )

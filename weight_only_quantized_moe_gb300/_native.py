@@ -41,6 +41,12 @@ class QmoeLayer(ctypes.Structure):
     ]
 
 
+class QmoePlanInfo(ctypes.Structure):
+    _fields_ = [("token_tile", c_int32), ("issuers", c_int32), ("acc_bufs", c_int32), ("split1", c_int32),
+                ("split2", c_int32), ("w_stages", c_int32), ("ab_stages", c_int32), ("stage_bytes", c_int32),
+                ("workspace_bytes", c_int64), ("reserved", c_int32 * 6)]
+
+
 class QmoeOptions(ctypes.Structure):
     _fields_ = [("split1", c_int32), ("split2", c_int32), ("token_tile", c_int32), ("fault_injection", c_int32),
                 ("issuers", c_int32), ("reserved", c_int32 * 3)]
@@ -89,6 +95,8 @@ _SIGS = {
                                  c_int64, c_void_p]),
     "qmoe_workspace_size": (c_size_t, [POINTER(QmoeLayer), c_int64, c_int32]),
     "qmoe_workspace_size_ex": (c_size_t, [POINTER(QmoeLayer), c_int64, c_int32, POINTER(QmoeOptions)]),
+    "qmoe_describe_plan": (c_int32, [POINTER(QmoeLayer), c_int64, c_int32, POINTER(QmoeOptions), c_int32,
+                                     POINTER(QmoePlanInfo)]),
     "qmoe_forward": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_void_p, c_int32, c_void_p,
                                c_void_p, c_size_t, c_void_p]),
     "qmoe_forward_ex": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_void_p, c_int32, c_void_p,

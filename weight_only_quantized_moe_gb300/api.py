@@ -290,6 +290,17 @@ def qmoe_workspace_size(layer: DeviceLayer, M: int, k: int, opts=None) -> int:
     return int(n)
 
 
+def qmoe_describe_plan(layer, M: int, k: int, opts=None, num_sms: int = 0) -> dict:
+    """The launch plan of a forward (token tile, issuers, splits, ring depths,
+    workspace bytes) for a DeviceLayer or a raw QmoeLayer struct; host only
+    when num_sms > 0."""
+    struct = layer.struct if hasattr(layer, "struct") else layer
+    info = N.QmoePlanInfo()
+    st = N.lib().qmoe_describe_plan(byref(struct), M, k, None if opts is None else byref(opts), num_sms, byref(info))
+    N.check(st, "qmoe_describe_plan")
+    return {f: getattr(info, f) for f, _ in N.QmoePlanInfo._fields_ if f != "reserved"}
+
+
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 

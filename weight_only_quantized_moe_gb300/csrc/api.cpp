@@ -943,6 +943,25 @@ size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k,
   return pl.total;
 }
 
+qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts,
+                               int32_t num_sms, qmoe_plan_info* info) {
+  if (info == nullptr || num_sms < 0) return QMOE_ERR_INVALID_ARG;
+  Plan pl;
+  const qmoe_status st = make_plan(layer, M, top_k, opts, num_sms > 0 ? num_sms : current_sm_count(), &pl);
+  if (st != QMOE_OK) return st;
+  *info = qmoe_plan_info{};
+  info->token_tile = pl.T;
+  info->issuers = pl.issuers;
+  info->acc_bufs = pl.acc_bufs;
+  info->split1 = pl.S1;
+  info->split2 = pl.S2;
+  info->w_stages = pl.w_stages;
+  info->ab_stages = pl.ab_stages;
+  info->stage_bytes = pl.stage_bytes;
+  info->workspace_bytes = static_cast<int64_t>(pl.total);
+  return QMOE_OK;
+}
+
 size_t qmoe_workspace_size(const qmoe_layer* layer, int64_t M, int32_t top_k) {
   return qmoe_workspace_size_ex(layer, M, top_k, nullptr);
 }
