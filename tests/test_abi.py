@@ -2,6 +2,7 @@
 function include/qmoe.h declares, packs weights in the documented layout with
 a bit-exact round trip, and rejects bad arguments before touching a device."""
 import ctypes
+import os
 import re
 
 import numpy as np
@@ -374,3 +375,23 @@ def test_plan_overrides_and_other_workloads():
     assert _plan(ds, 1, k=6)["token_tile"] == 16
     with pytest.raises(q.QmoeError):
         q.qmoe_describe_plan(_layer_struct(**MIXTRAL), 16, 2, None, -1)
+
+
+def test_header_is_plain_c99(tmp_path):
+    """include/qmoe.h compiles as strict C99 (no C++ or torch types in the ABI), and its structs
+    have the sizes the binding declares."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = tmp_path / "h.c"
+    src.write_text('#include "qmoe.h"\n'
+                   "typedef char a[sizeof(qmoe_options) == %d ? 1 : -1];\n"
+                   "typedef char b[sizeof(qmoe_plan_info) == %d ? 1 : -1];\n"
+                   "typedef char c[sizeof(qmoe_layer) == %d ? 1 : -1];\n"
+                   % (ctypes.sizeof(N.QmoeOptions), ctypes.sizeof(N.QmoePlanInfo), ctypes.sizeof(N.QmoeLayer)))
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src), "-o",
+                        str(tmp_path / "h.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
