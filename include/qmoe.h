@@ -42,8 +42,9 @@
  *   - Faults the host cannot see (a top-k id outside [0, E), a kernel wait that
  *     ran past its time limit) are recorded in the workspace and read back with
  *     qmoe_read_device_status.
- *   - The library is stateless apart from per-device caches of the SM count and
- *     the driver's tensor-map entry point; calls are thread-safe.
+ *   - The library is stateless apart from a per-device cache of the SM count
+ *     (and, for qmoe_forward_noalloc, of its scratch array's address); calls
+ *     are thread-safe.
  */
 #ifndef QMOE_H_
 #define QMOE_H_
@@ -293,7 +294,14 @@ qmoe_status qmoe_moe_align(const int32_t* topk_ids, int64_t M, int32_t top_k, in
 /* Forward                                                                   */
 /* ------------------------------------------------------------------------ */
 
-/* Workspace bytes qmoe_forward needs for this layer, M and top_k (0 on invalid input). */
+/*
+ * Workspace bytes qmoe_forward needs for this layer, M and top_k (0 on invalid
+ * input).  The batch size M is an explicit argument of every sizing and launch
+ * call ("[WIP] AWQ Faster Kernels", discussion: the kernel choice depends on
+ * the number of tokens, which must reach the kernel chooser).  The workspace
+ * holds the moe_align output ("Marlin moe integration", review thread), the
+ * gathered activations, the intermediate and the split-K partial sums.
+ */
 size_t qmoe_workspace_size(const qmoe_layer* layer, int64_t M, int32_t top_k);
 size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts);
 
@@ -325,6 +333,12 @@ qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k
                                int32_t num_sms, qmoe_plan_info* info);
 
 /*
+ * The fused MoE layer ("Marlin moe integration", description and review
+ * thread: the hot-path call takes the activations, the already-quantized
+ * expert weights and scales, and the router's top-k ids and weights, and runs
+ * the grouped expert GEMMs; "[Kernel] W8A16 Int8 inside FusedMoE",
+ * description: the int8 weights are cast to FP16/BF16 inside the kernel
+ * before the matmul).
  * out[M, H] (act_dtype, overwritten) = the layer applied to x[M, H] (act_dtype)
  * with routing topk_ids int32 [M, top_k] and topk_weights float32 [M, top_k].
  * All buffers are device memory; x, out and the workspace 256-byte aligned.
@@ -392,11 +406,19 @@ qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64
  *     them on the GPU.  The array keeps the last call's contents; the forward
  *     needs none of it cleared.
  *   - Device-side faults (a bad expert id, a kernel wait timeout) are recorded
- *     in the shared array and are not reported by this entry point.
+ *     in the shared array; qmoe_read_noalloc_status reads them back.
+ *   - Invalid arguments give the same status as qmoe_forward, also at M == 0.
  */
 qmoe_status qmoe_forward_noalloc(const qmoe_layer* layer, const void* x, int64_t M,
                                  const int32_t* topk_ids, const float* topk_weights, int32_t top_k,
                                  void* out, void* stream);
+
+/*
+ * Synchronise `stream` and return the first device-side fault recorded by the
+ * most recent qmoe_forward_noalloc on the current device (QMOE_OK if none, or
+ * if none has run).  Like that entry point it has no counterpart on the pages.
+ */
+qmoe_status qmoe_read_noalloc_status(void* stream);
 
 /*
  * Router, the step before the layer (the pages take its output, the top-k

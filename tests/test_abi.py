@@ -151,6 +151,14 @@ def test_workspace_size_and_validation_are_host_only():
     assert st == q.QMOE_ERR_UNSUPPORTED
     st = L.qmoe_forward(ctypes.byref(ok), None, 4, None, None, 2, None, None, 0, None)
     assert st == q.QMOE_ERR_WORKSPACE
+    # the no-allocation forward reports an invalid layer or size exactly as qmoe_forward
+    # does, before any device access, also at M == 0
+    for bad, M, k in ((_layer_struct(H=200), 0, 2), (_layer_struct(E=0), 0, 2), (_layer_struct(group_size=64), 0, 2),
+                      (_layer_struct(qt=99), 0, 2), (ok, 0, 9), (_layer_struct(H=200), 4, 2), (ok, -1, 2)):
+        want = L.qmoe_forward(ctypes.byref(bad), None, M, None, None, k, None, None, 0, None)
+        got = L.qmoe_forward_noalloc(ctypes.byref(bad), None, M, None, None, k, None, None)
+        assert want != q.QMOE_OK and got == want, (M, k, want, got)
+    assert L.qmoe_forward_noalloc(None, None, 0, None, None, 2, None, None) == q.QMOE_ERR_INVALID_ARG
     # moe_align argument checks
     assert L.qmoe_moe_align(None, 4, 2, 8, 16, None, None, None, 1000, None) == q.QMOE_ERR_INVALID_ARG
     assert L.qmoe_moe_align(None, 4, 2, 8, 0, None, None, None, 1000, None) == q.QMOE_ERR_INVALID_ARG

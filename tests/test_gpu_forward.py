@@ -4,6 +4,8 @@ Shapes are small enough for the oracle to finish in seconds yet span several
 128-row weight tiles, several 128-wide K stages, ragged token chunks, split-K
 and multi-chunk experts.
 """
+import copy
+
 import numpy as np
 import pytest
 import torch
@@ -124,6 +126,29 @@ def test_activation_magnitudes(qt, act, ao, exps, spread):
         assert np.isfinite(got).all()
         for m in range(M):
             assert_parity(got[m:m + 1], ref[m:m + 1], f"{wl.name} 2^{ex} row {m}")
+
+
+def test_bf16_rows_near_the_top_of_the_range():
+    """bf16 rows whose largest magnitude is ~2^118 (bf16 reaches 2^128): the
+    power-of-two row scaling must bring them into f16 range.  Per-column int8
+    applies its fp32 scale to the accumulator, so W13 scales of ~2^-123 keep
+    the layer's values finite: h = 16 * (x . W)."""
+    wl = _wl("int8", "bf16")
+    L0, _ = _layer(wl)
+    L = copy.copy(L0)
+    L.s13 = (L0.s13.astype(np.float64) * 2.0 ** -112).astype(np.float32)
+    dl = device_layer(L)
+    M = 24
+    base = make_inputs(wl, M, seed=41)
+    x = round_to(np.ldexp(base.x.astype(np.float64), 116), "bf16").astype(np.float32)
+    inp = Inputs(x, base.topk_ids, base.topk_weights, base.logits)
+    xd, ids, w = device_inputs(wl, inp)
+    out, _ = run_forward(dl, xd, ids, w)
+    got = out.float().cpu().numpy()
+    ref = oracle.moe_forward(L, inp.x, inp.topk_ids, inp.topk_weights)
+    assert np.isfinite(got).all()
+    for m in range(M):
+        assert_parity(got[m:m + 1], ref[m:m + 1], f"bf16 2^116 row {m}")
 
 
 def test_multi_chunk_expert_and_empty_experts():

@@ -29,6 +29,7 @@ from .api import (  # noqa: F401
     qmoe_forward_host,
     qmoe_forward_logits,
     qmoe_forward_noalloc,
+    qmoe_read_noalloc_status,
     qmoe_forward_profiled,
     qmoe_moe_align,
     qmoe_pack_int4,

@@ -115,6 +115,7 @@ _SIGS = {
                                       c_void_p, c_void_p, c_size_t, c_void_p]),
     "qmoe_forward_noalloc": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_void_p, c_int32,
                                        c_void_p, c_void_p]),
+    "qmoe_read_noalloc_status": (c_int32, [c_void_p]),
 }
 
 

@@ -383,6 +383,11 @@ def qmoe_forward_noalloc(layer: DeviceLayer, x: torch.Tensor, topk_ids: torch.Te
     return out
 
 
+def qmoe_read_noalloc_status(stream=None) -> int:
+    """Device-side fault recorded by the last qmoe_forward_noalloc on the current device."""
+    return int(N.lib().qmoe_read_noalloc_status(_stream_ptr(stream)))
+
+
 _LOGIT_DT = {torch.float32: N.QMOE_F32, torch.float16: N.QMOE_F16, torch.bfloat16: N.QMOE_BF16}
 
 

@@ -178,8 +178,10 @@ cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
 // Returns (2^e, 2^-e) for a row whose largest magnitude is amax.
 __device__ __forceinline__ float2 row_exponent_scale(float amax) {
   if (!(amax > 0.0f) || !(amax <= 3.4028235e38f)) return make_float2(1.0f, 1.0f);  // zero, inf or NaN
+  // e in [-126, 126] keeps both 2^e and 2^-e normal fp32 numbers; then every
+  // row with a normal largest magnitude above 2^-112 lands in [2^14, 2^15)
   int e = ((__float_as_int(amax) >> 23) & 0xFF) - 127 - 14;
-  e = max(-100, min(100, e));
+  e = max(-126, min(126, e));
   // both powers of two built from their exponent fields
   return make_float2(__int_as_float((127 + e) << 23), __int_as_float((127 - e) << 23));
 }

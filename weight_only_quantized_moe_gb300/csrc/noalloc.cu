@@ -54,9 +54,11 @@ extern "C" qmoe_status qmoe_forward_noalloc(const qmoe_layer* layer, const void*
                                             void* out, void* stream) {
   const size_t need = qmoe_workspace_size(layer, M, top_k);
   if (need == 0) {
-    // invalid layer or sizes; M == 0 is a valid no-op
-    if (M == 0 && layer != nullptr) return QMOE_OK;
-    return QMOE_ERR_INVALID_ARG;
+    // the layer or the sizes are invalid: the regular forward's validation
+    // names the reason (it fails before it looks at the workspace)
+    const qmoe_status st = qmoe::forward_into_workspace(layer, x, M, topk_ids, topk_weights, top_k, out, nullptr, 0,
+                                                        static_cast<cudaStream_t>(stream));
+    return st != QMOE_OK ? st : QMOE_ERR_INVALID_ARG;
   }
   if (need > kNoAllocScratchBytes) return QMOE_ERR_WORKSPACE;
   qmoe_status st;
@@ -64,4 +66,13 @@ extern "C" qmoe_status qmoe_forward_noalloc(const qmoe_layer* layer, const void*
   if (scratch == nullptr) return st;
   return qmoe::forward_into_workspace(layer, x, M, topk_ids, topk_weights, top_k, out, scratch,
                                       kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" qmoe_status qmoe_read_noalloc_status(void* stream) {
+  qmoe_status st;
+  void* scratch = scratch_on_current_device(&st);
+  if (scratch == nullptr) return st;
+  // the status word sits at the start of the workspace, where the forward's
+  // first kernel clears it
+  return qmoe_read_device_status(scratch, stream);
 }

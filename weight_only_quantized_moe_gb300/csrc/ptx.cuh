@@ -1,5 +1,5 @@
-// ptx.cuh - inline-PTX wrappers for sm_103a: mbarriers, bulk/tensor TMA copies
-// and the tcgen05 tensor-core / tensor-memory instructions.
+// ptx.cuh - inline-PTX wrappers for sm_103a: mbarriers, 1-D bulk TMA copies
+// (cp.async.bulk) and the tcgen05 tensor-core / tensor-memory instructions.
 //
 // Every wait on an mbarrier here is bounded: it gives up after a time limit
 // (measured with %globaltimer) or as soon as the CTA-wide abort flag is set,
