@@ -7,7 +7,14 @@ of M tokens of a synthetic workload shaped like the pages' models.  Prints ONE
 JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--M M] [--no-sweep]
+                    [--workload NAME] [--M M] [--no-sweep] [--workloads A,B]
+
+The headline (value, e2e, roofline, clocks) is --workload at --M over exactly K
+timed steps.  The same line's "workloads" list then reports every workload at
+every batch size it is measured at (Mixtral-8x7B int4 decode, act-order, int8,
+the DeepSeek-V2-like layer, Mixtral-8x22B prefill, 2:4-sparse int4), each over
+at least K steps and at least 0.3 s of timed work, with its own per-kernel
+times, roofline and clock record.
 
 --impl reference times the CPU oracle (float64 numpy) on a bounded sample of
 the same workload; it is the only other place this file runs the oracle.
@@ -47,18 +54,23 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--M", type=int, default=None)
-    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="headline workload only")
+    ap.add_argument("--workloads", type=lambda v: v.split(","), default=None,
+                    help="comma-separated subset of the reported workloads")
     ap.add_argument("--cpu-sample-s", type=float, default=20.0)
     return ap.parse_args()
 
 
 def peaks():
+    """HBM copy bandwidth (GB/s) and dense bf16 tensor rate (TFLOP/s, burst and
+    sustained) measured on this GPU pool, else the recipe's fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
-    return 6800.0, 1900.0, 1700.0, "fallback"
+        return {"hbm": float(d["hbm_gbs"]), "tc_burst": float(d["bf16_tflops"]),
+                "tc_sust": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    return {"hbm": 6800.0, "tc_burst": 1900.0, "tc_sust": 1700.0, "src": "fallback"}
 
 
 def workload_config(wl, M, extra=None):
@@ -117,7 +129,7 @@ def cpu_cores():
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    """Samples the SM clock and the clock-event reasons of one GPU every ~2 ms
+    """Samples the SM clock and the clock-event reasons of one GPU every ~0.5 ms
     while the timed region runs (NVML through ctypes; read-only queries)."""
     SM = 1  # NVML_CLOCK_SM
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
@@ -158,7 +170,7 @@ class ClockSampler:
             if (self.nvml.nvmlDeviceGetClockInfo(self.handle, self.SM, ctypes.byref(c)) == 0 and
                     self.reasons_fn(self.handle, ctypes.byref(r)) == 0):
                 self.rows.append((float(c.value), int(r.value)))
-            time.sleep(0.002)
+            time.sleep(0.0005)
 
     def __enter__(self):
         import threading
@@ -191,22 +203,21 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-# GPU arm
+# work per call and rooflines (host arithmetic)
 # ----------------------------------------------------------------------------
-def algorithmic_bytes(wl, dl, inp):
+def algorithmic_bytes(wl, expert_w13_bytes, expert_w2_bytes, topk_ids, M):
     """Bytes the method must move per layer call: the touched experts' packed
-    weights and scales, x in, intermediate write + read, out."""
-    d = len(np.unique(inp.topk_ids))
-    M = inp.x.shape[0]
+    weights and scales, x in, intermediate write + read, out.  Per GEMM launch:
+    gate/up = touched W13 + gathered tokens read + intermediate written;
+    down = touched W2 + intermediate read + per-pair fp32 outputs written."""
+    d = int(len(np.unique(topk_ids)))
     P = M * wl.k
-    per_expert_w13 = dl.w13.numel() // wl.E + (2 * wl.I * 4 if wl.qt == "int8" else 0)
-    per_expert_w2 = dl.w2.numel() // wl.E + (wl.H * 4 if wl.qt == "int8" else 0)
     act = 2
-    gemm1 = d * per_expert_w13 + P * wl.H * act + P * wl.I * act
-    gemm2 = d * per_expert_w2 + P * wl.I * act + P * wl.H * 4
-    total = d * (per_expert_w13 + per_expert_w2) + M * wl.H * act * 2 + 2 * P * wl.I * act
+    gemm1 = d * expert_w13_bytes + P * wl.H * act + P * wl.I * act
+    gemm2 = d * expert_w2_bytes + P * wl.I * act + P * wl.H * 4
+    total = d * (expert_w13_bytes + expert_w2_bytes) + M * wl.H * act * 2 + 2 * P * wl.I * act
     return {"distinct_experts": d, "gemm_gate_up": gemm1, "gemm_down": gemm2, "layer": total,
-            "weights": d * (per_expert_w13 + per_expert_w2)}
+            "weights": d * (expert_w13_bytes + expert_w2_bytes)}
 
 
 def kernel_source_hash():
@@ -233,6 +244,176 @@ def recorded_traffic(workload, M, kernel):
     return None
 
 
+def gemm_flops(wl, M, kernel):
+    P = M * wl.k
+    return 2.0 * P * (2 * wl.I if kernel == "gemm_gate_up" else wl.I) * wl.H
+
+
+def roofline_entry(wl, M, ms, kernel_ms, by, pk):
+    """Roofline of one (workload, M): the dominant GEMM launch against its binding
+    peak (HBM or tensor, by its arithmetic intensity against the peaks' ratio),
+    and the whole layer against both peaks."""
+    hbm, tc_burst, tc_sust = pk["hbm"], pk["tc_burst"], pk["tc_sust"]
+    dominant = max(("gemm_gate_up", "gemm_down"), key=lambda n: kernel_ms[n])
+    kflops = gemm_flops(wl, M, dominant)
+    ks = kernel_ms[dominant] * 1e-3
+    if kflops / by[dominant] > tc_burst * 1e12 / (hbm * 1e9):
+        ach = kflops / ks / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tc_burst, "unit": "TFLOP/s", "frac": ach / tc_burst,
+                "frac_of_sustained_peak": ach / tc_sust,
+                "peak_source": f"{pk['src']} bf16_tflops burst (cuBLAS bf16 GEMM; the f16 MMAs run at the bf16 rate)",
+                "algorithmic_flops_per_launch": kflops}
+    else:
+        ach = by[dominant] / ks / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"{pk['src']} hbm_gbs (copy bandwidth)",
+                "algorithmic_bytes_per_launch": by[dominant]}
+    roof["kernel"] = dominant
+    roof["kernel_ms"] = kernel_ms[dominant]
+    t = ms * 1e-3
+    flops = wl.flops(M)
+    layer = {"tokens_per_s": M / t, "tflops": flops / t / 1e12, "weight_gbs": by["weights"] / t / 1e9,
+             "frac_hbm_weights": by["weights"] / t / 1e9 / hbm, "frac_hbm_layer": by["layer"] / t / 1e9 / hbm,
+             "frac_tensor_layer": flops / t / 1e12 / tc_burst,
+             "binding": "tensor" if flops / by["layer"] > tc_burst * 1e12 / (hbm * 1e9) else "hbm"}
+    layer["frac_binding"] = layer["frac_tensor_layer"] if layer["binding"] == "tensor" else layer["frac_hbm_layer"]
+    return roof, layer
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+# every (workload, M) the layer is reported at, besides the headline
+REPORTED = (("mixtral8x7b_w4", (1, 4, 8, 16, 64)), ("mixtral8x7b_w4_actorder", (1, 16, 128, 512)),
+            ("mixtral8x7b_w8", (1, 16, 128, 512)), ("deepseekv2_w8", (1, 32, 256, 1024)),
+            ("mixtral8x22b_w4", (2048, 4096, 8192)), ("mixtral8x7b_w4s24", (1, 16, 64)))
+MIN_TIMED_S = 0.3      # timed region per reported entry (clock samples every ~0.5 ms)
+MAX_ROTATION_BYTES = 24 << 30
+
+
+class GpuWorkload:
+    """One workload's packed layer on the device, rotated across copies so that
+    no step finds its experts' weights in L2."""
+
+    def __init__(self, q, wl, dev):
+        import torch
+        self.q, self.wl, self.dev = q, wl, dev
+        layer = make_layer(wl, seed=0)
+        self.base = q.DeviceLayer.from_canonical(wl.qt, wl.act, layer.q13, layer.s13, layer.q2, layer.s2, layer.g13,
+                                                 layer.g2, device=dev, z13=layer.z13, z2=layer.z2,
+                                                 group_size=wl.group_size)
+        del layer
+        b = self.base
+        self.w13_e = b.w13.numel() // wl.E + (2 * wl.I * 4 if wl.qt == "int8" else 0)
+        self.w2_e = b.w2.numel() // wl.E + (wl.H * 4 if wl.qt == "int8" else 0)
+        self.copies = [b]
+        self.torch = torch
+
+    def ensure_copies(self, touched_bytes):
+        """Enough copies that one lap of the rotation touches 3x the L2 size."""
+        b = self.base
+        want = min(8, math.ceil(3 * L2_BYTES / max(1, touched_bytes)) + 1)
+        want = max(1, min(want, MAX_ROTATION_BYTES // max(1, b.weight_bytes())))
+        while len(self.copies) < want:
+            c = lambda t: None if t is None else t.clone()
+            self.copies.append(self.q.DeviceLayer(b.qt, b.E, b.H, b.I, b.act, b.w13.clone(), b.w2.clone(), c(b.s13),
+                                                  c(b.s2), c(b.perm13), b.group_size))
+        return len(self.copies)
+
+    def inputs(self, M):
+        torch = self.torch
+        inp = make_inputs(self.wl, M, seed=0)
+        x = torch.from_numpy(inp.x).to(self.base.torch_dtype).to(self.dev)
+        ids = torch.from_numpy(inp.topk_ids).to(self.dev)
+        w = torch.from_numpy(inp.topk_weights).to(self.dev)
+        return inp, x, ids, w
+
+    def measure(self, M, steps, warmup, world=1, min_s=0.0):
+        """Time `steps` forwards (more when min_s asks for a longer timed region),
+        then the same number again with CUDA events around each kernel launch."""
+        torch, q, wl = self.torch, self.q, self.wl
+        inp, x, ids, w = self.inputs(M)
+        by = algorithmic_bytes(wl, self.w13_e, self.w2_e, inp.topk_ids, M)
+        ncop = self.ensure_copies(by["weights"])
+        out = torch.empty_like(x)
+        ws = q.alloc_workspace(q.qmoe_workspace_size(self.base, M, wl.k), self.dev)
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(warmup):
+            q.qmoe_forward(self.copies[i % ncop], x, ids, w, out=out, workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st = q.qmoe_read_device_status(ws)
+        if st != q.QMOE_OK:
+            raise RuntimeError(f"{wl.name} M={M}: device status after warm-up: {q.status_string(st)}")
+        if min_s > 0 and warmup > 0:
+            est = e0.elapsed_time(e1) / warmup * 1e-3
+            steps = int(min(4000, max(steps, math.ceil(min_s / max(est, 1e-6)))))
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(self.dev.index) as clk:
+            e0.record(stream)
+            for i in range(steps):
+                q.qmoe_forward(self.copies[i % ncop], x, ids, w, out=out, workspace=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        # second pass: CUDA events on the launch stream around each kernel launch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(LAUNCH_NAMES))] for _ in range(steps)]
+        launches = 0
+        for i in range(steps):
+            launches += q.qmoe_forward_profiled(self.copies[i % ncop], x, ids, w, out, ws, evs[i])
+        torch.cuda.synchronize()
+        kms = {name: sum(evs[i][2 * j].elapsed_time(evs[i][2 * j + 1]) for i in range(steps)) / steps
+               for j, name in enumerate(LAUNCH_NAMES)}
+        st = q.qmoe_read_device_status(ws)
+        if st != q.QMOE_OK:
+            raise RuntimeError(f"{wl.name} M={M}: device status: {q.status_string(st)}")
+        return {"M": M, "ms": ms, "steps": steps, "clocks": clk.summary(), "inp": inp, "kernel_ms": kms,
+                "launches_per_step": launches / steps, "bytes": by, "copies": ncop, "x": x, "ids": ids, "w": w}
+
+    def release(self):
+        self.copies = []
+        self.base = None
+        self.torch.cuda.empty_cache()
+
+
+def e2e_host(gw, r, steps, warmup, world):
+    """The same layer end to end through the host-buffer entry point: every step
+    copies x, the top-k ids and weights from pinned host memory to the device,
+    runs the forward, and copies out back."""
+    torch, q, wl = gw.torch, gw.q, gw.wl
+    M = r["M"]
+    xh = r["x"].cpu().pin_memory()
+    idh = r["ids"].cpu().pin_memory()
+    wh = r["w"].cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    wsh = q.alloc_workspace(q.qmoe_workspace_size_host(gw.base, M, wl.k), gw.dev)
+    ncop = len(gw.copies)
+    for i in range(warmup):
+        q.qmoe_forward_host(gw.copies[i % ncop], xh, idh, wh, outh, wsh)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        q.qmoe_forward_host(gw.copies[i % ncop], xh, idh, wh, outh, wsh)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1) / steps, world, gw.dev)
+
+
+def entry_line(wl, r, pk):
+    roof, layer = roofline_entry(wl, r["M"], r["ms"], r["kernel_ms"], r["bytes"], pk)
+    roof["traffic"] = recorded_traffic(wl.name, r["M"], roof["kernel"])
+    return {"workload": wl.name, "M": r["M"], "ms": r["ms"], "steps": r["steps"], **layer,
+            "distinct_experts": r["bytes"]["distinct_experts"], "roofline": roof,
+            "kernel_ms": {n: round(v, 5) for n, v in r["kernel_ms"].items()}, "clocks": r["clocks"],
+            "rotation_copies": r["copies"]}
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -243,109 +424,26 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     qbuild.build()
     q.lib()
+    pk = peaks()
     wl = WORKLOADS[args.workload]
     M = args.M or (DEFAULT_M if DEFAULT_M in wl.Ms else wl.Ms[0])
-    layer = make_layer(wl, seed=0)
-    base = q.DeviceLayer.from_canonical(wl.qt, wl.act, layer.q13, layer.s13, layer.q2, layer.s2, layer.g13,
-                                        layer.g2, device=dev)
-    # rotate through copies of the packed weights so that no step finds them in L2
-    copies = [base]
-    n_copies = max(1, min(4, math.ceil(3 * L2_BYTES / max(1, base.weight_bytes())) + 1))
-    for _ in range(n_copies - 1):
-        copies.append(q.DeviceLayer(base.qt, base.E, base.H, base.I, base.act, base.w13.clone(), base.w2.clone(),
-                                    None if base.s13 is None else base.s13.clone(),
-                                    None if base.s2 is None else base.s2.clone(),
-                                    None if base.perm13 is None else base.perm13.clone()))
-    del layer
-    stream = torch.cuda.current_stream()
-
-    def measure(M, steps, warmup, profile=True):
-        inp = make_inputs(wl, M, seed=0)
-        x = torch.from_numpy(inp.x).to(base.torch_dtype).to(dev)
-        ids = torch.from_numpy(inp.topk_ids).to(dev)
-        w = torch.from_numpy(inp.topk_weights).to(dev)
-        out = torch.empty_like(x)
-        ws = q.alloc_workspace(q.qmoe_workspace_size(base, M, wl.k), dev)
-        for i in range(warmup):
-            q.qmoe_forward(copies[i % len(copies)], x, ids, w, out=out, workspace=ws)
-        st = q.qmoe_read_device_status(ws)
-        if st != q.QMOE_OK:
-            raise RuntimeError(f"device status after warm-up: {q.status_string(st)}")
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(dev.index) as clk:
-            e0.record(stream)
-            for i in range(steps):
-                q.qmoe_forward(copies[i % len(copies)], x, ids, w, out=out, workspace=ws)
-            e1.record(stream)
-            torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
-        res = {"M": M, "ms": ms, "clocks": clk.summary(), "inp": inp}
-        if profile:
-            # second pass over the same K steps with CUDA events around each kernel launch
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(LAUNCH_NAMES))] for _ in range(steps)]
-            launches = 0
-            for i in range(steps):
-                launches += q.qmoe_forward_profiled(copies[i % len(copies)], x, ids, w, out, ws, evs[i])
-            torch.cuda.synchronize()
-            per = {}
-            for j, name in enumerate(LAUNCH_NAMES):
-                per[name] = sum(evs[i][2 * j].elapsed_time(evs[i][2 * j + 1]) for i in range(steps)) / steps
-            res["kernel_ms"] = per
-            res["launches_per_step"] = launches / steps
-        st = q.qmoe_read_device_status(ws)
-        if st != q.QMOE_OK:
-            raise RuntimeError(f"device status: {q.status_string(st)}")
-        res["bytes"] = algorithmic_bytes(wl, base, inp)
-        res["copies"] = len(copies)
-        res["x"], res["ids"], res["w"] = x, ids, w
-        return res
-
-    main = measure(M, args.steps, args.warmup)
+    gw = GpuWorkload(q, wl, dev)
+    main = gw.measure(M, args.steps, args.warmup, world)
     ms = max_over_ranks(main["ms"], world, dev)
-
-    # end to end through the host-buffer entry point: pinned H2D of x/ids/weights,
-    # the forward, D2H of out, every step
-    xh = main["x"].cpu().pin_memory()
-    idh = main["ids"].cpu().pin_memory()
-    wh = main["w"].cpu().pin_memory()
-    outh = torch.empty_like(xh).pin_memory()
-    wsh = q.alloc_workspace(q.qmoe_workspace_size_host(base, M, wl.k), dev)
-    for i in range(args.warmup):
-        q.qmoe_forward_host(copies[i % len(copies)], xh, idh, wh, outh, wsh)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        q.qmoe_forward_host(copies[i % len(copies)], xh, idh, wh, outh, wsh)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-
-    sweep = []
-    if not args.no_sweep and rank == 0:
-        for Ms in wl.Ms:
-            if Ms == M:
-                continue
-            r = measure(Ms, max(5, args.steps // 5), 3)
-            sweep.append(r)
-    return wl, M, main, ms, e2e_ms, sweep, base
-
-
-def summarize(wl, r, hbm, tc):
-    M = r["M"]
-    ms = r["ms"]
-    k = r["kernel_ms"]
-    by = r["bytes"]
-    flops = wl.flops(M)
-    return {"M": M, "ms": round(ms, 5), "tokens_per_s": M / (ms * 1e-3),
-            "tflops": flops / (ms * 1e-3) / 1e12,
-            "weight_gbs": by["weights"] / (ms * 1e-3) / 1e9,
-            "hbm_frac_layer": by["layer"] / (ms * 1e-3) / 1e9 / hbm,
-            "distinct_experts": by["distinct_experts"],
-            "kernel_ms": {n: round(v, 5) for n, v in k.items()}}
+    e2e_ms = e2e_host(gw, main, args.steps, args.warmup, world)
+    entries = []
+    if not args.no_sweep:
+        todo = [(n, Ms) for n, Ms in REPORTED if args.workloads is None or n in args.workloads]
+        for name, Ms in todo:
+            if name != wl.name:
+                gw.release()
+                gw = GpuWorkload(q, WORKLOADS[name], dev)
+            for Mi in Ms:
+                r = gw.measure(Mi, args.steps, 3, world, min_s=MIN_TIMED_S)
+                entries.append(entry_line(gw.wl, r, pk))
+                del r
+        gw.release()
+    return wl, M, main, ms, e2e_ms, entries, pk
 
 
 def main():
@@ -359,35 +457,17 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    wl, M, main_r, ms, e2e_ms, sweep, base = run_gpu(args, rank, world)
-    hbm, tc_burst, tc_sust, peak_src = peaks()
+    wl, M, main_r, ms, e2e_ms, entries, pk = run_gpu(args, rank, world)
     if rank == 0:
         import oracle  # noqa: F401  (CPU baseline leg only)
         layer_cpu = make_layer(wl, seed=0)
         n_tok, secs = oracle_sample(wl, layer_cpu, main_r["inp"], args.cpu_sample_s)
+        del layer_cpu
         cpu_tps = n_tok / secs
         by = main_r["bytes"]
-        kms = main_r["kernel_ms"]
-        dominant = max(("gemm_gate_up", "gemm_down"), key=lambda n: kms[n])
-        flops = wl.flops(M)
-        # the dominant GEMM's roofline: HBM (weight stream) or tensor pipe, by its
-        # arithmetic intensity against the measured peaks' ratio
-        P = M * wl.k
-        kflops = 2.0 * P * (2 * wl.I if dominant == "gemm_gate_up" else wl.I) * wl.H
-        kms_s = kms[dominant] * 1e-3
-        if kflops / by[dominant] > tc_burst * 1e12 / (hbm * 1e9):
-            roof = {"bound": "tensor", "achieved": kflops / kms_s / 1e12, "peak": tc_burst, "unit": "TFLOP/s",
-                    "frac": kflops / kms_s / 1e12 / tc_burst,
-                    "peak_source": f"{peak_src} bf16_tflops burst (MEASURED_PEAKS.json cuBLAS bf16 GEMM; "
-                                   "the f16 MMAs run at the bf16 rate)",
-                    "algorithmic_flops_per_launch": kflops}
-        else:
-            roof = {"bound": "hbm", "achieved": by[dominant] / kms_s / 1e9, "peak": hbm, "unit": "GB/s",
-                    "frac": by[dominant] / kms_s / 1e9 / hbm,
-                    "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
-                    "algorithmic_bytes_per_launch": by[dominant]}
-        roof.update({"kernel": dominant, "traffic": recorded_traffic(wl.name, M, dominant),
-                     "layer_frac_hbm": by["layer"] / (ms * 1e-3) / 1e9 / hbm})
+        roof, layer = roofline_entry(wl, M, ms, main_r["kernel_ms"], by, pk)
+        roof["traffic"] = recorded_traffic(wl.name, M, roof["kernel"])
+        roof["layer_frac_hbm"] = layer["frac_hbm_layer"]
         line = {
             "metric": METRIC,
             "value": whole_job_tokens_per_s(M, world, ms),
@@ -399,12 +479,13 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": f"{wl.act} MMA operands, f32 accumulate, {wl.qt} weights",
+            "dtype": f"f16 MMA operands, f32 accumulate, {wl.qt} weights, {wl.act} activations",
             "data": "synthetic (seeded N(0,0.02) weights quantized offline, N(0,1) activations, random router)",
             "config": workload_config(wl, M),
-            "tflops": world * flops / (ms * 1e-3) / 1e12,
-            "weight_gbs": world * by["weights"] / (ms * 1e-3) / 1e9,
+            "tflops": world * layer["tflops"],
+            "weight_gbs": world * layer["weight_gbs"],
             "roofline": roof,
+            "layer": layer,
             "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"float64 numpy oracle on the first {n_tok} of the {M} tokens "
                                        f"(each token dequantizes its {wl.k} experts), {secs:.1f} s"},
@@ -413,11 +494,12 @@ def main():
                     "d2h_bytes_per_step": int(M * wl.H * 2), "ms_per_step": e2e_ms},
             "gpu_launches": int(round(main_r["launches_per_step"] * args.steps)),
             "clocks": main_r["clocks"],
-            "kernel_ms": {n: round(v, 5) for n, v in kms.items()},
-            "sweep": [summarize(wl, r, hbm, tc_burst) for r in sweep],
+            "kernel_ms": {n: round(v, 5) for n, v in main_r["kernel_ms"].items()},
+            "workloads": entries,
         }
         line["config"]["l2"] = (f"inputs larger than L2: {by['weights'] / 1e6:.0f} MB of touched expert weights per "
-                                f"step, rotated across {main_r['copies']} packed copies between steps (L2 129 MB)")
+                                f"step, rotated across {main_r['copies']} packed copies between steps (L2 129 MB); "
+                                "each reported workload likewise")
         print(json.dumps(line))
     if world > 1:
         import torch

@@ -17,6 +17,7 @@ from .moe import (  # noqa: F401
     silu,
     expert_ffn,
     moe_forward,
+    moe_forward_batches,
     moe_forward_rows,
     moe_align,
     route_topk,

@@ -148,6 +148,45 @@ def expert_ffn(xrows: np.ndarray, w13: np.ndarray, w2: np.ndarray) -> np.ndarray
     return t @ w2.T                                         # [R, H]
 
 
+def moe_forward_batches(layer, batches, experts=None) -> list:
+    """Layer outputs for the tokens ``rows`` of several token batches of one layer.
+
+    batches: sequence of (x [M, H], topk_ids [M, k], topk_weights [M, k], rows).
+    Returns one float64 [len(rows), H] array per batch (each token row is
+    independent of the others).  Each expert's matrices are dequantized once
+    for all batches.  With ``experts`` (a subset of expert ids) only the slots
+    routed to those experts contribute: out[m] = sum over slots j with
+    topk_ids[m, j] in ``experts`` of topk_weights[m, j] * y(m, j); summed over
+    a partition of the experts this is the whole output.
+    """
+    E = layer.wl.E
+    H = layer.wl.H
+    todo = range(E) if experts is None else experts
+    prep = []
+    for x, topk_ids, topk_weights, rows in batches:
+        rows = np.asarray(list(rows), np.int64)
+        ids = np.asarray(topk_ids)[rows]                    # [R, k]
+        w = np.asarray(topk_weights, np.float64)[rows]      # [R, k]
+        y = np.zeros((rows.size, ids.shape[1], H), np.float64)   # y(m, j); 0 for slots not computed
+        prep.append((np.asarray(x, np.float64)[rows], ids, w, y))
+    for e in todo:
+        sels = [np.nonzero(ids == e) for _, ids, _, _ in prep]
+        if all(sel[0].size == 0 for sel in sels):
+            continue
+        w13, w2 = dequant_layer_expert(layer, e)
+        for (xr, _, _, y), sel in zip(prep, sels):
+            if sel[0].size:
+                y[sel[0], sel[1], :] = expert_ffn(xr[sel[0]], w13, w2)
+        del w13, w2
+    outs = []
+    for _, ids, w, y in prep:
+        out = np.zeros((ids.shape[0], H), np.float64)
+        for j in range(ids.shape[1]):
+            out += w[:, j:j + 1] * y[:, j, :]
+        outs.append(out)
+    return outs
+
+
 def moe_forward_rows(layer, x: np.ndarray, topk_ids: np.ndarray,
                      topk_weights: np.ndarray, rows) -> np.ndarray:
     """Layer output for the tokens ``rows`` only (each row is independent).
@@ -155,24 +194,7 @@ def moe_forward_rows(layer, x: np.ndarray, topk_ids: np.ndarray,
     Returns float64 [len(rows), H].  Used to check sampled tokens of large
     workloads; ``moe_forward`` is this over all rows.
     """
-    rows = np.asarray(list(rows), np.int64)
-    E = layer.wl.E
-    ids = np.asarray(topk_ids)[rows]                        # [R, k]
-    w = np.asarray(topk_weights, np.float64)[rows]          # [R, k]
-    R, k = ids.shape
-    H = layer.wl.H
-    y = np.zeros((R, k, H), np.float64)                     # y(m, j)
-    for e in range(E):
-        sel = np.nonzero(ids == e)
-        if sel[0].size == 0:
-            continue
-        w13, w2 = dequant_layer_expert(layer, e)
-        y[sel[0], sel[1], :] = expert_ffn(np.asarray(x, np.float64)[rows[sel[0]]], w13, w2)
-        del w13, w2
-    out = np.zeros((R, H), np.float64)
-    for j in range(k):
-        out += w[:, j:j + 1] * y[:, j, :]
-    return out
+    return moe_forward_batches(layer, [(x, topk_ids, topk_weights, rows)])[0]
 
 
 def moe_forward(layer, x: np.ndarray, topk_ids: np.ndarray,

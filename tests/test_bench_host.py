@@ -27,3 +27,34 @@ def test_recorded_traffic_matches_current_source_only(tmp_path, monkeypatch):
 def test_whole_job_tokens_per_s():
     assert bench.whole_job_tokens_per_s(16, 1, 1.0) == 16000.0
     assert bench.whole_job_tokens_per_s(16, 4, 2.0) == 32000.0
+
+
+def test_algorithmic_bytes_and_roofline_arithmetic():
+    from synth import WORKLOADS
+    import numpy as np
+    wl = WORKLOADS["mixtral8x7b_w4"]
+    M = 4
+    ids = np.array([[0, 1], [1, 2], [0, 2], [5, 1]], np.int32)
+    w13, w2 = 1000, 500
+    by = bench.algorithmic_bytes(wl, w13, w2, ids, M)
+    assert by["distinct_experts"] == 4
+    P = M * wl.k
+    assert by["weights"] == 4 * (w13 + w2)
+    assert by["gemm_gate_up"] == 4 * w13 + P * wl.H * 2 + P * wl.I * 2
+    assert by["gemm_down"] == 4 * w2 + P * wl.I * 2 + P * wl.H * 4
+    assert by["layer"] == 4 * (w13 + w2) + 2 * M * wl.H * 2 + 2 * P * wl.I * 2
+    pk = {"hbm": 1000.0, "tc_burst": 2000.0, "tc_sust": 1800.0, "src": "test"}
+    # weight-stream bound: 1e9 bytes in 2 ms -> 500 GB/s -> 0.5 of a 1000 GB/s peak
+    by = {"gemm_gate_up": 1e9, "gemm_down": 1e8, "layer": 2e9, "weights": 1.5e9, "distinct_experts": 8}
+    roof, layer = bench.roofline_entry(wl, 1, 4.0, {"gemm_gate_up": 2.0, "gemm_down": 1.0}, by, pk)
+    assert roof["bound"] == "hbm" and roof["kernel"] == "gemm_gate_up"
+    assert abs(roof["frac"] - 0.5) < 1e-12
+    assert abs(layer["frac_hbm_layer"] - 0.5) < 1e-12 and abs(layer["frac_hbm_weights"] - 0.375) < 1e-12
+    # a compute-heavy launch is judged against the tensor peak
+    Mb = 8192
+    by = {"gemm_gate_up": 1e9, "gemm_down": 5e8, "layer": 2e9, "weights": 1e9, "distinct_experts": 8}
+    roof, layer = bench.roofline_entry(wl, Mb, 10.0, {"gemm_gate_up": 6.0, "gemm_down": 3.0}, by, pk)
+    fl = bench.gemm_flops(wl, Mb, "gemm_gate_up")
+    assert roof["bound"] == "tensor" and abs(roof["achieved"] - fl / 6e-3 / 1e12) < 1e-6
+    assert abs(roof["frac_of_sustained_peak"] * 1800.0 - roof["achieved"]) < 1e-9
+    assert layer["binding"] == "tensor"

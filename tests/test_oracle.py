@@ -348,6 +348,30 @@ def test_forward_rows_match_full(small):
     assert np.array_equal(part, full[[5, 1]])
 
 
+def test_forward_batches_partition_and_brute_force():
+    """Several token sets of one layer in one call: each equals the scalar brute
+    force of its rows; summed over a partition of the experts the per-subset
+    outputs give the whole output, and an expert subset that no slot uses
+    contributes exactly zero."""
+    wl = _wl(E=5, k=2, H=32, I=48, group_size=16, act_order=True)
+    layer = make_layer(wl, seed=23)
+    a = make_inputs(wl, 6, seed=1)
+    b = make_inputs(wl, 4, seed=2)
+    batches = [(a.x, a.topk_ids, a.topk_weights, [4, 0, 2]), (b.x, b.topk_ids, b.topk_weights, [3, 1])]
+    got = oracle.moe_forward_batches(layer, batches)
+    for (x, ids, w, rows), g in zip(batches, got):
+        want = _brute_force(layer, x[rows], ids[rows], w[rows])
+        np.testing.assert_allclose(g, want, rtol=1e-10, atol=1e-12)
+    parts = [oracle.moe_forward_batches(layer, batches, experts=sub) for sub in ([0, 3], [1], [2, 4])]
+    for i in range(2):
+        np.testing.assert_allclose(sum(p[i] for p in parts), got[i], rtol=1e-12, atol=1e-14)
+    used = set(np.concatenate([a.topk_ids[[4, 0, 2]].ravel(), b.topk_ids[[3, 1]].ravel()]).tolist())
+    unused = [e for e in range(wl.E) if e not in used]
+    if unused:
+        for z in oracle.moe_forward_batches(layer, batches, experts=unused):
+            assert np.all(z == 0.0)
+
+
 # ----------------------------------------------------------------------------
 # moe_align
 # ----------------------------------------------------------------------------
