@@ -147,7 +147,12 @@ typedef struct {
    * kernel exits with the CUDA context intact (the output is then garbage). */
   int32_t fault_injection;
   int32_t issuers;
-  int32_t reserved[3];
+  /* Depth of the GEMMs' shared-memory token-tile ring as a multiple (1..3) of
+   * the TMEM A ring (0: automatic, 2 where shared memory leaves the weight ring
+   * at least 8 slots, else 1).  A value whose ring does not fit gives
+   * QMOE_ERR_INVALID_ARG. */
+  int32_t token_ring;
+  int32_t reserved[2];
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */
@@ -310,7 +315,8 @@ size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k,
  * num_sms > 0).  Fields: token_tile (token rows per GEMM work item), issuers
  * (MMA-issuing threads per CTA), acc_bufs (TMEM accumulators per issuer),
  * split1 / split2 (split-K of the gate/up and down GEMMs), w_stages (packed-
- * weight ring depth), ab_stages (token-tile / TMEM A ring depth), stage_bytes
+ * weight ring depth), ab_stages (TMEM A ring depth), b_stages (token-tile ring
+ * depth, a multiple of ab_stages), stage_bytes
  * (packed bytes per 128 x 128 block), workspace_bytes.  num_sms: the GPU's
  * SM count the plan is sized for (0: the current device's).  Errors as
  * qmoe_workspace_size_ex (QMOE_ERR_INVALID_ARG / QMOE_ERR_UNSUPPORTED), and
@@ -326,7 +332,8 @@ typedef struct {
   int32_t ab_stages;
   int32_t stage_bytes;
   int64_t workspace_bytes;
-  int32_t reserved[6];
+  int32_t b_stages;
+  int32_t reserved[5];
 } qmoe_plan_info;
 
 qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts,

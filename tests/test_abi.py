@@ -371,13 +371,28 @@ def test_plan_rings_and_tmem_constraints():
                 assert p["ab_stages"] % mult == 0 and p["ab_stages"] >= mult
                 assert NI * p["acc_bufs"] * T + 64 * p["ab_stages"] <= 512
                 wslot = (per + 1023) // 1024 * 1024
-                assert 1024 + p["w_stages"] * wslot + p["ab_stages"] * T * 256 + 1024 <= 232448
+                assert p["b_stages"] % p["ab_stages"] == 0 and p["b_stages"] <= 3 * p["ab_stages"]
+                assert 1024 + p["w_stages"] * wslot + p["b_stages"] * T * 256 + 1024 <= 232448
+                # barriers below the selector table at the end of the 1 KB barrier area
+                assert (2 * p["w_stages"] + p["ab_stages"] + p["b_stages"] + 7) * 8 + 8 <= 1024 - 128
                 assert p["stage_bytes"] == per
 
 
 def test_plan_overrides_and_other_workloads():
     p = _plan(MIXTRAL, 16, split1=3, split2=5, token_tile=48, issuers=2)
     assert (p["split1"], p["split2"], p["token_tile"], p["issuers"]) == (3, 5, 48, 2)
+    # token-tile ring twice the A ring at decode sizes, equal at 128-row tiles (shared memory)
+    p16 = _plan(MIXTRAL, 16)
+    assert p16["b_stages"] == 2 * p16["ab_stages"] and p16["w_stages"] >= 8
+    p2k = _plan(MIXTRAL, 2048)
+    assert p2k["b_stages"] == p2k["ab_stages"]
+    for m in (1, 2, 3):
+        pm = _plan(MIXTRAL, 16, token_ring=m)
+        assert pm["b_stages"] == m * pm["ab_stages"]
+    with pytest.raises(q.QmoeError):
+        _plan(MIXTRAL, 2048, token_ring=3)       # 12 x 32 KB token tiles do not fit
+    with pytest.raises(q.QmoeError):
+        _plan(MIXTRAL, 16, token_ring=4)
     ds = dict(E=160, H=5120, I=1536, group_size=-1, qt=N.QMOE_INT8_PER_COL, scale_dtype=N.QMOE_F32)
     assert _plan(ds, 1024, k=6)["token_tile"] == 64      # 6144 pairs over 160 experts
     assert _plan(ds, 1, k=6)["token_tile"] == 16

@@ -126,7 +126,7 @@ qmoe_status validate_layer_dims(const qmoe_layer* L) {
 struct Plan {
   int64_t M = 0, P = 0;
   int k = 0;
-  int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0;
+  int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0, b_stages = 0;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -211,10 +211,30 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.a_col0 = p.issuers * p.acc_bufs * T;
   p.ab_stages = a_slots(p.acc_bufs);
   if (p.ab_stages < ring_mult) return (o != nullptr && o->issuers != 0) ? QMOE_ERR_INVALID_ARG : QMOE_ERR_UNSUPPORTED;
+  // Token-tile ring: a multiple m of the A ring, so that a token tile can be
+  // fetched up to m - 1 A-ring laps before its MMAs and its L2 latency stays
+  // off the A slots' cycle.  The deepest m <= 2 that leaves the weight ring at
+  // least 8 slots (weights stream from HBM and want the deeper ring).
   const size_t wslot = (static_cast<size_t>(p.stage_bytes) + 1023) & ~size_t(1023);
-  const size_t b_bytes = static_cast<size_t>(p.ab_stages) * T * 256;
-  if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return QMOE_ERR_UNSUPPORTED;
-  p.w_stages = static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
+  auto w_depth = [&](int nb2) {
+    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256;
+    if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
+    return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
+  };
+  int ring_m = 1;
+  if (o != nullptr && o->token_ring != 0) {
+    if (o->token_ring < 1 || o->token_ring > 3) return QMOE_ERR_INVALID_ARG;
+    ring_m = o->token_ring;
+    if (w_depth(ring_m * p.ab_stages) < 2) return QMOE_ERR_INVALID_ARG;
+  } else {
+    for (int m = 2; m > 1; --m)
+      if (w_depth(m * p.ab_stages) >= 8) {
+        ring_m = m;
+        break;
+      }
+  }
+  p.b_stages = ring_m * p.ab_stages;
+  p.w_stages = w_depth(p.b_stages);
   if (p.w_stages < 2 || p.ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
   // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
   p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
@@ -347,6 +367,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.issuers = pl.issuers;
   g1.w_stages = pl.w_stages;
   g1.ab_stages = pl.ab_stages;
+  g1.b_stages = pl.b_stages;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -957,6 +978,7 @@ qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k
   info->split2 = pl.S2;
   info->w_stages = pl.w_stages;
   info->ab_stages = pl.ab_stages;
+  info->b_stages = pl.b_stages;
   info->stage_bytes = pl.stage_bytes;
   info->workspace_bytes = static_cast<int64_t>(pl.total);
   return QMOE_OK;

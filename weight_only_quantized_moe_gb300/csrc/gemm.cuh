@@ -25,11 +25,14 @@
 //     the MMA's A operand straight from tensor memory; dequantized weights
 //     never touch shared memory, which carries only the packed bytes and the
 //     token tile.
-//   * one pipeline stage = one 128-K quantization group.  Two rings: packed
-//     weights (deep: they stream from HBM) and token tiles (each slot paired
-//     with a TMEM A slot; token tiles come from L2).  Both arrive by 1-D bulk
-//     TMA copies: the producers of the B operand (gather, rescale) store it
-//     pre-staged, per 128-K group and 8-row group, in the 128-byte-swizzled
+//   * one pipeline stage = one 128-K quantization group.  Three rings: packed
+//     weights in shared memory (deep: they stream from HBM), token tiles in
+//     shared memory (token tiles come from L2) and dequantized A tiles in
+//     TMEM.  The token-tile ring is a multiple (1 to 3) of the A ring, so a
+//     token tile is fetched several stages before its MMAs and its L2 latency
+//     stays off the A slots' cycle.  Weights and token tiles arrive by 1-D
+//     bulk TMA copies: the producers of the B operand (gather, rescale) store
+//     it pre-staged, per 128-K group and 8-row group, in the 128-byte-swizzled
 //     K-major layout the MMA's shared-memory descriptor reads, so a chunk's
 //     tile for one stage is one contiguous run.
 //   * warp roles (25 warps): two TMA producer threads (warps 4, 7) and two
@@ -42,13 +45,16 @@
 //     the tensor pipe is, so that two accumulator buffers fit in TMEM.  Warps
 //     0-3 are the epilogue.  A persistent grid walks the work items.
 //   * barriers per stage: the dequant set waits for the weights and the token
-//     tile (one barrier counts both copies), releases the weight slot, writes A
-//     and signals it; the issuer
-//     waits for that one signal, issues the stage's MMAs and commits one
-//     release of the token-tile/A slot.  Every ring's size is a multiple of
-//     the stride of each role that uses it (2 for producers and dequant sets,
-//     NI for the issuers), so each slot belongs to one role of each kind and
-//     each role sees every phase of the barriers it waits on.
+//     tile (one barrier counts both copies), releases the weight slot,
+//     converts, waits until the MMAs of the stage that last used its A slot
+//     are done (implied by the token tile's arrival when both rings have the
+//     same depth), writes A and signals it; the issuer waits for that one
+//     signal, issues the stage's MMAs and commits one "stage done" barrier,
+//     which frees the stage's A slot and its token-tile slot.  Every ring's
+//     size is a multiple of the stride of each role that uses it (2 for
+//     producers and dequant sets, NI for the issuers), so each slot belongs
+//     to one role of each kind and each role sees every phase of the barriers
+//     it waits on.
 //   * every mbarrier wait is bounded (see ptx.cuh); a wait that gives up
 //     records QMOE_ERR_TIMEOUT in the status word and the CTA winds down after
 //     waiting for its own copies and MMAs, then frees its TMEM.
@@ -75,9 +81,9 @@ constexpr int kBarrierBytes = 1024;
 
 __host__ __device__ inline uint32_t gemm_w_slot(int group_bytes) { return (group_bytes + 1023u) & ~1023u; }
 // Dynamic shared memory: weight ring, token-tile ring, barriers (+1 KB alignment slack).
-__host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int ab_stages, int token_tile) {
+__host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int b_stages, int token_tile) {
   return 1024 + static_cast<size_t>(w_stages) * gemm_w_slot(group_bytes) +
-         static_cast<size_t>(ab_stages) * token_tile * 256 + kBarrierBytes;
+         static_cast<size_t>(b_stages) * token_tile * 256 + kBarrierBytes;
 }
 
 struct WorkItem {
@@ -323,11 +329,12 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 
 // ---------------------------------------------------------------------------
 // The kernel.  Shared memory: weight ring (w_stages slots), token-tile ring
-// (ab_stages slots of T rows), barriers.  TMEM columns: issuer i owns acc_bufs
-// fp32 accumulators of T columns at [(i*acc_bufs + b) * T]; token-tile slot j
-// pairs with the 64-column A slot at a_col0 + 64j.  Every role walks only its
-// own stages (every 2nd for producers and dequant sets, every NI-th for the MMA
-// issuers), stepping its ring position by the same stride.
+// (b_stages slots of T rows), barriers.  TMEM columns: issuer i owns acc_bufs
+// fp32 accumulators of T columns at [(i*acc_bufs + b) * T]; stage g uses the
+// 64-column A slot a_col0 + 64 (g mod ab_stages) and the token-tile slot
+// g mod b_stages, whose "done" barrier the issuer commits.  Every role walks
+// only its own stages (every 2nd for producers and dequant sets, every NI-th
+// for the MMA issuers), stepping its ring positions by the same stride.
 // ---------------------------------------------------------------------------
 template <int KIND, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int T = p.token_tile;
-  const int NW = p.w_stages, NB = p.ab_stages, ACCB = p.acc_bufs, NI = p.issuers;
+  const int NW = p.w_stages, NB = p.ab_stages, NB2 = p.b_stages, ACCB = p.acc_bufs, NI = p.issuers;
   const uint32_t wslot = gemm_w_slot(p.stage_bytes);
   const uint32_t bslot = static_cast<uint32_t>(T) * 256u;
   uint8_t* wring = smem;
@@ -344,11 +351,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 
   // wfull[i] completes when a stage's weights AND its token tile have landed (the
   // producer arms it for both copies; the token-tile copy, issued later, counts on it)
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(bring + NB * bslot);
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(bring + NB2 * bslot);
   uint64_t* wempty = wfull + NW;
   uint64_t* afull = wempty + NW;
-  uint64_t* sfree = afull + NB;  // token-tile slot and its A slot are free again
-  uint64_t* accfull = sfree + NB;
+  // done[j]: the MMAs of the stage in token-tile slot j completed, so that
+  // slot and the stage's A slot are free again
+  uint64_t* done = afull + NB;
+  uint64_t* accfull = done + NB2;
   uint64_t* accempty = accfull + 2;
   uint64_t* drain = accempty + 2;  // one per MMA issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
@@ -364,10 +373,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_init(smem_u32(wfull + s), 1);
       mbar_init(smem_u32(wempty + s), kDequantWarps);
     }
-    for (int j = 0; j < NB; ++j) {
-      mbar_init(smem_u32(afull + j), kDequantWarps);
-      mbar_init(smem_u32(sfree + j), 1);
-    }
+    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), kDequantWarps);
+    for (int j = 0; j < NB2; ++j) mbar_init(smem_u32(done + j), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
       mbar_init(smem_u32(accempty + b), 4);  // the 4 epilogue warps
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         // the chunk's rows of one stage of the pre-staged B operand: one contiguous run
         const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u;
         const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256;
-        for (int g = first_own(g0, id, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
+        for (int g = first_own(g0, id, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB2)) {
           const int ks = it.ks0 + (g - g0);
           const bool inject = p.fault_injection == 1 && blockIdx.x == 0 && g == 0;  // armed, never filled
           if (!mbar_wait(smem_u32(wempty + wr.idx), wr.phase ^ 1u, abort_flag, 128)) {
@@ -430,9 +437,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             tma_load_1d(smem_u32(wring + wr.idx * wslot), wsrc + static_cast<int64_t>(ks) * p.stage_bytes,
                         static_cast<uint32_t>(p.stage_bytes), wb, pol_w);
           last_w = g;
-          // the token-tile slot and its TMEM A slot are free once the MMAs of the
-          // slot's previous stage completed
-          if (!mbar_wait(smem_u32(sfree + br.idx), br.phase ^ 1u, abort_flag, 128)) {
+          // the token-tile slot is free once the MMAs of its previous stage completed
+          if (!mbar_wait(smem_u32(done + br.idx), br.phase ^ 1u, abort_flag, 128)) {
             ok = false;
             break;
           }
@@ -459,8 +465,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     // (large tiles) warp 5 takes every stage.
     const int id = (warp == kMmaWarp3) ? 2 : warp - kMmaWarp;
     if (lane == 0 && id < NI) {
-      Ring br;
-      br.idx = id;
+      Ring ar, br;  // A slot (NB) and token-tile slot / done barrier (NB2) of the stage
+      ar.idx = br.idx = id;
       int g0 = 0, itn = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -476,19 +482,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         }
         const uint32_t d_tmem = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
         uint32_t acc0 = 0u;  // the issuer's first stage of the item overwrites its accumulator
-        for (int g = first_own(g0, id, NI); g < g0 + n_st; g += NI, br.step(NI, NB)) {
+        for (int g = first_own(g0, id, NI); g < g0 + n_st; g += NI, ar.step(NI, NB), br.step(NI, NB2)) {
           // the dequant set signals A only after the stage's token tile has landed
-          if (!mbar_wait(smem_u32(afull + br.idx), br.phase, abort_flag, 16)) {
+          if (!mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 16)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(br.idx * 64);
+          const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // token tile [8-row group][64-K block][8 rows][128 B]: 8-row groups 2048 bytes apart
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
           mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
           acc0 = 1u;
-          mma_commit(smem_u32(sfree + br.idx));
+          mma_commit(smem_u32(done + br.idx));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
@@ -508,17 +514,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     const int half = (warp >> 2) & 1;   // K half of the stage row: columns 32*half .. +31
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    Ring wr, br;
-    wr.idx = br.idx = set;
+    // wr: weight slot of the stage; ar: its A slot; dr: the done barrier of the
+    // stage NB earlier, the last one that used the same A slot (phase of lap -1,
+    // which a fresh barrier reports complete, for the first NB stages)
+    Ring wr, ar, dr;
+    wr.idx = ar.idx = set;
+    dr.idx = set - NB + NB2;
+    dr.phase = 1u;
     int g0 = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
       const int n_st = it.ks1 - it.ks0;
-      for (int g = first_own(g0, set, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB)) {
-        // weights and token tile landed; the latter also means the MMAs of the A
-        // slot's previous stage completed (the producer waited for that)
+      for (int g = first_own(g0, set, 2); g < g0 + n_st;
+           g += 2, wr.step(2, NW), ar.step(2, NB), dr.step(2, NB2)) {
+        // weights and token tile landed
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
         if (!ok) break;
         tc_fence_after();
@@ -549,12 +560,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
           dequant_int8_half<KIND == kQ8G, BF16S>(pk, sbits, out);
         }
-        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(br.idx * 64 + 32 * half);
+        // the A slot is free once the MMAs of the stage NB earlier completed; with
+        // token-tile and A rings of one depth the token tile's arrival implied it
+        // (the producer waited for the same barrier phase before copying it)
+        if (NB2 != NB) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
         tmem_st_32x32b_x32<0>(ta, out);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(afull + br.idx));
+        if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
       }
       g0 += n_st;
     }

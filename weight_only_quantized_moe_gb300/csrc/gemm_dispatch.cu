@@ -14,7 +14,7 @@ cudaError_t launch_gemm_i8g_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8g_bf16(const GemmParams&, int, cudaStream_t);
 
 size_t gemm_smem_bytes(const GemmParams& p) {
-  return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.ab_stages, p.token_tile);
+  return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.b_stages, p.token_tile);
 }
 
 cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream) {
@@ -22,9 +22,11 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
   if (p.issuers < 1 || p.issuers > kMaxIssuers) return cudaErrorInvalidValue;
   const int mult = (p.issuers == 3) ? 6 : 2;
   if (p.w_stages < 2 || (p.w_stages & 1) || p.ab_stages < mult || p.ab_stages % mult != 0) return cudaErrorInvalidValue;
-  // barriers (2 per weight slot, 2 per token-tile slot, 4 + kMaxIssuers more, TMEM address,
-  // abort flag) below the 128-byte selector table at the end of the barrier area
-  if ((2 * p.w_stages + 2 * p.ab_stages + 4 + kMaxIssuers) * 8 + 8 > kBarrierBytes - 128) return cudaErrorInvalidValue;
+  if (p.b_stages < p.ab_stages || p.b_stages % p.ab_stages != 0) return cudaErrorInvalidValue;
+  // barriers (2 per weight slot, 1 per A slot, 1 per token-tile slot, 4 + kMaxIssuers more,
+  // TMEM address, abort flag) below the 128-byte selector table at the end of the barrier area
+  if ((2 * p.w_stages + p.ab_stages + p.b_stages + 4 + kMaxIssuers) * 8 + 8 > kBarrierBytes - 128)
+    return cudaErrorInvalidValue;
   switch (kind) {
     case kQ4: return bf16_scales ? launch_gemm_i4_bf16(p, grid, stream) : launch_gemm_i4_f16(p, grid, stream);
     case kQ4Z: return bf16_scales ? launch_gemm_i4z_bf16(p, grid, stream) : launch_gemm_i4z_f16(p, grid, stream);

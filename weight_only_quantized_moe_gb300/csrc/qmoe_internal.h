@@ -76,7 +76,8 @@ struct GemmParams {
   int32_t issuers;           // MMA-issuing threads (1 or 2)
   int32_t a_col0;            // first TMEM column of the A slots
   int32_t w_stages;          // packed-weight ring depth (even)
-  int32_t ab_stages;         // token-tile ring depth = TMEM A slots of 64 columns (even)
+  int32_t ab_stages;         // TMEM A slots of 64 columns (even)
+  int32_t b_stages;          // token-tile ring depth in shared memory (a multiple of ab_stages)
   int32_t stage_bytes;       // packed weight bytes per 128-K group
   int32_t epi_mode;
   int32_t P;                 // number of token-expert pairs
