@@ -286,9 +286,14 @@ def roofline_entry(wl, M, ms, kernel_ms, by, pk):
 # every (workload, M) the layer is reported at, besides the headline
 REPORTED = (("mixtral8x7b_w4", (1, 4, 8, 16, 64)), ("mixtral8x7b_w4_actorder", (1, 16, 128, 512)),
             ("mixtral8x7b_w8", (1, 16, 128, 512)), ("deepseekv2_w8", (1, 32, 256, 1024)),
-            ("mixtral8x22b_w4", (2048, 4096, 8192)), ("mixtral8x7b_w4s24", (1, 16, 64)))
+            ("mixtral8x22b_w4", (2048, 4096, 8192)), ("mixtral8x7b_w4s24", (1, 16, 64)),
+            ("mixtral8x7b_w8s24", (1, 16, 64)))
 MIN_TIMED_S = 0.3      # timed region per reported entry (clock samples every ~0.5 ms)
 MAX_ROTATION_BYTES = 24 << 30
+# dense linear layer (one weight matrix, no routing): dense and 2:4-sparse, 4 and 8 bits
+LINEAR_REPORTED = (("int4", 128, "f16"), ("int4s24", 128, "f16"), ("int8", -1, "bf16"), ("int8s24", -1, "bf16"))
+LINEAR_SHAPE = (16384, 4096)   # N output features, K input features
+LINEAR_MS = (1, 16, 128)
 
 
 class GpuWorkload:
@@ -304,15 +309,16 @@ class GpuWorkload:
                                                  group_size=wl.group_size)
         del layer
         b = self.base
-        self.w13_e = b.w13.numel() // wl.E + (2 * wl.I * 4 if wl.qt == "int8" else 0)
-        self.w2_e = b.w2.numel() // wl.E + (wl.H * 4 if wl.qt == "int8" else 0)
+        fs = b.s13 is not None  # float32 scales per output feature, outside the packed blocks
+        self.w13_e = b.w13.numel() // wl.E + (2 * wl.I * 4 if fs else 0)
+        self.w2_e = b.w2.numel() // wl.E + (wl.H * 4 if fs else 0)
         self.copies = [b]
         self.torch = torch
 
     def ensure_copies(self, touched_bytes):
         """Enough copies that one lap of the rotation touches 3x the L2 size."""
         b = self.base
-        want = min(8, math.ceil(3 * L2_BYTES / max(1, touched_bytes)) + 1)
+        want = min(16, math.ceil(3 * L2_BYTES / max(1, touched_bytes)) + 1)
         want = max(1, min(want, MAX_ROTATION_BYTES // max(1, b.weight_bytes())))
         while len(self.copies) < want:
             c = lambda t: None if t is None else t.clone()
@@ -373,6 +379,72 @@ class GpuWorkload:
             raise RuntimeError(f"{wl.name} M={M}: device status: {q.status_string(st)}")
         return {"M": M, "ms": ms, "steps": steps, "clocks": clk.summary(), "inp": inp, "kernel_ms": kms,
                 "launches_per_step": launches / steps, "bytes": by, "copies": ncop, "x": x, "ids": ids, "w": w}
+
+    def release(self):
+        self.copies = []
+        self.base = None
+        self.torch.cuda.empty_cache()
+
+
+class GpuLinear:
+    """A dense linear layer's packed weight on the device, rotated across copies."""
+
+    def __init__(self, q, qt, gs, act, N, K, dev):
+        import torch
+        from synth import make_linear
+        self.q, self.qt, self.gs, self.act, self.N, self.K, self.dev, self.torch = q, qt, gs, act, N, K, dev, torch
+        lin = make_linear(N, K, qt, gs, act, seed=0)
+        self.base = q.DeviceLinear.from_canonical(qt, act, lin.q, lin.s, gs, lin.z, lin.g_idx, device=dev)
+        del lin
+        b = self.base
+        self.wbytes = b.w.numel() + (4 * b.s.numel() if b.s is not None else 0)
+        n = max(1, min(16, math.ceil(3 * L2_BYTES / self.wbytes) + 1))
+        self.copies = [b] + [q.DeviceLinear(qt, N, K, act, b.w.clone(), None if b.s is None else b.s.clone(), None, gs)
+                             for _ in range(n - 1)]
+
+    def measure(self, M, steps, warmup, min_s=0.0):
+        torch, q = self.torch, self.q
+        from synth import make_linear_inputs
+        x = torch.from_numpy(make_linear_inputs(self.K, M, self.act, seed=0)).to(self.base.torch_dtype).to(self.dev)
+        out = torch.empty((M, self.N), dtype=x.dtype, device=self.dev)
+        ws = q.alloc_workspace(q.qmoe_linear_workspace_size(self.base, M), self.dev)
+        nc = len(self.copies)
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(warmup):
+            q.qmoe_linear_forward(self.copies[i % nc], x, out=out, workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if q.qmoe_read_device_status(ws) != q.QMOE_OK:
+            raise RuntimeError(f"linear {self.qt} M={M}: device status after warm-up")
+        if min_s > 0 and warmup > 0:
+            est = e0.elapsed_time(e1) / warmup * 1e-3
+            steps = int(min(4000, max(steps, math.ceil(min_s / max(est, 1e-6)))))
+        with ClockSampler(self.dev.index) as clk:
+            e0.record(stream)
+            for i in range(steps):
+                q.qmoe_linear_forward(self.copies[i % nc], x, out=out, workspace=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        plan = q.qmoe_linear_describe_plan(self.base, M)
+        return {"ms": ms, "steps": steps, "clocks": clk.summary(), "plan": plan}
+
+    def entry(self, M, r, pk):
+        t = r["ms"] * 1e-3
+        byts = self.wbytes + M * self.K * 2 + M * self.N * 2
+        flops = 2.0 * M * self.N * self.K
+        hbm_frac = byts / t / 1e9 / pk["hbm"]
+        tc_frac = flops / t / 1e12 / pk["tc_burst"]
+        bound = "tensor" if flops / byts > pk["tc_burst"] * 1e12 / (pk["hbm"] * 1e9) else "hbm"
+        return {"layer": "dense linear", "quant": self.qt, "group_size": self.gs, "act_dtype": self.act,
+                "N": self.N, "K": self.K, "M": M, "ms": r["ms"], "steps": r["steps"],
+                "weight_bytes": self.wbytes, "weight_gbs": self.wbytes / t / 1e9, "tflops": flops / t / 1e12,
+                "frac_hbm": hbm_frac, "frac_tensor": tc_frac, "binding": bound,
+                "frac_binding": tc_frac if bound == "tensor" else hbm_frac,
+                "plan": {k: r["plan"][k] for k in ("token_tile", "issuers", "split1")}, "clocks": r["clocks"],
+                "rotation_copies": len(self.copies)}
 
     def release(self):
         self.copies = []
@@ -443,6 +515,14 @@ def run_gpu(args, rank, world):
                 entries.append(entry_line(gw.wl, r, pk))
                 del r
         gw.release()
+        N_out, K = LINEAR_SHAPE
+        for qt, gs, act in LINEAR_REPORTED:
+            if args.workloads is not None and "linear" not in args.workloads:
+                break
+            gl = GpuLinear(q, qt, gs, act, N_out, K, dev)
+            for Mi in LINEAR_MS:
+                entries.append(gl.entry(Mi, gl.measure(Mi, args.steps, 3, min_s=MIN_TIMED_S), pk))
+            gl.release()
     return wl, M, main, ms, e2e_ms, entries, pk
 
 

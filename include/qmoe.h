@@ -76,9 +76,14 @@ typedef enum {
   QMOE_INT4_GROUP_ZP = 3, /* 4-bit codes 0..15 with a zero point 0..15 and a scale per group
                              (128 input channels, or all of them with group_size -1) */
   QMOE_INT8_GROUP = 4,    /* signed 8-bit codes, one scale per 128 input channels */
-  QMOE_INT4_GROUP_24 = 5  /* as QMOE_INT4_GROUP, 2:4 sparse along K: in every aligned group of
+  QMOE_INT4_GROUP_24 = 5, /* as QMOE_INT4_GROUP, 2:4 sparse along K: in every aligned group of
                              4 input channels at most 2 codes differ from 8 (value 0); only
                              those 2 codes and their positions are stored */
+  QMOE_INT8_24 = 6        /* signed 8-bit codes, 2:4 sparse along K (at most 2 non-zero codes in
+                             every aligned group of 4 input channels; the 2 kept codes and their
+                             positions are stored), with one float32 scale per output feature
+                             (group_size -1) or one scale of the activation type per 128 input
+                             channels (group_size 128) */
 } qmoe_quant_type;
 
 typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
@@ -90,19 +95,22 @@ typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
  *
  *   E, H, I      experts, hidden size, expert intermediate size.
  *                Constraints: 1 <= E <= 1024; H % 128 == 0; I % 128 == 0.
- *   group_size   QMOE_INT4_GROUP / QMOE_INT4_GROUP_ZP / QMOE_INT4_GROUP_24: 128
- *                or -1 (channel-wise); QMOE_INT8_PER_COL: -1; QMOE_INT8_GROUP: 128.
- *                QMOE_INT4_GROUP_24 takes no act-order permutation.
+ *   group_size   QMOE_INT4_GROUP / QMOE_INT4_GROUP_ZP / QMOE_INT4_GROUP_24 /
+ *                QMOE_INT8_24: 128 or -1 (channel-wise); QMOE_INT8_PER_COL: -1;
+ *                QMOE_INT8_GROUP: 128.  The 2:4-sparse formats take no
+ *                act-order permutation.
  *   qt           quantization type.
  *   act_dtype    F16 or BF16: type of x and out (the MMAs run in f16).
- *   scale_dtype  int4 and grouped int8: must equal act_dtype (scales are
- *                normalised to the activation type when packed);
- *                per-column int8: F32.
+ *   scale_dtype  int4 and grouped int8 (also 2:4-sparse int8 with group_size
+ *                128): must equal act_dtype (scales are normalised to the
+ *                activation type when packed); per-column int8 and
+ *                channel-wise 2:4-sparse int8: F32.
  *   w13, w2      packed expert weights (sizes: qmoe_packed_bytes), 256-byte aligned.
- *   s13, s2      per-column int8 only: float32 scales packed by
- *                qmoe_pack_int8 ([E, 2I] in packed row order, [E, H]); NULL
- *                otherwise (the other formats keep their scales and zero
- *                points inside the packed weights).
+ *   s13, s2      per-column int8 and channel-wise 2:4-sparse int8 only:
+ *                float32 scales packed by qmoe_pack_int8 / qmoe_pack_int8_24
+ *                ([E, 2I] in packed row order, [E, H]); NULL otherwise (the
+ *                other formats keep their scales and zero points inside the
+ *                packed weights).
  *   perm13       int4 act-order only (group_size 128): int32 [E, H] written
  *                by qmoe_pack_int4 / qmoe_pack_int4_zp (hidden channel of
  *                each sorted K position); NULL otherwise.
@@ -152,7 +160,11 @@ typedef struct {
    * at least 8 slots, else 1).  A value whose ring does not fit gives
    * QMOE_ERR_INVALID_ARG. */
   int32_t token_ring;
-  int32_t reserved[2];
+  /* Dequant warp sets of the GEMMs: 2 (8 warps each, half a stage row per
+   * warp) or 4 (4 warps each, whole rows per warp); 0: automatic.  4 needs a
+   * token-tile ring that is a multiple of 4 (QMOE_ERR_INVALID_ARG otherwise). */
+  int32_t dq_sets;
+  int32_t reserved[1];
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */
@@ -165,7 +177,8 @@ typedef struct {
  * Per 128 x 128 block: QMOE_INT4_GROUP 8448 (group_size 128 or -1),
  * QMOE_INT4_GROUP_ZP 8576 (group_size 128 or -1), QMOE_INT4_GROUP_24 6400
  * (group_size 128 or -1), QMOE_INT8_PER_COL 16384 (group_size -1),
- * QMOE_INT8_GROUP 16640 (group_size 128); times E * (rows/128) * (K/128).
+ * QMOE_INT8_GROUP 16640 (group_size 128), QMOE_INT8_24 10240 (group_size -1)
+ * or 10496 (group_size 128); times E * (rows/128) * (K/128).
  */
 size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K, int32_t group_size);
 
@@ -252,6 +265,31 @@ qmoe_status qmoe_pack_int4_24(int32_t E, int32_t H, int32_t I, int32_t group_siz
 qmoe_status qmoe_unpack_int4_24(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
                                 const void* w2_packed, uint8_t* q13, uint16_t* s13, uint8_t* q2, uint16_t* s2);
 
+/*
+ * Pack 2:4-sparse int8 ("Add GPTQ Marlin 2:4 sparse structured support":
+ * 8-bit, group 128 or channel-wise, 2:4 structured sparsity).  Canonical
+ * inputs (host): q13 int8 [E, 2I, H] and q2 int8 [E, H, I] dense codes
+ * -127..127 where every aligned group of 4 consecutive input channels holds
+ * at most 2 non-zero codes.  group_size -1 (scale_dtype QMOE_F32): s13 float
+ * [E, 2I], s2 float [E, H], one scale per output feature, W = q * s[n];
+ * outputs s13_packed float [E, 2I] (packed row order) and s2_packed float
+ * [E, H] as for qmoe_pack_int8.  group_size 128 (scale_dtype F16 or BF16):
+ * s13 uint16 [E, H/128, 2I], s2 uint16 [E, I/128, H] scale bit patterns,
+ * W = q * s[k/128, n], kept inside the packed blocks (s13_packed / s2_packed
+ * may be NULL).  Per group of 4 the packer keeps the non-zero codes, padded
+ * with the lowest remaining channels.  More than 2 non-zero codes in a group,
+ * or a code of -128, gives QMOE_ERR_INVALID_ARG.  The layer's qt is
+ * QMOE_INT8_24.
+ */
+qmoe_status qmoe_pack_int8_24(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                              const int8_t* q13, const void* s13, const int8_t* q2, const void* s2,
+                              void* w13_packed, float* s13_packed, void* w2_packed, float* s2_packed);
+
+/* Exact inverse of qmoe_pack_int8_24 (dense codes, 0 at the pruned channels; s13 / s2 as packed). */
+qmoe_status qmoe_unpack_int8_24(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                                const float* s13_packed, const void* w2_packed, const float* s2_packed,
+                                int8_t* q13, void* s13, int8_t* q2, void* s2);
+
 /* Exact inverse of qmoe_pack_int8_group. */
 qmoe_status qmoe_unpack_int8_group(int32_t E, int32_t H, int32_t I, const void* w13_packed, const void* w2_packed,
                                    int8_t* q13, uint16_t* s13, int8_t* q2, uint16_t* s2);
@@ -316,7 +354,7 @@ size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k,
  * (MMA-issuing threads per CTA), acc_bufs (TMEM accumulators per issuer),
  * split1 / split2 (split-K of the gate/up and down GEMMs), w_stages (packed-
  * weight ring depth), ab_stages (TMEM A ring depth), b_stages (token-tile ring
- * depth, a multiple of ab_stages), stage_bytes
+ * depth, a multiple of ab_stages), dq_sets (dequant warp sets), stage_bytes
  * (packed bytes per 128 x 128 block), workspace_bytes.  num_sms: the GPU's
  * SM count the plan is sized for (0: the current device's).  Errors as
  * qmoe_workspace_size_ex (QMOE_ERR_INVALID_ARG / QMOE_ERR_UNSUPPORTED), and
@@ -333,7 +371,8 @@ typedef struct {
   int32_t stage_bytes;
   int64_t workspace_bytes;
   int32_t b_stages;
-  int32_t reserved[5];
+  int32_t dq_sets;
+  int32_t reserved[4];
 } qmoe_plan_info;
 
 qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts,
@@ -453,6 +492,79 @@ size_t qmoe_workspace_size_logits(const qmoe_layer* layer, int64_t M, int32_t to
 qmoe_status qmoe_forward_logits(const qmoe_layer* layer, const void* x, int64_t M, const void* logits,
                                 qmoe_dtype logits_dtype, int32_t top_k, int32_t renormalize, void* out,
                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dense linear layer                                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A dense linear layer out = x . W^T with W [N, K] weight-only quantized in
+ * any of the formats above ("Add GPTQ Marlin 2:4 sparse structured support":
+ * the GPTQ Marlin linear layer, 4 or 8 bits, group 128 or channel-wise, dense
+ * or 2:4 sparse).  It runs the MoE layer's GEMM kernel with one weight matrix
+ * and no routing or activation function.
+ *   N, K         output and input features (multiples of 128).
+ *   group_size, qt, act_dtype, scale_dtype   as for qmoe_layer.
+ *   w            packed by qmoe_pack_linear (qmoe_packed_bytes(qt, 1, N, K,
+ *                group_size) bytes), 256-byte aligned.
+ *   s            per-column int8 and channel-wise 2:4-sparse int8: float32
+ *                [N] (s_packed of qmoe_pack_linear); NULL otherwise.
+ *   perm         int4 act-order (QMOE_INT4_GROUP / _ZP, group 128): int32 [K]
+ *                written by qmoe_pack_linear; NULL otherwise.
+ */
+typedef struct {
+  int32_t N, K;
+  int32_t group_size;
+  qmoe_quant_type qt;
+  qmoe_dtype act_dtype;
+  qmoe_dtype scale_dtype;
+  const void* w;
+  const float* s;
+  const int32_t* perm;
+} qmoe_linear;
+
+/*
+ * Pack one weight matrix for qmoe_linear (host memory in and out).
+ *   q      codes [N, K], one per byte: uint8 0..15 (int4 formats) or int8
+ *          -127..127 (int8 formats); 2:4 formats as for the MoE packers.
+ *   s      scales: uint16 bit patterns of scale_dtype [K/128 (1 when
+ *          group_size is -1), N] for the int4 formats, grouped int8 and
+ *          grouped 2:4 int8; float [N] (scale_dtype QMOE_F32) for per-column
+ *          int8 and channel-wise 2:4 int8.
+ *   z      QMOE_INT4_GROUP_ZP only: zero points uint8 [K/128 or 1, N]; NULL otherwise.
+ *   g_idx  int4 / int4 with zero points, group 128: int32 [K] act-order
+ *          groups (each group exactly 128 channels) or NULL.
+ * Outputs: w_packed (qmoe_packed_bytes(qt, 1, N, K, group_size) bytes);
+ * s_packed float [N] for the float-scale formats (ignored otherwise);
+ * perm_out int32 [K] when g_idx != NULL.  Errors as for the MoE packers.
+ */
+qmoe_status qmoe_pack_linear(qmoe_quant_type qt, int32_t N, int32_t K, int32_t group_size, qmoe_dtype scale_dtype,
+                             const void* q, const void* s, const uint8_t* z, const int32_t* g_idx,
+                             void* w_packed, float* s_packed, int32_t* perm_out);
+
+/* Exact inverse of qmoe_pack_linear given the same g_idx (q, s, z as its inputs). */
+qmoe_status qmoe_unpack_linear(qmoe_quant_type qt, int32_t N, int32_t K, int32_t group_size, const void* w_packed,
+                               const float* s_packed, const int32_t* g_idx, void* q, void* s, uint8_t* z);
+
+/* Workspace bytes of qmoe_linear_forward (0 on invalid input); opts may be NULL. */
+size_t qmoe_linear_workspace_size(const qmoe_linear* layer, int64_t M, const qmoe_options* opts);
+
+/* The launch plan of qmoe_linear_forward, as qmoe_describe_plan (split1 is its split-K, split2 0). */
+qmoe_status qmoe_linear_describe_plan(const qmoe_linear* layer, int64_t M, const qmoe_options* opts,
+                                      int32_t num_sms, qmoe_plan_info* info);
+
+/*
+ * out[M, N] (act_dtype, overwritten) = x[M, K] (act_dtype) . W^T, f16 MMA
+ * operands with fp32 accumulation (as the MoE layer).  Device buffers; x, out
+ * and the workspace 256-byte aligned; the workspace needs
+ * qmoe_linear_workspace_size bytes.  opts: split1 (split-K), token_tile,
+ * issuers, token_ring as for qmoe_forward_ex (NULL: automatic).  M == 0
+ * launches nothing.  Asynchronous on `stream`; device-side faults are read
+ * with qmoe_read_device_status on the workspace.
+ */
+qmoe_status qmoe_linear_forward(const qmoe_linear* layer, const void* x, int64_t M, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                const qmoe_options* opts);
 
 /*
  * Synchronise `stream` and return the first device-side fault recorded in

@@ -14,6 +14,8 @@ from .moe import (  # noqa: F401
     dequant_int8,
     dequant_int8_group,
     dequant_layer_expert,
+    dequant_linear,
+    linear_forward,
     silu,
     expert_ffn,
     moe_forward,

@@ -83,13 +83,14 @@ def decompress_24(values: np.ndarray, positions: np.ndarray, zero_code: int = 8)
     sparse structured support"): for every aligned group j of 4 input channels,
     values[n, 2j] and values[n, 2j+1] are the codes at channels 4j + i0 and
     4j + i1 with positions[n, j] = (i0, i1), i0 < i1; the other two channels
-    hold `zero_code` (value 0 under zero point 8).
-    values: uint8 [N, K/2]; positions: int [N, K/4, 2]."""
+    hold `zero_code` (value 0: 8 for int4 codes with zero point 8, 0 for
+    signed int8 codes).
+    values: uint8 [N, K/2] (int4 codes) or int8 [N, K/2]; positions: int [N, K/4, 2]."""
     values = np.asarray(values)
     positions = np.asarray(positions, np.int64)
     N, half = values.shape
     K = 2 * half
-    q = np.full((N, K), zero_code, np.uint8)
+    q = np.full((N, K), zero_code, values.dtype)
     rows = np.arange(N)[:, None]
     base = 4 * np.arange(K // 4)[None, :]
     q[rows, base + positions[:, :, 0]] = values[:, 0::2]
@@ -123,13 +124,30 @@ def dequant_layer_expert(layer, e: int):
         z2 = None if layer.z2 is None else layer.z2[e]
         w13 = dequant_int4(layer.q13[e], layer.s13[e], g13, wl.group_size, z13)
         w2 = dequant_int4(layer.q2[e], layer.s2[e], g2, wl.group_size, z2)
-    elif wl.qt == "int8g":
+    elif wl.qt == "int8g" or (wl.qt == "int8s24" and wl.group_size > 0):
+        # int8s24: the canonical codes are dense, 0 at the pruned channels
         w13 = dequant_int8_group(layer.q13[e], layer.s13[e], wl.group_size)
         w2 = dequant_int8_group(layer.q2[e], layer.s2[e], wl.group_size)
     else:
         w13 = dequant_int8(layer.q13[e], layer.s13[e])
         w2 = dequant_int8(layer.q2[e], layer.s2[e])
     return w13, w2
+
+
+def dequant_linear(lin) -> np.ndarray:
+    """Dequantized W [N, K] of a canonical dense linear layer (any format above)."""
+    if lin.qt in ("int4", "int4zp", "int4s24"):
+        return dequant_int4(lin.q, lin.s, lin.g_idx, lin.group_size, lin.z)
+    if lin.qt == "int8g" or (lin.qt == "int8s24" and lin.group_size > 0):
+        return dequant_int8_group(lin.q, lin.s, lin.group_size)
+    return dequant_int8(lin.q, lin.s)
+
+
+def linear_forward(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """out[m, n] = sum_k x[m, k] * W[n, k]: the dense linear layer that "Add GPTQ
+    Marlin 2:4 sparse structured support" runs with 4- or 8-bit weights, dense
+    or 2:4 sparse (float64)."""
+    return np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
 
 
 # ----------------------------------------------------------------------------

@@ -12,7 +12,11 @@ from .gen import (  # noqa: F401
     WORKLOADS,
     Workload,
     QuantLayer,
+    QuantLinear,
     Inputs,
+    make_linear,
+    make_linear_inputs,
+    quantize_int8_24,
     make_layer,
     make_inputs,
     prune_24,

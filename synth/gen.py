@@ -33,9 +33,10 @@ class Workload:
     H: int            # hidden size
     I: int            # expert intermediate size
     qt: str           # "int4" (zero point 8), "int4zp" (per-group zero points), "int4s24"
-                      # (int4, 2:4 sparse along K), "int8" (per output column) or "int8g"
-                      # (group scales)
-    group_size: int   # 128 or -1 (whole K is one group) for int4 / int4zp; -1 for int8; 128 for int8g
+                      # (int4, 2:4 sparse along K), "int8" (per output column), "int8g"
+                      # (group scales) or "int8s24" (int8, 2:4 sparse along K)
+    group_size: int   # 128 or -1 (whole K is one group) for int4 / int4zp / int4s24 / int8s24;
+                      # -1 for int8; 128 for int8g
     act: str          # activation / scale storage type: "f16" or "bf16"
     act_order: bool   # int4 only: random per-expert g_idx permutation
     zipf: float       # 0: unbiased router; >0: Zipf exponent of the per-expert logit bias
@@ -58,6 +59,8 @@ class Workload:
             return n // 2 + groups * 2 + groups // 2
         if self.qt == "int8g":
             return n + groups * 2
+        if self.qt == "int8s24":   # half the codes, 2 bits of position each
+            return n // 2 + n // 8 + (groups * 2 if self.group_size > 0 else (2 * self.I + self.H) * 4)
         return n + (2 * self.I + self.H) * 4
 
 
@@ -78,6 +81,9 @@ WORKLOADS = {
                               False, 1.1, (1, 32, 256, 1024)),
     # Mixtral-8x7B shape with 2:4-sparse int4 g128 experts
     "mixtral8x7b_w4s24": Workload("mixtral8x7b_w4s24", 8, 2, 4096, 14336, "int4s24", 128, "f16",
+                                  False, 0.0, (1, 16, 64)),
+    # Mixtral-8x7B shape with 2:4-sparse per-column int8 experts (bf16 activations)
+    "mixtral8x7b_w8s24": Workload("mixtral8x7b_w8s24", 8, 2, 4096, 14336, "int8s24", -1, "bf16",
                                   False, 0.0, (1, 16, 64)),
     # Mixtral-8x22B prefill, tensor-core-bound
     "mixtral8x22b_w4": Workload("mixtral8x22b_w4", 8, 2, 6144, 16384, "int4", 128, "bf16",
@@ -168,6 +174,19 @@ def quantize_int4_24(w: np.ndarray, group_size: int, scale_dtype: str):
     and every aligned group of 4 codes along K holds at most 2 codes other
     than 8.  Returns codes uint8 [N, K] and scales float32 [K/G, N]."""
     return quantize_int4_rtn(prune_24(w), group_size, None, scale_dtype)
+
+
+def quantize_int8_24(w: np.ndarray, group_size: int, scale_dtype: str):
+    """2:4-sparse int8 ("Add GPTQ Marlin 2:4 sparse structured support": 8-bit,
+    group 128 or channel-wise): prune_24, then symmetric int8 RTN on the pruned
+    matrix (per output feature for group_size -1, per 128 input channels
+    otherwise), so every pruned entry has code 0 and every aligned group of 4
+    codes along K holds at most 2 non-zero codes.  Returns codes int8 [N, K] and
+    scales float32 [N] (channel-wise) or [K/G, N] (grouped)."""
+    wp = prune_24(w)
+    if group_size < 0:
+        return quantize_int8_rtn(wp)
+    return quantize_int8_group(wp, group_size, scale_dtype)
 
 
 def quantize_int4_rtn_zp(w: np.ndarray, group_size: int, g_idx: np.ndarray | None, scale_dtype: str):
@@ -265,6 +284,9 @@ def _gen_expert(wl: Workload, seed: int, e: int):
         if wl.qt == "int4s24":
             q, s = quantize_int4_24(w, wl.group_size, wl.act)
             out[mat] = (q, s, None, None)
+        elif wl.qt == "int8s24":
+            q, s = quantize_int8_24(w, wl.group_size, wl.act)
+            out[mat] = (q, s, None, None)
         elif wl.qt in ("int4", "int4zp"):
             g = None
             if wl.act_order:
@@ -288,10 +310,10 @@ def _gen_expert(wl: Workload, seed: int, e: int):
 def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> QuantLayer:
     E, H, I = wl.E, wl.H, wl.I
     z13 = z2 = None
-    if wl.qt in ("int4", "int4zp", "int4s24", "int8g"):
+    if wl.qt in ("int4", "int4zp", "int4s24", "int8g") or (wl.qt == "int8s24" and wl.group_size > 0):
         n13 = 1 if wl.group_size < 0 else H // wl.group_size
         n2 = 1 if wl.group_size < 0 else I // wl.group_size
-        cdt = np.int8 if wl.qt == "int8g" else np.uint8
+        cdt = np.int8 if wl.qt in ("int8g", "int8s24") else np.uint8
         q13 = np.empty((E, 2 * I, H), cdt)
         s13 = np.empty((E, n13, 2 * I), np.float32)
         q2 = np.empty((E, H, I), cdt)
@@ -330,6 +352,55 @@ def make_layer(wl: Workload, seed: int = 0, threads: int | None = None) -> Quant
         for e in range(E):
             one(e)
     return QuantLayer(wl, q13, s13, q2, s2, g13, g2, z13, z2)
+
+
+@dataclass
+class QuantLinear:
+    """Canonical (pre-pack) quantized weight of one dense linear layer W [N, K].
+
+    q: codes [N, K] (uint8 0..15 for the int4 formats, int8 for the int8
+    formats); s: scales float32 [K/G, N] (int4 formats, grouped int8 formats;
+    [1, N] for channel-wise int4) or [N] (per-column int8 formats); z: zero
+    points uint8 like s (int4zp); g_idx: int32 [K] act-order groups or None.
+    """
+    qt: str
+    act: str
+    group_size: int
+    q: np.ndarray
+    s: np.ndarray
+    z: np.ndarray | None = None
+    g_idx: np.ndarray | None = None
+
+
+def make_linear(N: int, K: int, qt: str, group_size: int, act: str, act_order: bool = False, seed: int = 0,
+                w_std: float = 0.02) -> QuantLinear:
+    """A dense linear layer's weight, N(0, w_std) quantized offline like the experts."""
+    rng = np.random.default_rng([seed, 7, 0])
+    w = rng.standard_normal((N, K), dtype=np.float32)
+    w *= np.float32(w_std)
+    g = _actorder_gidx(np.random.default_rng([seed, 7, 1]), K, group_size) if act_order else None
+    if qt == "int4":
+        q, s = quantize_int4_rtn(w, group_size, g, act)
+        return QuantLinear(qt, act, group_size, q, s, None, g)
+    if qt == "int4zp":
+        q, s, z = quantize_int4_rtn_zp(w, group_size, g, act)
+        return QuantLinear(qt, act, group_size, q, s, z, g)
+    if qt == "int4s24":
+        q, s = quantize_int4_24(w, group_size, act)
+        return QuantLinear(qt, act, group_size, q, s)
+    if qt == "int8s24":
+        q, s = quantize_int8_24(w, group_size, act)
+        return QuantLinear(qt, act, group_size, q, s)
+    if qt == "int8g":
+        q, s = quantize_int8_group(w, group_size, act)
+        return QuantLinear(qt, act, group_size, q, s)
+    q, s = quantize_int8_rtn(w)
+    return QuantLinear("int8", act, -1, q, s)
+
+
+def make_linear_inputs(K: int, M: int, act: str, seed: int = 0) -> np.ndarray:
+    """Activations [M, K] ~ N(0, 1), exact in the activation type."""
+    return round_to(np.random.default_rng(seed + 1).standard_normal((M, K), dtype=np.float32), act)
 
 
 # ----------------------------------------------------------------------------

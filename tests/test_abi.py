@@ -414,7 +414,102 @@ def test_header_is_plain_c99(tmp_path):
                    "typedef char a[sizeof(qmoe_options) == %d ? 1 : -1];\n"
                    "typedef char b[sizeof(qmoe_plan_info) == %d ? 1 : -1];\n"
                    "typedef char c[sizeof(qmoe_layer) == %d ? 1 : -1];\n"
-                   % (ctypes.sizeof(N.QmoeOptions), ctypes.sizeof(N.QmoePlanInfo), ctypes.sizeof(N.QmoeLayer)))
+                   "typedef char d[sizeof(qmoe_linear) == %d ? 1 : -1];\n"
+                   % (ctypes.sizeof(N.QmoeOptions), ctypes.sizeof(N.QmoePlanInfo), ctypes.sizeof(N.QmoeLayer),
+                      ctypes.sizeof(N.QmoeLinear)))
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src), "-o",
                         str(tmp_path / "h.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+# ----------------------------------------------------------------------------
+# 2:4-sparse int8 and the dense linear layer
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("gs,act", [(-1, "bf16"), (128, "f16"), (128, "bf16")])
+def test_pack_int8_24_round_trip_and_layout(gs, act):
+    from synth import make_layer, to_u16_bits
+    wl = Workload("t", 3, 2, 256, 384, "int8s24", gs, act, False, 0.0, (1,))
+    L = make_layer(wl, seed=6)
+    if gs == -1:
+        pk = q.qmoe_pack_int8_24(3, 256, 384, "f32", L.q13, L.s13, L.q2, L.s2, -1)
+        assert pk["w13"].nbytes == 3 * (768 // 128) * 2 * 10240
+        q13, s13, q2, s2 = q.qmoe_unpack_int8_24(3, 256, 384, pk["w13"], pk["s13"], pk["w2"], pk["s2"], -1)
+        assert np.array_equal(s13, L.s13) and np.array_equal(s2, L.s2)
+    else:
+        s13b, s2b = to_u16_bits(L.s13, act), to_u16_bits(L.s2, act)
+        pk = q.qmoe_pack_int8_24(3, 256, 384, act, L.q13, s13b, L.q2, s2b, 128)
+        assert pk["w13"].nbytes == 3 * (768 // 128) * 2 * 10496
+        q13, s13, q2, s2 = q.qmoe_unpack_int8_24(3, 256, 384, pk["w13"], None, pk["w2"], None, 128)
+        assert np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
+    assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
+    # documented layout of W2, expert 0, tile 0, K stage 0: row r, half h, group g:
+    # kept codes at bytes (h*128 + r)*32 + 2g + {0,1}; positions nibble g at 8192 + (h*128 + r)*8
+    blk = pk["w2"][:10240 if gs == -1 else 10496]
+    for r in (0, 77):
+        for h in (0, 1):
+            pos = int.from_bytes(bytes(blk[8192 + (h * 128 + r) * 8: 8192 + (h * 128 + r) * 8 + 8]), "little")
+            for g in range(16):
+                i0, i1 = (pos >> (4 * g)) & 3, (pos >> (4 * g + 2)) & 3
+                assert i0 < i1
+                c4 = L.q2[0, r, 64 * h + 4 * g: 64 * h + 4 * g + 4]
+                v = blk[(h * 128 + r) * 32 + 2 * g: (h * 128 + r) * 32 + 2 * g + 2].view(np.int8)
+                assert (v[0], v[1]) == (c4[i0], c4[i1])
+                assert all(c4[i] == 0 for i in range(4) if i not in (i0, i1))
+
+
+def test_pack_int8_24_rejects_three_of_four_and_minus_128():
+    q13 = np.zeros((1, 256, 128), np.int8)
+    q2 = np.zeros((1, 128, 128), np.int8)
+    s13 = np.ones((1, 256), np.float32)
+    s2 = np.ones((1, 128), np.float32)
+    q13[0, 5, 8:11] = [1, 2, 3]
+    with pytest.raises(q.QmoeError):
+        q.qmoe_pack_int8_24(1, 128, 128, "f32", q13, s13, q2, s2, -1)
+    q13[0, 5, 8:11] = [1, 0, 3]
+    q2[0, 0, 0] = -128
+    with pytest.raises(q.QmoeError):
+        q.qmoe_pack_int8_24(1, 128, 128, "f32", q13, s13, q2, s2, -1)
+    q2[0, 0, 0] = -127
+    q.qmoe_pack_int8_24(1, 128, 128, "f32", q13, s13, q2, s2, -1)
+
+
+LINEAR_FORMATS = [("int4", 128, "f16", True), ("int4", -1, "bf16", False), ("int4zp", 128, "bf16", True),
+                  ("int4s24", 128, "f16", False), ("int8", -1, "bf16", False), ("int8g", 128, "f16", False),
+                  ("int8s24", -1, "bf16", False), ("int8s24", 128, "f16", False)]
+
+
+@pytest.mark.parametrize("qt,gs,act,ao", LINEAR_FORMATS)
+def test_pack_linear_round_trip(qt, gs, act, ao):
+    from synth import make_linear, to_u16_bits
+    lin = make_linear(256, 384, qt, gs, act, act_order=ao, seed=2)
+    pk = q.qmoe_pack_linear(qt, 256, 384, act, lin.q, lin.s, gs, lin.z, lin.g_idx)
+    assert pk["w"].nbytes == q.packed_bytes(qt, 1, 256, 384, gs)
+    res = q.qmoe_unpack_linear(qt, 256, 384, pk, gs, lin.g_idx)
+    assert np.array_equal(res[0], lin.q)
+    if lin.s.ndim == 1:
+        assert np.array_equal(res[1], lin.s)
+    else:
+        assert np.array_equal(res[1], to_u16_bits(lin.s, act))
+    if qt == "int4zp":
+        assert np.array_equal(res[2], lin.z)
+    if ao:
+        p = pk["perm"]
+        assert sorted(p.tolist()) == list(range(384)) and np.all(np.diff(lin.g_idx[p]) >= 0)
+
+
+def test_linear_plan_and_validation_are_host_only():
+    L = q.lib()
+    ok = N.QmoeLinear(4096, 14336, 128, N.QMOE_INT4_GROUP, N.QMOE_F16, N.QMOE_F16, None, None, None)
+    assert L.qmoe_linear_workspace_size(ctypes.byref(ok), 16, None) > 0
+    p = q.qmoe_linear_describe_plan(ok, 16, num_sms=152)
+    assert p["token_tile"] == 16 and p["issuers"] == 3 and p["split1"] >= 1 and p["split2"] == 0
+    assert q.qmoe_linear_describe_plan(ok, 100, num_sms=152)["token_tile"] == 128
+    for bad in (N.QmoeLinear(100, 128, 128, N.QMOE_INT4_GROUP, N.QMOE_F16, N.QMOE_F16, None, None, None),
+                N.QmoeLinear(128, 128, 64, N.QMOE_INT4_GROUP, N.QMOE_F16, N.QMOE_F16, None, None, None),
+                N.QmoeLinear(128, 128, -1, N.QMOE_INT8_24, N.QMOE_F16, N.QMOE_F16, None, None, None),
+                N.QmoeLinear(128, 128, 128, 99, N.QMOE_F16, N.QMOE_F16, None, None, None)):
+        assert L.qmoe_linear_workspace_size(ctypes.byref(bad), 16, None) == 0
+        assert L.qmoe_linear_forward(ctypes.byref(bad), None, 16, None, None, 0, None, None) != q.QMOE_OK
+    # a valid layer with no workspace: rejected before any device access
+    assert L.qmoe_linear_forward(ctypes.byref(ok), None, 16, None, None, 0, None, None) == q.QMOE_ERR_WORKSPACE
+    assert L.qmoe_linear_forward(ctypes.byref(ok), None, 0, None, None, 0, None, None) == q.QMOE_OK

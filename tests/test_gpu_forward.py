@@ -57,7 +57,8 @@ VARIANTS = [("int4", "f16", False), ("int4", "bf16", False), ("int4", "f16", Tru
 OTHER_FORMATS = [("int4zp", "f16", False, 128), ("int4zp", "bf16", True, 128), ("int4zp", "bf16", False, -1),
                  ("int4", "f16", False, -1), ("int4", "bf16", False, -1), ("int8g", "f16", False, 128),
                  ("int8g", "bf16", False, 128), ("int4s24", "f16", False, 128), ("int4s24", "bf16", False, 128),
-                 ("int4s24", "f16", False, -1)]
+                 ("int4s24", "f16", False, -1), ("int8s24", "bf16", False, -1), ("int8s24", "f16", False, 128),
+                 ("int8s24", "bf16", False, 128)]
 
 
 @pytest.mark.parametrize("qt,act,ao", VARIANTS)
@@ -72,7 +73,7 @@ def test_forward_parity_other_formats(qt, act, ao, gs, M):
     _check(_wl(qt, act, ao, gs=gs), M)
 
 
-@pytest.mark.parametrize("qt,act,ao,gs", OTHER_FORMATS[:2] + OTHER_FORMATS[5:6] + OTHER_FORMATS[7:8])
+@pytest.mark.parametrize("qt,act,ao,gs", OTHER_FORMATS[:2] + OTHER_FORMATS[5:6] + OTHER_FORMATS[7:8] + OTHER_FORMATS[10:12])
 @pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 128)])
 def test_forward_other_formats_forced_split_and_tile(qt, act, ao, gs, split1, split2, tile):
     _check(_wl(qt, act, ao, gs=gs), 40, opts=q.make_options(split1, split2, tile))
@@ -82,6 +83,17 @@ def test_forward_other_formats_forced_split_and_tile(qt, act, ao, gs, split1, sp
 @pytest.mark.parametrize("split1,split2,tile", [(3, 2, 0), (2, 1, 16), (1, 2, 128), (3, 2, 32)])
 def test_forward_forced_split_and_tile(qt, act, ao, split1, split2, tile):
     _check(_wl(qt, act, ao), 40, opts=q.make_options(split1, split2, tile))
+
+
+@pytest.mark.parametrize("qt,act,ao,gs", [("int4", "f16", False, 128), ("int4", "bf16", True, 128),
+                                          ("int4zp", "bf16", False, 128), ("int8", "bf16", False, -1),
+                                          ("int8g", "f16", False, 128), ("int4s24", "f16", False, 128),
+                                          ("int8s24", "bf16", False, -1)])
+@pytest.mark.parametrize("M,split1,split2,tile", [(1, 0, 0, 0), (40, 0, 0, 0), (129, 0, 0, 0), (40, 3, 2, 0),
+                                                  (300, 1, 1, 128), (40, 2, 1, 64)])
+def test_forward_four_dequant_sets(qt, act, ao, gs, M, split1, split2, tile):
+    """The GEMMs with four dequant sets of four whole-row warps (every tile size)."""
+    _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile, dq_sets=4))
 
 
 @pytest.mark.parametrize("qt,act", [("int8", "f16"), ("int8", "bf16")])

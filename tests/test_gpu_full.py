@@ -27,7 +27,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 # every (workload, M) the benchmark reports
 FULL_WORKLOADS = ("mixtral8x7b_w4", "mixtral8x7b_w4_actorder", "mixtral8x7b_w8", "deepseekv2_w8",
-                  "mixtral8x22b_w4", "mixtral8x7b_w4s24")
+                  "mixtral8x22b_w4", "mixtral8x7b_w4s24", "mixtral8x7b_w8s24")
 FULL = [(name, M) for name in FULL_WORKLOADS for M in WORKLOADS[name].Ms]
 
 # the Mixtral-8x7B shape in the other weight formats (zero points, group-128 int8)

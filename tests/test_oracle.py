@@ -16,8 +16,9 @@ import numpy as np
 import pytest
 
 import oracle
-from synth import (QuantLayer, Workload, make_inputs, make_layer, prune_24, quantize_int4_24, quantize_int4_rtn,
-                   quantize_int4_rtn_zp, quantize_int8_group, quantize_int8_rtn)
+from synth import (QuantLayer, Workload, make_inputs, make_layer, make_linear, make_linear_inputs, prune_24,
+                   quantize_int4_24, quantize_int4_rtn, quantize_int4_rtn_zp, quantize_int8_24, quantize_int8_group,
+                   quantize_int8_rtn)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -292,14 +293,14 @@ def _brute_force(layer, x, ids, w):
     out = [[0.0] * H for _ in range(M)]
 
     def wq(q, s, gi, z, e, n, c):
-        if wl.qt in ("int4", "int4zp", "int4s24", "int8g"):
+        if wl.qt in ("int4", "int4zp", "int4s24", "int8g") or (wl.qt == "int8s24" and wl.group_size > 0):
             if gi is not None:
                 g = int(gi[e, c])
             elif wl.group_size < 0:
                 g = 0
             else:
                 g = c // wl.group_size
-            zero = 0 if wl.qt == "int8g" else (8 if z is None else int(z[e, g, n]))
+            zero = 0 if wl.qt in ("int8g", "int8s24") else (8 if z is None else int(z[e, g, n]))
             return (int(q[e, n, c]) - zero) * float(s[e, g, n])
         return int(q[e, n, c]) * float(s[e, n])
 
@@ -331,7 +332,7 @@ def _brute_force(layer, x, ids, w):
 @pytest.mark.parametrize("qt,act_order,gs", [("int4", False, 16), ("int4", True, 16), ("int8", False, -1),
                                              ("int4zp", False, 16), ("int4zp", True, 16), ("int4", False, -1),
                                              ("int4zp", False, -1), ("int8g", False, 16), ("int4s24", False, 16),
-                                             ("int4s24", False, -1)])
+                                             ("int4s24", False, -1), ("int8s24", False, -1), ("int8s24", False, 16)])
 def test_brute_force_tiny(qt, act_order, gs):
     wl = _wl(E=4, k=2, H=32, I=48, qt=qt, group_size=gs, act_order=act_order)
     layer = make_layer(wl, seed=17)
@@ -631,3 +632,97 @@ def test_quantize_int4_24_structure_and_round_trip(gs):
     deq = oracle.dequant_int4(q, s, None, gs)
     g = np.arange(64) // (64 if gs < 0 else gs)
     assert np.all(np.abs(deq - p) <= s[g, :].T / 2 + 1e-12)
+
+
+# ----------------------------------------------------------------------------
+# 2:4-sparse int8 and the dense linear layer
+# ("Add GPTQ Marlin 2:4 sparse structured support": 4 or 8 bits, group 128 or
+# channel-wise, dense or 2:4 sparse, a dense linear layer)
+# ----------------------------------------------------------------------------
+def test_decompress_24_int8_worked_example_and_inverse():
+    # signed codes, zero code 0: group 0 keeps channels 1 and 3, group 1 keeps 4 and 5
+    values = np.array([[-7, 127, -127, 3]], np.int8)
+    positions = np.array([[[1, 3], [0, 1]]])
+    got = oracle.decompress_24(values, positions, zero_code=0)
+    assert got.dtype == np.int8
+    np.testing.assert_array_equal(got, [[0, -7, 0, 127, -127, 3, 0, 0]])
+    rng = np.random.default_rng(9)
+    q = np.zeros((5, 32), np.int8)
+    for n in range(5):
+        for j in range(8):
+            keep = rng.choice(4, size=rng.integers(0, 3), replace=False)
+            q[n, 4 * j + keep] = rng.integers(-127, 128, size=keep.size)
+    vals = np.zeros((5, 16), np.int8)
+    pos = np.zeros((5, 8, 2), np.int64)
+    for n in range(5):
+        for j in range(8):
+            nz = [i for i in range(4) if q[n, 4 * j + i] != 0]
+            nz += [i for i in range(4) if i not in nz][:2 - len(nz)]
+            nz = sorted(nz)
+            pos[n, j] = nz
+            vals[n, 2 * j:2 * j + 2] = q[n, 4 * j + nz[0]], q[n, 4 * j + nz[1]]
+    np.testing.assert_array_equal(oracle.decompress_24(vals, pos, zero_code=0), q)
+
+
+@pytest.mark.parametrize("gs", [-1, 128])
+def test_quantize_int8_24_structure_and_round_trip(gs):
+    rng = np.random.default_rng(10)
+    w = (rng.standard_normal((12, 256)) * 0.02).astype(np.float32)
+    q, s = quantize_int8_24(w, gs, "bf16")
+    assert q.dtype == np.int8 and np.abs(q.astype(np.int32)).max() <= 127
+    assert np.all((q.reshape(12, 64, 4) != 0).sum(axis=2) <= 2)
+    wp = prune_24(w)
+    if gs < 0:
+        assert s.shape == (12,)
+        wd = oracle.dequant_int8(q, s)
+        tol = np.repeat(s[:, None], 256, axis=1)
+    else:
+        assert s.shape == (2, 12)
+        wd = oracle.dequant_int8_group(q, s, gs)
+        tol = np.repeat(s.T, gs, axis=1)
+    assert np.all(np.abs(wd - wp) <= tol * (0.5 + 1e-6))
+    assert np.all(wd[wp == 0] == 0)
+
+
+def test_linear_forward_closed_form_and_brute_force():
+    # W = diag(d) . P (a scaled permutation): out[m, n] = d[n] * x[m, pi[n]]
+    rng = np.random.default_rng(11)
+    K = 16
+    pi = rng.permutation(K)
+    d = rng.integers(-7, 8, size=K).astype(np.float64)
+    W = np.zeros((K, K))
+    W[np.arange(K), pi] = d
+    x = rng.standard_normal((3, K))
+    np.testing.assert_allclose(oracle.linear_forward(x, W), d[None, :] * x[:, pi], rtol=0, atol=1e-14)
+    # scalar loops on a quantized layer of every format, dequantized inside the dot product
+    for qt, gs, ao in [("int4", 32, True), ("int4zp", 32, False), ("int4s24", -1, False), ("int8", -1, False),
+                       ("int8g", 32, False), ("int8s24", 32, False), ("int8s24", -1, False)]:
+        lin = make_linear(8, 64, qt, gs, "bf16", act_order=ao, seed=3)
+        xs = make_linear_inputs(64, 2, "bf16", seed=4)
+        got = oracle.linear_forward(xs, oracle.dequant_linear(lin))
+        want = np.zeros((2, 8))
+        for m in range(2):
+            for n in range(8):
+                acc = 0.0
+                for k in range(64):
+                    if qt.startswith("int4"):
+                        g = int(lin.g_idx[k]) if lin.g_idx is not None else (0 if gs < 0 else k // gs)
+                        zero = 8 if lin.z is None else int(lin.z[g, n])
+                        wv = (int(lin.q[n, k]) - zero) * float(lin.s[g, n])
+                    elif lin.s.ndim == 1:
+                        wv = int(lin.q[n, k]) * float(lin.s[n])
+                    else:
+                        wv = int(lin.q[n, k]) * float(lin.s[k // gs, n])
+                    acc += float(xs[m, k]) * wv
+                want[m, n] = acc
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12, err_msg=qt)
+
+
+def test_int8_24_expert_layer_brute_force():
+    wl = _wl(E=3, k=2, H=32, I=48, qt="int8s24", group_size=-1)
+    layer = make_layer(wl, seed=19)
+    assert np.all((layer.q13.reshape(3, 96, 8, 4) != 0).sum(axis=3) <= 2)
+    inp = make_inputs(wl, 3, seed=19)
+    got = oracle.moe_forward(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    want = _brute_force(layer, inp.x, inp.topk_ids, inp.topk_weights)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)

@@ -53,11 +53,12 @@ class Bar:
         return ok
 
 
-def simulate(n_stages, NW, NB, NB2, NI, seed):
+def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
+    """DS dequant sets take stages g = s, s + DS, ... (each set's warps arrive as one)."""
     rng = random.Random(seed)
     wfull = [Bar(1) for _ in range(NW)]
-    wempty = [Bar(8) for _ in range(NW)]
-    afull = [Bar(8) for _ in range(NB)]
+    wempty = [Bar(16 // DS) for _ in range(NW)]
+    afull = [Bar(16 // DS) for _ in range(NB)]
     done = [Bar(1) for _ in range(NB2)]
     wslot = [None] * NW        # stage whose weights the slot holds
     wread = [None] * NW        # last stage whose weights were read from the slot
@@ -81,13 +82,13 @@ def simulate(n_stages, NW, NB, NB2, NI, seed):
             yield
 
     def dequant(s):
-        for g in range(s, n_stages, 2):
+        for g in range(s, n_stages, DS):
             w, a = g % NW, g % NB
             while not wfull[w].test(g // NW):
                 yield
             assert wslot[w] == g and bslot[g % NB2] == g
             wread[w] = g
-            wempty[w].arrive(8)
+            wempty[w].arrive(16 // DS)
             yield  # conversion
             if NB2 != NB:
                 gp = g - NB
@@ -95,7 +96,7 @@ def simulate(n_stages, NW, NB, NB2, NI, seed):
                     yield
             assert g < NB or (g - NB) in mma_done, "A slot rewritten before its MMAs completed"
             aslot[a] = g
-            afull[a].arrive(8)
+            afull[a].arrive(16 // DS)
             yield
 
     def issuer(i):
@@ -106,7 +107,7 @@ def simulate(n_stages, NW, NB, NB2, NI, seed):
             inflight.append(("mma", g))
             yield
 
-    agents = [producer(0), producer(1), dequant(0), dequant(1)] + [issuer(i) for i in range(NI)]
+    agents = [producer(0), producer(1)] + [dequant(s) for s in range(DS)] + [issuer(i) for i in range(NI)]
     live = list(agents)
     mma_queue = []
     steps = 0
@@ -149,6 +150,16 @@ CONFIGS = [
 def test_protocol_random_interleavings(NW, NB, NB2, NI):
     for seed in range(12):
         simulate(3 * NB2 + 2 * NW + 7, NW, NB, NB2, NI, seed)
+
+
+# four dequant sets of four full-row warps: weight ring and token-tile ring multiples of 4
+CONFIGS4 = [(16, 6, 12, 3), (12, 6, 12, 3), (8, 6, 12, 3), (12, 4, 8, 2), (8, 4, 4, 2), (12, 4, 4, 1), (8, 4, 8, 1)]
+
+
+@pytest.mark.parametrize("NW,NB,NB2,NI", CONFIGS4)
+def test_protocol_four_dequant_sets(NW, NB, NB2, NI):
+    for seed in range(12):
+        simulate(3 * NB2 + 2 * NW + 9, NW, NB, NB2, NI, seed, DS=4)
 
 
 def test_model_detects_a_missing_wait():

@@ -28,6 +28,7 @@ QMOE_INT8_PER_COL = 2
 QMOE_INT4_GROUP_ZP = 3
 QMOE_INT8_GROUP = 4
 QMOE_INT4_GROUP_24 = 5
+QMOE_INT8_24 = 6
 QMOE_F16 = 1
 QMOE_BF16 = 2
 QMOE_F32 = 3
@@ -41,15 +42,24 @@ class QmoeLayer(ctypes.Structure):
     ]
 
 
+class QmoeLinear(ctypes.Structure):
+    _fields_ = [
+        ("N", c_int32), ("K", c_int32), ("group_size", c_int32), ("qt", c_int32), ("act_dtype", c_int32),
+        ("scale_dtype", c_int32), ("w", c_void_p), ("s", c_void_p), ("perm", c_void_p),
+    ]
+
+
 class QmoePlanInfo(ctypes.Structure):
     _fields_ = [("token_tile", c_int32), ("issuers", c_int32), ("acc_bufs", c_int32), ("split1", c_int32),
                 ("split2", c_int32), ("w_stages", c_int32), ("ab_stages", c_int32), ("stage_bytes", c_int32),
-                ("workspace_bytes", c_int64), ("b_stages", c_int32), ("reserved", c_int32 * 5)]
+                ("workspace_bytes", c_int64), ("b_stages", c_int32), ("dq_sets", c_int32),
+                ("reserved", c_int32 * 4)]
 
 
 class QmoeOptions(ctypes.Structure):
     _fields_ = [("split1", c_int32), ("split2", c_int32), ("token_tile", c_int32), ("fault_injection", c_int32),
-                ("issuers", c_int32), ("token_ring", c_int32), ("reserved", c_int32 * 2)]
+                ("issuers", c_int32), ("token_ring", c_int32), ("dq_sets", c_int32),
+                ("reserved", c_int32 * 1)]
 
 
 class QmoeError(RuntimeError):
@@ -116,6 +126,19 @@ _SIGS = {
     "qmoe_forward_noalloc": (c_int32, [POINTER(QmoeLayer), c_void_p, c_int64, c_void_p, c_void_p, c_int32,
                                        c_void_p, c_void_p]),
     "qmoe_read_noalloc_status": (c_int32, [c_void_p]),
+    "qmoe_pack_int8_24": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, POINTER(c_float), c_void_p, POINTER(c_float)]),
+    "qmoe_unpack_int8_24": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_void_p, POINTER(c_float), c_void_p,
+                                      POINTER(c_float), c_void_p, c_void_p, c_void_p, c_void_p]),
+    "qmoe_pack_linear": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, POINTER(c_float), c_void_p]),
+    "qmoe_unpack_linear": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_void_p, POINTER(c_float), c_void_p,
+                                     c_void_p, c_void_p, c_void_p]),
+    "qmoe_linear_workspace_size": (c_size_t, [POINTER(QmoeLinear), c_int64, POINTER(QmoeOptions)]),
+    "qmoe_linear_describe_plan": (c_int32, [POINTER(QmoeLinear), c_int64, POINTER(QmoeOptions), c_int32,
+                                            POINTER(QmoePlanInfo)]),
+    "qmoe_linear_forward": (c_int32, [POINTER(QmoeLinear), c_void_p, c_int64, c_void_p, c_void_p, c_size_t, c_void_p,
+                                      POINTER(QmoeOptions)]),
 }
 
 

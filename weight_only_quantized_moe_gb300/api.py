@@ -15,11 +15,11 @@ from . import _native as N
 _ACT = {"f16": N.QMOE_F16, "bf16": N.QMOE_BF16}
 _TORCH_ACT = {"f16": torch.float16, "bf16": torch.bfloat16}
 _QT = {"int4": N.QMOE_INT4_GROUP, "int4zp": N.QMOE_INT4_GROUP_ZP, "int8": N.QMOE_INT8_PER_COL,
-       "int8g": N.QMOE_INT8_GROUP, "int4s24": N.QMOE_INT4_GROUP_24}
+       "int8g": N.QMOE_INT8_GROUP, "int4s24": N.QMOE_INT4_GROUP_24, "int8s24": N.QMOE_INT8_24}
 
 
 def default_group_size(qt: str) -> int:
-    return -1 if qt == "int8" else 128
+    return -1 if qt in ("int8", "int8s24") else 128
 
 
 def _np_ptr(a, ctype):
@@ -158,6 +158,84 @@ def qmoe_unpack_int4_24(E, H, I, w13, w2, group_size=128):
     return q13, s13, q2, s2
 
 
+def _float_scales(qt: str, group_size: int) -> bool:
+    """Formats whose scales are float32, one per output feature (applied to the accumulator)."""
+    return qt == "int8" or (qt == "int8s24" and group_size == -1)
+
+
+def qmoe_pack_int8_24(E, H, I, scale_dtype, q13, s13, q2, s2, group_size=-1):
+    """Pack 2:4-sparse int8: dense codes (0 at the pruned channels).  group_size -1:
+    float32 scales [E, N] (scale_dtype "f32"); 128: uint16 bit patterns [E, K/128, N]."""
+    q13 = np.ascontiguousarray(q13, np.int8)
+    q2 = np.ascontiguousarray(q2, np.int8)
+    cw = group_size == -1
+    sdt = np.float32 if cw else np.uint16
+    s13 = np.ascontiguousarray(s13, sdt)
+    s2 = np.ascontiguousarray(s2, sdt)
+    w13 = np.empty(packed_bytes("int8s24", E, 2 * I, H, group_size), np.uint8)
+    w2 = np.empty(packed_bytes("int8s24", E, H, I, group_size), np.uint8)
+    s13p = np.empty((E, 2 * I), np.float32) if cw else None
+    s2p = np.empty((E, H), np.float32) if cw else None
+    st = N.lib().qmoe_pack_int8_24(E, H, I, group_size, N.QMOE_F32 if cw else _ACT[scale_dtype],
+                                   q13.ctypes.data_as(c_void_p), s13.ctypes.data_as(c_void_p),
+                                   q2.ctypes.data_as(c_void_p), s2.ctypes.data_as(c_void_p),
+                                   w13.ctypes.data_as(c_void_p), _np_ptr(s13p, c_float), w2.ctypes.data_as(c_void_p),
+                                   _np_ptr(s2p, c_float))
+    N.check(st, "qmoe_pack_int8_24")
+    return {"w13": w13, "w2": w2, "s13": s13p, "s2": s2p}
+
+
+def qmoe_unpack_int8_24(E, H, I, w13, s13p, w2, s2p, group_size=-1):
+    """Inverse of qmoe_pack_int8_24: dense (q13, s13, q2, s2)."""
+    cw = group_size == -1
+    q13 = np.empty((E, 2 * I, H), np.int8)
+    q2 = np.empty((E, H, I), np.int8)
+    s13 = np.empty((E, 2 * I), np.float32) if cw else np.empty((E, H // 128, 2 * I), np.uint16)
+    s2 = np.empty((E, H), np.float32) if cw else np.empty((E, I // 128, H), np.uint16)
+    st = N.lib().qmoe_unpack_int8_24(E, H, I, group_size, w13.ctypes.data_as(c_void_p), _np_ptr(s13p, c_float),
+                                     w2.ctypes.data_as(c_void_p), _np_ptr(s2p, c_float), q13.ctypes.data_as(c_void_p),
+                                     s13.ctypes.data_as(c_void_p), q2.ctypes.data_as(c_void_p),
+                                     s2.ctypes.data_as(c_void_p))
+    N.check(st, "qmoe_unpack_int8_24")
+    return q13, s13, q2, s2
+
+
+def qmoe_pack_linear(qt, N_out, K, act, q, s, group_size=None, z=None, g_idx=None):
+    """Pack one [N, K] weight matrix for the dense linear layer (see include/qmoe.h).
+    int4 formats: q uint8, s float32 [K/G or 1, N] exact in ``act``; int8 group / 2:4
+    group: q int8, s float32 [K/128, N]; per-column formats: q int8, s float32 [N]."""
+    gs = default_group_size(qt) if group_size is None else group_size
+    fs = _float_scales(qt, gs)
+    qa = np.ascontiguousarray(q, np.uint8 if qt.startswith("int4") else np.int8)
+    sa = np.ascontiguousarray(s, np.float32) if fs else _scale_bits(s, act)
+    za = None if z is None else np.ascontiguousarray(z, np.uint8)
+    ga = None if g_idx is None else np.ascontiguousarray(g_idx, np.int32)
+    w = np.empty(packed_bytes(qt, 1, N_out, K, gs), np.uint8)
+    sp = np.empty(N_out, np.float32) if fs else None
+    perm = np.empty(K, np.int32) if ga is not None else None
+    st = N.lib().qmoe_pack_linear(_QT[qt], N_out, K, gs, N.QMOE_F32 if fs else _ACT[act], qa.ctypes.data_as(c_void_p),
+                                  sa.ctypes.data_as(c_void_p), _np_ptr(za, c_uint8), _np_ptr(ga, c_int32),
+                                  w.ctypes.data_as(c_void_p), _np_ptr(sp, c_float), _np_ptr(perm, c_int32))
+    N.check(st, "qmoe_pack_linear")
+    return {"w": w, "s": sp, "perm": perm}
+
+
+def qmoe_unpack_linear(qt, N_out, K, packed, group_size=None, g_idx=None):
+    """Inverse of qmoe_pack_linear: (q, s) with s as uint16 bits or float32, plus z for int4zp."""
+    gs = default_group_size(qt) if group_size is None else group_size
+    fs = _float_scales(qt, gs)
+    ng = 1 if gs < 0 else K // 128
+    q = np.empty((N_out, K), np.uint8 if qt.startswith("int4") else np.int8)
+    s = np.empty(N_out, np.float32) if fs else np.empty((ng, N_out), np.uint16)
+    z = np.empty((ng, N_out), np.uint8) if qt == "int4zp" else None
+    ga = None if g_idx is None else np.ascontiguousarray(g_idx, np.int32)
+    st = N.lib().qmoe_unpack_linear(_QT[qt], N_out, K, gs, packed["w"].ctypes.data_as(c_void_p),
+                                    _np_ptr(packed.get("s"), c_float), _np_ptr(ga, c_int32), q.ctypes.data_as(c_void_p),
+                                    s.ctypes.data_as(c_void_p), _np_ptr(z, c_uint8))
+    N.check(st, "qmoe_unpack_linear")
+    return (q, s, z) if z is not None else (q, s)
+
+
 def qmoe_pack_int8(E, H, I, q13, s13, q2, s2):
     q13 = np.ascontiguousarray(q13, np.int8)
     q2 = np.ascontiguousarray(q2, np.int8)
@@ -204,7 +282,7 @@ class DeviceLayer:
         self.w13, self.w2, self.s13, self.s2, self.perm13 = w13, w2, s13, s2, perm13
         self.struct = N.QmoeLayer(
             E, H, I, self.group_size, _QT[qt], _ACT[act],
-            N.QMOE_F32 if qt == "int8" else _ACT[act],
+            N.QMOE_F32 if _float_scales(qt, self.group_size) else _ACT[act],
             w13.data_ptr(), w2.data_ptr(),
             None if s13 is None else s13.data_ptr(), None if s2 is None else s2.data_ptr(),
             None if perm13 is None else perm13.data_ptr())
@@ -225,10 +303,12 @@ class DeviceLayer:
             if a is None:
                 return None
             return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        gs = default_group_size(qt) if group_size is None else group_size
+        fs = _float_scales(qt, gs)
         return cls(qt, E, H, I, act, dev(packed["w13"]), dev(packed["w2"]),
-                   dev(packed.get("s13")) if qt == "int8" else None,
-                   dev(packed.get("s2")) if qt == "int8" else None,
-                   dev(packed.get("perm13")), group_size)
+                   dev(packed.get("s13")) if fs else None,
+                   dev(packed.get("s2")) if fs else None,
+                   dev(packed.get("perm13")), gs)
 
     @classmethod
     def from_canonical(cls, qt, act, q13, s13, q2, s2, g13=None, g2=None, device="cuda", z13=None, z2=None,
@@ -251,6 +331,11 @@ class DeviceLayer:
             packed = qmoe_pack_int4_24(E, H, I, act, q13, _scale_bits(s13, act), q2, _scale_bits(s2, act), gs)
         elif qt == "int8g":
             packed = qmoe_pack_int8_group(E, H, I, act, q13, _scale_bits(s13, act), q2, _scale_bits(s2, act))
+        elif qt == "int8s24":
+            if gs == -1:
+                packed = qmoe_pack_int8_24(E, H, I, "f32", q13, s13, q2, s2, -1)
+            else:
+                packed = qmoe_pack_int8_24(E, H, I, act, q13, _scale_bits(s13, act), q2, _scale_bits(s2, act), gs)
         else:
             packed = qmoe_pack_int8(E, H, I, q13, s13, q2, s2)
         return cls.from_packed(qt, E, H, I, act, packed, device, gs)
@@ -259,8 +344,8 @@ class DeviceLayer:
 # ----------------------------------------------------------------------------
 # device entry points
 # ----------------------------------------------------------------------------
-def make_options(split1=0, split2=0, token_tile=0, fault_injection=0, issuers=0, token_ring=0):
-    return N.QmoeOptions(split1, split2, token_tile, fault_injection, issuers, token_ring)
+def make_options(split1=0, split2=0, token_tile=0, fault_injection=0, issuers=0, token_ring=0, dq_sets=0):
+    return N.QmoeOptions(split1, split2, token_tile, fault_injection, issuers, token_ring, dq_sets)
 
 
 def qmoe_moe_align(topk_ids: torch.Tensor, E: int, block: int, capacity: int | None = None, stream=None):
@@ -429,4 +514,66 @@ def qmoe_forward_logits(layer: DeviceLayer, x: torch.Tensor, logits: torch.Tenso
                                      _LOGIT_DT[logits.dtype], k, 1 if renormalize else 0, c_void_p(out.data_ptr()),
                                      c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
     N.check(st, "qmoe_forward_logits")
+    return out
+
+
+# ----------------------------------------------------------------------------
+# dense linear layer
+# ----------------------------------------------------------------------------
+class DeviceLinear:
+    """One packed [N, K] weight matrix on a CUDA device plus its C descriptor."""
+
+    def __init__(self, qt, N_out, K, act, w, s=None, perm=None, group_size=None):
+        self.qt, self.N, self.K, self.act = qt, N_out, K, act
+        self.group_size = default_group_size(qt) if group_size is None else group_size
+        self.w, self.s, self.perm = w, s, perm
+        self.struct = N.QmoeLinear(N_out, K, self.group_size, _QT[qt], _ACT[act],
+                                   N.QMOE_F32 if _float_scales(qt, self.group_size) else _ACT[act], w.data_ptr(),
+                                   None if s is None else s.data_ptr(), None if perm is None else perm.data_ptr())
+
+    @property
+    def torch_dtype(self):
+        return _TORCH_ACT[self.act]
+
+    @classmethod
+    def from_canonical(cls, qt, act, q, s, group_size=None, z=None, g_idx=None, device="cuda"):
+        """Pack canonical codes [N, K] and scales (see qmoe_pack_linear) and upload them."""
+        N_out, K = q.shape
+        gs = default_group_size(qt) if group_size is None else group_size
+        pk = qmoe_pack_linear(qt, N_out, K, act, q, s, gs, z, g_idx)
+
+        def dev(a):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        return cls(qt, N_out, K, act, dev(pk["w"]), dev(pk["s"]), dev(pk["perm"]), gs)
+
+
+def qmoe_linear_workspace_size(layer: DeviceLinear, M: int, opts=None) -> int:
+    n = int(N.lib().qmoe_linear_workspace_size(byref(layer.struct), M, None if opts is None else byref(opts)))
+    if n == 0:
+        raise N.QmoeError(N.QMOE_ERR_INVALID_ARG, "qmoe_linear_workspace_size")
+    return n
+
+
+def qmoe_linear_describe_plan(layer, M: int, opts=None, num_sms: int = 0) -> dict:
+    struct = layer.struct if hasattr(layer, "struct") else layer
+    info = N.QmoePlanInfo()
+    st = N.lib().qmoe_linear_describe_plan(byref(struct), M, None if opts is None else byref(opts), num_sms,
+                                           byref(info))
+    N.check(st, "qmoe_linear_describe_plan")
+    return {f: getattr(info, f) for f, _ in N.QmoePlanInfo._fields_ if f != "reserved"}
+
+
+def qmoe_linear_forward(layer: DeviceLinear, x: torch.Tensor, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, opts=None, stream=None):
+    """out[M, N] = x[M, K] . W^T on the GPU (the library's GEMM kernel)."""
+    M, K = x.shape
+    assert x.dtype == layer.torch_dtype and x.is_contiguous() and K == layer.K
+    if out is None:
+        out = torch.empty((M, layer.N), dtype=x.dtype, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(qmoe_linear_workspace_size(layer, M, opts), x.device)
+    st = N.lib().qmoe_linear_forward(byref(layer.struct), c_void_p(x.data_ptr()), M, c_void_p(out.data_ptr()),
+                                     c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream),
+                                     None if opts is None else byref(opts))
+    N.check(st, "qmoe_linear_forward")
     return out

@@ -36,6 +36,9 @@ SOURCES = [
     "gemm_i8.cu",
     "gemm_i8g_f16.cu",
     "gemm_i8g_bf16.cu",
+    "gemm_i8s.cu",
+    "gemm_i8sg_f16.cu",
+    "gemm_i8sg_bf16.cu",
     "noalloc.cu",
 ]
 

@@ -76,57 +76,76 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ---------------------------------------------------------------------------
 // layer validation and the forward plan
 // ---------------------------------------------------------------------------
-int stage_bytes_of(int32_t qt) {
+int stage_bytes_of(int32_t qt, int32_t gs) {
   switch (qt) {
     case QMOE_INT4_GROUP: return kInt4StageBytes;
     case QMOE_INT4_GROUP_ZP: return kInt4ZpStageBytes;
     case QMOE_INT8_GROUP: return kInt8GroupStageBytes;
     case QMOE_INT4_GROUP_24: return kInt4SparseStageBytes;
+    case QMOE_INT8_24: return gs == -1 ? kInt8SparseStageBytes : kInt8SparseGroupStageBytes;
     default: return kInt8StageBytes;
   }
 }
 
-QuantKind kind_of(int32_t qt) {
+QuantKind kind_of(int32_t qt, int32_t gs) {
   switch (qt) {
     case QMOE_INT4_GROUP: return kQ4;
     case QMOE_INT4_GROUP_ZP: return kQ4Z;
     case QMOE_INT8_GROUP: return kQ8G;
     case QMOE_INT4_GROUP_24: return kQ4S;
+    case QMOE_INT8_24: return gs == -1 ? kQ8S : kQ8SG;
     default: return kQ8;
   }
 }
 
-qmoe_status validate_layer_dims(const qmoe_layer* L) {
-  if (L == nullptr) return QMOE_ERR_INVALID_ARG;
-  if (L->E < 1 || L->E > 1024 || L->H <= 0 || L->I <= 0) return QMOE_ERR_INVALID_ARG;
-  if (L->H % 128 != 0 || L->I % 128 != 0) return QMOE_ERR_UNSUPPORTED;
-  if (L->act_dtype != QMOE_F16 && L->act_dtype != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
-  if (L->qt == QMOE_INT4_GROUP || L->qt == QMOE_INT4_GROUP_ZP) {
-    if (L->group_size != 128 && L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
-    if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
-    if (L->group_size == -1 && L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
-  } else if (L->qt == QMOE_INT4_GROUP_24) {
-    if (L->group_size != 128 && L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
-    if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
-    if (L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
-  } else if (L->qt == QMOE_INT8_GROUP) {
-    if (L->group_size != 128) return QMOE_ERR_UNSUPPORTED;
-    if (L->scale_dtype != L->act_dtype) return QMOE_ERR_UNSUPPORTED;
-    if (L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
-  } else if (L->qt == QMOE_INT8_PER_COL) {
-    if (L->group_size != -1) return QMOE_ERR_UNSUPPORTED;
-    if (L->scale_dtype != QMOE_F32) return QMOE_ERR_UNSUPPORTED;
-    if (L->perm13 != nullptr) return QMOE_ERR_UNSUPPORTED;
+// Formats whose scales are one float32 per output feature, outside the packed blocks
+// (applied to the accumulator in the GEMM epilogue).
+bool has_row_scales(int32_t qt, int32_t gs) {
+  return qt == QMOE_INT8_PER_COL || (qt == QMOE_INT8_24 && gs == -1);
+}
+
+// Format, group size, scale type and act-order checks shared by the MoE layer
+// and the dense linear layer.
+qmoe_status validate_format(int32_t qt, int32_t gs, int32_t act, int32_t sdt, bool has_perm) {
+  if (act != QMOE_F16 && act != QMOE_BF16) return QMOE_ERR_UNSUPPORTED;
+  if (qt == QMOE_INT4_GROUP || qt == QMOE_INT4_GROUP_ZP) {
+    if (gs != 128 && gs != -1) return QMOE_ERR_UNSUPPORTED;
+    if (sdt != act) return QMOE_ERR_UNSUPPORTED;
+    if (gs == -1 && has_perm) return QMOE_ERR_UNSUPPORTED;
+  } else if (qt == QMOE_INT4_GROUP_24) {
+    if (gs != 128 && gs != -1) return QMOE_ERR_UNSUPPORTED;
+    if (sdt != act) return QMOE_ERR_UNSUPPORTED;
+    if (has_perm) return QMOE_ERR_UNSUPPORTED;
+  } else if (qt == QMOE_INT8_GROUP) {
+    if (gs != 128) return QMOE_ERR_UNSUPPORTED;
+    if (sdt != act) return QMOE_ERR_UNSUPPORTED;
+    if (has_perm) return QMOE_ERR_UNSUPPORTED;
+  } else if (qt == QMOE_INT8_PER_COL) {
+    if (gs != -1) return QMOE_ERR_UNSUPPORTED;
+    if (sdt != QMOE_F32) return QMOE_ERR_UNSUPPORTED;
+    if (has_perm) return QMOE_ERR_UNSUPPORTED;
+  } else if (qt == QMOE_INT8_24) {
+    if (gs != 128 && gs != -1) return QMOE_ERR_UNSUPPORTED;
+    if (sdt != (gs == -1 ? QMOE_F32 : act)) return QMOE_ERR_UNSUPPORTED;
+    if (has_perm) return QMOE_ERR_UNSUPPORTED;
   } else {
     return QMOE_ERR_INVALID_ARG;
   }
   return QMOE_OK;
 }
 
+qmoe_status validate_layer_dims(const qmoe_layer* L) {
+  if (L == nullptr) return QMOE_ERR_INVALID_ARG;
+  if (L->E < 1 || L->E > 1024 || L->H <= 0 || L->I <= 0) return QMOE_ERR_INVALID_ARG;
+  if (L->H % 128 != 0 || L->I % 128 != 0) return QMOE_ERR_UNSUPPORTED;
+  return validate_format(L->qt, L->group_size, L->act_dtype, L->scale_dtype, L->perm13 != nullptr);
+}
+
 struct Plan {
   int64_t M = 0, P = 0;
   int k = 0;
   int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0, b_stages = 0;
+  int dq_sets = 2;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -159,6 +178,78 @@ int choose_split(int64_t n_items, int k_stages, int C, double epi, double reduce
   return best_cost < base * must_gain ? best : 1;
 }
 
+// Issuers, TMEM accumulators and ring depths of the GEMM for the token tile
+// p->T and the packed block size p->stage_bytes (shared by the MoE layer and the
+// dense linear layer).
+qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
+  // MMA issuers (stage g to issuer g mod n, one accumulator each): one thread
+  // issues a tcgen05.mma about every 86 cycles whatever its N, so small token
+  // tiles take three; a 128-row tile keeps the tensor pipe busy from one
+  // thread, which leaves TMEM for two accumulator buffers so the epilogue
+  // overlaps the next item's MMAs.
+  const int T = p->T;
+  p->issuers = (T <= 32) ? 3 : (T <= 64) ? 2 : 1;
+  if (o != nullptr && o->issuers != 0) {
+    if (o->issuers < 1 || o->issuers > 3) return QMOE_ERR_INVALID_ARG;
+    p->issuers = o->issuers;
+  }
+  // Ring sizes are multiples of every role's stride (2 for the producers and
+  // dequant sets, the issuer count for the issuers): each slot then belongs to
+  // one role of each kind, and each waiter sees every phase of its barriers.
+  // (Otherwise a role would see only some uses of a slot and a parity wait
+  // could pass on a phase two behind.)
+  const int ring_mult = (p->issuers == 3) ? 6 : 2;
+  // TMEM (512 columns): accumulators (issuers x buffers x T columns), then the
+  // 64-column A slots paired with the token-tile ring (at most 8)
+  auto a_slots = [&](int accb) {
+    const int n = std::min(8, (512 - p->issuers * accb * T) / 64);
+    return n / ring_mult * ring_mult;
+  };
+  p->acc_bufs = a_slots(2) >= ring_mult ? 2 : 1;
+  p->a_col0 = p->issuers * p->acc_bufs * T;
+  p->ab_stages = a_slots(p->acc_bufs);
+  if (p->ab_stages < ring_mult) return (o != nullptr && o->issuers != 0) ? QMOE_ERR_INVALID_ARG : QMOE_ERR_UNSUPPORTED;
+  // Token-tile ring: a multiple m of the A ring, so that a token tile can be
+  // fetched up to m - 1 A-ring laps before its MMAs and its L2 latency stays
+  // off the A slots' cycle.  The deepest m <= 2 that leaves the weight ring at
+  // least 8 slots (weights stream from HBM and want the deeper ring).
+  const size_t wslot = (static_cast<size_t>(p->stage_bytes) + 1023) & ~size_t(1023);
+  auto w_depth = [&](int nb2) {
+    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256;
+    if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
+    return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
+  };
+  int ring_m = 1;
+  if (o != nullptr && o->token_ring != 0) {
+    if (o->token_ring < 1 || o->token_ring > 3) return QMOE_ERR_INVALID_ARG;
+    ring_m = o->token_ring;
+    if (w_depth(ring_m * p->ab_stages) < 2) return QMOE_ERR_INVALID_ARG;
+  } else {
+    for (int m = 2; m > 1; --m)
+      if (w_depth(m * p->ab_stages) >= 8) {
+        ring_m = m;
+        break;
+      }
+  }
+  p->b_stages = ring_m * p->ab_stages;
+  p->w_stages = w_depth(p->b_stages);
+  if (p->w_stages < 2 || p->ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
+  // Dequant sets: 2 sets of 8 warps (each converts half of a stage row for its
+  // 32 rows) or 4 sets of 4 warps (each converts whole rows).  A set takes every
+  // DS-th stage, so the weight ring and the token-tile ring must be multiples of
+  // DS for each slot's barriers to belong to one set.
+  p->dq_sets = 2;
+  if (o != nullptr && o->dq_sets != 0) {
+    if (o->dq_sets != 2 && o->dq_sets != 4) return QMOE_ERR_INVALID_ARG;
+    p->dq_sets = o->dq_sets;
+  }
+  if (p->dq_sets == 4) {
+    p->w_stages &= ~3;
+    if (p->w_stages < 4 || p->b_stages % 4 != 0) return QMOE_ERR_INVALID_ARG;
+  }
+  return QMOE_OK;
+}
+
 qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_options* o, int sms, Plan* pl) {
   qmoe_status st = validate_layer_dims(L);
   if (st != QMOE_OK) return st;
@@ -180,62 +271,12 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     T = o->token_tile;
   }
   p.T = T;
-  p.stage_bytes = stage_bytes_of(L->qt);
+  p.stage_bytes = stage_bytes_of(L->qt, L->group_size);
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
-  // MMA issuers (stage g to issuer g mod n, one accumulator each): one thread
-  // issues a tcgen05.mma about every 86 cycles whatever its N, so small token
-  // tiles take three; a 128-row tile keeps the tensor pipe busy from one
-  // thread, which leaves TMEM for two accumulator buffers so the epilogue
-  // overlaps the next item's MMAs.
-  p.issuers = (T <= 32) ? 3 : (T <= 64) ? 2 : 1;
-  if (o != nullptr && o->issuers != 0) {
-    if (o->issuers < 1 || o->issuers > 3) return QMOE_ERR_INVALID_ARG;
-    p.issuers = o->issuers;
-  }
-  // Ring sizes are multiples of every role's stride (2 for the producers and
-  // dequant sets, the issuer count for the issuers): each slot then belongs to
-  // one role of each kind, and each waiter sees every phase of its barriers.
-  // (Otherwise a role would see only some uses of a slot and a parity wait
-  // could pass on a phase two behind.)
-  const int ring_mult = (p.issuers == 3) ? 6 : 2;
-  // TMEM (512 columns): accumulators (issuers x buffers x T columns), then the
-  // 64-column A slots paired with the token-tile ring (at most 8)
-  auto a_slots = [&](int accb) {
-    const int n = std::min(8, (512 - p.issuers * accb * T) / 64);
-    return n / ring_mult * ring_mult;
-  };
-  p.acc_bufs = a_slots(2) >= ring_mult ? 2 : 1;
-  p.a_col0 = p.issuers * p.acc_bufs * T;
-  p.ab_stages = a_slots(p.acc_bufs);
-  if (p.ab_stages < ring_mult) return (o != nullptr && o->issuers != 0) ? QMOE_ERR_INVALID_ARG : QMOE_ERR_UNSUPPORTED;
-  // Token-tile ring: a multiple m of the A ring, so that a token tile can be
-  // fetched up to m - 1 A-ring laps before its MMAs and its L2 latency stays
-  // off the A slots' cycle.  The deepest m <= 2 that leaves the weight ring at
-  // least 8 slots (weights stream from HBM and want the deeper ring).
-  const size_t wslot = (static_cast<size_t>(p.stage_bytes) + 1023) & ~size_t(1023);
-  auto w_depth = [&](int nb2) {
-    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256;
-    if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
-    return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
-  };
-  int ring_m = 1;
-  if (o != nullptr && o->token_ring != 0) {
-    if (o->token_ring < 1 || o->token_ring > 3) return QMOE_ERR_INVALID_ARG;
-    ring_m = o->token_ring;
-    if (w_depth(ring_m * p.ab_stages) < 2) return QMOE_ERR_INVALID_ARG;
-  } else {
-    for (int m = 2; m > 1; --m)
-      if (w_depth(m * p.ab_stages) >= 8) {
-        ring_m = m;
-        break;
-      }
-  }
-  p.b_stages = ring_m * p.ab_stages;
-  p.w_stages = w_depth(p.b_stages);
-  if (p.w_stages < 2 || p.ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
+  if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
   // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
   p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
   p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
@@ -300,7 +341,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   for (const void* p : ptrs)
     if ((st = check_dev_ptr(p, dev)) != QMOE_OK) return st;
   // only per-column int8 keeps its scales outside the packed weight blocks
-  const bool row_scales = L->qt == QMOE_INT8_PER_COL;
+  const bool row_scales = has_row_scales(L->qt, L->group_size);
   if (row_scales) {
     if ((st = check_dev_ptr(L->s13, dev)) != QMOE_OK) return st;
     if ((st = check_dev_ptr(L->s2, dev)) != QMOE_OK) return st;
@@ -368,6 +409,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.w_stages = pl.w_stages;
   g1.ab_stages = pl.ab_stages;
   g1.b_stages = pl.b_stages;
+  g1.dq_sets = pl.dq_sets;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -405,7 +447,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
-    err = launch_gemm(kind_of(L->qt), bf16, g1, grid1, stream);  // in-block scales have the activation dtype
+    err = launch_gemm(kind_of(L->qt, L->group_size), bf16, g1, grid1, stream);  // in-block scales have the activation dtype
     launched += (err == cudaSuccess);
   }
   rec(5);
@@ -423,7 +465,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(9);
   rec(10);
   if (err == cudaSuccess) {
-    err = launch_gemm(kind_of(L->qt), bf16, g2, grid2, stream);
+    err = launch_gemm(kind_of(L->qt, L->group_size), bf16, g2, grid2, stream);
     launched += (err == cudaSuccess);
   }
   rec(11);
@@ -434,6 +476,158 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   }
   rec(13);
   if (n_launches != nullptr) *n_launches = launched;
+  return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// dense linear layer: out[M, N] = x[M, K] . W^T with W [N, K] weight-only
+// quantized in any of the packed formats (one GEMM, no routing, no SiLU)
+// ---------------------------------------------------------------------------
+struct LinearPlan {
+  Plan g;            // token tile, issuers, rings (n_tiles1 / kst1 / S1 describe the one GEMM)
+  int64_t M = 0;
+  size_t off_status = 0, off_sorted = 0, off_expert = 0, off_scalars = 0, off_chunks = 0, off_xg = 0,
+         off_xscale = 0, off_h = 0, total = 0;
+};
+
+qmoe_status validate_linear(const qmoe_linear* L) {
+  if (L == nullptr) return QMOE_ERR_INVALID_ARG;
+  if (L->N <= 0 || L->K <= 0) return QMOE_ERR_INVALID_ARG;
+  if (L->N % 128 != 0 || L->K % 128 != 0) return QMOE_ERR_UNSUPPORTED;
+  return validate_format(L->qt, L->group_size, L->act_dtype, L->scale_dtype, L->perm != nullptr);
+}
+
+qmoe_status make_linear_plan(const qmoe_linear* L, int64_t M, const qmoe_options* o, int sms, LinearPlan* lp) {
+  qmoe_status st = validate_linear(L);
+  if (st != QMOE_OK) return st;
+  if (M < 0) return QMOE_ERR_INVALID_ARG;
+  if (M >= (int64_t(1) << 31) - kAlignBlock) return QMOE_ERR_UNSUPPORTED;
+  LinearPlan q;
+  Plan& p = q.g;
+  q.M = M;
+  p.M = M;
+  p.k = 1;
+  p.P = M;
+  // token tile: the power of two from 16 to 128 that holds all M rows, else 128
+  int T = 16;
+  while (T < 128 && T < M) T *= 2;
+  if (o != nullptr && o->token_tile != 0) {
+    if (o->token_tile < 16 || o->token_tile > kMaxTokenTile || o->token_tile % 16 != 0) return QMOE_ERR_INVALID_ARG;
+    T = o->token_tile;
+  }
+  p.T = T;
+  p.stage_bytes = stage_bytes_of(L->qt, L->group_size);
+  p.n_tiles1 = L->N / kTileRows;
+  p.kst1 = L->K / kStageK;
+  if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
+  p.cap = (M + kAlignBlock - 1 + 15) / 16 * 16;
+  p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
+  p.max_chunks = (p.cap + T - 1) / T + 1;
+  const int64_t chunks = std::max<int64_t>(1, (M + T - 1) / T);
+  const double epi = 4.0 + T / 8.0;
+  p.S1 = choose_split(chunks * p.n_tiles1, p.kst1, sms, epi, 2.0 + 8.0 * M * L->N / 1.3e6, 0.9);
+  if (o != nullptr && o->split1 != 0) {
+    if (o->split1 < 1 || o->split1 > 64 || o->split1 > p.kst1) return QMOE_ERR_INVALID_ARG;
+    p.S1 = o->split1;
+  }
+  size_t off = 0;
+  q.off_status = off;   off += 256;
+  q.off_sorted = off;   off += al256(p.cap * 4);
+  q.off_expert = off;   off += al256(p.nblocks * 4);
+  q.off_scalars = off;  off += 256;
+  q.off_chunks = off;   off += al256(p.max_chunks * sizeof(Chunk));
+  q.off_xg = off;       off += al256(static_cast<size_t>(p.cap) * L->K * 2);
+  q.off_xscale = off;   off += al256(static_cast<size_t>(p.cap) * 4);
+  q.off_h = off;        off += (p.S1 > 1) ? al256(static_cast<size_t>(p.S1) * p.cap * L->N * 4) : 0;
+  q.total = off;
+  *lp = q;
+  return QMOE_OK;
+}
+
+qmoe_status linear_forward_impl(const qmoe_linear* L, const void* x, int64_t M, void* out, void* ws, size_t ws_bytes,
+                                cudaStream_t stream, const qmoe_options* opts) {
+  const int sms = current_sm_count();
+  LinearPlan lp;
+  qmoe_status st = make_linear_plan(L, M, opts, sms, &lp);
+  if (st != QMOE_OK) return st;
+  if (M == 0) return QMOE_OK;
+  if (ws == nullptr || ws_bytes < lp.total) return QMOE_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QMOE_ERR_CUDA;
+  }
+  const void* ptrs[] = {x, out, ws, L->w};
+  for (const void* p : ptrs)
+    if ((st = check_dev_ptr(p, dev)) != QMOE_OK) return st;
+  const bool row_scales = has_row_scales(L->qt, L->group_size);
+  if (row_scales && (st = check_dev_ptr(L->s, dev)) != QMOE_OK) return st;
+  if (L->perm != nullptr && (st = check_dev_ptr(L->perm, dev)) != QMOE_OK) return st;
+  if (!aligned(x, 256) || !aligned(out, 256) || !aligned(ws, 256) || !aligned(L->w, 256) ||
+      (L->perm != nullptr && !aligned(L->perm, 16)) || (row_scales && !aligned(L->s, 16)))
+    return QMOE_ERR_INVALID_ARG;
+  const Plan& pl = lp.g;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(base + lp.off_status);
+  int32_t* sorted = reinterpret_cast<int32_t*>(base + lp.off_sorted);
+  int32_t* expert = reinterpret_cast<int32_t*>(base + lp.off_expert);
+  int32_t* npp = reinterpret_cast<int32_t*>(base + lp.off_scalars);
+  int32_t* nch = npp + 1;
+  Chunk* chunks = reinterpret_cast<Chunk*>(base + lp.off_chunks);
+  void* xg = base + lp.off_xg;
+  float* xscale = reinterpret_cast<float*>(base + lp.off_xscale);
+  float* h = reinterpret_cast<float*>(base + lp.off_h);
+  const bool bf16 = L->act_dtype == QMOE_BF16;
+  const int P = static_cast<int>(M);
+  // every row is "expert 0": the align kernel lays out rows 0..M-1 and the chunk table
+  cudaError_t err = launch_align(nullptr, P, 1, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status,
+                                 stream);
+  if (err == cudaSuccess)
+    err = launch_gather(x, bf16, sorted, expert, npp, L->perm, P, 1, L->K, kAlignBlock, pl.cap, xg, xscale, sms,
+                        stream);
+  GemmParams g{};
+  g.w = static_cast<const uint8_t*>(L->w);
+  g.b = static_cast<const uint8_t*>(xg);
+  g.b_unit_stride = pl.cap * 256;
+  g.row_scale = row_scales ? L->s : nullptr;
+  g.col_scale = xscale;
+  g.chunks = chunks;
+  g.n_chunks = nch;
+  g.sorted_ids = sorted;
+  g.topk_w = nullptr;
+  g.status = status;
+  g.n_tiles = pl.n_tiles1;
+  g.k_groups = pl.kst1;
+  g.split = pl.S1;
+  g.token_tile = pl.T;
+  g.acc_bufs = pl.acc_bufs;
+  g.a_col0 = pl.a_col0;
+  g.issuers = pl.issuers;
+  g.w_stages = pl.w_stages;
+  g.ab_stages = pl.ab_stages;
+  g.b_stages = pl.b_stages;
+  g.dq_sets = pl.dq_sets;
+  g.fault_injection = 0;
+  g.stage_bytes = pl.stage_bytes;
+  g.P = P;
+  g.chunk_group = 8;
+  g.inter_ld = 0;
+  g.out_bf16 = bf16 ? 1 : 0;
+  if (pl.S1 == 1) {
+    g.epi_mode = kEpiLinearOut;
+    g.out = out;
+    g.out_ld = L->N;
+    g.out_split_stride = 0;
+  } else {
+    g.epi_mode = kEpiPartialRows;
+    g.out = h;
+    g.out_ld = L->N;
+    g.out_split_stride = pl.cap * static_cast<int64_t>(L->N);
+  }
+  const int64_t items = pl.max_chunks * pl.n_tiles1 * pl.S1;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, items));
+  if (err == cudaSuccess) err = launch_gemm(kind_of(L->qt, L->group_size), bf16, g, grid, stream);
+  if (err == cudaSuccess && pl.S1 > 1) err = launch_linear_reduce(h, pl.S1, pl.cap, M, L->N, bf16, out, sms, stream);
   return err == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
 
@@ -676,6 +870,83 @@ void unpack_int8_matrix(const uint8_t* in, bool grouped, int rows, int K, int I_
     }
 }
 
+// 2:4-sparse int8 tile stage: kept codes [half][row][32 B], positions
+// [half][row][8 B] at 8192, then (with group scales) 128 x 2 B scales at 10240.
+// Half h covers K = 64h .. 64h+63, 16 groups of 4 channels; byte 2g + v of a
+// row's 32 code bytes is kept code v of group g.  Positions: nibble g
+// (little-endian over the 8 bytes) is i0 | i1 << 2, i0 < i1 the kept channels.
+// The kept channels are those with a non-zero code, padded with the lowest
+// remaining channels; more than 2 non-zero codes, or a code of -128, sets `bad`.
+void pack_int8_24_matrix(const int8_t* q, const uint16_t* s, int rows, int K, int I_for_w13, uint8_t* out,
+                         std::atomic<bool>& bad) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  const size_t blk_bytes = s ? kInt8SparseGroupStageBytes : kInt8SparseStageBytes;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      uint8_t* blk = out + (static_cast<size_t>(t) * kst + ks) * blk_bytes;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
+        const int8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
+        for (int h = 0; h < 2; ++h) {
+          uint64_t pos = 0;
+          uint8_t* vdst = blk + (h * 128 + r) * 32;
+          for (int g = 0; g < 16; ++g) {
+            const int8_t* c4 = qrow + 64 * h + 4 * g;
+            int keep[4], n = 0;
+            for (int i = 0; i < 4; ++i) {
+              if (c4[i] == -128) bad = true;
+              if (c4[i] != 0) {
+                if (n == 2) bad = true;
+                else keep[n++] = i;
+              }
+            }
+            for (int i = 0; i < 4 && n < 2; ++i)
+              if (c4[i] == 0 && (n == 0 || keep[0] != i)) keep[n++] = i;
+            if (keep[0] > keep[1]) std::swap(keep[0], keep[1]);
+            vdst[2 * g] = static_cast<uint8_t>(c4[keep[0]]);
+            vdst[2 * g + 1] = static_cast<uint8_t>(c4[keep[1]]);
+            pos |= static_cast<uint64_t>(keep[0] | (keep[1] << 2)) << (4 * g);
+          }
+          uint8_t* pdst = blk + 8192 + (h * 128 + r) * 8;
+          for (int b = 0; b < 8; ++b) pdst[b] = static_cast<uint8_t>(pos >> (8 * b));
+        }
+        if (s) {
+          const uint16_t sb = s[static_cast<size_t>(ks) * rows + cr];
+          blk[10240 + r * 2] = sb & 0xFF;
+          blk[10240 + r * 2 + 1] = sb >> 8;
+        }
+      }
+    }
+}
+
+void unpack_int8_24_matrix(const uint8_t* in, bool grouped, int rows, int K, int I_for_w13, int8_t* q, uint16_t* s) {
+  const int n_tiles = rows / 128, kst = K / 128;
+  const size_t blk_bytes = grouped ? kInt8SparseGroupStageBytes : kInt8SparseStageBytes;
+  for (int t = 0; t < n_tiles; ++t)
+    for (int ks = 0; ks < kst; ++ks) {
+      const uint8_t* blk = in + (static_cast<size_t>(t) * kst + ks) * blk_bytes;
+      for (int r = 0; r < 128; ++r) {
+        const int cr = I_for_w13 > 0 ? w13_canon_row(t, r, I_for_w13, nullptr) : t * 128 + r;
+        int8_t* qrow = q + static_cast<size_t>(cr) * K + ks * 128;
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t* vsrc = blk + (h * 128 + r) * 32;
+          const uint8_t* psrc = blk + 8192 + (h * 128 + r) * 8;
+          uint64_t pos = 0;
+          for (int b = 0; b < 8; ++b) pos |= static_cast<uint64_t>(psrc[b]) << (8 * b);
+          for (int g = 0; g < 16; ++g) {
+            const int p = static_cast<int>((pos >> (4 * g)) & 15);
+            int8_t* c4 = qrow + 64 * h + 4 * g;
+            for (int x = 0; x < 4; ++x) c4[x] = 0;
+            c4[p & 3] = static_cast<int8_t>(vsrc[2 * g]);
+            c4[p >> 2] = static_cast<int8_t>(vsrc[2 * g + 1]);
+          }
+        }
+        if (grouped && s)
+          s[static_cast<size_t>(ks) * rows + cr] = static_cast<uint16_t>(blk[10240 + r * 2] | (blk[10240 + r * 2 + 1] << 8));
+      }
+    }
+}
+
 bool pack_dims_ok(int32_t E, int32_t H, int32_t I) {
   return E >= 1 && E <= 1024 && H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0;
 }
@@ -719,6 +990,8 @@ size_t qmoe_packed_bytes(qmoe_quant_type qt, int32_t E, int32_t rows, int32_t K,
   if (qt == QMOE_INT8_PER_COL && group_size == -1) return tiles * kInt8StageBytes;
   if (qt == QMOE_INT8_GROUP && group_size == 128) return tiles * kInt8GroupStageBytes;
   if (qt == QMOE_INT4_GROUP_24 && g128_or_cw) return tiles * kInt4SparseStageBytes;
+  if (qt == QMOE_INT8_24 && group_size == -1) return tiles * kInt8SparseStageBytes;
+  if (qt == QMOE_INT8_24 && group_size == 128) return tiles * kInt8SparseGroupStageBytes;
   return 0;
 }
 
@@ -979,6 +1252,7 @@ qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k
   info->w_stages = pl.w_stages;
   info->ab_stages = pl.ab_stages;
   info->b_stages = pl.b_stages;
+  info->dq_sets = pl.dq_sets;
   info->stage_bytes = pl.stage_bytes;
   info->workspace_bytes = static_cast<int64_t>(pl.total);
   return QMOE_OK;
@@ -1101,6 +1375,178 @@ qmoe_status qmoe_forward_logits(const qmoe_layer* layer, const void* x, int64_t 
   qmoe_status st = qmoe_route_topk(logits, logits_dtype, M, layer->E, top_k, renormalize, ids, wts, stream);
   if (st != QMOE_OK) return st;
   return forward_impl(layer, x, M, ids, wts, top_k, out, workspace, w, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+qmoe_status qmoe_pack_int8_24(int32_t E, int32_t H, int32_t I, int32_t group_size, qmoe_dtype scale_dtype,
+                              const int8_t* q13, const void* s13, const int8_t* q2, const void* s2, void* w13_packed,
+                              float* s13_packed, void* w2_packed, float* s2_packed) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128 && group_size != -1) return QMOE_ERR_UNSUPPORTED;
+  const bool cw = group_size == -1;
+  if (cw ? scale_dtype != QMOE_F32 : (scale_dtype != QMOE_F16 && scale_dtype != QMOE_BF16)) return QMOE_ERR_UNSUPPORTED;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed || (cw && (!s13_packed || !s2_packed)))
+    return QMOE_ERR_INVALID_ARG;
+  std::atomic<bool> bad{false};
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT8_24, 1, 2 * I, H, group_size);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT8_24, 1, H, I, group_size);
+  const uint16_t* g13 = cw ? nullptr : static_cast<const uint16_t*>(s13);
+  const uint16_t* g2 = cw ? nullptr : static_cast<const uint16_t*>(s2);
+  parallel_for(E, [&](int64_t e) {
+    pack_int8_24_matrix(q13 + static_cast<size_t>(e) * 2 * I * H, g13 ? g13 + static_cast<size_t>(e) * (H / 128) * 2 * I : nullptr,
+                        2 * I, H, I, static_cast<uint8_t*>(w13_packed) + e * b13, bad);
+    pack_int8_24_matrix(q2 + static_cast<size_t>(e) * H * I, g2 ? g2 + static_cast<size_t>(e) * (I / 128) * H : nullptr, H,
+                        I, 0, static_cast<uint8_t*>(w2_packed) + e * b2, bad);
+    if (cw) {
+      const float* f13 = static_cast<const float*>(s13);
+      for (int t = 0; t < 2 * I / 128; ++t)
+        for (int r = 0; r < 128; ++r)
+          s13_packed[static_cast<size_t>(e) * 2 * I + t * 128 + r] = f13[static_cast<size_t>(e) * 2 * I + w13_canon_row(t, r, I, nullptr)];
+      std::memcpy(s2_packed + static_cast<size_t>(e) * H, static_cast<const float*>(s2) + static_cast<size_t>(e) * H,
+                  sizeof(float) * H);
+    }
+  });
+  return bad ? QMOE_ERR_INVALID_ARG : QMOE_OK;
+}
+
+qmoe_status qmoe_unpack_int8_24(int32_t E, int32_t H, int32_t I, int32_t group_size, const void* w13_packed,
+                                const float* s13_packed, const void* w2_packed, const float* s2_packed, int8_t* q13,
+                                void* s13, int8_t* q2, void* s2) {
+  if (!pack_dims_ok(E, H, I)) return QMOE_ERR_INVALID_ARG;
+  if (group_size != 128 && group_size != -1) return QMOE_ERR_UNSUPPORTED;
+  const bool cw = group_size == -1;
+  if (!q13 || !s13 || !q2 || !s2 || !w13_packed || !w2_packed || (cw && (!s13_packed || !s2_packed)))
+    return QMOE_ERR_INVALID_ARG;
+  const size_t b13 = qmoe_packed_bytes(QMOE_INT8_24, 1, 2 * I, H, group_size);
+  const size_t b2 = qmoe_packed_bytes(QMOE_INT8_24, 1, H, I, group_size);
+  parallel_for(E, [&](int64_t e) {
+    unpack_int8_24_matrix(static_cast<const uint8_t*>(w13_packed) + e * b13, !cw, 2 * I, H, I,
+                          q13 + static_cast<size_t>(e) * 2 * I * H,
+                          cw ? nullptr : static_cast<uint16_t*>(s13) + static_cast<size_t>(e) * (H / 128) * 2 * I);
+    unpack_int8_24_matrix(static_cast<const uint8_t*>(w2_packed) + e * b2, !cw, H, I, 0,
+                          q2 + static_cast<size_t>(e) * H * I,
+                          cw ? nullptr : static_cast<uint16_t*>(s2) + static_cast<size_t>(e) * (I / 128) * H);
+    if (cw) {
+      float* f13 = static_cast<float*>(s13);
+      for (int t = 0; t < 2 * I / 128; ++t)
+        for (int r = 0; r < 128; ++r)
+          f13[static_cast<size_t>(e) * 2 * I + w13_canon_row(t, r, I, nullptr)] = s13_packed[static_cast<size_t>(e) * 2 * I + t * 128 + r];
+      std::memcpy(static_cast<float*>(s2) + static_cast<size_t>(e) * H, s2_packed + static_cast<size_t>(e) * H,
+                  sizeof(float) * H);
+    }
+  });
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_pack_linear(qmoe_quant_type qt, int32_t N, int32_t K, int32_t group_size, qmoe_dtype scale_dtype,
+                             const void* q, const void* s, const uint8_t* z, const int32_t* g_idx, void* w_packed,
+                             float* s_packed, int32_t* perm_out) {
+  if (N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return QMOE_ERR_INVALID_ARG;
+  if (qmoe_packed_bytes(qt, 1, N, K, group_size) == 0) return QMOE_ERR_UNSUPPORTED;
+  if (!q || !s || !w_packed) return QMOE_ERR_INVALID_ARG;
+  const bool act_ok = scale_dtype == QMOE_F16 || scale_dtype == QMOE_BF16;
+  const bool row_scales = has_row_scales(qt, group_size);
+  if (row_scales ? scale_dtype != QMOE_F32 : !act_ok) return QMOE_ERR_UNSUPPORTED;
+  if (row_scales && !s_packed) return QMOE_ERR_INVALID_ARG;
+  if ((z != nullptr) != (qt == QMOE_INT4_GROUP_ZP)) return QMOE_ERR_INVALID_ARG;
+  const bool int4_any = qt == QMOE_INT4_GROUP || qt == QMOE_INT4_GROUP_ZP;
+  if (g_idx && (!int4_any || group_size != 128)) return QMOE_ERR_UNSUPPORTED;
+  if (g_idx && !perm_out) return QMOE_ERR_INVALID_ARG;
+  std::atomic<bool> bad{false};
+  std::vector<int32_t> perm;
+  if (g_idx) {
+    if (!sorted_by_group(g_idx, K, perm)) return QMOE_ERR_UNSUPPORTED;
+    std::memcpy(perm_out, perm.data(), sizeof(int32_t) * K);
+  }
+  uint8_t* out = static_cast<uint8_t*>(w_packed);
+  const bool cw = group_size == -1;
+  switch (qt) {
+    case QMOE_INT4_GROUP:
+    case QMOE_INT4_GROUP_ZP:
+      pack_int4_matrix(static_cast<const uint8_t*>(q), static_cast<const uint16_t*>(s), z, cw, N, K, 0, nullptr,
+                       g_idx ? perm.data() : nullptr, out, bad);
+      break;
+    case QMOE_INT4_GROUP_24:
+      pack_int4_24_matrix(static_cast<const uint8_t*>(q), static_cast<const uint16_t*>(s), cw, N, K, 0, out, bad);
+      break;
+    case QMOE_INT8_GROUP:
+      pack_int8_matrix(static_cast<const int8_t*>(q), static_cast<const uint16_t*>(s), N, K, 0, out, bad);
+      break;
+    case QMOE_INT8_24:
+      pack_int8_24_matrix(static_cast<const int8_t*>(q), cw ? nullptr : static_cast<const uint16_t*>(s), N, K, 0, out,
+                          bad);
+      break;
+    default:
+      pack_int8_matrix(static_cast<const int8_t*>(q), nullptr, N, K, 0, out, bad);
+      break;
+  }
+  if (row_scales) std::memcpy(s_packed, s, sizeof(float) * N);
+  return bad ? QMOE_ERR_INVALID_ARG : QMOE_OK;
+}
+
+qmoe_status qmoe_unpack_linear(qmoe_quant_type qt, int32_t N, int32_t K, int32_t group_size, const void* w_packed,
+                               const float* s_packed, const int32_t* g_idx, void* q, void* s, uint8_t* z) {
+  if (N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return QMOE_ERR_INVALID_ARG;
+  if (qmoe_packed_bytes(qt, 1, N, K, group_size) == 0) return QMOE_ERR_UNSUPPORTED;
+  const bool row_scales = has_row_scales(qt, group_size);
+  if (!w_packed || !q || !s || (row_scales && !s_packed) || ((z != nullptr) != (qt == QMOE_INT4_GROUP_ZP)))
+    return QMOE_ERR_INVALID_ARG;
+  std::vector<int32_t> perm;
+  if (g_idx && !sorted_by_group(g_idx, K, perm)) return QMOE_ERR_UNSUPPORTED;
+  const uint8_t* in = static_cast<const uint8_t*>(w_packed);
+  const bool cw = group_size == -1;
+  switch (qt) {
+    case QMOE_INT4_GROUP:
+    case QMOE_INT4_GROUP_ZP:
+      unpack_int4_matrix(in, z != nullptr, cw, N, K, 0, nullptr, g_idx ? perm.data() : nullptr,
+                         static_cast<uint8_t*>(q), static_cast<uint16_t*>(s), z);
+      break;
+    case QMOE_INT4_GROUP_24:
+      unpack_int4_24_matrix(in, cw, N, K, 0, static_cast<uint8_t*>(q), static_cast<uint16_t*>(s));
+      break;
+    case QMOE_INT8_GROUP:
+      unpack_int8_matrix(in, true, N, K, 0, static_cast<int8_t*>(q), static_cast<uint16_t*>(s));
+      break;
+    case QMOE_INT8_24:
+      unpack_int8_24_matrix(in, !cw, N, K, 0, static_cast<int8_t*>(q), cw ? nullptr : static_cast<uint16_t*>(s));
+      break;
+    default:
+      unpack_int8_matrix(in, false, N, K, 0, static_cast<int8_t*>(q), nullptr);
+      break;
+  }
+  if (row_scales) std::memcpy(s, s_packed, sizeof(float) * N);
+  return QMOE_OK;
+}
+
+size_t qmoe_linear_workspace_size(const qmoe_linear* layer, int64_t M, const qmoe_options* opts) {
+  LinearPlan lp;
+  if (make_linear_plan(layer, M, opts, current_sm_count(), &lp) != QMOE_OK) return 0;
+  return lp.total;
+}
+
+qmoe_status qmoe_linear_describe_plan(const qmoe_linear* layer, int64_t M, const qmoe_options* opts, int32_t num_sms,
+                                      qmoe_plan_info* info) {
+  if (info == nullptr || num_sms < 0) return QMOE_ERR_INVALID_ARG;
+  LinearPlan lp;
+  const qmoe_status st = make_linear_plan(layer, M, opts, num_sms > 0 ? num_sms : current_sm_count(), &lp);
+  if (st != QMOE_OK) return st;
+  *info = qmoe_plan_info{};
+  info->token_tile = lp.g.T;
+  info->issuers = lp.g.issuers;
+  info->acc_bufs = lp.g.acc_bufs;
+  info->split1 = lp.g.S1;
+  info->split2 = 0;
+  info->w_stages = lp.g.w_stages;
+  info->ab_stages = lp.g.ab_stages;
+  info->b_stages = lp.g.b_stages;
+  info->dq_sets = lp.g.dq_sets;
+  info->stage_bytes = lp.g.stage_bytes;
+  info->workspace_bytes = static_cast<int64_t>(lp.total);
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_linear_forward(const qmoe_linear* layer, const void* x, int64_t M, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream, const qmoe_options* opts) {
+  return linear_forward_impl(layer, x, M, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), opts);
 }
 
 qmoe_status qmoe_read_device_status(const void* workspace, void* stream) {

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   for (int base = beg; base < end; base += 32) {
     const int p = base + lane;
     const bool in = p < end;
-    const int e = in ? __ldg(ids + p) : -1;
+    const int e = in ? (ids != nullptr ? __ldg(ids + p) : 0) : -1;  // no ids: every pair is expert 0
     const bool valid = in && e >= 0 && e < E;
     if (in && !valid) s_bad = 1;
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   for (int base = beg; base < end; base += 32) {
     const int p = base + lane;
     const bool in = p < end;
-    const int ex = in ? __ldg(ids + p) : -1;
+    const int ex = in ? (ids != nullptr ? __ldg(ids + p) : 0) : -1;
     const bool valid = in && ex >= 0 && ex < E;
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? ex : -1);
     if (valid) {
@@ -430,6 +430,52 @@ cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E
                          top_k, H, static_cast<uint16_t*>(out));
   return launch_kernel(out_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, y, topk_ids, E, split, M,
                        top_k, H, static_cast<uint16_t*>(out));
+}
+
+// ---------------------------------------------------------------------------
+// Dense linear, split K: out[m, n] = sum_s h[s, m, n] in a fixed order, cast to
+// the activation type (the GEMM's epilogue applied every scale).
+// ---------------------------------------------------------------------------
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+    linear_reduce_kernel(const float* __restrict__ h, int32_t split, int64_t cap_rows, int64_t M, int32_t N,
+                         uint16_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t total = M * (N / 4);
+  const int64_t slab = cap_rows * static_cast<int64_t>(N);
+  for (int64_t t = blockIdx.x * 256LL + threadIdx.x; t < total; t += static_cast<int64_t>(gridDim.x) * 256) {
+    const int64_t m = t / (N / 4);
+    const int n4 = static_cast<int>(t - m * (N / 4));
+    const int64_t base = m * N + 4LL * n4;
+    float4 acc = __ldg(reinterpret_cast<const float4*>(h + base));
+    for (int s = 1; s < split; ++s) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(h + s * slab + base));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    uint2 packed;
+    if (BF16) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+      packed.x = *reinterpret_cast<uint32_t*>(&a);
+      packed.y = *reinterpret_cast<uint32_t*>(&b);
+    } else {
+      __half2 a = __floats2half2_rn(acc.x, acc.y), b = __floats2half2_rn(acc.z, acc.w);
+      packed.x = *reinterpret_cast<uint32_t*>(&a);
+      packed.y = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint2*>(out + m * N)[n4] = packed;
+  }
+}
+
+cudaError_t launch_linear_reduce(const float* h, int32_t split, int64_t cap_rows, int64_t M, int32_t N, bool bf16,
+                                 void* out, int num_sms, cudaStream_t stream) {
+  const int64_t want = (M * (N / 4) + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
+  if (bf16)
+    return launch_kernel(linear_reduce_kernel<true>, dim3(grid), dim3(256), 0, stream, true, h, split, cap_rows, M,
+                         N, static_cast<uint16_t*>(out));
+  return launch_kernel(linear_reduce_kernel<false>, dim3(grid), dim3(256), 0, stream, true, h, split, cap_rows, M, N,
+                       static_cast<uint16_t*>(out));
 }
 
 // ---------------------------------------------------------------------------

@@ -73,8 +73,7 @@ constexpr int kProducerWarp = 4;
 constexpr int kProducerWarp2 = 7;
 constexpr int kMmaWarp = 5;        // issuers 0 and 1: warps 5 and 6; issuer 2: warp 24
 constexpr int kMmaWarp3 = 24;
-constexpr int kDequantWarp0 = 8;   // warps 8..23: two sets of 8
-constexpr int kDequantWarps = 8;   // per set
+constexpr int kDequantWarp0 = 8;   // warps 8..23: two sets of 8 or four sets of 4
 constexpr int kMaxIssuers = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarrierBytes = 1024;
@@ -230,6 +229,15 @@ __device__ __forceinline__ void dequant_int4_24_half(const uint4& pk, const uint
   }
 }
 
+// 2:4-sparse int8: a row's half (64 K, 16 groups of 4 channels) is 32 bytes
+// of kept codes and 8 bytes of positions.  Word j of the codes holds groups
+// 2j and 2j+1 as bytes (first kept, second kept) of each, so the int8
+// conversion below turns each word into two f16x2 values, one per group;
+// positions and placement as for 2:4-sparse int4 (the same selector table).
+template <bool GS, bool BF16S>
+__device__ __forceinline__ void dequant_int8_24_half(const uint4 (&pk)[2], const uint2& pos, uint32_t sbits,
+                                                     const uint2* sel_tab, uint32_t (&out)[32]);
+
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
 // conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.  A per-row
 // (per-column of W) scale is applied to the fp32 accumulator in the epilogue;
@@ -279,6 +287,34 @@ __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t
   }
 }
 
+template <bool GS, bool BF16S>
+__device__ __forceinline__ void dequant_int8_24_half(const uint4 (&pk)[2], const uint2& pos, uint32_t sbits,
+                                                     const uint2* sel_tab, uint32_t (&out)[32]) {
+  uint32_t s2bits = 0;
+  if (GS) {
+    const uint16_t s16 =
+        BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16))) : static_cast<uint16_t>(sbits);
+    s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t r[2];
+      cvt_int8_word<GS>(w[j], s2bits, r[0], r[1]);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int g = 8 * c + 2 * j + x;
+        const uint32_t m = ((g < 8 ? pos.x : pos.y) >> (4 * (g & 7))) & 15u;
+        const uint2 sel = sel_tab[m];
+        out[2 * g] = __byte_perm(r[x], 0u, sel.x);
+        out[2 * g + 1] = __byte_perm(r[x], 0u, sel.y);
+      }
+    }
+  }
+}
+
 // The 8 MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
 // between two tcgen05.mma instructions roughly triples their issue cost.  The
 // A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
@@ -316,6 +352,19 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
     float* h = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
 #pragma unroll
     for (int c = 0; c < 16; ++c) h[static_cast<int64_t>(it.row0 + c0 + c) * p.out_ld + it.tile * kTileRows + row] = f[c];
+  } else if (p.epi_mode == kEpiLinearOut) {
+    // dense linear: B row r is token r (rows >= P are padding); out[r, n] in the activation type
+    uint16_t* o = static_cast<uint16_t*>(p.out);
+    const int n = it.tile * kTileRows + row;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int r = it.row0 + c0 + c;
+      if (r < p.P) {
+        const uint16_t v = p.out_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f[c]))
+                                      : __half_as_ushort(__float2half_rn(f[c]));
+        o[static_cast<int64_t>(r) * p.out_ld + n] = v;
+      }
+    }
   } else {
     float* y = static_cast<float*>(p.out) + it.split_idx * p.out_split_stride;
 #pragma unroll
@@ -369,11 +418,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    const uint32_t wps = 16u / static_cast<uint32_t>(p.dq_sets);  // warps of a dequant set
     for (int s = 0; s < NW; ++s) {
       mbar_init(smem_u32(wfull + s), 1);
-      mbar_init(smem_u32(wempty + s), kDequantWarps);
+      mbar_init(smem_u32(wempty + s), wps);
     }
-    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), kDequantWarps);
+    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), wps);
     for (int j = 0; j < NB2; ++j) mbar_init(smem_u32(done + j), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
@@ -383,7 +433,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (KIND == kQ4S && threadIdx.x < 16) {
+  if ((KIND == kQ4S || KIND == kQ8S || KIND == kQ8SG) && threadIdx.x < 16) {
     const int m = static_cast<int>(threadIdx.x);
     sel_tab[m] = make_uint2(sparse24_pair_selector(m, 0) | (sparse24_pair_selector(m, 1) << 8),
                             sparse24_pair_selector(m, 2) | (sparse24_pair_selector(m, 3) << 8));
@@ -509,9 +559,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant sets
-    const int set = (warp - kDequantWarp0) >> 3;
-    const int q = warp & 3;             // TMEM lane quadrant = rows 32q .. 32q+31
-    const int half = (warp >> 2) & 1;   // K half of the stage row: columns 32*half .. +31
+    // DS sets of 16/DS warps; set s takes stages s, s + DS, ...  With 2 sets a
+    // warp converts one K half of its 32 rows (its TMEM lane quadrant); with 4
+    // sets a warp converts both halves of its rows, which halves the per-stage
+    // wait / store / arrive work and keeps four stages in conversion at once.
+    const int DS = p.dq_sets;
+    const int wps = 16 / DS;
+    const int dw = warp - kDequantWarp0;
+    const int set = dw / wps;
+    const int q = warp & 3;                                  // TMEM lane quadrant = rows 32q .. 32q+31
+    const int h0 = (wps == 8) ? ((dw >> 2) & 1) : 0;         // first K half this warp converts
+    const int h1 = (wps == 8) ? h0 + 1 : 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     // wr: weight slot of the stage; ar: its A slot; dr: the done barrier of the
@@ -527,49 +585,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       WorkItem it;
       decode_item(p, nch, i, it);
       const int n_st = it.ks1 - it.ks0;
-      for (int g = first_own(g0, set, 2); g < g0 + n_st;
-           g += 2, wr.step(2, NW), ar.step(2, NB), dr.step(2, NB2)) {
+      for (int g = first_own(g0, set, DS); g < g0 + n_st;
+           g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2)) {
         // weights and token tile landed
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint8_t* wst = wring + wr.idx * wslot;
-        uint32_t out[32];
-        if (INT4) {
-          uint4 pk[2];
+        for (int half = h0; half < h1; ++half) {
+          const bool last = half + 1 == h1;  // the weight slot is released after the last half's loads
+          uint32_t out[32];
+          if (INT4) {
+            uint4 pk[2];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((2 * half + c) * 128 + row) * 16);
-          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
-          const uint32_t zp = (KIND == kQ4Z) ? static_cast<uint32_t>(wst[8448 + row]) : 8u;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-          dequant_int4_half<BF16S>(pk, sbits, zp, out);
-        } else if (KIND == kQ4S) {
-          const uint4 pk = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 16);
-          const uint2 pos = *reinterpret_cast<const uint2*>(wst + 4096 + (half * 128 + row) * 8);
-          const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 6144 + row * 2);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-          dequant_int4_24_half<BF16S>(pk, pos, sbits, sel_tab, out);
-        } else {
-          uint4 pk[4];
+            for (int c = 0; c < 2; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((2 * half + c) * 128 + row) * 16);
+            const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
+            const uint32_t zp = (KIND == kQ4Z) ? static_cast<uint32_t>(wst[8448 + row]) : 8u;
+            __syncwarp();
+            if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+            dequant_int4_half<BF16S>(pk, sbits, zp, out);
+          } else if (KIND == kQ4S) {
+            const uint4 pk = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 16);
+            const uint2 pos = *reinterpret_cast<const uint2*>(wst + 4096 + (half * 128 + row) * 8);
+            const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 6144 + row * 2);
+            __syncwarp();
+            if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+            dequant_int4_24_half<BF16S>(pk, pos, sbits, sel_tab, out);
+          } else if (KIND == kQ8S || KIND == kQ8SG) {
+            uint4 pk[2];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((4 * half + c) * 128 + row) * 16);
-          const uint32_t sbits = (KIND == kQ8G) ? *reinterpret_cast<const uint16_t*>(wst + 16384 + row * 2) : 0u;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-          dequant_int8_half<KIND == kQ8G, BF16S>(pk, sbits, out);
+            for (int c = 0; c < 2; ++c)
+              pk[c] = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 32 + 16 * c);
+            const uint2 pos = *reinterpret_cast<const uint2*>(wst + 8192 + (half * 128 + row) * 8);
+            const uint32_t sbits = (KIND == kQ8SG) ? *reinterpret_cast<const uint16_t*>(wst + 10240 + row * 2) : 0u;
+            __syncwarp();
+            if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+            dequant_int8_24_half<KIND == kQ8SG, BF16S>(pk, pos, sbits, sel_tab, out);
+          } else {
+            uint4 pk[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((4 * half + c) * 128 + row) * 16);
+            const uint32_t sbits = (KIND == kQ8G) ? *reinterpret_cast<const uint16_t*>(wst + 16384 + row * 2) : 0u;
+            __syncwarp();
+            if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+            dequant_int8_half<KIND == kQ8G, BF16S>(pk, sbits, out);
+          }
+          // the A slot is free once the MMAs of the stage NB earlier completed; with
+          // token-tile and A rings of one depth the token tile's arrival implied it
+          // (the producer waited for the same barrier phase before copying it)
+          if (NB2 != NB && half == h0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
+          tmem_st_32x32b_x32<0>(ta, out);
         }
-        // the A slot is free once the MMAs of the stage NB earlier completed; with
-        // token-tile and A rings of one depth the token tile's arrival implied it
-        // (the producer waited for the same barrier phase before copying it)
-        if (NB2 != NB) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
-        tmem_st_32x32b_x32<0>(ta, out);
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -599,7 +671,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 #pragma unroll
       for (int j = 0; j < kMaxIssuers; ++j) has[j] = j < NI && first_own(g0, j, NI) < g0 + n_st;
       g0 += n_st;
-      const float rs = (KIND != kQ8)
+      const float rs = (KIND != kQ8 && KIND != kQ8S)
                            ? 1.0f
                            : __ldg(p.row_scale + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * kTileRows + row);
       for (int c0 = 0; c0 < it.nrows; c0 += 16) {

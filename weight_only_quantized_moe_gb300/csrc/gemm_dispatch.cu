@@ -12,6 +12,9 @@ cudaError_t launch_gemm_i4s_bf16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8g_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8g_bf16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i8s(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i8sg_f16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i8sg_bf16(const GemmParams&, int, cudaStream_t);
 
 size_t gemm_smem_bytes(const GemmParams& p) {
   return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.b_stages, p.token_tile);
@@ -23,6 +26,9 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
   const int mult = (p.issuers == 3) ? 6 : 2;
   if (p.w_stages < 2 || (p.w_stages & 1) || p.ab_stages < mult || p.ab_stages % mult != 0) return cudaErrorInvalidValue;
   if (p.b_stages < p.ab_stages || p.b_stages % p.ab_stages != 0) return cudaErrorInvalidValue;
+  // dequant sets: each weight slot and each token-tile ("done") barrier must belong to one set
+  if (p.dq_sets != 2 && p.dq_sets != 4) return cudaErrorInvalidValue;
+  if (p.w_stages % p.dq_sets != 0 || p.b_stages % p.dq_sets != 0) return cudaErrorInvalidValue;
   // barriers (2 per weight slot, 1 per A slot, 1 per token-tile slot, 4 + kMaxIssuers more,
   // TMEM address, abort flag) below the 128-byte selector table at the end of the barrier area
   if ((2 * p.w_stages + p.ab_stages + p.b_stages + 4 + kMaxIssuers) * 8 + 8 > kBarrierBytes - 128)
@@ -32,6 +38,8 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
     case kQ4Z: return bf16_scales ? launch_gemm_i4z_bf16(p, grid, stream) : launch_gemm_i4z_f16(p, grid, stream);
     case kQ8G: return bf16_scales ? launch_gemm_i8g_bf16(p, grid, stream) : launch_gemm_i8g_f16(p, grid, stream);
     case kQ4S: return bf16_scales ? launch_gemm_i4s_bf16(p, grid, stream) : launch_gemm_i4s_f16(p, grid, stream);
+    case kQ8S: return launch_gemm_i8s(p, grid, stream);
+    case kQ8SG: return bf16_scales ? launch_gemm_i8sg_bf16(p, grid, stream) : launch_gemm_i8sg_f16(p, grid, stream);
     default: return launch_gemm_i8(p, grid, stream);
   }
 }

@@ -1,0 +1,11 @@
+// gemm_i8s.cu - instantiation of the grouped dequant GEMM for 2:4-sparse int8 weights with
+// per-column scales (one translation unit per variant so they compile in parallel).
+#include "gemm.cuh"
+
+namespace qmoe {
+
+cudaError_t launch_gemm_i8s(const GemmParams& p, int grid, cudaStream_t stream) {
+  return launch_gemm_t<kQ8S, false>(p, grid, stream);
+}
+
+}  // namespace qmoe

@@ -17,9 +17,13 @@ constexpr int kInt4ZpStageBytes = 8576;   // int4 block + 128 zero-point bytes
 constexpr int kInt8GroupStageBytes = 16640;  // int8 block + 128 x 2 B scales
 // 2:4-sparse int4: 128 rows x 64 kept codes (4 KB), their 2-bit positions (2 KB), 128 x 2 B scales
 constexpr int kInt4SparseStageBytes = 6400;
+// 2:4-sparse int8: 128 rows x 64 kept codes (8 KB), their 2-bit positions (2 KB); with group
+// scales 128 x 2 B more (per-column scales live outside the blocks)
+constexpr int kInt8SparseStageBytes = 10240;
+constexpr int kInt8SparseGroupStageBytes = 10496;
 
 // Weight formats of the GEMM kernel (template parameter).
-enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3, kQ4S = 4 };
+enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3, kQ4S = 4, kQ8S = 5, kQ8SG = 6 };
 constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
 constexpr int kMaxTokenTile = 128;
 
@@ -37,8 +41,9 @@ struct Chunk {
 
 enum EpiMode : int32_t {
   kEpiSiluToAct = 0,   // gate/up GEMM, whole K: fp32 inter[row, j] = SiLU(gate)*up
-  kEpiPartialRows = 1, // gate/up GEMM, split K: fp32 partial [split][row][2I] (interleaved gate/up)
-  kEpiWeightedPairs = 2 // down GEMM: fp32 y[split][pair][H] = topk_weight * acc
+  kEpiPartialRows = 1, // gate/up GEMM or dense linear, split K: fp32 partial [split][row][N]
+  kEpiWeightedPairs = 2, // down GEMM: fp32 y[split][pair][H] = topk_weight * acc
+  kEpiLinearOut = 3    // dense linear, whole K: out[row, n] in the activation type, rows < P
 };
 
 // Pre-staged B operand (the gathered activations, the f16 intermediate): K is
@@ -84,6 +89,8 @@ struct GemmParams {
   int32_t chunk_group;       // work-item raster: chunks per group
   int32_t inter_ld;          // I (for the SiLU epilogue)
   int32_t fault_injection;   // 1: CTA 0 arms its first stage without copies (failure-path test)
+  int32_t out_bf16;          // kEpiLinearOut: output type bf16 (else f16)
+  int32_t dq_sets;           // dequant sets (2 of 8 half-row warps, or 4 of 4 full-row warps)
 };
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
@@ -124,6 +131,11 @@ cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_p
 
 cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E, int32_t split, int64_t M,
                               int32_t top_k, int32_t H, bool bf16, void* out, int num_sms, cudaStream_t stream);
+
+// Dense linear, split K: out[m, n] = sum_s h[s, m, n] (fp32 partials, slabs of cap_rows x N) cast to the
+// activation type, m < M.
+cudaError_t launch_linear_reduce(const float* h, int32_t split, int64_t cap_rows, int64_t M, int32_t N, bool bf16,
+                                 void* out, int num_sms, cudaStream_t stream);
 
 // dtype: 0 f32, 1 f16, 2 bf16 logits; 1 <= E <= 1024, 1 <= k <= min(E, 32).
 cudaError_t launch_route_topk(const void* logits, int dtype, int64_t M, int32_t E, int32_t k, int32_t renormalize,
