@@ -113,7 +113,8 @@ typedef enum { QMOE_F16 = 1, QMOE_BF16 = 2, QMOE_F32 = 3 } qmoe_dtype;
  *                packed weights).
  *   perm13       int4 act-order only (group_size 128): int32 [E, H] written
  *                by qmoe_pack_int4 / qmoe_pack_int4_zp (hidden channel of
- *                each sorted K position); NULL otherwise.
+ *                each sorted K position); NULL otherwise.  With act-order H is
+ *                at most 65536 (QMOE_ERR_UNSUPPORTED otherwise).
  *                Act-order of W2 needs no runtime table: it is folded into the
  *                row order of the packed W13.
  */
@@ -161,10 +162,15 @@ typedef struct {
    * QMOE_ERR_INVALID_ARG. */
   int32_t token_ring;
   /* Dequant warp sets of the GEMMs: 2 (8 warps each, half a stage row per
-   * warp) or 4 (4 warps each, whole rows per warp); 0: automatic.  4 needs a
-   * token-tile ring that is a multiple of 4 (QMOE_ERR_INVALID_ARG otherwise). */
+   * warp) or 4 (4 warps each, whole rows per warp); 0: automatic (4 wherever
+   * the rings allow it).  4 needs a token-tile ring that is a multiple of 4
+   * (QMOE_ERR_INVALID_ARG otherwise). */
   int32_t dq_sets;
-  int32_t reserved[1];
+  /* L2 policy of the GEMMs' weight copies: 0 automatic (evict-normal when an
+   * expert has more pairs than one token tile, so that the chunks that share
+   * a weight tile find it in L2; evict-first otherwise), 1 evict-normal,
+   * 2 evict-first.  Other values give QMOE_ERR_INVALID_ARG. */
+  int32_t weight_l2;
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */
@@ -409,7 +415,8 @@ qmoe_status qmoe_forward_ex(const qmoe_layer* layer, const void* x, int64_t M,
  * 4 intermediate rescale, 5 down GEMM, 6 output reduce) event 2i is recorded
  * on `stream` just before
  * it and event 2i+1 just after.  A launch the plan skips (3 when the gate/up
- * GEMM is not split) gets both events at the same point.  *n_launches
+ * GEMM is not split; 1 for batches of at most 1024 token-expert pairs, whose
+ * gather runs inside launch 0) gets both events at the same point.  *n_launches
  * (optional) receives the number of kernels launched.  Null events give
  * QMOE_ERR_INVALID_ARG.
  */

@@ -61,3 +61,44 @@ def test_larger_capacity_and_empty():
 def test_bad_ids_are_dropped():
     ids = np.array([[0, 5], [2, 0], [-1, 1]], np.int32)
     _check(ids, 3, 2)
+
+
+def _al256(n):
+    return (n + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("M,k,E,zipf", [(1, 2, 8, 0.0), (5, 2, 8, 0.0), (16, 6, 160, 1.1), (300, 2, 8, 0.0),
+                                        (512, 2, 8, 0.0), (170, 6, 160, 1.1), (513, 2, 8, 0.0), (1024, 6, 160, 1.1)])
+def test_forward_grouping_matches_oracle(M, k, E, zipf):
+    """The grouping a forward computes (by the fused align+gather kernel for up to
+    1024 pairs, by moe_align above) is bit-exact: it is read back from the
+    workspace, whose first regions are the status word (256 bytes), sorted_ids
+    [cap] and expert_ids [cap / 16], each rounded up to 256 bytes, then the padded
+    total; cap = P + 15 E rounded up to 16."""
+    import torch
+    import oracle
+    import weight_only_quantized_moe_gb300 as q
+    from synth import Workload, make_inputs, make_layer
+    from tests.gpu_util import device_inputs, device_layer
+    wl = Workload("grp", E, k, 128, 128, "int4", 128, "f16", False, zipf, (1,))
+    dl = device_layer(make_layer(wl, seed=1))
+    inp = make_inputs(wl, M, seed=M)
+    x, ids, w = device_inputs(wl, inp)
+    ws = q.alloc_workspace(q.qmoe_workspace_size(dl, M, k))
+    ws.fill_(0x7F)
+    q.qmoe_forward(dl, x, ids, w, workspace=ws)
+    torch.cuda.synchronize()
+    P = M * k
+    cap = (P + E * 15 + 15) // 16 * 16
+    nblocks = (cap + 15) // 16
+    want_sorted, want_expert, want_total = oracle.moe_align(inp.topk_ids, E, 16, cap)
+    raw = ws.cpu().numpy()
+    got_sorted = raw[256:256 + 4 * cap].view(np.int32)
+    off_e = 256 + _al256(4 * cap)
+    got_expert = raw[off_e:off_e + 4 * nblocks].view(np.int32)
+    off_s = off_e + _al256(4 * nblocks)
+    got_total = int(raw[off_s:off_s + 4].view(np.int32)[0])
+    assert got_total == want_total
+    np.testing.assert_array_equal(got_sorted, want_sorted)
+    np.testing.assert_array_equal(got_expert, want_expert[:nblocks])
+    assert q.qmoe_read_device_status(ws) == q.QMOE_OK

@@ -91,9 +91,10 @@ def test_forward_forced_split_and_tile(qt, act, ao, split1, split2, tile):
                                           ("int8s24", "bf16", False, -1)])
 @pytest.mark.parametrize("M,split1,split2,tile", [(1, 0, 0, 0), (40, 0, 0, 0), (129, 0, 0, 0), (40, 3, 2, 0),
                                                   (300, 1, 1, 128), (40, 2, 1, 64)])
-def test_forward_four_dequant_sets(qt, act, ao, gs, M, split1, split2, tile):
-    """The GEMMs with four dequant sets of four whole-row warps (every tile size)."""
-    _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile, dq_sets=4))
+def test_forward_two_dequant_sets(qt, act, ao, gs, M, split1, split2, tile):
+    """The GEMMs with two dequant sets of eight half-row warps (the default is four
+    sets of four whole-row warps wherever the rings allow it), every tile size."""
+    _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile, dq_sets=2))
 
 
 @pytest.mark.parametrize("qt,act", [("int8", "f16"), ("int8", "bf16")])

@@ -134,10 +134,14 @@ qmoe_status validate_format(int32_t qt, int32_t gs, int32_t act, int32_t sdt, bo
   return QMOE_OK;
 }
 
+// Act-order gathers stage one token row (2 bytes per channel) in shared memory.
+constexpr int32_t kMaxActOrderK = 65536;
+
 qmoe_status validate_layer_dims(const qmoe_layer* L) {
   if (L == nullptr) return QMOE_ERR_INVALID_ARG;
   if (L->E < 1 || L->E > 1024 || L->H <= 0 || L->I <= 0) return QMOE_ERR_INVALID_ARG;
   if (L->H % 128 != 0 || L->I % 128 != 0) return QMOE_ERR_UNSUPPORTED;
+  if (L->perm13 != nullptr && L->H > kMaxActOrderK) return QMOE_ERR_UNSUPPORTED;
   return validate_format(L->qt, L->group_size, L->act_dtype, L->scale_dtype, L->perm13 != nullptr);
 }
 
@@ -234,19 +238,22 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
   p->b_stages = ring_m * p->ab_stages;
   p->w_stages = w_depth(p->b_stages);
   if (p->w_stages < 2 || p->ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
-  // Dequant sets: 2 sets of 8 warps (each converts half of a stage row for its
-  // 32 rows) or 4 sets of 4 warps (each converts whole rows).  A set takes every
+  // Dequant sets: 4 sets of 4 warps (each converts whole stage rows for its 32
+  // rows) or 2 sets of 8 warps (each converts half rows).  A set takes every
   // DS-th stage, so the weight ring and the token-tile ring must be multiples of
-  // DS for each slot's barriers to belong to one set.
-  p->dq_sets = 2;
+  // DS for each slot's barriers to belong to one set.  Four sets halve the
+  // per-stage wait / store / arrive work of the dequant warps and keep four
+  // stages in conversion at once (measured on GB300: 3-10 % faster at every
+  // size, most at decode), so they are chosen wherever the rings allow.
+  if (o != nullptr && (o->weight_l2 < 0 || o->weight_l2 > 2)) return QMOE_ERR_INVALID_ARG;
+  const bool four_ok = (p->w_stages & ~3) >= 4 && p->b_stages % 4 == 0;
+  p->dq_sets = four_ok ? 4 : 2;
   if (o != nullptr && o->dq_sets != 0) {
     if (o->dq_sets != 2 && o->dq_sets != 4) return QMOE_ERR_INVALID_ARG;
+    if (o->dq_sets == 4 && !four_ok) return QMOE_ERR_INVALID_ARG;
     p->dq_sets = o->dq_sets;
   }
-  if (p->dq_sets == 4) {
-    p->w_stages &= ~3;
-    if (p->w_stages < 4 || p->b_stages % 4 != 0) return QMOE_ERR_INVALID_ARG;
-  }
+  if (p->dq_sets == 4) p->w_stages &= ~3;
   return QMOE_OK;
 }
 
@@ -376,18 +383,29 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
     if (events != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(events[idx]), stream);
   };
   int launched = 0;
-  rec(0);
-  cudaError_t err = launch_align(topk_ids, P, L->E, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch,
-                                 status, stream);
-  rec(1);
-  launched += (err == cudaSuccess);
-  rec(2);
-  if (err == cudaSuccess) {
-    err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, sms,
-                        stream);
+  cudaError_t err;
+  if (align_gather_small_fits(P, L->E, kAlignBlock, L->H, L->perm13 != nullptr)) {
+    // small batch: grouping and gather in one kernel (launch 1 then takes no time)
+    rec(0);
+    err = launch_align_gather_small(topk_ids, P, L->E, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch,
+                                    status, x, bf16, L->perm13, k, L->H, pl.cap, xg, xscale, sms, stream);
+    rec(1);
     launched += (err == cudaSuccess);
+    rec(2);
+    rec(3);
+  } else {
+    rec(0);
+    err = launch_align(topk_ids, P, L->E, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status, stream);
+    rec(1);
+    launched += (err == cudaSuccess);
+    rec(2);
+    if (err == cudaSuccess) {
+      err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, sms,
+                          stream);
+      launched += (err == cudaSuccess);
+    }
+    rec(3);
   }
-  rec(3);
   GemmParams g1{};
   g1.w = static_cast<const uint8_t*>(L->w13);
   g1.b = static_cast<const uint8_t*>(xg);
@@ -415,6 +433,9 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.P = P;
   g1.chunk_group = 8;
   g1.inter_ld = L->I;
+  // more pairs per expert than a token tile holds: several chunks read each weight tile
+  g1.w_shared = (opts != nullptr && opts->weight_l2 != 0) ? (opts->weight_l2 == 1)
+                                                           : (pl.P > static_cast<int64_t>(L->E) * pl.T);
   if (pl.S1 == 1) {
     g1.epi_mode = kEpiSiluToAct;
     g1.out = inter32;
@@ -494,6 +515,7 @@ qmoe_status validate_linear(const qmoe_linear* L) {
   if (L == nullptr) return QMOE_ERR_INVALID_ARG;
   if (L->N <= 0 || L->K <= 0) return QMOE_ERR_INVALID_ARG;
   if (L->N % 128 != 0 || L->K % 128 != 0) return QMOE_ERR_UNSUPPORTED;
+  if (L->perm != nullptr && L->K > kMaxActOrderK) return QMOE_ERR_UNSUPPORTED;
   return validate_format(L->qt, L->group_size, L->act_dtype, L->scale_dtype, L->perm != nullptr);
 }
 
@@ -580,11 +602,16 @@ qmoe_status linear_forward_impl(const qmoe_linear* L, const void* x, int64_t M, 
   const bool bf16 = L->act_dtype == QMOE_BF16;
   const int P = static_cast<int>(M);
   // every row is "expert 0": the align kernel lays out rows 0..M-1 and the chunk table
-  cudaError_t err = launch_align(nullptr, P, 1, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status,
-                                 stream);
-  if (err == cudaSuccess)
-    err = launch_gather(x, bf16, sorted, expert, npp, L->perm, P, 1, L->K, kAlignBlock, pl.cap, xg, xscale, sms,
-                        stream);
+  cudaError_t err;
+  if (align_gather_small_fits(P, 1, kAlignBlock, L->K, L->perm != nullptr)) {
+    err = launch_align_gather_small(nullptr, P, 1, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status,
+                                    x, bf16, L->perm, 1, L->K, pl.cap, xg, xscale, sms, stream);
+  } else {
+    err = launch_align(nullptr, P, 1, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status, stream);
+    if (err == cudaSuccess)
+      err = launch_gather(x, bf16, sorted, expert, npp, L->perm, P, 1, L->K, kAlignBlock, pl.cap, xg, xscale, sms,
+                          stream);
+  }
   GemmParams g{};
   g.w = static_cast<const uint8_t*>(L->w);
   g.b = static_cast<const uint8_t*>(xg);
@@ -612,6 +639,7 @@ qmoe_status linear_forward_impl(const qmoe_linear* L, const void* x, int64_t M, 
   g.P = P;
   g.chunk_group = 8;
   g.inter_ld = 0;
+  g.w_shared = (opts != nullptr && opts->weight_l2 != 0) ? (opts->weight_l2 == 1) : (M > pl.T);
   g.out_bf16 = bf16 ? 1 : 0;
   if (pl.S1 == 1) {
     g.epi_mode = kEpiLinearOut;

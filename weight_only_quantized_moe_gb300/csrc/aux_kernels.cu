@@ -4,6 +4,8 @@
 //   split-K SiLU reduce   (sum gate/up partials, apply SiLU(gate)*up)
 //   intermediate rescale  (fp32 intermediate -> per-row scaled f16 for the down GEMM)
 //   output reduce         (sum the top-k weighted expert outputs per token)
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -226,54 +228,221 @@ __device__ __forceinline__ uint4 scale_to_f16x8(const uint16_t (&e)[8], float in
   return o;
 }
 
+// One row of the gather, by one warp: x[p / top_k] scaled into f16 (permuted by
+// perm_e when given, through the warp's shared-memory row buffer `stage`), or
+// zeros for a padding row (p >= P).
+template <bool BF16>
+__device__ __forceinline__ void gather_one_row(const uint16_t* __restrict__ x, int p, int row, int P, int top_k, int H,
+                                               int64_t cap, const int32_t* __restrict__ perm_e, uint4* stage,
+                                               uint8_t* __restrict__ xg, float* __restrict__ xscale, int lane) {
+  if (p >= P) {
+    for (int c = lane; c < H / 8; c += 32)
+      *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = make_uint4(0, 0, 0, 0);
+    if (lane == 0) xscale[row] = 1.0f;
+    return;
+  }
+  const uint16_t* src = x + static_cast<int64_t>(p / top_k) * H;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  // act-order: the row is staged in this warp's shared-memory buffer (coalesced
+  // 16-byte loads) and permuted from there
+  float amax = 0.0f;
+  for (int i = lane; i < H / 8; i += 32) {
+    const uint4 v = __ldg(s4 + i);
+    if (perm_e != nullptr) stage[i] = v;
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(act_to_float<BF16>(e[k])));
+  }
+  amax = warp_max(amax);
+  const float2 sc = row_exponent_scale(amax);
+  const float inv = sc.y;
+  if (lane == 0) xscale[row] = sc.x;
+  if (perm_e == nullptr) {
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 v = __ldg(s4 + c);
+      uint16_t e[8];
+      *reinterpret_cast<uint4*>(e) = v;
+      *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
+    }
+  } else {
+    __syncwarp();  // the staged row is complete
+    const uint16_t* srow = reinterpret_cast<const uint16_t*>(stage);
+    const int4* pr4 = reinterpret_cast<const int4*>(perm_e);
+    for (int c = lane; c < H / 8; c += 32) {
+      const int4 ka = __ldg(pr4 + 2 * c), kb = __ldg(pr4 + 2 * c + 1);
+      uint16_t e[8] = {srow[ka.x], srow[ka.y], srow[ka.z], srow[ka.w], srow[kb.x], srow[kb.y], srow[kb.z], srow[kb.w]};
+      *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
+    }
+    __syncwarp();  // before the next row overwrites the buffer
+  }
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                   const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_post_padded,
                   const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B, int64_t cap,
                   uint8_t* __restrict__ xg, float* __restrict__ xscale) {
+  extern __shared__ uint4 row_buf[];  // act-order only: one token row per warp
   pdl_launch_dependents();
   pdl_wait();
   const int total = *num_post_padded;
   const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (kGatherThreads / 32);
-  for (int row = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); row < total; row += warps) {
-    const int p = sorted_ids[row];
-    if (p >= P) {
-      for (int c = lane; c < H / 8; c += 32)
-        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = make_uint4(0, 0, 0, 0);
-      if (lane == 0) xscale[row] = 1.0f;
-      continue;
-    }
-    const uint16_t* src = x + static_cast<int64_t>(p / top_k) * H;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    float amax = 0.0f;
-    for (int i = lane; i < H / 8; i += 32) {
-      const uint4 v = __ldg(s4 + i);
-      const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+  const int wpb = blockDim.x >> 5;  // warps (rows in flight) per block
+  const int warps = gridDim.x * wpb;
+  uint4* stage = perm13 != nullptr ? row_buf + (threadIdx.x >> 5) * (H / 8) : nullptr;
+  for (int row = blockIdx.x * wpb + (threadIdx.x >> 5); row < total; row += warps) {
+    const int32_t* perm_e = perm13 != nullptr ? perm13 + static_cast<int64_t>(expert_ids[row / B]) * H : nullptr;
+    gather_one_row<BF16>(x, sorted_ids[row], row, P, top_k, H, cap, perm_e, stage, xg, xscale, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// moe_align and the token gather in one kernel, for small batches (P pairs at
+// most kSmallPairs).  Every block groups the pairs itself in shared memory (the
+// same result as moe_align_kernel: experts ascending, pairs ascending inside an
+// expert, padding and tail = P, chunks of the token tile), block 0 publishes
+// the grouping for the GEMMs, and each block then gathers its rows.  This takes
+// one kernel boundary off the critical path of decode-sized batches.
+// ---------------------------------------------------------------------------
+constexpr int kSmallPairs = 1024;
+
+// Exclusive scan of one value per thread over a block of kGatherThreads threads.
+__device__ __forceinline__ int block_exclusive_scan_256(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kW = kGatherThreads / 32;
+  int incl = v;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(act_to_float<BF16>(e[k])));
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kW ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < kW; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += o;
     }
-    amax = warp_max(amax);
-    const float2 sc = row_exponent_scale(amax);
-    const float inv = sc.y;
-    if (lane == 0) xscale[row] = sc.x;
-    if (perm13 == nullptr) {
-      for (int c = lane; c < H / 8; c += 32) {
-        const uint4 v = __ldg(s4 + c);
-        uint16_t e[8];
-        *reinterpret_cast<uint4*>(e) = v;
-        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
+    if (lane < kW) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[kW - 1];
+  __syncthreads();
+  return excl;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kGatherThreads)
+    align_gather_small_kernel(const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t B, int64_t capacity,
+                              int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                              int32_t* __restrict__ num_post_padded, int32_t T, Chunk* __restrict__ chunks,
+                              int32_t* __restrict__ n_chunks, int32_t* __restrict__ status,
+                              const uint16_t* __restrict__ x, const int32_t* __restrict__ perm13, int32_t top_k,
+                              int32_t H, int64_t cap, uint8_t* __restrict__ xg, float* __restrict__ xscale) {
+  extern __shared__ __align__(16) int32_t sm_i[];
+  __shared__ int warp_sums[kGatherThreads / 32];
+  __shared__ int s_bad;
+  const int rows_max = P + E * (B - 1);
+  int32_t* s_ids = sm_i;                 // [P]
+  int32_t* s_cnt = s_ids + P;            // [E] pair counts
+  int32_t* s_off = s_cnt + E;            // [E] first row of each expert
+  int32_t* s_cur = s_off + E;            // [E] scatter cursors
+  int32_t* s_sorted = s_cur + E;         // [rows_max]
+  uint4* stage_base = reinterpret_cast<uint4*>(s_sorted + ((rows_max + 3) & ~3));  // act-order row buffers
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();  // no-op unless launched as a dependent
+
+  if (tid == 0) s_bad = 0;
+  for (int i = tid; i < E; i += kGatherThreads) s_cnt[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < P; i += kGatherThreads) {
+    const int e = ids != nullptr ? __ldg(ids + i) : 0;  // no ids: every pair is expert 0
+    s_ids[i] = e;
+    if (e >= 0 && e < E)
+      atomicAdd(s_cnt + e, 1);
+    else
+      s_bad = 1;
+  }
+  __syncthreads();
+  // padded sizes, offsets and chunk counts: thread t owns experts [t*per, (t+1)*per)
+  const int per = (E + kGatherThreads - 1) / kGatherThreads;
+  const int e0 = tid * per, e1 = min(E, e0 + per);
+  int pad_sum = 0, nch_sum = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int pad = (s_cnt[e] + B - 1) / B * B;
+    pad_sum += pad;
+    nch_sum += (T > 0) ? (pad + T - 1) / T : 0;
+  }
+  int total, total_chunks;
+  int run = block_exclusive_scan_256(pad_sum, warp_sums, &total);
+  int crun = block_exclusive_scan_256(nch_sum, warp_sums, &total_chunks);
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = s_cnt[e];
+    const int pad = (cnt + B - 1) / B * B;
+    s_off[e] = run;
+    s_cur[e] = run;
+    for (int i = run + cnt; i < run + pad; ++i) s_sorted[i] = P;  // padding rows of expert e
+    if (blockIdx.x == 0) {
+      for (int b = run / B; b < (run + pad) / B; ++b) expert_ids[b] = e;
+      const int nch = (T > 0) ? (pad + T - 1) / T : 0;
+      for (int c = 0; c < nch; ++c) {
+        Chunk ch;
+        ch.expert = e;
+        ch.row0 = run + c * T;
+        ch.nrows = min(T, pad - c * T);
+        ch.pad = 0;
+        chunks[crun + c] = ch;
       }
-    } else {
-      const int4* pr4 = reinterpret_cast<const int4*>(perm13 + static_cast<int64_t>(expert_ids[row / B]) * H);
-      for (int c = lane; c < H / 8; c += 32) {
-        const int4 ka = __ldg(pr4 + 2 * c), kb = __ldg(pr4 + 2 * c + 1);
-        uint16_t e[8] = {__ldg(src + ka.x), __ldg(src + ka.y), __ldg(src + ka.z), __ldg(src + ka.w),
-                         __ldg(src + kb.x), __ldg(src + kb.y), __ldg(src + kb.z), __ldg(src + kb.w)};
-        *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
-      }
+      crun += nch;
     }
+    run += pad;
+  }
+  __syncthreads();
+  // stable scatter: one warp walks the pairs in order, grouping lanes by expert
+  if (warp == 0) {
+    for (int base = 0; base < P; base += 32) {
+      const int p = base + lane;
+      const int e = p < P ? s_ids[p] : -1;
+      const bool valid = e >= 0 && e < E;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+      if (valid) s_sorted[s_cur[e] + __popc(peers & ((1u << lane) - 1u))] = p;
+      __syncwarp();
+      if (valid && lane == __ffs(peers) - 1) s_cur[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int64_t i = tid; i < capacity; i += kGatherThreads) sorted_ids[i] = i < total ? s_sorted[i] : P;
+    const int64_t nblocks = (capacity + B - 1) / B;
+    for (int64_t b = total / B + tid; b < nblocks; b += kGatherThreads) expert_ids[b] = -1;
+    if (tid == 0) {
+      *num_post_padded = total;
+      if (n_chunks != nullptr) *n_chunks = total_chunks;
+      if (status != nullptr) *status = s_bad ? kStatusBadExpert : 0;
+    }
+  }
+  // the gather of this block's rows
+  uint4* stage = perm13 != nullptr ? stage_base + warp * (H / 8) : nullptr;
+  const int wpb = kGatherThreads / 32;
+  for (int row = blockIdx.x * wpb + warp; row < total; row += gridDim.x * wpb) {
+    const int32_t* perm_e = nullptr;
+    if (perm13 != nullptr) {
+      // the expert whose rows [s_off[e], s_off[e] + padded) hold this row: the last e with
+      // s_off[e] <= row (an empty expert shares its offset with the next one, which comes later)
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= row) lo = mid; else hi = mid - 1;
+      }
+      perm_e = perm13 + static_cast<int64_t>(lo) * H;
+    }
+    gather_one_row<BF16>(x, s_sorted[row], row, P, top_k, H, cap, perm_e, stage, xg, xscale, lane);
   }
 }
 
@@ -281,10 +450,19 @@ cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, c
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
                           int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
                           cudaStream_t stream) {
-  const int64_t want = (cap_rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
+  // act-order: each warp stages its token row in shared memory (H x 2 bytes per
+  // warp, at most 8 warps and about 200 KB per block)
+  int wpb = kGatherThreads / 32;
+  if (perm13 != nullptr) wpb = std::max(1, std::min(wpb, static_cast<int>((200 * 1024) / (2 * static_cast<int64_t>(H)))));
+  const int64_t want = (cap_rows + wpb - 1) / wpb;
   const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
   auto kern = bf16 ? gather_kernel<true> : gather_kernel<false>;
-  return launch_kernel(kern, dim3(grid), dim3(kGatherThreads), 0, stream, true, static_cast<const uint16_t*>(x),
+  const size_t smem = perm13 != nullptr ? static_cast<size_t>(wpb) * H * 2 : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+  }
+  return launch_kernel(kern, dim3(grid), dim3(32 * wpb), smem, stream, true, static_cast<const uint16_t*>(x),
                        sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block, cap_rows,
                        static_cast<uint8_t*>(xg), xscale);
 }
@@ -313,6 +491,36 @@ __global__ void __launch_bounds__(256)
     }
     reinterpret_cast<float2*>(inter32 + row * I)[j2] = make_float2(silu_f(acc.x) * acc.y, silu_f(acc.z) * acc.w);
   }
+}
+
+size_t align_gather_small_smem(int32_t P, int32_t E, int32_t block, int32_t H, bool act_order) {
+  const int64_t rows_max = static_cast<int64_t>(P) + static_cast<int64_t>(E) * (block - 1);
+  const size_t ints = static_cast<size_t>(P) + 3 * static_cast<size_t>(E) + ((rows_max + 3) & ~int64_t(3));
+  return ints * 4 + (act_order ? static_cast<size_t>(kGatherThreads / 32) * H * 2 : 0);
+}
+
+bool align_gather_small_fits(int32_t P, int32_t E, int32_t block, int32_t H, bool act_order) {
+  return P <= kSmallPairs && align_gather_small_smem(P, E, block, H, act_order) <= 200 * 1024;
+}
+
+cudaError_t launch_align_gather_small(const int32_t* topk_ids, int32_t P, int32_t E, int32_t block, int64_t capacity,
+                                      int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                                      int32_t token_tile, Chunk* chunks, int32_t* n_chunks, int32_t* status,
+                                      const void* x, bool bf16, const int32_t* perm13, int32_t top_k, int32_t H,
+                                      int64_t cap_rows, void* xg, float* xscale, int num_sms, cudaStream_t stream) {
+  const size_t smem = align_gather_small_smem(P, E, block, H, perm13 != nullptr);
+  const int wpb = kGatherThreads / 32;
+  const int64_t want = (cap_rows + wpb - 1) / wpb;
+  const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
+  auto kern = bf16 ? align_gather_small_kernel<true> : align_gather_small_kernel<false>;
+  if (smem > 48 * 1024) {
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+  }
+  // first kernel of a forward: ordinary stream order behind the caller's work
+  return launch_kernel(kern, dim3(grid), dim3(kGatherThreads), smem, stream, false, topk_ids, P, E, block, capacity,
+                       sorted_ids, expert_ids, num_post_padded, token_tile, chunks, n_chunks, status,
+                       static_cast<const uint16_t*>(x), perm13, top_k, H, cap_rows, static_cast<uint8_t*>(xg), xscale);
 }
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,

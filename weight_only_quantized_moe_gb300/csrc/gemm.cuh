@@ -459,7 +459,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     // Two threads (warps 4 and 7) issue the copies of even and odd stages.
     if (lane == 0) {
       const int id = (warp == kProducerWarp) ? 0 : 1;
-      const uint64_t pol_w = policy_evict_first();
+      // weights read by one CTA stream through L2 (evict first); weights shared by
+      // several chunks of one expert stay for the co-scheduled CTAs (evict normal)
+      const uint64_t pol_w = p.w_shared ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
       Ring wr, br;
       wr.idx = br.idx = id;

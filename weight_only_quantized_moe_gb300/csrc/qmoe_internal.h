@@ -91,6 +91,7 @@ struct GemmParams {
   int32_t fault_injection;   // 1: CTA 0 arms its first stage without copies (failure-path test)
   int32_t out_bf16;          // kEpiLinearOut: output type bf16 (else f16)
   int32_t dq_sets;           // dequant sets (2 of 8 half-row warps, or 4 of 4 full-row warps)
+  int32_t w_shared;          // 1: an expert's weight tiles are read by several chunks (L2 evict-normal)
 };
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
@@ -121,6 +122,14 @@ cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, c
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
                           int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
                           cudaStream_t stream);
+
+// moe_align and the gather fused for small batches (P <= 1024 pairs, shared memory permitting).
+bool align_gather_small_fits(int32_t P, int32_t E, int32_t block, int32_t H, bool act_order);
+cudaError_t launch_align_gather_small(const int32_t* topk_ids, int32_t P, int32_t E, int32_t block, int64_t capacity,
+                                      int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                                      int32_t token_tile, Chunk* chunks, int32_t* n_chunks, int32_t* status,
+                                      const void* x, bool bf16, const int32_t* perm13, int32_t top_k, int32_t H,
+                                      int64_t cap_rows, void* xg, float* xscale, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
                                int32_t I, float* inter32, int num_sms, cudaStream_t stream);
