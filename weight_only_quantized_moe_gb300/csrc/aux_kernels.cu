@@ -352,7 +352,8 @@ __global__ void __launch_bounds__(kGatherThreads)
   int32_t* s_off = s_cnt + E;            // [E] first row of each expert
   int32_t* s_cur = s_off + E;            // [E] scatter cursors
   int32_t* s_sorted = s_cur + E;         // [rows_max]
-  uint4* stage_base = reinterpret_cast<uint4*>(s_sorted + ((rows_max + 3) & ~3));  // act-order row buffers
+  // act-order row buffers (uint4): 16-byte aligned after the integer arrays
+  uint4* stage_base = reinterpret_cast<uint4*>(sm_i + ((P + 3 * E + rows_max + 3) & ~3));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
   pdl_wait();  // no-op unless launched as a dependent
@@ -495,7 +496,8 @@ __global__ void __launch_bounds__(256)
 
 size_t align_gather_small_smem(int32_t P, int32_t E, int32_t block, int32_t H, bool act_order) {
   const int64_t rows_max = static_cast<int64_t>(P) + static_cast<int64_t>(E) * (block - 1);
-  const size_t ints = static_cast<size_t>(P) + 3 * static_cast<size_t>(E) + ((rows_max + 3) & ~int64_t(3));
+  // the integer arrays, rounded up to 16 bytes where the row buffers start
+  const size_t ints = (static_cast<size_t>(P) + 3 * static_cast<size_t>(E) + static_cast<size_t>(rows_max) + 3) & ~size_t(3);
   return ints * 4 + (act_order ? static_cast<size_t>(kGatherThreads / 32) * H * 2 : 0);
 }
 
