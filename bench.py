@@ -292,7 +292,7 @@ MIN_TIMED_S = 0.3      # timed region per reported entry (clock samples every ~0
 MAX_ROTATION_BYTES = 24 << 30
 # dense linear layer (one weight matrix, no routing): dense and 2:4-sparse, 4 and 8 bits
 LINEAR_REPORTED = (("int4", 128, "f16"), ("int4s24", 128, "f16"), ("int8", -1, "bf16"), ("int8s24", -1, "bf16"))
-LINEAR_SHAPE = (16384, 4096)   # N output features, K input features
+LINEAR_SHAPE = (28672, 4096)   # N output features, K input features (a Mixtral-8x7B expert's gate+up)
 LINEAR_MS = (1, 16, 128)
 
 
