@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
     dll = ctypes.CDLL(N.LIB_PATH)
     missing = [n for n in names if not hasattr(dll, n)]
     assert not missing, missing
-    assert q.lib().qmoe_abi_version() == 1
+    assert q.lib().qmoe_abi_version() == 2
     for s in range(0, 8):
         assert q.status_string(s)
 
@@ -228,8 +228,8 @@ def test_pack_rejects_bad_zero_points():
 
 
 def test_options_layout_and_issuer_validation():
-    """qmoe_options is 8 int32 fields; the issuer-count knob is checked on the host."""
-    assert ctypes.sizeof(N.QmoeOptions) == 32
+    """qmoe_options is 16 int32 fields (9 knobs and 7 reserved); the knobs are checked on the host."""
+    assert ctypes.sizeof(N.QmoeOptions) == 64
     L = q.lib()
     ok = _layer_struct()
 
@@ -243,6 +243,11 @@ def test_options_layout_and_issuer_validation():
     assert size(4096, issuers=3) == 0          # 384 accumulator columns leave no room for A slots
     assert size(16, issuers=4) == 0
     assert size(16, issuers=-1) == 0
+    for bad in (dict(dq_sets=3), dict(weight_l2=3), dict(sparse_mma=3), dict(token_ring=4), dict(dq_sets=-1)):
+        assert size(16, **bad) == 0, bad
+    for good in (dict(dq_sets=2), dict(dq_sets=4), dict(weight_l2=1), dict(weight_l2=2), dict(sparse_mma=1),
+                 dict(sparse_mma=2), dict(token_ring=1)):
+        assert size(16, **good) > 0, good
 
 
 @pytest.mark.parametrize("act,gs", [("f16", 128), ("bf16", 128), ("f16", -1)])

@@ -150,6 +150,7 @@ struct Plan {
   int k = 0;
   int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0, b_stages = 0;
   int dq_sets = 2;
+  int sparse_mma = 0;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -246,6 +247,8 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
   // stages in conversion at once (measured on GB300: 3-10 % faster at every
   // size, most at decode), so they are chosen wherever the rings allow.
   if (o != nullptr && (o->weight_l2 < 0 || o->weight_l2 > 2)) return QMOE_ERR_INVALID_ARG;
+  if (o != nullptr && (o->sparse_mma < 0 || o->sparse_mma > 2)) return QMOE_ERR_INVALID_ARG;
+  p->sparse_mma = (o != nullptr && o->sparse_mma == 1) ? 1 : 0;
   const bool four_ok = (p->w_stages & ~3) >= 4 && p->b_stages % 4 == 0;
   p->dq_sets = four_ok ? 4 : 2;
   if (o != nullptr && o->dq_sets != 0) {
@@ -428,6 +431,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.ab_stages = pl.ab_stages;
   g1.b_stages = pl.b_stages;
   g1.dq_sets = pl.dq_sets;
+  g1.sparse_mma = pl.sparse_mma;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -634,6 +638,7 @@ qmoe_status linear_forward_impl(const qmoe_linear* L, const void* x, int64_t M, 
   g.ab_stages = pl.ab_stages;
   g.b_stages = pl.b_stages;
   g.dq_sets = pl.dq_sets;
+  g.sparse_mma = pl.sparse_mma;
   g.fault_injection = 0;
   g.stage_bytes = pl.stage_bytes;
   g.P = P;

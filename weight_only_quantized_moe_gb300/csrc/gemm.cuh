@@ -76,6 +76,7 @@ constexpr int kMmaWarp3 = 24;
 constexpr int kDequantWarp0 = 8;   // warps 8..23: two sets of 8 or four sets of 4
 constexpr int kMaxIssuers = 3;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescSparse = 1u << 2;  // instruction descriptor: A is 2:4 structured sparse
 constexpr int kBarrierBytes = 1024;
 
 __host__ __device__ inline uint32_t gemm_w_slot(int group_bytes) { return (group_bytes + 1023u) & ~1023u; }
@@ -315,6 +316,48 @@ __device__ __forceinline__ void dequant_int8_24_half(const uint4 (&pk)[2], const
   }
 }
 
+// Sparse-MMA form of the 2:4 formats: a row's half (64 K, 16 groups) becomes 16
+// f16x2 values, the two kept values of group g (first, second) in value g, no
+// placement; the tensor core reads the positions from the metadata word.
+template <bool BF16S>
+__device__ __forceinline__ void dequant_int4_24_vals_half(const uint4& pk, uint32_t sbits, uint32_t (&out)[16]) {
+  const uint32_t bias_bits = 0x64086408u;  // 1024 + 8
+  const uint32_t m64z = 0xD480D480u;       // -(64 + 8)
+  const uint16_t s16 = BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16))) : static_cast<uint16_t>(sbits);
+  const uint32_t s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
+  const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    cvt_int4_word_half(w[j], bias_bits, m64z, s2bits, out[4 * j], out[4 * j + 1]);
+    cvt_int4_word_half(w[j] >> 8, bias_bits, m64z, s2bits, out[4 * j + 2], out[4 * j + 3]);
+  }
+}
+
+template <bool GS, bool BF16S>
+__device__ __forceinline__ void dequant_int8_24_vals_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t (&out)[16]) {
+  uint32_t s2bits = 0;
+  if (GS) {
+    const uint16_t s16 =
+        BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16))) : static_cast<uint16_t>(sbits);
+    s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cvt_int8_word<GS>(w[j], s2bits, out[8 * c + 2 * j], out[8 * c + 2 * j + 1]);
+  }
+}
+
+// The 4 sparse MMAs of one stage (K = 32 of the dense matrix each): the A slot holds
+// the kept values in columns 0..31 (8 per MMA) and the position words in 32..35.
+__device__ __forceinline__ void mma_stage_sp(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts_sp_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 1) * 64 + (kk & 1) * 4),
+                  a + 32u + static_cast<uint32_t>(kk), idesc, kk > 0 ? 1u : acc0);
+}
+
 // The 8 MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
 // between two tcgen05.mma instructions roughly triples their issue cost.  The
 // A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
@@ -388,6 +431,7 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 template <int KIND, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
   constexpr bool INT4 = KIND == kQ4 || KIND == kQ4Z;
+  constexpr bool SPARSE = KIND == kQ4S || KIND == kQ8S || KIND == kQ8SG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -544,7 +588,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // token tile [8-row group][64-K block][8 rows][128 B]: 8-row groups 2048 bytes apart
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
-          mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
+          if (SPARSE && p.sparse_mma)
+            mma_stage_sp(d_tmem, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
+          else
+            mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
           acc0 = 1u;
           mma_commit(smem_u32(done + br.idx));
         }
@@ -583,6 +630,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     dr.phase = 1u;
     int g0 = 0;
     bool ok = true;
+    // A-slot wait (first half) and the sparse-MMA store of one half: kept values to
+    // columns 16h .. 16h+15 of the A slot, the two position words to 32 + 2h, 33 + 2h
+    auto sparse_store = [&](int half, int hfirst, const uint2& pos, const uint32_t (&vals)[16]) -> bool {
+      if (NB2 != NB && half == hfirst) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+        if (!ok) return false;
+        tc_fence_after();
+      }
+      const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64);
+      tmem_st_32x32b_x16(ta + static_cast<uint32_t>(16 * half), vals);
+      tmem_st_32x32b_x2(ta + 32u + static_cast<uint32_t>(2 * half), pos.x, pos.y);
+      return true;
+    };
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
@@ -612,6 +672,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 6144 + row * 2);
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+            if (p.sparse_mma) {
+              uint32_t vals[16];
+              dequant_int4_24_vals_half<BF16S>(pk, sbits, vals);
+              if (!sparse_store(half, h0, pos, vals)) break;
+              continue;
+            }
             dequant_int4_24_half<BF16S>(pk, pos, sbits, sel_tab, out);
           } else if (KIND == kQ8S || KIND == kQ8SG) {
             uint4 pk[2];
@@ -622,6 +688,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             const uint32_t sbits = (KIND == kQ8SG) ? *reinterpret_cast<const uint16_t*>(wst + 10240 + row * 2) : 0u;
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
+            if (p.sparse_mma) {
+              uint32_t vals[16];
+              dequant_int8_24_vals_half<KIND == kQ8SG, BF16S>(pk, sbits, vals);
+              if (!sparse_store(half, h0, pos, vals)) break;
+              continue;
+            }
             dequant_int8_24_half<KIND == kQ8SG, BF16S>(pk, pos, sbits, sel_tab, out);
           } else {
             uint4 pk[4];
