@@ -171,12 +171,7 @@ typedef struct {
    * a weight tile find it in L2; evict-first otherwise), 1 evict-normal,
    * 2 evict-first.  Other values give QMOE_ERR_INVALID_ARG. */
   int32_t weight_l2;
-  /* 2:4-sparse formats: 1 feeds the kept values and their positions to the
-   * tensor core's structured-sparse MMA (K = 32 per instruction, no placement
-   * work); 2 places the kept values into a dense tile with byte permutes and
-   * runs the dense MMA; 0 automatic. */
-  int32_t sparse_mma;
-  int32_t reserved[7];
+  int32_t reserved[8];  /* must be zero */
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */

@@ -228,7 +228,7 @@ def test_pack_rejects_bad_zero_points():
 
 
 def test_options_layout_and_issuer_validation():
-    """qmoe_options is 16 int32 fields (9 knobs and 7 reserved); the knobs are checked on the host."""
+    """qmoe_options is 16 int32 fields (8 knobs and 8 reserved); the knobs are checked on the host."""
     assert ctypes.sizeof(N.QmoeOptions) == 64
     L = q.lib()
     ok = _layer_struct()
@@ -243,11 +243,24 @@ def test_options_layout_and_issuer_validation():
     assert size(4096, issuers=3) == 0          # 384 accumulator columns leave no room for A slots
     assert size(16, issuers=4) == 0
     assert size(16, issuers=-1) == 0
-    for bad in (dict(dq_sets=3), dict(weight_l2=3), dict(sparse_mma=3), dict(token_ring=4), dict(dq_sets=-1)):
+    for bad in (dict(dq_sets=3), dict(weight_l2=3), dict(token_ring=4), dict(dq_sets=-1)):
         assert size(16, **bad) == 0, bad
-    for good in (dict(dq_sets=2), dict(dq_sets=4), dict(weight_l2=1), dict(weight_l2=2), dict(sparse_mma=1),
-                 dict(sparse_mma=2), dict(token_ring=1)):
+    for good in (dict(dq_sets=2), dict(dq_sets=4), dict(weight_l2=1), dict(weight_l2=2), dict(token_ring=1)):
         assert size(16, **good) > 0, good
+
+
+def _sparse_position(area, r, G):
+    """Position nibble (i0 | i1 << 2) of group G (0..31, 4 input channels each) of row r in a
+    2048-byte position area, in the order the structured-sparse MMA reads it: MMA k = G // 8 covers
+    groups 8k .. 8k+7 as sub-blocks s = (G // 4) % 2; lane L = 16b + 8s + i holds sub-block s of row
+    16b + i in bits 0-15 and of row 16b + 8 + i in bits 16-31; its word for MMA k is at byte
+    (k // 2) * 1024 + 8L + 4 (k % 2)."""
+    k, s, t = G // 8, (G // 4) % 2, G % 4
+    b, hi, i = r // 16, (r // 8) % 2, r % 8
+    L = 16 * b + 8 * s + i
+    off = (k // 2) * 1024 + 8 * L + 4 * (k % 2)
+    word = int.from_bytes(bytes(area[off:off + 4]), "little")
+    return (word >> (16 * hi + 4 * t)) & 15
 
 
 @pytest.mark.parametrize("act,gs", [("f16", 128), ("bf16", 128), ("f16", -1)])
@@ -267,7 +280,6 @@ def test_pack_int4_24_round_trip_and_layout(act, gs):
     for r in (0, 77, 127):
         for h in (0, 1):
             codes = blk[(h * 128 + r) * 16:(h * 128 + r) * 16 + 16]
-            pos = int.from_bytes(bytes(blk[4096 + (h * 128 + r) * 8:4096 + (h * 128 + r) * 8 + 8]), "little")
             vals = np.zeros((1, 32), np.uint8)
             positions = np.zeros((1, 16, 2), np.int64)
             for g in range(16):
@@ -275,7 +287,7 @@ def test_pack_int4_24_round_trip_and_layout(act, gs):
                 word = int.from_bytes(bytes(codes[4 * j:4 * j + 4]), "little")
                 vals[0, 2 * g] = (word >> (4 * i)) & 15
                 vals[0, 2 * g + 1] = (word >> (4 * (i + 4))) & 15
-                m = (pos >> (4 * g)) & 15
+                m = _sparse_position(blk[4096:6144], r, 16 * h + g)
                 positions[0, g] = (m & 3, m >> 2)
                 assert (m & 3) < (m >> 2)
             dense = oracle.decompress_24(vals, positions)
@@ -448,13 +460,13 @@ def test_pack_int8_24_round_trip_and_layout(gs, act):
         assert np.array_equal(s13, s13b) and np.array_equal(s2, s2b)
     assert np.array_equal(q13, L.q13) and np.array_equal(q2, L.q2)
     # documented layout of W2, expert 0, tile 0, K stage 0: row r, half h, group g:
-    # kept codes at bytes (h*128 + r)*32 + 2g + {0,1}; positions nibble g at 8192 + (h*128 + r)*8
+    # kept codes at bytes (h*128 + r)*32 + 2g + {0,1}; positions in the sparse-MMA lane order at 8192
     blk = pk["w2"][:10240 if gs == -1 else 10496]
-    for r in (0, 77):
+    for r in (0, 77, 8, 127):
         for h in (0, 1):
-            pos = int.from_bytes(bytes(blk[8192 + (h * 128 + r) * 8: 8192 + (h * 128 + r) * 8 + 8]), "little")
             for g in range(16):
-                i0, i1 = (pos >> (4 * g)) & 3, (pos >> (4 * g + 2)) & 3
+                m = _sparse_position(blk[8192:10240], r, 16 * h + g)
+                i0, i1 = m & 3, m >> 2
                 assert i0 < i1
                 c4 = L.q2[0, r, 64 * h + 4 * g: 64 * h + 4 * g + 4]
                 v = blk[(h * 128 + r) * 32 + 2 * g: (h * 128 + r) * 32 + 2 * g + 2].view(np.int8)

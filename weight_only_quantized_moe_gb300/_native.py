@@ -59,7 +59,7 @@ class QmoePlanInfo(ctypes.Structure):
 class QmoeOptions(ctypes.Structure):
     _fields_ = [("split1", c_int32), ("split2", c_int32), ("token_tile", c_int32), ("fault_injection", c_int32),
                 ("issuers", c_int32), ("token_ring", c_int32), ("dq_sets", c_int32),
-                ("weight_l2", c_int32), ("sparse_mma", c_int32), ("reserved", c_int32 * 7)]
+                ("weight_l2", c_int32), ("reserved", c_int32 * 8)]
 
 
 class QmoeError(RuntimeError):

@@ -186,59 +186,6 @@ __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t
   }
 }
 
-// 2:4-sparse int4: a row's half (64 K, 16 groups of 4 channels) is 16 bytes of
-// kept codes and 8 bytes of positions.  Word j of the codes holds groups
-// 4j..4j+3 with nibble i the first kept code of group 4j+i and nibble i+4 its
-// second, so the int4 conversion above turns each word into four f16x2 values
-// (first kept, second kept) * s, one per group.  Position nibble g holds
-// i0 | i1 << 2 (the kept channels of group g); a 16-entry table maps it to two
-// byte-permute selectors that place the kept values at K 4g+i0 and 4g+i1 of
-// output columns 2g (K 4g, 4g+1) and 2g+1 (K 4g+2, 4g+3) and zeros elsewhere.
-// Table entry m: byte pair 0x10 picks the first kept value, 0x32 the second,
-// 0x54 a zero (from the permute's second operand).
-__host__ __device__ inline uint32_t sparse24_pair_selector(int m, int p) {
-  const int i0 = m & 3, i1 = m >> 2;
-  return p == i0 ? 0x10u : (p == i1 ? 0x32u : 0x54u);
-}
-
-template <bool BF16S>
-__device__ __forceinline__ void dequant_int4_24_half(const uint4& pk, const uint2& pos, uint32_t sbits,
-                                                     const uint2* sel_tab, uint32_t (&out)[32]) {
-  const uint32_t bias_bits = 0x64086408u;  // 1024 + 8
-  const uint32_t m64z = 0xD480D480u;       // -(64 + 8)
-  uint16_t s16;
-  if (BF16S) {
-    s16 = __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
-  } else {
-    s16 = static_cast<uint16_t>(sbits);
-  }
-  const uint32_t s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
-  const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t r[4];
-    cvt_int4_word_half(w[j], bias_bits, m64z, s2bits, r[0], r[1]);
-    cvt_int4_word_half(w[j] >> 8, bias_bits, m64z, s2bits, r[2], r[3]);
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int g = 4 * j + x;
-      const uint32_t m = ((g < 8 ? pos.x : pos.y) >> (4 * (g & 7))) & 15u;
-      const uint2 sel = sel_tab[m];
-      out[2 * g] = __byte_perm(r[x], 0u, sel.x);
-      out[2 * g + 1] = __byte_perm(r[x], 0u, sel.y);
-    }
-  }
-}
-
-// 2:4-sparse int8: a row's half (64 K, 16 groups of 4 channels) is 32 bytes
-// of kept codes and 8 bytes of positions.  Word j of the codes holds groups
-// 2j and 2j+1 as bytes (first kept, second kept) of each, so the int8
-// conversion below turns each word into two f16x2 values, one per group;
-// positions and placement as for 2:4-sparse int4 (the same selector table).
-template <bool GS, bool BF16S>
-__device__ __forceinline__ void dequant_int8_24_half(const uint4 (&pk)[2], const uint2& pos, uint32_t sbits,
-                                                     const uint2* sel_tab, uint32_t (&out)[32]);
-
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
 // conversion is exact: (0x64 << 8 | (q + 128)) - 1152 in f16.  A per-row
 // (per-column of W) scale is applied to the fp32 accumulator in the epilogue;
@@ -288,37 +235,15 @@ __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t
   }
 }
 
-template <bool GS, bool BF16S>
-__device__ __forceinline__ void dequant_int8_24_half(const uint4 (&pk)[2], const uint2& pos, uint32_t sbits,
-                                                     const uint2* sel_tab, uint32_t (&out)[32]) {
-  uint32_t s2bits = 0;
-  if (GS) {
-    const uint16_t s16 =
-        BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16))) : static_cast<uint16_t>(sbits);
-    s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
-  }
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t r[2];
-      cvt_int8_word<GS>(w[j], s2bits, r[0], r[1]);
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const int g = 8 * c + 2 * j + x;
-        const uint32_t m = ((g < 8 ? pos.x : pos.y) >> (4 * (g & 7))) & 15u;
-        const uint2 sel = sel_tab[m];
-        out[2 * g] = __byte_perm(r[x], 0u, sel.x);
-        out[2 * g + 1] = __byte_perm(r[x], 0u, sel.y);
-      }
-    }
-  }
-}
-
-// Sparse-MMA form of the 2:4 formats: a row's half (64 K, 16 groups) becomes 16
-// f16x2 values, the two kept values of group g (first, second) in value g, no
-// placement; the tensor core reads the positions from the metadata word.
+// 2:4-sparse formats: a row's half (64 K, 16 groups of 4 channels) holds the two
+// kept codes of each group and their positions.  The kept codes become 16 f16x2
+// values, value g = (first, second) kept value of group g, and go to tensor memory
+// as the structured-sparse MMA's A operand; the MMA reads the positions from the
+// metadata words the packer stores in its lane order, so no placement work is
+// done here.  int4: word j of the 16 code bytes holds groups 4j..4j+3 with nibble i
+// the first kept code of group 4j+i and nibble i+4 its second, so the int4
+// conversion turns each word into the values of four groups.  int8: word j of the
+// 32 code bytes holds groups 2j and 2j+1 as bytes (first, second) of each.
 template <bool BF16S>
 __device__ __forceinline__ void dequant_int4_24_vals_half(const uint4& pk, uint32_t sbits, uint32_t (&out)[16]) {
   const uint32_t bias_bits = 0x64086408u;  // 1024 + 8
@@ -455,8 +380,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint64_t* drain = accempty + 2;  // one per MMA issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  // 2:4-sparse int4: position -> byte-permute selectors, in the barrier area's last 128 bytes
-  uint2* sel_tab = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(wfull) + kBarrierBytes - 128);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -476,11 +399,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(drain + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
-  }
-  if ((KIND == kQ4S || KIND == kQ8S || KIND == kQ8SG) && threadIdx.x < 16) {
-    const int m = static_cast<int>(threadIdx.x);
-    sel_tab[m] = make_uint2(sparse24_pair_selector(m, 0) | (sparse24_pair_selector(m, 1) << 8),
-                            sparse24_pair_selector(m, 2) | (sparse24_pair_selector(m, 3) << 8));
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -588,7 +506,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // token tile [8-row group][64-K block][8 rows][128 B]: 8-row groups 2048 bytes apart
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
-          if (SPARSE && p.sparse_mma)
+          if (SPARSE)
             mma_stage_sp(d_tmem, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
           else
             mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
@@ -672,13 +590,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 6144 + row * 2);
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-            if (p.sparse_mma) {
-              uint32_t vals[16];
-              dequant_int4_24_vals_half<BF16S>(pk, sbits, vals);
-              if (!sparse_store(half, h0, pos, vals)) break;
-              continue;
-            }
-            dequant_int4_24_half<BF16S>(pk, pos, sbits, sel_tab, out);
+            uint32_t vals[16];
+            dequant_int4_24_vals_half<BF16S>(pk, sbits, vals);
+            if (!sparse_store(half, h0, pos, vals)) break;
+            continue;
           } else if (KIND == kQ8S || KIND == kQ8SG) {
             uint4 pk[2];
 #pragma unroll
@@ -688,13 +603,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             const uint32_t sbits = (KIND == kQ8SG) ? *reinterpret_cast<const uint16_t*>(wst + 10240 + row * 2) : 0u;
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-            if (p.sparse_mma) {
-              uint32_t vals[16];
-              dequant_int8_24_vals_half<KIND == kQ8SG, BF16S>(pk, sbits, vals);
-              if (!sparse_store(half, h0, pos, vals)) break;
-              continue;
-            }
-            dequant_int8_24_half<KIND == kQ8SG, BF16S>(pk, pos, sbits, sel_tab, out);
+            uint32_t vals[16];
+            dequant_int8_24_vals_half<KIND == kQ8SG, BF16S>(pk, sbits, vals);
+            if (!sparse_store(half, h0, pos, vals)) break;
+            continue;
           } else {
             uint4 pk[4];
 #pragma unroll

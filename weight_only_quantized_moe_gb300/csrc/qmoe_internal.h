@@ -92,7 +92,6 @@ struct GemmParams {
   int32_t out_bf16;          // kEpiLinearOut: output type bf16 (else f16)
   int32_t dq_sets;           // dequant sets (2 of 8 half-row warps, or 4 of 4 full-row warps)
   int32_t w_shared;          // 1: an expert's weight tiles are read by several chunks (L2 evict-normal)
-  int32_t sparse_mma;        // 2:4 formats: 1 = kept values + position metadata to the sparse MMA
 };
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
