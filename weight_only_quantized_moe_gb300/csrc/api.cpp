@@ -374,6 +374,8 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   float* iscale = reinterpret_cast<float*>(base + pl.off_iscale);
   float* h = reinterpret_cast<float*>(base + pl.off_h);
   float* y = reinterpret_cast<float*>(base + pl.off_y);
+  float* c13 = nullptr;  // per-group corrections of the token operands (per-group-scaled int4 GEMM)
+  float* c2 = nullptr;
   const bool bf16 = L->act_dtype == QMOE_BF16;
   const int P = static_cast<int>(pl.P);
 
@@ -388,7 +390,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
     // small batch: grouping and gather in one kernel (launch 1 then takes no time)
     rec(0);
     err = launch_align_gather_small(topk_ids, P, L->E, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch,
-                                    status, x, bf16, L->perm13, k, L->H, pl.cap, xg, xscale, sms, stream);
+                                    status, x, bf16, L->perm13, k, L->H, pl.cap, xg, xscale, c13, sms, stream);
     rec(1);
     launched += (err == cudaSuccess);
     rec(2);
@@ -400,8 +402,8 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
     launched += (err == cudaSuccess);
     rec(2);
     if (err == cudaSuccess) {
-      err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, sms,
-                          stream);
+      err = launch_gather(x, bf16, sorted, expert, npp, L->perm13, P, k, L->H, kAlignBlock, pl.cap, xg, xscale, c13,
+                          sms, stream);
       launched += (err == cudaSuccess);
     }
     rec(3);
@@ -480,7 +482,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(7);
   rec(8);
   if (err == cudaSuccess) {
-    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, sms, stream);
+    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, c2, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(9);
@@ -605,12 +607,12 @@ qmoe_status linear_forward_impl(const qmoe_linear* L, const void* x, int64_t M, 
   cudaError_t err;
   if (align_gather_small_fits(P, 1, kAlignBlock, L->K, L->perm != nullptr)) {
     err = launch_align_gather_small(nullptr, P, 1, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status,
-                                    x, bf16, L->perm, 1, L->K, pl.cap, xg, xscale, sms, stream);
+                                    x, bf16, L->perm, 1, L->K, pl.cap, xg, xscale, nullptr, sms, stream);
   } else {
     err = launch_align(nullptr, P, 1, kAlignBlock, pl.cap, sorted, expert, npp, pl.T, chunks, nch, status, stream);
     if (err == cudaSuccess)
-      err = launch_gather(x, bf16, sorted, expert, npp, L->perm, P, 1, L->K, kAlignBlock, pl.cap, xg, xscale, sms,
-                          stream);
+      err = launch_gather(x, bf16, sorted, expert, npp, L->perm, P, 1, L->K, kAlignBlock, pl.cap, xg, xscale, nullptr,
+                          sms, stream);
   }
   GemmParams g{};
   g.w = static_cast<const uint8_t*>(L->w);

@@ -228,17 +228,52 @@ __device__ __forceinline__ uint4 scale_to_f16x8(const uint16_t (&e)[8], float in
   return o;
 }
 
+// Token operand of the per-group-scaled int4 GEMM (16-row token tiles, symmetric
+// int4): the GEMM feeds the MMA the raw magic-number halves of the codes, 1024 + q
+// at input channels k with k % 4 in {0, 1} and 1024 + 16 q at k % 4 in {2, 3}, so
+// the token values at the second kind are stored divided by 16 (exact, a power
+// of two) and, per row and 128-channel group g, the correction
+//     C[g][row] = 1032 * X_lo + 72 * X_hi,
+// X_lo / X_hi = the sums of the row's stored values over the group's channels of
+// each kind (the X_hi values taken before the division), satisfies
+//     sum_k (q_k - 8) x_k = D - C,   D = the MMA's sum of (magic half) * (stored value).
+// A 16-byte piece holds channels 8c .. 8c+7: words 1 and 3 are the divided kind.
+__device__ __forceinline__ void pg_piece(uint4& o, float& xlo, float& xhi) {
+  const __half2 sixteenth = __float2half2_rn(0.0625f);
+  __half2 w1 = *reinterpret_cast<__half2*>(&o.y), w3 = *reinterpret_cast<__half2*>(&o.w);
+  w1 = __hmul2(w1, sixteenth);
+  w3 = __hmul2(w3, sixteenth);
+  o.y = *reinterpret_cast<uint32_t*>(&w1);
+  o.w = *reinterpret_cast<uint32_t*>(&w3);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&o.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&o.z));
+  const float2 c1 = __half22float2(w1), c3 = __half22float2(w3);
+  xlo += (a.x + a.y) + (b.x + b.y);
+  xhi += 16.0f * ((c1.x + c1.y) + (c3.x + c3.y));
+}
+
+// Sum over the 16 lanes of each half warp (the 16 pieces of one 128-channel group).
+__device__ __forceinline__ float half_warp_sum(float v) {
+#pragma unroll
+  for (int d = 8; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
 // One row of the gather, by one warp: x[p / top_k] scaled into f16 (permuted by
 // perm_e when given, through the warp's shared-memory row buffer `stage`), or
-// zeros for a padding row (p >= P).
+// zeros for a padding row (p >= P).  With pg_corr the row is stored in the
+// per-group-scaled layout above and its corrections go to pg_corr[g * cap + row].
 template <bool BF16>
 __device__ __forceinline__ void gather_one_row(const uint16_t* __restrict__ x, int p, int row, int P, int top_k, int H,
                                                int64_t cap, const int32_t* __restrict__ perm_e, uint4* stage,
-                                               uint8_t* __restrict__ xg, float* __restrict__ xscale, int lane) {
+                                               uint8_t* __restrict__ xg, float* __restrict__ xscale,
+                                               float* __restrict__ pg_corr, int lane) {
   if (p >= P) {
     for (int c = lane; c < H / 8; c += 32)
       *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = make_uint4(0, 0, 0, 0);
     if (lane == 0) xscale[row] = 1.0f;
+    if (pg_corr != nullptr)
+      for (int g = lane; g < H / 128; g += 32) pg_corr[g * cap + row] = 0.0f;
     return;
   }
   const uint16_t* src = x + static_cast<int64_t>(p / top_k) * H;
@@ -257,24 +292,33 @@ __device__ __forceinline__ void gather_one_row(const uint16_t* __restrict__ x, i
   const float2 sc = row_exponent_scale(amax);
   const float inv = sc.y;
   if (lane == 0) xscale[row] = sc.x;
-  if (perm_e == nullptr) {
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 v = __ldg(s4 + c);
+  if (perm_e != nullptr) __syncwarp();  // the staged row is complete
+  const uint16_t* srow = reinterpret_cast<const uint16_t*>(stage);
+  const int4* pr4 = reinterpret_cast<const int4*>(perm_e);
+  // every lane runs every iteration (the per-group sums shuffle across the half warp)
+  for (int c0 = 0; c0 < H / 8; c0 += 32) {
+    const int c = c0 + lane;
+    float xlo = 0.0f, xhi = 0.0f;
+    if (c < H / 8) {
       uint16_t e[8];
-      *reinterpret_cast<uint4*>(e) = v;
-      *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
+      if (perm_e == nullptr) {
+        *reinterpret_cast<uint4*>(e) = __ldg(s4 + c);
+      } else {
+        const int4 ka = __ldg(pr4 + 2 * c), kb = __ldg(pr4 + 2 * c + 1);
+        e[0] = srow[ka.x]; e[1] = srow[ka.y]; e[2] = srow[ka.z]; e[3] = srow[ka.w];
+        e[4] = srow[kb.x]; e[5] = srow[kb.y]; e[6] = srow[kb.z]; e[7] = srow[kb.w];
+      }
+      uint4 o = scale_to_f16x8<BF16>(e, inv);
+      if (pg_corr != nullptr) pg_piece(o, xlo, xhi);
+      *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = o;
     }
-  } else {
-    __syncwarp();  // the staged row is complete
-    const uint16_t* srow = reinterpret_cast<const uint16_t*>(stage);
-    const int4* pr4 = reinterpret_cast<const int4*>(perm_e);
-    for (int c = lane; c < H / 8; c += 32) {
-      const int4 ka = __ldg(pr4 + 2 * c), kb = __ldg(pr4 + 2 * c + 1);
-      uint16_t e[8] = {srow[ka.x], srow[ka.y], srow[ka.z], srow[ka.w], srow[kb.x], srow[kb.y], srow[kb.z], srow[kb.w]};
-      *reinterpret_cast<uint4*>(xg + staged_offset(row, 8 * c, cap)) = scale_to_f16x8<BF16>(e, inv);
+    if (pg_corr != nullptr) {
+      const float corr = half_warp_sum(1032.0f * xlo + 72.0f * xhi);
+      const int g = (c0 >> 4) + (lane >> 4);  // the group of this half warp's 16 pieces
+      if ((lane & 15) == 0 && c < H / 8) pg_corr[g * cap + row] = corr;
     }
-    __syncwarp();  // before the next row overwrites the buffer
   }
+  if (perm_e != nullptr) __syncwarp();  // before the next row overwrites the buffer
 }
 
 template <bool BF16>
@@ -282,7 +326,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                   const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_post_padded,
                   const int32_t* __restrict__ perm13, int32_t P, int32_t top_k, int32_t H, int32_t B, int64_t cap,
-                  uint8_t* __restrict__ xg, float* __restrict__ xscale) {
+                  uint8_t* __restrict__ xg, float* __restrict__ xscale, float* __restrict__ pg_corr) {
   extern __shared__ uint4 row_buf[];  // act-order only: one token row per warp
   pdl_launch_dependents();
   pdl_wait();
@@ -293,7 +337,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   uint4* stage = perm13 != nullptr ? row_buf + (threadIdx.x >> 5) * (H / 8) : nullptr;
   for (int row = blockIdx.x * wpb + (threadIdx.x >> 5); row < total; row += warps) {
     const int32_t* perm_e = perm13 != nullptr ? perm13 + static_cast<int64_t>(expert_ids[row / B]) * H : nullptr;
-    gather_one_row<BF16>(x, sorted_ids[row], row, P, top_k, H, cap, perm_e, stage, xg, xscale, lane);
+    gather_one_row<BF16>(x, sorted_ids[row], row, P, top_k, H, cap, perm_e, stage, xg, xscale, pg_corr, lane);
   }
 }
 
@@ -342,7 +386,8 @@ __global__ void __launch_bounds__(kGatherThreads)
                               int32_t* __restrict__ num_post_padded, int32_t T, Chunk* __restrict__ chunks,
                               int32_t* __restrict__ n_chunks, int32_t* __restrict__ status,
                               const uint16_t* __restrict__ x, const int32_t* __restrict__ perm13, int32_t top_k,
-                              int32_t H, int64_t cap, uint8_t* __restrict__ xg, float* __restrict__ xscale) {
+                              int32_t H, int64_t cap, uint8_t* __restrict__ xg, float* __restrict__ xscale,
+                              float* __restrict__ pg_corr) {
   extern __shared__ __align__(16) int32_t sm_i[];
   __shared__ int warp_sums[kGatherThreads / 32];
   __shared__ int s_bad;
@@ -443,14 +488,14 @@ __global__ void __launch_bounds__(kGatherThreads)
       }
       perm_e = perm13 + static_cast<int64_t>(lo) * H;
     }
-    gather_one_row<BF16>(x, s_sorted[row], row, P, top_k, H, cap, perm_e, stage, xg, xscale, lane);
+    gather_one_row<BF16>(x, s_sorted[row], row, P, top_k, H, cap, perm_e, stage, xg, xscale, pg_corr, lane);
   }
 }
 
 cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
-                          cudaStream_t stream) {
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, float* pg_corr,
+                          int num_sms, cudaStream_t stream) {
   // act-order: each warp stages its token row in shared memory (H x 2 bytes per
   // warp, at most 8 warps and about 200 KB per block)
   int wpb = kGatherThreads / 32;
@@ -465,7 +510,7 @@ cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, c
   }
   return launch_kernel(kern, dim3(grid), dim3(32 * wpb), smem, stream, true, static_cast<const uint16_t*>(x),
                        sorted_ids, expert_ids, num_post_padded, perm13, P, top_k, H, block, cap_rows,
-                       static_cast<uint8_t*>(xg), xscale);
+                       static_cast<uint8_t*>(xg), xscale, pg_corr);
 }
 
 // ---------------------------------------------------------------------------
@@ -509,7 +554,8 @@ cudaError_t launch_align_gather_small(const int32_t* topk_ids, int32_t P, int32_
                                       int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
                                       int32_t token_tile, Chunk* chunks, int32_t* n_chunks, int32_t* status,
                                       const void* x, bool bf16, const int32_t* perm13, int32_t top_k, int32_t H,
-                                      int64_t cap_rows, void* xg, float* xscale, int num_sms, cudaStream_t stream) {
+                                      int64_t cap_rows, void* xg, float* xscale, float* pg_corr, int num_sms,
+                                      cudaStream_t stream) {
   const size_t smem = align_gather_small_smem(P, E, block, H, perm13 != nullptr);
   const int wpb = kGatherThreads / 32;
   const int64_t want = (cap_rows + wpb - 1) / wpb;
@@ -522,7 +568,8 @@ cudaError_t launch_align_gather_small(const int32_t* topk_ids, int32_t P, int32_
   // first kernel of a forward: ordinary stream order behind the caller's work
   return launch_kernel(kern, dim3(grid), dim3(kGatherThreads), smem, stream, false, topk_ids, P, E, block, capacity,
                        sorted_ids, expert_ids, num_post_padded, token_tile, chunks, n_chunks, status,
-                       static_cast<const uint16_t*>(x), perm13, top_k, H, cap_rows, static_cast<uint8_t*>(xg), xscale);
+                       static_cast<const uint16_t*>(x), perm13, top_k, H, cap_rows, static_cast<uint8_t*>(xg), xscale,
+                       pg_corr);
 }
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
@@ -542,7 +589,7 @@ constexpr int kRescaleThreads = 256;
 __global__ void __launch_bounds__(kRescaleThreads)
     inter_rescale_kernel(const float* __restrict__ inter32, const int32_t* __restrict__ num_post_padded,
                          const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I, int64_t cap,
-                         uint8_t* __restrict__ inter16, float* __restrict__ iscale) {
+                         uint8_t* __restrict__ inter16, float* __restrict__ iscale, float* __restrict__ pg_corr) {
   __shared__ float red[kRescaleThreads / 32];
   pdl_launch_dependents();
   pdl_wait();
@@ -553,6 +600,8 @@ __global__ void __launch_bounds__(kRescaleThreads)
       for (int c = threadIdx.x; c < I / 8; c += kRescaleThreads)
         *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, cap)) = make_uint4(0, 0, 0, 0);
       if (threadIdx.x == 0) iscale[row] = 1.0f;
+      if (pg_corr != nullptr)
+        for (int g = threadIdx.x; g < I / 128; g += kRescaleThreads) pg_corr[g * cap + row] = 0.0f;
       continue;
     }
     const float4* s4 = reinterpret_cast<const float4*>(inter32 + static_cast<int64_t>(row) * I);
@@ -570,24 +619,34 @@ __global__ void __launch_bounds__(kRescaleThreads)
     __syncthreads();  // red is reused by the next row
     const float2 sc = row_exponent_scale(amax);
     if (threadIdx.x == 0) iscale[row] = sc.x;
-    for (int c = threadIdx.x; c < I / 8; c += kRescaleThreads) {
-      const float4 a = __ldg(s4 + 2 * c), b = __ldg(s4 + 2 * c + 1);
-      uint4 o;
-      o.x = static_cast<uint32_t>(f16_bits(a.x * sc.y)) | (static_cast<uint32_t>(f16_bits(a.y * sc.y)) << 16);
-      o.y = static_cast<uint32_t>(f16_bits(a.z * sc.y)) | (static_cast<uint32_t>(f16_bits(a.w * sc.y)) << 16);
-      o.z = static_cast<uint32_t>(f16_bits(b.x * sc.y)) | (static_cast<uint32_t>(f16_bits(b.y * sc.y)) << 16);
-      o.w = static_cast<uint32_t>(f16_bits(b.z * sc.y)) | (static_cast<uint32_t>(f16_bits(b.w * sc.y)) << 16);
-      *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, cap)) = o;
+    // every thread runs every iteration (the per-group sums shuffle across half warps)
+    for (int c0 = 0; c0 < I / 8; c0 += kRescaleThreads) {
+      const int c = c0 + threadIdx.x;
+      float xlo = 0.0f, xhi = 0.0f;
+      if (c < I / 8) {
+        const float4 a = __ldg(s4 + 2 * c), b = __ldg(s4 + 2 * c + 1);
+        uint4 o;
+        o.x = static_cast<uint32_t>(f16_bits(a.x * sc.y)) | (static_cast<uint32_t>(f16_bits(a.y * sc.y)) << 16);
+        o.y = static_cast<uint32_t>(f16_bits(a.z * sc.y)) | (static_cast<uint32_t>(f16_bits(a.w * sc.y)) << 16);
+        o.z = static_cast<uint32_t>(f16_bits(b.x * sc.y)) | (static_cast<uint32_t>(f16_bits(b.y * sc.y)) << 16);
+        o.w = static_cast<uint32_t>(f16_bits(b.z * sc.y)) | (static_cast<uint32_t>(f16_bits(b.w * sc.y)) << 16);
+        if (pg_corr != nullptr) pg_piece(o, xlo, xhi);
+        *reinterpret_cast<uint4*>(inter16 + staged_offset(row, 8 * c, cap)) = o;
+      }
+      if (pg_corr != nullptr) {
+        const float corr = half_warp_sum(1032.0f * xlo + 72.0f * xhi);
+        if ((threadIdx.x & 15) == 0 && c < I / 8) pg_corr[(c >> 4) * cap + row] = corr;
+      }
     }
   }
 }
 
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
-                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
-                                 cudaStream_t stream) {
+                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, float* pg_corr,
+                                 int num_sms, cudaStream_t stream) {
   const int grid = static_cast<int>(cap_rows < 8LL * num_sms ? (cap_rows > 0 ? cap_rows : 1) : 8LL * num_sms);
   return launch_kernel(inter_rescale_kernel, dim3(grid), dim3(kRescaleThreads), 0, stream, true, inter32,
-                       num_post_padded, sorted_ids, P, I, cap_rows, static_cast<uint8_t*>(inter16), iscale);
+                       num_post_padded, sorted_ids, P, I, cap_rows, static_cast<uint8_t*>(inter16), iscale, pg_corr);
 }
 
 // ---------------------------------------------------------------------------

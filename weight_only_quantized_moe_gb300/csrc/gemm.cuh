@@ -275,12 +275,13 @@ __device__ __forceinline__ void dequant_int8_24_vals_half(const uint4 (&pk)[2], 
 }
 
 // The 4 sparse MMAs of one stage (K = 32 of the dense matrix each): the A slot holds
-// the kept values in columns 0..31 (8 per MMA) and the position words in 32..35.
+// the kept values in columns 0..31 (8 per MMA) and MMA kk's position words in
+// column 32 + 8 kk (8-column aligned, as the A operand's steps).
 __device__ __forceinline__ void mma_stage_sp(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)
     mma_ts_sp_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 1) * 64 + (kk & 1) * 4),
-                  a + 32u + static_cast<uint32_t>(kk), idesc, kk > 0 ? 1u : acc0);
+                  a + 32u + static_cast<uint32_t>(8 * kk), idesc, kk > 0 ? 1u : acc0);
 }
 
 // The 8 MMAs of one stage (K = 16 each) as one branch-free sequence: a branch
@@ -549,7 +550,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     int g0 = 0;
     bool ok = true;
     // A-slot wait (first half) and the sparse-MMA store of one half: kept values to
-    // columns 16h .. 16h+15 of the A slot, the two position words to 32 + 2h, 33 + 2h
+    // columns 16h .. 16h+15 of the A slot, the position words of MMAs 2h and 2h+1 to
+    // columns 32 + 16h and 40 + 16h
     auto sparse_store = [&](int half, int hfirst, const uint2& pos, const uint32_t (&vals)[16]) -> bool {
       if (NB2 != NB && half == hfirst) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
@@ -558,7 +560,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       }
       const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64);
       tmem_st_32x32b_x16(ta + static_cast<uint32_t>(16 * half), vals);
-      tmem_st_32x32b_x2(ta + 32u + static_cast<uint32_t>(2 * half), pos.x, pos.y);
+      tmem_st_32x32b_x1(ta + 32u + static_cast<uint32_t>(16 * half), pos.x);
+      tmem_st_32x32b_x1(ta + 40u + static_cast<uint32_t>(16 * half), pos.y);
       return true;
     };
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {

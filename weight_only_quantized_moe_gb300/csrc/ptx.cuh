@@ -186,7 +186,8 @@ __device__ __forceinline__ void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uin
 
 // D[tmem] (+)= A[tmem] * B[smem]^T with 2:4 structured sparsity in A: M = 128, N from idesc,
 // K = 32 of the dense matrix per instruction (16-bit types); A holds the 16 kept values of each
-// row (8 TMEM columns) and `meta_tmem` the 32-bit position word of each row (one column).
+// row (8 TMEM columns) and `meta_tmem` the 32-bit position words (one column, 8-column aligned
+// like the A operand's steps).
 __device__ __forceinline__ void mma_ts_sp_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t meta_tmem,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -253,9 +254,9 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       : "memory");
 }
 
-// Warp-collective TMEM store: 2 consecutive 32-bit columns per lane.
-__device__ __forceinline__ void tmem_st_32x32b_x2(uint32_t taddr, uint32_t v0, uint32_t v1) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v0), "r"(v1) : "memory");
+// Warp-collective TMEM store: one 32-bit column per lane.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

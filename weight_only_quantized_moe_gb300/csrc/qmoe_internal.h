@@ -120,8 +120,8 @@ cudaError_t launch_align(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
 
 cudaError_t launch_gather(const void* x, bool bf16, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* num_post_padded, const int32_t* perm13, int32_t P, int32_t top_k,
-                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, int num_sms,
-                          cudaStream_t stream);
+                          int32_t H, int32_t block, int64_t cap_rows, void* xg, float* xscale, float* pg_corr,
+                          int num_sms, cudaStream_t stream);
 
 // moe_align and the gather fused for small batches (P <= 1024 pairs, shared memory permitting).
 bool align_gather_small_fits(int32_t P, int32_t E, int32_t block, int32_t H, bool act_order);
@@ -129,14 +129,15 @@ cudaError_t launch_align_gather_small(const int32_t* topk_ids, int32_t P, int32_
                                       int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
                                       int32_t token_tile, Chunk* chunks, int32_t* n_chunks, int32_t* status,
                                       const void* x, bool bf16, const int32_t* perm13, int32_t top_k, int32_t H,
-                                      int64_t cap_rows, void* xg, float* xscale, int num_sms, cudaStream_t stream);
+                                      int64_t cap_rows, void* xg, float* xscale, float* pg_corr, int num_sms,
+                                      cudaStream_t stream);
 
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
                                int32_t I, float* inter32, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
-                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, int num_sms,
-                                 cudaStream_t stream);
+                                 int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, float* pg_corr,
+                                 int num_sms, cudaStream_t stream);
 
 cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E, int32_t split, int64_t M,
                               int32_t top_k, int32_t H, bool bf16, void* out, int num_sms, cudaStream_t stream);
