@@ -97,6 +97,16 @@ def test_forward_two_dequant_sets(qt, act, ao, gs, M, split1, split2, tile):
     _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile, dq_sets=2))
 
 
+@pytest.mark.parametrize("act,ao,gs", [("f16", False, 128), ("bf16", True, 128), ("f16", False, -1), ("bf16", False, -1)])
+@pytest.mark.parametrize("M,split1,split2", [(1, 0, 0), (7, 0, 0), (40, 0, 0), (40, 3, 2), (16, 1, 1), (33, 2, 5)])
+@pytest.mark.parametrize("epi", [1, 2])
+def test_int4_group_epilogue_on_and_off(act, ao, gs, M, split1, split2, epi):
+    """Symmetric int4 at 16-row token tiles with the per-group fp32 scaling epilogue
+    (raw magic-number A, tokens pre-divided by 16 at the x16 positions, per-stage
+    TMEM sums) and without it."""
+    _check(_wl("int4", act, ao, gs=gs), M, opts=q.make_options(split1, split2, 16, int4_group_epilogue=epi))
+
+
 @pytest.mark.parametrize("qt,act", [("int8", "f16"), ("int8", "bf16")])
 def test_int8_token_tile_128_single_accumulator_per_issuer(qt, act):
     # 128-row chunks: each MMA issuer has one TMEM accumulator, summed by the epilogue

@@ -150,11 +150,12 @@ struct Plan {
   int k = 0;
   int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0, b_stages = 0;
   int dq_sets = 2;
+  int pg = 0, d_col0 = 0;
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
   size_t off_status = 0, off_sorted = 0, off_expert = 0, off_scalars = 0, off_chunks = 0, off_xg = 0, off_xscale = 0,
-         off_inter32 = 0, off_inter16 = 0, off_iscale = 0, off_h = 0, off_y = 0, total = 0;
+         off_inter32 = 0, off_inter16 = 0, off_iscale = 0, off_h = 0, off_y = 0, off_c13 = 0, off_c2 = 0, total = 0;
 };
 
 // Makespan, in pipeline stages, of n work items of k stages each split s ways
@@ -209,17 +210,26 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
     const int n = std::min(8, (512 - p->issuers * accb * T) / 64);
     return n / ring_mult * ring_mult;
   };
-  p->acc_bufs = a_slots(2) >= ring_mult ? 2 : 1;
-  p->a_col0 = p->issuers * p->acc_bufs * T;
-  p->ab_stages = a_slots(p->acc_bufs);
+  if (p->pg) {
+    // per-group scaling: no accumulators; each A slot has a 16-column D slot after the A slots
+    p->acc_bufs = 1;
+    p->a_col0 = 0;
+    p->ab_stages = std::min(8, 512 / (64 + 16)) / ring_mult * ring_mult;
+    p->d_col0 = 64 * p->ab_stages;
+  } else {
+    p->acc_bufs = a_slots(2) >= ring_mult ? 2 : 1;
+    p->a_col0 = p->issuers * p->acc_bufs * T;
+    p->ab_stages = a_slots(p->acc_bufs);
+  }
   if (p->ab_stages < ring_mult) return (o != nullptr && o->issuers != 0) ? QMOE_ERR_INVALID_ARG : QMOE_ERR_UNSUPPORTED;
   // Token-tile ring: a multiple m of the A ring, so that a token tile can be
   // fetched up to m - 1 A-ring laps before its MMAs and its L2 latency stays
   // off the A slots' cycle.  The deepest m <= 2 that leaves the weight ring at
   // least 8 slots (weights stream from HBM and want the deeper ring).
   const size_t wslot = (static_cast<size_t>(p->stage_bytes) + 1023) & ~size_t(1023);
+  const size_t extra = p->pg ? 16 * 128 * 4 : 0;  // per-group scales
   auto w_depth = [&](int nb2) {
-    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256;
+    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256 + extra;
     if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
     return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
   };
@@ -235,6 +245,7 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
         break;
       }
   }
+  if (p->pg && ring_m != 2) return QMOE_ERR_INVALID_ARG;  // its scale ring relies on the A-slot waits
   p->b_stages = ring_m * p->ab_stages;
   p->w_stages = w_depth(p->b_stages);
   if (p->w_stages < 2 || p->ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
@@ -279,6 +290,15 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   }
   p.T = T;
   p.stage_bytes = stage_bytes_of(L->qt, L->group_size);
+  // Per-group scaling (symmetric int4, 16-row token tiles): the dequant warps keep
+  // only the magic-number unpacks and the idle epilogue warps apply each group's
+  // scale in fp32 (measured on GB300: the scale multiply and zero-point subtract
+  // were ~12 % of the int4 decode GEMM's time).
+  if (o != nullptr && (o->int4_group_epilogue < 0 || o->int4_group_epilogue > 2)) return QMOE_ERR_INVALID_ARG;
+  // (its scale ring relies on a token-tile ring twice the A ring)
+  const bool ring_ok = o == nullptr || o->token_ring == 0 || o->token_ring == 2;
+  p.pg = (L->qt == QMOE_INT4_GROUP && T == 16 && ring_ok && !(o != nullptr && o->int4_group_epilogue == 2)) ? 1 : 0;
+  if (o != nullptr && o->int4_group_epilogue == 1 && !p.pg) return QMOE_ERR_INVALID_ARG;
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
@@ -324,6 +344,10 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.off_iscale = off;   off += al256(static_cast<size_t>(p.cap) * 4);
   p.off_h = off;        off += (p.S1 > 1) ? al256(static_cast<size_t>(p.S1) * p.cap * 2 * L->I * 4) : 0;
   p.off_y = off;        off += al256(static_cast<size_t>(p.S2) * P * L->H * 4);
+  if (p.pg) {
+    p.off_c13 = off;    off += al256(static_cast<size_t>(p.cap) * p.kst1 * 4);
+    p.off_c2 = off;     off += al256(static_cast<size_t>(p.cap) * p.kst2 * 4);
+  }
   p.total = off;
   *pl = p;
   return QMOE_OK;
@@ -374,8 +398,9 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   float* iscale = reinterpret_cast<float*>(base + pl.off_iscale);
   float* h = reinterpret_cast<float*>(base + pl.off_h);
   float* y = reinterpret_cast<float*>(base + pl.off_y);
-  float* c13 = nullptr;  // per-group corrections of the token operands (per-group-scaled int4 GEMM)
-  float* c2 = nullptr;
+  // per-group corrections of the token operands (per-group-scaled int4 GEMM)
+  float* c13 = pl.pg ? reinterpret_cast<float*>(base + pl.off_c13) : nullptr;
+  float* c2 = pl.pg ? reinterpret_cast<float*>(base + pl.off_c2) : nullptr;
   const bool bf16 = L->act_dtype == QMOE_BF16;
   const int P = static_cast<int>(pl.P);
 
@@ -430,6 +455,10 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.ab_stages = pl.ab_stages;
   g1.b_stages = pl.b_stages;
   g1.dq_sets = pl.dq_sets;
+  g1.pg = pl.pg;
+  g1.d_col0 = pl.d_col0;
+  g1.pg_corr = c13;
+  g1.pg_cap = pl.cap;
   g1.fault_injection = (opts != nullptr) ? opts->fault_injection : 0;
   g1.stage_bytes = pl.stage_bytes;
   g1.P = P;
@@ -459,6 +488,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g2.k_groups = pl.kst2;
   g2.split = pl.S2;
   g2.epi_mode = kEpiWeightedPairs;
+  g2.pg_corr = c2;
   g2.fault_injection = 0;
   g2.out = y;
   g2.out_ld = L->H;

@@ -80,10 +80,18 @@ constexpr uint32_t kIdescSparse = 1u << 2;  // instruction descriptor: A is 2:4 
 constexpr int kBarrierBytes = 1024;
 
 __host__ __device__ inline uint32_t gemm_w_slot(int group_bytes) { return (group_bytes + 1023u) & ~1023u; }
-// Dynamic shared memory: weight ring, token-tile ring, barriers (+1 KB alignment slack).
-__host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int b_stages, int token_tile) {
+// Per-group-scaled int4: one fp32 scale per row for each of the last 2 x (A slots)
+// stages (at most 16): the dequant warps write stage g's scales after the MMAs of
+// stage g - A slots completed, which happened after the epilogue had read stage
+// g - 2 x (A slots)'s scales (it reads a stage's scales before it releases the
+// stage's D slot, and the issuer waits for that release).
+constexpr int kPgScaleBytes = 16 * 128 * 4;
+// Dynamic shared memory: weight ring, token-tile ring, barriers, per-group scales
+// (per-group-scaled int4 only), +1 KB alignment slack.
+__host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int b_stages, int token_tile,
+                                                         bool pg) {
   return 1024 + static_cast<size_t>(w_stages) * gemm_w_slot(group_bytes) +
-         static_cast<size_t>(b_stages) * token_tile * 256 + kBarrierBytes;
+         static_cast<size_t>(b_stages) * token_tile * 256 + kBarrierBytes + (pg ? kPgScaleBytes : 0);
 }
 
 struct WorkItem {
@@ -235,6 +243,29 @@ __device__ __forceinline__ void dequant_int8_half(const uint4 (&pk)[4], uint32_t
   }
 }
 
+// Per-group-scaled int4 (16-row token tiles, zero point 8): half a stage row to
+// 32 TMEM columns of raw magic-number halves, 1024 + q at the low nibble of each
+// byte pair and 1024 + 16 q at the high one (two LOP3 per word and one shift for
+// the second pair); the scale, the zero point and the 1/16 are applied later, per
+// stage, by the epilogue (see the gather's per-group corrections).
+__device__ __forceinline__ void dequant_int4_raw_half(const uint4 (&pk)[2], uint32_t (&out)[32]) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w8 = w[j] >> 8;
+      asm("lop3.b32 %0, %4, 0x000F000F, 0x64006400, 0xEA;\n\t"
+          "lop3.b32 %1, %4, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+          "lop3.b32 %2, %5, 0x000F000F, 0x64006400, 0xEA;\n\t"
+          "lop3.b32 %3, %5, 0x00F000F0, 0x64006400, 0xEA;"
+          : "=r"(out[16 * c + 4 * j]), "=r"(out[16 * c + 4 * j + 1]), "=r"(out[16 * c + 4 * j + 2]),
+            "=r"(out[16 * c + 4 * j + 3])
+          : "r"(w[j]), "r"(w8));
+    }
+  }
+}
+
 // 2:4-sparse formats: a row's half (64 K, 16 groups of 4 channels) holds the two
 // kept codes of each group and their positions.  The kept codes become 16 f16x2
 // values, value g = (first, second) kept value of group g, and go to tensor memory
@@ -381,6 +412,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint64_t* drain = accempty + 2;  // one per MMA issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // per-group-scaled int4: the dequant warps leave each row's group scale here per A slot
+  float* pg_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(wfull) + kBarrierBytes);
+  const bool PG = INT4 && p.pg;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -391,7 +425,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_init(smem_u32(wfull + s), 1);
       mbar_init(smem_u32(wempty + s), wps);
     }
-    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), wps);
+    // with per-group scaling the 4 epilogue warps also release each A slot's D slot
+    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), wps + (PG ? 4u : 0u));
     for (int j = 0; j < NB2; ++j) mbar_init(smem_u32(done + j), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
@@ -491,11 +526,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
         const int b = (ACCB == 2) ? (itn & 1) : 0;
         const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
-        if (!mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
+        if (!PG && !mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
           ok = false;
           break;
         }
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
+        const uint32_t d_acc = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
         uint32_t acc0 = 0u;  // the issuer's first stage of the item overwrites its accumulator
         for (int g = first_own(g0, id, NI); g < g0 + n_st; g += NI, ar.step(NI, NB), br.step(NI, NB2)) {
           // the dequant set signals A only after the stage's token tile has landed
@@ -507,16 +542,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // token tile [8-row group][64-K block][8 rows][128 B]: 8-row groups 2048 bytes apart
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
-          if (SPARSE)
-            mma_stage_sp(d_tmem, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
-          else
-            mma_stage(d_tmem, a_tmem, bdesc0, idesc, acc0);
+          if (SPARSE) {
+            mma_stage_sp(d_acc, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
+          } else if (PG) {
+            // per-group scaling: the stage's sum goes to the D slot of its A slot, fresh
+            mma_stage(tmem + static_cast<uint32_t>(p.d_col0) + static_cast<uint32_t>(ar.idx * 16), a_tmem, bdesc0, idesc,
+                      0u);
+          } else {
+            mma_stage(d_acc, a_tmem, bdesc0, idesc, acc0);
+          }
           acc0 = 1u;
           mma_commit(smem_u32(done + br.idx));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
-        mma_commit(smem_u32(accfull + b));
+        if (!PG) mma_commit(smem_u32(accfull + b));
         g0 += n_st;
         ++itn;
       }
@@ -543,8 +583,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     // wr: weight slot of the stage; ar: its A slot; dr: the done barrier of the
     // stage NB earlier, the last one that used the same A slot (phase of lap -1,
     // which a fresh barrier reports complete, for the first NB stages)
-    Ring wr, ar, dr;
-    wr.idx = ar.idx = set;
+    Ring wr, ar, dr, sr;  // sr: the stage's per-group scale slot (2 x NB of them)
+    wr.idx = ar.idx = sr.idx = set;
     dr.idx = set - NB + NB2;
     dr.phase = 1u;
     int g0 = 0;
@@ -569,12 +609,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       decode_item(p, nch, i, it);
       const int n_st = it.ks1 - it.ks0;
       for (int g = first_own(g0, set, DS); g < g0 + n_st;
-           g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2)) {
+           g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2), sr.step(DS, 2 * NB)) {
         // weights and token tile landed
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint8_t* wst = wring + wr.idx * wslot;
+        float pg_sv = 0.0f;
         for (int half = h0; half < h1; ++half) {
           const bool last = half + 1 == h1;  // the weight slot is released after the last half's loads
           uint32_t out[32];
@@ -586,7 +627,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             const uint32_t zp = (KIND == kQ4Z) ? static_cast<uint32_t>(wst[8448 + row]) : 8u;
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
-            dequant_int4_half<BF16S>(pk, sbits, zp, out);
+            if (PG) {
+              // the group scale (the f16 value the standard path multiplies by), for the epilogue
+              pg_sv = BF16S ? __half2float(__float2half_rn(__uint_as_float(sbits << 16)))
+                            : __half2float(__ushort_as_half(static_cast<uint16_t>(sbits)));
+              dequant_int4_raw_half(pk, out);
+            } else {
+              dequant_int4_half<BF16S>(pk, sbits, zp, out);
+            }
           } else if (KIND == kQ4S) {
             const uint4 pk = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 16);
             const uint2 pos = *reinterpret_cast<const uint2*>(wst + 4096 + (half * 128 + row) * 8);
@@ -627,6 +675,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             if (!ok) break;
             tc_fence_after();
           }
+          if (PG && half == 0) pg_scale[sr.idx * 128 + row] = pg_sv;
           const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
           tmem_st_32x32b_x32<0>(ta, out);
         }
@@ -646,7 +695,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int itn = 0, g0 = 0;
     bool ok = true;
-    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+    if (PG) {
+      // Per-group scaling: every stage's sum D (fp32, its own D slot) becomes
+      //   acc += s_g * (D - C_g[token]),
+      // s_g the row's group scale, C_g the token row's correction for the raw
+      // magic-number halves (see the gather).  The stage's A slot is released to
+      // the issuer (afull) once D is read; the first use of each slot is released
+      // here at the start.
+      if (lane == 0)
+        for (int j = 0; j < NB; ++j) mbar_arrive(smem_u32(afull + j));
+      Ring ar, dn;
+      int sidx = 0;  // stage index modulo 2 x (A slots): the stage's scale slot
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        WorkItem it;
+        decode_item(p, nch, i, it);
+        const int n_st = it.ks1 - it.ks0;
+        float acc[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
+        for (int st = 0; st < n_st; ++st, ar.step(1, NB), dn.step(1, NB2), sidx = (sidx + 1 == 2 * NB) ? 0 : sidx + 1) {
+          // the dequant warps wrote the stage's scales before their afull arrival
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 64));
+          if (!ok) break;
+          const float sg = pg_scale[sidx * 128 + row];
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dn.idx), dn.phase, abort_flag, 64));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tmem + lane_base + static_cast<uint32_t>(p.d_col0 + ar.idx * 16), v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
+          const float4* c4 = reinterpret_cast<const float4*>(p.pg_corr + static_cast<int64_t>(it.ks0 + st) * p.pg_cap +
+                                                             it.row0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 cv = __ldg(c4 + c);
+            acc[4 * c] = fmaf(sg, __uint_as_float(v[4 * c]) - cv.x, acc[4 * c]);
+            acc[4 * c + 1] = fmaf(sg, __uint_as_float(v[4 * c + 1]) - cv.y, acc[4 * c + 1]);
+            acc[4 * c + 2] = fmaf(sg, __uint_as_float(v[4 * c + 2]) - cv.z, acc[4 * c + 2]);
+            acc[4 * c + 3] = fmaf(sg, __uint_as_float(v[4 * c + 3]) - cv.w, acc[4 * c + 3]);
+          }
+        }
+        if (!ok) break;
+        const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + it.row0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 v4 = __ldg(cs4 + c);
+          acc[4 * c] *= v4.x;
+          acc[4 * c + 1] *= v4.y;
+          acc[4 * c + 2] *= v4.z;
+          acc[4 * c + 3] *= v4.w;
+        }
+        epilogue_store(p, it, 0, row, lane, acc);
+      }
+    }
+    for (int i = PG ? n_items : static_cast<int>(blockIdx.x); i < n_items && ok; i += gridDim.x) {
       WorkItem it;
       decode_item(p, nch, i, it);
       const int b = (ACCB == 2) ? (itn & 1) : 0;

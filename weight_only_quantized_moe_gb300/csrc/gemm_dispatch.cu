@@ -17,7 +17,7 @@ cudaError_t launch_gemm_i8sg_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8sg_bf16(const GemmParams&, int, cudaStream_t);
 
 size_t gemm_smem_bytes(const GemmParams& p) {
-  return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.b_stages, p.token_tile);
+  return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.b_stages, p.token_tile, p.pg != 0);
 }
 
 cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream) {
@@ -28,6 +28,10 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
   if (p.b_stages < p.ab_stages || p.b_stages % p.ab_stages != 0) return cudaErrorInvalidValue;
   // dequant sets: each weight slot and each token-tile ("done") barrier must belong to one set
   if (p.dq_sets != 2 && p.dq_sets != 4) return cudaErrorInvalidValue;
+  // per-group scaling: 16-row tiles, at most 8 A slots, D slots after the A slots within 512 columns
+  if (p.pg && (p.token_tile != 16 || p.ab_stages > 8 || p.pg_corr == nullptr ||
+               p.d_col0 < p.a_col0 + 64 * p.ab_stages || p.d_col0 + 16 * p.ab_stages > 512))
+    return cudaErrorInvalidValue;
   if (p.w_stages % p.dq_sets != 0 || p.b_stages % p.dq_sets != 0) return cudaErrorInvalidValue;
   // barriers (2 per weight slot, 1 per A slot, 1 per token-tile slot, 4 + kMaxIssuers more,
   // TMEM address, abort flag) below the 128-byte selector table at the end of the barrier area

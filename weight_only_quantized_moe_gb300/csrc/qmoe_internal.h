@@ -92,6 +92,10 @@ struct GemmParams {
   int32_t out_bf16;          // kEpiLinearOut: output type bf16 (else f16)
   int32_t dq_sets;           // dequant sets (2 of 8 half-row warps, or 4 of 4 full-row warps)
   int32_t w_shared;          // 1: an expert's weight tiles are read by several chunks (L2 evict-normal)
+  int32_t pg;                // int4, 16-row tiles: raw magic-number A, per-stage D slots, per-group fp32 scaling
+  int32_t d_col0;            // per-group scaling: first TMEM column of the 16-column D slots (one per A slot)
+  const float* pg_corr;      // per-group scaling: token-row corrections [k_groups][pg_cap]
+  int64_t pg_cap;
 };
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
