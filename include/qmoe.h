@@ -171,7 +171,7 @@ typedef struct {
    * a weight tile find it in L2; evict-first otherwise), 1 evict-normal,
    * 2 evict-first.  Other values give QMOE_ERR_INVALID_ARG. */
   int32_t weight_l2;
-  /* Symmetric int4 with 16-row token tiles: 0 automatic (on), 1 on, 2 off.  On,
+  /* Symmetric int4 with 16-row token tiles: 0 automatic (off), 1 on, 2 off.  On,
    * the dequant warps hand the tensor core the raw magic-number halves of the
    * codes (1024 + q and 1024 + 16 q against tokens pre-divided by 16) and the
    * epilogue applies each 128-channel group's scale and zero point in fp32, per

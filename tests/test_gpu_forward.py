@@ -107,6 +107,15 @@ def test_int4_group_epilogue_on_and_off(act, ao, gs, M, split1, split2, epi):
     _check(_wl("int4", act, ao, gs=gs), M, opts=q.make_options(split1, split2, 16, int4_group_epilogue=epi))
 
 
+@pytest.mark.parametrize("M,ring,sets", [(1, 1, 0), (40, 1, 0), (40, 2, 2), (7, 2, 2), (33, 1, 2)])
+def test_int4_group_epilogue_rings(M, ring, sets):
+    """The per-group scaling epilogue with a token-tile ring of one A-ring depth
+    (its D slots then come back through the same "done" barriers as the token
+    tiles) and with two dequant sets of half-row warps."""
+    _check(_wl("int4", "f16", False, gs=128), M,
+           opts=q.make_options(0, 0, 16, token_ring=ring, dq_sets=sets, int4_group_epilogue=1))
+
+
 @pytest.mark.parametrize("qt,act", [("int8", "f16"), ("int8", "bf16")])
 def test_int8_token_tile_128_single_accumulator_per_issuer(qt, act):
     # 128-row chunks: each MMA issuer has one TMEM accumulator, summed by the epilogue

@@ -29,6 +29,8 @@ SOURCES = [
     "gemm_dispatch.cu",
     "gemm_i4_f16.cu",
     "gemm_i4_bf16.cu",
+    "gemm_i4p_f16.cu",
+    "gemm_i4p_bf16.cu",
     "gemm_i4z_f16.cu",
     "gemm_i4z_bf16.cu",
     "gemm_i4s_f16.cu",

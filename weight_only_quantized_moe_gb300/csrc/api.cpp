@@ -227,9 +227,9 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
   // off the A slots' cycle.  The deepest m <= 2 that leaves the weight ring at
   // least 8 slots (weights stream from HBM and want the deeper ring).
   const size_t wslot = (static_cast<size_t>(p->stage_bytes) + 1023) & ~size_t(1023);
-  const size_t extra = p->pg ? 16 * 128 * 4 : 0;  // per-group scales
   auto w_depth = [&](int nb2) {
-    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256 + extra;
+    // (+ the per-group-scaled int4 epilogue's staging buffers)
+    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256 + (p->pg ? kPgStageBytes : 0);
     if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
     return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
   };
@@ -245,7 +245,6 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
         break;
       }
   }
-  if (p->pg && ring_m != 2) return QMOE_ERR_INVALID_ARG;  // its scale ring relies on the A-slot waits
   p->b_stages = ring_m * p->ab_stages;
   p->w_stages = w_depth(p->b_stages);
   if (p->w_stages < 2 || p->ab_stages < 2) return QMOE_ERR_UNSUPPORTED;
@@ -291,14 +290,15 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.T = T;
   p.stage_bytes = stage_bytes_of(L->qt, L->group_size);
   // Per-group scaling (symmetric int4, 16-row token tiles): the dequant warps keep
-  // only the magic-number unpacks and the idle epilogue warps apply each group's
-  // scale in fp32 (measured on GB300: the scale multiply and zero-point subtract
-  // were ~12 % of the int4 decode GEMM's time).
+  // only the magic-number unpacks and the epilogue warps apply each group's scale
+  // in fp32 (the scale multiply and zero-point subtract were ~12 % of the int4
+  // decode GEMM's time in an ablation on GB300).
   if (o != nullptr && (o->int4_group_epilogue < 0 || o->int4_group_epilogue > 2)) return QMOE_ERR_INVALID_ARG;
-  // (its scale ring relies on a token-tile ring twice the A ring)
-  const bool ring_ok = o == nullptr || o->token_ring == 0 || o->token_ring == 2;
-  p.pg = (L->qt == QMOE_INT4_GROUP && T == 16 && ring_ok && !(o != nullptr && o->int4_group_epilogue == 2)) ? 1 : 0;
-  if (o != nullptr && o->int4_group_epilogue == 1 && !p.pg) return QMOE_ERR_INVALID_ARG;
+  // Automatic: off (measured on GB300 with Mixtral-8x7B int4 at M = 16: the four
+  // epilogue warps need ~1000 cycles per stage, above the standard path's ~650).
+  const bool pg_ok = L->qt == QMOE_INT4_GROUP && T == 16;
+  if (o != nullptr && o->int4_group_epilogue == 1 && !pg_ok) return QMOE_ERR_INVALID_ARG;
+  p.pg = (pg_ok && o != nullptr && o->int4_group_epilogue == 1) ? 1 : 0;
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;

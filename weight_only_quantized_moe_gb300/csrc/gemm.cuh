@@ -80,18 +80,12 @@ constexpr uint32_t kIdescSparse = 1u << 2;  // instruction descriptor: A is 2:4 
 constexpr int kBarrierBytes = 1024;
 
 __host__ __device__ inline uint32_t gemm_w_slot(int group_bytes) { return (group_bytes + 1023u) & ~1023u; }
-// Per-group-scaled int4: one fp32 scale per row for each of the last 2 x (A slots)
-// stages (at most 16): the dequant warps write stage g's scales after the MMAs of
-// stage g - A slots completed, which happened after the epilogue had read stage
-// g - 2 x (A slots)'s scales (it reads a stage's scales before it releases the
-// stage's D slot, and the issuer waits for that release).
-constexpr int kPgScaleBytes = 16 * 128 * 4;
-// Dynamic shared memory: weight ring, token-tile ring, barriers, per-group scales
-// (per-group-scaled int4 only), +1 KB alignment slack.
+// Dynamic shared memory: weight ring, token-tile ring, barriers, the per-group
+// staging buffers (per-group-scaled int4 only), +1 KB alignment slack.
 __host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int b_stages, int token_tile,
                                                          bool pg) {
   return 1024 + static_cast<size_t>(w_stages) * gemm_w_slot(group_bytes) +
-         static_cast<size_t>(b_stages) * token_tile * 256 + kBarrierBytes + (pg ? kPgScaleBytes : 0);
+         static_cast<size_t>(b_stages) * token_tile * 256 + kBarrierBytes + (pg ? kPgStageBytes : 0);
 }
 
 struct WorkItem {
@@ -387,7 +381,8 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 // ---------------------------------------------------------------------------
 template <int KIND, bool BF16S>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
-  constexpr bool INT4 = KIND == kQ4 || KIND == kQ4Z;
+  constexpr bool INT4 = KIND == kQ4 || KIND == kQ4Z || KIND == kQ4P;
+  constexpr bool PG = KIND == kQ4P;  // per-group scaling in the epilogue
   constexpr bool SPARSE = KIND == kQ4S || KIND == kQ8S || KIND == kQ8SG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -412,9 +407,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   uint64_t* drain = accempty + 2;  // one per MMA issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  // per-group-scaled int4: the dequant warps leave each row's group scale here per A slot
-  float* pg_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(wfull) + kBarrierBytes);
-  const bool PG = INT4 && p.pg;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -583,8 +575,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     // wr: weight slot of the stage; ar: its A slot; dr: the done barrier of the
     // stage NB earlier, the last one that used the same A slot (phase of lap -1,
     // which a fresh barrier reports complete, for the first NB stages)
-    Ring wr, ar, dr, sr;  // sr: the stage's per-group scale slot (2 x NB of them)
-    wr.idx = ar.idx = sr.idx = set;
+    Ring wr, ar, dr;
+    wr.idx = ar.idx = set;
     dr.idx = set - NB + NB2;
     dr.phase = 1u;
     int g0 = 0;
@@ -609,13 +601,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       decode_item(p, nch, i, it);
       const int n_st = it.ks1 - it.ks0;
       for (int g = first_own(g0, set, DS); g < g0 + n_st;
-           g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2), sr.step(DS, 2 * NB)) {
+           g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2)) {
         // weights and token tile landed
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint8_t* wst = wring + wr.idx * wslot;
-        float pg_sv = 0.0f;
         for (int half = h0; half < h1; ++half) {
           const bool last = half + 1 == h1;  // the weight slot is released after the last half's loads
           uint32_t out[32];
@@ -628,10 +619,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
             if (PG) {
-              // the group scale (the f16 value the standard path multiplies by), for the epilogue
-              pg_sv = BF16S ? __half2float(__float2half_rn(__uint_as_float(sbits << 16)))
-                            : __half2float(__ushort_as_half(static_cast<uint16_t>(sbits)));
-              dequant_int4_raw_half(pk, out);
+              dequant_int4_raw_half(pk, out);  // the epilogue applies scale and zero point
             } else {
               dequant_int4_half<BF16S>(pk, sbits, zp, out);
             }
@@ -675,7 +663,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             if (!ok) break;
             tc_fence_after();
           }
-          if (PG && half == 0) pg_scale[sr.idx * 128 + row] = pg_sv;
           const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
           tmem_st_32x32b_x32<0>(ta, out);
         }
@@ -699,26 +686,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       // Per-group scaling: every stage's sum D (fp32, its own D slot) becomes
       //   acc += s_g * (D - C_g[token]),
       // s_g the row's group scale, C_g the token row's correction for the raw
-      // magic-number halves (see the gather).  The stage's A slot is released to
-      // the issuer (afull) once D is read; the first use of each slot is released
-      // here at the start.
+      // magic-number halves (see the gather).  Reading D releases the stage's A
+      // slot to the issuer (the afull barrier also counts these 4 arrivals); the
+      // first use of each slot is released here at the start.
+      //
+      // Scales and corrections reach shared memory by per-thread async copies,
+      // for segments of kPgSeg stages of the CTA's stage sequence, two segments
+      // ahead, into buffers private to the warp (so a wait_group and a
+      // __syncwarp order them; no barrier across warps).
       if (lane == 0)
         for (int j = 0; j < NB; ++j) mbar_arrive(smem_u32(afull + j));
-      Ring ar, dn;
-      int sidx = 0;  // stage index modulo 2 x (A slots): the stage's scale slot
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      uint8_t* wbuf = reinterpret_cast<uint8_t*>(wfull) + kBarrierBytes + q * 2 * kPgWarpBuf;
+      struct Seg {
+        int i, s0, n;  // item, first stage within it, stages (0: past the last item)
         WorkItem it;
-        decode_item(p, nch, i, it);
-        const int n_st = it.ks1 - it.ks0;
-        float acc[16];
+      };
+      auto seg_first = [&](Seg& sg) {
+        sg.i = blockIdx.x;
+        sg.s0 = 0;
+        if (sg.i < n_items) decode_item(p, nch, sg.i, sg.it);
+        sg.n = sg.i < n_items ? min(kPgSeg, sg.it.ks1 - sg.it.ks0) : 0;
+      };
+      auto seg_next = [&](Seg& sg) {
+        if (sg.n == 0) return;
+        sg.s0 += sg.n;
+        if (sg.s0 == sg.it.ks1 - sg.it.ks0) {
+          sg.i += gridDim.x;
+          sg.s0 = 0;
+          if (sg.i >= n_items) {
+            sg.n = 0;
+            return;
+          }
+          decode_item(p, nch, sg.i, sg.it);
+        }
+        sg.n = min(kPgSeg, sg.it.ks1 - sg.it.ks0 - sg.s0);
+      };
+      // segment -> buffer b: 4 x n pieces of 16 bytes each of scales (the warp's
+      // 64 bytes of a stage's 256) and of corrections (a stage's 16 fp32)
+      auto seg_fetch = [&](const Seg& sg, int b) {
+        uint8_t* dst = wbuf + b * kPgWarpBuf;
+        const uint8_t* sbase = p.w +
+                               ((static_cast<int64_t>(sg.it.e) * p.n_tiles + sg.it.tile) * p.k_groups + sg.it.ks0 + sg.s0) *
+                                   static_cast<int64_t>(p.stage_bytes) +
+                               8192 + q * 64;
+        const float* cbase = p.pg_corr + static_cast<int64_t>(sg.it.ks0 + sg.s0) * p.pg_cap + sg.it.row0;
+        for (int j = lane; j < 4 * sg.n; j += 32) {
+          const int st = j >> 2, part = j & 3;
+          cp_async_16(smem_u32(dst + st * 64 + part * 16), sbase + static_cast<int64_t>(st) * p.stage_bytes + part * 16);
+          cp_async_16(smem_u32(dst + kPgSeg * 64 + st * 64 + part * 16), cbase + static_cast<int64_t>(st) * p.pg_cap + 4 * part);
+        }
+        cp_async_commit();
+      };
+      Seg use, fetch;
+      seg_first(use);
+      fetch = use;
+      seg_fetch(fetch, 0);
+      seg_next(fetch);
+      seg_fetch(fetch, 1);
+      seg_next(fetch);
+      Ring ar, dn;
+      int ub = 0;
+      float acc[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
-        for (int st = 0; st < n_st; ++st, ar.step(1, NB), dn.step(1, NB2), sidx = (sidx + 1 == 2 * NB) ? 0 : sidx + 1) {
-          // the dequant warps wrote the stage's scales before their afull arrival
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 64));
-          if (!ok) break;
-          const float sg = pg_scale[sidx * 128 + row];
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dn.idx), dn.phase, abort_flag, 64));
+      for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
+      while (use.n > 0 && ok) {
+        cp_async_wait_group<1>();
+        __syncwarp();
+        const uint8_t* buf = wbuf + ub * kPgWarpBuf;
+        for (int st = 0; st < use.n; ++st, ar.step(1, NB), dn.step(1, NB2)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dn.idx), dn.phase, abort_flag, 32));
           if (!ok) break;
           tc_fence_after();
           uint32_t v[16];
@@ -727,11 +763,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
-          const float4* c4 = reinterpret_cast<const float4*>(p.pg_corr + static_cast<int64_t>(it.ks0 + st) * p.pg_cap +
-                                                             it.row0);
+          // the f16 value of the group scale that the standard path multiplies by
+          const uint16_t sb = reinterpret_cast<const uint16_t*>(buf + st * 64)[lane];
+          const float sg = BF16S ? __half2float(__float2half_rn(__uint_as_float(static_cast<uint32_t>(sb) << 16)))
+                                 : __half2float(__ushort_as_half(sb));
+          const float4* c4 = reinterpret_cast<const float4*>(buf + kPgSeg * 64 + st * 64);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const float4 cv = __ldg(c4 + c);
+            const float4 cv = c4[c];
             acc[4 * c] = fmaf(sg, __uint_as_float(v[4 * c]) - cv.x, acc[4 * c]);
             acc[4 * c + 1] = fmaf(sg, __uint_as_float(v[4 * c + 1]) - cv.y, acc[4 * c + 1]);
             acc[4 * c + 2] = fmaf(sg, __uint_as_float(v[4 * c + 2]) - cv.z, acc[4 * c + 2]);
@@ -739,17 +778,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           }
         }
         if (!ok) break;
-        const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + it.row0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 v4 = __ldg(cs4 + c);
-          acc[4 * c] *= v4.x;
-          acc[4 * c + 1] *= v4.y;
-          acc[4 * c + 2] *= v4.z;
-          acc[4 * c + 3] *= v4.w;
+        // every lane is done with this buffer: refill it two segments ahead
+        __syncwarp();
+        if (fetch.n > 0) {
+          seg_fetch(fetch, ub);
+          seg_next(fetch);
+        } else {
+          cp_async_commit();  // an empty group keeps the wait_group count in step
         }
-        epilogue_store(p, it, 0, row, lane, acc);
+        ub ^= 1;
+        if (use.s0 + use.n == use.it.ks1 - use.it.ks0) {
+          const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + use.it.row0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 v4 = __ldg(cs4 + c);
+            acc[4 * c] *= v4.x;
+            acc[4 * c + 1] *= v4.y;
+            acc[4 * c + 2] *= v4.z;
+            acc[4 * c + 3] *= v4.w;
+          }
+          epilogue_store(p, use.it, 0, row, lane, acc);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
+        }
+        seg_next(use);
       }
+      // no copy of this thread may still be in flight when the CTA exits
+      cp_async_wait_group<0>();
     }
     for (int i = PG ? n_items : static_cast<int>(blockIdx.x); i < n_items && ok; i += gridDim.x) {
       WorkItem it;

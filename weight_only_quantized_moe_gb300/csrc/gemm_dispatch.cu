@@ -5,6 +5,8 @@ namespace qmoe {
 
 cudaError_t launch_gemm_i4_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i4_bf16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i4p_f16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i4p_bf16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i4z_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i4z_bf16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i4s_f16(const GemmParams&, int, cudaStream_t);
@@ -29,16 +31,18 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
   // dequant sets: each weight slot and each token-tile ("done") barrier must belong to one set
   if (p.dq_sets != 2 && p.dq_sets != 4) return cudaErrorInvalidValue;
   // per-group scaling: 16-row tiles, at most 8 A slots, D slots after the A slots within 512 columns
-  if (p.pg && (p.token_tile != 16 || p.ab_stages > 8 || p.pg_corr == nullptr ||
+  if (p.pg && (kind != kQ4 || p.token_tile != 16 || p.ab_stages > 8 || p.pg_corr == nullptr ||
                p.d_col0 < p.a_col0 + 64 * p.ab_stages || p.d_col0 + 16 * p.ab_stages > 512))
     return cudaErrorInvalidValue;
   if (p.w_stages % p.dq_sets != 0 || p.b_stages % p.dq_sets != 0) return cudaErrorInvalidValue;
-  // barriers (2 per weight slot, 1 per A slot, 1 per token-tile slot, 4 + kMaxIssuers more,
-  // TMEM address, abort flag) below the 128-byte selector table at the end of the barrier area
-  if ((2 * p.w_stages + p.ab_stages + p.b_stages + 4 + kMaxIssuers) * 8 + 8 > kBarrierBytes - 128)
+  // barriers (2 per weight slot, 1 per A slot, 1 per token-tile slot, 4 + kMaxIssuers more),
+  // the TMEM address and the abort flag fit the barrier area
+  if ((2 * p.w_stages + p.ab_stages + p.b_stages + 4 + kMaxIssuers) * 8 + 8 > kBarrierBytes)
     return cudaErrorInvalidValue;
   switch (kind) {
-    case kQ4: return bf16_scales ? launch_gemm_i4_bf16(p, grid, stream) : launch_gemm_i4_f16(p, grid, stream);
+    case kQ4:
+      if (p.pg) return bf16_scales ? launch_gemm_i4p_bf16(p, grid, stream) : launch_gemm_i4p_f16(p, grid, stream);
+      return bf16_scales ? launch_gemm_i4_bf16(p, grid, stream) : launch_gemm_i4_f16(p, grid, stream);
     case kQ4Z: return bf16_scales ? launch_gemm_i4z_bf16(p, grid, stream) : launch_gemm_i4z_f16(p, grid, stream);
     case kQ8G: return bf16_scales ? launch_gemm_i8g_bf16(p, grid, stream) : launch_gemm_i8g_f16(p, grid, stream);
     case kQ4S: return bf16_scales ? launch_gemm_i4s_bf16(p, grid, stream) : launch_gemm_i4s_f16(p, grid, stream);

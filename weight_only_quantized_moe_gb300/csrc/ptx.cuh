@@ -133,6 +133,18 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       : "memory");
 }
 
+// Per-thread asynchronous 16-byte global -> shared copy (src, dst 16-byte aligned),
+// completed by cp_async_wait_group (the thread's own copies; a __syncwarp after it
+// makes them visible to the warp's other lanes).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed copy groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

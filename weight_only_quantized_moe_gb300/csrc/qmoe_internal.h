@@ -23,7 +23,15 @@ constexpr int kInt8SparseStageBytes = 10240;
 constexpr int kInt8SparseGroupStageBytes = 10496;
 
 // Weight formats of the GEMM kernel (template parameter).
-enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3, kQ4S = 4, kQ8S = 5, kQ8SG = 6 };
+// Per-group-scaled int4: each GEMM epilogue warp stages, for segments of kPgSeg
+// pipeline stages, its 32 rows' group scales (2 bytes each) and the chunk's 16
+// token-row corrections (fp32) in two shared-memory buffers of its own.
+constexpr int kPgSeg = 16;
+constexpr int kPgWarpBuf = kPgSeg * (32 * 2 + 16 * 4);  // one buffer: scales, then corrections
+constexpr int kPgStageBytes = 4 * 2 * kPgWarpBuf;       // 4 warps x 2 buffers
+// kQ4P: symmetric int4 with per-group fp32 scaling in the epilogue (kernel variant
+// of kQ4 chosen by GemmParams::pg; not a storage format)
+enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3, kQ4S = 4, kQ8S = 5, kQ8SG = 6, kQ4P = 7 };
 constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
 constexpr int kMaxTokenTile = 128;
 
