@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--workloads", type=lambda v: v.split(","), default=None,
                     help="comma-separated subset of the reported workloads")
     ap.add_argument("--cpu-sample-s", type=float, default=20.0)
+    ap.add_argument("--ncu-pass", action="store_true",
+                    help="no timing: run each reported (workload, M) forward 3 times on one weight copy, for an "
+                         "ncu capture of per-launch counters (the 3rd forward of each entry is the one to read)")
     return ap.parse_args()
 
 
@@ -534,6 +537,8 @@ def main():
         if rank != 0:
             return
         return run_reference(args)
+    if args.ncu_pass:
+        return run_ncu_pass(args)
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
@@ -585,6 +590,37 @@ def main():
         import torch
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+
+
+def run_ncu_pass(args):
+    """Each reported (workload, M) runs 3 forwards on one packed copy (7 launches
+    each, 2 of them GEMMs), in REPORTED order, and prints one JSON line per entry
+    after its forwards, so a capture of the GEMM launches maps to entries by order."""
+    import torch
+    import weight_only_quantized_moe_gb300 as q
+    q.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for name, Ms in REPORTED:
+        if args.workloads and name not in args.workloads:
+            continue
+        gw = GpuWorkload(q, WORKLOADS[name], dev)
+        for M in Ms:
+            if args.M and M != args.M:
+                continue
+            inp, x, ids, w = gw.inputs(M)
+            out = torch.empty_like(x)
+            ws = q.alloc_workspace(q.qmoe_workspace_size(gw.base, M, gw.wl.k), dev)
+            for _ in range(3):
+                q.qmoe_forward(gw.base, x, ids, w, out=out, workspace=ws)
+            torch.cuda.synchronize()
+            st = q.qmoe_read_device_status(ws)
+            print(json.dumps({"ncu_pass": name, "M": M, "status": q.status_string(st),
+                              "plan": q.qmoe_describe_plan(gw.base, M, gw.wl.k)}), flush=True)
+            if st != q.QMOE_OK:
+                raise RuntimeError(f"{name} M={M}: device status {q.status_string(st)}")
+            del x, ids, w, out, ws
+        gw.release()
 
 
 def run_reference(args):

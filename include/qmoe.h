@@ -136,7 +136,7 @@ typedef struct {
  * floating-point summation order whatever the knobs say.
  *   split1, split2  split-K factor of the gate/up and down GEMMs (1..64).
  *   token_tile      largest number of token rows one GEMM work item carries
- *                   (multiple of 16, 16..128).
+ *                   (multiple of 16, 16..256).
  *   issuers         threads issuing the GEMMs' tensor-core MMAs (1..3), each
  *                   with its own TMEM accumulator; the automatic choice is 3
  *                   for token tiles of up to 32 rows, 2 up to 64, else 1.  The

@@ -97,6 +97,17 @@ def test_forward_two_dequant_sets(qt, act, ao, gs, M, split1, split2, tile):
     _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile, dq_sets=2))
 
 
+@pytest.mark.parametrize("qt,act,ao,gs", [("int4", "f16", False, 128), ("int4", "bf16", True, 128),
+                                          ("int8", "bf16", False, -1), ("int4zp", "f16", False, 128),
+                                          ("int4s24", "f16", False, 128), ("int8s24", "bf16", False, -1)])
+@pytest.mark.parametrize("M,split1,split2,tile", [(300, 0, 0, 192), (1200, 0, 0, 256), (1200, 0, 0, 192),
+                                                  (1200, 2, 1, 256), (129, 0, 0, 144), (1100, 0, 0, 208)])
+def test_forward_large_token_tiles(qt, act, ao, gs, M, split1, split2, tile):
+    """Token tiles above 128 rows (MMA N up to 256): one issuer, a two-slot A
+    ring, and a single accumulator buffer where two do not fit tensor memory."""
+    _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile))
+
+
 @pytest.mark.parametrize("act,ao,gs", [("f16", False, 128), ("bf16", True, 128), ("f16", False, -1), ("bf16", False, -1)])
 @pytest.mark.parametrize("M,split1,split2", [(1, 0, 0), (7, 0, 0), (40, 0, 0), (40, 3, 2), (16, 1, 1), (33, 2, 2)])
 @pytest.mark.parametrize("epi", [1, 2])

@@ -53,8 +53,30 @@ class Bar:
         return ok
 
 
+class Ring:
+    """The kernel's ring position: a role starts at its own index and steps by its
+    stride with a single wrap (as the device code does)."""
+
+    def __init__(self, idx, phase=0):
+        self.idx, self.phase = idx, phase
+
+    def step(self, r, n):
+        self.idx += r
+        if self.idx >= n:
+            self.idx -= n
+            self.phase ^= 1
+
+    def at(self, g, n, what):
+        """Check the position against stage g's slot (g mod n) and lap parity."""
+        assert 0 <= self.idx < n, f"{what} ring position {self.idx} outside {n} slots"
+        assert self.idx == g % n, f"{what} ring position {self.idx} is not stage {g}'s slot {g % n}"
+        assert self.phase == (g // n) & 1, f"{what} ring phase of stage {g}"
+        return self.idx
+
+
 def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
-    """DS dequant sets take stages g = s, s + DS, ... (each set's warps arrive as one)."""
+    """DS dequant sets take stages g = s, s + DS, ... (each set's warps arrive as one).
+    Slot indices come from the kernel's ring stepping, checked against g mod n."""
     rng = random.Random(seed)
     wfull = [Bar(1) for _ in range(NW)]
     wempty = [Bar(16 // DS) for _ in range(NW)]
@@ -68,8 +90,11 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
     inflight = []              # async events: (kind, stage)
 
     def producer(p):
+        wr, br = Ring(p), Ring(p)
         for g in range(p, n_stages, 2):
-            w, b = g % NW, g % NB2
+            w, b = wr.at(g, NW, "producer weight"), br.at(g, NB2, "producer token-tile")
+            wr.step(2, NW)
+            br.step(2, NB2)
             while not wempty[w].test(g // NW - 1):
                 yield
             assert g < NW or wread[w] == g - NW, "weight slot refilled before it was read"
@@ -82,8 +107,17 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             yield
 
     def dequant(s):
+        wr, ar = Ring(s), Ring(s)
+        dr = Ring(s - NB + NB2, 1)  # the done barrier of stage g - NB (lap -1 for the first NB stages)
         for g in range(s, n_stages, DS):
-            w, a = g % NW, g % NB
+            w, a = wr.at(g, NW, "dequant weight"), ar.at(g, NB, "dequant A")
+            if NB2 != NB:
+                # waits on done[(g - NB) mod NB2] at the parity of lap (g - NB) // NB2 (-1 before the first)
+                assert 0 <= dr.idx < NB2 and dr.idx == (g - NB) % NB2, f"dequant done ring position {dr.idx}"
+                assert dr.phase == ((g - NB) // NB2) & 1, f"dequant done ring phase of stage {g}"
+            wr.step(DS, NW)
+            ar.step(DS, NB)
+            dr.step(DS, NB2)
             while not wfull[w].test(g // NW):
                 yield
             assert wslot[w] == g and bslot[g % NB2] == g
@@ -100,8 +134,12 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             yield
 
     def issuer(i):
+        ar, br = Ring(i), Ring(i)
         for g in range(i, n_stages, NI):
-            a = g % NB
+            a = ar.at(g, NB, "issuer A")
+            br.at(g, NB2, "issuer token-tile")
+            ar.step(NI, NB)
+            br.step(NI, NB2)
             while not afull[a].test(g // NB):
                 yield
             inflight.append(("mma", g))
@@ -188,8 +226,11 @@ def _simulate_without_aslot_wait(n_stages, NW, NB, NB2, NI, seed):
     mma_done, inflight, mma_queue = set(), [], []
 
     def producer(p):
+        wr, br = Ring(p), Ring(p)
         for g in range(p, n_stages, 2):
-            w, b = g % NW, g % NB2
+            w, b = wr.at(g, NW, "producer weight"), br.at(g, NB2, "producer token-tile")
+            wr.step(2, NW)
+            br.step(2, NB2)
             while not wempty[w].test(g // NW - 1):
                 yield
             wfull[w].arrive(1, tx=2)
@@ -241,3 +282,41 @@ def _simulate_without_aslot_wait(n_stages, NW, NB, NB2, NI, seed):
             assert aslot[g0 % NB] == g0 and bslot[g0 % NB2] == g0, "MMA read another stage's operands"
             mma_done.add(g0)
             done[g0 % NB2].arrive(1)
+
+
+def _planner_shapes():
+    """(NW, NB, NB2, NI, DS) of every plan the planner makes for the Mixtral-8x7B
+    int4 / int8 and DeepSeek-like shapes, automatic and with token tiles 16..256."""
+    import weight_only_quantized_moe_gb300 as q
+    from weight_only_quantized_moe_gb300 import _native as N
+    from tests.test_abi import _layer_struct
+    shapes = set()
+    for kw in (dict(E=8, H=4096, I=14336, group_size=128, qt=N.QMOE_INT4_GROUP),
+               dict(E=8, H=4096, I=14336, group_size=-1, qt=N.QMOE_INT8_PER_COL),
+               dict(E=8, H=6144, I=16384, group_size=128, qt=N.QMOE_INT4_GROUP)):
+        for M in (1, 16, 64, 256, 2048):
+            for T in [0] + list(range(16, 257, 16)):
+                for ring in (0, 1):
+                    try:
+                        p = q.qmoe_describe_plan(_layer_struct(**kw), M, 2, q.make_options(token_tile=T, token_ring=ring),
+                                                 152)
+                    except Exception:
+                        continue
+                    shapes.add((p["w_stages"], p["ab_stages"], p["b_stages"], p["issuers"], p["dq_sets"]))
+    return sorted(shapes)
+
+
+def test_protocol_every_planner_shape():
+    """Every ring shape the planner produces (token tiles up to 256 rows, both
+    token-tile ring depths) passes the model, ring stepping included."""
+    shapes = _planner_shapes()
+    assert len(shapes) >= 8
+    for NW, NB, NB2, NI, DS in shapes:
+        for seed in range(4):
+            simulate(3 * NB2 + 2 * NW + 9, NW, NB, NB2, NI, seed, DS=DS)
+
+
+def test_model_detects_a_ring_smaller_than_the_set_count():
+    """Two A slots with four dequant sets: sets 2 and 3 would start past the ring."""
+    with pytest.raises(AssertionError, match="outside"):
+        simulate(40, 8, 2, 4, 1, 0, DS=4)

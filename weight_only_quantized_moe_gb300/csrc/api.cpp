@@ -233,6 +233,9 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
     if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
     return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
   };
+  // large token tiles: fewer A slots (hence token-tile slots) where shared memory
+  // would otherwise hold too few weight slots
+  while (p->ab_stages > ring_mult && w_depth(p->ab_stages) < 4) p->ab_stages -= ring_mult;
   int ring_m = 1;
   if (o != nullptr && o->token_ring != 0) {
     if (o->token_ring < 1 || o->token_ring > 3) return QMOE_ERR_INVALID_ARG;
@@ -256,7 +259,8 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
   // stages in conversion at once (measured on GB300: 3-10 % faster at every
   // size, most at decode), so they are chosen wherever the rings allow.
   if (o != nullptr && (o->weight_l2 < 0 || o->weight_l2 > 2)) return QMOE_ERR_INVALID_ARG;
-  const bool four_ok = (p->w_stages & ~3) >= 4 && p->b_stages % 4 == 0;
+  // (a set starts at A slot `set` and steps by the set count: at least 4 A slots)
+  const bool four_ok = (p->w_stages & ~3) >= 4 && p->b_stages % 4 == 0 && p->ab_stages >= 4;
   p->dq_sets = four_ok ? 4 : 2;
   if (o != nullptr && o->dq_sets != 0) {
     if (o->dq_sets != 2 && o->dq_sets != 4) return QMOE_ERR_INVALID_ARG;

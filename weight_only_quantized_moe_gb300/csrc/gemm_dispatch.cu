@@ -30,6 +30,9 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
   if (p.b_stages < p.ab_stages || p.b_stages % p.ab_stages != 0) return cudaErrorInvalidValue;
   // dequant sets: each weight slot and each token-tile ("done") barrier must belong to one set
   if (p.dq_sets != 2 && p.dq_sets != 4) return cudaErrorInvalidValue;
+  // every role starts at ring position = its index and steps by its stride with
+  // one wrap: each ring holds at least as many slots as the stride of its users
+  if (p.ab_stages < p.dq_sets || p.ab_stages < p.issuers || p.w_stages < p.dq_sets) return cudaErrorInvalidValue;
   // per-group scaling: 16-row tiles, at most 8 A slots, D slots after the A slots within 512 columns
   if (p.pg && (kind != kQ4 || p.token_tile != 16 || p.ab_stages > 8 || p.pg_corr == nullptr ||
                p.d_col0 < p.a_col0 + 64 * p.ab_stages || p.d_col0 + 16 * p.ab_stages > 512))
