@@ -320,3 +320,19 @@ def test_model_detects_a_ring_smaller_than_the_set_count():
     """Two A slots with four dequant sets: sets 2 and 3 would start past the ring."""
     with pytest.raises(AssertionError, match="outside"):
         simulate(40, 8, 2, 4, 1, 0, DS=4)
+
+
+def test_model_detects_an_a_ring_not_a_multiple_of_the_issuers():
+    """Why the A ring is a multiple of the issuer count: with 4 slots and 3
+    issuers, an issuer can reach stage g while the slot's barrier is still two
+    phases behind (stage g - 4 belongs to another issuer), and the parity test
+    passes wrongly; some interleaving shows it."""
+    found = False
+    for seed in range(60):
+        try:
+            simulate(60, 8, 4, 8, 3, seed, DS=4)
+        except AssertionError as e:
+            assert "another stage" in str(e) or "two phases" in str(e)
+            found = True
+            break
+    assert found
