@@ -134,13 +134,15 @@ def test_int8_token_tile_128_single_accumulator_per_issuer(qt, act):
 
 
 @pytest.mark.parametrize("qt,act", [("int4", "bf16"), ("int4", "f16"), ("int8", "bf16"), ("int8", "f16")])
-def test_token_tile_above_128_rejected(qt, act):
-    # TMEM (512 columns) holds one fp32 accumulator of the token tile per MMA issuer plus the A stages
+def test_token_tile_limits_rejected(qt, act):
+    # token tiles up to 256 rows; TMEM (512 columns) holds one fp32 accumulator of the
+    # token tile per MMA issuer plus the A slots, so two issuers of 256 rows do not fit
     wl = _wl(qt, act)
     _, dl = _layer(wl)
-    with pytest.raises(q.QmoeError) as ei:
-        q.qmoe_workspace_size(dl, 40, 2, q.make_options(0, 0, 256))
-    assert ei.value.status == q.QMOE_ERR_INVALID_ARG
+    for opts in (q.make_options(0, 0, 272), q.make_options(0, 0, 256, issuers=2)):
+        with pytest.raises(q.QmoeError) as ei:
+            q.qmoe_workspace_size(dl, 40, 2, opts)
+        assert ei.value.status == q.QMOE_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("qt,act,ao,exps,spread", [("int4", "bf16", False, (24, -24), 8),

@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       ch.expert = e;
       ch.row0 = off + c * T;
       ch.nrows = min(T, pad - c * T);
+      ch.first = coff;
+      ch.count = nch;
       ch.pad = 0;
       chunks[coff + c] = ch;
     }
@@ -441,6 +443,8 @@ __global__ void __launch_bounds__(kGatherThreads)
         ch.expert = e;
         ch.row0 = run + c * T;
         ch.nrows = min(T, pad - c * T);
+        ch.first = crun;
+        ch.count = nch;
         ch.pad = 0;
         chunks[crun + c] = ch;
       }

@@ -93,18 +93,31 @@ struct WorkItem {
 };
 
 // Work item i -> (split, chunk, tile).  Items of one split are rastered in
-// groups of `chunk_group` chunks: tiles vary slowest inside a group so that the
-// CTAs running at the same time share the group's token tiles and each expert
-// weight tile in L2.
+// groups of chunks with the tile varying slowest inside a group, so that the
+// CTAs running at the same time share the group's token tiles and each weight
+// tile in L2.  chunk_group > 0: groups of that many consecutive chunks (decode:
+// one chunk per expert, several experts per group).  chunk_group = -G: every
+// group is a piece of at most G chunks of one expert (large batches: each
+// weight tile is then read once per piece, while the piece's token tiles stay
+// in L2); group (start s, n chunks) owns items [s, s + n) x n_tiles, so the
+// chunk at item / n_tiles names the group.
 __device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i, WorkItem& w) {
   const int per_split = nch * p.n_tiles;
   const int s = i / per_split;
   const int r = i - s * per_split;
-  const int grp_items = p.chunk_group * p.n_tiles;
-  const int g = r / grp_items;
-  const int rem = r - g * grp_items;
-  const int c0 = g * p.chunk_group;
-  const int cg = min(p.chunk_group, nch - c0);
+  int c0, cg;
+  if (p.chunk_group > 0) {
+    const int grp_items = p.chunk_group * p.n_tiles;
+    c0 = (r / grp_items) * p.chunk_group;
+    cg = min(p.chunk_group, nch - c0);
+  } else {
+    const int G = -p.chunk_group;
+    const Chunk cu = p.chunks[r / p.n_tiles];
+    const int piece = (r / p.n_tiles - cu.first) / G;
+    c0 = cu.first + piece * G;
+    cg = min(G, cu.count - piece * G);
+  }
+  const int rem = r - c0 * p.n_tiles;
   const int tile = rem / cg;
   const int c = c0 + (rem - tile * cg);
   const Chunk ch = p.chunks[c];

@@ -44,6 +44,8 @@ struct Chunk {
   int32_t expert;
   int32_t row0;
   int32_t nrows;  // multiple of 16, <= token tile
+  int32_t first;  // index of the expert's first chunk
+  int32_t count;  // chunks of the expert
   int32_t pad;
 };
 
@@ -94,7 +96,7 @@ struct GemmParams {
   int32_t stage_bytes;       // packed weight bytes per 128-K group
   int32_t epi_mode;
   int32_t P;                 // number of token-expert pairs
-  int32_t chunk_group;       // work-item raster: chunks per group
+  int32_t chunk_group;       // work-item raster: chunks per group (> 0), or -G: pieces of at most G chunks of one expert
   int32_t inter_ld;          // I (for the SiLU epilogue)
   int32_t fault_injection;   // 1: CTA 0 arms its first stage without copies (failure-path test)
   int32_t out_bf16;          // kEpiLinearOut: output type bf16 (else f16)
