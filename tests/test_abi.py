@@ -354,10 +354,11 @@ MIXTRAL = dict(E=8, H=4096, I=14336, group_size=128, qt=N.QMOE_INT4_GROUP)
 
 
 @pytest.mark.parametrize("M,T,ni,s2", [(1, 16, 3, 2), (4, 16, 3, 3), (16, 16, 3, 4), (32, 16, 3, 4), (64, 32, 3, 4),
-                                       (128, 64, 2, 4), (256, 128, 1, 1), (2048, 128, 1, 1)])
+                                       (128, 64, 2, 4), (256, 128, 2, 1), (2048, 128, 1, 1)])
 def test_plan_token_tile_issuers_and_split(M, T, ni, s2):
-    """Token tile: the power of two >= 1.5 x mean pairs per expert (16..128); issuers 3 / 2 / 1 by tile;
-    down-GEMM split as fitted on GB300 for the Mixtral-8x7B shape."""
+    """Token tile: the power of two >= 1.5 x mean pairs per expert (16..128); issuers 3 / 2 / 1 by tile
+    (2 for 128-row tiles whose chunks average at most 64 rows); down-GEMM split as fitted on GB300 for the
+    Mixtral-8x7B shape."""
     p = _plan(MIXTRAL, M)
     assert (p["token_tile"], p["issuers"], p["split2"]) == (T, ni, s2)
     assert p["split1"] == 1 and p["stage_bytes"] == 8448
