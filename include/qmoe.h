@@ -177,7 +177,13 @@ typedef struct {
    * epilogue applies each 128-channel group's scale and zero point in fp32, per
    * pipeline stage.  1 where it does not apply gives QMOE_ERR_INVALID_ARG. */
   int32_t int4_group_epilogue;
-  int32_t reserved[7];  /* must be zero */
+  /* Top-k reduction (summing each token's expert outputs and K splits):
+   * 0 automatic (a separate kernel), 1 in the down GEMM's epilogue (the warp
+   * that completes a token's arrival count sums its partials; one launch
+   * fewer, slower on GB300), 2 a separate kernel.  Both sum in the same fixed
+   * order (results are bit-identical).  Other values give QMOE_ERR_INVALID_ARG. */
+  int32_t topk_reduce;
+  int32_t reserved[6];  /* must be zero */
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */

@@ -228,7 +228,7 @@ def test_pack_rejects_bad_zero_points():
 
 
 def test_options_layout_and_issuer_validation():
-    """qmoe_options is 16 int32 fields (8 knobs and 8 reserved); the knobs are checked on the host."""
+    """qmoe_options is 16 int32 fields (10 knobs and 6 reserved); the knobs are checked on the host."""
     assert ctypes.sizeof(N.QmoeOptions) == 64
     L = q.lib()
     ok = _layer_struct()
@@ -243,10 +243,15 @@ def test_options_layout_and_issuer_validation():
     assert size(4096, issuers=3) == 0          # 384 accumulator columns leave no room for A slots
     assert size(16, issuers=4) == 0
     assert size(16, issuers=-1) == 0
-    for bad in (dict(dq_sets=3), dict(weight_l2=3), dict(token_ring=4), dict(dq_sets=-1)):
+    for bad in (dict(dq_sets=3), dict(weight_l2=3), dict(token_ring=4), dict(dq_sets=-1), dict(topk_reduce=3),
+                dict(topk_reduce=-1)):
         assert size(16, **bad) == 0, bad
-    for good in (dict(dq_sets=2), dict(dq_sets=4), dict(weight_l2=1), dict(weight_l2=2), dict(token_ring=1)):
+    for good in (dict(dq_sets=2), dict(dq_sets=4), dict(weight_l2=1), dict(weight_l2=2), dict(token_ring=1),
+                 dict(topk_reduce=1), dict(topk_reduce=2)):
         assert size(16, **good) > 0, good
+    # the in-GEMM reduction adds its arrival counters (M x H/128 x 4 int32) to the workspace
+    assert size(16, topk_reduce=1) > size(16, topk_reduce=2)
+    assert size(16) == size(16, topk_reduce=2)
 
 
 def _sparse_position(area, r, G):

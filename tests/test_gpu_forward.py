@@ -264,6 +264,47 @@ def test_bad_expert_id_is_reported_and_dropped():
     assert_parity(out.float().cpu().numpy(), ref, "bad id dropped")
 
 
+@pytest.mark.parametrize("qt,act,ao", [("int4", "f16", False), ("int4", "bf16", True), ("int8", "bf16", False),
+                                      ("int4s24", "f16", False)])
+@pytest.mark.parametrize("M,split2", [(1, 0), (7, 0), (40, 0), (40, 2), (129, 1), (129, 0), (600, 0)])
+def test_topk_reduce_in_gemm_bit_identical(qt, act, ao, M, split2):
+    """The top-k reduction in the down GEMM's epilogue (arrival counters, last
+    warp sums) and the separate reduce kernel sum in the same order: outputs are
+    bit-identical, and match the oracle."""
+    wl = _wl(qt, act, ao)
+    L, dl = _layer(wl)
+    inp = make_inputs(wl, M, seed=21)
+    x, ids, w = device_inputs(wl, inp)
+    outs = []
+    for mode in (1, 2):
+        out, _ = run_forward(dl, x, ids, w, opts=q.make_options(0, split2, topk_reduce=mode))
+        outs.append(out.float().cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    assert_parity(outs[0], oracle.moe_forward(L, inp.x, inp.topk_ids, inp.topk_weights), f"{wl.name} M={M}")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_token_without_valid_expert_is_zero(mode):
+    """A token all of whose top-k ids are invalid has no pair in any GEMM item:
+    its output row is zero on both reduction paths (status reports the bad ids)."""
+    wl = _wl()
+    L, dl = _layer(wl)
+    inp = make_inputs(wl, 9, seed=4)
+    ids = inp.topk_ids.copy()
+    ids[3, :] = -1
+    ids[5, 0] = 1000
+    x, dids, w = device_inputs(wl, Inputs(inp.x, ids, inp.topk_weights, inp.logits))
+    out, st = run_forward(dl, x, dids, w, opts=q.make_options(topk_reduce=mode), check_status=False)
+    assert st == q.QMOE_ERR_BAD_EXPERT_ID
+    got = out.float().cpu().numpy()
+    assert np.all(got[3] == 0.0)
+    wts = inp.topk_weights.copy()
+    wts[3, :] = 0.0
+    wts[5, 0] = 0.0
+    ids_ok = np.where(ids < 0, 0, np.where(ids >= wl.E, 0, ids)).astype(ids.dtype)
+    assert_parity(got, oracle.moe_forward(L, inp.x, ids_ok, wts), "invalid ids dropped")
+
+
 def test_rejects_wrong_device_pointer_and_small_workspace():
     wl = _wl()
     _, dl = _layer(wl)

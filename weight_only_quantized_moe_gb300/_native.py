@@ -59,8 +59,8 @@ class QmoePlanInfo(ctypes.Structure):
 class QmoeOptions(ctypes.Structure):
     _fields_ = [("split1", c_int32), ("split2", c_int32), ("token_tile", c_int32), ("fault_injection", c_int32),
                 ("issuers", c_int32), ("token_ring", c_int32), ("dq_sets", c_int32),
-                ("weight_l2", c_int32), ("int4_group_epilogue", c_int32),
-                ("reserved", c_int32 * 7)]
+                ("weight_l2", c_int32), ("int4_group_epilogue", c_int32), ("topk_reduce", c_int32),
+                ("reserved", c_int32 * 6)]
 
 
 class QmoeError(RuntimeError):

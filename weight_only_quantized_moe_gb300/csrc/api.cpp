@@ -157,6 +157,8 @@ struct Plan {
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
   size_t off_status = 0, off_sorted = 0, off_expert = 0, off_scalars = 0, off_chunks = 0, off_xg = 0, off_xscale = 0,
          off_inter32 = 0, off_inter16 = 0, off_iscale = 0, off_h = 0, off_y = 0, off_c13 = 0, off_c2 = 0, total = 0;
+  int fused_reduce = 0;  // top-k reduction in the down GEMM's epilogue
+  size_t off_cnt = 0;
 };
 
 // Makespan, in pipeline stages, of n work items of k stages each split s ways
@@ -355,6 +357,14 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     p.S2 = o->split2;
   }
 
+  // Top-k reduction: automatic = the separate kernel.  In the down GEMM's
+  // epilogue (option 1) it saves a launch but was slower at every batch size
+  // measured on GB300 (Mixtral-8x7B int4 M = 16: down GEMM 72 -> 115 us): the
+  // last warp to arrive sums its tokens' partials with dependent L2 loads on
+  // the epilogue's path.
+  if (o != nullptr && (o->topk_reduce < 0 || o->topk_reduce > 2)) return QMOE_ERR_INVALID_ARG;
+  p.fused_reduce = (o != nullptr && o->topk_reduce == 1) ? 1 : 0;
+
   size_t off = 0;
   p.off_status = off;   off += 256;
   p.off_sorted = off;   off += al256(p.cap * 4);
@@ -368,6 +378,9 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.off_iscale = off;   off += al256(static_cast<size_t>(p.cap) * 4);
   p.off_h = off;        off += (p.S1 > 1) ? al256(static_cast<size_t>(p.S1) * p.cap * 2 * L->I * 4) : 0;
   p.off_y = off;        off += al256(static_cast<size_t>(p.S2) * P * L->H * 4);
+  if (p.fused_reduce) {
+    p.off_cnt = off;    off += al256(static_cast<size_t>(M) * p.n_tiles2 * 4 * 4);
+  }
   if (p.pg) {
     p.off_c13 = off;    off += al256(static_cast<size_t>(p.cap) * p.kst1 * 4);
     p.off_c2 = off;     off += al256(static_cast<size_t>(p.cap) * p.kst2 * 4);
@@ -518,6 +531,14 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g2.out = y;
   g2.out_ld = L->H;
   g2.out_split_stride = pl.P * static_cast<int64_t>(L->H);
+  if (pl.fused_reduce) {
+    g2.red_cnt = reinterpret_cast<int32_t*>(base + pl.off_cnt);
+    g2.topk_ids = topk_ids;
+    g2.red_out = static_cast<uint16_t*>(out);
+    g2.top_k = k;
+    g2.n_experts = L->E;
+    g2.out_bf16 = bf16 ? 1 : 0;
+  }
 
   const int64_t items1 = pl.max_chunks * pl.n_tiles1 * pl.S1;
   const int64_t items2 = pl.max_chunks * pl.n_tiles2 * pl.S2;
@@ -537,7 +558,18 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   rec(7);
   rec(8);
   if (err == cudaSuccess) {
-    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, c2, sms, stream);
+    TopkPrep prep{};
+    if (pl.fused_reduce) {
+      prep.cnt = g2.red_cnt;
+      prep.n_cnt = M * static_cast<int64_t>(pl.n_tiles2) * 4;
+      prep.topk_ids = topk_ids;
+      prep.M = M;
+      prep.top_k = k;
+      prep.E = L->E;
+      prep.H = L->H;
+      prep.out = static_cast<uint16_t*>(out);
+    }
+    err = launch_inter_rescale(inter32, npp, sorted, P, L->I, pl.cap, inter16, iscale, c2, prep, sms, stream);
     launched += (err == cudaSuccess);
   }
   rec(9);
@@ -548,7 +580,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   }
   rec(11);
   rec(12);
-  if (err == cudaSuccess) {
+  if (err == cudaSuccess && !pl.fused_reduce) {
     err = launch_out_reduce(y, topk_ids, L->E, pl.S2, M, k, L->H, bf16, out, sms, stream);
     launched += (err == cudaSuccess);
   }

@@ -593,10 +593,25 @@ constexpr int kRescaleThreads = 256;
 __global__ void __launch_bounds__(kRescaleThreads)
     inter_rescale_kernel(const float* __restrict__ inter32, const int32_t* __restrict__ num_post_padded,
                          const int32_t* __restrict__ sorted_ids, int32_t P, int32_t I, int64_t cap,
-                         uint8_t* __restrict__ inter16, float* __restrict__ iscale, float* __restrict__ pg_corr) {
+                         uint8_t* __restrict__ inter16, float* __restrict__ iscale, float* __restrict__ pg_corr,
+                         const TopkPrep prep) {
   __shared__ float red[kRescaleThreads / 32];
   pdl_launch_dependents();
   pdl_wait();
+  if (prep.cnt != nullptr) {
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRescaleThreads + threadIdx.x;
+    const int64_t ts = static_cast<int64_t>(gridDim.x) * kRescaleThreads;
+    for (int64_t i = t0; i < prep.n_cnt; i += ts) prep.cnt[i] = 0;
+    for (int64_t m = t0; m < prep.M; m += ts) {
+      bool any = false;
+      for (int j = 0; j < prep.top_k; ++j) {
+        const int e = prep.topk_ids[m * prep.top_k + j];
+        any = any || (e >= 0 && e < prep.E);
+      }
+      if (!any)
+        for (int n = 0; n < prep.H; ++n) prep.out[m * prep.H + n] = 0;
+    }
+  }
   const int total = *num_post_padded;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int row = blockIdx.x; row < total; row += gridDim.x) {
@@ -647,10 +662,11 @@ __global__ void __launch_bounds__(kRescaleThreads)
 
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
                                  int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, float* pg_corr,
-                                 int num_sms, cudaStream_t stream) {
+                                 const TopkPrep& prep, int num_sms, cudaStream_t stream) {
   const int grid = static_cast<int>(cap_rows < 8LL * num_sms ? (cap_rows > 0 ? cap_rows : 1) : 8LL * num_sms);
   return launch_kernel(inter_rescale_kernel, dim3(grid), dim3(kRescaleThreads), 0, stream, true, inter32,
-                       num_post_padded, sorted_ids, P, I, cap_rows, static_cast<uint8_t*>(inter16), iscale, pg_corr);
+                       num_post_padded, sorted_ids, P, I, cap_rows, static_cast<uint8_t*>(inter16), iscale, pg_corr,
+                       prep);
 }
 
 // ---------------------------------------------------------------------------

@@ -339,6 +339,55 @@ __device__ __forceinline__ float silu_dev(float g) { return __fdividef(g, 1.0f +
 // every scale applied).  Modes: SiLU(gate)*up into the fp32 intermediate
 // (gate/up rows are adjacent lanes), fp32 gate/up partials, or the
 // routing-weighted down output.
+// Top-k reduction in the down GEMM's epilogue.  Output element (token m, feature
+// n) is the sum over m's valid experts j and the K splits s of the partials
+// y[s][m*top_k + j][n], which several items (CTAs) write.  Each epilogue warp,
+// after storing its 32 rows of 16 token columns, counts one arrival per column
+// on the (token, 128-row tile, lane quadrant) counter; the warp whose arrival
+// completes the count (valid experts x splits) sums that token's 32 rows in the
+// fixed order (j, then s) of the separate reduce kernel and writes them.  No
+// warp waits for another: the fences order every partial store before its
+// arrival and the final reads after the last one.
+static __device__ __noinline__ void reduce_topk(const GemmParams& p, const WorkItem& it, int c0, int row, int lane) {
+  __threadfence();
+  __syncwarp();
+  int m = -1;
+  bool last = false;
+  if (lane < 16) {
+    const int pair = __ldg(p.sorted_ids + it.row0 + c0 + lane);
+    if (pair < p.P) {
+      m = pair / p.top_k;
+      int need = 0;
+      for (int j = 0; j < p.top_k; ++j) {
+        const int e = __ldg(p.topk_ids + static_cast<int64_t>(m) * p.top_k + j);
+        need += (e >= 0 && e < p.n_experts) ? 1 : 0;
+      }
+      need *= p.split;
+      const int64_t ci = (static_cast<int64_t>(m) * p.n_tiles + it.tile) * 4 + (row >> 5);
+      last = atomicAdd(p.red_cnt + ci, 1) == need - 1;
+    }
+  }
+  unsigned todo = __ballot_sync(0xffffffffu, last);
+  if (todo == 0) return;
+  __threadfence();
+  const int64_t n = static_cast<int64_t>(it.tile) * kTileRows + row;
+  const float* y0 = static_cast<const float*>(p.out);
+  while (todo != 0) {
+    const int c = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const int mm = __shfl_sync(0xffffffffu, m, c);
+    float acc = 0.0f;
+    for (int j = 0; j < p.top_k; ++j) {
+      const int e = __ldg(p.topk_ids + static_cast<int64_t>(mm) * p.top_k + j);
+      if (e < 0 || e >= p.n_experts) continue;
+      const float* yp = y0 + (static_cast<int64_t>(mm) * p.top_k + j) * p.out_ld + n;
+      for (int s = 0; s < p.split; ++s) acc += __ldcg(yp + s * p.out_split_stride);
+    }
+    p.red_out[static_cast<int64_t>(mm) * p.out_ld + n] =
+        p.out_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(acc)) : __half_as_ushort(__float2half_rn(acc));
+  }
+}
+
 __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkItem& it, int c0, int row, int lane,
                                                const float (&f)[16]) {
   if (p.epi_mode == kEpiSiluToAct) {
@@ -380,6 +429,7 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
       if (pair < p.P)
         y[static_cast<int64_t>(pair) * p.out_ld + it.tile * kTileRows + row] = f[c] * __ldg(p.topk_w + pair);
     }
+    if (p.red_cnt != nullptr) reduce_topk(p, it, c0, row, lane);
   }
 }
 

@@ -106,6 +106,13 @@ struct GemmParams {
   int32_t d_col0;            // per-group scaling: first TMEM column of the 16-column D slots (one per A slot)
   const float* pg_corr;      // per-group scaling: token-row corrections [k_groups][pg_cap]
   int64_t pg_cap;
+  // down GEMM with the top-k reduction in its epilogue (red_cnt null: a separate
+  // kernel sums the partial outputs)
+  int32_t* red_cnt;          // [M][n_tiles][4] arrival counters, zero at launch
+  const int32_t* topk_ids;   // [M][top_k]
+  uint16_t* red_out;         // [M][out_ld] layer output in the activation type (out_bf16)
+  int32_t top_k;
+  int32_t n_experts;
 };
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
@@ -149,9 +156,22 @@ cudaError_t launch_align_gather_small(const int32_t* topk_ids, int32_t P, int32_
 cudaError_t launch_silu_reduce(const float* h, const int32_t* num_post_padded, int32_t split, int64_t cap_rows,
                                int32_t I, float* inter32, int num_sms, cudaStream_t stream);
 
+// Preparation of the down GEMM's in-epilogue top-k reduction, done by the
+// intermediate rescale kernel (null cnt: none): zero the arrival counters, and
+// write zero output rows for tokens with no valid expert (no GEMM item reaches them).
+struct TopkPrep {
+  int32_t* cnt;
+  int64_t n_cnt;
+  const int32_t* topk_ids;
+  int64_t M;
+  int32_t top_k;
+  int32_t E;
+  int32_t H;
+  uint16_t* out;
+};
 cudaError_t launch_inter_rescale(const float* inter32, const int32_t* num_post_padded, const int32_t* sorted_ids,
                                  int32_t P, int32_t I, int64_t cap_rows, void* inter16, float* iscale, float* pg_corr,
-                                 int num_sms, cudaStream_t stream);
+                                 const TopkPrep& prep, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_out_reduce(const float* y, const int32_t* topk_ids, int32_t E, int32_t split, int64_t M,
                               int32_t top_k, int32_t H, bool bf16, void* out, int num_sms, cudaStream_t stream);
