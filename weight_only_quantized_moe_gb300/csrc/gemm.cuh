@@ -178,6 +178,25 @@ __device__ __forceinline__ void cvt_int4_word_half(uint32_t src, uint32_t bias, 
       : "r"(src), "r"(bias), "r"(m64z), "r"(s2), "r"(0x2C002C00u));
 }
 
+// One 16-byte chunk of a row (32 K) to 16 f16x2 values, with the constants of
+// dequant_int4_half.
+__device__ __forceinline__ void dequant_int4_chunk(const uint4& pk, uint32_t bias_bits, uint32_t m64z, uint32_t s2bits,
+                                                   uint32_t (&out)[16]) {
+  const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    cvt_int4_word_half(w[j], bias_bits, m64z, s2bits, out[4 * j], out[4 * j + 1]);
+    cvt_int4_word_half(w[j] >> 8, bias_bits, m64z, s2bits, out[4 * j + 2], out[4 * j + 3]);
+  }
+}
+
+template <bool BF16S>
+__device__ __forceinline__ uint32_t int4_scale_pair(uint32_t sbits) {
+  const uint16_t s16 = BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)))
+                             : static_cast<uint16_t>(sbits);
+  return static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
+}
+
 template <bool BF16S>
 __device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t z,
                                                   uint32_t (&out)[32]) {
@@ -669,27 +688,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const uint8_t* wst = wring + wr.idx * wslot;
+        const uint32_t ws_a = smem_u32(wring + wr.idx * wslot);  // the stage's weight slot (shared window)
         for (int half = h0; half < h1; ++half) {
           const bool last = half + 1 == h1;  // the weight slot is released after the last half's loads
           uint32_t out[32];
           if (INT4) {
             uint4 pk[2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((2 * half + c) * 128 + row) * 16);
-            const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 8192 + row * 2);
-            const uint32_t zp = (KIND == kQ4Z) ? static_cast<uint32_t>(wst[8448 + row]) : 8u;
+            for (int c = 0; c < 2; ++c) pk[c] = lds_u128(ws_a + ((2 * half + c) * 128 + row) * 16);
+            const uint32_t sbits = lds_u16(ws_a + 8192 + row * 2);
+            const uint32_t zp = (KIND == kQ4Z) ? lds_u8(ws_a + 8448 + row) : 8u;
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
             if (PG) {
               dequant_int4_raw_half(pk, out);  // the epilogue applies scale and zero point
             } else {
-              dequant_int4_half<BF16S>(pk, sbits, zp, out);
+              // two 16-column pieces, each converted and stored in turn (16 live
+              // registers of converted values instead of 32)
+              const uint32_t bias_bits = 0x64006400u | zp | (zp << 16);
+              const uint32_t m64z = 0xD400D400u | (zp << 4) | (zp << 20);
+              const uint32_t s2bits = int4_scale_pair<BF16S>(sbits);
+              const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                uint32_t o16[16];
+                dequant_int4_chunk(pk[c], bias_bits, m64z, s2bits, o16);
+                if (c == 0 && NB2 != NB && half == h0) {
+                  ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+                  if (!ok) break;
+                  tc_fence_after();
+                }
+                tmem_st_32x32b_x16(ta + 16u * c, o16);
+              }
+              if (!ok) break;
+              continue;
             }
           } else if (KIND == kQ4S) {
-            const uint4 pk = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 16);
-            const uint2 pos = *reinterpret_cast<const uint2*>(wst + 4096 + (half * 128 + row) * 8);
-            const uint32_t sbits = *reinterpret_cast<const uint16_t*>(wst + 6144 + row * 2);
+            const uint4 pk = lds_u128(ws_a + (half * 128 + row) * 16);
+            const uint2 pos = lds_u64(ws_a + 4096 + (half * 128 + row) * 8);
+            const uint32_t sbits = lds_u16(ws_a + 6144 + row * 2);
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
             uint32_t vals[16];
@@ -700,9 +737,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             uint4 pk[2];
 #pragma unroll
             for (int c = 0; c < 2; ++c)
-              pk[c] = *reinterpret_cast<const uint4*>(wst + (half * 128 + row) * 32 + 16 * c);
-            const uint2 pos = *reinterpret_cast<const uint2*>(wst + 8192 + (half * 128 + row) * 8);
-            const uint32_t sbits = (KIND == kQ8SG) ? *reinterpret_cast<const uint16_t*>(wst + 10240 + row * 2) : 0u;
+              pk[c] = lds_u128(ws_a + (half * 128 + row) * 32 + 16 * c);
+            const uint2 pos = lds_u64(ws_a + 8192 + (half * 128 + row) * 8);
+            const uint32_t sbits = (KIND == kQ8SG) ? lds_u16(ws_a + 10240 + row * 2) : 0u;
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
             uint32_t vals[16];
@@ -712,8 +749,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           } else {
             uint4 pk[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) pk[c] = *reinterpret_cast<const uint4*>(wst + ((4 * half + c) * 128 + row) * 16);
-            const uint32_t sbits = (KIND == kQ8G) ? *reinterpret_cast<const uint16_t*>(wst + 16384 + row * 2) : 0u;
+            for (int c = 0; c < 4; ++c) pk[c] = lds_u128(ws_a + ((4 * half + c) * 128 + row) * 16);
+            const uint32_t sbits = (KIND == kQ8G) ? lds_u16(ws_a + 16384 + row * 2) : 0u;
             __syncwarp();
             if (last && lane == 0) mbar_arrive(smem_u32(wempty + wr.idx));
             dequant_int8_half<KIND == kQ8G, BF16S>(pk, sbits, out);
@@ -827,13 +864,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
           // the f16 value of the group scale that the standard path multiplies by
-          const uint16_t sb = reinterpret_cast<const uint16_t*>(buf + st * 64)[lane];
+          const uint32_t buf_a = smem_u32(buf);
+          const uint16_t sb = static_cast<uint16_t>(lds_u16(buf_a + st * 64 + 2 * lane));
           const float sg = BF16S ? __half2float(__float2half_rn(__uint_as_float(static_cast<uint32_t>(sb) << 16)))
                                  : __half2float(__ushort_as_half(sb));
-          const float4* c4 = reinterpret_cast<const float4*>(buf + kPgSeg * 64 + st * 64);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const float4 cv = c4[c];
+            const uint4 cb = lds_u128(buf_a + kPgSeg * 64 + st * 64 + 16 * c);
+            const float4 cv = make_float4(__uint_as_float(cb.x), __uint_as_float(cb.y), __uint_as_float(cb.z),
+                                          __uint_as_float(cb.w));
             acc[4 * c] = fmaf(sg, __uint_as_float(v[4 * c]) - cv.x, acc[4 * c]);
             acc[4 * c + 1] = fmaf(sg, __uint_as_float(v[4 * c + 1]) - cv.y, acc[4 * c + 1]);
             acc[4 * c + 2] = fmaf(sg, __uint_as_float(v[4 * c + 2]) - cv.z, acc[4 * c + 2]);
