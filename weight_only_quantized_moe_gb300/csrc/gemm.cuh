@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     // columns 32 + 16h and 40 + 16h
     auto sparse_store = [&](int half, int hfirst, const uint2& pos, const uint32_t (&vals)[16]) -> bool {
       if (NB2 != NB && half == hfirst) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag, 512));
         if (!ok) return false;
         tc_fence_after();
       }
@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       for (int g = first_own(g0, set, DS); g < g0 + n_st;
            g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2)) {
         // weights and token tile landed
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(wfull + wr.idx), wr.phase, abort_flag, 512));
         if (!ok) break;
         tc_fence_after();
         const uint32_t ws_a = smem_u32(wring + wr.idx * wslot);  // the stage's weight slot (shared window)
@@ -714,7 +714,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
                 uint32_t o16[16];
                 dequant_int4_chunk(pk[c], bias_bits, m64z, s2bits, o16);
                 if (c == 0 && NB2 != NB && half == h0) {
-                  ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+                  ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag, 512));
                   if (!ok) break;
                   tc_fence_after();
                 }
@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           // token-tile and A rings of one depth the token tile's arrival implied it
           // (the producer waited for the same barrier phase before copying it)
           if (NB2 != NB && half == h0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done + dr.idx), dr.phase, abort_flag, 512));
             if (!ok) break;
             tc_fence_after();
           }

@@ -95,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
       sleep_ns = sleep_ns * 2 < max_sleep_ns ? sleep_ns * 2 : max_sleep_ns;
     }
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if ((it & 7) == 0 && *abort_flag) return false;
     if ((it & 31) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
