@@ -76,7 +76,9 @@ class Ring:
 
 def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
     """DS dequant sets take stages g = s, s + DS, ... (each set's warps arrive as one).
-    Slot indices come from the kernel's ring stepping, checked against g mod n."""
+    Slot indices come from the kernel's ring stepping, checked against g mod n.
+    An issued stage's MMAs enter the CTA's tensor-core queue in issue order and
+    execute from its head at random later times."""
     rng = random.Random(seed)
     wfull = [Bar(1) for _ in range(NW)]
     wempty = [Bar(16 // DS) for _ in range(NW)]
@@ -142,7 +144,8 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             br.step(NI, NB2)
             while not afull[a].test(g // NB):
                 yield
-            inflight.append(("mma", g))
+            mma_queue.append(g)
+            inflight.append(("exec", g))
             yield
 
     agents = [producer(0), producer(1)] + [dequant(s) for s in range(DS)] + [issuer(i) for i in range(NI)]
@@ -169,7 +172,6 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             wfull[g % NW].complete_tx(1)
         else:
             # MMAs of one CTA execute in issue order; each reads its stage's A and token tiles
-            mma_queue.append(g)
             g0 = mma_queue.pop(0)
             assert aslot[g0 % NB] == g0 and bslot[g0 % NB2] == g0, "MMA read another stage's operands"
             mma_done.add(g0)

@@ -354,10 +354,6 @@ __device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a, uint64_t bdesc
 
 __device__ __forceinline__ float silu_dev(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values with
-// every scale applied).  Modes: SiLU(gate)*up into the fp32 intermediate
-// (gate/up rows are adjacent lanes), fp32 gate/up partials, or the
-// routing-weighted down output.
 // Top-k reduction in the down GEMM's epilogue.  Output element (token m, feature
 // n) is the sum over m's valid experts j and the K splits s of the partials
 // y[s][m*top_k + j][n], which several items (CTAs) write.  Each epilogue warp,
@@ -407,6 +403,10 @@ static __device__ __noinline__ void reduce_topk(const GemmParams& p, const WorkI
   }
 }
 
+// Epilogue of 16 token columns [c0, c0+16) of one weight row (fp32 values with
+// every scale applied).  Modes: SiLU(gate)*up into the fp32 intermediate
+// (gate/up rows are adjacent lanes), fp32 gate/up partials, or the
+// routing-weighted down output.
 __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkItem& it, int c0, int row, int lane,
                                                const float (&f)[16]) {
   if (p.epi_mode == kEpiSiluToAct) {
