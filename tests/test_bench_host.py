@@ -58,3 +58,25 @@ def test_algorithmic_bytes_and_roofline_arithmetic():
     assert roof["bound"] == "tensor" and abs(roof["achieved"] - fl / 6e-3 / 1e12) < 1e-6
     assert abs(roof["frac_of_sustained_peak"] * 1800.0 - roof["achieved"]) < 1e-9
     assert layer["binding"] == "tensor"
+
+
+def test_recorded_dram_traffic_matches_the_kernel_source():
+    """Every line of profiles/dram_traffic.txt was captured from the current GEMM
+    source (its hash column), and every (workload, M) the benchmark reports has
+    both GEMM launches recorded, so the bench line's roofline.traffic is never
+    null for a stale reason."""
+    path = os.path.join(bench.ROOT, "profiles", "dram_traffic.txt")
+    h = bench.kernel_source_hash()
+    seen = set()
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if not p or p[0].startswith("#"):
+                continue
+            assert p[4] == h, f"{p[0]} M={p[1]} {p[2]}: captured from source {p[4]}, current {h}"
+            assert int(p[3]) > 0
+            seen.add((p[0], int(p[1]), p[2]))
+    for name, Ms in bench.REPORTED:
+        for M in Ms:
+            for k in ("gemm_gate_up", "gemm_down"):
+                assert (name, M, k) in seen, (name, M, k)
