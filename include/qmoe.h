@@ -139,9 +139,11 @@ typedef struct {
  *                   (multiple of 16, 16..256).
  *   issuers         threads issuing the GEMMs' tensor-core MMAs (1..3), each
  *                   with its own TMEM accumulator; the automatic choice is 3
- *                   for token tiles of up to 32 rows, 2 up to 64, else 1.  The
- *                   automatic token tile is the power of two from 16 to 128
- *                   at least 1.5 times the mean number of pairs per expert.
+ *                   for token tiles of up to 32 rows, 2 up to 64 (and for
+ *                   128-row tiles when the experts average at most 64 pairs),
+ *                   else 1.  The automatic token tile is the power of two from
+ *                   16 to 128 at least 1.5 times the mean number of pairs per
+ *                   expert.
  * Other values, or an issuer count whose accumulators leave too little tensor
  * memory for the pipeline, give QMOE_ERR_INVALID_ARG.
  */
@@ -164,7 +166,7 @@ typedef struct {
   /* Dequant warp sets of the GEMMs: 2 (8 warps each, half a stage row per
    * warp) or 4 (4 warps each, whole rows per warp); 0: automatic (4 wherever
    * the rings allow it).  4 needs a token-tile ring that is a multiple of 4
-   * (QMOE_ERR_INVALID_ARG otherwise). */
+   * and at least 4 TMEM A slots (QMOE_ERR_INVALID_ARG otherwise). */
   int32_t dq_sets;
   /* L2 policy of the GEMMs' weight copies: 0 automatic (evict-normal when an
    * expert has more pairs than one token tile, so that the chunks that share
