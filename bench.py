@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--ncu-pass", action="store_true",
                     help="no timing: run each reported (workload, M) forward 3 times on one weight copy, for an "
                          "ncu capture of per-launch counters (the 3rd forward of each entry is the one to read)")
+    ap.add_argument("--record-traffic", nargs=2, metavar=("NCU_CSV", "NCU_PASS_LOG"), default=None,
+                    help="no GPU: write profiles/dram_traffic.txt from an ncu --csv capture of --ncu-pass "
+                         "(dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum) and that run's stdout")
     return ap.parse_args()
 
 
@@ -537,6 +540,8 @@ def main():
         if rank != 0:
             return
         return run_reference(args)
+    if args.record_traffic:
+        return record_traffic(*args.record_traffic)
     if args.ncu_pass:
         return run_ncu_pass(args)
     if world > 1:
@@ -621,6 +626,44 @@ def run_ncu_pass(args):
                 raise RuntimeError(f"{name} M={M}: device status {q.status_string(st)}")
             del x, ids, w, out, ws
         gw.release()
+
+
+def record_traffic(csv_path, pass_log):
+    """profiles/dram_traffic.txt from a one-pass ncu capture of `--ncu-pass`: the
+    GEMM launches come in entry order, 6 per entry (3 forwards x gate/up, down);
+    the third forward's pair is recorded, with the current kernel-source hash."""
+    import csv
+    with open(csv_path) as f:
+        rows = list(csv.reader([line for line in f if line.startswith('"')]))
+    col = {h: i for i, h in enumerate(rows[0])}
+    launch = {}
+    for r in rows[1:]:
+        launch.setdefault(int(r[col["ID"]]), {})[r[col["Metric Name"]]] = float(r[col["Metric Value"]])
+    with open(pass_log) as f:
+        entries = [json.loads(line) for line in f if line.startswith('{"ncu_pass"')]
+    ids = sorted(launch)
+    if len(ids) != 6 * len(entries):
+        raise SystemExit(f"{len(ids)} GEMM launches for {len(entries)} entries (want 6 each)")
+    h = kernel_source_hash()
+    out = ["# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,",
+           "# read by bench.py for the roofline \"traffic\" field.  The fifth column is the first 16 hex",
+           "# digits of sha256(gemm.cuh + ptx.cuh) of the kernel source that was captured; bench.py",
+           "# reports null when the current source differs.  Commands (one pass per launch, cold L2):",
+           "#   python bench.py --ncu-pass > pass.log 2>&1 && ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+           "gpu__time_duration.sum \\",
+           "#       --clock-control none -k regex:qmoe_gemm --csv --print-units base --log-file traffic.csv "
+           "python bench.py --ncu-pass > pass.log",
+           "#   python bench.py --record-traffic traffic.csv pass.log",
+           "# (each entry runs 3 forwards; the 3rd forward's gate/up and down launches are recorded)",
+           "# workload M kernel bytes_per_launch source_sha256_16 read_bytes write_bytes duration_ns"]
+    for n, e in enumerate(entries):
+        for kname, lid in (("gemm_gate_up", ids[6 * n + 4]), ("gemm_down", ids[6 * n + 5])):
+            g = launch[lid]
+            rd, wr = int(g["dram__bytes_read.sum"]), int(g["dram__bytes_write.sum"])
+            out.append(f'{e["ncu_pass"]} {e["M"]} {kname} {rd + wr} {h} {rd} {wr} {int(g["gpu__time_duration.sum"])}')
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.txt"), "w") as f:
+        f.write("\n".join(out) + "\n")
+    print(f"{len(out) - 9} launches recorded for source {h}")
 
 
 def run_reference(args):

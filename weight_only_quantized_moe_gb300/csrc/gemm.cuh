@@ -178,8 +178,9 @@ __device__ __forceinline__ void cvt_int4_word_half(uint32_t src, uint32_t bias, 
       : "r"(src), "r"(bias), "r"(m64z), "r"(s2), "r"(0x2C002C00u));
 }
 
-// One 16-byte chunk of a row (32 K) to 16 f16x2 values, with the constants of
-// dequant_int4_half.
+// One 16-byte chunk of a row (32 K) to 16 f16x2 values (q - z) * s.  Constants:
+// bias_bits = 1024 + z and m64z = -(64 + z) as f16x2 (see int4_zp_constants),
+// s2bits = the f16 scale in both halves (int4_scale_pair).
 __device__ __forceinline__ void dequant_int4_chunk(const uint4& pk, uint32_t bias_bits, uint32_t m64z, uint32_t s2bits,
                                                    uint32_t (&out)[16]) {
   const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
@@ -190,34 +191,17 @@ __device__ __forceinline__ void dequant_int4_chunk(const uint4& pk, uint32_t bia
   }
 }
 
+__device__ __forceinline__ void int4_zp_constants(uint32_t z, uint32_t& bias_bits, uint32_t& m64z) {
+  bias_bits = 0x64006400u | z | (z << 16);  // 1024 + z
+  m64z = 0xD400D400u | (z << 4) | (z << 20);  // -(64 + z)
+}
+
+// The group scale as an f16 pair (a bf16 scale is rounded to f16 once).
 template <bool BF16S>
 __device__ __forceinline__ uint32_t int4_scale_pair(uint32_t sbits) {
   const uint16_t s16 = BF16S ? __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)))
                              : static_cast<uint16_t>(sbits);
   return static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
-}
-
-template <bool BF16S>
-__device__ __forceinline__ void dequant_int4_half(const uint4 (&pk)[2], uint32_t sbits, uint32_t z,
-                                                  uint32_t (&out)[32]) {
-  const uint32_t bias_bits = 0x64006400u | z | (z << 16);                      // 1024 + z
-  const uint32_t m64z = 0xD400D400u | (z << 4) | (z << 20);                    // -(64 + z)
-  uint16_t s16;
-  if (BF16S) {
-    s16 = __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
-  } else {
-    s16 = static_cast<uint16_t>(sbits);
-  }
-  const uint32_t s2bits = static_cast<uint32_t>(s16) | (static_cast<uint32_t>(s16) << 16);
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const uint32_t w[4] = {pk[c].x, pk[c].y, pk[c].z, pk[c].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      cvt_int4_word_half(w[j], bias_bits, m64z, s2bits, out[16 * c + 4 * j], out[16 * c + 4 * j + 1]);
-      cvt_int4_word_half(w[j] >> 8, bias_bits, m64z, s2bits, out[16 * c + 4 * j + 2], out[16 * c + 4 * j + 3]);
-    }
-  }
 }
 
 // int8: packed chunk c (16 bytes) holds K = 16c .. 16c+15 in byte order.  The
@@ -705,8 +689,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             } else {
               // two 16-column pieces, each converted and stored in turn (16 live
               // registers of converted values instead of 32)
-              const uint32_t bias_bits = 0x64006400u | zp | (zp << 16);
-              const uint32_t m64z = 0xD400D400u | (zp << 4) | (zp << 20);
+              uint32_t bias_bits, m64z;
+              int4_zp_constants(zp, bias_bits, m64z);
               const uint32_t s2bits = int4_scale_pair<BF16S>(sbits);
               const uint32_t ta = tmem + lane_base + a_col0 + static_cast<uint32_t>(ar.idx * 64 + 32 * half);
 #pragma unroll
