@@ -33,6 +33,7 @@ constexpr int kPgStageBytes = 4 * 2 * kPgWarpBuf;       // 4 warps x 2 buffers
 // of kQ4 chosen by GemmParams::pg; not a storage format)
 enum QuantKind : int { kQ4 = 0, kQ4Z = 1, kQ8 = 2, kQ8G = 3, kQ4S = 4, kQ8S = 5, kQ8SG = 6, kQ4P = 7 };
 constexpr int kAlignBlock = 16;       // moe_align block used by the forward (the MMA N granule)
+constexpr int kNoPadPairs = 8;       // batches up to this many pairs leave padding rows unwritten
 constexpr int kMaxTokenTile = 256;
 
 // Device-side status codes (values match qmoe_status).
