@@ -419,6 +419,13 @@ def test_plan_overrides_and_other_workloads():
     ds = dict(E=160, H=5120, I=1536, group_size=-1, qt=N.QMOE_INT8_PER_COL, scale_dtype=N.QMOE_F32)
     assert _plan(ds, 1024, k=6)["token_tile"] == 64      # 6144 pairs over 160 experts
     assert _plan(ds, 1, k=6)["token_tile"] == 16
+    # fine-grained experts (E >= 16 k): at least 32 rows from M = 32, where an uneven router
+    # can give one expert several 16-row chunks; few experts keep the mean-based tile
+    assert [_plan(ds, M, k=6)["token_tile"] for M in (16, 31, 32, 256, 512, 2048)] == [16, 16, 32, 32, 32, 128]
+    assert _plan(dict(ds, E=95), 32, k=6)["token_tile"] == 16      # E < 16 k
+    assert _plan(dict(ds, E=96), 32, k=6)["token_tile"] == 32
+    assert _plan(ds, 256, k=6, token_tile=16)["token_tile"] == 16  # the option still decides
+    assert _plan(MIXTRAL, 32)["token_tile"] == 16                  # E / k = 4
     with pytest.raises(q.QmoeError):
         q.qmoe_describe_plan(_layer_struct(**MIXTRAL), 16, 2, None, -1)
 
