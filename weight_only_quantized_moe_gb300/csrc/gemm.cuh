@@ -318,10 +318,11 @@ __device__ __forceinline__ void dequant_int8_24_vals_half(const uint4 (&pk)[2], 
 // The 4 sparse MMAs of one stage (K = 32 of the dense matrix each): the A slot holds
 // the kept values in columns 0..31 (8 per MMA) and MMA kk's position words in
 // column 32 + 8 kk (8-column aligned, as the A operand's steps).
-__device__ __forceinline__ void mma_stage_sp(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
+__device__ __forceinline__ void mma_stage_sp(uint32_t issue, uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc,
+                                             uint32_t acc0) {
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)
-    mma_ts_sp_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 1) * 64 + (kk & 1) * 4),
+    mma_ts_sp_f16(issue, d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 1) * 64 + (kk & 1) * 4),
                   a + 32u + static_cast<uint32_t>(8 * kk), idesc, kk > 0 ? 1u : acc0);
 }
 
@@ -329,10 +330,12 @@ __device__ __forceinline__ void mma_stage_sp(uint32_t d, uint32_t a, uint64_t bd
 // between two tcgen05.mma instructions roughly triples their issue cost.  The
 // A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
 // 128-byte swizzled rows, the second 64-K block 1024 bytes after the first.
-__device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc, uint32_t acc0) {
+// Executed by the whole issuer warp; the lane with `issue` set issues.
+__device__ __forceinline__ void mma_stage(uint32_t issue, uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc,
+                                          uint32_t acc0) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts_f16(d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2),
+    mma_ts_f16(issue, d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2),
                idesc, kk > 0 ? 1u : acc0);
 }
 
@@ -568,11 +571,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1 || warp == kMmaWarp3) {
     // ------------------------------------------------------------ MMA issuers
     // With NI issuers, issuer i takes stages i, i+NI, ... into its own
-    // accumulator: one thread's MMA issue rate, with the wait and commit around
+    // accumulator: one warp's MMA issue rate, with the wait and commit around
     // each stage, is below what the tensor core accepts at small N.  With one
     // (large tiles) warp 5 takes every stage.
     const int id = (warp == kMmaWarp3) ? 2 : warp - kMmaWarp;
-    if (lane == 0 && id < NI) {
+    // The whole warp walks the loop, converged, and one elected lane issues: the
+    // slot addresses and descriptors then stay warp-uniform.
+    if (id < NI) {
+      const uint32_t issue = elect_one_sync();
       Ring ar, br;  // A slot (NB) and token-tile slot / done barrier (NB2) of the stage
       ar.idx = br.idx = id;
       int g0 = 0, itn = 0;
@@ -584,43 +590,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
         const int b = (ACCB == 2) ? (itn & 1) : 0;
         const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
-        if (!PG && !mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16)) {
-          ok = false;
-          break;
+        if (!PG) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accempty + b), (use & 1u) ^ 1u, abort_flag, 16));
+          if (!ok) break;
         }
         const uint32_t d_acc = tmem + static_cast<uint32_t>((id * ACCB + b) * T);
         uint32_t acc0 = 0u;  // the issuer's first stage of the item overwrites its accumulator
         for (int g = first_own(g0, id, NI); g < g0 + n_st; g += NI, ar.step(NI, NB), br.step(NI, NB2)) {
           // the dequant set signals A only after the stage's token tile has landed
-          if (!mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 16)) {
-            ok = false;
-            break;
-          }
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(afull + ar.idx), ar.phase, abort_flag, 16));
+          if (!ok) break;
           tc_fence_after();
           const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ar.idx * 64);
           // token tile [8-row group][64-K block][8 rows][128 B]: 8-row groups 2048 bytes apart
           const uint64_t bdesc0 = make_sdesc_k_sw128(smem_u32(bring + br.idx * bslot), 2048u);
           if (SPARSE) {
-            mma_stage_sp(d_acc, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
+            mma_stage_sp(issue, d_acc, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
           } else if (PG) {
             // per-group scaling: the stage's sum goes to the D slot of its A slot, fresh
-            mma_stage(tmem + static_cast<uint32_t>(p.d_col0) + static_cast<uint32_t>(ar.idx * 16), a_tmem, bdesc0, idesc,
-                      0u);
+            mma_stage(issue, tmem + static_cast<uint32_t>(p.d_col0) + static_cast<uint32_t>(ar.idx * 16), a_tmem,
+                      bdesc0, idesc, 0u);
           } else {
-            mma_stage(d_acc, a_tmem, bdesc0, idesc, acc0);
+            mma_stage(issue, d_acc, a_tmem, bdesc0, idesc, acc0);
           }
           acc0 = 1u;
-          mma_commit(smem_u32(done + br.idx));
+          mma_commit(issue, smem_u32(done + br.idx));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
-        if (!PG) mma_commit(smem_u32(accfull + b));
+        if (!PG) mma_commit(issue, smem_u32(accfull + b));
         g0 += n_st;
         ++itn;
       }
-      if (!ok) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
-      // all MMAs this thread issued must finish before TMEM is released
-      mma_commit(smem_u32(drain + id));
+      if (!ok && issue) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
+      // all MMAs this warp issued must finish before TMEM is released
+      mma_commit(issue, smem_u32(drain + id));
       mbar_wait_drain(smem_u32(drain + id), 0);
     }
   } else if (warp >= kDequantWarp0) {

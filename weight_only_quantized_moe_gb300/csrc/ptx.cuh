@@ -209,14 +209,31 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T ; M = 128, N from idesc, K = 16 (16-bit types).
-__device__ __forceinline__ void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// 1 in one lane of a converged warp, 0 in the others (the same lane for a full mask).
+__device__ __forceinline__ uint32_t elect_one_sync() {
+  uint32_t leader;
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(leader));
+  return leader;
+}
+
+// The MMA and commit forms below are executed by a whole converged warp and issued
+// by the lane whose `issue` is non-zero (elect_one_sync): their operands then stay
+// warp-uniform, where a branch to one lane would have the compiler move every
+// operand of every instruction from that lane into uniform registers.
+
+// D[tmem] (+)= A[tmem] * B[smem]^T ; M = 128, N from idesc, K = 16 (16-bit types).
+__device__ __forceinline__ void mma_ts_f16(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
 
@@ -224,20 +241,26 @@ __device__ __forceinline__ void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uin
 // K = 32 of the dense matrix per instruction (16-bit types); A holds the 16 kept values of each
 // row (8 TMEM columns) and `meta_tmem` the 32-bit position words (one column, 8-column aligned
 // like the A operand's steps).
-__device__ __forceinline__ void mma_ts_sp_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t meta_tmem,
-                                              uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_sp_f16(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t meta_tmem, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %5, 0;\n\t"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%0], [%1], %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+      "setp.ne.b32 q, %6, 0;\n\t"
+      "@q tcgen05.mma.sp.cta_group::1.kind::f16 [%0], [%1], %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
+// Arrive once on `bar` when every tcgen05 operation issued so far by the issuing lane
+// has completed.
+__device__ __forceinline__ void mma_commit(uint32_t issue, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(issue)
+      : "memory");
 }
 
 // Instruction descriptor of kind::f16: D f32, A/B f16 or bf16, both K-major, M = 128.
