@@ -137,13 +137,13 @@ typedef struct {
  *   split1, split2  split-K factor of the gate/up and down GEMMs (1..64).
  *   token_tile      largest number of token rows one GEMM work item carries
  *                   (multiple of 16, 16..256).
- *   issuers         threads issuing the GEMMs' tensor-core MMAs (1..3), each
- *                   with its own TMEM accumulator; the automatic choice is 3
- *                   for token tiles of up to 32 rows, 2 up to 64 (and for
- *                   128-row tiles when the experts average at most 64 pairs),
- *                   else 1.  The automatic token tile is the power of two from
- *                   16 to 128 at least 1.5 times the mean number of pairs per
- *                   expert.
+ *   issuers         warps issuing the GEMMs' tensor-core MMAs (1..3), each
+ *                   with its own TMEM accumulator; the automatic choice is 2
+ *                   for token tiles of up to 64 rows, else 1.  The automatic
+ *                   token tile is the power of two from 16 to 128 at least 1.5
+ *                   times the mean number of pairs per expert, and at least 32
+ *                   when E >= 16 * top_k and M >= 32 (an expert's pairs can
+ *                   reach M, E / top_k times the mean).
  * Other values, or an issuer count whose accumulators leave too little tensor
  * memory for the pipeline, give QMOE_ERR_INVALID_ARG.
  */
@@ -372,7 +372,7 @@ size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k,
 /*
  * The launch plan qmoe_forward_ex would use (host only; no device access when
  * num_sms > 0).  Fields: token_tile (token rows per GEMM work item), issuers
- * (MMA-issuing threads per CTA), acc_bufs (TMEM accumulators per issuer),
+ * (MMA-issuing warps per CTA), acc_bufs (TMEM accumulators per issuer),
  * split1 / split2 (split-K of the gate/up and down GEMMs), w_stages (packed-
  * weight ring depth), ab_stages (TMEM A ring depth), b_stages (token-tile ring
  * depth, a multiple of ab_stages), dq_sets (dequant warp sets), stage_bytes

@@ -151,7 +151,6 @@ struct Plan {
   int T = 0, acc_bufs = 0, issuers = 0, a_col0 = 0, stage_bytes = 0, w_stages = 0, ab_stages = 0, b_stages = 0;
   int dq_sets = 2;
   int pg = 0, d_col0 = 0;
-  double mean_rows = 0.0;  // mean token rows per expert (pairs / experts)
   int S1 = 1, S2 = 1;
   int n_tiles1 = 0, n_tiles2 = 0, kst1 = 0, kst2 = 0;
   int64_t cap = 0, nblocks = 0, max_chunks = 0;
@@ -205,16 +204,16 @@ int chunk_raster(int64_t P, int E, int T, int64_t K) {
 // p->T and the packed block size p->stage_bytes (shared by the MoE layer and the
 // dense linear layer).
 qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
-  // MMA issuers (stage g to issuer g mod n, one accumulator each): one thread
-  // issues a tcgen05.mma about every 86 cycles whatever its N, so small token
-  // tiles take three; a 128-row tile keeps the tensor pipe busy from one
-  // thread, which leaves TMEM for two accumulator buffers so the epilogue
-  // overlaps the next item's MMAs.
+  // MMA issuers (stage g to issuer g mod n, one accumulator each): with small
+  // token tiles one issuing warp's rate, with the wait and commit around each
+  // stage, is below what the tensor core accepts, so tiles up to 64 rows take
+  // two; a 128-row tile keeps the tensor pipe busy from one warp, which leaves
+  // TMEM for two accumulator buffers so the epilogue overlaps the next item's
+  // MMAs.  (Measured on GB300: two issuers 1-5 % faster than three and 5-16 %
+  // faster than one at 16-64 rows for every weight format; one issuer 9 %
+  // faster than two at 128 rows, Mixtral-8x7B int4 M = 256.)
   const int T = p->T;
-  // (128-row tiles whose chunks average at most 64 rows issue MMAs of N <= 64,
-  // at half the tensor work per instruction: two issuers; measured on GB300 with
-  // Mixtral-8x7B int4 at M = 256: 7 % faster, and 3-9 % slower with full tiles)
-  p->issuers = (T <= 32) ? 3 : (T <= 64) ? 2 : (p->mean_rows <= 64.0 ? 2 : 1);
+  p->issuers = (T <= 64) ? 2 : 1;
   if (o != nullptr && o->issuers != 0) {
     if (o->issuers < 1 || o->issuers > 3) return QMOE_ERR_INVALID_ARG;
     p->issuers = o->issuers;
@@ -313,9 +312,8 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   // uneven router sends several 16-row chunks to its busiest experts, each
   // dequantizing the same weights again: plan at least 32 rows there once M
   // can fill them.  (Measured on GB300 with 160 experts top-6: under a
-  // Zipf(1.1)-biased router 3-16 % faster at M = 32..256; under an unbiased
-  // one at most 1.5 % slower, from the single accumulator buffer that three
-  // issuers leave at 32 rows.)
+  // Zipf(1.1)-biased router 3-17 % faster at M = 32..256; under an unbiased
+  // one at most 0.9 % slower.)
   if (T < 32 && L->E >= 16 * k && M >= 32) T = 32;
   if (o != nullptr && o->token_tile != 0) {
     if (o->token_tile < 16 || o->token_tile > kMaxTokenTile || o->token_tile % 16 != 0) return QMOE_ERR_INVALID_ARG;
@@ -337,7 +335,6 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
-  p.mean_rows = static_cast<double>(P) / L->E;
   if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
   // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
   p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
@@ -639,7 +636,6 @@ qmoe_status make_linear_plan(const qmoe_linear* L, int64_t M, const qmoe_options
   p.stage_bytes = stage_bytes_of(L->qt, L->group_size);
   p.n_tiles1 = L->N / kTileRows;
   p.kst1 = L->K / kStageK;
-  p.mean_rows = static_cast<double>(M);
   if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
   p.cap = (M + kAlignBlock - 1 + 15) / 16 * 16;
   p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
