@@ -185,7 +185,17 @@ typedef struct {
    * fewer, slower on GB300), 2 a separate kernel.  Both sum in the same fixed
    * order (results are bit-identical).  Other values give QMOE_ERR_INVALID_ARG. */
   int32_t topk_reduce;
-  int32_t reserved[6];  /* must be zero */
+  /* GEMMs on CTA pairs: 0 automatic, 1 on, 2 off.  On, each GEMM runs as
+   * clusters of two CTAs on two SMs: one M = 256 tensor-core MMA (tcgen05
+   * cta_group::2) covers both CTAs' 128-row weight tiles, and each CTA copies
+   * only half of the token tile's rows into its shared memory.  Symmetric int4
+   * (QMOE_INT4_GROUP) and QMOE_INT8_PER_COL only, not with topk_reduce = 1 or
+   * int4_group_epilogue = 1 (QMOE_ERR_INVALID_ARG otherwise).  Automatic (with
+   * token_ring automatic): on where shared memory leaves a single CTA a
+   * token-tile ring of one A-ring depth or fewer than 8 weight slots (large
+   * token tiles; 64-row tiles of int8). */
+  int32_t cta_pair;
+  int32_t reserved[5];  /* must be zero */
 } qmoe_options;
 
 /* ------------------------------------------------------------------------ */
@@ -375,7 +385,8 @@ size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k,
  * (MMA-issuing warps per CTA), acc_bufs (TMEM accumulators per issuer),
  * split1 / split2 (split-K of the gate/up and down GEMMs), w_stages (packed-
  * weight ring depth), ab_stages (TMEM A ring depth), b_stages (token-tile ring
- * depth, a multiple of ab_stages), dq_sets (dequant warp sets), stage_bytes
+ * depth, a multiple of ab_stages), dq_sets (dequant warp sets), cta_pair (1: the
+ * GEMMs run on CTA pairs), stage_bytes
  * (packed bytes per 128 x 128 block), workspace_bytes.  num_sms: the GPU's
  * SM count the plan is sized for (0: the current device's).  Errors as
  * qmoe_workspace_size_ex (QMOE_ERR_INVALID_ARG / QMOE_ERR_UNSUPPORTED), and
@@ -393,7 +404,8 @@ typedef struct {
   int64_t workspace_bytes;
   int32_t b_stages;
   int32_t dq_sets;
-  int32_t reserved[4];
+  int32_t cta_pair;
+  int32_t reserved[3];
 } qmoe_plan_info;
 
 qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts,

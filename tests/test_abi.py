@@ -228,7 +228,7 @@ def test_pack_rejects_bad_zero_points():
 
 
 def test_options_layout_and_issuer_validation():
-    """qmoe_options is 16 int32 fields (10 knobs and 6 reserved); the knobs are checked on the host."""
+    """qmoe_options is 16 int32 fields (11 knobs and 5 reserved); the knobs are checked on the host."""
     assert ctypes.sizeof(N.QmoeOptions) == 64
     L = q.lib()
     ok = _layer_struct()
@@ -252,6 +252,40 @@ def test_options_layout_and_issuer_validation():
     # the in-GEMM reduction adds its arrival counters (M x H/128 x 4 int32) to the workspace
     assert size(16, topk_reduce=1) > size(16, topk_reduce=2)
     assert size(16) == size(16, topk_reduce=2)
+
+
+def test_cta_pair_option():
+    """CTA pairs: symmetric int4 and per-column int8 only, not with the in-GEMM top-k
+    reduction or the per-group int4 epilogue, not for the dense linear layer; the plan
+    reports them and each CTA's token-tile slots hold half the rows, so 128-row tiles
+    get a deeper token ring."""
+    L = q.lib()
+    ok = _layer_struct()
+
+    def size(M, layer=ok, **kw):
+        return L.qmoe_workspace_size_ex(ctypes.byref(layer), M, 2, ctypes.byref(q.make_options(**kw)))
+
+    for good in (dict(cta_pair=1), dict(cta_pair=2), dict(cta_pair=1, token_tile=128), dict(cta_pair=1, topk_reduce=2)):
+        assert size(16, **good) > 0, good
+    for bad in (dict(cta_pair=3), dict(cta_pair=-1), dict(cta_pair=1, topk_reduce=1),
+                dict(cta_pair=1, token_tile=16, int4_group_epilogue=1)):
+        assert size(16, **bad) == 0, bad
+    for qt, gs in ((N.QMOE_INT4_GROUP_ZP, 128), (N.QMOE_INT8_GROUP, 128), (N.QMOE_INT4_GROUP_24, 128)):
+        assert size(16, _layer_struct(qt=qt, group_size=gs), cta_pair=1) == 0, qt
+    i8 = _layer_struct(qt=N.QMOE_INT8_PER_COL, group_size=-1, scale_dtype=N.QMOE_F32)
+    assert size(16, i8, cta_pair=1) > 0
+    # automatic: pairs where a single CTA's rings are short (128-row int4 tiles: a token ring of one
+    # A-ring depth; 64-row int8 tiles), single CTAs where they are deep (decode, 64-row int4 tiles)
+    single, pair = _plan(MIXTRAL, 2048, cta_pair=2), _plan(MIXTRAL, 2048, cta_pair=1)
+    assert single["b_stages"] == single["ab_stages"] and pair["b_stages"] == 2 * single["b_stages"]
+    assert _plan(MIXTRAL, 2048)["cta_pair"] == 1 and _plan(MIXTRAL, 2048)["b_stages"] == pair["b_stages"]
+    assert _plan(MIXTRAL, 16)["cta_pair"] == 0 and _plan(MIXTRAL, 128)["cta_pair"] == 0
+    I8 = dict(E=8, H=4096, I=14336, group_size=-1, qt=N.QMOE_INT8_PER_COL, scale_dtype=N.QMOE_F32)
+    assert [_plan(I8, M)["cta_pair"] for M in (16, 128, 512)] == [0, 1, 1]
+    assert _plan(MIXTRAL, 2048, token_ring=1)["cta_pair"] == 0      # rings set by hand: no automatic pair
+    lin = N.QmoeLinear(4096, 14336, 128, N.QMOE_INT4_GROUP, N.QMOE_F16, N.QMOE_F16, None, None, None)
+    assert L.qmoe_linear_workspace_size(ctypes.byref(lin), 16, ctypes.byref(q.make_options(cta_pair=1))) == 0
+    assert L.qmoe_linear_workspace_size(ctypes.byref(lin), 16, ctypes.byref(q.make_options(cta_pair=2))) > 0
 
 
 def _sparse_position(area, r, G):
@@ -394,7 +428,7 @@ def test_plan_rings_and_tmem_constraints():
                 assert NI * p["acc_bufs"] * T + 64 * p["ab_stages"] <= 512
                 wslot = (per + 1023) // 1024 * 1024
                 assert p["b_stages"] % p["ab_stages"] == 0 and p["b_stages"] <= 3 * p["ab_stages"]
-                assert 1024 + p["w_stages"] * wslot + p["b_stages"] * T * 256 + 1024 <= 232448
+                assert 1024 + p["w_stages"] * wslot + p["b_stages"] * T * (128 if p["cta_pair"] else 256) + 1024 <= 232448
                 # barriers below the selector table at the end of the 1 KB barrier area
                 assert (2 * p["w_stages"] + p["ab_stages"] + p["b_stages"] + 7) * 8 + 8 <= 1024 - 128
                 assert p["stage_bytes"] == per
@@ -403,10 +437,11 @@ def test_plan_rings_and_tmem_constraints():
 def test_plan_overrides_and_other_workloads():
     p = _plan(MIXTRAL, 16, split1=3, split2=5, token_tile=48, issuers=2)
     assert (p["split1"], p["split2"], p["token_tile"], p["issuers"]) == (3, 5, 48, 2)
-    # token-tile ring twice the A ring at decode sizes, equal at 128-row tiles (shared memory)
+    # token-tile ring twice the A ring at decode sizes, equal at 128-row tiles on single CTAs (shared
+    # memory), twice again on CTA pairs (half of each tile per CTA)
     p16 = _plan(MIXTRAL, 16)
     assert p16["b_stages"] == 2 * p16["ab_stages"] and p16["w_stages"] >= 8
-    p2k = _plan(MIXTRAL, 2048)
+    p2k = _plan(MIXTRAL, 2048, cta_pair=2)
     assert p2k["b_stages"] == p2k["ab_stages"]
     for m in (1, 2, 3):
         pm = _plan(MIXTRAL, 16, token_ring=m)

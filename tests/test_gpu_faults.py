@@ -13,7 +13,10 @@ from tests.gpu_util import assert_parity, device_inputs, device_layer, ensure_bu
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_stage_times_out_and_context_survives():
+@pytest.mark.parametrize("pair", [0, 1])
+def test_withheld_stage_times_out_and_context_survives(pair):
+    """Single CTAs, and CTA pairs (CTA 0 withholds its stage; its peer's waits on
+    the pair's MMAs then run out as well)."""
     ensure_built()
     wl = Workload("fault", 8, 2, 256, 256, "int4", 128, "f16", False, 0.0, (1,))
     L = make_layer(wl, seed=1)
@@ -21,7 +24,7 @@ def test_withheld_stage_times_out_and_context_survives():
     inp = make_inputs(wl, 12, seed=2)
     x, ids, w = device_inputs(wl, inp)
     t0 = time.time()
-    _, st = run_forward(dl, x, ids, w, opts=q.make_options(fault_injection=1), check_status=False)
+    _, st = run_forward(dl, x, ids, w, opts=q.make_options(fault_injection=1, cta_pair=pair), check_status=False)
     elapsed = time.time() - t0
     assert st == q.QMOE_ERR_TIMEOUT, q.status_string(st)
     assert elapsed < 30

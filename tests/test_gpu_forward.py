@@ -108,6 +108,26 @@ def test_forward_large_token_tiles(qt, act, ao, gs, M, split1, split2, tile):
     _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile))
 
 
+@pytest.mark.parametrize("qt,act,ao,gs", [("int4", "f16", False, 128), ("int4", "bf16", True, 128),
+                                          ("int4", "bf16", False, -1), ("int8", "bf16", False, -1),
+                                          ("int8", "f16", False, -1)])
+@pytest.mark.parametrize("M,split1,split2,tile", [(1, 0, 0, 0), (7, 0, 0, 0), (40, 0, 0, 0), (129, 0, 0, 0),
+                                                  (40, 3, 2, 0), (300, 1, 1, 128), (40, 2, 1, 64), (129, 0, 0, 32),
+                                                  (1200, 0, 0, 128), (300, 0, 0, 256)])
+def test_forward_cta_pairs(qt, act, ao, gs, M, split1, split2, tile):
+    """The GEMMs on CTA pairs: M = 256 MMAs over two SMs, each CTA with half of
+    every token tile; the down GEMM's 3 weight tiles (H = 384) leave the last
+    pair's odd CTA a phantom that computes and stores nothing of its own."""
+    _check(_wl(qt, act, ao, gs=gs), M, opts=q.make_options(split1, split2, tile, cta_pair=1))
+
+
+@pytest.mark.parametrize("M,tile,ring,sets", [(40, 64, 1, 0), (129, 128, 0, 2), (300, 64, 2, 0), (7, 16, 1, 2)])
+def test_forward_cta_pairs_rings(M, tile, ring, sets):
+    """CTA pairs with a token-tile ring of one or two A-ring depths and with two
+    dequant sets."""
+    _check(_wl("int4", "f16", False), M, opts=q.make_options(0, 0, tile, token_ring=ring, dq_sets=sets, cta_pair=1))
+
+
 @pytest.mark.parametrize("act,ao,gs", [("f16", False, 128), ("bf16", True, 128), ("f16", False, -1), ("bf16", False, -1)])
 @pytest.mark.parametrize("M,split1,split2", [(1, 0, 0), (7, 0, 0), (40, 0, 0), (40, 3, 2), (16, 1, 1), (33, 2, 2)])
 @pytest.mark.parametrize("epi", [1, 2])

@@ -74,41 +74,48 @@ class Ring:
         return self.idx
 
 
-def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
+def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2, pair=False):
     """DS dequant sets take stages g = s, s + DS, ... (each set's warps arrive as one).
     Slot indices come from the kernel's ring stepping, checked against g mod n.
     An issued stage's MMAs enter the CTA's tensor-core queue in issue order and
-    execute from its head at random later times."""
-    rng = random.Random(seed)
-    wfull = [Bar(1) for _ in range(NW)]
-    wempty = [Bar(16 // DS) for _ in range(NW)]
-    afull = [Bar(16 // DS) for _ in range(NB)]
-    done = [Bar(1) for _ in range(NB2)]
-    wslot = [None] * NW        # stage whose weights the slot holds
-    wread = [None] * NW        # last stage whose weights were read from the slot
-    aslot = [None] * NB
-    bslot = [None] * NB2
-    mma_done = set()
-    inflight = []              # async events: (kind, stage)
+    execute from its head at random later times.
 
-    def producer(p):
+    pair: the CTA-pair form.  Two CTAs walk the same stages, each with its own
+    producers, dequant sets, weight ring and token-tile ring; the A barriers
+    live in CTA 0 and count both CTAs' sets; CTA 0's issuers issue MMAs that read
+    both CTAs' A slots and token tiles, and each stage's commit arrives on the
+    "done" barrier of both CTAs."""
+    rng = random.Random(seed)
+    C = 2 if pair else 1
+    wfull = [[Bar(1) for _ in range(NW)] for _ in range(C)]
+    wempty = [[Bar(16 // DS) for _ in range(NW)] for _ in range(C)]
+    afull = [Bar(C * (16 // DS)) for _ in range(NB)]
+    done = [[Bar(1) for _ in range(NB2)] for _ in range(C)]
+    wslot = [[None] * NW for _ in range(C)]   # stage whose weights the slot holds
+    wread = [[None] * NW for _ in range(C)]   # last stage whose weights were read from the slot
+    aslot = [[None] * NB for _ in range(C)]
+    bslot = [[None] * NB2 for _ in range(C)]
+    mma_done = set()
+    inflight = []              # async events: (kind, cta, stage)
+
+    def producer(c, p):
         wr, br = Ring(p), Ring(p)
         for g in range(p, n_stages, 2):
             w, b = wr.at(g, NW, "producer weight"), br.at(g, NB2, "producer token-tile")
             wr.step(2, NW)
             br.step(2, NB2)
-            while not wempty[w].test(g // NW - 1):
+            while not wempty[c][w].test(g // NW - 1):
                 yield
-            assert g < NW or wread[w] == g - NW, "weight slot refilled before it was read"
-            wfull[w].arrive(1, tx=2)
-            inflight.append(("w", g))
-            while not done[b].test(g // NB2 - 1):
+            assert g < NW or wread[c][w] == g - NW, "weight slot refilled before it was read"
+            wfull[c][w].arrive(1, tx=2)
+            inflight.append(("w", c, g))
+            while not done[c][b].test(g // NB2 - 1):
                 yield
             assert g < NB2 or (g - NB2) in mma_done, "token-tile slot refilled before its MMAs completed"
-            inflight.append(("b", g))
+            inflight.append(("b", c, g))
             yield
 
-    def dequant(s):
+    def dequant(c, s):
         wr, ar = Ring(s), Ring(s)
         dr = Ring(s - NB + NB2, 1)  # the done barrier of stage g - NB (lap -1 for the first NB stages)
         for g in range(s, n_stages, DS):
@@ -120,18 +127,18 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             wr.step(DS, NW)
             ar.step(DS, NB)
             dr.step(DS, NB2)
-            while not wfull[w].test(g // NW):
+            while not wfull[c][w].test(g // NW):
                 yield
-            assert wslot[w] == g and bslot[g % NB2] == g
-            wread[w] = g
-            wempty[w].arrive(16 // DS)
+            assert wslot[c][w] == g and bslot[c][g % NB2] == g
+            wread[c][w] = g
+            wempty[c][w].arrive(16 // DS)
             yield  # conversion
             if NB2 != NB:
                 gp = g - NB
-                while not done[gp % NB2].test(gp // NB2 if gp >= 0 else -1):
+                while not done[c][gp % NB2].test(gp // NB2 if gp >= 0 else -1):
                     yield
             assert g < NB or (g - NB) in mma_done, "A slot rewritten before its MMAs completed"
-            aslot[a] = g
+            aslot[c][a] = g
             afull[a].arrive(16 // DS)
             yield
 
@@ -145,16 +152,17 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             while not afull[a].test(g // NB):
                 yield
             mma_queue.append(g)
-            inflight.append(("exec", g))
+            inflight.append(("exec", 0, g))
             yield
 
-    agents = [producer(0), producer(1)] + [dequant(s) for s in range(DS)] + [issuer(i) for i in range(NI)]
+    agents = [producer(c, p) for c in range(C) for p in (0, 1)] + [dequant(c, s) for c in range(C) for s in range(DS)]
+    agents += [issuer(i) for i in range(NI)]
     live = list(agents)
     mma_queue = []
     steps = 0
     while live or inflight:
         steps += 1
-        assert steps < 200000, "no progress (deadlock)"
+        assert steps < 400000, "no progress (deadlock)"
         choices = [("agent", a) for a in live] + [("ev", k) for k in range(len(inflight))]
         kind, x = rng.choice(choices)
         if kind == "agent":
@@ -163,19 +171,21 @@ def simulate(n_stages, NW, NB, NB2, NI, seed, DS=2):
             except StopIteration:
                 live.remove(x)
             continue
-        ev, g = inflight.pop(x)
+        ev, c, g = inflight.pop(x)
         if ev == "w":
-            wslot[g % NW] = g
-            wfull[g % NW].complete_tx(1)
+            wslot[c][g % NW] = g
+            wfull[c][g % NW].complete_tx(1)
         elif ev == "b":
-            bslot[g % NB2] = g
-            wfull[g % NW].complete_tx(1)
+            bslot[c][g % NB2] = g
+            wfull[c][g % NW].complete_tx(1)
         else:
-            # MMAs of one CTA execute in issue order; each reads its stage's A and token tiles
+            # MMAs execute in issue order; each reads its stage's A and token tiles (in both CTAs of a pair)
             g0 = mma_queue.pop(0)
-            assert aslot[g0 % NB] == g0 and bslot[g0 % NB2] == g0, "MMA read another stage's operands"
+            for cc in range(C):
+                assert aslot[cc][g0 % NB] == g0 and bslot[cc][g0 % NB2] == g0, "MMA read another stage's operands"
             mma_done.add(g0)
-            done[g0 % NB2].arrive(1)
+            for cc in range(C):
+                done[cc][g0 % NB2].arrive(1)
     assert len(mma_done) == n_stages
 
 
@@ -200,6 +210,15 @@ CONFIGS4 = [(16, 6, 12, 3), (12, 6, 12, 3), (8, 6, 12, 3), (12, 4, 8, 2), (8, 4,
 def test_protocol_four_dequant_sets(NW, NB, NB2, NI):
     for seed in range(12):
         simulate(3 * NB2 + 2 * NW + 9, NW, NB, NB2, NI, seed, DS=4)
+
+
+@pytest.mark.parametrize("NW,NB,NB2,NI,DS", [(8, 4, 4, 1, 4), (12, 4, 8, 1, 4), (8, 4, 4, 2, 4), (10, 4, 4, 1, 2),
+                                            (16, 6, 12, 2, 4), (4, 4, 4, 1, 4)])
+def test_protocol_cta_pairs(NW, NB, NB2, NI, DS):
+    """The CTA-pair form: both CTAs' dequant sets arrive on CTA 0's A barriers,
+    and every MMA reads both CTAs' operands of its own stage."""
+    for seed in range(10):
+        simulate(3 * NB2 + 2 * NW + 9, NW, NB, NB2, NI, seed, DS=DS, pair=True)
 
 
 def test_model_detects_a_missing_wait():
@@ -299,23 +318,26 @@ def _planner_shapes():
         for M in (1, 16, 64, 256, 2048):
             for T in [0] + list(range(16, 257, 16)):
                 for ring in (0, 1):
-                    try:
-                        p = q.qmoe_describe_plan(_layer_struct(**kw), M, 2, q.make_options(token_tile=T, token_ring=ring),
-                                                 152)
-                    except Exception:
-                        continue
-                    shapes.add((p["w_stages"], p["ab_stages"], p["b_stages"], p["issuers"], p["dq_sets"]))
+                    for pair in (0, 1):
+                        try:
+                            opts = q.make_options(token_tile=T, token_ring=ring, cta_pair=pair)
+                            p = q.qmoe_describe_plan(_layer_struct(**kw), M, 2, opts, 152)
+                        except Exception:
+                            continue
+                        shapes.add((p["w_stages"], p["ab_stages"], p["b_stages"], p["issuers"], p["dq_sets"],
+                                    p["cta_pair"]))
     return sorted(shapes)
 
 
 def test_protocol_every_planner_shape():
     """Every ring shape the planner produces (token tiles up to 256 rows, both
-    token-tile ring depths) passes the model, ring stepping included."""
+    token-tile ring depths, single CTAs and CTA pairs) passes the model, ring
+    stepping included."""
     shapes = _planner_shapes()
-    assert len(shapes) >= 8
-    for NW, NB, NB2, NI, DS in shapes:
+    assert len(shapes) >= 8 and any(s[-1] for s in shapes)
+    for NW, NB, NB2, NI, DS, pair in shapes:
         for seed in range(4):
-            simulate(3 * NB2 + 2 * NW + 9, NW, NB, NB2, NI, seed, DS=DS)
+            simulate(3 * NB2 + 2 * NW + 9, NW, NB, NB2, NI, seed, DS=DS, pair=bool(pair))
 
 
 def test_model_detects_a_ring_smaller_than_the_set_count():

@@ -53,14 +53,14 @@ class QmoePlanInfo(ctypes.Structure):
     _fields_ = [("token_tile", c_int32), ("issuers", c_int32), ("acc_bufs", c_int32), ("split1", c_int32),
                 ("split2", c_int32), ("w_stages", c_int32), ("ab_stages", c_int32), ("stage_bytes", c_int32),
                 ("workspace_bytes", c_int64), ("b_stages", c_int32), ("dq_sets", c_int32),
-                ("reserved", c_int32 * 4)]
+                ("cta_pair", c_int32), ("reserved", c_int32 * 3)]
 
 
 class QmoeOptions(ctypes.Structure):
     _fields_ = [("split1", c_int32), ("split2", c_int32), ("token_tile", c_int32), ("fault_injection", c_int32),
                 ("issuers", c_int32), ("token_ring", c_int32), ("dq_sets", c_int32),
                 ("weight_l2", c_int32), ("int4_group_epilogue", c_int32), ("topk_reduce", c_int32),
-                ("reserved", c_int32 * 6)]
+                ("cta_pair", c_int32), ("reserved", c_int32 * 5)]
 
 
 class QmoeError(RuntimeError):

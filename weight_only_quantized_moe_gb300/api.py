@@ -345,9 +345,9 @@ class DeviceLayer:
 # device entry points
 # ----------------------------------------------------------------------------
 def make_options(split1=0, split2=0, token_tile=0, fault_injection=0, issuers=0, token_ring=0, dq_sets=0,
-                 weight_l2=0, int4_group_epilogue=0, topk_reduce=0):
+                 weight_l2=0, int4_group_epilogue=0, topk_reduce=0, cta_pair=0):
     return N.QmoeOptions(split1, split2, token_tile, fault_injection, issuers, token_ring, dq_sets, weight_l2,
-                         int4_group_epilogue, topk_reduce)
+                         int4_group_epilogue, topk_reduce, cta_pair)
 
 
 def qmoe_moe_align(topk_ids: torch.Tensor, E: int, block: int, capacity: int | None = None, stream=None):

@@ -41,6 +41,9 @@ SOURCES = [
     "gemm_i8s.cu",
     "gemm_i8sg_f16.cu",
     "gemm_i8sg_bf16.cu",
+    "gemm_i4_f16_pair.cu",
+    "gemm_i4_bf16_pair.cu",
+    "gemm_i8_pair.cu",
     "noalloc.cu",
 ]
 

@@ -158,6 +158,7 @@ struct Plan {
          off_inter32 = 0, off_inter16 = 0, off_iscale = 0, off_h = 0, off_y = 0, off_c13 = 0, off_c2 = 0, total = 0;
   int fused_reduce = 0;  // top-k reduction in the down GEMM's epilogue
   size_t off_cnt = 0;
+  int pair = 0;          // GEMMs on CTA pairs (M = 256 MMAs, half the token rows per CTA)
 };
 
 // Makespan, in pipeline stages, of n work items of k stages each split s ways
@@ -249,7 +250,8 @@ qmoe_status size_gemm_rings(const qmoe_options* o, Plan* p) {
   const size_t wslot = (static_cast<size_t>(p->stage_bytes) + 1023) & ~size_t(1023);
   auto w_depth = [&](int nb2) {
     // (+ the per-group-scaled int4 epilogue's staging buffers)
-    const size_t b_bytes = static_cast<size_t>(nb2) * T * 256 + (p->pg ? kPgStageBytes : 0);
+    // (a CTA of a pair holds half of each token tile's rows)
+    const size_t b_bytes = static_cast<size_t>(nb2) * T * (p->pair ? 128 : 256) + (p->pg ? kPgStageBytes : 0);
     if (b_bytes + 2048 + 2 * wslot > kMaxDynSmem) return 0;
     return static_cast<int>(std::min<size_t>(16, (kMaxDynSmem - 2048 - b_bytes) / wslot)) & ~1;
   };
@@ -331,11 +333,29 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   const bool pg_ok = L->qt == QMOE_INT4_GROUP && T == 16;
   if (o != nullptr && o->int4_group_epilogue == 1 && !pg_ok) return QMOE_ERR_INVALID_ARG;
   p.pg = (pg_ok && o != nullptr && o->int4_group_epilogue == 1) ? 1 : 0;
+  // CTA pairs (option cta_pair: 0 automatic, 1 on, 2 off): symmetric int4 and
+  // per-channel int8 with the standard epilogues
+  if (o != nullptr && (o->cta_pair < 0 || o->cta_pair > 2)) return QMOE_ERR_INVALID_ARG;
+  const bool pair_ok = (L->qt == QMOE_INT4_GROUP || L->qt == QMOE_INT8_PER_COL) && !p.pg &&
+                       !(o != nullptr && o->topk_reduce == 1);
+  if (o != nullptr && o->cta_pair == 1 && !pair_ok) return QMOE_ERR_INVALID_ARG;
+  p.pair = (o != nullptr && o->cta_pair == 1) ? 1 : 0;
   p.n_tiles1 = 2 * L->I / kTileRows;
   p.n_tiles2 = L->H / kTileRows;
   p.kst1 = L->H / kStageK;
   p.kst2 = L->I / kStageK;
   if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
+  // Automatic CTA pairs where shared memory held the single-CTA rings short (a
+  // token-tile ring of one A-ring depth, or fewer than 8 weight slots): each CTA
+  // of a pair holds half of every token tile, so the pair gets the deeper rings
+  // (measured on GB300: Mixtral-8x22B int4 prefill 7-10 % faster, Mixtral-8x7B
+  // int4 M = 512 8 %, int8 M = 128 and 512 9 % and 3 %, 160 experts top-6 int8
+  // M = 1024 7.5 %; where the rings were already deep, pairs were ~2 % slower).
+  if (pair_ok && (o == nullptr || (o->cta_pair == 0 && o->token_ring == 0)) &&
+      (p.b_stages == p.ab_stages || p.w_stages < 8)) {
+    p.pair = 1;
+    if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
+  }
   // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
   p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
   p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
@@ -499,6 +519,7 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
   g1.b_stages = pl.b_stages;
   g1.dq_sets = pl.dq_sets;
   g1.pg = pl.pg;
+  g1.pair = pl.pair;
   g1.d_col0 = pl.d_col0;
   g1.pg_corr = c13;
   g1.pg_cap = pl.cap;
@@ -546,10 +567,13 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
     g2.out_bf16 = bf16 ? 1 : 0;
   }
 
-  const int64_t items1 = pl.max_chunks * pl.n_tiles1 * pl.S1;
-  const int64_t items2 = pl.max_chunks * pl.n_tiles2 * pl.S2;
-  const int grid1 = static_cast<int>(std::min<int64_t>(sms, items1));
-  const int grid2 = static_cast<int>(std::min<int64_t>(sms, items2));
+  // (CTA pairs: work items over tile pairs, two CTAs per item)
+  const int64_t items1 = pl.max_chunks * (pl.pair ? (pl.n_tiles1 + 1) / 2 : pl.n_tiles1) * pl.S1;
+  const int64_t items2 = pl.max_chunks * (pl.pair ? (pl.n_tiles2 + 1) / 2 : pl.n_tiles2) * pl.S2;
+  const int grid1 = pl.pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, items1))
+                            : static_cast<int>(std::min<int64_t>(sms, items1));
+  const int grid2 = pl.pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, items2))
+                            : static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
     err = launch_gemm(kind_of(L->qt, L->group_size), bf16, g1, grid1, stream);  // in-block scales have the activation dtype
@@ -633,6 +657,8 @@ qmoe_status make_linear_plan(const qmoe_linear* L, int64_t M, const qmoe_options
     T = o->token_tile;
   }
   p.T = T;
+  // (the dense linear layer runs on single CTAs)
+  if (o != nullptr && (o->cta_pair < 0 || o->cta_pair > 2 || o->cta_pair == 1)) return QMOE_ERR_INVALID_ARG;
   p.stage_bytes = stage_bytes_of(L->qt, L->group_size);
   p.n_tiles1 = L->N / kTileRows;
   p.kst1 = L->K / kStageK;
@@ -1412,6 +1438,7 @@ qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k
   info->ab_stages = pl.ab_stages;
   info->b_stages = pl.b_stages;
   info->dq_sets = pl.dq_sets;
+  info->cta_pair = pl.pair;
   info->stage_bytes = pl.stage_bytes;
   info->workspace_bytes = static_cast<int64_t>(pl.total);
   return QMOE_OK;

@@ -80,16 +80,22 @@ constexpr uint32_t kIdescSparse = 1u << 2;  // instruction descriptor: A is 2:4 
 constexpr int kBarrierBytes = 1024;
 
 __host__ __device__ inline uint32_t gemm_w_slot(int group_bytes) { return (group_bytes + 1023u) & ~1023u; }
+// Bytes of one token-tile ring slot: the tile's rows of one 128-K stage (a CTA of
+// a pair holds half of them).
+__host__ __device__ inline uint32_t gemm_b_slot(int token_tile, bool pair) {
+  return static_cast<uint32_t>(token_tile) * (pair ? 128u : 256u);
+}
 // Dynamic shared memory: weight ring, token-tile ring, barriers, the per-group
 // staging buffers (per-group-scaled int4 only), +1 KB alignment slack.
 __host__ __device__ inline size_t gemm_smem_layout_bytes(int w_stages, int group_bytes, int b_stages, int token_tile,
-                                                         bool pg) {
+                                                         bool pg, bool pair) {
   return 1024 + static_cast<size_t>(w_stages) * gemm_w_slot(group_bytes) +
-         static_cast<size_t>(b_stages) * token_tile * 256 + kBarrierBytes + (pg ? kPgStageBytes : 0);
+         static_cast<size_t>(b_stages) * gemm_b_slot(token_tile, pair) + kBarrierBytes + (pg ? kPgStageBytes : 0);
 }
 
 struct WorkItem {
   int e, row0, nrows, tile, split_idx, ks0, ks1;
+  bool phantom;  // CTA pair, odd tile count: the odd CTA's tile of the last pair does not exist
 };
 
 // Work item i -> (split, chunk, tile).  Items of one split are rastered in
@@ -100,31 +106,39 @@ struct WorkItem {
 // group is a piece of at most G chunks of one expert (large batches: each
 // weight tile is then read once per piece, while the piece's token tiles stay
 // in L2); group (start s, n chunks) owns items [s, s + n) x n_tiles, so the
-// chunk at item / n_tiles names the group.
-__device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i, WorkItem& w) {
-  const int per_split = nch * p.n_tiles;
+// chunk at item / n_tiles names the group.  On CTA pairs the items run over tile
+// pairs instead of tiles, and CTA `rank` of the pair takes tile 2 * pair + rank;
+// with an odd tile count the last pair's odd tile is a phantom: that CTA reads
+// the last real tile again (the pair MMA needs its A rows and its half of the
+// token rows) and stores nothing.
+template <bool PAIR>
+__device__ __forceinline__ void decode_item(const GemmParams& p, int nch, int i, uint32_t rank, WorkItem& w) {
+  const int n_units = PAIR ? (p.n_tiles + 1) >> 1 : p.n_tiles;
+  const int per_split = nch * n_units;
   const int s = i / per_split;
   const int r = i - s * per_split;
   int c0, cg;
   if (p.chunk_group > 0) {
-    const int grp_items = p.chunk_group * p.n_tiles;
+    const int grp_items = p.chunk_group * n_units;
     c0 = (r / grp_items) * p.chunk_group;
     cg = min(p.chunk_group, nch - c0);
   } else {
     const int G = -p.chunk_group;
-    const Chunk cu = p.chunks[r / p.n_tiles];
-    const int piece = (r / p.n_tiles - cu.first) / G;
+    const Chunk cu = p.chunks[r / n_units];
+    const int piece = (r / n_units - cu.first) / G;
     c0 = cu.first + piece * G;
     cg = min(G, cu.count - piece * G);
   }
-  const int rem = r - c0 * p.n_tiles;
-  const int tile = rem / cg;
-  const int c = c0 + (rem - tile * cg);
+  const int rem = r - c0 * n_units;
+  const int unit = rem / cg;
+  const int c = c0 + (rem - unit * cg);
   const Chunk ch = p.chunks[c];
+  const int tile = PAIR ? 2 * unit + static_cast<int>(rank) : unit;
   w.e = ch.expert;
   w.row0 = ch.row0;
   w.nrows = ch.nrows;
-  w.tile = tile;
+  w.phantom = PAIR && tile >= p.n_tiles;
+  w.tile = w.phantom ? p.n_tiles - 1 : tile;
   w.split_idx = s;
   w.ks0 = static_cast<int>(static_cast<int64_t>(p.k_groups) * s / p.split);
   w.ks1 = static_cast<int>(static_cast<int64_t>(p.k_groups) * (s + 1) / p.split);
@@ -330,13 +344,20 @@ __device__ __forceinline__ void mma_stage_sp(uint32_t issue, uint32_t d, uint32_
 // between two tcgen05.mma instructions roughly triples their issue cost.  The
 // A operand's K step kk is TMEM column a + 8kk; B's is 32 bytes along the
 // 128-byte swizzled rows, the second 64-K block 1024 bytes after the first.
-// Executed by the whole issuer warp; the lane with `issue` set issues.
+// Executed by the whole issuer warp; the lane with `issue` set issues (M = 256
+// pair MMAs from a CTA pair's even CTA).
+template <bool PAIR>
 __device__ __forceinline__ void mma_stage(uint32_t issue, uint32_t d, uint32_t a, uint64_t bdesc0, uint32_t idesc,
                                           uint32_t acc0) {
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    mma_ts_f16(issue, d, a + static_cast<uint32_t>(kk * 8), bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2),
-               idesc, kk > 0 ? 1u : acc0);
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t ak = a + static_cast<uint32_t>(kk * 8);
+    const uint64_t bk = bdesc0 + static_cast<uint64_t>((kk >> 2) * 64 + (kk & 3) * 2);
+    if constexpr (PAIR)
+      mma_ts_f16_pair(issue, d, ak, bk, idesc, kk > 0 ? 1u : acc0);
+    else
+      mma_ts_f16(issue, d, ak, bk, idesc, kk > 0 ? 1u : acc0);
+  }
 }
 
 __device__ __forceinline__ float silu_dev(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -448,18 +469,19 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const WorkIt
 // only its own stages (every 2nd for producers and dequant sets, every NI-th
 // for the MMA issuers), stepping its ring positions by the same stride.
 // ---------------------------------------------------------------------------
-template <int KIND, bool BF16S>
+template <int KIND, bool BF16S, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmParams p) {
   constexpr bool INT4 = KIND == kQ4 || KIND == kQ4Z || KIND == kQ4P;
   constexpr bool PG = KIND == kQ4P;  // per-group scaling in the epilogue
   constexpr bool SPARSE = KIND == kQ4S || KIND == kQ8S || KIND == kQ8SG;
+  static_assert(!PAIR || (!PG && !SPARSE), "CTA pairs run the dense formats with the standard epilogue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int T = p.token_tile;
   const int NW = p.w_stages, NB = p.ab_stages, NB2 = p.b_stages, ACCB = p.acc_bufs, NI = p.issuers;
   const uint32_t wslot = gemm_w_slot(p.stage_bytes);
-  const uint32_t bslot = static_cast<uint32_t>(T) * 256u;
+  const uint32_t bslot = gemm_b_slot(T, PAIR);
   uint8_t* wring = smem;
   uint8_t* bring = smem + NW * wslot;
 
@@ -479,6 +501,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: both CTAs of a cluster walk the same items and stages; rank 0
+  // issues the pair's MMAs
+  const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
+  const int item0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int item_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     const uint32_t wps = 16u / static_cast<uint32_t>(p.dq_sets);  // warps of a dequant set
@@ -486,20 +513,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       mbar_init(smem_u32(wfull + s), 1);
       mbar_init(smem_u32(wempty + s), wps);
     }
-    // with per-group scaling the 4 epilogue warps also release each A slot's D slot
-    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), wps + (PG ? 4u : 0u));
+    // with per-group scaling the 4 epilogue warps also release each A slot's D slot;
+    // on CTA pairs the even CTA's A and accumulator barriers count both CTAs' warps
+    for (int j = 0; j < NB; ++j) mbar_init(smem_u32(afull + j), (PAIR ? 2u : 1u) * wps + (PG ? 4u : 0u));
     for (int j = 0; j < NB2; ++j) mbar_init(smem_u32(done + j), 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(accfull + b), NI);  // one commit from each MMA issuer per item
-      mbar_init(smem_u32(accempty + b), 4);  // the 4 epilogue warps
+      mbar_init(smem_u32(accfull + b), NI);               // one commit from each MMA issuer per item
+      mbar_init(smem_u32(accempty + b), PAIR ? 8u : 4u);  // the 4 epilogue warps (of each CTA)
     }
     for (int i = 0; i < kMaxIssuers; ++i) mbar_init(smem_u32(drain + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -510,7 +544,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   pdl_wait();
 
   const int nch = *p.n_chunks;
-  const int n_items = nch * p.n_tiles * p.split;
+  const int n_items = nch * (PAIR ? (p.n_tiles + 1) >> 1 : p.n_tiles) * p.split;
   const uint32_t a_col0 = static_cast<uint32_t>(p.a_col0);
 
   if (warp == kProducerWarp || warp == kProducerWarp2) {
@@ -526,15 +560,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       wr.idx = br.idx = id;
       int g0 = 0, last_w = -1, last_b = -1;
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      for (int i = item0; i < n_items && ok; i += item_step) {
         WorkItem it;
-        decode_item(p, nch, i, it);
+        decode_item<PAIR>(p, nch, i, rank, it);
         const int n_st = it.ks1 - it.ks0;
         const uint8_t* wsrc =
             p.w + (static_cast<int64_t>(it.e) * p.n_tiles + it.tile) * p.k_groups * static_cast<int64_t>(p.stage_bytes);
         // the chunk's rows of one stage of the pre-staged B operand: one contiguous run
-        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * 256u;
-        const uint8_t* bsrc = p.b + static_cast<int64_t>(it.row0) * 256;
+        // (a CTA pair's CTA: its half of the rows, whole 8-row groups as chunks hold
+        // multiples of 16 rows)
+        const uint32_t b_run = static_cast<uint32_t>(it.nrows) * (PAIR ? 128u : 256u);
+        const uint8_t* bsrc =
+            p.b + (static_cast<int64_t>(it.row0) + static_cast<int64_t>(rank) * (it.nrows >> 1)) * 256;
         for (int g = first_own(g0, id, 2); g < g0 + n_st; g += 2, wr.step(2, NW), br.step(2, NB2)) {
           const int ks = it.ks0 + (g - g0);
           const bool inject = p.fault_injection == 1 && blockIdx.x == 0 && g == 0;  // armed, never filled
@@ -577,17 +614,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
     const int id = (warp == kMmaWarp3) ? 2 : warp - kMmaWarp;
     // The whole warp walks the loop, converged, and one elected lane issues: the
     // slot addresses and descriptors then stay warp-uniform.
-    if (id < NI) {
+    // On CTA pairs the even CTA issues M = 256 MMAs for both and multicasts its
+    // commits to both CTAs' barriers.
+    auto commit = [&](uint32_t issue, uint32_t bar) {
+      if constexpr (PAIR)
+        mma_commit_pair(issue, bar);
+      else
+        mma_commit(issue, bar);
+    };
+    if (id < NI && rank == 0) {
       const uint32_t issue = elect_one_sync();
       Ring ar, br;  // A slot (NB) and token-tile slot / done barrier (NB2) of the stage
       ar.idx = br.idx = id;
       int g0 = 0, itn = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      for (int i = item0; i < n_items && ok; i += item_step) {
         WorkItem it;
-        decode_item(p, nch, i, it);
+        decode_item<PAIR>(p, nch, i, rank, it);
         const int n_st = it.ks1 - it.ks0;
-        const uint32_t idesc = make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
+        const uint32_t idesc = PAIR ? make_idesc_m256(static_cast<uint32_t>(it.nrows), false)
+                                    : make_idesc_m128(static_cast<uint32_t>(it.nrows), false);
         const int b = (ACCB == 2) ? (itn & 1) : 0;
         const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
         if (!PG) {
@@ -608,23 +654,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
             mma_stage_sp(issue, d_acc, a_tmem, bdesc0, idesc | kIdescSparse, acc0);
           } else if (PG) {
             // per-group scaling: the stage's sum goes to the D slot of its A slot, fresh
-            mma_stage(issue, tmem + static_cast<uint32_t>(p.d_col0) + static_cast<uint32_t>(ar.idx * 16), a_tmem,
-                      bdesc0, idesc, 0u);
+            mma_stage<PAIR>(issue, tmem + static_cast<uint32_t>(p.d_col0) + static_cast<uint32_t>(ar.idx * 16),
+                            a_tmem, bdesc0, idesc, 0u);
           } else {
-            mma_stage(issue, d_acc, a_tmem, bdesc0, idesc, acc0);
+            mma_stage<PAIR>(issue, d_acc, a_tmem, bdesc0, idesc, acc0);
           }
           acc0 = 1u;
-          mma_commit(issue, smem_u32(done + br.idx));
+          commit(issue, smem_u32(done + br.idx));
         }
         if (!ok) break;
         // every issuer signals the item's end, also when it had no stage of it
-        if (!PG) mma_commit(issue, smem_u32(accfull + b));
+        if (!PG) commit(issue, smem_u32(accfull + b));
         g0 += n_st;
         ++itn;
       }
       if (!ok && issue) raise_abort(reinterpret_cast<volatile int*>(abort_flag), p.status);
-      // all MMAs this warp issued must finish before TMEM is released
-      mma_commit(issue, smem_u32(drain + id));
+      // all MMAs this warp issued must finish before TMEM is released (in both CTAs of a pair)
+      commit(issue, smem_u32(drain + id));
+      mbar_wait_drain(smem_u32(drain + id), 0);
+    } else if (PAIR && id < NI) {
+      // a pair's odd CTA: its TMEM and shared memory stay in use until the even
+      // CTA's issuer reports all its MMAs complete
       mbar_wait_drain(smem_u32(drain + id), 0);
     }
   } else if (warp >= kDequantWarp0) {
@@ -666,9 +716,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       tmem_st_32x32b_x1(ta + 40u + static_cast<uint32_t>(16 * half), pos.y);
       return true;
     };
-    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+    for (int i = item0; i < n_items && ok; i += item_step) {
       WorkItem it;
-      decode_item(p, nch, i, it);
+      decode_item<PAIR>(p, nch, i, rank, it);
       const int n_st = it.ks1 - it.ks0;
       for (int g = first_own(g0, set, DS); g < g0 + n_st;
            g += DS, wr.step(DS, NW), ar.step(DS, NB), dr.step(DS, NB2)) {
@@ -758,7 +808,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(afull + ar.idx));
+        if (lane == 0) {
+          // (a pair's A barriers live in the even CTA and count both CTAs' sets)
+          if (PAIR)
+            mbar_arrive_remote(map_to_rank(smem_u32(afull + ar.idx), 0));
+          else
+            mbar_arrive(smem_u32(afull + ar.idx));
+        }
       }
       g0 += n_st;
     }
@@ -790,22 +846,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         WorkItem it;
       };
       auto seg_first = [&](Seg& sg) {
-        sg.i = blockIdx.x;
+        sg.i = item0;
         sg.s0 = 0;
-        if (sg.i < n_items) decode_item(p, nch, sg.i, sg.it);
+        if (sg.i < n_items) decode_item<PAIR>(p, nch, sg.i, rank, sg.it);
         sg.n = sg.i < n_items ? min(kPgSeg, sg.it.ks1 - sg.it.ks0) : 0;
       };
       auto seg_next = [&](Seg& sg) {
         if (sg.n == 0) return;
         sg.s0 += sg.n;
         if (sg.s0 == sg.it.ks1 - sg.it.ks0) {
-          sg.i += gridDim.x;
+          sg.i += item_step;
           sg.s0 = 0;
           if (sg.i >= n_items) {
             sg.n = 0;
             return;
           }
-          decode_item(p, nch, sg.i, sg.it);
+          decode_item<PAIR>(p, nch, sg.i, rank, sg.it);
         }
         sg.n = min(kPgSeg, sg.it.ks1 - sg.it.ks0 - sg.s0);
       };
@@ -896,9 +952,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
       // no copy of this thread may still be in flight when the CTA exits
       cp_async_wait_group<0>();
     }
-    for (int i = PG ? n_items : static_cast<int>(blockIdx.x); i < n_items && ok; i += gridDim.x) {
+    for (int i = PG ? n_items : item0; i < n_items && ok; i += item_step) {
       WorkItem it;
-      decode_item(p, nch, i, it);
+      decode_item<PAIR>(p, nch, i, rank, it);
       const int b = (ACCB == 2) ? (itn & 1) : 0;
       const uint32_t use = (ACCB == 2) ? (itn >> 1) : itn;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accfull + b), use & 1u, abort_flag, 512));
@@ -929,7 +985,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
         if (c0 + 16 >= it.nrows) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(accempty + b));
+          if (lane == 0) {
+            if (PAIR)
+              mbar_arrive_remote(map_to_rank(smem_u32(accempty + b), 0));
+            else
+              mbar_arrive(smem_u32(accempty + b));
+          }
         }
         const float4* cs4 = reinterpret_cast<const float4*>(p.col_scale + it.row0 + c0);
 #pragma unroll
@@ -940,7 +1001,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
           f[4 * c + 2] *= rs * v4.z;
           f[4 * c + 3] *= rs * v4.w;
         }
-        epilogue_store(p, it, c0, row, lane, f);
+        if (!it.phantom) epilogue_store(p, it, c0, row, lane, f);
       }
       ++itn;
     }
@@ -948,21 +1009,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qmoe_gemm_kernel(const GemmPa
   }
 
   // ------------------------------------------------------------ teardown
+  // (on CTA pairs no remote arrive and no pair MMA touches either CTA after the
+  // cluster barrier)
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int KIND, bool BF16S>
+template <int KIND, bool BF16S, bool PAIR = false>
 cudaError_t launch_gemm_t(const GemmParams& p, int grid, cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p);
-  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<KIND, BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = cudaFuncSetAttribute(qmoe_gemm_kernel<KIND, BF16S, PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_kernel(qmoe_gemm_kernel<KIND, BF16S>, dim3(grid), dim3(kGemmThreads), smem, stream, true, p);
+  if (!PAIR) return launch_kernel(qmoe_gemm_kernel<KIND, BF16S, PAIR>, dim3(grid), dim3(kGemmThreads), smem, stream, true, p);
+  // clusters of 2 CTAs (an even grid)
+  if (grid % 2 != 0 || p.pair == 0) return cudaErrorInvalidValue;
+  return launch_kernel_cluster(qmoe_gemm_kernel<KIND, BF16S, PAIR>, dim3(grid), dim3(kGemmThreads), smem, stream, true,
+                               2u, p);
 }
 
 }  // namespace qmoe

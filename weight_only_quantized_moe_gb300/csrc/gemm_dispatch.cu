@@ -17,9 +17,12 @@ cudaError_t launch_gemm_i8g_bf16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8s(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8sg_f16(const GemmParams&, int, cudaStream_t);
 cudaError_t launch_gemm_i8sg_bf16(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i4_f16_pair(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i4_bf16_pair(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_gemm_i8_pair(const GemmParams&, int, cudaStream_t);
 
 size_t gemm_smem_bytes(const GemmParams& p) {
-  return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.b_stages, p.token_tile, p.pg != 0);
+  return gemm_smem_layout_bytes(p.w_stages, p.stage_bytes, p.b_stages, p.token_tile, p.pg != 0, p.pair != 0);
 }
 
 cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, int grid, cudaStream_t stream) {
@@ -42,6 +45,14 @@ cudaError_t launch_gemm(QuantKind kind, bool bf16_scales, const GemmParams& p, i
   // the TMEM address and the abort flag fit the barrier area
   if ((2 * p.w_stages + p.ab_stages + p.b_stages + 4 + kMaxIssuers) * 8 + 8 > kBarrierBytes)
     return cudaErrorInvalidValue;
+  // CTA pairs: dense int4 (symmetric) and per-column int8 with the standard epilogue and
+  // the separate top-k reduction; token tiles whose halves are whole 8-row groups
+  if (p.pair) {
+    if (p.pg || p.red_cnt != nullptr || p.token_tile % 16 != 0) return cudaErrorInvalidValue;
+    if (kind == kQ4) return bf16_scales ? launch_gemm_i4_bf16_pair(p, grid, stream) : launch_gemm_i4_f16_pair(p, grid, stream);
+    if (kind == kQ8) return launch_gemm_i8_pair(p, grid, stream);
+    return cudaErrorInvalidValue;
+  }
   switch (kind) {
     case kQ4:
       if (p.pg) return bf16_scales ? launch_gemm_i4p_bf16(p, grid, stream) : launch_gemm_i4p_f16(p, grid, stream);

@@ -38,6 +38,27 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
+// thread-block clusters (the GEMM's CTA-pair form)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of the cluster arrives; returns once all have (release / acquire
+// at cluster scope, so barrier initialisation and shared-memory writes before it
+// are visible to the other CTAs after it).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared::cluster address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -77,6 +98,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
+}
+
+// Arrive once on the barrier at shared::cluster address `remote_bar` (another
+// CTA's, or this CTA's own through the cluster window).  Default semantics
+// (release at CTA scope): the callers order their tensor-memory stores or loads
+// with tcgen05.wait + tcgen05.fence::before_thread_sync and the waiter with
+// tcgen05.fence::after_thread_sync, as for a local barrier; a release at cluster
+// scope costs the arriving thread ~320 cycles (measured on GB300).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
 // Wait until the phase with the given parity has completed.  Returns false if
@@ -202,6 +233,18 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// The same for a CTA pair (cta_group::2): one warp in each CTA of the pair executes
+// them with the same column count, and both CTAs receive the same TMEM address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -263,6 +306,32 @@ __device__ __forceinline__ void mma_commit(uint32_t issue, uint32_t bar) {
       : "memory");
 }
 
+// Pair MMA, issued from the even CTA of a CTA pair: D (+)= A * B^T with M = 256
+// (rows 0-127 in the even CTA's TMEM lanes, 128-255 in the odd CTA's, A and D at
+// the same TMEM address in both), N from idesc (each CTA's shared memory holds N/2
+// rows of B at the same address), K = 16 (16-bit types).
+__device__ __forceinline__ void mma_ts_f16_pair(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
+// Arrive once on the barrier at this shared-memory offset in both CTAs of the pair
+// when every tcgen05 operation issued so far by the issuing lane has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t issue, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(static_cast<uint16_t>(0x3)), "r"(issue)
+      : "memory");
+}
+
 // Instruction descriptor of kind::f16: D f32, A/B f16 or bf16, both K-major, M = 128.
 __host__ __device__ __forceinline__ uint32_t make_idesc_m128(uint32_t n, bool bf16) {
   const uint32_t ab = bf16 ? 1u : 0u;
@@ -271,6 +340,12 @@ __host__ __device__ __forceinline__ uint32_t make_idesc_m128(uint32_t n, bool bf
          | (ab << 10)          // B format
          | ((n >> 3) << 17)    // N / 8
          | ((128u >> 4) << 24);  // M / 16
+}
+
+// The same with M = 256 (a CTA pair's MMA).
+__host__ __device__ __forceinline__ uint32_t make_idesc_m256(uint32_t n, bool bf16) {
+  const uint32_t ab = bf16 ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((n >> 3) << 17) | ((256u >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
