@@ -454,12 +454,16 @@ qmoe_status qmoe_forward_profiled(const qmoe_layer* layer, const void* x, int64_
                                   int32_t* n_launches);
 
 /*
- * Same layer with x, topk_ids, topk_weights and out in HOST memory (page-locked
- * memory makes the copies asynchronous).  The call enqueues the host-to-device
- * copies of the inputs, the forward, and the device-to-host copy of out on
- * `stream`; out is valid once the stream has been synchronised.  The workspace
- * (device) must hold qmoe_workspace_size_host bytes: the device staging of the
- * inputs and output lives in it.
+ * Same layer with x, topk_ids, topk_weights and out in HOST memory; out is
+ * valid once `stream` has been synchronised.  When all four are page-locked
+ * buffers mapped into the device's address space (cudaHostAlloc memory on a
+ * unified-addressing system, e.g. pinned memory on a Grace-Blackwell node,
+ * where the GPU reaches it over NVLink-C2C) with x and out 256-byte aligned,
+ * the forward's kernels read the inputs and write out in place and no copy is
+ * enqueued.  Otherwise the call enqueues host-to-device copies of the inputs
+ * into device staging, the forward, and the device-to-host copy of out
+ * (page-locked memory makes those copies asynchronous).  The workspace
+ * (device) must hold qmoe_workspace_size_host bytes (the staging lives in it).
  */
 size_t qmoe_workspace_size_host(const qmoe_layer* layer, int64_t M, int32_t top_k);
 qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64_t M,

@@ -253,8 +253,47 @@ def test_deterministic_and_host_path_identical():
     outh = torch.empty_like(xh).pin_memory()
     ws = q.alloc_workspace(q.qmoe_workspace_size_host(dl, 50, wl.k))
     q.qmoe_forward_host(dl, xh, idsh, wh, outh, ws)
+    torch.cuda.synchronize()
     assert q.qmoe_read_device_status(ws) == q.QMOE_OK
     assert torch.equal(outh, a.cpu())
+
+
+def _offset_pinned(t, offset_bytes):
+    """A pinned copy of t whose data starts offset_bytes past a pinned allocation's start."""
+    n = t.numel() * t.element_size()
+    raw = torch.empty(n + offset_bytes, dtype=torch.uint8).pin_memory()
+    view = raw[offset_bytes:offset_bytes + n].view(t.dtype).view(t.shape)
+    view.copy_(t)
+    return view
+
+
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned_unaligned"])
+@pytest.mark.parametrize("M", [1, 50, 300])
+def test_host_path_memory_kinds(memory, M):
+    """qmoe_forward_host with page-locked mapped buffers (the kernels read the
+    inputs and write out in host memory in place), with pageable buffers and
+    with pinned buffers whose x and out miss the 256-byte alignment (both staged
+    through device copies): all bit-identical to the device-buffer forward."""
+    wl = _wl("int4", "bf16", False)
+    L, dl = _layer(wl)
+    inp = make_inputs(wl, M, seed=9)
+    x, ids, w = device_inputs(wl, inp)
+    want, _ = run_forward(dl, x, ids, w)
+    if memory == "pinned":
+        xh, idsh, wh = x.cpu().pin_memory(), ids.cpu().pin_memory(), w.cpu().pin_memory()
+        outh = torch.full_like(xh, float("nan")).pin_memory()
+    elif memory == "pageable":
+        xh, idsh, wh = x.cpu(), ids.cpu(), w.cpu()
+        outh = torch.full_like(xh, float("nan"))
+    else:
+        xh, idsh, wh = _offset_pinned(x.cpu(), 16), ids.cpu().pin_memory(), w.cpu().pin_memory()
+        outh = _offset_pinned(torch.full_like(x.cpu(), float("nan")), 16)
+    ws = q.alloc_workspace(q.qmoe_workspace_size_host(dl, M, wl.k))
+    for _ in range(2):
+        q.qmoe_forward_host(dl, xh, idsh, wh, outh, ws)
+        torch.cuda.synchronize()
+        assert q.qmoe_read_device_status(ws) == q.QMOE_OK
+        assert torch.equal(outh, want.cpu()), memory
 
 
 def test_zero_tokens_is_a_no_op():

@@ -73,6 +73,18 @@ qmoe_status check_dev_ptr(const void* p, int dev) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Device address of a page-locked host buffer mapped into the device's address
+// space, else nullptr (pageable or device memory, or an unknown pointer).
+const void* mapped_host_ptr(const void* p) {
+  if (p == nullptr) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // ---------------------------------------------------------------------------
 // layer validation and the forward plan
 // ---------------------------------------------------------------------------
@@ -416,10 +428,13 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
   return QMOE_OK;
 }
 
+// host_io: x, topk_ids, topk_weights and out are the device addresses of
+// page-locked, device-mapped host buffers (checked by the caller); the kernels
+// read and write them in place with plain loads and stores.
 qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const int32_t* topk_ids,
                          const float* topk_weights, int32_t k, void* out, void* ws, size_t ws_bytes,
                          cudaStream_t stream, const qmoe_options* opts, void* const* events = nullptr,
-                         int32_t* n_launches = nullptr) {
+                         int32_t* n_launches = nullptr, bool host_io = false) {
   const int sms = current_sm_count();
   Plan pl;
   qmoe_status st = make_plan(L, M, k, opts, sms, &pl);
@@ -431,9 +446,10 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
     cudaGetLastError();
     return QMOE_ERR_CUDA;
   }
-  const void* ptrs[] = {x, topk_ids, topk_weights, out, ws, L->w13, L->w2};
-  for (const void* p : ptrs)
-    if ((st = check_dev_ptr(p, dev)) != QMOE_OK) return st;
+  const void* ptrs[] = {ws, L->w13, L->w2, x, topk_ids, topk_weights, out};
+  const int n_checked = host_io ? 3 : 7;  // (host_io: the caller checked the four I/O buffers)
+  for (int i = 0; i < n_checked; ++i)
+    if ((st = check_dev_ptr(ptrs[i], dev)) != QMOE_OK) return st;
   // only per-column int8 keeps its scales outside the packed weight blocks
   const bool row_scales = has_row_scales(L->qt, L->group_size);
   if (row_scales) {
@@ -1490,13 +1506,24 @@ qmoe_status qmoe_forward_host(const qmoe_layer* layer, const void* x_host, int64
   if (workspace == nullptr || workspace_bytes < qmoe_workspace_size_host(layer, M, top_k)) return QMOE_ERR_WORKSPACE;
   const size_t xb = static_cast<size_t>(M) * layer->H * 2;
   const size_t pb = static_cast<size_t>(M) * top_k * 4;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Page-locked host buffers that the GPU can address (over NVLink-C2C on a
+  // Grace-Blackwell node): the forward reads the inputs and writes the output
+  // in place, with no staging copies; other host memory is staged below.
+  const void* xm = mapped_host_ptr(x_host);
+  const void* im = mapped_host_ptr(topk_ids_host);
+  const void* wm = mapped_host_ptr(topk_weights_host);
+  const void* om = mapped_host_ptr(out_host);
+  if (xm != nullptr && im != nullptr && wm != nullptr && om != nullptr && aligned(xm, 256) && aligned(om, 256) &&
+      aligned(im, 4) && aligned(wm, 4))
+    return forward_impl(layer, xm, M, static_cast<const int32_t*>(im), static_cast<const float*>(wm), top_k,
+                        const_cast<void*>(om), workspace, w, s, nullptr, nullptr, nullptr, true);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   uint8_t* stage = base + al256(w);
   void* x_dev = stage;
   int32_t* ids_dev = reinterpret_cast<int32_t*>(stage + al256(xb));
   float* w_dev = reinterpret_cast<float*>(stage + al256(xb) + al256(pb));
   void* out_dev = stage + al256(xb) + 2 * al256(pb);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(ids_dev, topk_ids_host, pb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(w_dev, topk_weights_host, pb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
