@@ -386,7 +386,9 @@ size_t qmoe_workspace_size_ex(const qmoe_layer* layer, int64_t M, int32_t top_k,
  * split1 / split2 (split-K of the gate/up and down GEMMs), w_stages (packed-
  * weight ring depth), ab_stages (TMEM A ring depth), b_stages (token-tile ring
  * depth, a multiple of ab_stages), dq_sets (dequant warp sets), cta_pair (1: the
- * GEMMs run on CTA pairs), stage_bytes
+ * gate/up GEMM runs on CTA pairs; the ring fields describe that GEMM),
+ * cta_pair_down (1: the down GEMM runs on CTA pairs too; automatic plans keep it
+ * on single CTAs when its K spans fewer than 32 stages of 128), stage_bytes
  * (packed bytes per 128 x 128 block), workspace_bytes.  num_sms: the GPU's
  * SM count the plan is sized for (0: the current device's).  Errors as
  * qmoe_workspace_size_ex (QMOE_ERR_INVALID_ARG / QMOE_ERR_UNSUPPORTED), and
@@ -405,7 +407,8 @@ typedef struct {
   int32_t b_stages;
   int32_t dq_sets;
   int32_t cta_pair;
-  int32_t reserved[3];
+  int32_t cta_pair_down;
+  int32_t reserved[2];
 } qmoe_plan_info;
 
 qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k, const qmoe_options* opts,

@@ -283,6 +283,12 @@ def test_cta_pair_option():
     I8 = dict(E=8, H=4096, I=14336, group_size=-1, qt=N.QMOE_INT8_PER_COL, scale_dtype=N.QMOE_F32)
     assert [_plan(I8, M)["cta_pair"] for M in (16, 128, 512)] == [0, 1, 1]
     assert _plan(MIXTRAL, 2048, token_ring=1)["cta_pair"] == 0      # rings set by hand: no automatic pair
+    # the down GEMM follows, except where its K spans fewer than 32 stages (I = 1536: 12)
+    assert _plan(MIXTRAL, 2048)["cta_pair_down"] == 1 and _plan(MIXTRAL, 16)["cta_pair_down"] == 0
+    DS = dict(E=160, H=5120, I=1536, group_size=-1, qt=N.QMOE_INT8_PER_COL, scale_dtype=N.QMOE_F32)
+    p1024 = _plan(DS, 1024, k=6)
+    assert p1024["cta_pair"] == 1 and p1024["cta_pair_down"] == 0
+    assert _plan(DS, 1024, k=6, cta_pair=1)["cta_pair_down"] == 1        # the option pairs both
     lin = N.QmoeLinear(4096, 14336, 128, N.QMOE_INT4_GROUP, N.QMOE_F16, N.QMOE_F16, None, None, None)
     assert L.qmoe_linear_workspace_size(ctypes.byref(lin), 16, ctypes.byref(q.make_options(cta_pair=1))) == 0
     assert L.qmoe_linear_workspace_size(ctypes.byref(lin), 16, ctypes.byref(q.make_options(cta_pair=2))) > 0

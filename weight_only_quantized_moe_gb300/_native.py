@@ -53,7 +53,7 @@ class QmoePlanInfo(ctypes.Structure):
     _fields_ = [("token_tile", c_int32), ("issuers", c_int32), ("acc_bufs", c_int32), ("split1", c_int32),
                 ("split2", c_int32), ("w_stages", c_int32), ("ab_stages", c_int32), ("stage_bytes", c_int32),
                 ("workspace_bytes", c_int64), ("b_stages", c_int32), ("dq_sets", c_int32),
-                ("cta_pair", c_int32), ("reserved", c_int32 * 3)]
+                ("cta_pair", c_int32), ("cta_pair_down", c_int32), ("reserved", c_int32 * 2)]
 
 
 class QmoeOptions(ctypes.Structure):

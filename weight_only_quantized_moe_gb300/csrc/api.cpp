@@ -171,7 +171,24 @@ struct Plan {
   int fused_reduce = 0;  // top-k reduction in the down GEMM's epilogue
   size_t off_cnt = 0;
   int pair = 0;          // GEMMs on CTA pairs (M = 256 MMAs, half the token rows per CTA)
+  // the down GEMM's launch shape where it differs from the gate/up GEMM's
+  struct Rings {
+    int issuers = 0, acc_bufs = 0, a_col0 = 0, w_stages = 0, ab_stages = 0, b_stages = 0, dq_sets = 2, pair = 0;
+  } r2;
 };
+
+Plan::Rings rings_of(const Plan& p) {
+  Plan::Rings r;
+  r.issuers = p.issuers;
+  r.acc_bufs = p.acc_bufs;
+  r.a_col0 = p.a_col0;
+  r.w_stages = p.w_stages;
+  r.ab_stages = p.ab_stages;
+  r.b_stages = p.b_stages;
+  r.dq_sets = p.dq_sets;
+  r.pair = p.pair;
+  return r;
+}
 
 // Makespan, in pipeline stages, of n work items of k stages each split s ways
 // over C persistent CTAs.  A CTA's items run back to back; each item costs the
@@ -368,6 +385,17 @@ qmoe_status make_plan(const qmoe_layer* L, int64_t M, int32_t k, const qmoe_opti
     p.pair = 1;
     if ((st = size_gemm_rings(o, &p)) != QMOE_OK) return st;
   }
+  // The down GEMM on single CTAs where its K spans fewer than 32 stages: its
+  // items are then too short for the pair's deeper rings to pay for the pair's
+  // per-item fill and epilogue (measured on GB300 with 160 experts top-6, K =
+  // 1536 in 12 stages: 4 % slower on pairs at M = 1024, while every down GEMM
+  // with K of 112-128 stages was 2-13 % faster).
+  p.r2 = rings_of(p);
+  if (p.pair && (o == nullptr || o->cta_pair == 0) && p.kst2 < 32) {
+    Plan q = p;
+    q.pair = 0;
+    if (size_gemm_rings(o, &q) == QMOE_OK) p.r2 = rings_of(q);
+  }
   // rows of the staged B operands: a multiple of 16 (whole 8-row swizzle groups)
   p.cap = (P + static_cast<int64_t>(L->E) * (kAlignBlock - 1) + 15) / 16 * 16;
   p.nblocks = (p.cap + kAlignBlock - 1) / kAlignBlock;
@@ -559,6 +587,14 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
     g1.out_split_stride = pl.cap * 2LL * L->I;
   }
   GemmParams g2 = g1;
+  g2.issuers = pl.r2.issuers;
+  g2.acc_bufs = pl.r2.acc_bufs;
+  g2.a_col0 = pl.r2.a_col0;
+  g2.w_stages = pl.r2.w_stages;
+  g2.ab_stages = pl.r2.ab_stages;
+  g2.b_stages = pl.r2.b_stages;
+  g2.dq_sets = pl.r2.dq_sets;
+  g2.pair = pl.r2.pair;
   g2.w = static_cast<const uint8_t*>(L->w2);
   g2.b = static_cast<const uint8_t*>(inter16);
   g2.b_unit_stride = pl.cap * 256;
@@ -585,10 +621,10 @@ qmoe_status forward_impl(const qmoe_layer* L, const void* x, int64_t M, const in
 
   // (CTA pairs: work items over tile pairs, two CTAs per item)
   const int64_t items1 = pl.max_chunks * (pl.pair ? (pl.n_tiles1 + 1) / 2 : pl.n_tiles1) * pl.S1;
-  const int64_t items2 = pl.max_chunks * (pl.pair ? (pl.n_tiles2 + 1) / 2 : pl.n_tiles2) * pl.S2;
+  const int64_t items2 = pl.max_chunks * (pl.r2.pair ? (pl.n_tiles2 + 1) / 2 : pl.n_tiles2) * pl.S2;
   const int grid1 = pl.pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, items1))
                             : static_cast<int>(std::min<int64_t>(sms, items1));
-  const int grid2 = pl.pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, items2))
+  const int grid2 = pl.r2.pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, items2))
                             : static_cast<int>(std::min<int64_t>(sms, items2));
   rec(4);
   if (err == cudaSuccess) {
@@ -1455,6 +1491,7 @@ qmoe_status qmoe_describe_plan(const qmoe_layer* layer, int64_t M, int32_t top_k
   info->b_stages = pl.b_stages;
   info->dq_sets = pl.dq_sets;
   info->cta_pair = pl.pair;
+  info->cta_pair_down = pl.r2.pair;
   info->stage_bytes = pl.stage_bytes;
   info->workspace_bytes = static_cast<int64_t>(pl.total);
   return QMOE_OK;
@@ -1752,6 +1789,8 @@ qmoe_status qmoe_linear_describe_plan(const qmoe_linear* layer, int64_t M, const
   info->ab_stages = lp.g.ab_stages;
   info->b_stages = lp.g.b_stages;
   info->dq_sets = lp.g.dq_sets;
+  info->cta_pair = 0;
+  info->cta_pair_down = 0;
   info->stage_bytes = lp.g.stage_bytes;
   info->workspace_bytes = static_cast<int64_t>(lp.total);
   return QMOE_OK;
