@@ -35,15 +35,23 @@
 //     it pre-staged, per 128-K group and 8-row group, in the 128-byte-swizzled
 //     K-major layout the MMA's shared-memory descriptor reads, so a chunk's
 //     tile for one stage is one contiguous run.
-//   * warp roles (25 warps): two TMA producer threads (warps 4, 7) and two
-//     dequant sets of 8 warps (warps 8-15, 16-23) take the even and the odd
-//     stages; each dequant warp converts half of a stage row for 32 rows (one
-//     TMEM lane quadrant).  The MMAs are issued by up to three threads (warps
-//     5, 6, 24; stage g goes to issuer g mod NI, each with its own
-//     accumulator) while the token tile is small and one thread's MMA issue
-//     rate is the limit, and by one thread (warp 5) when the tile is large and
-//     the tensor pipe is, so that two accumulator buffers fit in TMEM.  Warps
-//     0-3 are the epilogue.  A persistent grid walks the work items.
+//   * warp roles (25 warps): two TMA producer threads (warps 4, 7) take the
+//     even and the odd stages; the dequant warps 8-23 form four sets of four
+//     (stage g to set g mod 4; each warp converts whole stage rows for the 32
+//     rows of its TMEM lane quadrant) or two sets of eight (half rows).  The
+//     MMAs are issued by warps 5 and 6 (stage g to issuer g mod NI, each with
+//     its own accumulator; warp 24 is a third issuer on request), each warp
+//     converged with one elected lane issuing, while the token tile is small
+//     and one warp's issue rate is the limit, and by warp 5 alone when the
+//     tile is large and the tensor pipe is, so that two accumulator buffers
+//     fit in TMEM.  Warps 0-3 are the epilogue.  A persistent grid walks the
+//     work items.
+//   * CTA pairs (PAIR): clusters of two CTAs on two SMs walk the same items,
+//     each with a pair of 128-row weight tiles; each CTA dequantizes its own
+//     tile into its own TMEM and copies half of the token tile's rows, and the
+//     even CTA issues M = 256 MMAs (cta_group::2) over both, with commits
+//     multicast to both CTAs; the odd CTA's dequant sets and epilogue warps
+//     arrive on the even CTA's A and accumulator barriers.
 //   * barriers per stage: the dequant set waits for the weights and the token
 //     tile (one barrier counts both copies), releases the weight slot,
 //     converts, waits until the MMAs of the stage that last used its A slot
