@@ -89,7 +89,7 @@ struct GemmParams {
   int32_t split;
   int32_t token_tile;        // T: B rows per stage buffer, TMEM columns per accumulator
   int32_t acc_bufs;          // TMEM accumulators per MMA issuer (1 or 2)
-  int32_t issuers;           // MMA-issuing threads (1 or 2)
+  int32_t issuers;           // MMA-issuing warps (1 to 3)
   int32_t a_col0;            // first TMEM column of the A slots
   int32_t w_stages;          // packed-weight ring depth (even)
   int32_t ab_stages;         // TMEM A slots of 64 columns (even)
