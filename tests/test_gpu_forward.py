@@ -294,6 +294,17 @@ def test_host_path_memory_kinds(memory, M):
         torch.cuda.synchronize()
         assert q.qmoe_read_device_status(ws) == q.QMOE_OK
         assert torch.equal(outh, want.cpu()), memory
+    # the host rewrites its buffers in place between calls (a serving loop): the
+    # next call must see the new contents, not data cached from the last one
+    inp2 = make_inputs(wl, M, seed=19)
+    x2, ids2, w2 = device_inputs(wl, inp2)
+    want2, _ = run_forward(dl, x2, ids2, w2)
+    xh.copy_(x2.cpu())
+    idsh.copy_(ids2.cpu())
+    wh.copy_(w2.cpu())
+    q.qmoe_forward_host(dl, xh, idsh, wh, outh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(outh, want2.cpu()), memory + " after rewriting the host inputs"
 
 
 def test_zero_tokens_is_a_no_op():
